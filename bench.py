@@ -1,0 +1,437 @@
+"""Benchmark of the TurboQuant packed-KV hot path on GB300.
+
+One step = the whole hot path over one batch of the 64 x 8192 K4/V4 decode-batch
+workload: tq_write_kv of all 524,288 token rows for K, the same for V, an L2 flush,
+then tq_paged_decode of 64 queries (32 q heads, 8 kv heads, D=128) over the pages.
+
+Prints ONE JSON line (rank 0).  `value` is the decode's packed-KV throughput in GB/s
+(algorithmic bytes: packed K and V rows read plus q and out, over the decode's
+CUDA-event time); the writer's rows/s and the decode's seq/s ride along.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--batch B]
+
+--impl reference times the CPU oracle (the only other implementation: the pages
+publish no code to run) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TQ paged decode KV GB/s (% of HBM peak) and seq/s; tq_write_kv rows/s"
+WORKLOAD_CFG = 4
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--batch", type=int, default=None, help="keep only the first B sequences (profiling runs)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def row_bytes(d, b):
+    return -(-d * b // 8) + 4
+
+
+def decode_bytes(w):
+    """Algorithmic decode bytes: packed K+V rows of every attended token-head, plus q and out."""
+    kv = int(w.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * (row_bytes(w.head_dim, w.k_bits) +
+                                                                     row_bytes(w.head_dim, w.v_bits))
+    qo = 2 * w.q.size * w.q.itemsize
+    return kv + qo
+
+
+def write_bytes(w, raw, slots, bits):
+    """Algorithmic writer bytes for one component: raw rows read, packed rows written, slots read."""
+    written = int((slots >= 0).sum()) * w.num_kv_heads
+    return raw.size * raw.itemsize + written * row_bytes(w.head_dim, bits) + slots.size * 8
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_kv_cache_06_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    ent = rec.get("kernels", {}).get(kernel_key)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+class OracleSample:
+    """Times the oracle (as it stands) on a bounded sample of the workload: the write of
+    the first n_write_tokens tokens (K and V) and the decode of the first n_seq
+    sequences.  The pages the decode reads are written by the oracle once, untimed."""
+
+    def __init__(self, w, n_seq, n_write_tokens):
+        from oracle import tq_oracle as o
+
+        self.o, self.w, self.n_seq = o, w, n_seq
+        d = w.head_dim
+        self.signs = o.splitmix64_signs(d, 42)
+        self.ck = o.codebook_f32(d, w.k_bits)[0]
+        self.cv = o.codebook_f32(d, w.v_bits)[0]
+        rb_k, rb_v = row_bytes(d, w.k_bits), row_bytes(d, w.v_bits)
+        ntok = int(w.seq_token_offsets()[n_seq])
+        self.nw = min(n_write_tokens, ntok)
+        kp = np.zeros((w.num_blocks, w.block_size, w.num_kv_heads, rb_k), dtype=np.uint8)
+        vp = np.zeros((w.num_blocks, w.block_size, w.num_kv_heads, rb_v), dtype=np.uint8)
+        self.kp = o.write_kv(w.k_raw[:ntok], kp, w.slots[:ntok], self.signs, self.ck, w.k_bits)
+        self.vp = o.write_kv(w.v_raw[:ntok], vp, w.slots[:ntok], self.signs, self.cv, w.v_bits)
+        self.dec_bytes = int(w.seq_lens[:n_seq].astype(np.int64).sum()) * w.num_kv_heads * (rb_k + rb_v) + \
+            2 * w.q[:n_seq].size * w.q.itemsize
+
+    def run(self):
+        o, w, nw = self.o, self.w, self.nw
+        t0 = time.perf_counter()
+        o.write_kv(w.k_raw[:nw], self.kp, w.slots[:nw], self.signs, self.ck, w.k_bits)
+        o.write_kv(w.v_raw[:nw], self.vp, w.slots[:nw], self.signs, self.cv, w.v_bits)
+        t_write = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        o.paged_decode(w.q[:self.n_seq], self.kp, self.vp, w.k_bits, w.v_bits, w.block_table[:self.n_seq],
+                       w.seq_lens[:self.n_seq], self.signs, self.ck, self.cv)
+        t_dec = time.perf_counter() - t0
+        return {"decode_gbs": self.dec_bytes / t_dec / 1e9, "decode_seq_per_s": self.n_seq / t_dec,
+                "write_rows_per_s": 2 * nw * w.num_kv_heads / t_write, "t_decode_s": t_dec, "t_write_s": t_write}
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def workload_config(w, batch_override):
+    return {"workload": f"{w.name}: write {w.num_tokens} tokens K+V, then decode", "batch": w.batch,
+            "seq_len": int(w.seq_lens.max()), "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits, "block_size": w.block_size,
+            "num_blocks": w.num_blocks, "raw_dtype": str(w.k_raw.dtype),
+            "l2": "inputs > L2 (1.07 GB raw per component); 256 MB L2 flush before each decode",
+            "batch_override": batch_override}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from quantized_kv_cache_06_gb300.workloads import make_workload
+
+    w = make_workload(WORKLOAD_CFG, batch=args.batch)
+    n_seq, n_write = 2, 4096
+    sampler = OracleSample(w, n_seq, n_write)
+    for _ in range(args.warmup):
+        sampler.run()
+    vals, secs = [], []
+    for _ in range(args.steps):
+        r = sampler.run()
+        vals.append(r["decode_gbs"])
+        secs.append(r["t_decode_s"] + r["t_write_s"])
+    value = statistics.median(vals)
+    cores = blas_threads()
+    sample = (f"oracle decode of {n_seq} of {w.batch} sequences (all {w.num_q_heads} q heads, full context) and "
+              f"write of {n_write} tokens x {w.num_kv_heads} heads for K and V, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, args.batch),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+
+    import quantized_kv_cache_06_gb300 as tq
+    from quantized_kv_cache_06_gb300.workloads import make_workload
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    tq.lib()
+
+    w = make_workload(WORKLOAD_CFG, batch=args.batch)
+    d = w.head_dim
+    signs = tq.tq_build_rotation(d, 42, dev)
+    ck = tq.tq_codebook(d, w.k_bits, dev)[0]
+    cv = tq.tq_codebook(d, w.v_bits, dev)[0]
+    rb_k, rb_v = tq.tq_row_bytes(d, w.k_bits), tq.tq_row_bytes(d, w.v_bits)
+    kraw = torch.from_numpy(w.k_raw).to(dev)
+    vraw = torch.from_numpy(w.v_raw).to(dev)
+    slots = torch.from_numpy(w.slots).to(dev)
+    q = torch.from_numpy(w.q).to(dev)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    lens = torch.from_numpy(w.seq_lens).to(dev)
+    kp = torch.zeros(w.num_blocks, w.block_size, w.num_kv_heads, rb_k, dtype=torch.uint8, device=dev)
+    vp = torch.zeros(w.num_blocks, w.block_size, w.num_kv_heads, rb_v, dtype=torch.uint8, device=dev)
+    out = torch.empty(w.q.shape, dtype=q.dtype, device=dev)
+    ws = torch.empty(max(16, tq.tq_paged_decode_workspace(w.batch, w.num_q_heads, w.num_kv_heads, d,
+                                                           w.block_table.shape[1], w.block_size)),
+                     dtype=torch.uint8, device=dev)
+    st_k = torch.zeros(1, dtype=torch.int32, device=dev)
+    st_v = torch.zeros(1, dtype=torch.int32, device=dev)
+    st_d = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tq.tq_write_kv(kraw, kp, slots, signs, ck, status=st_k, check=False)
+        if ev is not None:
+            ev[1].record(stream)
+        tq.tq_write_kv(vraw, vp, slots, signs, cv, status=st_v, check=False)
+        if ev is not None:
+            ev[2].record(stream)
+        flush.zero_()
+        if ev is not None:
+            ev[3].record(stream)
+        tq.tq_paged_decode(q, kp, vp, bt, lens, signs, ck, cv, out=out, workspace=ws, status=st_d)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for s in (st_k, st_v, st_d):
+        tq.raise_for_device_status(s)
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(events[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    wk = [e[0].elapsed_time(e[1]) for e in events]
+    wv = [e[1].elapsed_time(e[2]) for e in events]
+    dec = [e[3].elapsed_time(e[4]) for e in events]
+    ms_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step, statistics.mean(dec)], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, dec_max = float(t[0]), float(t[1])
+    else:
+        dec_max = statistics.mean(dec)
+
+    dbytes = decode_bytes(w)
+    kbytes = write_bytes(w, w.k_raw, w.slots, w.k_bits)
+    vbytes = write_bytes(w, w.v_raw, w.slots, w.v_bits)
+    dec_s = dec_max / 1e3
+    value = world * dbytes / dec_s / 1e9
+    head_rows = 2 * w.num_tokens * w.num_kv_heads
+    write_s = (statistics.mean(wk) + statistics.mean(wv)) / 1e3
+    peak, peak_kind = peaks()
+    dec_gbs = dbytes / dec_s / 1e9
+    wr_gbs = (kbytes + vbytes) / write_s / 1e9
+    roof_dec = {"kernel": "tq_paged_decode (split + combine kernels)", "bound": "hbm", "achieved": dec_gbs,
+                "peak": peak, "unit": "GB/s", "frac": dec_gbs / peak, "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": dbytes, "traffic": ncu_traffic("decode")}
+    roof_wr = {"kernel": "tq_write_kv (validate + write kernels)", "bound": "hbm", "achieved": wr_gbs, "peak": peak,
+               "unit": "GB/s", "frac": wr_gbs / peak, "peak_source": peak_kind,
+               "algorithmic_bytes_per_launch": (kbytes + vbytes) / 2, "traffic": ncu_traffic("write")}
+    dominant = roof_dec if dec_max / 1e3 > write_s / 2 else roof_wr
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(w, args.batch),
+            "decode_us": dec_max * 1e3, "decode_gbs_per_gpu": dec_gbs, "decode_frac_of_peak": dec_gbs / peak,
+            "decode_seq_per_s": world * w.batch / dec_s,
+            "write_us_per_component": write_s / 2 * 1e6, "write_rows_per_s": world * head_rows / write_s,
+            "write_token_rows_per_s": world * 2 * w.num_tokens / write_s, "write_gbs_per_gpu": wr_gbs,
+            "roofline": dominant, "roofline_decode": roof_dec, "roofline_write": roof_wr,
+            "gpu_launches": args.steps * 6, "clocks": clk}
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        r = OracleSample(w, 2, 4096).run()
+        line["cpu_baseline"] = {"value": r["decode_gbs"], "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": "oracle decode of 2 sequences (32 q heads, 8192 tokens) and write of "
+                                          "4096 tokens x 8 heads for K and V",
+                                "decode_seq_per_s": r["decode_seq_per_s"], "write_rows_per_s": r["write_rows_per_s"]}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5):
+    """Same step from pinned host buffers: H2D of the step's inputs, write K, write V,
+    decode, D2H of the output, all inside the timed region."""
+    import torch
+
+    hk = torch.from_numpy(w.k_raw).pin_memory()
+    hv = torch.from_numpy(w.v_raw).pin_memory()
+    hs = torch.from_numpy(w.slots).pin_memory()
+    hq = torch.from_numpy(w.q).pin_memory()
+    hbt = torch.from_numpy(w.block_table).pin_memory()
+    hl = torch.from_numpy(w.seq_lens).pin_memory()
+    hout = torch.empty(w.q.shape, dtype=hq.dtype).pin_memory()
+    dk, dv = torch.empty_like(hk, device=dev), torch.empty_like(hv, device=dev)
+    ds, dq = torch.empty_like(hs, device=dev), torch.empty_like(hq, device=dev)
+    dbt, dl = torch.empty_like(hbt, device=dev), torch.empty_like(hl, device=dev)
+    dout = torch.empty_like(hq, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def one():
+        for h, dd in ((hk, dk), (hv, dv), (hs, ds), (hq, dq), (hbt, dbt), (hl, dl)):
+            dd.copy_(h, non_blocking=True)
+        tq.tq_write_kv(dk, kp, ds, signs, ck, status=st, check=False)
+        tq.tq_write_kv(dv, vp, ds, signs, cv, status=st, check=False)
+        tq.tq_paged_decode(dq, kp, vp, dbt, dl, signs, ck, cv, out=dout, workspace=ws)
+        hout.copy_(dout, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hs, hq, hbt, hl))
+    return {"value": world * dbytes / sec / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": hout.numel() * hout.element_size(), "ms_per_step": sec * 1e3}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

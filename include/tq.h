@@ -1,0 +1,154 @@
+/*
+ * tq.h -- C ABI of the GB300 TurboQuant packed-KV library (libtq_gb300.so).
+ *
+ * The library implements the two data-parallel steps of TurboQuant's packed KV
+ * cache as hand-written CUDA kernels for sm_103a:
+ *
+ *   tq_write_kv      rotate, quantise, bit-pack and scatter K or V rows into uint8
+ *                    pages ("vLLM Usage": TQ Byte Layout, Slot Mapping, TQ Packed
+ *                    Page Contract; "Architecture": PackedPageCache).
+ *   tq_paged_decode  single-query attention that reads those pages through a block
+ *                    table without materialising dense K/V ("Architecture":
+ *                    Diagnostic vs Serving Paths, direct-QK and packed-V).
+ *
+ * plus the host-side set-up the contract call needs (rotation signs, Lloyd-Max
+ * codebook, row size).
+ *
+ * Conventions shared by every entry point:
+ *   - Every buffer is owned by the caller.  "device" pointers must point to memory of
+ *     the current CUDA device; "host" pointers to ordinary host memory.  The library
+ *     never allocates or frees device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Device work is enqueued on it and the call returns without synchronising.
+ *   - Every call returns a tq_status.  On a non-OK return, tq_last_error() gives a
+ *     message for the calling thread.  Argument errors are detected on the host
+ *     before anything is enqueued.  Errors that depend on device data (slots, block
+ *     ids, sequence lengths) are reported through `status_dev`, a device int32 the
+ *     caller reads after the stream reaches it: 0 = OK, otherwise a tq_status code
+ *     (the largest one when several kinds occur).  No kernel traps or asserts.
+ *   - Geometry: head_dim D is a power of two in [32, 256]; bits b in {2, 3, 4, 5};
+ *     row_bytes RB(D, b) = ceil(D*b/8) + 4.  A page tensor is
+ *     uint8[num_blocks][block_size][num_kv_heads][RB], contiguous, no padding, one
+ *     tensor per component (K and V are independent and may use different bits).
+ *   - Row layout (reading of "TQ Byte Layout"): index j of a row occupies bits
+ *     [j*b, (j+1)*b) of the index bytes, LSB first (stream bit k = bit k%8 of byte
+ *     k/8); bytes [RB-4, RB) hold the row's L2 norm as a little-endian fp32.
+ *   - Rotation: R = H_D diag(s) / sqrt(D) with H_D the Sylvester Hadamard matrix
+ *     (sign flip, then normalised Walsh-Hadamard transform; RHT in "TQ Packed Page
+ *     Contract").
+ */
+#ifndef TQ_GB300_H
+#define TQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tq_status {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,        /* null pointer, negative size, inconsistent shapes */
+  TQ_ERR_UNSUPPORTED = 2,        /* valid but outside what the kernels handle (D, bits, GQA group) */
+  TQ_ERR_SLOT_OUT_OF_RANGE = 3,  /* a write slot >= num_blocks * block_size */
+  TQ_ERR_BLOCK_OUT_OF_RANGE = 4, /* a block-table entry read by decode lies outside [0, num_blocks) */
+  TQ_ERR_CUDA = 5                /* a CUDA runtime call failed (message in tq_last_error) */
+} tq_status;
+
+typedef enum tq_dtype { TQ_F32 = 0, TQ_F16 = 1, TQ_BF16 = 2 } tq_dtype;
+
+/* Message for the last non-OK status returned on the calling thread ("" if none).
+ * The pointer stays valid until the next library call on that thread. */
+const char* tq_last_error(void);
+
+/* Row size in bytes for one component, one token and one KV head: ceil(D*b/8) + 4
+ * ("vLLM Usage", TQ Byte Layout).  Returns -1 when head_dim or bits is unsupported. */
+int64_t tq_row_bytes(int head_dim, int bits);
+
+/* RHT signs for build_rotation(dim, RHT, seed) ("vLLM Usage", TQ Packed Page Contract).
+ * Writes head_dim values in {-1.0f, +1.0f} to signs_host[0..D): sign i is -1 when the
+ * top bit of the i-th output of splitmix64 seeded with `seed` is set (a reading: the
+ * pages fix only the mode and the seed).  Host only; errors: TQ_ERR_INVALID_ARG
+ * (null), TQ_ERR_UNSUPPORTED (head_dim). */
+tq_status tq_build_rotation(int head_dim, uint64_t seed, float* signs_host);
+
+/* Lloyd-Max codebook for one coordinate of a uniformly random unit vector in R^D
+ * (get_codebook_tensors(dim, bits) in "TQ Packed Page Contract"; Lloyd-Max / Beta in
+ * "vLLM Reference Audit", Feature Checklist).  Density on [-1, 1]:
+ * f_D(x) = Gamma(D/2) / (sqrt(pi) Gamma((D-1)/2)) (1 - x^2)^((D-3)/2).
+ * centroids_host[0 .. 2^b) receives the ascending fp32 centroids (fp64 fixed point,
+ * rounded once); boundaries_host[0 .. 2^b - 1), if not NULL, receives the decision
+ * points the writer uses: the midpoint of neighbouring fp32 centroids, rounded to
+ * fp32.  Host only; results are cached per (D, b).  Errors: TQ_ERR_INVALID_ARG,
+ * TQ_ERR_UNSUPPORTED. */
+tq_status tq_codebook(int head_dim, int bits, float* centroids_host, float* boundaries_host);
+
+/* Packed-KV row writer (write_tq4_kv in "TQ Packed Page Contract").
+ *
+ *   raw        device, raw_dtype[num_tokens][num_kv_heads][head_dim], contiguous.
+ *   slots      device, int64[num_tokens], flat slots: row (t, h) goes to
+ *              pages[slots[t] / block_size][slots[t] % block_size][h][:].
+ *              Negative slots are skipped ("Slot Mapping").
+ *   pages      device, uint8[num_blocks][block_size][num_kv_heads][RB(D, bits)].
+ *   signs      device, float[head_dim] from tq_build_rotation.
+ *   centroids  device, float[2^bits] ascending, from tq_codebook.
+ *   status_dev device int32, required: set to 0 at the start of the call, then to
+ *              TQ_ERR_SLOT_OUT_OF_RANGE if any slot >= num_blocks * block_size -- in
+ *              that case NO row is written (validation runs before the write).
+ *
+ * Each row x is encoded as: nu = ||x||_2 (fp32), u = x / nu (0 if nu == 0),
+ * y = R u (fp32, in-register FWHT), index_j = #{k : boundary_k < y_j} (the nearest
+ * centroid, ties to the lower index), packed LSB-first, norm appended.  Rows of
+ * skipped tokens keep their previous bytes.  Duplicate non-negative slots: which
+ * token's row survives is unspecified.  Asynchronous; errors detected on the host:
+ * TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA. */
+tq_status tq_write_kv(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, int num_kv_heads,
+                      int head_dim, int bits, const int64_t* slots, uint8_t* pages,
+                      int64_t num_blocks, int block_size, const float* signs,
+                      const float* centroids, int32_t* status_dev, void* stream);
+
+/* Bytes of device workspace tq_paged_decode needs for these shapes on the current
+ * device (split-K partials).  0 when the arguments are invalid. */
+size_t tq_paged_decode_workspace(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size);
+
+/* Paged decode attention over packed pages (decode_tq4_paged in "TQ Packed Page
+ * Contract"; "Architecture", Diagnostic vs Serving Paths).
+ *
+ *   q            device, q_dtype[batch][num_q_heads][head_dim].
+ *   k_pages      device, uint8[num_blocks][block_size][num_kv_heads][RB(D, k_bits)].
+ *   v_pages      device, uint8[num_blocks][block_size][num_kv_heads][RB(D, v_bits)].
+ *   block_table  device, int32[batch][max_blocks_per_seq]: token t of sequence b is
+ *                row (t % block_size) of block block_table[b][t / block_size].
+ *   seq_lens     device, int32[batch]; 0 gives a zero output row.
+ *   signs        device, float[head_dim]; k_centroids / v_centroids device,
+ *                float[2^k_bits] / float[2^v_bits].
+ *   scale        softmax scale; <= 0 selects 1/sqrt(head_dim).
+ *   out          device, out_dtype[batch][num_q_heads][head_dim].
+ *   workspace    device, >= tq_paged_decode_workspace(...) bytes, 16-byte aligned.
+ *   status_dev   device int32 or NULL.  If not NULL it is set to 0 at the start of
+ *                the call, then to TQ_ERR_BLOCK_OUT_OF_RANGE if a block id read lies
+ *                outside [0, num_blocks) (its tokens are left out of the softmax),
+ *                or TQ_ERR_INVALID_ARG if a seq_len is negative or exceeds
+ *                max_blocks_per_seq * block_size (it is clamped).
+ *
+ * q head h attends with kv head h / (num_q_heads / num_kv_heads).  Scores are
+ * scale * nu_k * <R q, c_k[idx]> computed from the packed indices; values are
+ * accumulated in rotated space, sum p nu_v c_v[idx_v], with an online softmax, and
+ * one inverse rotation R^T is applied per output row.  Asynchronous; host-detected
+ * errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA. */
+tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_heads,
+                          int num_kv_heads, int head_dim, const uint8_t* k_pages, int k_bits,
+                          const uint8_t* v_pages, int v_bits, int64_t num_blocks, int block_size,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, const float* signs, const float* k_centroids,
+                          const float* v_centroids, float scale, void* out, tq_dtype out_dtype,
+                          void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_GB300_H */

@@ -1,0 +1,24 @@
+"""GB300-native TurboQuant packed KV cache: row writer and paged decode attention.
+
+The compute lives in libtq_gb300.so (hand-written CUDA for sm_103a, C ABI in
+include/tq.h).  This package is its thin Python binding; it loads the library on
+first use and raises if it has not been built.
+"""
+
+from ._lib import (  # noqa: F401
+    TQ_ERR_BLOCK_OUT_OF_RANGE,
+    TQ_ERR_CUDA,
+    TQ_ERR_INVALID_ARG,
+    TQ_ERR_SLOT_OUT_OF_RANGE,
+    TQ_ERR_UNSUPPORTED,
+    TQ_OK,
+    TQError,
+    lib,
+    raise_for_device_status,
+    tq_build_rotation,
+    tq_codebook,
+    tq_paged_decode,
+    tq_paged_decode_workspace,
+    tq_row_bytes,
+    tq_write_kv,
+)

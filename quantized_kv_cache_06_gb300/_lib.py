@@ -1,0 +1,229 @@
+"""ctypes binding of libtq_gb300.so (include/tq.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels (or, for the rotation signs
+and the codebook, in its host C++).  If the library has not been built these
+functions raise: there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+TQ_OK = 0
+TQ_ERR_INVALID_ARG = 1
+TQ_ERR_UNSUPPORTED = 2
+TQ_ERR_SLOT_OUT_OF_RANGE = 3
+TQ_ERR_BLOCK_OUT_OF_RANGE = 4
+TQ_ERR_CUDA = 5
+
+STATUS_NAMES = {
+    TQ_OK: "TQ_OK",
+    TQ_ERR_INVALID_ARG: "TQ_ERR_INVALID_ARG",
+    TQ_ERR_UNSUPPORTED: "TQ_ERR_UNSUPPORTED",
+    TQ_ERR_SLOT_OUT_OF_RANGE: "TQ_ERR_SLOT_OUT_OF_RANGE",
+    TQ_ERR_BLOCK_OUT_OF_RANGE: "TQ_ERR_BLOCK_OUT_OF_RANGE",
+    TQ_ERR_CUDA: "TQ_ERR_CUDA",
+}
+
+_DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+# Every symbol include/tq.h declares, with (restype, argtypes).
+_c_int, _c_i64, _c_u64, _c_f, _c_p, _c_sz = (ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float,
+                                            ctypes.c_void_p, ctypes.c_size_t)
+SIGNATURES = {
+    "tq_last_error": (ctypes.c_char_p, []),
+    "tq_row_bytes": (_c_i64, [_c_int, _c_int]),
+    "tq_build_rotation": (_c_int, [_c_int, _c_u64, _c_p]),
+    "tq_codebook": (_c_int, [_c_int, _c_int, _c_p, _c_p]),
+    "tq_write_kv": (_c_int, [_c_p, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_p, _c_p, _c_i64, _c_int,
+                             _c_p, _c_p, _c_p, _c_p]),
+    "tq_paged_decode_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tq_paged_decode": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
+                                 _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_int,
+                                 _c_p, _c_sz, _c_p, _c_p]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class TQError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                                       "(python -m quantized_kv_cache_06_gb300.build, needs nvcc for sm_103a)")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != TQ_OK:
+        msg = lib().tq_last_error().decode(errors="replace")
+        raise TQError(status, msg)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need_cuda(name: str, *tensors: torch.Tensor) -> torch.device:
+    dev = tensors[0].device
+    for t in tensors:
+        if t.device.type != "cuda" or t.device != dev:
+            raise ValueError(f"{name}: all tensors must be on the same CUDA device")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: tensors must be contiguous")
+    return dev
+
+
+_status_bufs: dict = {}
+
+
+def _status_buffer(device: torch.device) -> torch.Tensor:
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    buf = _status_bufs.get(key)
+    if buf is None:
+        buf = torch.zeros(1, dtype=torch.int32, device=device)
+        _status_bufs[key] = buf
+    return buf
+
+
+def raise_for_device_status(status: torch.Tensor) -> None:
+    """Synchronises on `status` (a device int32 the library wrote) and raises on a non-zero code."""
+    code = int(status.item())
+    if code != TQ_OK:
+        raise TQError(code, "reported by the device status word")
+
+
+# ---------------------------------------------------------------- host set-up
+
+def tq_row_bytes(head_dim: int, bits: int) -> int:
+    n = lib().tq_row_bytes(int(head_dim), int(bits))
+    if n < 0:
+        raise TQError(TQ_ERR_UNSUPPORTED, f"head_dim {head_dim} / bits {bits} unsupported")
+    return int(n)
+
+
+def tq_build_rotation(head_dim: int, seed: int = 42, device=None) -> torch.Tensor:
+    """RHT signs (float32 [head_dim], +-1) for build_rotation(dim, RHT, seed)."""
+    out = torch.empty(int(head_dim), dtype=torch.float32)
+    _check(lib().tq_build_rotation(int(head_dim), int(seed) & ((1 << 64) - 1), out.data_ptr()))
+    return out if device is None else out.to(device)
+
+
+def tq_codebook(head_dim: int, bits: int, device=None):
+    """(centroids float32 [2^bits], boundaries float32 [2^bits - 1])."""
+    n = 1 << int(bits)
+    c = torch.empty(n, dtype=torch.float32)
+    b = torch.empty(n - 1, dtype=torch.float32)
+    _check(lib().tq_codebook(int(head_dim), int(bits), c.data_ptr(), b.data_ptr()))
+    if device is not None:
+        c, b = c.to(device), b.to(device)
+    return c, b
+
+
+def _bits_from_centroids(centroids: torch.Tensor) -> int:
+    n = centroids.numel()
+    bits = n.bit_length() - 1
+    if n < 4 or (1 << bits) != n:
+        raise ValueError(f"centroids must hold 2^bits values, got {n}")
+    return bits
+
+
+# ---------------------------------------------------------------- writer
+
+def tq_write_kv(raw: torch.Tensor, pages: torch.Tensor, slots: torch.Tensor, signs: torch.Tensor,
+                centroids: torch.Tensor, status: torch.Tensor | None = None, check: bool = True) -> torch.Tensor:
+    """write_tq4_kv(raw, pages, slots, rotation, centroids): encode raw[T, H, D] into pages[NB, bs, H, RB].
+
+    Returns the device status word.  With check=True the call synchronises on it and
+    raises TQError(TQ_ERR_SLOT_OUT_OF_RANGE) when a slot was out of range (then no row
+    was written).
+    """
+    dev = _need_cuda("tq_write_kv", raw, pages, slots, signs, centroids)
+    if raw.dim() != 3 or pages.dim() != 4 or slots.dim() != 1 or slots.numel() != raw.shape[0]:
+        raise ValueError("tq_write_kv: raw [T, H, D], pages [NB, bs, H, RB], slots [T] expected")
+    if raw.dtype not in _DTYPES or pages.dtype != torch.uint8 or slots.dtype != torch.int64:
+        raise ValueError("tq_write_kv: raw f32/f16/bf16, pages uint8, slots int64 expected")
+    t, h, d = raw.shape
+    bits = _bits_from_centroids(centroids)
+    if pages.shape[2] != h or pages.shape[3] != tq_row_bytes(d, bits):
+        raise ValueError(f"tq_write_kv: pages {tuple(pages.shape)} do not match H={h}, RB={tq_row_bytes(d, bits)}")
+    if status is None:
+        status = _status_buffer(dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_write_kv(_ptr(raw), _DTYPES[raw.dtype], t, h, d, bits, _ptr(slots), _ptr(pages),
+                                 pages.shape[0], pages.shape[1], _ptr(signs), _ptr(centroids), _ptr(status),
+                                 _stream(dev)))
+    if check:
+        raise_for_device_status(status)
+    return status
+
+
+# ---------------------------------------------------------------- decode
+
+def tq_paged_decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                              max_blocks_per_seq: int, block_size: int) -> int:
+    return int(lib().tq_paged_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                               block_size))
+
+
+def tq_paged_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                    seq_lens: torch.Tensor, signs: torch.Tensor, k_centroids: torch.Tensor,
+                    v_centroids: torch.Tensor, scale: float | None = None, out: torch.Tensor | None = None,
+                    out_dtype: torch.dtype | None = None, workspace: torch.Tensor | None = None,
+                    status: torch.Tensor | None = None, check: bool = False) -> torch.Tensor:
+    """decode_tq4_paged: attention of q[B, Hq, D] over packed K/V pages through block_table[B, maxblk]."""
+    dev = _need_cuda("tq_paged_decode", q, k_pages, v_pages, block_table, seq_lens, signs, k_centroids,
+                     v_centroids)
+    if q.dim() != 3 or k_pages.dim() != 4 or v_pages.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("tq_paged_decode: q [B, Hq, D], pages [NB, bs, H, RB], block_table [B, maxblk] expected")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32 or q.dtype not in _DTYPES:
+        raise ValueError("tq_paged_decode: block_table / seq_lens int32, q f32/f16/bf16 expected")
+    b, hq, d = q.shape
+    nb, bs, h, _ = k_pages.shape
+    kb, vb = _bits_from_centroids(k_centroids), _bits_from_centroids(v_centroids)
+    if k_pages.shape[3] != tq_row_bytes(d, kb) or v_pages.shape[3] != tq_row_bytes(d, vb) or \
+            tuple(v_pages.shape[:3]) != (nb, bs, h) or block_table.shape[0] != b or seq_lens.numel() != b:
+        raise ValueError("tq_paged_decode: page / table shapes inconsistent with q and the codebooks")
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=out_dtype, device=dev)
+    maxb = block_table.shape[1]
+    need = tq_paged_decode_workspace(b, hq, h, d, maxb, bs)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_paged_decode(_ptr(q), _DTYPES[q.dtype], b, hq, h, d, _ptr(k_pages), kb, _ptr(v_pages), vb,
+                                     nb, bs, _ptr(block_table), maxb, _ptr(seq_lens), _ptr(signs),
+                                     _ptr(k_centroids), _ptr(v_centroids), float(scale or 0.0), _ptr(out),
+                                     _DTYPES[out.dtype], _ptr(workspace), workspace.numel(), _ptr(status),
+                                     _stream(dev)))
+    if check and status is not None:
+        raise_for_device_status(status)
+    return out

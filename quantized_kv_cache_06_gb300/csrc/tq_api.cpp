@@ -1,0 +1,305 @@
+// Host side of the C ABI declared in include/tq.h: argument checks, rotation signs,
+// the Lloyd-Max codebook, and the kernel launches.
+//
+// The codebook is solved here independently of the test oracle: cell masses and
+// first moments come from composite Gauss-Legendre quadrature of the coordinate
+// density, and the initial centroids from bisection on the quadrature CDF.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "tq.h"
+#include "tq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+tq_status fail(tq_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+tq_status ok() {
+  g_last_error.clear();
+  return TQ_OK;
+}
+
+bool pow2_dim_ok(int d) { return d >= 32 && d <= 256 && (d & (d - 1)) == 0; }
+bool bits_ok(int b) { return b >= 2 && b <= 5; }
+bool dtype_ok(int t) { return t == TQ_F32 || t == TQ_F16 || t == TQ_BF16; }
+size_t dtype_size(int t) { return t == TQ_F32 ? 4 : 2; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+tq_status check_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(TQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- codebook
+
+// Gauss-Legendre nodes and weights on [-1, 1] (Newton iteration on P_n).
+void gauss_legendre(int n, std::vector<double>& x, std::vector<double>& w) {
+  x.assign(n, 0.0);
+  w.assign(n, 0.0);
+  for (int i = 0; i < (n + 1) / 2; ++i) {
+    double z = std::cos(M_PI * (i + 0.75) / (n + 0.5));
+    double pn = 0.0, dp = 1.0;
+    for (int it = 0; it < 100; ++it) {
+      double p_prev = 1.0, p = z;
+      for (int k = 2; k <= n; ++k) {
+        const double p_next = ((2.0 * k - 1.0) * z * p - (k - 1.0) * p_prev) / k;
+        p_prev = p;
+        p = p_next;
+      }
+      pn = p;
+      dp = n * (z * p - p_prev) / (z * z - 1.0);
+      const double dz = pn / dp;
+      z -= dz;
+      if (std::fabs(dz) < 1e-17) break;
+    }
+    x[i] = -z;
+    x[n - 1 - i] = z;
+    w[i] = w[n - 1 - i] = 2.0 / ((1.0 - z * z) * dp * dp);
+  }
+}
+
+struct CoordDensity {
+  double log_c, p;
+  std::vector<double> gx, gw;
+  explicit CoordDensity(int d) {
+    log_c = std::lgamma(d / 2.0) - 0.5 * std::log(M_PI) - std::lgamma((d - 1) / 2.0);
+    p = (d - 3) / 2.0;
+    gauss_legendre(24, gx, gw);
+  }
+  double f(double x) const {
+    const double t = 1.0 - x * x;
+    return t <= 0.0 ? 0.0 : std::exp(log_c + p * std::log1p(-x * x));
+  }
+  // (integral of f, integral of x f) over [lo, hi], 8 panels of 24-point Gauss-Legendre.
+  std::pair<double, double> moments(double lo, double hi) const {
+    const int panels = 8;
+    const double h = (hi - lo) / panels;
+    double m0 = 0.0, m1 = 0.0;
+    for (int k = 0; k < panels; ++k) {
+      const double a = lo + k * h, mid = a + 0.5 * h;
+      for (size_t i = 0; i < gx.size(); ++i) {
+        const double x = mid + 0.5 * h * gx[i];
+        const double fx = gw[i] * 0.5 * h * f(x);
+        m0 += fx;
+        m1 += x * fx;
+      }
+    }
+    return {m0, m1};
+  }
+};
+
+std::vector<double> solve_lloyd_max(int d, int bits) {
+  const int n = 1 << bits;
+  CoordDensity dens(d);
+  // Initial centroids: (k + 1/2)/n quantiles by bisection on the quadrature CDF.
+  std::vector<double> c(n);
+  for (int k = 0; k < n; ++k) {
+    const double target = (k + 0.5) / n;
+    double lo = -1.0, hi = 1.0;
+    for (int it = 0; it < 60; ++it) {
+      const double mid = 0.5 * (lo + hi);
+      const double cdf = 0.5 + (mid >= 0 ? dens.moments(0.0, mid).first : -dens.moments(mid, 0.0).first);
+      (cdf < target ? lo : hi) = mid;
+    }
+    c[k] = 0.5 * (lo + hi);
+  }
+  std::vector<double> edges(n + 1), cn(n);
+  for (int iter = 0; iter < 1000000; ++iter) {
+    edges[0] = -1.0;
+    edges[n] = 1.0;
+    for (int k = 1; k < n; ++k) edges[k] = 0.5 * (c[k - 1] + c[k]);
+    double moved = 0.0;
+    for (int k = 0; k < n; ++k) {
+      const auto mm = dens.moments(edges[k], edges[k + 1]);
+      cn[k] = mm.second / mm.first;
+      moved = std::fmax(moved, std::fabs(cn[k] - c[k]));
+    }
+    c.swap(cn);
+    if (moved < 1e-14) break;
+  }
+  // The density is even: make the solution exactly odd-symmetric.
+  std::vector<double> s(n);
+  for (int k = 0; k < n; ++k) s[k] = 0.5 * (c[k] - c[n - 1 - k]);
+  return s;
+}
+
+std::mutex g_cb_mutex;
+std::map<std::pair<int, int>, std::vector<float>> g_cb_cache;
+
+const std::vector<float>& codebook_f32(int d, int bits) {
+  std::lock_guard<std::mutex> lock(g_cb_mutex);
+  auto key = std::make_pair(d, bits);
+  auto it = g_cb_cache.find(key);
+  if (it != g_cb_cache.end()) return it->second;
+  const std::vector<double> c = solve_lloyd_max(d, bits);
+  std::vector<float> c32(c.size());
+  for (size_t i = 0; i < c.size(); ++i) c32[i] = (float)c[i];
+  return g_cb_cache.emplace(key, std::move(c32)).first->second;
+}
+
+int current_device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return sms > 0 ? sms : 1;
+}
+
+tq_status decode_shape_check(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             int max_blocks_per_seq, int block_size) {
+  if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 0 || block_size < 1)
+    return fail(TQ_ERR_INVALID_ARG, "decode: invalid sizes (batch=%d, q_heads=%d, kv_heads=%d, max_blocks=%d, block_size=%d)",
+                batch, num_q_heads, num_kv_heads, max_blocks_per_seq, block_size);
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(TQ_ERR_INVALID_ARG, "decode: num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads, num_kv_heads);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  const int g = num_q_heads / num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8)
+    return fail(TQ_ERR_UNSUPPORTED, "decode: GQA group %d not supported (1, 2, 4 or 8)", g);
+  return ok();
+}
+
+tq::DecodeArgs make_decode_args(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                int max_blocks_per_seq, int block_size) {
+  tq::DecodeArgs a{};
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.block_size = block_size;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tq_last_error(void) { return g_last_error.c_str(); }
+
+int64_t tq_row_bytes(int head_dim, int bits) {
+  if (!pow2_dim_ok(head_dim) || !bits_ok(bits)) return -1;
+  return ((int64_t)head_dim * bits + 7) / 8 + 4;
+}
+
+tq_status tq_build_rotation(int head_dim, uint64_t seed, float* signs_host) {
+  if (!signs_host) return fail(TQ_ERR_INVALID_ARG, "tq_build_rotation: signs_host is NULL");
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  uint64_t state = seed;
+  for (int i = 0; i < head_dim; ++i) {
+    state += 0x9E3779B97F4A7C15ull;  // splitmix64 (Steele, Lea & Flood 2014)
+    uint64_t z = state;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    signs_host[i] = (z >> 63) ? -1.0f : 1.0f;
+  }
+  return ok();
+}
+
+tq_status tq_codebook(int head_dim, int bits, float* centroids_host, float* boundaries_host) {
+  if (!centroids_host) return fail(TQ_ERR_INVALID_ARG, "tq_codebook: centroids_host is NULL");
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!bits_ok(bits)) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 2, 3, 4 or 5", bits);
+  const std::vector<float>& c = codebook_f32(head_dim, bits);
+  std::memcpy(centroids_host, c.data(), c.size() * sizeof(float));
+  if (boundaries_host)
+    for (size_t k = 0; k + 1 < c.size(); ++k)
+      boundaries_host[k] = (float)(0.5 * ((double)c[k] + (double)c[k + 1]));
+  return ok();
+}
+
+tq_status tq_write_kv(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, int num_kv_heads,
+                      int head_dim, int bits, const int64_t* slots, uint8_t* pages,
+                      int64_t num_blocks, int block_size, const float* signs,
+                      const float* centroids, int32_t* status_dev, void* stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 0 || block_size < 1)
+    return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: invalid sizes (tokens=%lld, kv_heads=%d, blocks=%lld, block_size=%d)",
+                (long long)num_tokens, num_kv_heads, (long long)num_blocks, block_size);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!bits_ok(bits)) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 2, 3, 4 or 5", bits);
+  if (!dtype_ok(raw_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: unknown raw dtype %d", (int)raw_dtype);
+  if (!status_dev) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: status_dev is required");
+  if (num_tokens > 0 && (!raw || !slots || !pages || !signs || !centroids))
+    return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: null pointer argument");
+  if (num_tokens > 0 && (!aligned(raw, 16) || !aligned(pages, 16) || !aligned(slots, 8) || !aligned(signs, 4) ||
+                         !aligned(centroids, 4) || !aligned(status_dev, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: raw and pages must be 16-byte aligned, slots 8-byte aligned");
+  tq::WriteArgs a{raw, (int)raw_dtype, num_tokens, num_kv_heads, head_dim, bits, slots, pages,
+                  num_blocks, block_size, signs, centroids, status_dev};
+  return check_cuda(tq::launch_write(a, static_cast<cudaStream_t>(stream)), "tq_write_kv launch");
+}
+
+size_t tq_paged_decode_workspace(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size) {
+  if (decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size) != TQ_OK)
+    return 0;
+  tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  return tq::plan_decode(a, current_device_sms()).workspace_bytes;
+}
+
+tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_heads,
+                          int num_kv_heads, int head_dim, const uint8_t* k_pages, int k_bits,
+                          const uint8_t* v_pages, int v_bits, int64_t num_blocks, int block_size,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, const float* signs, const float* k_centroids,
+                          const float* v_centroids, float scale, void* out, tq_dtype out_dtype,
+                          void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                          void* stream) {
+  tq_status st = decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  if (st != TQ_OK) return st;
+  if (!bits_ok(k_bits) || !bits_ok(v_bits))
+    return fail(TQ_ERR_UNSUPPORTED, "k_bits %d / v_bits %d: must be 2, 3, 4 or 5", k_bits, v_bits);
+  if (!dtype_ok(q_dtype) || !dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: unknown dtype");
+  if (num_blocks < 0) return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: num_blocks < 0");
+  if (batch > 0 && (!q || !k_pages || !v_pages || !seq_lens || !signs || !k_centroids || !v_centroids || !out ||
+                    (max_blocks_per_seq > 0 && !block_table)))
+    return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: null pointer argument");
+  if (batch > 0 && (!aligned(q, dtype_size(q_dtype)) || !aligned(out, dtype_size(out_dtype)) ||
+                    !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(block_table, 4) ||
+                    !aligned(seq_lens, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: misaligned pointer (pages need 16-byte alignment)");
+  tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  a.q = q;
+  a.q_dtype = (int)q_dtype;
+  a.k_pages = k_pages;
+  a.k_bits = k_bits;
+  a.v_pages = v_pages;
+  a.v_bits = v_bits;
+  a.num_blocks = num_blocks;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.signs = signs;
+  a.k_centroids = k_centroids;
+  a.v_centroids = v_centroids;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = (int)out_dtype;
+  a.workspace = workspace;
+  a.status = status_dev;
+  const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());
+  if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
+    return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: workspace must be >= %zu bytes and 16-byte aligned (got %zu)",
+                plan.workspace_bytes, workspace_bytes);
+  return check_cuda(tq::launch_decode(a, plan, static_cast<cudaStream_t>(stream)), "tq_paged_decode launch");
+}
+
+}  // extern "C"

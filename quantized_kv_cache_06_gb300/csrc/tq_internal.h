@@ -1,0 +1,79 @@
+// Internal declarations shared by the host API (tq_api.cpp) and the kernels
+// (tq_write.cu, tq_decode.cu).  Not part of the public C ABI (include/tq.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tq {
+
+// Status codes written to the device status word; same values as tq_status.
+enum : int32_t {
+  kOk = 0,
+  kInvalidArg = 1,
+  kUnsupported = 2,
+  kSlotOutOfRange = 3,
+  kBlockOutOfRange = 4,
+};
+
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+struct WriteArgs {
+  const void* raw;
+  int dtype;
+  int64_t num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int bits;
+  const int64_t* slots;
+  uint8_t* pages;
+  int64_t num_blocks;
+  int block_size;
+  const float* signs;
+  const float* centroids;
+  int32_t* status;
+};
+
+// Enqueues: status <- 0, slot validation, row write.  Returns the first launch error.
+cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream);
+
+struct DecodePlan {
+  int kernel;            // which decode kernel runs (see tq_decode.cu)
+  int num_splits;        // split-K factor per sequence
+  int blocks_per_split;  // KV blocks per split
+  size_t workspace_bytes;
+};
+
+struct DecodeArgs {
+  const void* q;
+  int q_dtype;
+  int batch;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  const uint8_t* k_pages;
+  int k_bits;
+  const uint8_t* v_pages;
+  int v_bits;
+  int64_t num_blocks;
+  int block_size;
+  const int32_t* block_table;
+  int max_blocks_per_seq;
+  const int32_t* seq_lens;
+  const float* signs;
+  const float* k_centroids;
+  const float* v_centroids;
+  float scale;
+  void* out;
+  int out_dtype;
+  void* workspace;
+  int32_t* status;  // may be null
+};
+
+// Split plan for the shapes in `a` on a device with `num_sms` SMs.
+DecodePlan plan_decode(const DecodeArgs& a, int num_sms);
+
+// Enqueues the decode for plan `p`.  Returns the first launch error.
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
+
+}  // namespace tq

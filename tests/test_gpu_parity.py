@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA writer and decode (through the C ABI) against the CPU oracle
+on the same seeded inputs, for the five workloads and the edge cases.
+
+Writer: packed index bytes bit-exact except near-boundary coordinates (counted),
+norms to 1e-6 relative.  Decode: |gpu - oracle| <= 2e-3 + 2e-3 |oracle|; the oracle
+decodes the very page bytes the GPU wrote.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tq_oracle as o
+from parity import OracleCodec, assert_decode_close, assert_rows_match, compare_rows
+from quantized_kv_cache_06_gb300.workloads import SWEEP, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tq():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for the gpu tests")
+    from quantized_kv_cache_06_gb300 import build
+
+    build.build_library()
+    import quantized_kv_cache_06_gb300 as tq
+
+    return tq
+
+
+def lib_codebook(tq, d, bits):
+    return tq.tq_codebook(d, bits, "cuda")[0]
+
+
+def gpu_write(tq, raw_np, slots_np, num_blocks, block_size, bits, pages=None):
+    t, h, d = raw_np.shape
+    raw = torch.from_numpy(np.ascontiguousarray(raw_np)).cuda()
+    slots = torch.from_numpy(np.ascontiguousarray(slots_np)).cuda()
+    if pages is None:
+        pages = torch.zeros(num_blocks, block_size, h, tq.tq_row_bytes(d, bits), dtype=torch.uint8, device="cuda")
+    signs = tq.tq_build_rotation(d, 42, "cuda")
+    st = tq.tq_write_kv(raw, pages, slots, signs, lib_codebook(tq, d, bits), check=False)
+    return pages, int(st.item())
+
+
+def check_written_rows(pages_np, raw_np, slots_np, bits, codec, sample_tokens=None):
+    nb, bs, h, rb = pages_np.shape
+    flat = pages_np.reshape(nb * bs, h, rb)
+    tok = np.nonzero(slots_np >= 0)[0]
+    if sample_tokens is not None and tok.size > sample_tokens:
+        tok = np.sort(np.random.default_rng(123).choice(tok, sample_tokens, replace=False))
+    rows = flat[slots_np[tok]].reshape(-1, rb)
+    raw = np.asarray(raw_np[tok], dtype=np.float64).reshape(-1, raw_np.shape[2])
+    stats = compare_rows(rows, raw, codec, bits)
+    assert_rows_match(stats)
+    return stats
+
+
+def check_untouched(pages_np, slots_np, fill=0):
+    nb, bs = pages_np.shape[:2]
+    written = np.zeros(nb * bs, dtype=bool)
+    written[slots_np[slots_np >= 0]] = True
+    assert np.all(pages_np.reshape(nb * bs, -1)[~written] == fill)
+
+
+def gpu_decode(tq, w, kp, vp, q=None, seq_lens=None, block_table=None, scale=None, out_dtype=None):
+    d = w.head_dim
+    q = torch.from_numpy(np.ascontiguousarray(w.q if q is None else q)).cuda()
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_table if block_table is None else block_table)).cuda()
+    lens = torch.from_numpy(np.ascontiguousarray(w.seq_lens if seq_lens is None else seq_lens)).cuda()
+    st = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    out = tq.tq_paged_decode(q, kp, vp, bt, lens, tq.tq_build_rotation(d, 42, "cuda"), lib_codebook(tq, d, w.k_bits),
+                             lib_codebook(tq, d, w.v_bits), scale=scale, out_dtype=out_dtype, status=st)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), int(st.item())
+
+
+def oracle_decode(w, kp_np, vp_np, codec, heads=None, **kw):
+    args = dict(q=w.q, k_pages=kp_np, v_pages=vp_np, k_bits=w.k_bits, v_bits=w.v_bits, block_table=w.block_table,
+                seq_lens=w.seq_lens, signs=codec.signs, k_centroids32=codec.centroids(w.k_bits),
+                v_centroids32=codec.centroids(w.v_bits), heads=heads)
+    args.update(kw)
+    return o.paged_decode(**args)
+
+
+def run_workload(tq, w, sample_tokens=None, heads=None):
+    codec = OracleCodec(w.head_dim)
+    kp, st = gpu_write(tq, w.k_raw, w.slots, w.num_blocks, w.block_size, w.k_bits)
+    assert st == 0
+    vp, st = gpu_write(tq, w.v_raw, w.slots, w.num_blocks, w.block_size, w.v_bits)
+    assert st == 0
+    kp_np, vp_np = kp.cpu().numpy(), vp.cpu().numpy()
+    ks = check_written_rows(kp_np, w.k_raw, w.slots, w.k_bits, codec, sample_tokens)
+    vs = check_written_rows(vp_np, w.v_raw, w.slots, w.v_bits, codec, sample_tokens)
+    check_untouched(kp_np, w.slots)
+    check_untouched(vp_np, w.slots)
+    got, st = gpu_decode(tq, w, kp, vp)
+    assert st == 0
+    ref = oracle_decode(w, kp_np, vp_np, codec, heads=heads)
+    if heads is not None:
+        sel = tuple(np.array(heads).T)
+        got, ref = got[sel], ref[sel]
+    worst = assert_decode_close(got, ref)
+    return ks, vs, worst
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_workload1_tiny(tq):
+    w = make_workload(1)
+    ks, vs, worst = run_workload(tq, w)
+    assert ks["coords"] == 64 * 2 * 128
+
+
+def test_workload1_rotated_form_and_contract_shape(tq):
+    # the contract example: pages [32, 16, 2, 68] at dim 128 / 4 bits
+    w = make_workload(1)
+    kp, _ = gpu_write(tq, w.k_raw, w.slots, 32, 16, 4)
+    assert tuple(kp.shape) == (32, 16, 2, 68)
+
+
+def test_workload2_mixed_bits(tq):
+    w = make_workload(2)
+    assert (w.slots < 0).mean() > 0.05
+    run_workload(tq, w)
+
+
+@pytest.mark.parametrize("sub", range(len(SWEEP)), ids=[f"b{b}_d{d}" for b, d in SWEEP])
+def test_workload3_sweep(tq, sub):
+    w = make_workload(3, sub=sub)
+    heads = [(b, j) for b in (0, 7, 15) for j in range(0, 32, 5)]
+    run_workload(tq, w, sample_tokens=3000, heads=heads)
+
+
+def test_workload4_full_size(tq):
+    w = make_workload(4)
+    heads = [(b, j) for b in (0, 21, 63) for j in (0, 5, 17, 31)]
+    run_workload(tq, w, sample_tokens=4000, heads=heads)
+
+
+def test_workload5_full_size_with_prefill_write(tq):
+    w = make_workload(5)
+    heads = [(b, j) for b in range(4) for j in (0, 13, 63)]
+    codec = OracleCodec(w.head_dim)
+    ks, vs, _ = run_workload(tq, w, sample_tokens=3000, heads=heads)
+    # prefill-style re-write of sequence 0 with 5% negative slots: the skipped rows keep the
+    # bytes of the first write, the others hold the new rows
+    kp, _ = gpu_write(tq, w.k_raw, w.slots, w.num_blocks, w.block_size, w.k_bits)
+    before = kp.cpu().numpy()
+    kp, st = gpu_write(tq, w.write_k, w.write_slots, w.num_blocks, w.block_size, w.k_bits, pages=kp)
+    assert st == 0
+    after = kp.cpu().numpy()
+    skipped = w.slots[: w.write_slots.shape[0]][w.write_slots < 0]
+    flat_b = before.reshape(-1, before.shape[2], before.shape[3])
+    flat_a = after.reshape(-1, after.shape[2], after.shape[3])
+    assert np.array_equal(flat_a[skipped], flat_b[skipped])
+    check_written_rows(after, w.write_k, w.write_slots, w.k_bits, codec, sample_tokens=3000)
+
+
+# ---------------------------------------------------------------- writer edge cases
+
+def test_write_empty_batch(tq):
+    raw = np.zeros((0, 2, 64), dtype=np.float16)
+    pages, st = gpu_write(tq, raw, np.zeros(0, dtype=np.int64), 2, 4, 4)
+    assert st == 0 and int(pages.sum()) == 0
+
+
+def test_write_out_of_range_slot_writes_nothing(tq):
+    rng = np.random.default_rng(9)
+    raw = rng.standard_normal((10, 2, 64)).astype(np.float16)
+    slots = np.arange(10, dtype=np.int64)
+    slots[7] = 2 * 4  # == num_blocks * block_size: one past the end
+    pages = torch.full((2, 4, 2, o.row_bytes(64, 3)), 0x5A, dtype=torch.uint8, device="cuda")
+    pages, st = gpu_write(tq, raw, slots, 2, 4, 3, pages=pages)
+    assert st == tq.TQ_ERR_SLOT_OUT_OF_RANGE
+    assert torch.all(pages == 0x5A)
+    with pytest.raises(tq.TQError) as e:
+        tq.tq_write_kv(torch.from_numpy(raw).cuda(), pages, torch.from_numpy(slots).cuda(),
+                       tq.tq_build_rotation(64, 42, "cuda"), lib_codebook(tq, 64, 3))
+    assert e.value.status == tq.TQ_ERR_SLOT_OUT_OF_RANGE
+
+
+def test_write_all_negative_slots(tq):
+    raw = np.random.default_rng(1).standard_normal((6, 2, 128)).astype(np.float16)
+    pages, st = gpu_write(tq, raw, -np.ones(6, dtype=np.int64), 2, 4, 4)
+    assert st == 0 and int(pages.sum()) == 0
+
+
+@pytest.mark.parametrize("dtype", [np.float32, "bf16"])
+@pytest.mark.parametrize("d,bits", [(32, 5), (64, 3), (256, 2)])
+def test_write_dtypes_and_dims(tq, dtype, d, bits):
+    rng = np.random.default_rng(d + bits)
+    raw32 = (rng.standard_normal((37, 3, d)) * rng.lognormal(0, 0.5, (3, d))).astype(np.float32)
+    slots = rng.permutation(40)[:37].astype(np.int64)
+    codec = OracleCodec(d)
+    if dtype == "bf16":
+        raw_t = torch.from_numpy(raw32).to(torch.bfloat16)
+        raw_exact = raw_t.float().numpy()
+        pages = torch.zeros(10, 4, 3, o.row_bytes(d, bits), dtype=torch.uint8, device="cuda")
+        st = tq.tq_write_kv(raw_t.cuda(), pages, torch.from_numpy(slots).cuda(), tq.tq_build_rotation(d, 42, "cuda"),
+                            lib_codebook(tq, d, bits), check=False)
+        st = int(st.item())
+    else:
+        raw_exact = raw32
+        pages, st = gpu_write(tq, raw32, slots, 10, 4, bits)
+    assert st == 0
+    check_written_rows(pages.cpu().numpy(), raw_exact, slots, bits, codec)
+
+
+def test_write_zero_row(tq):
+    raw = np.zeros((1, 1, 128), dtype=np.float16)
+    pages, st = gpu_write(tq, raw, np.array([0], dtype=np.int64), 1, 1, 4)
+    row = pages.cpu().numpy()[0, 0, 0]
+    # u = 0 sits on the middle decision point (exactly 0): every index is the lower middle one
+    assert np.all(o.unpack_indices(row[None, :64], 128, 4) == 7)
+    assert row[64:].tobytes() == b"\0\0\0\0"
+
+
+# ---------------------------------------------------------------- decode edge cases
+
+def _small_case(tq, d=64, h=2, hq=8, kb=3, vb=5, lens=(5, 0, 33, 16), bs=8, seed=4):
+    rng = np.random.default_rng(seed)
+    from quantized_kv_cache_06_gb300.workloads import Workload, _block_table, _slots
+
+    lens = np.array(lens, dtype=np.int32)
+    nb = int(sum(-(-int(n) // bs) for n in lens)) + 3
+    bt = _block_table(rng, lens, bs, nb)
+    slots = _slots(lens, bt, bs)
+    k = rng.standard_normal((slots.size, h, d)).astype(np.float16)
+    v = rng.standard_normal((slots.size, h, d)).astype(np.float16)
+    q = rng.standard_normal((lens.size, hq, d)).astype(np.float16)
+    w = Workload("small", d, kb, vb, hq, h, bs, nb, lens, bt, k, v, slots, q)
+    kp, st = gpu_write(tq, k, slots, nb, bs, kb)
+    vp, st2 = gpu_write(tq, v, slots, nb, bs, vb)
+    assert st == 0 and st2 == 0
+    return w, kp, vp
+
+
+@pytest.mark.parametrize("d,h,hq", [(32, 4, 4), (64, 2, 4), (128, 1, 8), (256, 2, 4)])
+def test_decode_groups_and_dims(tq, d, h, hq):
+    w, kp, vp = _small_case(tq, d=d, h=h, hq=hq)
+    got, st = gpu_decode(tq, w, kp, vp)
+    assert st == 0
+    ref = oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(d))
+    assert_decode_close(got, ref)
+    assert np.all(got[1] == 0)  # seq_len 0
+
+
+def test_decode_scale_and_out_dtype(tq):
+    w, kp, vp = _small_case(tq)
+    got, st = gpu_decode(tq, w, kp, vp, scale=0.05, out_dtype=torch.float32)
+    ref = oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(64), scale=0.05)
+    assert st == 0
+    assert_decode_close(got, ref)
+
+
+def test_decode_bad_block_id_is_skipped_and_reported(tq):
+    w, kp, vp = _small_case(tq)
+    bt = w.block_table.copy()
+    bt[2, 1] = w.num_blocks + 11
+    bt[3, 0] = -2
+    got, st = gpu_decode(tq, w, kp, vp, block_table=bt)
+    assert st == tq.TQ_ERR_BLOCK_OUT_OF_RANGE
+    ref, flag = oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(64), block_table=bt,
+                              return_flags=True)
+    assert flag
+    assert_decode_close(got, ref)
+
+
+def test_decode_seq_len_over_capacity_is_clamped_and_reported(tq):
+    w, kp, vp = _small_case(tq)
+    lens = w.seq_lens.copy()
+    cap = w.block_table.shape[1] * w.block_size
+    lens[0] = cap + 100
+    got, st = gpu_decode(tq, w, kp, vp, seq_lens=lens)
+    assert st == tq.TQ_ERR_INVALID_ARG
+    lens[0] = cap
+    ref = oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(64), seq_lens=lens)
+    assert_decode_close(got, ref)
+
+
+def test_decode_empty_batch(tq):
+    w, kp, vp = _small_case(tq)
+    q = torch.zeros((0, 8, 64), dtype=torch.float16, device="cuda")
+    out = tq.tq_paged_decode(q, kp, vp, torch.zeros((0, 4), dtype=torch.int32, device="cuda"),
+                             torch.zeros(0, dtype=torch.int32, device="cuda"), tq.tq_build_rotation(64, 42, "cuda"),
+                             lib_codebook(tq, 64, 3), lib_codebook(tq, 64, 5))
+    torch.cuda.synchronize()
+    assert out.shape == (0, 8, 64)

@@ -1,0 +1,112 @@
+"""The C-ABI library: it builds for sm_103a, loads, exports every entry point that
+include/tq.h declares, and its host-side set-up (row size, RHT signs, Lloyd-Max
+codebook, argument checks) agrees with the oracle.  No GPU work is launched here:
+every call below returns before enqueuing anything."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, read_golden_rows
+from oracle import tq_oracle as o
+
+HEADER = os.path.join(ROOT, "include", "tq.h")
+
+
+@pytest.fixture(scope="module")
+def tq():
+    from quantized_kv_cache_06_gb300 import build
+
+    build.build_library()
+    import quantized_kv_cache_06_gb300 as tq
+
+    return tq
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ["tq_build_rotation", "tq_codebook", "tq_write_kv", "tq_paged_decode", "tq_paged_decode_workspace",
+                 "tq_row_bytes", "tq_last_error"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(tq):
+    lib = ctypes.CDLL(tq.lib()._name)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    from quantized_kv_cache_06_gb300 import _lib
+
+    assert set(_lib.SIGNATURES) == set(declared_functions())
+
+
+def test_row_bytes_matches_pages_table(tq):
+    for line in read_golden_rows("row_bytes_d128.txt"):
+        d, b, _, rb = map(int, line.split())
+        assert tq.tq_row_bytes(d, b) == rb
+    for d in (32, 64, 128, 256):
+        for b in (2, 3, 4, 5):
+            assert tq.tq_row_bytes(d, b) == o.row_bytes(d, b)
+    assert tq.lib().tq_row_bytes(48, 4) == -1
+    assert tq.lib().tq_row_bytes(128, 6) == -1
+
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("seed", [0, 42, 2**63 + 5])
+def test_rotation_signs_match_oracle(tq, d, seed):
+    got = tq.tq_build_rotation(d, seed).numpy()
+    assert np.array_equal(got.astype(np.float64), o.splitmix64_signs(d, seed))
+
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5])
+def test_codebook_matches_oracle(tq, d, bits):
+    c_lib, b_lib = tq.tq_codebook(d, bits)
+    c64, _ = o.lloyd_max(d, bits)
+    c_or = c64.astype(np.float32)
+    c_lib = c_lib.numpy()
+    # two independent solvers (incomplete-beta CDF vs Gauss-Legendre quadrature) meet the
+    # same fixed point to ~1e-12; after rounding to fp32 at most a rare 1-ulp difference.
+    ulp = np.spacing(np.abs(c_or))
+    assert np.all(np.abs(c_lib - c_or) <= ulp)
+    assert np.mean(c_lib == c_or) > 0.9
+    assert np.array_equal(c_lib, -c_lib[::-1])
+    mids = (0.5 * (c_lib[:-1].astype(np.float64) + c_lib[1:])).astype(np.float32)
+    assert np.array_equal(b_lib.numpy(), mids)
+    assert b_lib.numpy()[(1 << bits) // 2 - 1] == 0.0
+
+
+def test_host_argument_errors(tq):
+    lib = tq.lib()
+    buf = (ctypes.c_float * 64)()
+    assert lib.tq_build_rotation(100, 1, ctypes.addressof(buf)) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_build_rotation(64, 1, None) == tq.TQ_ERR_INVALID_ARG
+    assert "NULL" in lib.tq_last_error().decode()
+    assert lib.tq_codebook(128, 1, ctypes.addressof(buf), None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_codebook(128, 4, ctypes.addressof(buf), None) == tq.TQ_OK
+    assert lib.tq_last_error().decode() == ""
+    # writer: missing status word, bad bits, bad head_dim -- all rejected on the host
+    dummy = 1 << 20
+    assert lib.tq_write_kv(dummy, 1, 4, 2, 128, 4, dummy, dummy, 4, 16, dummy, dummy, None, None) == \
+        tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_write_kv(dummy, 1, 4, 2, 128, 6, dummy, dummy, 4, 16, dummy, dummy, dummy, None) == \
+        tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_write_kv(dummy, 1, 4, 2, 96, 4, dummy, dummy, 4, 16, dummy, dummy, dummy, None) == \
+        tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_write_kv(dummy + 2, 1, 4, 2, 128, 4, dummy, dummy, 4, 16, dummy, dummy, dummy, None) == \
+        tq.TQ_ERR_INVALID_ARG  # misaligned raw
+    # decode: GQA group not dividing, unsupported group, bad bits
+    args = lambda hq, h, kb: (dummy, 1, 2, hq, h, 128, dummy, kb, dummy, 4, 8, 16, dummy, 4, dummy, dummy, dummy,
+                              dummy, 0.0, dummy, 1, dummy, 1 << 30, None, None)
+    assert lib.tq_paged_decode(*args(12, 8, 4)) == tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_paged_decode(*args(48, 3, 4)) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_paged_decode(*args(32, 8, 7)) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_paged_decode_workspace(2, 12, 8, 128, 4, 16) == 0
