@@ -147,6 +147,33 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
                           void* workspace, size_t workspace_bytes, int32_t* status_dev,
                           void* stream);
 
+/* Allocation-free variant of tq_paged_decode.  The TurboQuant pages have no
+ * counterpart: it exists for callers that cannot call cudaMalloc -- a plugin whose
+ * host framework owns all device memory, a deployment held to a fixed memory
+ * budget, or a latency-critical loop that must not hit cudaMalloc/cudaFree (which
+ * can synchronise the device).
+ *
+ * Arguments, semantics and errors are those of tq_paged_decode, without `workspace`
+ * and `workspace_bytes`: the split-K partials live in a fixed 16 MiB device array
+ * inside the library, which every GPU that loads the library keeps until the
+ * process exits.  The caller still passes every input and output.  Shapes whose
+ * partials exceed 16 MiB (tq_paged_decode_workspace(...) > 16 MiB) are rejected
+ * with TQ_ERR_INVALID_ARG and a message naming the size.
+ *
+ * The first call on each device looks the array's device address up (with that
+ * device current); make that first call before any stream capture.  All calls share
+ * the one array and it keeps the last call's contents (the decode overwrites every
+ * partial it reads, so nothing needs clearing); calls whose work overlaps on the
+ * GPU -- on different streams, or from different host threads -- race on it, so
+ * serialise them.  Calls no cudaMalloc, cudaFree or allocating routine. */
+tq_status tq_paged_decode_static(const void* q, tq_dtype q_dtype, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, const uint8_t* k_pages, int k_bits,
+                                 const uint8_t* v_pages, int v_bits, int64_t num_blocks, int block_size,
+                                 const int32_t* block_table, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, const float* signs, const float* k_centroids,
+                                 const float* v_centroids, float scale, void* out, tq_dtype out_dtype,
+                                 int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     tq_build_rotation,
     tq_codebook,
     tq_paged_decode,
+    tq_paged_decode_static,
     tq_paged_decode_workspace,
     tq_row_bytes,
     tq_write_kv,

@@ -47,6 +47,9 @@ SIGNATURES = {
     "tq_paged_decode": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
                                  _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_int,
                                  _c_p, _c_sz, _c_p, _c_p]),
+    "tq_paged_decode_static": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p,
+                                        _c_int, _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_f,
+                                        _c_p, _c_int, _c_p, _c_p]),
 }
 
 _lib = None
@@ -226,4 +229,27 @@ def tq_paged_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tenso
                                      _stream(dev)))
     if check and status is not None:
         raise_for_device_status(status)
+    return out
+
+
+def tq_paged_decode_static(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                           seq_lens: torch.Tensor, signs: torch.Tensor, k_centroids: torch.Tensor,
+                           v_centroids: torch.Tensor, out: torch.Tensor, scale: float | None = None,
+                           status: torch.Tensor | None = None) -> torch.Tensor:
+    """Allocation-free decode for callers that cannot allocate device memory: the caller
+    passes `out`, and the split-K partials go to the library's fixed 16 MiB device array
+    (so concurrent calls on different streams race; serialise them)."""
+    dev = _need_cuda("tq_paged_decode_static", q, k_pages, v_pages, block_table, seq_lens, signs, k_centroids,
+                     v_centroids, out)
+    b, hq, d = q.shape
+    nb, bs, h, _ = k_pages.shape
+    kb, vb = _bits_from_centroids(k_centroids), _bits_from_centroids(v_centroids)
+    if out.shape != q.shape or out.dtype not in _DTYPES:
+        raise ValueError("tq_paged_decode_static: out must be [B, Hq, D] f32/f16/bf16")
+    with torch.cuda.device(dev):
+        _check(lib().tq_paged_decode_static(_ptr(q), _DTYPES[q.dtype], b, hq, h, d, _ptr(k_pages), kb,
+                                            _ptr(v_pages), vb, nb, bs, _ptr(block_table), block_table.shape[1],
+                                            _ptr(seq_lens), _ptr(signs), _ptr(k_centroids), _ptr(v_centroids),
+                                            float(scale or 0.0), _ptr(out), _DTYPES[out.dtype], _ptr(status),
+                                            _stream(dev)))
     return out

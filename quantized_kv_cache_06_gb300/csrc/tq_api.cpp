@@ -302,4 +302,31 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
   return check_cuda(tq::launch_decode(a, plan, static_cast<cudaStream_t>(stream)), "tq_paged_decode launch");
 }
 
+tq_status tq_paged_decode_static(const void* q, tq_dtype q_dtype, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, const uint8_t* k_pages, int k_bits,
+                                 const uint8_t* v_pages, int v_bits, int64_t num_blocks, int block_size,
+                                 const int32_t* block_table, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, const float* signs, const float* k_centroids,
+                                 const float* v_centroids, float scale, void* out, tq_dtype out_dtype,
+                                 int32_t* status_dev, void* stream) {
+  // Same work as tq_paged_decode, with the split-K partials in the library's fixed
+  // device array instead of a caller-provided workspace.  Nothing is allocated.
+  void* scratch = nullptr;
+  size_t capacity = 0;
+  const cudaError_t err = tq::static_decode_scratch(&scratch, &capacity);
+  if (err != cudaSuccess)
+    return fail(TQ_ERR_CUDA, "tq_paged_decode_static: scratch address lookup failed: %s", cudaGetErrorString(err));
+  tq_status st = decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  if (st != TQ_OK) return st;
+  tq::DecodeArgs shape = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  const size_t need = tq::plan_decode(shape, current_device_sms()).workspace_bytes;
+  if (need > capacity)
+    return fail(TQ_ERR_INVALID_ARG,
+                "tq_paged_decode_static: these shapes need %zu bytes of scratch, more than the fixed %zu bytes; "
+                "use tq_paged_decode with a caller workspace", need, capacity);
+  return tq_paged_decode(q, q_dtype, batch, num_q_heads, num_kv_heads, head_dim, k_pages, k_bits, v_pages, v_bits,
+                         num_blocks, block_size, block_table, max_blocks_per_seq, seq_lens, signs, k_centroids,
+                         v_centroids, scale, out, out_dtype, scratch, capacity, status_dev, stream);
+}
+
 }  // extern "C"

@@ -20,6 +20,7 @@
 //                        and sign flip) and casts to the output dtype.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -257,6 +258,45 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t
     case 256: return launch_split<8>(a, p, part, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+}  // namespace tq
+
+// ---------------------------------------------------------------------------------
+// Fixed scratch for callers that cannot allocate device memory (tq_paged_decode_static).
+// The array lives for the life of the process on every device that loads the library.
+// Every call shares it, so calls whose work overlaps on the GPU race on it.  The
+// decode writes every partial it later reads, so nothing in it needs clearing.
+// ---------------------------------------------------------------------------------
+
+namespace tq {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB
+__device__ __align__(256) unsigned char g_static_decode_scratch[kStaticScratchBytes];
+
+std::mutex g_static_scratch_mutex;
+void* g_static_scratch_ptr[128] = {};
+
+}  // namespace
+
+cudaError_t static_decode_scratch(void** ptr, size_t* capacity) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+  if (g_static_scratch_ptr[dev] == nullptr) {
+    // The array's name in host code is only a host-side handle; the device address
+    // must come from the runtime, with this device current.
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_static_decode_scratch);
+    if (err != cudaSuccess) return err;
+    g_static_scratch_ptr[dev] = p;
+  }
+  *ptr = g_static_scratch_ptr[dev];
+  *capacity = kStaticScratchBytes;
+  return cudaSuccess;
 }
 
 }  // namespace tq

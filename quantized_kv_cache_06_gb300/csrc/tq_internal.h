@@ -77,3 +77,12 @@ DecodePlan plan_decode(const DecodeArgs& a, int num_sms);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 
 }  // namespace tq
+
+namespace tq {
+
+// Fixed device scratch for tq_paged_decode_static: a file-scope __device__ array in
+// tq_decode.cu.  Returns its device address on the current device (looked up once
+// per device with cudaGetSymbolAddress) and its capacity in bytes.
+cudaError_t static_decode_scratch(void** ptr, size_t* capacity);
+
+}  // namespace tq
