@@ -6,6 +6,7 @@
 // density, and the initial centroids from bisection on the quadrature CDF.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -156,6 +157,52 @@ const std::vector<float>& codebook_f32(int d, int bits) {
   return g_cb_cache.emplace(key, std::move(c32)).first->second;
 }
 
+// Nearest fp16 value of a positive double (ties to even), written out from the fp16
+// format: 11 significant bits, exponent floor at 2^-14 (subnormal spacing 2^-24).
+double round_to_fp16(double x) {
+  int e = 0;
+  std::frexp(x, &e);  // x = m 2^e, m in [0.5, 1)
+  const int ee = e < -13 ? -13 : e;
+  const double ulp = std::ldexp(1.0, ee - 11);
+  return std::nearbyint(x / ulp) * ulp;
+}
+
+// Scale alpha in [1, 2) that brings every alpha * |c_k| closest to an fp16 grid point
+// (the tensor-core decode stores V centroids as fp16(alpha * c) and divides by alpha
+// afterwards); minimises the largest relative rounding error.  Cached per (D, b).
+std::mutex g_alpha_mutex;
+std::map<std::pair<int, int>, float> g_alpha_cache;
+
+float fp16_scale_for(int d, int bits) {
+  const std::vector<float>& c = codebook_f32(d, bits);
+  std::lock_guard<std::mutex> lock(g_alpha_mutex);
+  auto key = std::make_pair(d, bits);
+  auto it = g_alpha_cache.find(key);
+  if (it != g_alpha_cache.end()) return it->second;
+  std::vector<double> mags;
+  for (float v : c)
+    if (v > 0.f) mags.push_back(v);
+  float best = 1.0f;
+  double best_err = 1e300;
+  const int steps = 1 << 18;
+  for (int i = 0; i < steps; ++i) {
+    const float alpha = (float)(1.0 + (double)i / steps);
+    double worst = 0.0;
+    for (double m : mags) {
+      const double exact = (double)alpha * m;
+      const double stored = round_to_fp16((double)(alpha * (float)m));
+      worst = std::fmax(worst, std::fabs(stored - exact) / exact);
+      if (worst >= best_err) break;
+    }
+    if (worst < best_err) {
+      best_err = worst;
+      best = alpha;
+    }
+  }
+  g_alpha_cache.emplace(key, best);
+  return best;
+}
+
 int current_device_sms() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
@@ -252,8 +299,15 @@ size_t tq_paged_decode_workspace(int batch, int num_q_heads, int num_kv_heads, i
                                  int max_blocks_per_seq, int block_size) {
   if (decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size) != TQ_OK)
     return 0;
+  // The kernel choice also depends on k_bits / v_bits, which this query does not take:
+  // return the larger of the SIMT plan and the tensor-core plan.
   tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
-  return tq::plan_decode(a, current_device_sms()).workspace_bytes;
+  const int sms = current_device_sms();
+  size_t need = tq::plan_decode(a, sms).workspace_bytes;  // k_bits = 0: SIMT plan
+  a.k_bits = 4;
+  a.v_bits = 4;
+  need = std::max(need, tq::plan_decode(a, sms).workspace_bytes);
+  return need;
 }
 
 tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_heads,
@@ -295,6 +349,8 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
   a.out_dtype = (int)out_dtype;
   a.workspace = workspace;
   a.status = status_dev;
+  a.v_alpha = 1.0f;
+  if (batch > 0 && tq::tc_decode_supported(a)) a.v_alpha = fp16_scale_for(head_dim, v_bits);
   const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());
   if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
     return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: workspace must be >= %zu bytes and 16-byte aligned (got %zu)",

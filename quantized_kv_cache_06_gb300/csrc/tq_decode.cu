@@ -233,6 +233,16 @@ cudaError_t launch_split(const DecodeArgs& a, const DecodePlan& p, SplitView par
 
 DecodePlan plan_decode(const DecodeArgs& a, int num_sms) {
   DecodePlan p{};
+  if (a.k_bits > 0 && tc_decode_supported(a)) {
+    // Tensor-core kernel: one CTA per SM over the flat block list; partial slots for
+    // every (CTA, sequence) pair and warp slot, plus the block prefix sums.
+    p.kernel = 2;
+    p.num_splits = num_sms;
+    p.blocks_per_split = 0;
+    const size_t slots = (size_t)tc_warps_per_head(a.head_dim) * (num_sms + a.batch);
+    p.workspace_bytes = slots * a.num_q_heads * (a.head_dim + 2) * sizeof(float) + (a.batch + 1) * sizeof(int) + 16;
+    return p;
+  }
   p.kernel = 1;
   const int units = std::max(1, a.batch * a.num_kv_heads);
   const int target = num_sms * 8;
@@ -250,6 +260,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t
     if (err != cudaSuccess) return err;
   }
   if (a.batch == 0) return cudaSuccess;
+  if (p.kernel == 2) return launch_decode_tc(a, p, stream);
   SplitView part = split_view(a.workspace, a.batch, a.num_q_heads, p.num_splits, a.head_dim);
   switch (a.head_dim) {
     case 32: return launch_split<1>(a, p, part, stream);

@@ -1,0 +1,689 @@
+// Tensor-core paged decode over packed TurboQuant pages (sm_103a, mma.sync f16 -> f32).
+//
+// TurboQuant docs: "vLLM Usage" (TQ Packed Page Contract: decode_tq4_paged) and
+// "Architecture" (Diagnostic vs Serving Paths: keys consumed compressed, packed-V).
+//
+// Work split.  The blocks of all sequences form one flat list (sequence-major); CTA i
+// of C owns the contiguous range [N*i/C, N*(i+1)/C).  Every CTA is busy for the same
+// number of blocks whatever the length mix, and a CTA emits one split partial per
+// (sequence it touches, warp slot), so the combine pass reads C + B partials at most.
+//
+// Per CTA: WPH warps per kv head (warp w: head w % H, block slot w / H).  A stage holds
+// WPH consecutive blocks; their whole K and V slabs (block_size * H * row_bytes bytes,
+// contiguous in the page tensor) are staged with 16-byte cp.async into shared memory,
+// K rows padded so that the fragment reads are bank-conflict free.
+//
+// Scores.  For a 16-token tile of one kv head the warp computes S[16 tok x 8 q-heads]
+// = Khat[16 x D] * qrot^T with m16n8k16 MMAs.  The A operand is looked up from the
+// packed bytes: each 2b-bit field (two neighbouring coordinates) indexes a table of
+// (fp16 hi, fp16 lo) centroid pairs, replicated per lane to avoid bank conflicts; the
+// query is split into fp16 hi + lo as well, and hi*hi + lo*hi + hi*lo carries ~22
+// significant bits, so the score keeps fp32-level accuracy even for very large norms.
+// The k order inside a fragment is a fixed permutation of the coordinates; the query
+// fragment follows the same permutation.
+//
+// Values.  Accumulated in rotated space with the contraction over (token, parity):
+// O'[pair][2g + e] += sum_t Vhat[t][2 pair + e] * P'[g][t], so one table entry gives
+// both coordinates of a pair of one token.  V centroids are stored as fp16(alpha * c),
+// alpha chosen on the host so that alpha * c lands near fp16 grid points; 1/alpha is
+// applied when the partial is written.  P' = p * nu_v in fp16.
+//
+// Softmax: online, base 2 (log2 e folded into the query), per q head.  Rows of tokens
+// past the sequence end are masked; blocks with an out-of-range id are skipped and
+// reported through the status word.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kBS = 16;       // tokens per block (the only block size this kernel takes)
+constexpr int kNStages = 3;   // cp.async ring depth (stages of WPH blocks)
+constexpr float kLog2eTc = 1.4426950408889634f;
+
+struct BlockMeta {
+  int b;      // sequence
+  int j;      // block index within the sequence
+  int ntok;   // valid tokens in the block (1..16); 0 = no block in this slot
+  int valid;  // block id inside [0, num_blocks)
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// D = A * B + D, m16n8k16, A row-major f16, B col-major f16, f32 accumulators.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Split x into fp16 hi + fp16 lo (x ~= hi + lo to ~22 significant bits).
+__device__ __forceinline__ void split_half(float x, __half& hi, __half& lo) {
+  hi = __float2half_rn(x);
+  lo = __float2half_rn(x - __half2float(hi));
+}
+
+// Field (pair index) e of a 32-bit word of packed indices, 2*BITS bits per field.
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_field(uint32_t w, int e) {
+  constexpr int F = 2 * BITS;
+  return (w >> (F * e)) & ((1u << F) - 1u);
+}
+
+template <int D, int KB, int VB, int G, int WPH>
+struct TcCfg {
+  static constexpr int kRBK = D * KB / 8 + 4;          // row bytes
+  static constexpr int kRBV = D * VB / 8 + 4;
+  static constexpr int kWK = D * KB / 32;              // index words per K row
+  static constexpr int kWV = D * VB / 32;
+  static constexpr int kPWK = 16 / KB;                 // pairs per word
+  static constexpr int kPWV = 16 / VB;
+  static constexpr int kKSteps = D / 16;               // score k-steps
+  static constexpr int kMTiles = D / 32;               // value m-tiles
+  static constexpr int kNT = (2 * G + 7) / 8;          // value n-tiles (N = 2G)
+  static constexpr int kFK = 2 * KB, kFV = 2 * VB;     // field widths
+  static constexpr int kLutKEntries = 1 << kFK;
+  static constexpr int kLutVEntries = 1 << kFV;
+  static constexpr int kLutKCopies = kFK == 8 ? 16 : 1;
+  static constexpr int kLutVCopies = kFV == 8 ? 32 : 1;
+  static constexpr int kLutKBytes = kLutKEntries * kLutKCopies * 8;
+  static constexpr int kLutVBytes = kLutVEntries * kLutVCopies * 4;
+  static_assert(kWK % 4 == 0, "K row must split into 4 interleaved word columns");
+  static_assert(kWV % 8 == 0, "V row must split into 8 interleaved word columns");
+  static_assert(G == 4 || G == 8, "GQA group 4 or 8");
+};
+
+struct TcArgs {
+  DecodeArgs a;
+  int num_ctas;           // C
+  int k_tok_stride;       // smem bytes per token in a K slab (H*RBK + pad)
+  int v_tok_stride;
+  int k_slab_smem;        // bytes per K block in smem
+  int v_slab_smem;
+  float v_alpha;          // V centroid scale
+  float* part_acc;        // [WPH*(C+B)][Hq][D]
+  float* part_ml;         // [WPH*(C+B)][Hq][2]
+  int* prefix;            // [B+1] block prefix sums (written by CTA 0)
+};
+
+template <int D, int KB, int VB, int G, int WPH>
+__global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args) {
+  using Cfg = TcCfg<D, KB, VB, G, WPH>;
+  const DecodeArgs& a = args.a;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int H = a.num_kv_heads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nthreads = blockDim.x;
+  const int cta = blockIdx.x, C = args.num_ctas;
+  const int B = a.batch;
+  const int cap = a.max_blocks_per_seq * kBS;
+
+  unsigned char* lutK = smem;
+  unsigned char* lutV = lutK + Cfg::kLutKBytes;
+  unsigned char* stage_base = lutV + Cfg::kLutVBytes;
+  const int stage_bytes = WPH * (args.k_slab_smem + args.v_slab_smem);
+  BlockMeta* meta = reinterpret_cast<BlockMeta*>(stage_base + kNStages * stage_bytes);
+  int* scan_tmp = reinterpret_cast<int*>(meta + kNStages * WPH);  // [32 + 4]
+
+  // ---- tables: K (hi, lo) pairs, V fp16(alpha c) pairs -----------------------------
+  for (int i = tid; i < Cfg::kLutKEntries * Cfg::kLutKCopies; i += nthreads) {
+    const int f = i / Cfg::kLutKCopies;
+    const float ca = __ldg(a.k_centroids + (f & ((1 << KB) - 1)));
+    const float cb = __ldg(a.k_centroids + (f >> KB));
+    __half ha, la, hb, lb;
+    split_half(ca, ha, la);
+    split_half(cb, hb, lb);
+    __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&hi2);
+    v.y = *reinterpret_cast<uint32_t*>(&lo2);
+    reinterpret_cast<uint2*>(lutK)[i] = v;
+  }
+  for (int i = tid; i < Cfg::kLutVEntries * Cfg::kLutVCopies; i += nthreads) {
+    const int f = i / Cfg::kLutVCopies;
+    const float ca = __ldg(a.v_centroids + (f & ((1 << VB) - 1))) * args.v_alpha;
+    const float cb = __ldg(a.v_centroids + (f >> VB)) * args.v_alpha;
+    reinterpret_cast<uint32_t*>(lutV)[i] = pack_half2(ca, cb);
+  }
+
+  // ---- flat block list: N, this CTA's range, its first and last sequence ------------
+  auto nblocks_of = [&](int b) -> int {
+    int len = __ldg(a.seq_lens + b);
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    return (len + kBS - 1) / kBS;
+  };
+  // pass 1: total blocks
+  int local = 0;
+  bool bad_len = false;
+  for (int b = tid; b < B; b += nthreads) {
+    const int len = __ldg(a.seq_lens + b);
+    bad_len |= (len < 0 || len > cap);
+    local += nblocks_of(b);
+  }
+  if (cta == 0 && a.status && __any_sync(kFullMask, bad_len) && lane == 0) atomicMax(a.status, (int32_t)kInvalidArg);
+  local = __reduce_add_sync(kFullMask, (unsigned)local);
+  if (lane == 0) scan_tmp[warp] = local;
+  __syncthreads();
+  long long N = 0;
+  for (int w = 0; w < nthreads / 32; ++w) N += scan_tmp[w];
+  const long long g_lo = N * cta / C, g_hi = N * (cta + 1) / C;
+  __syncthreads();
+  // pass 2: prefix sums; locate the sequences holding g_lo and g_hi - 1
+  if (tid == 0) {
+    scan_tmp[32] = -1;
+    scan_tmp[33] = -1;
+    scan_tmp[34] = 0;
+    scan_tmp[35] = 0;
+  }
+  int carry = 0;
+  for (int base = 0; base < B; base += nthreads) {
+    const int b = base + tid;
+    const int nb = b < B ? nblocks_of(b) : 0;
+    int incl = nb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    __syncthreads();
+    if (lane == 31) scan_tmp[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += scan_tmp[w];
+    int total = 0;
+    for (int w = 0; w < nthreads / 32; ++w) total += scan_tmp[w];
+    const int excl = carry + wbase + incl - nb;
+    if (b < B) {
+      if (cta == 0) args.prefix[b] = excl;
+      if (nb > 0 && excl <= g_lo && g_lo < excl + nb) {
+        scan_tmp[32] = b;
+        scan_tmp[34] = (int)(g_lo - excl);
+      }
+      if (nb > 0 && excl <= g_hi - 1 && g_hi - 1 < excl + nb) scan_tmp[33] = b;
+    }
+    carry += total;
+  }
+  if (cta == 0 && tid == 0) args.prefix[B] = carry;
+  __syncthreads();
+  if (g_lo >= g_hi) return;  // nothing to do (uniform)
+  const int b_first = scan_tmp[32], b_last = scan_tmp[33], j_first = scan_tmp[34];
+
+  // ---- producer cursor (every thread keeps the same copy) ---------------------------
+  int pb = b_first, pj = j_first, pnb = nblocks_of(b_first);
+  long long pg = g_lo;
+  const long long total_blocks = g_hi - g_lo;
+  const int nstages = (int)((total_blocks + WPH - 1) / WPH);
+
+  const int k_chunks_row = H * Cfg::kRBK / 16;  // 16-byte chunks per token (when padded layout)
+  const bool k_padded = (H * Cfg::kRBK) % 16 == 0;
+  const bool v_padded = (H * Cfg::kRBV) % 16 == 0;
+  const int k_slab = kBS * H * Cfg::kRBK, v_slab = kBS * H * Cfg::kRBV;
+
+  auto issue_stage = [&](int st) {
+    const int buf = st % kNStages;
+    unsigned char* sb = stage_base + buf * stage_bytes;
+    for (int u = 0; u < WPH; ++u) {
+      BlockMeta m{0, 0, 0, 0};
+      int bid = -1;
+      if (pg < g_hi) {
+        m.b = pb;
+        m.j = pj;
+        int len = __ldg(a.seq_lens + pb);
+        len = len < 0 ? 0 : (len > cap ? cap : len);
+        m.ntok = min(kBS, len - pj * kBS);
+        bid = __ldg(a.block_table + (int64_t)pb * a.max_blocks_per_seq + pj);
+        m.valid = (bid >= 0 && (int64_t)bid < a.num_blocks);
+        // advance the cursor
+        ++pg;
+        if (++pj == pnb && pg < g_hi) {
+          do {
+            ++pb;
+            pnb = nblocks_of(pb);
+          } while (pnb == 0);
+          pj = 0;
+        }
+      }
+      if (tid == 0) meta[buf * WPH + u] = m;
+      if (m.ntok > 0 && !m.valid && tid == 0 && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+      if (m.ntok > 0 && m.valid) {
+        const unsigned char* ksrc = a.k_pages + (int64_t)bid * k_slab;
+        const unsigned char* vsrc = a.v_pages + (int64_t)bid * v_slab;
+        unsigned char* kdst = sb + u * (args.k_slab_smem + args.v_slab_smem);
+        unsigned char* vdst = kdst + args.k_slab_smem;
+        const int kc = k_slab / 16, vc = v_slab / 16;
+        for (int c = tid; c < kc; c += nthreads) {
+          const int tok = k_padded ? c / k_chunks_row : 0;
+          const int off = k_padded ? tok * args.k_tok_stride + (c - tok * k_chunks_row) * 16 : c * 16;
+          cp_async16(smem_u32(kdst + off), ksrc + c * 16);
+        }
+        const int v_chunks_row = H * Cfg::kRBV / 16;
+        for (int c = tid; c < vc; c += nthreads) {
+          const int tok = v_padded ? c / v_chunks_row : 0;
+          const int off = v_padded ? tok * args.v_tok_stride + (c - tok * v_chunks_row) * 16 : c * 16;
+          cp_async16(smem_u32(vdst + off), vsrc + c * 16);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  __syncthreads();  // tables ready before anyone reads them (also orders meta writes)
+
+  // ---- consumer state ----------------------------------------------------------------
+  const int h = warp % H;
+  const int slot_u = warp / H;
+  const int r = lane >> 2, c = lane & 3;
+  const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
+  const float qmul = scale * kLog2eTc / sqrtf((float)D);
+  const uint32_t lutK_lane = smem_u32(lutK) + (Cfg::kLutKCopies > 1 ? (lane & 15) * 8 : 0);
+  const uint32_t lutV_lane = smem_u32(lutV) + (Cfg::kLutVCopies > 1 ? lane * 4 : 0);
+  // value-B selectors: the P value goes to the low half when (r & 1) == 0, else the high half
+  const int hsel = (r >> 1) & 1;
+  const uint32_t sel_b = (r & 1) ? (0x0044u | ((2u * hsel) << 8) | ((2u * hsel + 1u) << 12))
+                                 : ((2u * hsel) | ((2u * hsel + 1u) << 4) | 0x4400u);
+
+  uint32_t bq_hi[Cfg::kKSteps][2], bq_lo[Cfg::kKSteps][2];
+  float o_acc[Cfg::kNT][Cfg::kMTiles][4];
+  float m_run[2], l_run[2];
+  int cur_b = -1;
+
+  auto reset_state = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < Cfg::kNT; ++nt)
+#pragma unroll
+      for (int i = 0; i < Cfg::kMTiles; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o_acc[nt][i][e] = 0.f;
+    m_run[0] = m_run[1] = -INFINITY;
+    l_run[0] = l_run[1] = 0.f;
+  };
+
+  // Rotated query of sequence b for this warp's G heads -> hi/lo B fragments.
+  auto load_query = [&](int b) {
+    constexpr int E = D / 32;
+    float qr[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int64_t base = ((int64_t)b * a.num_q_heads + (int64_t)h * G + g) * D + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i) qr[g][i] = load_as_f32(a.q, base + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
+      fwht_warp<E>(qr[g]);
+#pragma unroll
+      for (int i = 0; i < E; ++i) qr[g][i] *= qmul;
+    }
+    const int gq = r;  // this lane's B column (q head); columns >= G are zero
+#pragma unroll
+    for (int s = 0; s < Cfg::kKSteps; ++s) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = 2 * s + u;
+        const int jw = q / Cfg::kPWK, e = q % Cfg::kPWK;
+        const int p = Cfg::kPWK * (c + 4 * jw) + e;  // pair index; coordinates 2p, 2p+1
+        const int src = (2 * p) / E;
+        const int off = (2 * p) % E;  // identical on every lane (see the pair layout)
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float v0 = __shfl_sync(kFullMask, qr[g][off], src);
+          const float v1 = __shfl_sync(kFullMask, qr[g][(off + 1) % E], E == 1 ? src + 1 : src);
+          if (g == gq) {
+            x0 = v0;
+            x1 = v1;
+          }
+        }
+        __half h0, l0, h1, l1;
+        split_half(x0, h0, l0);
+        split_half(x1, h1, l1);
+        __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
+        bq_hi[s][u] = *reinterpret_cast<uint32_t*>(&hh);
+        bq_lo[s][u] = *reinterpret_cast<uint32_t*>(&ll);
+      }
+    }
+  };
+
+  const float inv_alpha = 1.0f / args.v_alpha;
+  // Writes this warp's partial for sequence b (empty when `empty`).
+  auto flush = [&](int b, bool empty) {
+    const int64_t slot = (int64_t)WPH * (cta + b) + slot_u;
+    // l: reduce the per-lane partial sums over the 8 row groups
+    float lsum[2] = {l_run[0], l_run[1]};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 4);
+      lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 8);
+      lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 16);
+    }
+    // score layout: lane (r, c) holds q heads 2c, 2c+1
+    if (r == 0) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int g = 2 * c + e;
+        if (g < G) {
+          float* ml = args.part_ml + (slot * a.num_q_heads + (int64_t)h * G + g) * 2;
+          ml[0] = empty ? -INFINITY : m_run[e];
+          ml[1] = empty ? 0.f : lsum[e];
+        }
+      }
+    }
+    // value layout: lane (r, c) holds q head c + 4 nt, pairs p_v(r, 2i + half)
+#pragma unroll
+    for (int nt = 0; nt < Cfg::kNT; ++nt) {
+      const int g = c + 4 * nt;
+      if (g < G) {
+        float* acc = args.part_acc + (slot * a.num_q_heads + (int64_t)h * G + g) * D;
+#pragma unroll
+        for (int i = 0; i < Cfg::kMTiles; ++i) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int q = 2 * i + half;
+            const int pv = Cfg::kPWV * (r + 8 * (q / Cfg::kPWV)) + (q % Cfg::kPWV);
+            float2 v;
+            v.x = empty ? 0.f : o_acc[nt][i][2 * half] * inv_alpha;
+            v.y = empty ? 0.f : o_acc[nt][i][2 * half + 1] * inv_alpha;
+            *reinterpret_cast<float2*>(acc + 2 * pv) = v;
+          }
+        }
+      }
+    }
+  };
+
+  // Move this warp to sequence b: close the current one and any non-empty sequences
+  // of this CTA in between (they get empty partials), then load b's query.
+  auto enter_sequence = [&](int b) {
+    int from = cur_b;
+    if (from >= 0) flush(from, false);
+    for (int x = (from < 0 ? b_first : from + 1); x < b; ++x)
+      if (nblocks_of(x) > 0) flush(x, true);
+    reset_state();
+    cur_b = b;
+    load_query(b);
+  };
+
+  // ---- main pipeline -----------------------------------------------------------------
+  for (int st = 0; st < kNStages - 1; ++st) {
+    if (st < nstages) issue_stage(st);
+    else cp_async_commit();
+  }
+
+  for (int st = 0; st < nstages; ++st) {
+    cp_async_wait<kNStages - 2>();
+    __syncthreads();
+    if (st + kNStages - 1 < nstages) issue_stage(st + kNStages - 1);
+    else cp_async_commit();
+
+    const int buf = st % kNStages;
+    const BlockMeta m = meta[buf * WPH + slot_u];
+    if (m.ntok == 0) continue;
+    if (m.b != cur_b) enter_sequence(m.b);
+    if (!m.valid) continue;
+
+    const unsigned char* kblk = stage_base + buf * stage_bytes + slot_u * (args.k_slab_smem + args.v_slab_smem);
+    const unsigned char* vblk = kblk + args.k_slab_smem;
+    const uint32_t kbase = smem_u32(kblk) + h * Cfg::kRBK;
+    const uint32_t vbase = smem_u32(vblk) + h * Cfg::kRBV;
+    const int kts = args.k_tok_stride, vts = args.v_tok_stride;
+
+    // --- scores S[tok][q head] -------------------------------------------------------
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
+      const uint32_t w0 = lds32(kbase + r * kts + (c + 4 * jw) * 4);
+      const uint32_t w1 = lds32(kbase + (r + 8) * kts + (c + 4 * jw) * 4);
+#pragma unroll
+      for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
+        const int s = (jw * Cfg::kPWK + e2) >> 1;
+        const uint2 x00 = lds64(lutK_lane + pair_field<KB>(w0, e2) * (8 * Cfg::kLutKCopies));
+        const uint2 x10 = lds64(lutK_lane + pair_field<KB>(w1, e2) * (8 * Cfg::kLutKCopies));
+        const uint2 x01 = lds64(lutK_lane + pair_field<KB>(w0, e2 + 1) * (8 * Cfg::kLutKCopies));
+        const uint2 x11 = lds64(lutK_lane + pair_field<KB>(w1, e2 + 1) * (8 * Cfg::kLutKCopies));
+        mma16816(sacc, x00.x, x10.x, x01.x, x11.x, bq_hi[s][0], bq_hi[s][1]);
+        mma16816(sacc, x00.x, x10.x, x01.x, x11.x, bq_lo[s][0], bq_lo[s][1]);
+        mma16816(sacc, x00.y, x10.y, x01.y, x11.y, bq_hi[s][0], bq_hi[s][1]);
+      }
+    }
+    // rows r, r+8 of the tile: token norms and masking
+    const float kn0 = __uint_as_float(lds32(kbase + r * kts + Cfg::kWK * 4));
+    const float kn1 = __uint_as_float(lds32(kbase + (r + 8) * kts + Cfg::kWK * 4));
+    const float vn0 = __uint_as_float(lds32(vbase + r * vts + Cfg::kWV * 4));
+    const float vn1 = __uint_as_float(lds32(vbase + (r + 8) * vts + Cfg::kWV * 4));
+    float sc[4];
+    sc[0] = r < m.ntok ? sacc[0] * kn0 : -INFINITY;
+    sc[1] = r < m.ntok ? sacc[1] * kn0 : -INFINITY;
+    sc[2] = r + 8 < m.ntok ? sacc[2] * kn1 : -INFINITY;
+    sc[3] = r + 8 < m.ntok ? sacc[3] * kn1 : -INFINITY;
+
+    // --- online softmax (q heads 2c, 2c+1 on this lane) ------------------------------
+    float corr[2], pv[4];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float mt = fmaxf(sc[e], sc[2 + e]);
+      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 4));
+      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
+      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
+      const float mn = fmaxf(m_run[e], mt);
+      corr[e] = exp2f(m_run[e] - mn);
+      const float p0 = exp2f(sc[e] - mn), p1 = exp2f(sc[2 + e] - mn);
+      l_run[e] = l_run[e] * corr[e] + p0 + p1;
+      m_run[e] = mn;
+      pv[e] = p0 * vn0;
+      pv[2 + e] = p1 * vn1;
+    }
+    // rescale the value accumulators (value layout holds q head c + 4 nt)
+    const bool any_rescale = __any_sync(kFullMask, corr[0] != 1.f || corr[1] != 1.f);
+    if (any_rescale) {
+#pragma unroll
+      for (int nt = 0; nt < Cfg::kNT; ++nt) {
+        const int g = c + 4 * nt;
+        const int srcl = (g >> 1) & 3;  // lane (r'=0, c'=g>>1)
+        const float c0 = __shfl_sync(kFullMask, corr[0], srcl);
+        const float c1 = __shfl_sync(kFullMask, corr[1], srcl);
+        const float cg = (g & 1) ? c1 : c0;
+#pragma unroll
+        for (int i = 0; i < Cfg::kMTiles; ++i)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o_acc[nt][i][e] *= cg;
+      }
+    }
+    const uint32_t p01 = pack_half2(pv[0], pv[1]);  // token r:   heads 2c, 2c+1
+    const uint32_t p23 = pack_half2(pv[2], pv[3]);  // token r+8: heads 2c, 2c+1
+
+    // --- values ------------------------------------------------------------------------
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {  // tokens {c, c+4} (ks=0) and {c+8, c+12} (ks=1)
+      const int t0 = c + 8 * ks, t1 = c + 4 + 8 * ks;
+      uint32_t bv[Cfg::kNT][2];
+#pragma unroll
+      for (int nt = 0; nt < Cfg::kNT; ++nt) {
+        const int cs = 2 * nt + (r >> 2);  // source lane column: q head (4 nt + r/2) / 2
+        const uint32_t src = ks == 0 ? p01 : p23;
+        const uint32_t x0 = __shfl_sync(kFullMask, src, 4 * c + cs);
+        const uint32_t x1 = __shfl_sync(kFullMask, src, 4 * (c + 4) + cs);
+        bv[nt][0] = __byte_perm(x0, 0u, sel_b);
+        bv[nt][1] = __byte_perm(x1, 0u, sel_b);
+      }
+#pragma unroll
+      for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
+        const uint32_t wa = lds32(vbase + t0 * vts + (r + 8 * jw) * 4);
+        const uint32_t wb = lds32(vbase + t1 * vts + (r + 8 * jw) * 4);
+#pragma unroll
+        for (int e = 0; e < Cfg::kPWV; e += 2) {
+          const int i = (jw * Cfg::kPWV + e) >> 1;  // m-tile: pairs q = 2i (row r), 2i+1 (row r+8)
+          const uint32_t a0 = lds32(lutV_lane + pair_field<VB>(wa, e) * (4 * Cfg::kLutVCopies));
+          const uint32_t a1 = lds32(lutV_lane + pair_field<VB>(wa, e + 1) * (4 * Cfg::kLutVCopies));
+          const uint32_t a2 = lds32(lutV_lane + pair_field<VB>(wb, e) * (4 * Cfg::kLutVCopies));
+          const uint32_t a3 = lds32(lutV_lane + pair_field<VB>(wb, e + 1) * (4 * Cfg::kLutVCopies));
+#pragma unroll
+          for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+        }
+      }
+    }
+  }
+  // close the last sequence and any later non-empty ones this CTA owns
+  if (cur_b < 0) {
+    for (int x = b_first; x <= b_last; ++x)
+      if (nblocks_of(x) > 0) flush(x, true);
+  } else {
+    flush(cur_b, false);
+    for (int x = cur_b + 1; x <= b_last; ++x)
+      if (nblocks_of(x) > 0) flush(x, true);
+  }
+  cp_async_wait<0>();
+}
+
+// One warp per (sequence, q head): merge the partials of the CTAs that touched the
+// sequence, normalise, apply R^T (FWHT + sign flip) and store.
+template <int E, int WPH>
+__global__ void __launch_bounds__(256)
+combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc, const float* __restrict__ part_ml,
+                  const int* __restrict__ prefix) {
+  constexpr int D = 32 * E;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= a.batch * a.num_q_heads) return;
+  const int b = row / a.num_q_heads, j = row - b * a.num_q_heads;
+  const long long N = prefix[a.batch];
+  const long long p0 = prefix[b], p1 = prefix[b + 1];
+  float v[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) v[i] = 0.f;
+  if (p1 > p0) {
+    const long long C = num_ctas;
+    const long long f = ((p0 + 1) * C - 1) / N, l = (p1 * C - 1) / N;  // first / last CTA
+    // CTAs whose block range is empty (possible when N < C) wrote nothing
+    auto owns_blocks = [&](long long i) { return N * i / C < N * (i + 1) / C; };
+    float mx = -INFINITY;
+    for (long long i = f; i <= l; ++i)
+      if (owns_blocks(i))
+        for (int u = 0; u < WPH; ++u) mx = fmaxf(mx, part_ml[((WPH * (i + b) + u) * a.num_q_heads + j) * 2]);
+    float lsum = 0.f;
+    for (long long i = f; i <= l; ++i) {
+      if (!owns_blocks(i)) continue;
+      for (int u = 0; u < WPH; ++u) {
+        const int64_t s = (WPH * (i + b) + u) * a.num_q_heads + j;
+        const float ms = part_ml[s * 2];
+        const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+        lsum = fmaf(w, part_ml[s * 2 + 1], lsum);
+#pragma unroll
+        for (int k = 0; k < E; ++k) v[k] = fmaf(w, part_acc[s * D + lane * E + k], v[k]);
+      }
+    }
+    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+#pragma unroll
+    for (int k = 0; k < E; ++k) v[k] *= inv;
+  }
+  fwht_warp<E>(v);
+  const float rs = 1.0f / sqrtf((float)D);
+#pragma unroll
+  for (int k = 0; k < E; ++k)
+    store_from_f32(a.out, (int64_t)row * D + lane * E + k, a.out_dtype, v[k] * __ldg(a.signs + lane * E + k) * rs);
+}
+
+template <int D, int KB, int VB, int G, int WPH>
+cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
+  using Cfg = TcCfg<D, KB, VB, G, WPH>;
+  TcArgs t{};
+  t.a = a;
+  t.num_ctas = p.num_splits;
+  const int H = a.num_kv_heads;
+  const int kraw = H * Cfg::kRBK, vraw = H * Cfg::kRBV;
+  // K: pad each token to a stride of 4*odd words mod 32 (conflict-free fragment reads)
+  int kpad = 0, vpad = 0;
+  if (kraw % 16 == 0)
+    for (int pad = 0; pad < 8; ++pad)
+      if ((((kraw + 16 * pad) / 4) % 32) % 8 == 4) { kpad = 16 * pad; break; }
+  if (vraw % 16 == 0)
+    for (int pad = 0; pad < 8; ++pad) {
+      const int w = ((vraw + 16 * pad) / 4) % 32;
+      if (w == 8 || w == 24) { vpad = 16 * pad; break; }
+    }
+  t.k_tok_stride = (kraw % 16 == 0) ? kraw + kpad : kraw;
+  t.v_tok_stride = (vraw % 16 == 0) ? vraw + vpad : vraw;
+  t.k_slab_smem = (kBS * t.k_tok_stride + 15) / 16 * 16;
+  t.v_slab_smem = (kBS * t.v_tok_stride + 15) / 16 * 16;
+  t.v_alpha = a.v_alpha > 0.f ? a.v_alpha : 1.0f;
+  const int B = a.batch, Hq = a.num_q_heads;
+  const int64_t slots = (int64_t)WPH * (p.num_splits + B);
+  t.part_acc = static_cast<float*>(a.workspace);
+  t.part_ml = t.part_acc + slots * Hq * D;
+  t.prefix = reinterpret_cast<int*>(t.part_ml + slots * Hq * 2);
+  const size_t smem = Cfg::kLutKBytes + Cfg::kLutVBytes +
+                      (size_t)kNStages * WPH * (t.k_slab_smem + t.v_slab_smem) +
+                      kNStages * WPH * sizeof(BlockMeta) + 36 * sizeof(int);
+  auto kern = decode_tc_kernel<D, KB, VB, G, WPH>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<p.num_splits, 32 * H * WPH, smem, stream>>>(t);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int rows = B * Hq;
+  combine_tc_kernel<D / 32, WPH><<<(rows + 7) / 8, 256, 0, stream>>>(a, p.num_splits, t.part_acc, t.part_ml,
+                                                                     t.prefix);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_decode_supported(const DecodeArgs& a) {
+  const int G = a.num_kv_heads > 0 ? a.num_q_heads / a.num_kv_heads : 0;
+  const bool bits_ok = (a.k_bits == 2 || a.k_bits == 4) && (a.v_bits == 2 || a.v_bits == 4);
+  // exactly the instantiations in launch_decode_tc
+  const bool dim_ok = a.head_dim == 128 || a.head_dim == 256 || (a.head_dim == 64 && a.k_bits == 4 && a.v_bits == 4);
+  return a.block_size == kBS && a.num_kv_heads >= 1 && a.num_kv_heads <= 8 && (G == 4 || G == 8) && bits_ok && dim_ok;
+}
+
+int tc_warps_per_head(int head_dim) { return head_dim >= 256 ? 1 : 2; }
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+#define TQ_TC_CASE(D, KB, VB, GG, WPH)                                                    \
+  if (a.head_dim == D && a.k_bits == KB && a.v_bits == VB && G == GG)                     \
+    return launch_tc_typed<D, KB, VB, GG, WPH>(a, p, stream);
+#define TQ_TC_BITS(D, GG, WPH) \
+  TQ_TC_CASE(D, 4, 4, GG, WPH) TQ_TC_CASE(D, 4, 2, GG, WPH) TQ_TC_CASE(D, 2, 4, GG, WPH) TQ_TC_CASE(D, 2, 2, GG, WPH)
+  TQ_TC_BITS(128, 4, 2)
+  TQ_TC_BITS(128, 8, 2)
+  TQ_TC_BITS(256, 4, 1)
+  TQ_TC_BITS(256, 8, 1)
+  TQ_TC_CASE(64, 4, 4, 4, 2)
+  TQ_TC_CASE(64, 4, 4, 8, 2)
+#undef TQ_TC_BITS
+#undef TQ_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tq

@@ -68,7 +68,14 @@ struct DecodeArgs {
   int out_dtype;
   void* workspace;
   int32_t* status;  // may be null
+  float v_alpha;    // fp16 scale of the V centroids (tensor-core decode); 1 when unknown
 };
+
+// Tensor-core decode (tq_decode_tc.cu): whether the shapes/bits in `a` have an
+// instantiation, its warps per kv head, and its launch.
+bool tc_decode_supported(const DecodeArgs& a);
+int tc_warps_per_head(int head_dim);
+cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 
 // Split plan for the shapes in `a` on a device with `num_sms` SMs.
 DecodePlan plan_decode(const DecodeArgs& a, int num_sms);

@@ -288,3 +288,59 @@ def test_decode_empty_batch(tq):
                              lib_codebook(tq, 64, 3), lib_codebook(tq, 64, 5))
     torch.cuda.synchronize()
     assert out.shape == (0, 8, 64)
+
+
+# ---------------------------------------------------------------- tensor-core decode edge cases
+# (block size 16, K/V bits in {2, 4}, GQA group 4 or 8: the shapes the tensor-core kernel takes)
+
+@pytest.mark.parametrize("kb,vb,hq", [(4, 4, 32), (4, 2, 32), (2, 4, 64), (2, 2, 64), (4, 2, 64)])
+def test_tc_decode_ragged_and_empty_sequences(tq, kb, vb, hq):
+    # lengths with empty sequences in the middle, ragged last blocks, a single token, and
+    # fewer blocks in total than there are SMs (some CTAs own no block)
+    w, kp, vp = _small_case(tq, d=128, h=8, hq=hq, kb=kb, vb=vb, lens=(5, 0, 33, 16, 1, 0, 200, 17), bs=16, seed=kb * 10 + vb)
+    got, st = gpu_decode(tq, w, kp, vp)
+    assert st == 0
+    ref = oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(128))
+    assert_decode_close(got, ref)
+    assert np.all(got[1] == 0) and np.all(got[5] == 0)
+
+
+@pytest.mark.parametrize("d", [64, 256])
+def test_tc_decode_other_head_dims(tq, d):
+    w, kp, vp = _small_case(tq, d=d, h=4, hq=16, kb=4, vb=4, lens=(70, 3, 129), bs=16, seed=d)
+    got, st = gpu_decode(tq, w, kp, vp)
+    assert st == 0
+    assert_decode_close(got, oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(d)))
+
+
+def test_tc_decode_bad_block_and_over_capacity(tq):
+    w, kp, vp = _small_case(tq, d=128, h=8, hq=32, kb=4, vb=2, lens=(40, 64, 7), bs=16, seed=5)
+    bt = w.block_table.copy()
+    bt[1, 2] = w.num_blocks + 3
+    got, st = gpu_decode(tq, w, kp, vp, block_table=bt)
+    assert st == tq.TQ_ERR_BLOCK_OUT_OF_RANGE
+    ref, flag = oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(128), block_table=bt,
+                              return_flags=True)
+    assert flag
+    assert_decode_close(got, ref)
+    lens = w.seq_lens.copy()
+    lens[2] = w.block_table.shape[1] * 16 + 40
+    got, st = gpu_decode(tq, w, kp, vp, seq_lens=lens)
+    assert st == tq.TQ_ERR_INVALID_ARG
+    lens[2] = w.block_table.shape[1] * 16
+    assert_decode_close(got, oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(128), seq_lens=lens))
+
+
+def test_tc_decode_many_short_sequences(tq):
+    # more sequences than SMs: CTAs cover several sequences each
+    rng = np.random.default_rng(17)
+    lens = tuple(int(x) for x in rng.integers(0, 50, size=300))
+    w, kp, vp = _small_case(tq, d=128, h=8, hq=32, kb=4, vb=4, lens=lens, bs=16, seed=17)
+    got, st = gpu_decode(tq, w, kp, vp)
+    assert st == 0
+    heads = [(b, j) for b in range(0, 300, 7) for j in (0, 9, 31)]
+    ref = oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(128), heads=heads)
+    sel = tuple(np.array(heads).T)
+    assert_decode_close(got[sel], ref[sel])
+    empty = [b for b, n in enumerate(lens) if n == 0]
+    assert np.all(got[empty] == 0)
