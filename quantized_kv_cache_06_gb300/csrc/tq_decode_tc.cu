@@ -66,15 +66,15 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
+__device__ __forceinline__ uint32_t ld32(const unsigned char* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint2 ld64(const unsigned char* p) { return *reinterpret_cast<const uint2*>(p); }
+
+// 2^x with the hardware approximation (denormal results flush to zero): the softmax
+// weights it produces are relative to the running max, so tiny values do not matter.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // D = A * B + D, m16n8k16, A row-major f16, B col-major f16, f32 accumulators.
@@ -98,13 +98,6 @@ __device__ __forceinline__ void split_half(float x, __half& hi, __half& lo) {
   lo = __float2half_rn(x - __half2float(hi));
 }
 
-// Field (pair index) e of a 32-bit word of packed indices, 2*BITS bits per field.
-template <int BITS>
-__device__ __forceinline__ uint32_t pair_field(uint32_t w, int e) {
-  constexpr int F = 2 * BITS;
-  return (w >> (F * e)) & ((1u << F) - 1u);
-}
-
 template <int D, int KB, int VB, int G, int WPH>
 struct TcCfg {
   static constexpr int kRBK = D * KB / 8 + 4;          // row bytes
@@ -116,16 +109,19 @@ struct TcCfg {
   static constexpr int kKSteps = D / 16;               // score k-steps
   static constexpr int kMTiles = D / 32;               // value m-tiles
   static constexpr int kNT = (2 * G + 7) / 8;          // value n-tiles (N = 2G)
-  static constexpr int kFK = 2 * KB, kFV = 2 * VB;     // field widths
-  static constexpr int kLutKEntries = 1 << kFK;
-  static constexpr int kLutVEntries = 1 << kFV;
-  static constexpr int kLutKCopies = kFK == 8 ? 16 : 1;
-  static constexpr int kLutVCopies = kFV == 8 ? 32 : 1;
-  static constexpr int kLutKBytes = kLutKEntries * kLutKCopies * 8;
-  static constexpr int kLutVBytes = kLutVEntries * kLutVCopies * 4;
+  // Byte-field table (4-bit indices): 256 entries x 256 bytes.  Bytes [0, 128) of an
+  // entry hold 16 lane copies of the K (hi, lo) pair, bytes [128, 256) 32 lane copies of
+  // the V fp16 pair, so one PRMT turns a packed byte into a conflict-free table offset.
+  static constexpr bool kByteTable = (KB == 4 || VB == 4);
+  static constexpr int kByteTableBytes = kByteTable ? 256 * 256 : 0;
+  // Nibble-field tables (2-bit indices): 16 entries, no replication needed.
+  static constexpr int kNibKBytes = 16 * 8;
+  static constexpr int kNibVBytes = 16 * 4;
+  static constexpr int kLutBytes = kByteTableBytes + kNibKBytes + kNibVBytes;
   static_assert(kWK % 4 == 0, "K row must split into 4 interleaved word columns");
   static_assert(kWV % 8 == 0, "V row must split into 8 interleaved word columns");
   static_assert(G == 4 || G == 8, "GQA group 4 or 8");
+  static_assert((KB == 2 || KB == 4) && (VB == 2 || VB == 4), "2- or 4-bit indices");
 };
 
 struct TcArgs {
@@ -141,6 +137,11 @@ struct TcArgs {
   int* prefix;            // [B+1] block prefix sums (written by CTA 0)
 };
 
+// Per-stage block metadata ring: kNStages + 1 entries so that warp 0 can fill the
+// entry of stage st + kNStages while stage st is being consumed.
+constexpr int kMetaRing = kNStages + 1;
+constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
+
 template <int D, int KB, int VB, int G, int WPH>
 __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args) {
   using Cfg = TcCfg<D, KB, VB, G, WPH>;
@@ -153,32 +154,54 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   const int B = a.batch;
   const int cap = a.max_blocks_per_seq * kBS;
 
-  unsigned char* lutK = smem;
-  unsigned char* lutV = lutK + Cfg::kLutKBytes;
-  unsigned char* stage_base = lutV + Cfg::kLutVBytes;
-  const int stage_bytes = WPH * (args.k_slab_smem + args.v_slab_smem);
+  unsigned char* lut8 = smem;                                  // byte-field table
+  unsigned char* lutK2 = lut8 + Cfg::kByteTableBytes;          // nibble K table
+  unsigned char* lutV2 = lutK2 + Cfg::kNibKBytes;              // nibble V table
+  unsigned char* stage_base = smem + Cfg::kLutBytes;
+  const int blk_bytes = args.k_slab_smem + args.v_slab_smem;
+  const int stage_bytes = WPH * blk_bytes;
   BlockMeta* meta = reinterpret_cast<BlockMeta*>(stage_base + kNStages * stage_bytes);
-  int* scan_tmp = reinterpret_cast<int*>(meta + kNStages * WPH);  // [32 + 4]
+  int* meta_bid = reinterpret_cast<int*>(meta + kMetaRing * WPH);
+  int* scan_tmp = meta_bid + kMetaRing * WPH;  // [36]
 
   // ---- tables: K (hi, lo) pairs, V fp16(alpha c) pairs -----------------------------
-  for (int i = tid; i < Cfg::kLutKEntries * Cfg::kLutKCopies; i += nthreads) {
-    const int f = i / Cfg::kLutKCopies;
-    const float ca = __ldg(a.k_centroids + (f & ((1 << KB) - 1)));
-    const float cb = __ldg(a.k_centroids + (f >> KB));
-    __half ha, la, hb, lb;
-    split_half(ca, ha, la);
-    split_half(cb, hb, lb);
-    __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&hi2);
-    v.y = *reinterpret_cast<uint32_t*>(&lo2);
-    reinterpret_cast<uint2*>(lutK)[i] = v;
+  if (KB == 4) {
+    for (int i = tid; i < 256 * 16; i += nthreads) {
+      const int f = i >> 4, copy = i & 15;
+      __half ha, la, hb, lb;
+      split_half(__ldg(a.k_centroids + (f & 15)), ha, la);
+      split_half(__ldg(a.k_centroids + (f >> 4)), hb, lb);
+      __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
+      uint2 v;
+      v.x = *reinterpret_cast<uint32_t*>(&hi2);
+      v.y = *reinterpret_cast<uint32_t*>(&lo2);
+      *reinterpret_cast<uint2*>(lut8 + f * 256 + copy * 8) = v;
+    }
+  } else {
+    for (int f = tid; f < 16; f += nthreads) {
+      __half ha, la, hb, lb;
+      split_half(__ldg(a.k_centroids + (f & 3)), ha, la);
+      split_half(__ldg(a.k_centroids + (f >> 2)), hb, lb);
+      __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
+      uint2 v;
+      v.x = *reinterpret_cast<uint32_t*>(&hi2);
+      v.y = *reinterpret_cast<uint32_t*>(&lo2);
+      *reinterpret_cast<uint2*>(lutK2 + f * 8) = v;
+    }
   }
-  for (int i = tid; i < Cfg::kLutVEntries * Cfg::kLutVCopies; i += nthreads) {
-    const int f = i / Cfg::kLutVCopies;
-    const float ca = __ldg(a.v_centroids + (f & ((1 << VB) - 1))) * args.v_alpha;
-    const float cb = __ldg(a.v_centroids + (f >> VB)) * args.v_alpha;
-    reinterpret_cast<uint32_t*>(lutV)[i] = pack_half2(ca, cb);
+  if (VB == 4) {
+    for (int i = tid; i < 256 * 32; i += nthreads) {
+      const int f = i >> 5, copy = i & 31;
+      const float ca = __ldg(a.v_centroids + (f & 15)) * args.v_alpha;
+      const float cb = __ldg(a.v_centroids + (f >> 4)) * args.v_alpha;
+      *reinterpret_cast<uint32_t*>(lut8 + f * 256 + 128 + copy * 4) = pack_half2(ca, cb);
+    }
+  } else {
+    for (int f = tid; f < 16; f += nthreads) {
+      const float ca = __ldg(a.v_centroids + (f & 3)) * args.v_alpha;
+      const float cb = __ldg(a.v_centroids + (f >> 2)) * args.v_alpha;
+      *reinterpret_cast<uint32_t*>(lutV2 + f * 4) = pack_half2(ca, cb);
+    }
   }
 
   // ---- flat block list: N, this CTA's range, its first and last sequence ------------
@@ -187,7 +210,6 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     len = len < 0 ? 0 : (len > cap ? cap : len);
     return (len + kBS - 1) / kBS;
   };
-  // pass 1: total blocks
   int local = 0;
   bool bad_len = false;
   for (int b = tid; b < B; b += nthreads) {
@@ -196,19 +218,17 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     local += nblocks_of(b);
   }
   if (cta == 0 && a.status && __any_sync(kFullMask, bad_len) && lane == 0) atomicMax(a.status, (int32_t)kInvalidArg);
-  local = __reduce_add_sync(kFullMask, (unsigned)local);
+  local = (int)__reduce_add_sync(kFullMask, (unsigned)local);
   if (lane == 0) scan_tmp[warp] = local;
   __syncthreads();
   long long N = 0;
   for (int w = 0; w < nthreads / 32; ++w) N += scan_tmp[w];
   const long long g_lo = N * cta / C, g_hi = N * (cta + 1) / C;
   __syncthreads();
-  // pass 2: prefix sums; locate the sequences holding g_lo and g_hi - 1
   if (tid == 0) {
     scan_tmp[32] = -1;
     scan_tmp[33] = -1;
     scan_tmp[34] = 0;
-    scan_tmp[35] = 0;
   }
   int carry = 0;
   for (int base = 0; base < B; base += nthreads) {
@@ -223,10 +243,11 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     __syncthreads();
     if (lane == 31) scan_tmp[warp] = incl;
     __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += scan_tmp[w];
-    int total = 0;
-    for (int w = 0; w < nthreads / 32; ++w) total += scan_tmp[w];
+    int wbase = 0, total = 0;
+    for (int w = 0; w < nthreads / 32; ++w) {
+      if (w < warp) wbase += scan_tmp[w];
+      total += scan_tmp[w];
+    }
     const int excl = carry + wbase + incl - nb;
     if (b < B) {
       if (cta == 0) args.prefix[b] = excl;
@@ -242,67 +263,88 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   __syncthreads();
   if (g_lo >= g_hi) return;  // nothing to do (uniform)
   const int b_first = scan_tmp[32], b_last = scan_tmp[33], j_first = scan_tmp[34];
+  const int nstages = (int)((g_hi - g_lo + WPH - 1) / WPH);
 
-  // ---- producer cursor (every thread keeps the same copy) ---------------------------
-  int pb = b_first, pj = j_first, pnb = nblocks_of(b_first);
-  long long pg = g_lo;
-  const long long total_blocks = g_hi - g_lo;
-  const int nstages = (int)((total_blocks + WPH - 1) / WPH);
+  // ---- block metadata: lane u < WPH of warp 0 owns blocks g_lo + WPH*st + u ----------
+  int cb = b_first, cj = j_first, cnb = nblocks_of(b_first);
+  long long cg = g_lo;
+  auto cursor_advance = [&](int steps) {
+    cg += steps;
+    cj += steps;
+    while (cg < g_hi && cj >= cnb) {
+      cj -= cnb;
+      ++cb;
+      cnb = nblocks_of(cb);
+    }
+  };
+  if (warp == 0 && lane < WPH) cursor_advance(lane);
+  auto fill_meta = [&](int st) {  // warp 0, lanes < WPH
+    BlockMeta m{0, 0, 0, 0};
+    int bid = -1;
+    if (cg < g_hi) {
+      int len = __ldg(a.seq_lens + cb);
+      len = len < 0 ? 0 : (len > cap ? cap : len);
+      m.b = cb;
+      m.j = cj;
+      m.ntok = min(kBS, len - cj * kBS);
+      bid = __ldg(a.block_table + (int64_t)cb * a.max_blocks_per_seq + cj);
+      m.valid = (bid >= 0 && (int64_t)bid < a.num_blocks);
+      if (!m.valid && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+      cursor_advance(WPH);
+    }
+    meta[(st % kMetaRing) * WPH + lane] = m;
+    meta_bid[(st % kMetaRing) * WPH + lane] = m.valid ? bid : -1;
+  };
 
-  const int k_chunks_row = H * Cfg::kRBK / 16;  // 16-byte chunks per token (when padded layout)
+  // ---- copies: 16-byte cp.async of whole K / V slabs, per-token padding in smem -------
   const bool k_padded = (H * Cfg::kRBK) % 16 == 0;
   const bool v_padded = (H * Cfg::kRBV) % 16 == 0;
   const int k_slab = kBS * H * Cfg::kRBK, v_slab = kBS * H * Cfg::kRBV;
+  const int kc = k_slab / 16, vc = v_slab / 16;
+  const int kcr = k_padded ? H * Cfg::kRBK / 16 : kc;  // chunks per token row
+  const int vcr = v_padded ? H * Cfg::kRBV / 16 : vc;
+  const int kts_pad = k_padded ? args.k_tok_stride : 0;
+  const int vts_pad = v_padded ? args.v_tok_stride : 0;
+  // per-thread start (token, column) and per-step increments, no division in the loop
+  const int k_t0 = tid / kcr, k_c0 = tid - k_t0 * kcr, k_dt = nthreads / kcr, k_dc = nthreads - k_dt * kcr;
+  const int v_t0 = tid / vcr, v_c0 = tid - v_t0 * vcr, v_dt = nthreads / vcr, v_dc = nthreads - v_dt * vcr;
 
   auto issue_stage = [&](int st) {
-    const int buf = st % kNStages;
-    unsigned char* sb = stage_base + buf * stage_bytes;
+    unsigned char* sb = stage_base + (st % kNStages) * stage_bytes;
+#pragma unroll
     for (int u = 0; u < WPH; ++u) {
-      BlockMeta m{0, 0, 0, 0};
-      int bid = -1;
-      if (pg < g_hi) {
-        m.b = pb;
-        m.j = pj;
-        int len = __ldg(a.seq_lens + pb);
-        len = len < 0 ? 0 : (len > cap ? cap : len);
-        m.ntok = min(kBS, len - pj * kBS);
-        bid = __ldg(a.block_table + (int64_t)pb * a.max_blocks_per_seq + pj);
-        m.valid = (bid >= 0 && (int64_t)bid < a.num_blocks);
-        // advance the cursor
-        ++pg;
-        if (++pj == pnb && pg < g_hi) {
-          do {
-            ++pb;
-            pnb = nblocks_of(pb);
-          } while (pnb == 0);
-          pj = 0;
+      const int bid = meta_bid[(st % kMetaRing) * WPH + u];
+      if (bid < 0) continue;
+      const unsigned char* ksrc = a.k_pages + (int64_t)bid * k_slab;
+      const unsigned char* vsrc = a.v_pages + (int64_t)bid * v_slab;
+      const uint32_t kdst = smem_u32(sb + u * blk_bytes);
+      const uint32_t vdst = kdst + args.k_slab_smem;
+      int t = k_t0, col = k_c0;
+      for (int c = tid; c < kc; c += nthreads) {
+        cp_async16(kdst + t * kts_pad + col * 16, ksrc + c * 16);
+        t += k_dt;
+        col += k_dc;
+        if (col >= kcr) {
+          col -= kcr;
+          ++t;
         }
       }
-      if (tid == 0) meta[buf * WPH + u] = m;
-      if (m.ntok > 0 && !m.valid && tid == 0 && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
-      if (m.ntok > 0 && m.valid) {
-        const unsigned char* ksrc = a.k_pages + (int64_t)bid * k_slab;
-        const unsigned char* vsrc = a.v_pages + (int64_t)bid * v_slab;
-        unsigned char* kdst = sb + u * (args.k_slab_smem + args.v_slab_smem);
-        unsigned char* vdst = kdst + args.k_slab_smem;
-        const int kc = k_slab / 16, vc = v_slab / 16;
-        for (int c = tid; c < kc; c += nthreads) {
-          const int tok = k_padded ? c / k_chunks_row : 0;
-          const int off = k_padded ? tok * args.k_tok_stride + (c - tok * k_chunks_row) * 16 : c * 16;
-          cp_async16(smem_u32(kdst + off), ksrc + c * 16);
-        }
-        const int v_chunks_row = H * Cfg::kRBV / 16;
-        for (int c = tid; c < vc; c += nthreads) {
-          const int tok = v_padded ? c / v_chunks_row : 0;
-          const int off = v_padded ? tok * args.v_tok_stride + (c - tok * v_chunks_row) * 16 : c * 16;
-          cp_async16(smem_u32(vdst + off), vsrc + c * 16);
+      t = v_t0;
+      col = v_c0;
+      for (int c = tid; c < vc; c += nthreads) {
+        cp_async16(vdst + t * vts_pad + col * 16, vsrc + c * 16);
+        t += v_dt;
+        col += v_dc;
+        if (col >= vcr) {
+          col -= vcr;
+          ++t;
         }
       }
     }
     cp_async_commit();
   };
 
-  __syncthreads();  // tables ready before anyone reads them (also orders meta writes)
+  __syncthreads();  // tables ready
 
   // ---- consumer state ----------------------------------------------------------------
   const int h = warp % H;
@@ -310,12 +352,23 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   const int r = lane >> 2, c = lane & 3;
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kLog2eTc / sqrtf((float)D);
-  const uint32_t lutK_lane = smem_u32(lutK) + (Cfg::kLutKCopies > 1 ? (lane & 15) * 8 : 0);
-  const uint32_t lutV_lane = smem_u32(lutV) + (Cfg::kLutVCopies > 1 ? lane * 4 : 0);
+  const int kts = args.k_tok_stride, vts = args.v_tok_stride;
+  const uint32_t k_lane_off = (lane & 15) * 8;       // K copy inside a byte-table entry
+  const uint32_t v_lane_off = 128 + lane * 4;        // V copy inside a byte-table entry
   // value-B selectors: the P value goes to the low half when (r & 1) == 0, else the high half
   const int hsel = (r >> 1) & 1;
   const uint32_t sel_b = (r & 1) ? (0x0044u | ((2u * hsel) << 8) | ((2u * hsel + 1u) << 12))
                                  : ((2u * hsel) | ((2u * hsel + 1u) << 4) | 0x4400u);
+
+  // table offsets: field e of word w
+  auto k_lookup = [&](uint32_t w, int e) -> uint2 {
+    if (KB == 4) return ld64(lut8 + __byte_perm(w, k_lane_off, 0x7604u | ((uint32_t)e << 4)));
+    return ld64(lutK2 + (((w >> (4 * e)) & 15u) << 3));
+  };
+  auto v_lookup = [&](uint32_t w, int e) -> uint32_t {
+    if (VB == 4) return ld32(lut8 + __byte_perm(w, v_lane_off, 0x7604u | ((uint32_t)e << 4)));
+    return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 2));
+  };
 
   uint32_t bq_hi[Cfg::kKSteps][2], bq_lo[Cfg::kKSteps][2];
   float o_acc[Cfg::kNT][Cfg::kMTiles][4];
@@ -380,7 +433,6 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   // Writes this warp's partial for sequence b (empty when `empty`).
   auto flush = [&](int b, bool empty) {
     const int64_t slot = (int64_t)WPH * (cta + b) + slot_u;
-    // l: reduce the per-lane partial sums over the 8 row groups
     float lsum[2] = {l_run[0], l_run[1]};
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -388,8 +440,7 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 8);
       lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 16);
     }
-    // score layout: lane (r, c) holds q heads 2c, 2c+1
-    if (r == 0) {
+    if (r == 0) {  // score layout: lane (r, c) holds q heads 2c, 2c+1
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int g = 2 * c + e;
@@ -400,9 +451,8 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
         }
       }
     }
-    // value layout: lane (r, c) holds q head c + 4 nt, pairs p_v(r, 2i + half)
 #pragma unroll
-    for (int nt = 0; nt < Cfg::kNT; ++nt) {
+    for (int nt = 0; nt < Cfg::kNT; ++nt) {  // value layout: q head c + 4 nt
       const int g = c + 4 * nt;
       if (g < G) {
         float* acc = args.part_acc + (slot * a.num_q_heads + (int64_t)h * G + g) * D;
@@ -425,7 +475,7 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   // Move this warp to sequence b: close the current one and any non-empty sequences
   // of this CTA in between (they get empty partials), then load b's query.
   auto enter_sequence = [&](int b) {
-    int from = cur_b;
+    const int from = cur_b;
     if (from >= 0) flush(from, false);
     for (int x = (from < 0 ? b_first : from + 1); x < b; ++x)
       if (nblocks_of(x) > 0) flush(x, true);
@@ -435,6 +485,9 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   };
 
   // ---- main pipeline -----------------------------------------------------------------
+  if (warp == 0 && lane < WPH)
+    for (int st = 0; st < kNStages && st < nstages; ++st) fill_meta(st);
+  __syncthreads();
   for (int st = 0; st < kNStages - 1; ++st) {
     if (st < nstages) issue_stage(st);
     else cp_async_commit();
@@ -445,49 +498,47 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     __syncthreads();
     if (st + kNStages - 1 < nstages) issue_stage(st + kNStages - 1);
     else cp_async_commit();
+    if (warp == 0 && lane < WPH && st + kNStages < nstages) fill_meta(st + kNStages);
 
     const int buf = st % kNStages;
-    const BlockMeta m = meta[buf * WPH + slot_u];
+    const BlockMeta m = meta[(st % kMetaRing) * WPH + slot_u];
     if (m.ntok == 0) continue;
     if (m.b != cur_b) enter_sequence(m.b);
     if (!m.valid) continue;
 
-    const unsigned char* kblk = stage_base + buf * stage_bytes + slot_u * (args.k_slab_smem + args.v_slab_smem);
+    const unsigned char* kblk = stage_base + buf * stage_bytes + slot_u * blk_bytes;
     const unsigned char* vblk = kblk + args.k_slab_smem;
-    const uint32_t kbase = smem_u32(kblk) + h * Cfg::kRBK;
-    const uint32_t vbase = smem_u32(vblk) + h * Cfg::kRBV;
-    const int kts = args.k_tok_stride, vts = args.v_tok_stride;
+    const unsigned char* kbase = kblk + h * Cfg::kRBK;
+    const unsigned char* vbase = vblk + h * Cfg::kRBV;
 
     // --- scores S[tok][q head] -------------------------------------------------------
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
-      const uint32_t w0 = lds32(kbase + r * kts + (c + 4 * jw) * 4);
-      const uint32_t w1 = lds32(kbase + (r + 8) * kts + (c + 4 * jw) * 4);
+      const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
+      const uint32_t w1 = ld32(kbase + (r + 8) * kts + (c + 4 * jw) * 4);
 #pragma unroll
       for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
         const int s = (jw * Cfg::kPWK + e2) >> 1;
-        const uint2 x00 = lds64(lutK_lane + pair_field<KB>(w0, e2) * (8 * Cfg::kLutKCopies));
-        const uint2 x10 = lds64(lutK_lane + pair_field<KB>(w1, e2) * (8 * Cfg::kLutKCopies));
-        const uint2 x01 = lds64(lutK_lane + pair_field<KB>(w0, e2 + 1) * (8 * Cfg::kLutKCopies));
-        const uint2 x11 = lds64(lutK_lane + pair_field<KB>(w1, e2 + 1) * (8 * Cfg::kLutKCopies));
+        const uint2 x00 = k_lookup(w0, e2), x10 = k_lookup(w1, e2);
+        const uint2 x01 = k_lookup(w0, e2 + 1), x11 = k_lookup(w1, e2 + 1);
         mma16816(sacc, x00.x, x10.x, x01.x, x11.x, bq_hi[s][0], bq_hi[s][1]);
         mma16816(sacc, x00.x, x10.x, x01.x, x11.x, bq_lo[s][0], bq_lo[s][1]);
         mma16816(sacc, x00.y, x10.y, x01.y, x11.y, bq_hi[s][0], bq_hi[s][1]);
       }
     }
-    // rows r, r+8 of the tile: token norms and masking
-    const float kn0 = __uint_as_float(lds32(kbase + r * kts + Cfg::kWK * 4));
-    const float kn1 = __uint_as_float(lds32(kbase + (r + 8) * kts + Cfg::kWK * 4));
-    const float vn0 = __uint_as_float(lds32(vbase + r * vts + Cfg::kWV * 4));
-    const float vn1 = __uint_as_float(lds32(vbase + (r + 8) * vts + Cfg::kWV * 4));
+    const float kn0 = __uint_as_float(ld32(kbase + r * kts + Cfg::kWK * 4));
+    const float kn1 = __uint_as_float(ld32(kbase + (r + 8) * kts + Cfg::kWK * 4));
+    const float vn0 = __uint_as_float(ld32(vbase + r * vts + Cfg::kWV * 4));
+    const float vn1 = __uint_as_float(ld32(vbase + (r + 8) * vts + Cfg::kWV * 4));
     float sc[4];
     sc[0] = r < m.ntok ? sacc[0] * kn0 : -INFINITY;
     sc[1] = r < m.ntok ? sacc[1] * kn0 : -INFINITY;
     sc[2] = r + 8 < m.ntok ? sacc[2] * kn1 : -INFINITY;
     sc[3] = r + 8 < m.ntok ? sacc[3] * kn1 : -INFINITY;
 
-    // --- online softmax (q heads 2c, 2c+1 on this lane) ------------------------------
+    // --- online softmax (q heads 2c, 2c+1 on this lane); the running max is only moved
+    // when the tile max passes it by more than kRescaleSlack, so p <= 2^slack.
     float corr[2], pv[4];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -495,19 +546,17 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 4));
       mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
       mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
-      const float mn = fmaxf(m_run[e], mt);
-      corr[e] = exp2f(m_run[e] - mn);
-      const float p0 = exp2f(sc[e] - mn), p1 = exp2f(sc[2 + e] - mn);
+      const float mn = mt > m_run[e] + kRescaleSlack ? mt : m_run[e];
+      corr[e] = fast_exp2(m_run[e] - mn);
+      const float p0 = fast_exp2(sc[e] - mn), p1 = fast_exp2(sc[2 + e] - mn);
       l_run[e] = l_run[e] * corr[e] + p0 + p1;
       m_run[e] = mn;
       pv[e] = p0 * vn0;
       pv[2 + e] = p1 * vn1;
     }
-    // rescale the value accumulators (value layout holds q head c + 4 nt)
-    const bool any_rescale = __any_sync(kFullMask, corr[0] != 1.f || corr[1] != 1.f);
-    if (any_rescale) {
+    if (__any_sync(kFullMask, corr[0] != 1.f || corr[1] != 1.f)) {
 #pragma unroll
-      for (int nt = 0; nt < Cfg::kNT; ++nt) {
+      for (int nt = 0; nt < Cfg::kNT; ++nt) {  // value layout holds q head c + 4 nt
         const int g = c + 4 * nt;
         const int srcl = (g >> 1) & 3;  // lane (r'=0, c'=g>>1)
         const float c0 = __shfl_sync(kFullMask, corr[0], srcl);
@@ -538,15 +587,13 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       }
 #pragma unroll
       for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
-        const uint32_t wa = lds32(vbase + t0 * vts + (r + 8 * jw) * 4);
-        const uint32_t wb = lds32(vbase + t1 * vts + (r + 8 * jw) * 4);
+        const uint32_t wa = ld32(vbase + t0 * vts + (r + 8 * jw) * 4);
+        const uint32_t wb = ld32(vbase + t1 * vts + (r + 8 * jw) * 4);
 #pragma unroll
         for (int e = 0; e < Cfg::kPWV; e += 2) {
           const int i = (jw * Cfg::kPWV + e) >> 1;  // m-tile: pairs q = 2i (row r), 2i+1 (row r+8)
-          const uint32_t a0 = lds32(lutV_lane + pair_field<VB>(wa, e) * (4 * Cfg::kLutVCopies));
-          const uint32_t a1 = lds32(lutV_lane + pair_field<VB>(wa, e + 1) * (4 * Cfg::kLutVCopies));
-          const uint32_t a2 = lds32(lutV_lane + pair_field<VB>(wb, e) * (4 * Cfg::kLutVCopies));
-          const uint32_t a3 = lds32(lutV_lane + pair_field<VB>(wb, e + 1) * (4 * Cfg::kLutVCopies));
+          const uint32_t a0 = v_lookup(wa, e), a1 = v_lookup(wa, e + 1);
+          const uint32_t a2 = v_lookup(wb, e), a3 = v_lookup(wb, e + 1);
 #pragma unroll
           for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
         }
@@ -641,9 +688,8 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   t.part_acc = static_cast<float*>(a.workspace);
   t.part_ml = t.part_acc + slots * Hq * D;
   t.prefix = reinterpret_cast<int*>(t.part_ml + slots * Hq * 2);
-  const size_t smem = Cfg::kLutKBytes + Cfg::kLutVBytes +
-                      (size_t)kNStages * WPH * (t.k_slab_smem + t.v_slab_smem) +
-                      kNStages * WPH * sizeof(BlockMeta) + 36 * sizeof(int);
+  const size_t smem = Cfg::kLutBytes + (size_t)kNStages * WPH * (t.k_slab_smem + t.v_slab_smem) +
+                      kMetaRing * WPH * (sizeof(BlockMeta) + sizeof(int)) + 36 * sizeof(int);
   auto kern = decode_tc_kernel<D, KB, VB, G, WPH>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;

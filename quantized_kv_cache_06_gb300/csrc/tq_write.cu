@@ -131,6 +131,12 @@ cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int64_t rows = a.num_tokens * a.num_kv_heads;
+  if (write_tc_supported(a)) {
+    // 16-row tiles, 8 warps per CTA, two CTAs per SM resident
+    const int64_t tiles = (rows + 15) / 16;
+    const int tgrid = (int)std::max<int64_t>(1, std::min<int64_t>((tiles + 7) / 8, (int64_t)sms * 2));
+    return launch_write_tc(a, stream, tgrid);
+  }
   const int grid = (int)std::min<int64_t>((rows + kWriteWarps - 1) / kWriteWarps, (int64_t)sms * 16);
   switch (a.dtype) {
     case kF32: return launch_write_typed<float>(a, stream, grid);

@@ -1,0 +1,388 @@
+// Tensor-core packed-KV row writer (fp16 / bf16 rows, head_dim 64 or 128, 2 or 4 bits).
+//
+// TurboQuant docs: "vLLM Usage" (TQ Byte Layout, Slot Mapping, TQ Packed Page Contract:
+// write_tq4_kv) and "Architecture" (PackedPageCache).
+//
+// A warp encodes 16 consecutive rows (t, h) at a time.
+//  * Rotation.  With d = 16 j + k, H_D = H_{D/16} (x) H_16 (Sylvester order), so
+//    y = H_D (s * x) is an m16n8k16 MMA per 16-column block j against
+//    B_j = diag(s_j) H_16 (entries +-1: exact in fp16 / bf16, products exact in the fp32
+//    accumulator), followed by the H_{D/16} butterflies across blocks, in registers.
+//  * Norm.  ||y||^2 = D ||x||^2: a sum of the thread's squares plus two quad shuffles.
+//  * Quantiser.  u = y / sqrt(sum y^2) lands in one of 256 equal cells covering the
+//    decision points; each cell stores (number of decision points below the cell, the
+//    first decision point at or above the cell), and the cells are placed so that no
+//    decision point lies near a cell edge.  index = lo + (u > point): one compare, exact
+//    "#{k : boundary_k < u}" whichever cell a rounding picks near an edge.  The table is
+//    replicated per lane (16 copies, 64-bit entries) so the lookups are conflict free.
+//  * Packing.  Bytes are assembled per row in shared memory (LSB-first fields, then the
+//    fp32 norm); a token's H rows are contiguous in the page (H * row_bytes bytes), so the
+//    warp stores whole token slabs with 16-byte stores.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <type_traits>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kWWarps = 8;          // warps per CTA
+constexpr int kQCells = 256;        // quantiser cells
+constexpr int kQCopies = 16;        // lane copies of the quantiser table
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16_w(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16_w_zfill(uint32_t dst, const void* src, int valid_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_commit_w() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait_w() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+               : "r"(addr));
+}
+template <typename T>
+__device__ __forceinline__ void mma_rot(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1);
+template <>
+__device__ __forceinline__ void mma_rot<__half>(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma_rot<__nv_bfloat16>(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                       uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// +-1 pair in the operand type: sign bits of the two halves from s0, s1 (true = negative)
+template <typename T>
+__device__ __forceinline__ uint32_t pm1_pair(bool neg0, bool neg1) {
+  const uint32_t one = std::is_same<T, __half>::value ? 0x3C00u : 0x3F80u;
+  return (one | (neg0 ? 0x8000u : 0u)) | ((one | (neg1 ? 0x8000u : 0u)) << 16);
+}
+
+struct QCell {
+  int lo;       // decision points strictly below the cell
+  float point;  // first decision point at or above the cell start (+inf if none)
+};
+
+struct WriteTcArgs {
+  WriteArgs a;
+};
+
+// Quantiser grid chosen from the decision points b_0 < ... < b_{m-1}: 256 cells of width
+// w = span / 200 starting 8 cells below b_0, at the first phase (of 32) that keeps every
+// b_k at least 1/64 cell from a cell edge and in a cell of its own.  Deterministic, so
+// every CTA picks the same grid.  Returns false when no phase qualifies (then the caller
+// reports an error instead of writing).
+__device__ bool choose_grid(const float* b, int m, float& q_lo, float& q_inv_w) {
+  const float span = b[m - 1] - b[0];
+  if (m == 1) {  // one decision point: any grid around it
+    q_inv_w = 1.0f;
+    q_lo = b[0] - 128.5f;
+    return true;
+  }
+  if (!(span > 0.f)) return false;
+  for (int t = 0; t < 8; ++t) {
+    const float w = span / 200.0f * (1.0f + 0.01f * t);
+    for (int p = 0; p < 32; ++p) {
+      const float lo = b[0] - w * (8.0f + p / 32.0f);
+      const float inv = 1.0f / w;
+      bool ok = true;
+      int prev = -1;
+      for (int k = 0; k < m && ok; ++k) {
+        const float x = (b[k] - lo) * inv;
+        const int cell = (int)floorf(x);
+        const float f = x - (float)cell;
+        ok = cell > prev && cell >= 1 && cell < 255 && f >= 1.0f / 64 && f <= 63.0f / 64;
+        prev = cell;
+      }
+      if (ok) {
+        q_lo = lo;
+        q_inv_w = inv;
+        return true;
+      }
+    }
+  }
+  return false;
+}
+
+template <typename T, int D, int BITS>
+__global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs args) {
+  constexpr int NB = D / 16;            // 16-column blocks
+  constexpr int RB = D * BITS / 8 + 4;  // row bytes
+  constexpr int IB = D * BITS / 8;      // index bytes
+  constexpr int ROWB = D * 2;           // raw row bytes
+  constexpr int TILE_BYTES = 16 * ROWB;
+  const WriteArgs& a = args.a;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, c = lane & 3;
+  const int H = a.num_kv_heads;
+
+  // shared memory: quantiser table | per warp: 2 raw tiles + 1 packed tile
+  QCell* qtab = reinterpret_cast<QCell*>(smem);
+  unsigned char* wbase = smem + kQCells * kQCopies * sizeof(QCell) + warp * (2 * TILE_BYTES + 16 * RB + 16);
+  unsigned char* raw_buf = wbase;
+  unsigned char* pack_buf = wbase + 2 * TILE_BYTES;
+
+  // decision points (correctly rounded midpoints of neighbouring fp32 centroids) and
+  // the quantiser grid
+  constexpr int NC = 1 << BITS;
+  __shared__ float bnd[NC - 1];
+  __shared__ float grid_lo, grid_inv;
+  __shared__ int grid_ok;
+  if (threadIdx.x < NC - 1) bnd[threadIdx.x] = 0.5f * (a.centroids[threadIdx.x] + a.centroids[threadIdx.x + 1]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float lo = 0.f, inv = 0.f;
+    grid_ok = choose_grid(bnd, NC - 1, lo, inv) ? 1 : 0;
+    grid_lo = lo;
+    grid_inv = inv;
+    if (!grid_ok && blockIdx.x == 0) atomicMax(a.status, (int32_t)kUnsupported);
+  }
+  __syncthreads();
+  if (!grid_ok || *a.status != kOk) return;  // bad codebook or a slot failed validation: write nothing
+  const float q_lo = grid_lo, q_inv_w = grid_inv;
+  for (int i = threadIdx.x; i < kQCells * kQCopies; i += blockDim.x) {
+    // cell = [q_lo + cell / q_inv_w, ...): decision points below its start, first one at or above
+    const int cell = i / kQCopies;
+    const float lo_edge = q_lo + (float)cell / q_inv_w;
+    int below = 0;
+    float point = INFINITY;
+    for (int k = 0; k < NC - 1; ++k) {
+      if (bnd[k] < lo_edge) ++below;
+      else if (point == INFINITY) point = bnd[k];
+    }
+    QCell q;
+    q.lo = cell == 0 ? 0 : below;
+    q.point = cell == 0 ? bnd[0] : point;
+    qtab[i] = q;
+  }
+  __syncthreads();
+
+  // B fragments: B_j[k][n] = s[16 j + k] * (-1)^popcount(k & n); this lane holds
+  // k in {2c, 2c+1} (reg 0) and {2c+8, 2c+9} (reg 1) for n = r (+8 for n-tile 1).
+  uint32_t bfr[NB][2][2];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int n = r + 8 * nt;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const int k0 = 2 * c + 8 * part, k1 = k0 + 1;
+        const bool n0 = (__ldg(a.signs + 16 * j + k0) < 0.f) ^ (__popc(k0 & n) & 1);
+        const bool n1 = (__ldg(a.signs + 16 * j + k1) < 0.f) ^ (__popc(k1 & n) & 1);
+        bfr[j][nt][part] = pm1_pair<T>(n0, n1);
+      }
+    }
+  }
+  const unsigned char* qlane = reinterpret_cast<const unsigned char*>(qtab) + (lane & 15) * sizeof(QCell);
+
+  const int64_t num_rows = a.num_tokens * H;
+  const int64_t num_tiles = (num_rows + 15) / 16;
+  const int64_t wstride = (int64_t)gridDim.x * kWWarps;
+  const T* raw = static_cast<const T*>(a.raw);
+
+  // issue the cp.async of tile `tile` into raw buffer `buf` (16 rows x ROWB bytes,
+  // 16-byte chunks XOR-swizzled by row so that ldmatrix reads are conflict free)
+  auto load_tile = [&](int64_t tile, int buf) {
+    if (tile < num_tiles) {
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(raw) + tile * TILE_BYTES;
+      const int64_t bytes_left = (num_rows - tile * 16) * ROWB;
+      const uint32_t dst0 = smem_addr(raw_buf + buf * TILE_BYTES);
+      constexpr int CH = TILE_BYTES / 16, CPR = ROWB / 16;
+#pragma unroll
+      for (int i = lane; i < CH; i += 32) {
+        const int row = i / CPR, col = i % CPR;
+        const uint32_t dst = dst0 + row * ROWB + ((col ^ (row & 7)) << 4);
+        const int64_t off = (int64_t)i * 16;
+        if (off + 16 <= bytes_left) cp_async16_w(dst, src + off);
+        else cp_async16_w_zfill(dst, src, 0);  // past the last row: zero fill, no read
+      }
+    }
+    cp_commit_w();
+  };
+
+  int64_t tile = (int64_t)blockIdx.x * kWWarps + warp;
+  int buf = 0;
+  load_tile(tile, 0);
+  for (; tile < num_tiles; tile += wstride, buf ^= 1) {
+    load_tile(tile + wstride, buf ^ 1);
+    cp_wait_w<1>();
+    __syncwarp();
+
+    // ---- rotation: MMA per block, then butterflies across blocks ------------------
+    float acc[NB][2][4];
+    const uint32_t tbase = smem_addr(raw_buf + buf * TILE_BYTES);
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      // ldmatrix.x4: lanes 0-7 rows 0-7 cols 16j..+7, 8-15 rows 8-15, 16-23 rows 0-7 cols +8, 24-31 rows 8-15 cols +8
+      const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int chunk = 2 * j + (lane >> 4);
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(tbase + row * ROWB + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
+        mma_rot<T>(acc[j][nt], a0, a1, a2, a3, bfr[j][nt][0], bfr[j][nt][1]);
+      }
+    }
+#pragma unroll
+    for (int hs = 1; hs < NB; hs <<= 1) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        if ((j & hs) == 0) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x = acc[j][nt][e], y = acc[j + hs][nt][e];
+              acc[j][nt][e] = x + y;
+              acc[j + hs][nt][e] = x - y;
+            }
+        }
+      }
+    }
+    // ---- norms of rows r (e = 0, 1) and r + 8 (e = 2, 3) -----------------------------
+    float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        ss0 = fmaf(acc[j][nt][0], acc[j][nt][0], ss0);
+        ss0 = fmaf(acc[j][nt][1], acc[j][nt][1], ss0);
+        ss1 = fmaf(acc[j][nt][2], acc[j][nt][2], ss1);
+        ss1 = fmaf(acc[j][nt][3], acc[j][nt][3], ss1);
+      }
+    ss0 += __shfl_xor_sync(kFullMask, ss0, 1);
+    ss0 += __shfl_xor_sync(kFullMask, ss0, 2);
+    ss1 += __shfl_xor_sync(kFullMask, ss1, 1);
+    ss1 += __shfl_xor_sync(kFullMask, ss1, 2);
+    // ||x|| = sqrt(ss / D); u = y / sqrt(ss)
+    const float nu0 = sqrtf(ss0 * (1.0f / D)), nu1 = sqrtf(ss1 * (1.0f / D));
+    const float inv0 = ss0 > 0.f ? 1.0f / sqrtf(ss0) : 0.f;
+    const float inv1 = ss1 > 0.f ? 1.0f / sqrtf(ss1) : 0.f;
+
+    // ---- quantise and pack into this warp's row buffer ------------------------------
+    auto quant = [&](float y, float inv) -> uint32_t {
+      const float u = y * inv;
+      const float cf = fminf(fmaxf((u - q_lo) * q_inv_w, 0.f), (float)(kQCells - 1));
+      const int cell = (int)cf;
+      const QCell q = *reinterpret_cast<const QCell*>(qlane + cell * (kQCopies * sizeof(QCell)));
+      return (uint32_t)(q.lo + (u > q.point ? 1 : 0));
+    };
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // row r (half 0) / row r + 8 (half 1)
+      const float inv = half ? inv1 : inv0;
+      unsigned char* prow = pack_buf + (r + 8 * half) * RB;
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint32_t i0 = quant(acc[j][nt][2 * half], inv);
+          const uint32_t i1 = quant(acc[j][nt][2 * half + 1], inv);
+          // columns 16 j + 8 nt + 2c, +1
+          if (BITS == 4) {
+            prow[8 * j + 4 * nt + c] = (unsigned char)(i0 | (i1 << 4));
+          } else {
+            // 2 bits: byte 4 j + 2 nt + c/2 holds columns 16 j + 8 nt + 4 (c/2) .. +3
+            const uint32_t mine = i0 | (i1 << 2);
+            const uint32_t other = __shfl_xor_sync(kFullMask, mine, 1);
+            if ((c & 1) == 0) prow[4 * j + 2 * nt + (c >> 1)] = (unsigned char)(mine | (other << 4));
+          }
+        }
+      }
+      if (c == 0) *reinterpret_cast<float*>(prow + IB) = half ? nu1 : nu0;
+    }
+    __syncwarp();
+
+    // ---- store: token slabs (H rows) or single rows ---------------------------------
+    const int64_t row0 = tile * 16;
+    if (16 % H == 0 && (H * RB) % 16 == 0) {
+      const int tokens = 16 / H;
+      constexpr int CH16 = 16 * RB / 16;  // 16-byte chunks in the tile
+      for (int i = lane; i < CH16; i += 32) {
+        const int tt = (i * 16) / (H * RB);  // token within the tile
+        const int64_t t = row0 / H + tt;
+        if (tt < tokens && t < a.num_tokens) {
+          const int64_t slot = __ldg(a.slots + t);
+          if (slot >= 0) {
+            const int off = i * 16 - tt * H * RB;
+            *reinterpret_cast<uint4*>(a.pages + slot * (int64_t)(H * RB) + off) =
+                *reinterpret_cast<const uint4*>(pack_buf + i * 16);
+          }
+        }
+      }
+    } else {
+      for (int i = lane; i < 16 * (RB / 4); i += 32) {
+        const int rr = i / (RB / 4), w = i % (RB / 4);
+        const int64_t row = row0 + rr;
+        if (row < num_rows) {
+          const int64_t t = row / H;
+          const int hh = (int)(row - t * H);
+          const int64_t slot = __ldg(a.slots + t);
+          if (slot >= 0)
+            reinterpret_cast<uint32_t*>(a.pages + (slot * H + hh) * (int64_t)RB)[w] =
+                reinterpret_cast<const uint32_t*>(pack_buf + rr * RB)[w];
+        }
+      }
+    }
+    __syncwarp();
+  }
+  cp_wait_w<0>();
+}
+
+}  // namespace
+
+bool write_tc_supported(const WriteArgs& a) {
+  const bool dt = a.dtype == kF16 || a.dtype == kBF16;
+  const bool hd = a.head_dim == 64 || a.head_dim == 128;
+  const bool bt = a.bits == 2 || a.bits == 4;
+  return dt && hd && bt && a.num_kv_heads >= 1;
+}
+
+cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
+  WriteTcArgs t;
+  t.a = a;
+#define TQ_WTC(T, D, BITS)                                                                                    \
+  if (a.head_dim == D && a.bits == BITS) {                                                                    \
+    constexpr int RB = D * BITS / 8 + 4;                                                                      \
+    const size_t smem = kQCells * kQCopies * sizeof(QCell) + kWWarps * (2 * 16 * D * 2 + 16 * RB + 16);      \
+    auto kern = write_tc_kernel<T, D, BITS>;                                                                  \
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
+    if (err != cudaSuccess) return err;                                                                       \
+    kern<<<grid, kWWarps * 32, smem, stream>>>(t);                                                            \
+    return cudaGetLastError();                                                                                \
+  }
+  if (a.dtype == kF16) {
+    TQ_WTC(__half, 64, 2) TQ_WTC(__half, 64, 4) TQ_WTC(__half, 128, 2) TQ_WTC(__half, 128, 4)
+  } else if (a.dtype == kBF16) {
+    TQ_WTC(__nv_bfloat16, 64, 2) TQ_WTC(__nv_bfloat16, 64, 4) TQ_WTC(__nv_bfloat16, 128, 2)
+    TQ_WTC(__nv_bfloat16, 128, 4)
+  }
+#undef TQ_WTC
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tq

@@ -344,3 +344,42 @@ def test_tc_decode_many_short_sequences(tq):
     assert_decode_close(got[sel], ref[sel])
     empty = [b for b, n in enumerate(lens) if n == 0]
     assert np.all(got[empty] == 0)
+
+
+# ---------------------------------------------------------------- tensor-core writer shapes
+# (fp16 / bf16 rows, head_dim 64 or 128, 2 or 4 bits; H dividing the 16-row tile or not)
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d,bits", [(64, 2), (64, 4), (128, 2), (128, 4)])
+@pytest.mark.parametrize("h", [1, 3, 8, 16])
+def test_tc_writer_shapes(tq, dtype, d, bits, h):
+    rng = np.random.default_rng(d * 7 + bits * 3 + h)
+    t = 37  # rows not a multiple of the 16-row tile
+    raw32 = (rng.standard_normal((t, h, d)) * rng.lognormal(0, 0.5, (h, d))).astype(np.float32)
+    raw32[5] = 0.0  # an all-zero token
+    slots = rng.permutation(48)[:t].astype(np.int64)
+    slots[rng.random(t) < 0.2] = -1
+    raw_t = torch.from_numpy(raw32).to(torch.float16 if dtype == "f16" else torch.bfloat16)
+    raw_exact = raw_t.float().numpy()
+    pages = torch.zeros(12, 4, h, o.row_bytes(d, bits), dtype=torch.uint8, device="cuda")
+    st = tq.tq_write_kv(raw_t.cuda(), pages, torch.from_numpy(slots).cuda(), tq.tq_build_rotation(d, 42, "cuda"),
+                        lib_codebook(tq, d, bits), check=False)
+    assert int(st.item()) == 0
+    pages_np = pages.cpu().numpy()
+    check_written_rows(pages_np, raw_exact, slots, bits, OracleCodec(d))
+    check_untouched(pages_np, slots)
+
+
+def test_tc_writer_large_values_and_tiny_rows(tq):
+    # rows spanning many binades (tiny, huge) still quantise exactly: u is scale free
+    rng = np.random.default_rng(3)
+    raw32 = rng.standard_normal((64, 8, 128)).astype(np.float32)
+    raw32[:16] *= 1e-3
+    raw32[16:32] *= 3e3
+    raw_t = torch.from_numpy(raw32).half()
+    slots = np.arange(64, dtype=np.int64)
+    pages = torch.zeros(4, 16, 8, 68, dtype=torch.uint8, device="cuda")
+    st = tq.tq_write_kv(raw_t.cuda(), pages, torch.from_numpy(slots).cuda(), tq.tq_build_rotation(128, 42, "cuda"),
+                        lib_codebook(tq, 128, 4), check=False)
+    assert int(st.item()) == 0
+    check_written_rows(pages.cpu().numpy(), raw_t.float().numpy(), slots, 4, OracleCodec(128))
