@@ -109,15 +109,16 @@ struct TcCfg {
   static constexpr int kKSteps = D / 16;               // score k-steps
   static constexpr int kMTiles = D / 32;               // value m-tiles
   static constexpr int kNT = (2 * G + 7) / 8;          // value n-tiles (N = 2G)
-  // Byte-field table (4-bit indices): 256 entries x 256 bytes.  Bytes [0, 128) of an
-  // entry hold 16 lane copies of the K (hi, lo) pair, bytes [128, 256) 32 lane copies of
-  // the V fp16 pair, so one PRMT turns a packed byte into a conflict-free table offset.
-  static constexpr bool kByteTable = (KB == 4 || VB == 4);
-  static constexpr int kByteTableBytes = kByteTable ? 256 * 256 : 0;
+  // Byte-field tables (4-bit indices), 32 lane copies per entry so lookups are bank
+  // conflict free.  K: 256 entries x 256 bytes, [0, 128) the fp16 hi pairs and
+  // [128, 256) the fp16 lo pairs, so one PRMT gives the offset of both.  V: 256 entries
+  // x 128 bytes of fp16(alpha c) pairs.
+  static constexpr int kKByteBytes = KB == 4 ? 256 * 256 : 0;
+  static constexpr int kVByteBytes = VB == 4 ? 256 * 128 : 0;
   // Nibble-field tables (2-bit indices): 16 entries, no replication needed.
   static constexpr int kNibKBytes = 16 * 8;
   static constexpr int kNibVBytes = 16 * 4;
-  static constexpr int kLutBytes = kByteTableBytes + kNibKBytes + kNibVBytes;
+  static constexpr int kLutBytes = kKByteBytes + kVByteBytes + kNibKBytes + kNibVBytes;
   static_assert(kWK % 4 == 0, "K row must split into 4 interleaved word columns");
   static_assert(kWV % 8 == 0, "V row must split into 8 interleaved word columns");
   static_assert(G == 4 || G == 8, "GQA group 4 or 8");
@@ -154,8 +155,9 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   const int B = a.batch;
   const int cap = a.max_blocks_per_seq * kBS;
 
-  unsigned char* lut8 = smem;                                  // byte-field table
-  unsigned char* lutK2 = lut8 + Cfg::kByteTableBytes;          // nibble K table
+  unsigned char* lutK8 = smem;                                 // K byte-field table
+  unsigned char* lutV8 = lutK8 + Cfg::kKByteBytes;             // V byte-field table
+  unsigned char* lutK2 = lutV8 + Cfg::kVByteBytes;             // nibble K table
   unsigned char* lutV2 = lutK2 + Cfg::kNibKBytes;              // nibble V table
   unsigned char* stage_base = smem + Cfg::kLutBytes;
   const int blk_bytes = args.k_slab_smem + args.v_slab_smem;
@@ -166,16 +168,14 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
 
   // ---- tables: K (hi, lo) pairs, V fp16(alpha c) pairs -----------------------------
   if (KB == 4) {
-    for (int i = tid; i < 256 * 16; i += nthreads) {
-      const int f = i >> 4, copy = i & 15;
+    for (int i = tid; i < 256 * 32; i += nthreads) {
+      const int f = i >> 5, copy = i & 31;
       __half ha, la, hb, lb;
       split_half(__ldg(a.k_centroids + (f & 15)), ha, la);
       split_half(__ldg(a.k_centroids + (f >> 4)), hb, lb);
       __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
-      uint2 v;
-      v.x = *reinterpret_cast<uint32_t*>(&hi2);
-      v.y = *reinterpret_cast<uint32_t*>(&lo2);
-      *reinterpret_cast<uint2*>(lut8 + f * 256 + copy * 8) = v;
+      *reinterpret_cast<uint32_t*>(lutK8 + f * 256 + copy * 4) = *reinterpret_cast<uint32_t*>(&hi2);
+      *reinterpret_cast<uint32_t*>(lutK8 + f * 256 + 128 + copy * 4) = *reinterpret_cast<uint32_t*>(&lo2);
     }
   } else {
     for (int f = tid; f < 16; f += nthreads) {
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       const int f = i >> 5, copy = i & 31;
       const float ca = __ldg(a.v_centroids + (f & 15)) * args.v_alpha;
       const float cb = __ldg(a.v_centroids + (f >> 4)) * args.v_alpha;
-      *reinterpret_cast<uint32_t*>(lut8 + f * 256 + 128 + copy * 4) = pack_half2(ca, cb);
+      *reinterpret_cast<uint32_t*>(lutV8 + f * 128 + copy * 4) = pack_half2(ca, cb);
     }
   } else {
     for (int f = tid; f < 16; f += nthreads) {
@@ -278,22 +278,35 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     }
   };
   if (warp == 0 && lane < WPH) cursor_advance(lane);
-  auto fill_meta = [&](int st) {  // warp 0, lanes < WPH
-    BlockMeta m{0, 0, 0, 0};
-    int bid = -1;
+  // Metadata of one stage is loaded (global reads in flight) one pipeline step before it
+  // is stored to shared memory, so warp 0 does not wait on those reads at a barrier.
+  BlockMeta pend_m{0, 0, 0, 0};
+  int pend_len = 0, pend_bid = -1;
+  auto meta_load = [&]() {  // warp 0, lanes < WPH: the next stage of this lane's cursor
+    pend_m = BlockMeta{0, 0, 0, 0};
+    pend_bid = -1;
+    pend_len = 0;
     if (cg < g_hi) {
-      int len = __ldg(a.seq_lens + cb);
-      len = len < 0 ? 0 : (len > cap ? cap : len);
-      m.b = cb;
-      m.j = cj;
-      m.ntok = min(kBS, len - cj * kBS);
-      bid = __ldg(a.block_table + (int64_t)cb * a.max_blocks_per_seq + cj);
-      m.valid = (bid >= 0 && (int64_t)bid < a.num_blocks);
-      if (!m.valid && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+      pend_len = __ldg(a.seq_lens + cb);
+      pend_m.b = cb;
+      pend_m.j = cj;
+      pend_bid = __ldg(a.block_table + (int64_t)cb * a.max_blocks_per_seq + cj);
+      pend_m.ntok = 1;  // marks a real block until meta_store fills the count
       cursor_advance(WPH);
     }
+  };
+  auto meta_store = [&](int st) {
+    BlockMeta m = pend_m;
+    int bid = -1;
+    if (m.ntok) {
+      const int len = pend_len < 0 ? 0 : (pend_len > cap ? cap : pend_len);
+      m.ntok = min(kBS, len - m.j * kBS);
+      m.valid = (pend_bid >= 0 && (int64_t)pend_bid < a.num_blocks);
+      if (!m.valid && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+      bid = m.valid ? pend_bid : -1;
+    }
     meta[(st % kMetaRing) * WPH + lane] = m;
-    meta_bid[(st % kMetaRing) * WPH + lane] = m.valid ? bid : -1;
+    meta_bid[(st % kMetaRing) * WPH + lane] = bid;
   };
 
   // ---- copies: 16-byte cp.async of whole K / V slabs, per-token padding in smem -------
@@ -353,20 +366,29 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kLog2eTc / sqrtf((float)D);
   const int kts = args.k_tok_stride, vts = args.v_tok_stride;
-  const uint32_t k_lane_off = (lane & 15) * 8;       // K copy inside a byte-table entry
-  const uint32_t v_lane_off = 128 + lane * 4;        // V copy inside a byte-table entry
+  const uint32_t k_lane_off = lane * 4;  // K copy inside a 256-byte entry
+  const uint32_t v_lane_off = lane * 8;  // V copy (offset halved after the PRMT: 128-byte entries)
   // value-B selectors: the P value goes to the low half when (r & 1) == 0, else the high half
   const int hsel = (r >> 1) & 1;
   const uint32_t sel_b = (r & 1) ? (0x0044u | ((2u * hsel) << 8) | ((2u * hsel + 1u) << 12))
                                  : ((2u * hsel) | ((2u * hsel + 1u) << 4) | 0x4400u);
 
-  // table offsets: field e of word w
+  // table lookups for field e of word w: (hi, lo) fp16 pairs for K, one fp16 pair for V
   auto k_lookup = [&](uint32_t w, int e) -> uint2 {
-    if (KB == 4) return ld64(lut8 + __byte_perm(w, k_lane_off, 0x7604u | ((uint32_t)e << 4)));
-    return ld64(lutK2 + (((w >> (4 * e)) & 15u) << 3));
+    uint2 v;
+    if (KB == 4) {
+      const unsigned char* p = lutK8 + __byte_perm(w, k_lane_off, 0x7604u | ((uint32_t)e << 4));
+      v.x = ld32(p);
+      v.y = ld32(p + 128);
+    } else {
+      const unsigned char* p = lutK2 + (((w >> (4 * e)) & 15u) << 3);
+      v.x = ld32(p);
+      v.y = ld32(p + 4);
+    }
+    return v;
   };
   auto v_lookup = [&](uint32_t w, int e) -> uint32_t {
-    if (VB == 4) return ld32(lut8 + __byte_perm(w, v_lane_off, 0x7604u | ((uint32_t)e << 4)));
+    if (VB == 4) return ld32(lutV8 + (__byte_perm(w, v_lane_off, 0x7604u | ((uint32_t)e << 4)) >> 1));
     return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 2));
   };
 
@@ -485,8 +507,13 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   };
 
   // ---- main pipeline -----------------------------------------------------------------
-  if (warp == 0 && lane < WPH)
-    for (int st = 0; st < kNStages && st < nstages; ++st) fill_meta(st);
+  if (warp == 0 && lane < WPH) {
+    for (int st = 0; st < kNStages && st < nstages; ++st) {
+      meta_load();
+      meta_store(st);
+    }
+    meta_load();  // stage kNStages, stored in the first iteration
+  }
   __syncthreads();
   for (int st = 0; st < kNStages - 1; ++st) {
     if (st < nstages) issue_stage(st);
@@ -498,7 +525,10 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     __syncthreads();
     if (st + kNStages - 1 < nstages) issue_stage(st + kNStages - 1);
     else cp_async_commit();
-    if (warp == 0 && lane < WPH && st + kNStages < nstages) fill_meta(st + kNStages);
+    if (warp == 0 && lane < WPH && st + kNStages < nstages) {
+      meta_store(st + kNStages);
+      meta_load();
+    }
 
     const int buf = st % kNStages;
     const BlockMeta m = meta[(st % kMetaRing) * WPH + slot_u];
@@ -512,7 +542,8 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     const unsigned char* vbase = vblk + h * Cfg::kRBV;
 
     // --- scores S[tok][q head] -------------------------------------------------------
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // three independent accumulator chains (hi*hi, hi*lo, lo*hi), summed at the end
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
       const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
@@ -523,10 +554,12 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
         const uint2 x00 = k_lookup(w0, e2), x10 = k_lookup(w1, e2);
         const uint2 x01 = k_lookup(w0, e2 + 1), x11 = k_lookup(w1, e2 + 1);
         mma16816(sacc, x00.x, x10.x, x01.x, x11.x, bq_hi[s][0], bq_hi[s][1]);
-        mma16816(sacc, x00.x, x10.x, x01.x, x11.x, bq_lo[s][0], bq_lo[s][1]);
-        mma16816(sacc, x00.y, x10.y, x01.y, x11.y, bq_hi[s][0], bq_hi[s][1]);
+        mma16816(sacc1, x00.x, x10.x, x01.x, x11.x, bq_lo[s][0], bq_lo[s][1]);
+        mma16816(sacc2, x00.y, x10.y, x01.y, x11.y, bq_hi[s][0], bq_hi[s][1]);
       }
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e] + sacc2[e];
     const float kn0 = __uint_as_float(ld32(kbase + r * kts + Cfg::kWK * 4));
     const float kn1 = __uint_as_float(ld32(kbase + (r + 8) * kts + Cfg::kWK * 4));
     const float vn0 = __uint_as_float(ld32(vbase + r * vts + Cfg::kWV * 4));

@@ -54,6 +54,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& a0, uint32_
                : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
                : "r"(addr));
 }
+// d = A * B (zero accumulator input), m16n8k16, fp32 result.
 template <typename T>
 __device__ __forceinline__ void mma_rot(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                         uint32_t b1);
@@ -61,17 +62,17 @@ template <>
 __device__ __forceinline__ void mma_rot<__half>(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                 uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 template <>
 __device__ __forceinline__ void mma_rot<__nv_bfloat16>(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                        uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 // +-1 pair in the operand type: sign bits of the two halves from s0, s1 (true = negative)
 template <typename T>
@@ -82,7 +83,7 @@ __device__ __forceinline__ uint32_t pm1_pair(bool neg0, bool neg1) {
 
 struct QCell {
   int lo;       // decision points strictly below the cell
-  float point;  // first decision point at or above the cell start (+inf if none)
+  float point;  // grid coordinate of the first decision point at or above the cell start (+inf if none)
 };
 
 struct WriteTcArgs {
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
   __syncthreads();
   if (!grid_ok || *a.status != kOk) return;  // bad codebook or a slot failed validation: write nothing
   const float q_lo = grid_lo, q_inv_w = grid_inv;
+  const float grid_b = -q_lo * q_inv_w;  // grid coordinate g = u * q_inv_w + grid_b
   for (int i = threadIdx.x; i < kQCells * kQCopies; i += blockDim.x) {
     // cell = [q_lo + cell / q_inv_w, ...): decision points below its start, first one at or above
     const int cell = i / kQCopies;
@@ -175,7 +177,8 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
     }
     QCell q;
     q.lo = cell == 0 ? 0 : below;
-    q.point = cell == 0 ? bnd[0] : point;
+    const float pt = cell == 0 ? bnd[0] : point;
+    q.point = pt == INFINITY ? INFINITY : fmaf(pt, q_inv_w, -q_lo * q_inv_w);  // grid coordinate
     qtab[i] = q;
   }
   __syncthreads();
@@ -229,10 +232,17 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
   load_tile(tile, 0);
   for (; tile < num_tiles; tile += wstride, buf ^= 1) {
     load_tile(tile + wstride, buf ^ 1);
+    // slot of the tile's token `lane` for the slab store below (a global load, read early)
+    int64_t my_slot = -1;
+    if (16 % H == 0 && lane < 16 / H) {
+      const int64_t t = tile * 16 / H + lane;
+      if (t < a.num_tokens) my_slot = __ldg(a.slots + t);
+    }
     cp_wait_w<1>();
     __syncwarp();
 
     // ---- rotation: MMA per block, then butterflies across blocks ------------------
+    // acc[j][nt] = (row r: cols 2c, 2c+1 | row r+8: cols 2c, 2c+1) of block j, n-tile nt
     float acc[NB][2][4];
     const uint32_t tbase = smem_addr(raw_buf + buf * TILE_BYTES);
 #pragma unroll
@@ -243,11 +253,9 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
       uint32_t a0, a1, a2, a3;
       ldmatrix_x4(tbase + row * ROWB + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
-        mma_rot<T>(acc[j][nt], a0, a1, a2, a3, bfr[j][nt][0], bfr[j][nt][1]);
-      }
+      for (int nt = 0; nt < 2; ++nt) mma_rot<T>(acc[j][nt], a0, a1, a2, a3, bfr[j][nt][0], bfr[j][nt][1]);
     }
+    const float2 minus1 = make_float2(-1.f, -1.f);
 #pragma unroll
     for (int hs = 1; hs < NB; hs <<= 1) {
 #pragma unroll
@@ -256,52 +264,61 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float x = acc[j][nt][e], y = acc[j + hs][nt][e];
-              acc[j][nt][e] = x + y;
-              acc[j + hs][nt][e] = x - y;
+            for (int e = 0; e < 4; e += 2) {
+              const float2 x = make_float2(acc[j][nt][e], acc[j][nt][e + 1]);
+              const float2 y = make_float2(acc[j + hs][nt][e], acc[j + hs][nt][e + 1]);
+              const float2 sum = __fadd2_rn(x, y), dif = __ffma2_rn(y, minus1, x);
+              acc[j][nt][e] = sum.x;
+              acc[j][nt][e + 1] = sum.y;
+              acc[j + hs][nt][e] = dif.x;
+              acc[j + hs][nt][e + 1] = dif.y;
             }
         }
       }
     }
     // ---- norms of rows r (e = 0, 1) and r + 8 (e = 2, 3) -----------------------------
-    float ss0 = 0.f, ss1 = 0.f;
+    float2 ssv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // row r: independent chains
+    float2 ssw[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // row r + 8
 #pragma unroll
     for (int j = 0; j < NB; ++j)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        ss0 = fmaf(acc[j][nt][0], acc[j][nt][0], ss0);
-        ss0 = fmaf(acc[j][nt][1], acc[j][nt][1], ss0);
-        ss1 = fmaf(acc[j][nt][2], acc[j][nt][2], ss1);
-        ss1 = fmaf(acc[j][nt][3], acc[j][nt][3], ss1);
+        const float2 p = make_float2(acc[j][nt][0], acc[j][nt][1]);
+        const float2 q = make_float2(acc[j][nt][2], acc[j][nt][3]);
+        ssv[nt] = __ffma2_rn(p, p, ssv[nt]);
+        ssw[nt] = __ffma2_rn(q, q, ssw[nt]);
       }
+    float ss0 = (ssv[0].x + ssv[0].y) + (ssv[1].x + ssv[1].y);
+    float ss1 = (ssw[0].x + ssw[0].y) + (ssw[1].x + ssw[1].y);
     ss0 += __shfl_xor_sync(kFullMask, ss0, 1);
     ss0 += __shfl_xor_sync(kFullMask, ss0, 2);
     ss1 += __shfl_xor_sync(kFullMask, ss1, 1);
     ss1 += __shfl_xor_sync(kFullMask, ss1, 2);
-    // ||x|| = sqrt(ss / D); u = y / sqrt(ss)
+    // ||x|| = sqrt(ss / D); u = y / sqrt(ss); grid coordinate g = u * q_inv_w + gb
     const float nu0 = sqrtf(ss0 * (1.0f / D)), nu1 = sqrtf(ss1 * (1.0f / D));
-    const float inv0 = ss0 > 0.f ? 1.0f / sqrtf(ss0) : 0.f;
-    const float inv1 = ss1 > 0.f ? 1.0f / sqrtf(ss1) : 0.f;
+    const float ga0 = ss0 > 0.f ? q_inv_w / sqrtf(ss0) : 0.f;
+    const float ga1 = ss1 > 0.f ? q_inv_w / sqrtf(ss1) : 0.f;
 
     // ---- quantise and pack into this warp's row buffer ------------------------------
-    auto quant = [&](float y, float inv) -> uint32_t {
-      const float u = y * inv;
-      const float cf = fminf(fmaxf((u - q_lo) * q_inv_w, 0.f), (float)(kQCells - 1));
-      const int cell = (int)cf;
+    // the cell and the comparison both use the grid coordinate; exact for every u not
+    // within a few ulp of a decision point, whichever neighbouring cell it lands in
+    auto quant = [&](float g) -> uint32_t {
+      const uint32_t cell = min(__float2uint_rz(g), (uint32_t)(kQCells - 1));
       const QCell q = *reinterpret_cast<const QCell*>(qlane + cell * (kQCopies * sizeof(QCell)));
-      return (uint32_t)(q.lo + (u > q.point ? 1 : 0));
+      return (uint32_t)(q.lo + (g > q.point ? 1 : 0));
     };
 #pragma unroll
     for (int half = 0; half < 2; ++half) {  // row r (half 0) / row r + 8 (half 1)
-      const float inv = half ? inv1 : inv0;
+      const float ga = half ? ga1 : ga0;
+      const float2 gav = make_float2(ga, ga), gbv = make_float2(grid_b, grid_b);
       unsigned char* prow = pack_buf + (r + 8 * half) * RB;
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          const uint32_t i0 = quant(acc[j][nt][2 * half], inv);
-          const uint32_t i1 = quant(acc[j][nt][2 * half + 1], inv);
+          const float2 g = __ffma2_rn(make_float2(acc[j][nt][2 * half], acc[j][nt][2 * half + 1]), gav, gbv);
+          const uint32_t i0 = quant(g.x);
+          const uint32_t i1 = quant(g.y);
           // columns 16 j + 8 nt + 2c, +1
           if (BITS == 4) {
             prow[8 * j + 4 * nt + c] = (unsigned char)(i0 | (i1 << 4));
@@ -320,18 +337,16 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
     // ---- store: token slabs (H rows) or single rows ---------------------------------
     const int64_t row0 = tile * 16;
     if (16 % H == 0 && (H * RB) % 16 == 0) {
-      const int tokens = 16 / H;
       constexpr int CH16 = 16 * RB / 16;  // 16-byte chunks in the tile
-      for (int i = lane; i < CH16; i += 32) {
-        const int tt = (i * 16) / (H * RB);  // token within the tile
-        const int64_t t = row0 / H + tt;
-        if (tt < tokens && t < a.num_tokens) {
-          const int64_t slot = __ldg(a.slots + t);
-          if (slot >= 0) {
-            const int off = i * 16 - tt * H * RB;
-            *reinterpret_cast<uint4*>(a.pages + slot * (int64_t)(H * RB) + off) =
-                *reinterpret_cast<const uint4*>(pack_buf + i * 16);
-          }
+#pragma unroll
+      for (int k = 0; k < (CH16 + 31) / 32; ++k) {
+        const int i = lane + 32 * k;
+        const int tt = min(i, CH16 - 1) * 16 / (H * RB);  // token within the tile
+        const int64_t slot = __shfl_sync(kFullMask, my_slot, tt);
+        if (i < CH16 && slot >= 0) {
+          const int off = i * 16 - tt * H * RB;
+          *reinterpret_cast<uint4*>(a.pages + slot * (int64_t)(H * RB) + off) =
+              *reinterpret_cast<const uint4*>(pack_buf + i * 16);
         }
       }
     } else {
