@@ -350,7 +350,11 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
   a.workspace = workspace;
   a.status = status_dev;
   a.v_alpha = 1.0f;
-  if (batch > 0 && tq::tc_decode_supported(a)) a.v_alpha = fp16_scale_for(head_dim, v_bits);
+  a.k_alpha = 1.0f;
+  if (batch > 0 && tq::tc_decode_supported(a)) {
+    a.v_alpha = fp16_scale_for(head_dim, v_bits);
+    a.k_alpha = fp16_scale_for(head_dim, k_bits);
+  }
   const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());
   if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
     return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: workspace must be >= %zu bytes and 16-byte aligned (got %zu)",

@@ -133,6 +133,7 @@ struct TcArgs {
   int k_slab_smem;        // bytes per K block in smem
   int v_slab_smem;
   float v_alpha;          // V centroid scale
+  float k_alpha;          // K centroid scale
   float* part_acc;        // [WPH*(C+B)][Hq][D]
   float* part_ml;         // [WPH*(C+B)][Hq][2]
   int* prefix;            // [B+1] block prefix sums (written by CTA 0)
@@ -142,6 +143,11 @@ struct TcArgs {
 // entry of stage st + kNStages while stage st is being consumed.
 constexpr int kMetaRing = kNStages + 1;
 constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
+// Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored with the fp16-hi key part
+// only.  With the alpha scaling the hi part is within ~1e-4 relative of the fp32
+// centroid, so the score error of such a tile stays far below the output tolerance;
+// tiles above the bound (rows with very large norms) add the fp16-lo part.
+constexpr float kFastScoreBound = 48.0f;
 
 template <int D, int KB, int VB, int G, int WPH>
 __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args) {
@@ -171,8 +177,8 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     for (int i = tid; i < 256 * 32; i += nthreads) {
       const int f = i >> 5, copy = i & 31;
       __half ha, la, hb, lb;
-      split_half(__ldg(a.k_centroids + (f & 15)), ha, la);
-      split_half(__ldg(a.k_centroids + (f >> 4)), hb, lb);
+      split_half(__ldg(a.k_centroids + (f & 15)) * args.k_alpha, ha, la);
+      split_half(__ldg(a.k_centroids + (f >> 4)) * args.k_alpha, hb, lb);
       __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
       *reinterpret_cast<uint32_t*>(lutK8 + f * 256 + copy * 4) = *reinterpret_cast<uint32_t*>(&hi2);
       *reinterpret_cast<uint32_t*>(lutK8 + f * 256 + 128 + copy * 4) = *reinterpret_cast<uint32_t*>(&lo2);
@@ -180,8 +186,8 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   } else {
     for (int f = tid; f < 16; f += nthreads) {
       __half ha, la, hb, lb;
-      split_half(__ldg(a.k_centroids + (f & 3)), ha, la);
-      split_half(__ldg(a.k_centroids + (f >> 2)), hb, lb);
+      split_half(__ldg(a.k_centroids + (f & 3)) * args.k_alpha, ha, la);
+      split_half(__ldg(a.k_centroids + (f >> 2)) * args.k_alpha, hb, lb);
       __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
       uint2 v;
       v.x = *reinterpret_cast<uint32_t*>(&hi2);
@@ -373,26 +379,24 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   const uint32_t sel_b = (r & 1) ? (0x0044u | ((2u * hsel) << 8) | ((2u * hsel + 1u) << 12))
                                  : ((2u * hsel) | ((2u * hsel + 1u) << 4) | 0x4400u);
 
-  // table lookups for field e of word w: (hi, lo) fp16 pairs for K, one fp16 pair for V
-  auto k_lookup = [&](uint32_t w, int e) -> uint2 {
-    uint2 v;
-    if (KB == 4) {
-      const unsigned char* p = lutK8 + __byte_perm(w, k_lane_off, 0x7604u | ((uint32_t)e << 4));
-      v.x = ld32(p);
-      v.y = ld32(p + 128);
-    } else {
-      const unsigned char* p = lutK2 + (((w >> (4 * e)) & 15u) << 3);
-      v.x = ld32(p);
-      v.y = ld32(p + 4);
-    }
-    return v;
+  // table lookups for field e of word w: K (hi, lo) fp16 pairs, V one fp16 pair
+  auto k_offset = [&](uint32_t w, int e) -> uint32_t {
+    if (KB == 4) return __byte_perm(w, k_lane_off, 0x7604u | ((uint32_t)e << 4));
+    return ((w >> (4 * e)) & 15u) << 3;
   };
+  auto k_hi = [&](uint32_t off) -> uint32_t { return ld32((KB == 4 ? lutK8 : lutK2) + off); };
+  auto k_lo = [&](uint32_t off) -> uint32_t { return ld32((KB == 4 ? lutK8 : lutK2) + off + (KB == 4 ? 128 : 4)); };
   auto v_lookup = [&](uint32_t w, int e) -> uint32_t {
     if (VB == 4) return ld32(lutV8 + (__byte_perm(w, v_lane_off, 0x7604u | ((uint32_t)e << 4)) >> 1));
     return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 2));
   };
 
-  uint32_t bq_hi[Cfg::kKSteps][2], bq_lo[Cfg::kKSteps][2];
+  // Query B fragments.  G = 4: one set whose columns 0-3 hold the fp16 hi part of the
+  // rotated query and columns 4-7 (the unused half of the n = 8 MMA) its fp16 lo part,
+  // so one MMA yields both products.  G = 8: separate hi and lo sets.
+  constexpr int kQSets = G == 4 ? 1 : 2;
+  uint32_t bq[kQSets][Cfg::kKSteps][2];
+  float qnorm_max = 0.f;  // max over this warp's heads of ||rotated query|| (log2 units)
   float o_acc[Cfg::kNT][Cfg::kMTiles][4];
   float m_run[2], l_run[2];
   int cur_b = -1;
@@ -413,15 +417,21 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     constexpr int E = D / 32;
     float qr[G][E];
 #pragma unroll
+    qnorm_max = 0.f;
     for (int g = 0; g < G; ++g) {
       const int64_t base = ((int64_t)b * a.num_q_heads + (int64_t)h * G + g) * D + lane * E;
 #pragma unroll
       for (int i = 0; i < E; ++i) qr[g][i] = load_as_f32(a.q, base + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
       fwht_warp<E>(qr[g]);
+      float ss = 0.f;
 #pragma unroll
-      for (int i = 0; i < E; ++i) qr[g][i] *= qmul;
+      for (int i = 0; i < E; ++i) {
+        qr[g][i] *= qmul;
+        ss = fmaf(qr[g][i], qr[g][i], ss);
+      }
+      qnorm_max = fmaxf(qnorm_max, sqrtf(warp_sum(ss)));
     }
-    const int gq = r;  // this lane's B column (q head); columns >= G are zero
+    const int gq = G == 4 ? (r & 3) : r;  // this lane's B column -> q head
 #pragma unroll
     for (int s = 0; s < Cfg::kKSteps; ++s) {
 #pragma unroll
@@ -445,13 +455,18 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
         split_half(x0, h0, l0);
         split_half(x1, h1, l1);
         __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
-        bq_hi[s][u] = *reinterpret_cast<uint32_t*>(&hh);
-        bq_lo[s][u] = *reinterpret_cast<uint32_t*>(&ll);
+        if (G == 4) {
+          bq[0][s][u] = r < 4 ? *reinterpret_cast<uint32_t*>(&hh) : *reinterpret_cast<uint32_t*>(&ll);
+        } else {
+          bq[0][s][u] = *reinterpret_cast<uint32_t*>(&hh);
+          bq[kQSets - 1][s][u] = *reinterpret_cast<uint32_t*>(&ll);
+        }
       }
     }
   };
 
   const float inv_alpha = 1.0f / args.v_alpha;
+  const float inv_alpha_k = 1.0f / args.k_alpha;
   // Writes this warp's partial for sequence b (empty when `empty`).
   auto flush = [&](int b, bool empty) {
     const int64_t slot = (int64_t)WPH * (cta + b) + slot_u;
@@ -542,33 +557,65 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     const unsigned char* vbase = vblk + h * Cfg::kRBV;
 
     // --- scores S[tok][q head] -------------------------------------------------------
-    // three independent accumulator chains (hi*hi, hi*lo, lo*hi), summed at the end
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
-      const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
-      const uint32_t w1 = ld32(kbase + (r + 8) * kts + (c + 4 * jw) * 4);
-#pragma unroll
-      for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
-        const int s = (jw * Cfg::kPWK + e2) >> 1;
-        const uint2 x00 = k_lookup(w0, e2), x10 = k_lookup(w1, e2);
-        const uint2 x01 = k_lookup(w0, e2 + 1), x11 = k_lookup(w1, e2 + 1);
-        mma16816(sacc, x00.x, x10.x, x01.x, x11.x, bq_hi[s][0], bq_hi[s][1]);
-        mma16816(sacc1, x00.x, x10.x, x01.x, x11.x, bq_lo[s][0], bq_lo[s][1]);
-        mma16816(sacc2, x00.y, x10.y, x01.y, x11.y, bq_hi[s][0], bq_hi[s][1]);
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e] + sacc2[e];
     const float kn0 = __uint_as_float(ld32(kbase + r * kts + Cfg::kWK * 4));
     const float kn1 = __uint_as_float(ld32(kbase + (r + 8) * kts + Cfg::kWK * 4));
     const float vn0 = __uint_as_float(ld32(vbase + r * vts + Cfg::kWV * 4));
     const float vn1 = __uint_as_float(ld32(vbase + (r + 8) * vts + Cfg::kWV * 4));
+    // Precision switch: a tile whose largest |score| bound nu_k * ||q|| stays within
+    // kFastScoreBound takes the fp16-hi key path (rounding error ~1e-4 relative after the
+    // alpha scaling); other tiles (large-norm rows) add the fp16-lo key part as well.
+    float nmax = fmaxf(r < m.ntok ? fabsf(kn0) : 0.f, r + 8 < m.ntok ? fabsf(kn1) : 0.f);
+    nmax = fmaxf(nmax, __shfl_xor_sync(kFullMask, nmax, 4));
+    nmax = fmaxf(nmax, __shfl_xor_sync(kFullMask, nmax, 8));
+    nmax = fmaxf(nmax, __shfl_xor_sync(kFullMask, nmax, 16));
+    const bool exact = __any_sync(kFullMask, nmax * qnorm_max > kFastScoreBound);
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
+    // G = 4: columns 0-3 get key * q_hi, 4-7 key * q_lo;  G = 8: separate q_lo chain
+    if (!exact) {
+#pragma unroll
+      for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
+        const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
+        const uint32_t w1 = ld32(kbase + (r + 8) * kts + (c + 4 * jw) * 4);
+#pragma unroll
+        for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
+          const int s = (jw * Cfg::kPWK + e2) >> 1;
+          const uint32_t h00 = k_hi(k_offset(w0, e2)), h10 = k_hi(k_offset(w1, e2));
+          const uint32_t h01 = k_hi(k_offset(w0, e2 + 1)), h11 = k_hi(k_offset(w1, e2 + 1));
+          mma16816(sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+          if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
+        const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
+        const uint32_t w1 = ld32(kbase + (r + 8) * kts + (c + 4 * jw) * 4);
+#pragma unroll
+        for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
+          const int s = (jw * Cfg::kPWK + e2) >> 1;
+          const uint32_t o00 = k_offset(w0, e2), o10 = k_offset(w1, e2);
+          const uint32_t o01 = k_offset(w0, e2 + 1), o11 = k_offset(w1, e2 + 1);
+          const uint32_t h00 = k_hi(o00), h10 = k_hi(o10), h01 = k_hi(o01), h11 = k_hi(o11);
+          const uint32_t l00 = k_lo(o00), l10 = k_lo(o10), l01 = k_lo(o01), l11 = k_lo(o11);
+          mma16816(sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+          if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+          mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e] + sacc2[e];
+    if (G == 4) {
+      // fold the q_lo columns (lanes c = 2, 3) onto the q_hi columns (lanes c = 0, 1)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(kFullMask, sacc[e], 2);
+    }
+    const float kn0s = kn0 * inv_alpha_k, kn1s = kn1 * inv_alpha_k;
     float sc[4];
-    sc[0] = r < m.ntok ? sacc[0] * kn0 : -INFINITY;
-    sc[1] = r < m.ntok ? sacc[1] * kn0 : -INFINITY;
-    sc[2] = r + 8 < m.ntok ? sacc[2] * kn1 : -INFINITY;
-    sc[3] = r + 8 < m.ntok ? sacc[3] * kn1 : -INFINITY;
+    sc[0] = r < m.ntok ? sacc[0] * kn0s : -INFINITY;
+    sc[1] = r < m.ntok ? sacc[1] * kn0s : -INFINITY;
+    sc[2] = r + 8 < m.ntok ? sacc[2] * kn1s : -INFINITY;
+    sc[3] = r + 8 < m.ntok ? sacc[3] * kn1s : -INFINITY;
 
     // --- online softmax (q heads 2c, 2c+1 on this lane); the running max is only moved
     // when the tile max passes it by more than kRescaleSlack, so p <= 2^slack.
@@ -716,6 +763,7 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   t.k_slab_smem = (kBS * t.k_tok_stride + 15) / 16 * 16;
   t.v_slab_smem = (kBS * t.v_tok_stride + 15) / 16 * 16;
   t.v_alpha = a.v_alpha > 0.f ? a.v_alpha : 1.0f;
+  t.k_alpha = a.k_alpha > 0.f ? a.k_alpha : 1.0f;
   const int B = a.batch, Hq = a.num_q_heads;
   const int64_t slots = (int64_t)WPH * (p.num_splits + B);
   t.part_acc = static_cast<float*>(a.workspace);

@@ -73,6 +73,7 @@ struct DecodeArgs {
   void* workspace;
   int32_t* status;  // may be null
   float v_alpha;    // fp16 scale of the V centroids (tensor-core decode); 1 when unknown
+  float k_alpha;    // fp16 scale of the K centroids (tensor-core decode); 1 when unknown
 };
 
 // Tensor-core decode (tq_decode_tc.cu): whether the shapes/bits in `a` have an

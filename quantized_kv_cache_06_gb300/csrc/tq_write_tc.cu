@@ -9,12 +9,12 @@
 //    B_j = diag(s_j) H_16 (entries +-1: exact in fp16 / bf16, products exact in the fp32
 //    accumulator), followed by the H_{D/16} butterflies across blocks, in registers.
 //  * Norm.  ||y||^2 = D ||x||^2: a sum of the thread's squares plus two quad shuffles.
-//  * Quantiser.  u = y / sqrt(sum y^2) lands in one of 256 equal cells covering the
-//    decision points; each cell stores (number of decision points below the cell, the
-//    first decision point at or above the cell), and the cells are placed so that no
-//    decision point lies near a cell edge.  index = lo + (u > point): one compare, exact
-//    "#{k : boundary_k < u}" whichever cell a rounding picks near an edge.  The table is
-//    replicated per lane (16 copies, 64-bit entries) so the lookups are conflict free.
+//  * Quantiser.  u = y / sqrt(sum y^2) lies in [-1, 1]; N equal cells cover that range
+//    and each stores (number of decision points below the cell, the first decision point
+//    at or above it), with N chosen so that no decision point lies near a cell edge.
+//    index = lo + (u > point): one compare, exact "#{k : boundary_k < u}" whichever cell
+//    a rounding picks near an edge.  The table is replicated per lane (16 copies, 64-bit
+//    entries) so the lookups are conflict free.
 //  * Packing.  Bytes are assembled per row in shared memory (LSB-first fields, then the
 //    fp32 norm); a token's H rows are contiguous in the page (H * row_bytes bytes), so the
 //    warp stores whole token slabs with 16-byte stores.
@@ -32,7 +32,8 @@ namespace tq {
 namespace {
 
 constexpr int kWWarps = 8;          // warps per CTA
-constexpr int kQCells = 256;        // quantiser cells
+constexpr int kGridMaxA = 128;       // largest grid scale: 2 * 128 cells over u in [-1, 1]
+constexpr int kQCells = 2 * kGridMaxA + 1;  // quantiser table entries
 constexpr int kQCopies = 16;        // lane copies of the quantiser table
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -90,36 +91,30 @@ struct WriteTcArgs {
   WriteArgs a;
 };
 
-// Quantiser grid chosen from the decision points b_0 < ... < b_{m-1}: 256 cells of width
-// w = span / 200 starting 8 cells below b_0, at the first phase (of 32) that keeps every
-// b_k at least 1/64 cell from a cell edge and in a cell of its own.  Deterministic, so
-// every CTA picks the same grid.  Returns false when no phase qualifies (then the caller
-// reports an error instead of writing).
-__device__ bool choose_grid(const float* b, int m, float& q_lo, float& q_inv_w) {
-  const float span = b[m - 1] - b[0];
-  if (m == 1) {  // one decision point: any grid around it
-    q_inv_w = 1.0f;
-    q_lo = b[0] - 128.5f;
-    return true;
-  }
-  if (!(span > 0.f)) return false;
-  for (int t = 0; t < 8; ++t) {
-    const float w = span / 200.0f * (1.0f + 0.01f * t);
-    for (int p = 0; p < 32; ++p) {
-      const float lo = b[0] - w * (8.0f + p / 32.0f);
-      const float inv = 1.0f / w;
+// Quantiser grid g = u A + B, B = A + phi with 0 < phi < 1, cell = floor(g).  u is a
+// coordinate of a unit vector, so g stays in [phi, 2A + phi] up to rounding: cells 0 to
+// 2A, with no clamp (the unsigned conversion also maps a negative g or a NaN to cell 0).
+// (A, phi) is the first pair, largest A first, that keeps every decision point b_k at
+// least 1/64 cell from a cell edge and no two in one cell.  Deterministic, so every CTA
+// picks the same grid.  Returns false when no pair qualifies (the caller then reports
+// an error instead of writing).
+__device__ bool choose_grid(const float* b, int m, float& q_a, float& q_b) {
+  const float phases[4] = {0.5f, 0.25f, 0.75f, 0.375f};
+  for (int n = kGridMaxA; n >= kGridMaxA / 4; n -= 2) {
+    for (int p = 0; p < 4; ++p) {
+      const float ga = (float)n, gb = (float)n + phases[p];
       bool ok = true;
       int prev = -1;
       for (int k = 0; k < m && ok; ++k) {
-        const float x = (b[k] - lo) * inv;
+        const float x = fmaf(b[k], ga, gb);
         const int cell = (int)floorf(x);
         const float f = x - (float)cell;
-        ok = cell > prev && cell >= 1 && cell < 255 && f >= 1.0f / 64 && f <= 63.0f / 64;
+        ok = cell > prev && f >= 1.0f / 64 && f <= 63.0f / 64;
         prev = cell;
       }
       if (ok) {
-        q_lo = lo;
-        q_inv_w = inv;
+        q_a = ga;
+        q_b = gb;
         return true;
       }
     }
@@ -150,35 +145,33 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
   // the quantiser grid
   constexpr int NC = 1 << BITS;
   __shared__ float bnd[NC - 1];
-  __shared__ float grid_lo, grid_inv;
+  __shared__ float grid_a, grid_b;
   __shared__ int grid_ok;
   if (threadIdx.x < NC - 1) bnd[threadIdx.x] = 0.5f * (a.centroids[threadIdx.x] + a.centroids[threadIdx.x + 1]);
   __syncthreads();
   if (threadIdx.x == 0) {
-    float lo = 0.f, inv = 0.f;
-    grid_ok = choose_grid(bnd, NC - 1, lo, inv) ? 1 : 0;
-    grid_lo = lo;
-    grid_inv = inv;
+    float ga = 0.f, gb = 0.f;
+    grid_ok = choose_grid(bnd, NC - 1, ga, gb) ? 1 : 0;
+    grid_a = ga;
+    grid_b = gb;
     if (!grid_ok && blockIdx.x == 0) atomicMax(a.status, (int32_t)kUnsupported);
   }
   __syncthreads();
   if (!grid_ok || *a.status != kOk) return;  // bad codebook or a slot failed validation: write nothing
-  const float q_lo = grid_lo, q_inv_w = grid_inv;
-  const float grid_b = -q_lo * q_inv_w;  // grid coordinate g = u * q_inv_w + grid_b
+  const float q_a = grid_a, q_b = grid_b;  // grid coordinate g = u * q_a + q_b, cell = floor(g)
   for (int i = threadIdx.x; i < kQCells * kQCopies; i += blockDim.x) {
-    // cell = [q_lo + cell / q_inv_w, ...): decision points below its start, first one at or above
+    // cell [cell, cell + 1) in grid units: decision points below its start, first one at or above
     const int cell = i / kQCopies;
-    const float lo_edge = q_lo + (float)cell / q_inv_w;
     int below = 0;
     float point = INFINITY;
     for (int k = 0; k < NC - 1; ++k) {
-      if (bnd[k] < lo_edge) ++below;
-      else if (point == INFINITY) point = bnd[k];
+      const float gk = fmaf(bnd[k], q_a, q_b);
+      if (gk < (float)cell) ++below;
+      else if (point == INFINITY) point = gk;
     }
     QCell q;
-    q.lo = cell == 0 ? 0 : below;
-    const float pt = cell == 0 ? bnd[0] : point;
-    q.point = pt == INFINITY ? INFINITY : fmaf(pt, q_inv_w, -q_lo * q_inv_w);  // grid coordinate
+    q.lo = below;
+    q.point = point;
     qtab[i] = q;
   }
   __syncthreads();
@@ -294,23 +287,27 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
     ss0 += __shfl_xor_sync(kFullMask, ss0, 2);
     ss1 += __shfl_xor_sync(kFullMask, ss1, 1);
     ss1 += __shfl_xor_sync(kFullMask, ss1, 2);
-    // ||x|| = sqrt(ss / D); u = y / sqrt(ss); grid coordinate g = u * q_inv_w + gb
+    // ||x|| = sqrt(ss / D); u = y / sqrt(ss); grid coordinate g = u * q_a + q_b.
+    // Every partial sum above only grows, so y^2 <= ss (1 + 2^-23) + 2^-150 for each y of
+    // the row, even when ss is subnormal; adding 2^-149 under the root therefore keeps
+    // |u| <= 1 + 2^-23 and g inside [0, 2 q_a + 1) with no clamp.  It moves ss by at most
+    // one ulp, and only below 2^-124; an all-zero row gets g = q_b, i.e. u = 0.
     const float nu0 = sqrtf(ss0 * (1.0f / D)), nu1 = sqrtf(ss1 * (1.0f / D));
-    const float ga0 = ss0 > 0.f ? q_inv_w / sqrtf(ss0) : 0.f;
-    const float ga1 = ss1 > 0.f ? q_inv_w / sqrtf(ss1) : 0.f;
+    const float ga0 = q_a / sqrtf(ss0 + 0x1p-149f);
+    const float ga1 = q_a / sqrtf(ss1 + 0x1p-149f);
 
     // ---- quantise and pack into this warp's row buffer ------------------------------
     // the cell and the comparison both use the grid coordinate; exact for every u not
     // within a few ulp of a decision point, whichever neighbouring cell it lands in
     auto quant = [&](float g) -> uint32_t {
-      const uint32_t cell = min(__float2uint_rz(g), (uint32_t)(kQCells - 1));
+      const uint32_t cell = __float2uint_rz(g);  // 0 for g < 0 or NaN, at most 2 q_a otherwise
       const QCell q = *reinterpret_cast<const QCell*>(qlane + cell * (kQCopies * sizeof(QCell)));
       return (uint32_t)(q.lo + (g > q.point ? 1 : 0));
     };
 #pragma unroll
     for (int half = 0; half < 2; ++half) {  // row r (half 0) / row r + 8 (half 1)
       const float ga = half ? ga1 : ga0;
-      const float2 gav = make_float2(ga, ga), gbv = make_float2(grid_b, grid_b);
+      const float2 gav = make_float2(ga, ga), gbv = make_float2(q_b, q_b);
       unsigned char* prow = pack_buf + (r + 8 * half) * RB;
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
