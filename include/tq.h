@@ -53,7 +53,10 @@ typedef enum tq_status {
   TQ_ERR_UNSUPPORTED = 2,        /* valid but outside what the kernels handle (D, bits, GQA group) */
   TQ_ERR_SLOT_OUT_OF_RANGE = 3,  /* a write slot >= num_blocks * block_size */
   TQ_ERR_BLOCK_OUT_OF_RANGE = 4, /* a block-table entry read by decode lies outside [0, num_blocks) */
-  TQ_ERR_CUDA = 5                /* a CUDA runtime call failed (message in tq_last_error) */
+  TQ_ERR_CUDA = 5,               /* a CUDA runtime call failed (message in tq_last_error) */
+  TQ_ERR_TIMEOUT = 6             /* a device-side wait gave up after its iteration limit; the
+                                    output of that call is incomplete (an internal error: no
+                                    valid input produces it) */
 } tq_status;
 
 typedef enum tq_dtype { TQ_F32 = 0, TQ_F16 = 1, TQ_BF16 = 2 } tq_dtype;

@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     TQ_ERR_CUDA,
     TQ_ERR_INVALID_ARG,
     TQ_ERR_SLOT_OUT_OF_RANGE,
+    TQ_ERR_TIMEOUT,
     TQ_ERR_UNSUPPORTED,
     TQ_OK,
     TQError,

@@ -21,6 +21,7 @@ TQ_ERR_UNSUPPORTED = 2
 TQ_ERR_SLOT_OUT_OF_RANGE = 3
 TQ_ERR_BLOCK_OUT_OF_RANGE = 4
 TQ_ERR_CUDA = 5
+TQ_ERR_TIMEOUT = 6
 
 STATUS_NAMES = {
     TQ_OK: "TQ_OK",
@@ -29,6 +30,7 @@ STATUS_NAMES = {
     TQ_ERR_SLOT_OUT_OF_RANGE: "TQ_ERR_SLOT_OUT_OF_RANGE",
     TQ_ERR_BLOCK_OUT_OF_RANGE: "TQ_ERR_BLOCK_OUT_OF_RANGE",
     TQ_ERR_CUDA: "TQ_ERR_CUDA",
+    TQ_ERR_TIMEOUT: "TQ_ERR_TIMEOUT",
 }
 
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}

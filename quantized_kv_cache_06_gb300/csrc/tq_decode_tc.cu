@@ -10,8 +10,12 @@
 //
 // Per CTA: WPH warps per kv head (warp w: head w % H, block slot w / H).  A stage holds
 // WPH consecutive blocks; their whole K and V slabs (block_size * H * row_bytes bytes,
-// contiguous in the page tensor) are staged with 16-byte cp.async into shared memory,
-// K rows padded so that the fragment reads are bank-conflict free.
+// contiguous in the page tensor) are brought into shared memory by one bulk async copy
+// each, issued by a producer warp (the CTA's last warp, which does no math) and
+// completed on a per-stage "full" mbarrier.  Every consumer warp signals a per-stage
+// "empty" mbarrier when it is done with the stage, and the producer waits on it before
+// it refills the buffers.  No CTA-wide barrier in the main loop.  (A consumer warp that
+// also issues the copies delays them by its own math and serialises copy and compute.)
 //
 // Scores.  For a 16-token tile of one kv head the warp computes S[16 tok x 8 q-heads]
 // = Khat[16 x D] * qrot^T with m16n8k16 MMAs.  The A operand is looked up from the
@@ -43,7 +47,6 @@ namespace tq {
 namespace {
 
 constexpr int kBS = 16;       // tokens per block (the only block size this kernel takes)
-constexpr int kNStages = 3;   // cp.async ring depth (stages of WPH blocks)
 constexpr float kLog2eTc = 1.4426950408889634f;
 
 struct BlockMeta {
@@ -57,17 +60,55 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+// mbarrier and bulk-copy primitives (shared-window addresses).  Every wait is bounded:
+// after kWaitLimit unsuccessful tries the caller reports kTimeout and stops.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(tx) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `bar` with parity `parity` to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// that completes `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Shared load from an absolute shared-window address.  Not volatile: its address is
+// computed from data read after the stage's wait, which orders it.
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32_off128(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1+128];\n" : "=r"(v) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t ld32(const unsigned char* p) { return *reinterpret_cast<const uint32_t*>(p); }
-__device__ __forceinline__ uint2 ld64(const unsigned char* p) { return *reinterpret_cast<const uint2*>(p); }
 
 // 2^x with the hardware approximation (denormal results flush to zero): the softmax
 // weights it produces are relative to the running max, so tiny values do not matter.
@@ -109,16 +150,16 @@ struct TcCfg {
   static constexpr int kKSteps = D / 16;               // score k-steps
   static constexpr int kMTiles = D / 32;               // value m-tiles
   static constexpr int kNT = (2 * G + 7) / 8;          // value n-tiles (N = 2G)
-  // Byte-field tables (4-bit indices), 32 lane copies per entry so lookups are bank
-  // conflict free.  K: 256 entries x 256 bytes, [0, 128) the fp16 hi pairs and
-  // [128, 256) the fp16 lo pairs, so one PRMT gives the offset of both.  V: 256 entries
-  // x 128 bytes of fp16(alpha c) pairs.
-  static constexpr int kKByteBytes = KB == 4 ? 256 * 256 : 0;
-  static constexpr int kVByteBytes = VB == 4 ? 256 * 128 : 0;
-  // Nibble-field tables (2-bit indices): 16 entries, no replication needed.
-  static constexpr int kNibKBytes = 16 * 8;
-  static constexpr int kNibVBytes = 16 * 4;
-  static constexpr int kLutBytes = kKByteBytes + kVByteBytes + kNibKBytes + kNibVBytes;
+  // Byte-field table T (4-bit indices): 256 entries x 256 bytes, [0, 128) the fp16 hi
+  // parts of the K centroid pairs and [128, 256) the V pairs fp16(alpha c), 32 lane
+  // copies each so lookups are bank conflict free.  T sits at a 64 KB aligned shared
+  // address, so one PRMT of (packed word, T base | lane * 4) yields the absolute
+  // address of an entry.
+  static constexpr bool kHasT = KB == 4 || VB == 4;
+  static constexpr int kTBytes = kHasT ? 256 * 256 : 0;
+  // The small tables (K lo parts of byte fields, read only by tiles that need the exact
+  // score, and the nibble-field tables of 2-bit indices) have one copy each and live in
+  // the fixed part of the shared memory.
   static_assert(kWK % 4 == 0, "K row must split into 4 interleaved word columns");
   static_assert(kWV % 8 == 0, "V row must split into 8 interleaved word columns");
   static_assert(G == 4 || G == 8, "GQA group 4 or 8");
@@ -130,18 +171,33 @@ struct TcArgs {
   int num_ctas;           // C
   int k_tok_stride;       // smem bytes per token in a K slab (H*RBK + pad)
   int v_tok_stride;
-  int k_slab_smem;        // bytes per K block in smem
+  int k_slab_smem;        // bytes of the K part of a block buffer
   int v_slab_smem;
+  int k_row_copy;         // 1: K copied one token row at a time (padded rows); 0: one slab copy
+  int v_row_copy;
   float v_alpha;          // V centroid scale
   float k_alpha;          // K centroid scale
+  int nst;                // pipeline stages (WPH block buffers each), 2..kMaxStages
+  int n_lo;               // block buffers below the T table
+  int buf_lo;             // dynamic-smem offset of buffer 0
+  int buf_hi;             // dynamic-smem offset of buffer n_lo
+  int buf_bytes;          // bytes per block buffer
+  int t_off;              // dynamic-smem offset of T (64 KB aligned shared address)
   float* part_acc;        // [WPH*(C+B)][Hq][D]
   float* part_ml;         // [WPH*(C+B)][Hq][2]
   int* prefix;            // [B+1] block prefix sums (written by CTA 0)
 };
 
-// Per-stage block metadata ring: kNStages + 1 entries so that warp 0 can fill the
-// entry of stage st + kNStages while stage st is being consumed.
-constexpr int kMetaRing = kNStages + 1;
+// Fixed part of the dynamic shared memory (offsets from its start).
+constexpr int kMaxStages = 8;
+constexpr int kOffBar = 0;                                  // full[kMaxStages], empty[kMaxStages]
+constexpr int kOffMeta = kOffBar + 2 * kMaxStages * 8;      // BlockMeta[kMaxStages][WPH <= 2]
+constexpr int kOffScan = kOffMeta + kMaxStages * 2 * 16;    // int[36]
+constexpr int kOffK2 = kOffScan + 36 * 4;                   // nibble K table, 16 x 8 bytes
+constexpr int kOffV2 = kOffK2 + 16 * 8;                     // nibble V table, 16 x 4 bytes
+constexpr int kOffL = kOffV2 + 16 * 4;                      // byte K lo table, 256 x 4 bytes
+constexpr int kMiscBytes = (kOffL + 256 * 4 + 127) / 128 * 128;
+
 constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
 // Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored with the fp16-hi key part
 // only.  With the alpha scaling the hi part is within ~1e-4 relative of the fp32
@@ -150,29 +206,39 @@ constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag beh
 constexpr float kFastScoreBound = 48.0f;
 
 template <int D, int KB, int VB, int G, int WPH>
-__global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args) {
+__global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs args) {
   using Cfg = TcCfg<D, KB, VB, G, WPH>;
   const DecodeArgs& a = args.a;
   extern __shared__ __align__(128) unsigned char smem[];
   const int H = a.num_kv_heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nthreads = blockDim.x;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int ncons = nwarps - 1;  // consumer warps; warp ncons is the producer
   const int cta = blockIdx.x, C = args.num_ctas;
   const int B = a.batch;
   const int cap = a.max_blocks_per_seq * kBS;
+  const int nst = args.nst;
 
-  unsigned char* lutK8 = smem;                                 // K byte-field table
-  unsigned char* lutV8 = lutK8 + Cfg::kKByteBytes;             // V byte-field table
-  unsigned char* lutK2 = lutV8 + Cfg::kVByteBytes;             // nibble K table
-  unsigned char* lutV2 = lutK2 + Cfg::kNibKBytes;              // nibble V table
-  unsigned char* stage_base = smem + Cfg::kLutBytes;
-  const int blk_bytes = args.k_slab_smem + args.v_slab_smem;
-  const int stage_bytes = WPH * blk_bytes;
-  BlockMeta* meta = reinterpret_cast<BlockMeta*>(stage_base + kNStages * stage_bytes);
-  int* meta_bid = reinterpret_cast<int*>(meta + kMetaRing * WPH);
-  int* scan_tmp = meta_bid + kMetaRing * WPH;  // [36]
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t t_base = smem_base + (uint32_t)args.t_off;
+  if (Cfg::kHasT && (t_base & 0xFFFFu) != 0u) {  // layout computed for another shared window
+    if (tid == 0 && a.status) atomicMax(a.status, (int32_t)kUnsupported);
+    return;
+  }
+  unsigned char* lutT = smem + args.t_off;
+  unsigned char* lutL = smem + kOffL;
+  unsigned char* lutK2 = smem + kOffK2;
+  unsigned char* lutV2 = smem + kOffV2;
+  BlockMeta* meta = reinterpret_cast<BlockMeta*>(smem + kOffMeta);
+  int* scan_tmp = reinterpret_cast<int*>(smem + kOffScan);
+  auto bar_full = [&](int i) -> uint32_t { return smem_base + kOffBar + 8u * i; };
+  auto bar_empty = [&](int i) -> uint32_t { return smem_base + kOffBar + 8u * (kMaxStages + i); };
+  auto buf_off = [&](int slot, int u) -> int {
+    const int idx = slot * WPH + u;
+    return idx < args.n_lo ? args.buf_lo + idx * args.buf_bytes : args.buf_hi + (idx - args.n_lo) * args.buf_bytes;
+  };
 
-  // ---- tables: K (hi, lo) pairs, V fp16(alpha c) pairs -----------------------------
+  // ---- tables: T (K hi | V pairs), L (K lo pairs), nibble tables -------------------
   if (KB == 4) {
     for (int i = tid; i < 256 * 32; i += nthreads) {
       const int f = i >> 5, copy = i & 31;
@@ -180,8 +246,8 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       split_half(__ldg(a.k_centroids + (f & 15)) * args.k_alpha, ha, la);
       split_half(__ldg(a.k_centroids + (f >> 4)) * args.k_alpha, hb, lb);
       __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
-      *reinterpret_cast<uint32_t*>(lutK8 + f * 256 + copy * 4) = *reinterpret_cast<uint32_t*>(&hi2);
-      *reinterpret_cast<uint32_t*>(lutK8 + f * 256 + 128 + copy * 4) = *reinterpret_cast<uint32_t*>(&lo2);
+      *reinterpret_cast<uint32_t*>(lutT + f * 256 + copy * 4) = *reinterpret_cast<uint32_t*>(&hi2);
+      if (copy == 0) *reinterpret_cast<uint32_t*>(lutL + f * 4) = *reinterpret_cast<uint32_t*>(&lo2);
     }
   } else {
     for (int f = tid; f < 16; f += nthreads) {
@@ -200,7 +266,7 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       const int f = i >> 5, copy = i & 31;
       const float ca = __ldg(a.v_centroids + (f & 15)) * args.v_alpha;
       const float cb = __ldg(a.v_centroids + (f >> 4)) * args.v_alpha;
-      *reinterpret_cast<uint32_t*>(lutV8 + f * 128 + copy * 4) = pack_half2(ca, cb);
+      *reinterpret_cast<uint32_t*>(lutT + f * 256 + 128 + copy * 4) = pack_half2(ca, cb);
     }
   } else {
     for (int f = tid; f < 16; f += nthreads) {
@@ -208,6 +274,13 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       const float cb = __ldg(a.v_centroids + (f >> 2)) * args.v_alpha;
       *reinterpret_cast<uint32_t*>(lutV2 + f * 4) = pack_half2(ca, cb);
     }
+  }
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), (uint32_t)ncons);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
 
   // ---- flat block list: N, this CTA's range, its first and last sequence ------------
@@ -228,7 +301,7 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   if (lane == 0) scan_tmp[warp] = local;
   __syncthreads();
   long long N = 0;
-  for (int w = 0; w < nthreads / 32; ++w) N += scan_tmp[w];
+  for (int w = 0; w < nwarps; ++w) N += scan_tmp[w];
   const long long g_lo = N * cta / C, g_hi = N * (cta + 1) / C;
   __syncthreads();
   if (tid == 0) {
@@ -250,7 +323,7 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     if (lane == 31) scan_tmp[warp] = incl;
     __syncthreads();
     int wbase = 0, total = 0;
-    for (int w = 0; w < nthreads / 32; ++w) {
+    for (int w = 0; w < nwarps; ++w) {
       if (w < warp) wbase += scan_tmp[w];
       total += scan_tmp[w];
     }
@@ -266,12 +339,12 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     carry += total;
   }
   if (cta == 0 && tid == 0) args.prefix[B] = carry;
-  __syncthreads();
-  if (g_lo >= g_hi) return;  // nothing to do (uniform)
+  __syncthreads();  // also: tables written, barriers initialised
+  if (g_lo >= g_hi) return;  // nothing to do (uniform; no copy was issued)
   const int b_first = scan_tmp[32], b_last = scan_tmp[33], j_first = scan_tmp[34];
   const int nstages = (int)((g_hi - g_lo + WPH - 1) / WPH);
 
-  // ---- block metadata: lane u < WPH of warp 0 owns blocks g_lo + WPH*st + u ----------
+  // ---- producer state: block cursor of lane u < WPH, blocks g_lo + WPH*st + u ---------
   int cb = b_first, cj = j_first, cnb = nblocks_of(b_first);
   long long cg = g_lo;
   auto cursor_advance = [&](int steps) {
@@ -283,12 +356,13 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       cnb = nblocks_of(cb);
     }
   };
-  if (warp == 0 && lane < WPH) cursor_advance(lane);
-  // Metadata of one stage is loaded (global reads in flight) one pipeline step before it
-  // is stored to shared memory, so warp 0 does not wait on those reads at a barrier.
+  const bool producer = warp == ncons;
+  if (producer && lane < WPH) cursor_advance(lane);
+  // The metadata of a stage is loaded (global reads in flight) one stage before it is
+  // stored, so the producer does not wait on those reads when it issues the copies.
   BlockMeta pend_m{0, 0, 0, 0};
   int pend_len = 0, pend_bid = -1;
-  auto meta_load = [&]() {  // warp 0, lanes < WPH: the next stage of this lane's cursor
+  auto meta_load = [&]() {  // producer lanes < WPH: the next stage of this lane's cursor
     pend_m = BlockMeta{0, 0, 0, 0};
     pend_bid = -1;
     pend_len = 0;
@@ -301,7 +375,8 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       cursor_advance(WPH);
     }
   };
-  auto meta_store = [&](int st) {
+  // Stores the pending metadata into ring slot `slot`; returns the block id to copy (-1: none).
+  auto meta_store = [&](int slot) -> int {
     BlockMeta m = pend_m;
     int bid = -1;
     if (m.ntok) {
@@ -311,59 +386,54 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
       if (!m.valid && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
       bid = m.valid ? pend_bid : -1;
     }
-    meta[(st % kMetaRing) * WPH + lane] = m;
-    meta_bid[(st % kMetaRing) * WPH + lane] = bid;
+    meta[slot * WPH + lane] = m;
+    return bid;
   };
 
-  // ---- copies: 16-byte cp.async of whole K / V slabs, per-token padding in smem -------
-  const bool k_padded = (H * Cfg::kRBK) % 16 == 0;
-  const bool v_padded = (H * Cfg::kRBV) % 16 == 0;
-  const int k_slab = kBS * H * Cfg::kRBK, v_slab = kBS * H * Cfg::kRBV;
-  const int kc = k_slab / 16, vc = v_slab / 16;
-  const int kcr = k_padded ? H * Cfg::kRBK / 16 : kc;  // chunks per token row
-  const int vcr = v_padded ? H * Cfg::kRBV / 16 : vc;
-  const int kts_pad = k_padded ? args.k_tok_stride : 0;
-  const int vts_pad = v_padded ? args.v_tok_stride : 0;
-  // per-thread start (token, column) and per-step increments, no division in the loop
-  const int k_t0 = tid / kcr, k_c0 = tid - k_t0 * kcr, k_dt = nthreads / kcr, k_dc = nthreads - k_dt * kcr;
-  const int v_t0 = tid / vcr, v_c0 = tid - v_t0 * vcr, v_dt = nthreads / vcr, v_dc = nthreads - v_dt * vcr;
-
-  auto issue_stage = [&](int st) {
-    unsigned char* sb = stage_base + (st % kNStages) * stage_bytes;
+  // ---- copies -------------------------------------------------------------------------
+  const int kraw = H * Cfg::kRBK, vraw = H * Cfg::kRBV;
+  const int k_slab = kBS * kraw, v_slab = kBS * vraw;
+  const uint32_t blk_tx = (uint32_t)(k_slab + v_slab);
+  // Producer step (all lanes of the producer): metadata of the next stage into ring slot `slot`, then
+  // the copies of its valid blocks on full[slot].  The caller has made sure the slot's
+  // buffers are free.
+  auto produce = [&](int slot) {
+    int bid = -1;
+    if (lane < WPH) {
+      bid = meta_store(slot);
+      meta_load();
+    }
+    __syncwarp();
+    int bids[WPH];
+    uint32_t tx = 0;
 #pragma unroll
     for (int u = 0; u < WPH; ++u) {
-      const int bid = meta_bid[(st % kMetaRing) * WPH + u];
-      if (bid < 0) continue;
-      const unsigned char* ksrc = a.k_pages + (int64_t)bid * k_slab;
-      const unsigned char* vsrc = a.v_pages + (int64_t)bid * v_slab;
-      const uint32_t kdst = smem_u32(sb + u * blk_bytes);
-      const uint32_t vdst = kdst + args.k_slab_smem;
-      int t = k_t0, col = k_c0;
-      for (int c = tid; c < kc; c += nthreads) {
-        cp_async16(kdst + t * kts_pad + col * 16, ksrc + c * 16);
-        t += k_dt;
-        col += k_dc;
-        if (col >= kcr) {
-          col -= kcr;
-          ++t;
-        }
-      }
-      t = v_t0;
-      col = v_c0;
-      for (int c = tid; c < vc; c += nthreads) {
-        cp_async16(vdst + t * vts_pad + col * 16, vsrc + c * 16);
-        t += v_dt;
-        col += v_dc;
-        if (col >= vcr) {
-          col -= vcr;
-          ++t;
-        }
+      bids[u] = __shfl_sync(kFullMask, bid, u);
+      if (bids[u] >= 0) tx += blk_tx;
+    }
+    if (lane == 0) mbar_arrive_expect_tx(bar_full(slot), tx);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < WPH; ++u) {
+      if (bids[u] < 0) continue;
+      const unsigned char* ksrc = a.k_pages + (int64_t)bids[u] * k_slab;
+      const unsigned char* vsrc = a.v_pages + (int64_t)bids[u] * v_slab;
+      const uint32_t kdst = smem_base + (uint32_t)buf_off(slot, u);
+      const uint32_t vdst = kdst + (uint32_t)args.k_slab_smem;
+      if (lane < 16) {
+        if (args.k_row_copy)
+          bulk_g2s(kdst + lane * args.k_tok_stride, ksrc + lane * kraw, (uint32_t)kraw, bar_full(slot));
+        else if (lane == 0)
+          bulk_g2s(kdst, ksrc, (uint32_t)k_slab, bar_full(slot));
+      } else {
+        const int t = lane - 16;
+        if (args.v_row_copy)
+          bulk_g2s(vdst + t * args.v_tok_stride, vsrc + t * vraw, (uint32_t)vraw, bar_full(slot));
+        else if (t == 0)
+          bulk_g2s(vdst, vsrc, (uint32_t)v_slab, bar_full(slot));
       }
     }
-    cp_async_commit();
   };
-
-  __syncthreads();  // tables ready
 
   // ---- consumer state ----------------------------------------------------------------
   const int h = warp % H;
@@ -372,22 +442,25 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kLog2eTc / sqrtf((float)D);
   const int kts = args.k_tok_stride, vts = args.v_tok_stride;
-  const uint32_t k_lane_off = lane * 4;  // K copy inside a 256-byte entry
-  const uint32_t v_lane_off = lane * 8;  // V copy (offset halved after the PRMT: 128-byte entries)
+  const uint32_t t_lane = t_base | (uint32_t)(lane * 4);  // T base (bits 16-31) | lane copy
   // value-B selectors: the P value goes to the low half when (r & 1) == 0, else the high half
   const int hsel = (r >> 1) & 1;
   const uint32_t sel_b = (r & 1) ? (0x0044u | ((2u * hsel) << 8) | ((2u * hsel + 1u) << 12))
                                  : ((2u * hsel) | ((2u * hsel + 1u) << 4) | 0x4400u);
 
-  // table lookups for field e of word w: K (hi, lo) fp16 pairs, V one fp16 pair
-  auto k_offset = [&](uint32_t w, int e) -> uint32_t {
-    if (KB == 4) return __byte_perm(w, k_lane_off, 0x7604u | ((uint32_t)e << 4));
-    return ((w >> (4 * e)) & 15u) << 3;
+  // Table lookups for field e of word w.  4-bit fields: one PRMT places byte e of w at
+  // bits 8-15 of (T base | lane * 4), the absolute address of this lane's copy.
+  auto t_addr = [&](uint32_t w, int e) -> uint32_t { return __byte_perm(w, t_lane, 0x7604u | ((uint32_t)e << 4)); };
+  auto k_hi = [&](uint32_t w, int e) -> uint32_t {
+    if (KB == 4) return lds32(t_addr(w, e));
+    return ld32(lutK2 + (((w >> (4 * e)) & 15u) << 3));
   };
-  auto k_hi = [&](uint32_t off) -> uint32_t { return ld32((KB == 4 ? lutK8 : lutK2) + off); };
-  auto k_lo = [&](uint32_t off) -> uint32_t { return ld32((KB == 4 ? lutK8 : lutK2) + off + (KB == 4 ? 128 : 4)); };
+  auto k_lo = [&](uint32_t w, int e) -> uint32_t {
+    if (KB == 4) return ld32(lutL + (((w >> (8 * e)) & 255u) << 2));
+    return ld32(lutK2 + (((w >> (4 * e)) & 15u) << 3) + 4);
+  };
   auto v_lookup = [&](uint32_t w, int e) -> uint32_t {
-    if (VB == 4) return ld32(lutV8 + (__byte_perm(w, v_lane_off, 0x7604u | ((uint32_t)e << 4)) >> 1));
+    if (VB == 4) return lds32_off128(t_addr(w, e));
     return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 2));
   };
 
@@ -416,8 +489,8 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
   auto load_query = [&](int b) {
     constexpr int E = D / 32;
     float qr[G][E];
-#pragma unroll
     qnorm_max = 0.f;
+#pragma unroll
     for (int g = 0; g < G; ++g) {
       const int64_t base = ((int64_t)b * a.num_q_heads + (int64_t)h * G + g) * D + lane * E;
 #pragma unroll
@@ -521,40 +594,10 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     load_query(b);
   };
 
-  // ---- main pipeline -----------------------------------------------------------------
-  if (warp == 0 && lane < WPH) {
-    for (int st = 0; st < kNStages && st < nstages; ++st) {
-      meta_load();
-      meta_store(st);
-    }
-    meta_load();  // stage kNStages, stored in the first iteration
-  }
-  __syncthreads();
-  for (int st = 0; st < kNStages - 1; ++st) {
-    if (st < nstages) issue_stage(st);
-    else cp_async_commit();
-  }
-
-  for (int st = 0; st < nstages; ++st) {
-    cp_async_wait<kNStages - 2>();
-    __syncthreads();
-    if (st + kNStages - 1 < nstages) issue_stage(st + kNStages - 1);
-    else cp_async_commit();
-    if (warp == 0 && lane < WPH && st + kNStages < nstages) {
-      meta_store(st + kNStages);
-      meta_load();
-    }
-
-    const int buf = st % kNStages;
-    const BlockMeta m = meta[(st % kMetaRing) * WPH + slot_u];
-    if (m.ntok == 0) continue;
-    if (m.b != cur_b) enter_sequence(m.b);
-    if (!m.valid) continue;
-
-    const unsigned char* kblk = stage_base + buf * stage_bytes + slot_u * blk_bytes;
-    const unsigned char* vblk = kblk + args.k_slab_smem;
+  // One 16-token tile of this warp's kv head: scores, online softmax, values.
+  auto tile = [&](const unsigned char* kblk, int ntok) {
     const unsigned char* kbase = kblk + h * Cfg::kRBK;
-    const unsigned char* vbase = vblk + h * Cfg::kRBV;
+    const unsigned char* vbase = kblk + args.k_slab_smem + h * Cfg::kRBV;
 
     // --- scores S[tok][q head] -------------------------------------------------------
     const float kn0 = __uint_as_float(ld32(kbase + r * kts + Cfg::kWK * 4));
@@ -564,14 +607,13 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     // Precision switch: a tile whose largest |score| bound nu_k * ||q|| stays within
     // kFastScoreBound takes the fp16-hi key path (rounding error ~1e-4 relative after the
     // alpha scaling); other tiles (large-norm rows) add the fp16-lo key part as well.
-    float nmax = fmaxf(r < m.ntok ? fabsf(kn0) : 0.f, r + 8 < m.ntok ? fabsf(kn1) : 0.f);
-    nmax = fmaxf(nmax, __shfl_xor_sync(kFullMask, nmax, 4));
-    nmax = fmaxf(nmax, __shfl_xor_sync(kFullMask, nmax, 8));
-    nmax = fmaxf(nmax, __shfl_xor_sync(kFullMask, nmax, 16));
-    const bool exact = __any_sync(kFullMask, nmax * qnorm_max > kFastScoreBound);
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
-    // G = 4: columns 0-3 get key * q_hi, 4-7 key * q_lo;  G = 8: separate q_lo chain
+    // Rows past the sequence end hold stale bytes: at worst they send a tile down the
+    // exact path, which is correct for any tile.
+    const bool exact = __any_sync(kFullMask, fmaxf(fabsf(kn0), fabsf(kn1)) * qnorm_max > kFastScoreBound);
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
     if (!exact) {
+      // G = 4: columns 0-3 get key_hi * q_hi, 4-7 key_hi * q_lo; G = 8: a q_lo chain
+      float sacc1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
         const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
@@ -579,13 +621,19 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
 #pragma unroll
         for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
           const int s = (jw * Cfg::kPWK + e2) >> 1;
-          const uint32_t h00 = k_hi(k_offset(w0, e2)), h10 = k_hi(k_offset(w1, e2));
-          const uint32_t h01 = k_hi(k_offset(w0, e2 + 1)), h11 = k_hi(k_offset(w1, e2 + 1));
+          const uint32_t h00 = k_hi(w0, e2), h10 = k_hi(w1, e2);
+          const uint32_t h01 = k_hi(w0, e2 + 1), h11 = k_hi(w1, e2 + 1);
           mma16816(sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
           if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
         }
       }
+      if (G == 8) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e];
+      }
     } else {
+      // adds key_lo * q_hi (G = 4: key_lo * [q_hi | q_lo])
+      float sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
         const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
@@ -593,29 +641,27 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
 #pragma unroll
         for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
           const int s = (jw * Cfg::kPWK + e2) >> 1;
-          const uint32_t o00 = k_offset(w0, e2), o10 = k_offset(w1, e2);
-          const uint32_t o01 = k_offset(w0, e2 + 1), o11 = k_offset(w1, e2 + 1);
-          const uint32_t h00 = k_hi(o00), h10 = k_hi(o10), h01 = k_hi(o01), h11 = k_hi(o11);
-          const uint32_t l00 = k_lo(o00), l10 = k_lo(o10), l01 = k_lo(o01), l11 = k_lo(o11);
+          const uint32_t h00 = k_hi(w0, e2), h10 = k_hi(w1, e2), h01 = k_hi(w0, e2 + 1), h11 = k_hi(w1, e2 + 1);
+          const uint32_t l00 = k_lo(w0, e2), l10 = k_lo(w1, e2), l01 = k_lo(w0, e2 + 1), l11 = k_lo(w1, e2 + 1);
           mma16816(sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
           if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
           mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
         }
       }
-    }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e] + sacc2[e];
+      for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e] + sacc2[e];
+    }
     if (G == 4) {
       // fold the q_lo columns (lanes c = 2, 3) onto the q_hi columns (lanes c = 0, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(kFullMask, sacc[e], 2);
     }
     const float kn0s = kn0 * inv_alpha_k, kn1s = kn1 * inv_alpha_k;
-    float sc[4];
-    sc[0] = r < m.ntok ? sacc[0] * kn0s : -INFINITY;
-    sc[1] = r < m.ntok ? sacc[1] * kn0s : -INFINITY;
-    sc[2] = r + 8 < m.ntok ? sacc[2] * kn1s : -INFINITY;
-    sc[3] = r + 8 < m.ntok ? sacc[3] * kn1s : -INFINITY;
+    float sc[4] = {sacc[0] * kn0s, sacc[1] * kn0s, sacc[2] * kn1s, sacc[3] * kn1s};
+    if (ntok < kBS) {  // last block of a sequence: mask the rows past its end
+      if (r >= ntok) sc[0] = sc[1] = -INFINITY;
+      if (r + 8 >= ntok) sc[2] = sc[3] = -INFINITY;
+    }
 
     // --- online softmax (q heads 2c, 2c+1 on this lane); the running max is only moved
     // when the tile max passes it by more than kRescaleSlack, so p <= 2^slack.
@@ -679,6 +725,43 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
         }
       }
     }
+  };
+
+  // ---- main pipeline -----------------------------------------------------------------
+  // Stage st lives in ring slot st % nst; full[slot] completes when its copies landed,
+  // empty[slot] when every consumer warp is done with it.
+  if (producer) {
+    int S = 0;
+    for (; S < nstages; ++S) {
+      const int ps = S % nst;
+      if (S >= nst && !mbar_wait(bar_empty(ps), (uint32_t)(((S / nst) - 1) & 1))) break;
+      if (S == 0 && lane < WPH) meta_load();
+      produce(ps);
+    }
+    if (S < nstages && lane == 0 && a.status) atomicMax(a.status, (int32_t)kTimeout);
+    // let this CTA's copies land before the producer leaves (the consumers normally
+    // have already waited for all of them)
+    for (int s2 = (S > nst ? S - nst : 0); s2 < S; ++s2) mbar_wait(bar_full(s2 % nst), (uint32_t)((s2 / nst) & 1));
+    return;
+  }
+  int slot = 0;
+  uint32_t par = 0;
+  for (int st = 0; st < nstages; ++st) {
+    if (!mbar_wait(bar_full(slot), par)) {
+      if (lane == 0 && a.status) atomicMax(a.status, (int32_t)kTimeout);
+      return;
+    }
+    const BlockMeta m = meta[slot * WPH + slot_u];
+    if (m.ntok != 0) {
+      if (m.b != cur_b) enter_sequence(m.b);
+      if (m.valid) tile(smem + buf_off(slot, slot_u), m.ntok);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty(slot));
+    if (++slot == nst) {
+      slot = 0;
+      par ^= 1u;
+    }
   }
   // close the last sequence and any later non-empty ones this CTA owns
   if (cur_b < 0) {
@@ -689,7 +772,6 @@ __global__ void __launch_bounds__(32 * 8 * WPH, 1) decode_tc_kernel(TcArgs args)
     for (int x = cur_b + 1; x <= b_last; ++x)
       if (nblocks_of(x) > 0) flush(x, true);
   }
-  cp_async_wait<0>();
 }
 
 // One warp per (sequence, q head): merge the partials of the CTAs that touched the
@@ -748,33 +830,63 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   t.num_ctas = p.num_splits;
   const int H = a.num_kv_heads;
   const int kraw = H * Cfg::kRBK, vraw = H * Cfg::kRBV;
-  // K: pad each token to a stride of 4*odd words mod 32 (conflict-free fragment reads)
-  int kpad = 0, vpad = 0;
-  if (kraw % 16 == 0)
-    for (int pad = 0; pad < 8; ++pad)
-      if ((((kraw + 16 * pad) / 4) % 32) % 8 == 4) { kpad = 16 * pad; break; }
-  if (vraw % 16 == 0)
-    for (int pad = 0; pad < 8; ++pad) {
-      const int w = ((vraw + 16 * pad) / 4) % 32;
-      if (w == 8 || w == 24) { vpad = 16 * pad; break; }
-    }
-  t.k_tok_stride = (kraw % 16 == 0) ? kraw + kpad : kraw;
-  t.v_tok_stride = (vraw % 16 == 0) ? vraw + vpad : vraw;
+  // Each K and V slab arrives as one bulk copy, unpadded.  (Per-token row copies would
+  // allow padded, conflict-free strides, but many small bulk copies do not keep enough
+  // bytes in flight; for 8 heads of 128 4-bit coordinates the unpadded K stride costs a
+  // 2-way conflict on the 8 index-word loads of a tile, the V stride none.)
+  t.k_row_copy = 0;
+  t.v_row_copy = 0;
+  t.k_tok_stride = kraw;
+  t.v_tok_stride = vraw;
   t.k_slab_smem = (kBS * t.k_tok_stride + 15) / 16 * 16;
   t.v_slab_smem = (kBS * t.v_tok_stride + 15) / 16 * 16;
   t.v_alpha = a.v_alpha > 0.f ? a.v_alpha : 1.0f;
   t.k_alpha = a.k_alpha > 0.f ? a.k_alpha : 1.0f;
+
+  // Shared-memory layout: [misc | buffers ... | T (64 KB, at a 64 KB aligned shared
+  // address) | buffers ...].  Dynamic shared memory starts right after the per-block
+  // reserved bytes in the shared window (the kernel checks the T alignment it gets).
+  int dev = 0, reserved = 0, max_dyn = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&max_dyn, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  t.buf_bytes = (t.k_slab_smem + t.v_slab_smem + 127) / 128 * 128;
+  int total_bufs = 0;
+  t.buf_lo = kMiscBytes;
+  if (Cfg::kHasT) {
+    int t_off = (65536 - reserved % 65536) % 65536;
+    while (t_off < kMiscBytes) t_off += 65536;
+    t.t_off = t_off;
+    t.n_lo = (t_off - kMiscBytes) / t.buf_bytes;
+    t.buf_hi = t_off + Cfg::kTBytes;
+    total_bufs = t.n_lo + std::max(0, (max_dyn - t.buf_hi) / t.buf_bytes);
+  } else {
+    t.t_off = 0;
+    t.n_lo = (max_dyn - kMiscBytes) / t.buf_bytes;
+    t.buf_hi = 0;
+    total_bufs = t.n_lo;
+  }
+  t.nst = std::min(kMaxStages, total_bufs / WPH);
+  if (t.nst < 2) return cudaErrorInvalidConfiguration;
+  const int nbuf = t.nst * WPH;
+  size_t smem = 0;
+  if (Cfg::kHasT) {
+    smem = (size_t)t.t_off + Cfg::kTBytes;
+    if (nbuf > t.n_lo) smem = (size_t)t.buf_hi + (size_t)(nbuf - t.n_lo) * t.buf_bytes;
+  } else {
+    smem = (size_t)kMiscBytes + (size_t)nbuf * t.buf_bytes;
+  }
+
   const int B = a.batch, Hq = a.num_q_heads;
   const int64_t slots = (int64_t)WPH * (p.num_splits + B);
   t.part_acc = static_cast<float*>(a.workspace);
   t.part_ml = t.part_acc + slots * Hq * D;
   t.prefix = reinterpret_cast<int*>(t.part_ml + slots * Hq * 2);
-  const size_t smem = Cfg::kLutBytes + (size_t)kNStages * WPH * (t.k_slab_smem + t.v_slab_smem) +
-                      kMetaRing * WPH * (sizeof(BlockMeta) + sizeof(int)) + 36 * sizeof(int);
   auto kern = decode_tc_kernel<D, KB, VB, G, WPH>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<p.num_splits, 32 * H * WPH, smem, stream>>>(t);
+  kern<<<p.num_splits, 32 * (H * WPH + 1), smem, stream>>>(t);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int rows = B * Hq;

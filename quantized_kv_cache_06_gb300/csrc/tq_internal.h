@@ -14,6 +14,7 @@ enum : int32_t {
   kUnsupported = 2,
   kSlotOutOfRange = 3,
   kBlockOutOfRange = 4,
+  kTimeout = 6,
 };
 
 enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
