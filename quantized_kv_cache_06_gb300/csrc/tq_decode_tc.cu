@@ -441,6 +441,7 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
   const int r = lane >> 2, c = lane & 3;
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kLog2eTc / sqrtf((float)D);
+  const float inv_alpha_k = 1.0f / args.k_alpha;
   const int kts = args.k_tok_stride, vts = args.v_tok_stride;
   const uint32_t t_lane = t_base | (uint32_t)(lane * 4);  // T base (bits 16-31) | lane copy
   // value-B selectors: the P value goes to the low half when (r & 1) == 0, else the high half
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
   uint32_t bq[kQSets][Cfg::kKSteps][2];
   float qnorm_max = 0.f;  // max over this warp's heads of ||rotated query|| (log2 units)
   float o_acc[Cfg::kNT][Cfg::kMTiles][4];
-  float m_run[2], l_run[2];
+  float m_run[2], l_run[2], m_thr[2];  // running max, sum, and max + kRescaleSlack per head
   int cur_b = -1;
 
   auto reset_state = [&]() {
@@ -481,7 +482,7 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
       for (int i = 0; i < Cfg::kMTiles; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o_acc[nt][i][e] = 0.f;
-    m_run[0] = m_run[1] = -INFINITY;
+    m_run[0] = m_run[1] = m_thr[0] = m_thr[1] = -INFINITY;
     l_run[0] = l_run[1] = 0.f;
   };
 
@@ -501,6 +502,7 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
       for (int i = 0; i < E; ++i) {
         qr[g][i] *= qmul;
         ss = fmaf(qr[g][i], qr[g][i], ss);
+        qr[g][i] *= inv_alpha_k;  // the K tables hold alpha * c
       }
       qnorm_max = fmaxf(qnorm_max, sqrtf(warp_sum(ss)));
     }
@@ -539,7 +541,6 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
   };
 
   const float inv_alpha = 1.0f / args.v_alpha;
-  const float inv_alpha_k = 1.0f / args.k_alpha;
   // Writes this warp's partial for sequence b (empty when `empty`).
   auto flush = [&](int b, bool empty) {
     const int64_t slot = (int64_t)WPH * (cta + b) + slot_u;
@@ -612,7 +613,8 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
     const bool exact = __any_sync(kFullMask, fmaxf(fabsf(kn0), fabsf(kn1)) * qnorm_max > kFastScoreBound);
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
     if (!exact) {
-      // G = 4: columns 0-3 get key_hi * q_hi, 4-7 key_hi * q_lo; G = 8: a q_lo chain
+      // G = 4: columns 0-3 get key_hi * q_hi, 4-7 key_hi * q_lo (two chains: even and odd
+      // k-steps); G = 8: a q_lo chain
       float sacc1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
@@ -623,14 +625,16 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
           const int s = (jw * Cfg::kPWK + e2) >> 1;
           const uint32_t h00 = k_hi(w0, e2), h10 = k_hi(w1, e2);
           const uint32_t h01 = k_hi(w0, e2 + 1), h11 = k_hi(w1, e2 + 1);
-          mma16816(sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
-          if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+          if (G == 8) {
+            mma16816(sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+            mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+          } else {
+            mma16816((s & 1) ? sacc1 : sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+          }
         }
       }
-      if (G == 8) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e];
-      }
+      for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e];
     } else {
       // adds key_lo * q_hi (G = 4: key_lo * [q_hi | q_lo])
       float sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -656,31 +660,30 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(kFullMask, sacc[e], 2);
     }
-    const float kn0s = kn0 * inv_alpha_k, kn1s = kn1 * inv_alpha_k;
-    float sc[4] = {sacc[0] * kn0s, sacc[1] * kn0s, sacc[2] * kn1s, sacc[3] * kn1s};
+    float sc[4] = {sacc[0] * kn0, sacc[1] * kn0, sacc[2] * kn1, sacc[3] * kn1};
     if (ntok < kBS) {  // last block of a sequence: mask the rows past its end
       if (r >= ntok) sc[0] = sc[1] = -INFINITY;
       if (r + 8 >= ntok) sc[2] = sc[3] = -INFINITY;
     }
 
-    // --- online softmax (q heads 2c, 2c+1 on this lane); the running max is only moved
-    // when the tile max passes it by more than kRescaleSlack, so p <= 2^slack.
-    float corr[2], pv[4];
+    // --- online softmax (q heads 2c, 2c+1 on this lane).  The running max only moves
+    // when a score passes it by more than kRescaleSlack, so p = 2^(s - m) <= 2^slack.
+    // Most tiles move no max: one compare per score and a vote replace the reduction.
+    const bool jump = fmaxf(sc[0], sc[2]) > m_thr[0] || fmaxf(sc[1], sc[3]) > m_thr[1];
+    if (__any_sync(kFullMask, jump)) {
+      float corr[2];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float mt = fmaxf(sc[e], sc[2 + e]);
-      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 4));
-      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
-      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
-      const float mn = mt > m_run[e] + kRescaleSlack ? mt : m_run[e];
-      corr[e] = fast_exp2(m_run[e] - mn);
-      const float p0 = fast_exp2(sc[e] - mn), p1 = fast_exp2(sc[2 + e] - mn);
-      l_run[e] = l_run[e] * corr[e] + p0 + p1;
-      m_run[e] = mn;
-      pv[e] = p0 * vn0;
-      pv[2 + e] = p1 * vn1;
-    }
-    if (__any_sync(kFullMask, corr[0] != 1.f || corr[1] != 1.f)) {
+      for (int e = 0; e < 2; ++e) {
+        float mt = fmaxf(sc[e], sc[2 + e]);
+        mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
+        const float mn = mt > m_thr[e] ? mt : m_run[e];
+        corr[e] = fast_exp2(m_run[e] - mn);
+        l_run[e] *= corr[e];
+        m_run[e] = mn;
+        m_thr[e] = mn + kRescaleSlack;
+      }
 #pragma unroll
       for (int nt = 0; nt < Cfg::kNT; ++nt) {  // value layout holds q head c + 4 nt
         const int g = c + 4 * nt;
@@ -693,6 +696,14 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
 #pragma unroll
           for (int e = 0; e < 4; ++e) o_acc[nt][i][e] *= cg;
       }
+    }
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float p0 = fast_exp2(sc[e] - m_run[e]), p1 = fast_exp2(sc[2 + e] - m_run[e]);
+      l_run[e] += p0 + p1;
+      pv[e] = p0 * vn0;
+      pv[2 + e] = p1 * vn1;
     }
     const uint32_t p01 = pack_half2(pv[0], pv[1]);  // token r:   heads 2c, 2c+1
     const uint32_t p23 = pack_half2(pv[2], pv[3]);  // token r+8: heads 2c, 2c+1

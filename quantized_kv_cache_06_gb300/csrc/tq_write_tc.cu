@@ -159,6 +159,11 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
   __syncthreads();
   if (!grid_ok || *a.status != kOk) return;  // bad codebook or a slot failed validation: write nothing
   const float q_a = grid_a, q_b = grid_b;  // grid coordinate g = u * q_a + q_b, cell = floor(g)
+  // The loop works in g' = g - 1/2 (exact: q_b is a small multiple of 1/8): adding
+  // 1.5 * 2^23 to g' leaves round(g') in the low mantissa bits, which is floor(g) but
+  // for g within rounding of an integer, where it may be floor(g) - 1 -- harmless, as no
+  // decision point lies within 1/64 cell of a cell edge.  g >= phi >= 1/4 keeps it >= 0.
+  const float q_bs = q_b - 0.5f;
   for (int i = threadIdx.x; i < kQCells * kQCopies; i += blockDim.x) {
     // cell [cell, cell + 1) in grid units: decision points below its start, first one at or above
     const int cell = i / kQCopies;
@@ -171,7 +176,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
     }
     QCell q;
     q.lo = below;
-    q.point = point;
+    q.point = point - 0.5f;  // in g' (exact, and +inf stays +inf)
     qtab[i] = q;
   }
   __syncthreads();
@@ -193,7 +198,10 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
       }
     }
   }
-  const unsigned char* qlane = reinterpret_cast<const unsigned char*>(qtab) + (lane & 15) * sizeof(QCell);
+  // shared address of cell n, this lane's copy: bits(g' + 1.5 * 2^23) * 128 + q_addr_bias
+  constexpr uint32_t kMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
+  const uint32_t q_addr_bias =
+      smem_addr(qtab) + (uint32_t)((lane & 15) * sizeof(QCell)) - kMagicBits * (uint32_t)(kQCopies * sizeof(QCell));
 
   const int64_t num_rows = a.num_tokens * H;
   const int64_t num_tiles = (num_rows + 15) / 16;
@@ -204,22 +212,33 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
   // 16-byte chunks XOR-swizzled by row so that ldmatrix reads are conflict free)
   auto load_tile = [&](int64_t tile, int buf) {
     if (tile < num_tiles) {
-      const unsigned char* src = reinterpret_cast<const unsigned char*>(raw) + tile * TILE_BYTES;
-      const int64_t bytes_left = (num_rows - tile * 16) * ROWB;
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(raw) + tile * TILE_BYTES + lane * 16;
       const uint32_t dst0 = smem_addr(raw_buf + buf * TILE_BYTES);
       constexpr int CH = TILE_BYTES / 16, CPR = ROWB / 16;
+      if ((tile + 1) * 16 <= num_rows) {  // whole tile: no per-chunk checks
 #pragma unroll
-      for (int i = lane; i < CH; i += 32) {
-        const int row = i / CPR, col = i % CPR;
-        const uint32_t dst = dst0 + row * ROWB + ((col ^ (row & 7)) << 4);
-        const int64_t off = (int64_t)i * 16;
-        if (off + 16 <= bytes_left) cp_async16_w(dst, src + off);
-        else cp_async16_w_zfill(dst, src, 0);  // past the last row: zero fill, no read
+        for (int k = 0; k < CH / 32; ++k) {
+          const int i = lane + 32 * k, row = i / CPR, col = i % CPR;
+          cp_async16_w(dst0 + row * ROWB + ((col ^ (row & 7)) << 4), src + k * 512);
+        }
+      } else {
+        const int64_t bytes_left = (num_rows - tile * 16) * ROWB;
+#pragma unroll
+        for (int k = 0; k < CH / 32; ++k) {
+          const int i = lane + 32 * k, row = i / CPR, col = i % CPR;
+          const uint32_t dst = dst0 + row * ROWB + ((col ^ (row & 7)) << 4);
+          if ((int64_t)i * 16 + 16 <= bytes_left) cp_async16_w(dst, src + k * 512);
+          else cp_async16_w_zfill(dst, src - lane * 16, 0);  // past the last row: zero fill, no read
+        }
       }
     }
     cp_commit_w();
   };
 
+  // chunk i of a tile belongs to token i / d, d = H * RB / 16: a reciprocal multiply,
+  // (i * ceil(2^16 / d)) >> 16, exact for i < 2^16 / d -- here i < RB <= 68 and d <= 68
+  const uint32_t cpt = (uint32_t)(H * RB / 16 > 0 ? H * RB / 16 : 1);
+  const uint32_t inv_cpt = (65536u + cpt - 1) / cpt;
   int64_t tile = (int64_t)blockIdx.x * kWWarps + warp;
   int buf = 0;
   load_tile(tile, 0);
@@ -295,30 +314,46 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
     const float nu0 = sqrtf(ss0 * (1.0f / D)), nu1 = sqrtf(ss1 * (1.0f / D));
     const float ga0 = q_a / sqrtf(ss0 + 0x1p-149f);
     const float ga1 = q_a / sqrtf(ss1 + 0x1p-149f);
+    // A NaN or infinite input (the only way to a non-finite sum) would give a NaN grid
+    // coordinate, whose bits address nothing: such rows are quantised as zero rows.
+    if (__any_sync(kFullMask, !(ss0 <= 3.402823466e38f) || !(ss1 <= 3.402823466e38f))) {
+      const bool bad0 = !(ss0 <= 3.402823466e38f), bad1 = !(ss1 <= 3.402823466e38f);
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          if (bad0) acc[j][nt][0] = acc[j][nt][1] = 0.f;
+          if (bad1) acc[j][nt][2] = acc[j][nt][3] = 0.f;
+        }
+    }
 
     // ---- quantise and pack into this warp's row buffer ------------------------------
     // the cell and the comparison both use the grid coordinate; exact for every u not
     // within a few ulp of a decision point, whichever neighbouring cell it lands in
-    auto quant = [&](float g) -> uint32_t {
-      const uint32_t cell = __float2uint_rz(g);  // 0 for g < 0 or NaN, at most 2 q_a otherwise
-      const QCell q = *reinterpret_cast<const QCell*>(qlane + cell * (kQCopies * sizeof(QCell)));
-      return (uint32_t)(q.lo + (g > q.point ? 1 : 0));
+    // g: shifted grid coordinate g'; m: g' + 1.5 * 2^23 (its bits give the cell)
+    auto quant = [&](float g, float m) -> uint32_t {
+      const uint32_t addr = __float_as_uint(m) * (uint32_t)(kQCopies * sizeof(QCell)) + q_addr_bias;
+      uint32_t lo, pt;
+      asm("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(lo), "=r"(pt) : "r"(addr));
+      return lo + (g > __uint_as_float(pt) ? 1u : 0u);
     };
+    const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {  // row r (half 0) / row r + 8 (half 1)
       const float ga = half ? ga1 : ga0;
-      const float2 gav = make_float2(ga, ga), gbv = make_float2(q_b, q_b);
+      const float2 gav = make_float2(ga, ga), gbv = make_float2(q_bs, q_bs);
       unsigned char* prow = pack_buf + (r + 8 * half) * RB;
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const float2 g = __ffma2_rn(make_float2(acc[j][nt][2 * half], acc[j][nt][2 * half + 1]), gav, gbv);
-          const uint32_t i0 = quant(g.x);
-          const uint32_t i1 = quant(g.y);
+          const float2 m = __fadd2_rn(g, magic2);
+          const uint32_t i0 = quant(g.x, m.x);
+          const uint32_t i1 = quant(g.y, m.y);
           // columns 16 j + 8 nt + 2c, +1
           if (BITS == 4) {
-            prow[8 * j + 4 * nt + c] = (unsigned char)(i0 | (i1 << 4));
+            prow[8 * j + 4 * nt + c] = (unsigned char)(i0 + (i1 << 4));
           } else {
             // 2 bits: byte 4 j + 2 nt + c/2 holds columns 16 j + 8 nt + 4 (c/2) .. +3
             const uint32_t mine = i0 | (i1 << 2);
@@ -338,7 +373,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
 #pragma unroll
       for (int k = 0; k < (CH16 + 31) / 32; ++k) {
         const int i = lane + 32 * k;
-        const int tt = min(i, CH16 - 1) * 16 / (H * RB);  // token within the tile
+        const int tt = (int)(((uint32_t)min(i, CH16 - 1) * inv_cpt) >> 16);  // token within the tile
         const int64_t slot = __shfl_sync(kFullMask, my_slot, tt);
         if (i < CH16 && slot >= 0) {
           const int off = i * 16 - tt * H * RB;
