@@ -54,6 +54,42 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def init_dist(world, local_rank, backend):
+    """One process per GPU (torchrun env); no-op for a single rank."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        else:
+            dist.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise max of `values` over all ranks (the slowest rank sets the time)."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def weak_scaling_rate(world, units_per_rank, max_seconds):
+    """Whole-job throughput: every rank processed `units_per_rank` within `max_seconds`."""
+    return world * units_per_rank / max_seconds
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -259,15 +295,12 @@ def run_gpu(args):
     from quantized_kv_cache_06_gb300.workloads import make_workload
 
     rank, world, local_rank = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    init_dist(world, local_rank, "nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     tq.lib()
 
-    w = make_workload(WORKLOAD_CFG, batch=args.batch)
+    w = make_workload(WORKLOAD_CFG, batch=args.batch, shard=rank)  # each rank its own batch
     d = w.head_dim
     signs = tq.tq_build_rotation(d, 42, dev)
     ck = tq.tq_codebook(d, w.k_bits, dev)[0]
@@ -317,8 +350,7 @@ def run_gpu(args):
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -327,28 +359,22 @@ def run_gpu(args):
         step(events[i])
     t1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     clk = clocks.stop()
     total_ms = t0.elapsed_time(t1)
     wk = [e[0].elapsed_time(e[1]) for e in events]
     wv = [e[1].elapsed_time(e[2]) for e in events]
     dec = [e[3].elapsed_time(e[4]) for e in events]
-    ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step, statistics.mean(dec)], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, dec_max = float(t[0]), float(t[1])
-    else:
-        dec_max = statistics.mean(dec)
+    ms_step, dec_max, wr_max = max_over_ranks(
+        [total_ms / args.steps, statistics.mean(dec), statistics.mean(wk) + statistics.mean(wv)], world, dev)
 
     dbytes = decode_bytes(w)
     kbytes = write_bytes(w, w.k_raw, w.slots, w.k_bits)
     vbytes = write_bytes(w, w.v_raw, w.slots, w.v_bits)
     dec_s = dec_max / 1e3
-    value = world * dbytes / dec_s / 1e9
+    value = weak_scaling_rate(world, dbytes, dec_s) / 1e9
     head_rows = 2 * w.num_tokens * w.num_kv_heads
-    write_s = (statistics.mean(wk) + statistics.mean(wv)) / 1e3
+    write_s = wr_max / 1e3
     peak, peak_kind = peaks()
     dec_gbs = dbytes / dec_s / 1e9
     wr_gbs = (kbytes + vbytes) / write_s / 1e9
@@ -364,9 +390,9 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(w, args.batch),
             "decode_us": dec_max * 1e3, "decode_gbs_per_gpu": dec_gbs, "decode_frac_of_peak": dec_gbs / peak,
-            "decode_seq_per_s": world * w.batch / dec_s,
-            "write_us_per_component": write_s / 2 * 1e6, "write_rows_per_s": world * head_rows / write_s,
-            "write_token_rows_per_s": world * 2 * w.num_tokens / write_s, "write_gbs_per_gpu": wr_gbs,
+            "decode_seq_per_s": weak_scaling_rate(world, w.batch, dec_s),
+            "write_us_per_component": write_s / 2 * 1e6, "write_rows_per_s": weak_scaling_rate(world, head_rows, write_s),
+            "write_token_rows_per_s": weak_scaling_rate(world, 2 * w.num_tokens, write_s), "write_gbs_per_gpu": wr_gbs,
             "roofline": dominant, "roofline_decode": roof_dec, "roofline_write": roof_wr,
             "gpu_launches": args.steps * 6, "clocks": clk}
 

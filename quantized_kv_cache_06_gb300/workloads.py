@@ -101,9 +101,11 @@ def _scaled_normal(rng, shape, dtype, scale=None, outlier_p=0.0, chunk=1 << 16):
     return out
 
 
-def make_workload(cfg: int, sub: int = 0, batch: int | None = None) -> Workload:
+def make_workload(cfg: int, sub: int = 0, batch: int | None = None, shard: int = 0) -> Workload:
     """Workload `cfg` (1..5); `sub` picks the sweep point of workload 3 (index into SWEEP);
-    `batch` optionally keeps only the first sequences (same per-sequence structure)."""
+    `batch` optionally keeps only the first sequences (same per-sequence structure);
+    `shard` > 0 draws another independent batch of the same shape (one per rank when the
+    batch is replicated across GPUs; shard 0 is the workload itself)."""
     if cfg == 1:
         rng = np.random.default_rng(1)
         d, h, hq, bs, nb = 128, 2, 16, 16, 32
@@ -117,24 +119,24 @@ def make_workload(cfg: int, sub: int = 0, batch: int | None = None) -> Workload:
 
     if cfg == 2:
         seq_lens = np.random.default_rng(0).integers(1, 2049, size=8).astype(np.int32)
-        rng = np.random.default_rng(2)
+        rng = np.random.default_rng(2 if shard == 0 else (2, shard))
         d, h, hq, bs, kb, vb = 128, 8, 32, 16, 4, 2
         name = "mixed K4/V2 D128 Hq32/H8 8 seqs len U[1,2048]"
     elif cfg == 3:
         kb, d = SWEEP[sub]
         vb = kb
         seq_lens = np.full(16, 4096, dtype=np.int32)
-        rng = np.random.default_rng(300 + sub)
+        rng = np.random.default_rng(300 + sub if shard == 0 else (300 + sub, shard))
         h, hq, bs = 8, 32, 16
         name = f"sweep K{kb}/V{vb} D{d} Hq32/H8 16x4096"
     elif cfg == 4:
         seq_lens = np.full(64, 8192, dtype=np.int32)
-        rng = np.random.default_rng(4)
+        rng = np.random.default_rng(4 if shard == 0 else (4, shard))
         d, h, hq, bs, kb, vb = 128, 8, 32, 16, 4, 4
         name = "decode batch K4/V4 D128 Hq32/H8 64x8192"
     elif cfg == 5:
         seq_lens = np.full(4, 131072, dtype=np.int32)
-        rng = np.random.default_rng(5)
+        rng = np.random.default_rng(5 if shard == 0 else (5, shard))
         d, h, hq, bs, kb, vb = 128, 8, 64, 16, 4, 2
         name = "long context K4/V2 D128 Hq64/H8 4x131072"
     else:
