@@ -239,7 +239,7 @@ DecodePlan plan_decode(const DecodeArgs& a, int num_sms) {
     p.kernel = 2;
     p.num_splits = num_sms;
     p.blocks_per_split = 0;
-    const size_t slots = (size_t)tc_warps_per_head(a.head_dim) * (num_sms + a.batch);
+    const size_t slots = (size_t)tc_partials_per_sequence_split() * (num_sms + a.batch);
     p.workspace_bytes = slots * a.num_q_heads * (a.head_dim + 2) * sizeof(float) + (a.batch + 1) * sizeof(int) + 16;
     return p;
   }

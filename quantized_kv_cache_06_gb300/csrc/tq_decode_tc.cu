@@ -35,10 +35,12 @@
 // Softmax: online, base 2 (log2 e folded into the query), per q head.  Rows of tokens
 // past the sequence end are masked; blocks with an out-of-range id are skipped and
 // reported through the status word.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -121,7 +123,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // D = A * B + D, m16n8k16, A row-major f16, B col-major f16, f32 accumulators.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -206,7 +208,7 @@ constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag beh
 constexpr float kFastScoreBound = 48.0f;
 
 template <int D, int KB, int VB, int G, int WPH>
-__global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs args) {
+__global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   using Cfg = TcCfg<D, KB, VB, G, WPH>;
   const DecodeArgs& a = args.a;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -238,43 +240,6 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
     return idx < args.n_lo ? args.buf_lo + idx * args.buf_bytes : args.buf_hi + (idx - args.n_lo) * args.buf_bytes;
   };
 
-  // ---- tables: T (K hi | V pairs), L (K lo pairs), nibble tables -------------------
-  if (KB == 4) {
-    for (int i = tid; i < 256 * 32; i += nthreads) {
-      const int f = i >> 5, copy = i & 31;
-      __half ha, la, hb, lb;
-      split_half(__ldg(a.k_centroids + (f & 15)) * args.k_alpha, ha, la);
-      split_half(__ldg(a.k_centroids + (f >> 4)) * args.k_alpha, hb, lb);
-      __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
-      *reinterpret_cast<uint32_t*>(lutT + f * 256 + copy * 4) = *reinterpret_cast<uint32_t*>(&hi2);
-      if (copy == 0) *reinterpret_cast<uint32_t*>(lutL + f * 4) = *reinterpret_cast<uint32_t*>(&lo2);
-    }
-  } else {
-    for (int f = tid; f < 16; f += nthreads) {
-      __half ha, la, hb, lb;
-      split_half(__ldg(a.k_centroids + (f & 3)) * args.k_alpha, ha, la);
-      split_half(__ldg(a.k_centroids + (f >> 2)) * args.k_alpha, hb, lb);
-      __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
-      uint2 v;
-      v.x = *reinterpret_cast<uint32_t*>(&hi2);
-      v.y = *reinterpret_cast<uint32_t*>(&lo2);
-      *reinterpret_cast<uint2*>(lutK2 + f * 8) = v;
-    }
-  }
-  if (VB == 4) {
-    for (int i = tid; i < 256 * 32; i += nthreads) {
-      const int f = i >> 5, copy = i & 31;
-      const float ca = __ldg(a.v_centroids + (f & 15)) * args.v_alpha;
-      const float cb = __ldg(a.v_centroids + (f >> 4)) * args.v_alpha;
-      *reinterpret_cast<uint32_t*>(lutT + f * 256 + 128 + copy * 4) = pack_half2(ca, cb);
-    }
-  } else {
-    for (int f = tid; f < 16; f += nthreads) {
-      const float ca = __ldg(a.v_centroids + (f & 3)) * args.v_alpha;
-      const float cb = __ldg(a.v_centroids + (f >> 2)) * args.v_alpha;
-      *reinterpret_cast<uint32_t*>(lutV2 + f * 4) = pack_half2(ca, cb);
-    }
-  }
   if (tid == 0) {
     for (int i = 0; i < nst; ++i) {
       mbar_init(bar_full(i), 1);
@@ -339,7 +304,7 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
     carry += total;
   }
   if (cta == 0 && tid == 0) args.prefix[B] = carry;
-  __syncthreads();  // also: tables written, barriers initialised
+  __syncthreads();  // also: barriers initialised
   if (g_lo >= g_hi) return;  // nothing to do (uniform; no copy was issued)
   const int b_first = scan_tmp[32], b_last = scan_tmp[33], j_first = scan_tmp[34];
   const int nstages = (int)((g_hi - g_lo + WPH - 1) / WPH);
@@ -436,8 +401,7 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
   };
 
   // ---- consumer state ----------------------------------------------------------------
-  const int h = warp % H;
-  const int slot_u = warp / H;
+  const int h = warp;  // consumer warp h: kv head h of every block
   const int r = lane >> 2, c = lane & 3;
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kLog2eTc / sqrtf((float)D);
@@ -491,11 +455,31 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
     constexpr int E = D / 32;
     float qr[G][E];
     qnorm_max = 0.f;
+    // all G*E loads of this lane in flight at once (one dtype branch outside the loops)
+    const int64_t base = ((int64_t)b * a.num_q_heads + (int64_t)h * G) * D + lane * E;
+    if (a.q_dtype == kF16) {
+      const __half* q16 = static_cast<const __half*>(a.q) + base;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < E; ++i) qr[g][i] = __half2float(q16[g * D + i]);
+    } else if (a.q_dtype == kBF16) {
+      const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) + base;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < E; ++i) qr[g][i] = __bfloat162float(qb[g * D + i]);
+    } else {
+      const float* qf = static_cast<const float*>(a.q) + base;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < E; ++i) qr[g][i] = __ldg(qf + g * D + i);
+    }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const int64_t base = ((int64_t)b * a.num_q_heads + (int64_t)h * G + g) * D + lane * E;
 #pragma unroll
-      for (int i = 0; i < E; ++i) qr[g][i] = load_as_f32(a.q, base + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
+      for (int i = 0; i < E; ++i) qr[g][i] *= __ldg(a.signs + lane * E + i);
       fwht_warp<E>(qr[g]);
       float ss = 0.f;
 #pragma unroll
@@ -543,7 +527,7 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
   const float inv_alpha = 1.0f / args.v_alpha;
   // Writes this warp's partial for sequence b (empty when `empty`).
   auto flush = [&](int b, bool empty) {
-    const int64_t slot = (int64_t)WPH * (cta + b) + slot_u;
+    const int64_t slot = (int64_t)cta + b;
     float lsum[2] = {l_run[0], l_run[1]};
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -595,86 +579,129 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
     load_query(b);
   };
 
-  // One 16-token tile of this warp's kv head: scores, online softmax, values.
-  auto tile = [&](const unsigned char* kblk, int ntok) {
-    const unsigned char* kbase = kblk + h * Cfg::kRBK;
-    const unsigned char* vbase = kblk + args.k_slab_smem + h * Cfg::kRBV;
-
-    // --- scores S[tok][q head] -------------------------------------------------------
-    const float kn0 = __uint_as_float(ld32(kbase + r * kts + Cfg::kWK * 4));
-    const float kn1 = __uint_as_float(ld32(kbase + (r + 8) * kts + Cfg::kWK * 4));
-    const float vn0 = __uint_as_float(ld32(vbase + r * vts + Cfg::kWV * 4));
-    const float vn1 = __uint_as_float(ld32(vbase + (r + 8) * vts + Cfg::kWV * 4));
-    // Precision switch: a tile whose largest |score| bound nu_k * ||q|| stays within
-    // kFastScoreBound takes the fp16-hi key path (rounding error ~1e-4 relative after the
-    // alpha scaling); other tiles (large-norm rows) add the fp16-lo key part as well.
-    // Rows past the sequence end hold stale bytes: at worst they send a tile down the
-    // exact path, which is correct for any tile.
-    const bool exact = __any_sync(kFullMask, fmaxf(fabsf(kn0), fabsf(kn1)) * qnorm_max > kFastScoreBound);
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+  // NTL (1 or 2) consecutive 16-token tiles of this warp's kv head in one sequence:
+  // scores, one joint online-softmax update, values.  Only the last tile may be partial
+  // (ntok_last tokens).  Two tiles give two independent lookup/MMA chains per phase.
+  auto tiles = [&](auto ntl_tag, const unsigned char* kblk0, const unsigned char* kblk1, int ntok_last) {
+    constexpr int NTL = decltype(ntl_tag)::value;
+    const unsigned char* kbase[NTL];
+    const unsigned char* vbase[NTL];
+    kbase[0] = kblk0 + h * Cfg::kRBK;
+    if (NTL == 2) kbase[NTL - 1] = kblk1 + h * Cfg::kRBK;
+    float kn[NTL][2], vn[NTL][2];
+    float kmax = 0.f;
+#pragma unroll
+    for (int t = 0; t < NTL; ++t) {
+      vbase[t] = kbase[t] - h * Cfg::kRBK + args.k_slab_smem + h * Cfg::kRBV;
+      kn[t][0] = __uint_as_float(ld32(kbase[t] + r * kts + Cfg::kWK * 4));
+      kn[t][1] = __uint_as_float(ld32(kbase[t] + (r + 8) * kts + Cfg::kWK * 4));
+      vn[t][0] = __uint_as_float(ld32(vbase[t] + r * vts + Cfg::kWV * 4));
+      vn[t][1] = __uint_as_float(ld32(vbase[t] + (r + 8) * vts + Cfg::kWV * 4));
+      kmax = fmaxf(kmax, fmaxf(fabsf(kn[t][0]), fabsf(kn[t][1])));
+    }
+    // Precision switch: tiles whose largest |score| bound nu_k * ||q|| stays within
+    // kFastScoreBound take the fp16-hi key path (rounding error ~1e-4 relative after the
+    // alpha scaling); otherwise (large-norm rows) the fp16-lo key part is added as well.
+    // Rows past the sequence end hold stale bytes: at worst they select the exact path,
+    // which is correct for any tile.
+    const bool exact = __any_sync(kFullMask, kmax * qnorm_max > kFastScoreBound);
+    float sacc[NTL][4];
+#pragma unroll
+    for (int t = 0; t < NTL; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[t][e] = 0.f;
     if (!exact) {
-      // G = 4: columns 0-3 get key_hi * q_hi, 4-7 key_hi * q_lo (two chains: even and odd
-      // k-steps); G = 8: a q_lo chain
-      float sacc1[4] = {0.f, 0.f, 0.f, 0.f};
+      // G = 4: columns 0-3 get key_hi * q_hi, 4-7 key_hi * q_lo; one tile runs its even and
+      // odd k-steps as two chains.  G = 8: a q_lo chain per tile.
+      float sacc1[NTL][4];
+#pragma unroll
+      for (int t = 0; t < NTL; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc1[t][e] = 0.f;
 #pragma unroll
       for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
-        const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
-        const uint32_t w1 = ld32(kbase + (r + 8) * kts + (c + 4 * jw) * 4);
+        uint32_t w0[NTL], w1[NTL];
+#pragma unroll
+        for (int t = 0; t < NTL; ++t) {
+          w0[t] = ld32(kbase[t] + r * kts + (c + 4 * jw) * 4);
+          w1[t] = ld32(kbase[t] + (r + 8) * kts + (c + 4 * jw) * 4);
+        }
 #pragma unroll
         for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
           const int s = (jw * Cfg::kPWK + e2) >> 1;
-          const uint32_t h00 = k_hi(w0, e2), h10 = k_hi(w1, e2);
-          const uint32_t h01 = k_hi(w0, e2 + 1), h11 = k_hi(w1, e2 + 1);
-          if (G == 8) {
-            mma16816(sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
-            mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
-          } else {
-            mma16816((s & 1) ? sacc1 : sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+#pragma unroll
+          for (int t = 0; t < NTL; ++t) {
+            const uint32_t h00 = k_hi(w0[t], e2), h10 = k_hi(w1[t], e2);
+            const uint32_t h01 = k_hi(w0[t], e2 + 1), h11 = k_hi(w1[t], e2 + 1);
+            if (G == 8) {
+              mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+              mma16816(sacc1[t], h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+            } else {
+              mma16816((NTL == 1 && (s & 1)) ? sacc1[t] : sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+            }
           }
         }
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e];
+      for (int t = 0; t < NTL; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[t][e] += sacc1[t][e];
     } else {
       // adds key_lo * q_hi (G = 4: key_lo * [q_hi | q_lo])
-      float sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
-        const uint32_t w0 = ld32(kbase + r * kts + (c + 4 * jw) * 4);
-        const uint32_t w1 = ld32(kbase + (r + 8) * kts + (c + 4 * jw) * 4);
+      for (int t = 0; t < NTL; ++t) {
+        float sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
-          const int s = (jw * Cfg::kPWK + e2) >> 1;
-          const uint32_t h00 = k_hi(w0, e2), h10 = k_hi(w1, e2), h01 = k_hi(w0, e2 + 1), h11 = k_hi(w1, e2 + 1);
-          const uint32_t l00 = k_lo(w0, e2), l10 = k_lo(w1, e2), l01 = k_lo(w0, e2 + 1), l11 = k_lo(w1, e2 + 1);
-          mma16816(sacc, h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
-          if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
-          mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
+        for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
+          const uint32_t w0 = ld32(kbase[t] + r * kts + (c + 4 * jw) * 4);
+          const uint32_t w1 = ld32(kbase[t] + (r + 8) * kts + (c + 4 * jw) * 4);
+#pragma unroll
+          for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
+            const int s = (jw * Cfg::kPWK + e2) >> 1;
+            const uint32_t h00 = k_hi(w0, e2), h10 = k_hi(w1, e2), h01 = k_hi(w0, e2 + 1), h11 = k_hi(w1, e2 + 1);
+            const uint32_t l00 = k_lo(w0, e2), l10 = k_lo(w1, e2), l01 = k_lo(w0, e2 + 1), l11 = k_lo(w1, e2 + 1);
+            mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+            if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+            mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
+          }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[t][e] += sacc1[e] + sacc2[e];
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[e] += sacc1[e] + sacc2[e];
     }
-    if (G == 4) {
-      // fold the q_lo columns (lanes c = 2, 3) onto the q_hi columns (lanes c = 0, 1)
+    float sc[NTL][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[e] += __shfl_xor_sync(kFullMask, sacc[e], 2);
+    for (int t = 0; t < NTL; ++t) {
+      if (G == 4) {
+        // fold the q_lo columns (lanes c = 2, 3) onto the q_hi columns (lanes c = 0, 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[t][e] += __shfl_xor_sync(kFullMask, sacc[t][e], 2);
+      }
+      sc[t][0] = sacc[t][0] * kn[t][0];
+      sc[t][1] = sacc[t][1] * kn[t][0];
+      sc[t][2] = sacc[t][2] * kn[t][1];
+      sc[t][3] = sacc[t][3] * kn[t][1];
     }
-    float sc[4] = {sacc[0] * kn0, sacc[1] * kn0, sacc[2] * kn1, sacc[3] * kn1};
-    if (ntok < kBS) {  // last block of a sequence: mask the rows past its end
-      if (r >= ntok) sc[0] = sc[1] = -INFINITY;
-      if (r + 8 >= ntok) sc[2] = sc[3] = -INFINITY;
+    if (ntok_last < kBS) {  // last block of a sequence: mask the rows past its end
+      if (r >= ntok_last) sc[NTL - 1][0] = sc[NTL - 1][1] = -INFINITY;
+      if (r + 8 >= ntok_last) sc[NTL - 1][2] = sc[NTL - 1][3] = -INFINITY;
     }
 
     // --- online softmax (q heads 2c, 2c+1 on this lane).  The running max only moves
     // when a score passes it by more than kRescaleSlack, so p = 2^(s - m) <= 2^slack.
     // Most tiles move no max: one compare per score and a vote replace the reduction.
-    const bool jump = fmaxf(sc[0], sc[2]) > m_thr[0] || fmaxf(sc[1], sc[3]) > m_thr[1];
-    if (__any_sync(kFullMask, jump)) {
+    float smax[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      smax[e] = fmaxf(sc[0][e], sc[0][2 + e]);
+#pragma unroll
+      for (int t = 1; t < NTL; ++t) smax[e] = fmaxf(smax[e], fmaxf(sc[t][e], sc[t][2 + e]));
+    }
+    if (__any_sync(kFullMask, smax[0] > m_thr[0] || smax[1] > m_thr[1])) {
       float corr[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float mt = fmaxf(sc[e], sc[2 + e]);
+        float mt = smax[e];
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 4));
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
@@ -697,46 +724,55 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
           for (int e = 0; e < 4; ++e) o_acc[nt][i][e] *= cg;
       }
     }
-    float pv[4];
+    uint32_t p01[NTL], p23[NTL];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float p0 = fast_exp2(sc[e] - m_run[e]), p1 = fast_exp2(sc[2 + e] - m_run[e]);
-      l_run[e] += p0 + p1;
-      pv[e] = p0 * vn0;
-      pv[2 + e] = p1 * vn1;
+    for (int t = 0; t < NTL; ++t) {
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float p0 = fast_exp2(sc[t][e] - m_run[e]), p1 = fast_exp2(sc[t][2 + e] - m_run[e]);
+        l_run[e] += p0 + p1;
+        pv[e] = p0 * vn[t][0];
+        pv[2 + e] = p1 * vn[t][1];
+      }
+      p01[t] = pack_half2(pv[0], pv[1]);  // token r:   heads 2c, 2c+1
+      p23[t] = pack_half2(pv[2], pv[3]);  // token r+8: heads 2c, 2c+1
     }
-    const uint32_t p01 = pack_half2(pv[0], pv[1]);  // token r:   heads 2c, 2c+1
-    const uint32_t p23 = pack_half2(pv[2], pv[3]);  // token r+8: heads 2c, 2c+1
 
     // --- values ------------------------------------------------------------------------
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {  // tokens {c, c+4} (ks=0) and {c+8, c+12} (ks=1)
-      const int t0 = c + 8 * ks, t1 = c + 4 + 8 * ks;
-      uint32_t bv[Cfg::kNT][2];
+    for (int t = 0; t < NTL; ++t) {
 #pragma unroll
-      for (int nt = 0; nt < Cfg::kNT; ++nt) {
-        const int cs = 2 * nt + (r >> 2);  // source lane column: q head (4 nt + r/2) / 2
-        const uint32_t src = ks == 0 ? p01 : p23;
-        const uint32_t x0 = __shfl_sync(kFullMask, src, 4 * c + cs);
-        const uint32_t x1 = __shfl_sync(kFullMask, src, 4 * (c + 4) + cs);
-        bv[nt][0] = __byte_perm(x0, 0u, sel_b);
-        bv[nt][1] = __byte_perm(x1, 0u, sel_b);
-      }
+      for (int ks = 0; ks < 2; ++ks) {  // tokens {c, c+4} (ks=0) and {c+8, c+12} (ks=1)
+        const int t0 = c + 8 * ks, t1 = c + 4 + 8 * ks;
+        uint32_t bv[Cfg::kNT][2];
 #pragma unroll
-      for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
-        const uint32_t wa = ld32(vbase + t0 * vts + (r + 8 * jw) * 4);
-        const uint32_t wb = ld32(vbase + t1 * vts + (r + 8 * jw) * 4);
+        for (int nt = 0; nt < Cfg::kNT; ++nt) {
+          const int cs = 2 * nt + (r >> 2);  // source lane column: q head (4 nt + r/2) / 2
+          const uint32_t src = ks == 0 ? p01[t] : p23[t];
+          const uint32_t x0 = __shfl_sync(kFullMask, src, 4 * c + cs);
+          const uint32_t x1 = __shfl_sync(kFullMask, src, 4 * (c + 4) + cs);
+          bv[nt][0] = __byte_perm(x0, 0u, sel_b);
+          bv[nt][1] = __byte_perm(x1, 0u, sel_b);
+        }
 #pragma unroll
-        for (int e = 0; e < Cfg::kPWV; e += 2) {
-          const int i = (jw * Cfg::kPWV + e) >> 1;  // m-tile: pairs q = 2i (row r), 2i+1 (row r+8)
-          const uint32_t a0 = v_lookup(wa, e), a1 = v_lookup(wa, e + 1);
-          const uint32_t a2 = v_lookup(wb, e), a3 = v_lookup(wb, e + 1);
+        for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
+          const uint32_t wa = ld32(vbase[t] + t0 * vts + (r + 8 * jw) * 4);
+          const uint32_t wb = ld32(vbase[t] + t1 * vts + (r + 8 * jw) * 4);
 #pragma unroll
-          for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+          for (int e = 0; e < Cfg::kPWV; e += 2) {
+            const int i = (jw * Cfg::kPWV + e) >> 1;  // m-tile: pairs q = 2i (row r), 2i+1 (row r+8)
+            const uint32_t a0 = v_lookup(wa, e), a1 = v_lookup(wa, e + 1);
+            const uint32_t a2 = v_lookup(wb, e), a3 = v_lookup(wb, e + 1);
+#pragma unroll
+            for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+          }
         }
       }
     }
   };
+  using One = std::integral_constant<int, 1>;
+  using Two = std::integral_constant<int, 2>;
 
   // ---- main pipeline -----------------------------------------------------------------
   // Stage st lives in ring slot st % nst; full[slot] completes when its copies landed,
@@ -755,6 +791,50 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
     for (int s2 = (S > nst ? S - nst : 0); s2 < S; ++s2) mbar_wait(bar_full(s2 % nst), (uint32_t)((s2 / nst) & 1));
     return;
   }
+  {
+      // ---- tables (consumer warps; the producer is already streaming) ------------------
+    if (KB == 4) {
+      for (int i = tid; i < 256 * 32; i += 32 * ncons) {
+        const int f = i >> 5, copy = i & 31;
+        __half ha, la, hb, lb;
+        split_half(__ldg(a.k_centroids + (f & 15)) * args.k_alpha, ha, la);
+        split_half(__ldg(a.k_centroids + (f >> 4)) * args.k_alpha, hb, lb);
+        __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
+        *reinterpret_cast<uint32_t*>(lutT + f * 256 + copy * 4) = *reinterpret_cast<uint32_t*>(&hi2);
+        if (copy == 0) *reinterpret_cast<uint32_t*>(lutL + f * 4) = *reinterpret_cast<uint32_t*>(&lo2);
+      }
+    } else {
+      for (int f = tid; f < 16; f += 32 * ncons) {
+        __half ha, la, hb, lb;
+        split_half(__ldg(a.k_centroids + (f & 3)) * args.k_alpha, ha, la);
+        split_half(__ldg(a.k_centroids + (f >> 2)) * args.k_alpha, hb, lb);
+        __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t*>(&hi2);
+        v.y = *reinterpret_cast<uint32_t*>(&lo2);
+        *reinterpret_cast<uint2*>(lutK2 + f * 8) = v;
+      }
+    }
+    if (VB == 4) {
+      for (int i = tid; i < 256 * 32; i += 32 * ncons) {
+        const int f = i >> 5, copy = i & 31;
+        const float ca = __ldg(a.v_centroids + (f & 15)) * args.v_alpha;
+        const float cb = __ldg(a.v_centroids + (f >> 4)) * args.v_alpha;
+        *reinterpret_cast<uint32_t*>(lutT + f * 256 + 128 + copy * 4) = pack_half2(ca, cb);
+      }
+    } else {
+      for (int f = tid; f < 16; f += 32 * ncons) {
+        const float ca = __ldg(a.v_centroids + (f & 3)) * args.v_alpha;
+        const float cb = __ldg(a.v_centroids + (f >> 2)) * args.v_alpha;
+        *reinterpret_cast<uint32_t*>(lutV2 + f * 4) = pack_half2(ca, cb);
+      }
+    }
+  asm volatile("bar.sync 1, %0;\n" ::"r"(32 * ncons) : "memory");  // consumer warps only
+  }
+  // the first block belongs to b_first: its query is read while the first copies land
+  reset_state();
+  cur_b = b_first;
+  load_query(b_first);
   int slot = 0;
   uint32_t par = 0;
   for (int st = 0; st < nstages; ++st) {
@@ -762,10 +842,20 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
       if (lane == 0 && a.status) atomicMax(a.status, (int32_t)kTimeout);
       return;
     }
-    const BlockMeta m = meta[slot * WPH + slot_u];
-    if (m.ntok != 0) {
-      if (m.b != cur_b) enter_sequence(m.b);
-      if (m.valid) tile(smem + buf_off(slot, slot_u), m.ntok);
+    const BlockMeta m0 = meta[slot * WPH];
+    const BlockMeta m1 = meta[slot * WPH + WPH - 1];
+    if (WPH == 2 && m0.ntok == kBS && m0.valid && m1.ntok != 0 && m1.valid && m1.b == m0.b) {
+      if (m0.b != cur_b) enter_sequence(m0.b);
+      tiles(Two{}, smem + buf_off(slot, 0), smem + buf_off(slot, 1), m1.ntok);
+    } else {
+#pragma unroll
+      for (int u = 0; u < WPH; ++u) {
+        const BlockMeta m = u == 0 ? m0 : m1;
+        if (m.ntok != 0) {
+          if (m.b != cur_b) enter_sequence(m.b);
+          if (m.valid) tiles(One{}, smem + buf_off(slot, u), nullptr, m.ntok);
+        }
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty(slot));
@@ -787,7 +877,7 @@ __global__ void __launch_bounds__(32 * (8 * WPH + 1), 1) decode_tc_kernel(TcArgs
 
 // One warp per (sequence, q head): merge the partials of the CTAs that touched the
 // sequence, normalise, apply R^T (FWHT + sign flip) and store.
-template <int E, int WPH>
+template <int E>
 __global__ void __launch_bounds__(256)
 combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc, const float* __restrict__ part_ml,
                   const int* __restrict__ prefix) {
@@ -809,12 +899,12 @@ combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc
     float mx = -INFINITY;
     for (long long i = f; i <= l; ++i)
       if (owns_blocks(i))
-        for (int u = 0; u < WPH; ++u) mx = fmaxf(mx, part_ml[((WPH * (i + b) + u) * a.num_q_heads + j) * 2]);
+        mx = fmaxf(mx, part_ml[((i + b) * a.num_q_heads + j) * 2]);
     float lsum = 0.f;
     for (long long i = f; i <= l; ++i) {
       if (!owns_blocks(i)) continue;
-      for (int u = 0; u < WPH; ++u) {
-        const int64_t s = (WPH * (i + b) + u) * a.num_q_heads + j;
+      {
+        const int64_t s = (i + b) * a.num_q_heads + j;
         const float ms = part_ml[s * 2];
         const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
         lsum = fmaf(w, part_ml[s * 2 + 1], lsum);
@@ -890,18 +980,18 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   }
 
   const int B = a.batch, Hq = a.num_q_heads;
-  const int64_t slots = (int64_t)WPH * (p.num_splits + B);
+  const int64_t slots = (int64_t)p.num_splits + B;
   t.part_acc = static_cast<float*>(a.workspace);
   t.part_ml = t.part_acc + slots * Hq * D;
   t.prefix = reinterpret_cast<int*>(t.part_ml + slots * Hq * 2);
   auto kern = decode_tc_kernel<D, KB, VB, G, WPH>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<p.num_splits, 32 * (H * WPH + 1), smem, stream>>>(t);
+  kern<<<p.num_splits, 32 * (H + 1), smem, stream>>>(t);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int rows = B * Hq;
-  combine_tc_kernel<D / 32, WPH><<<(rows + 7) / 8, 256, 0, stream>>>(a, p.num_splits, t.part_acc, t.part_ml,
+  combine_tc_kernel<D / 32><<<(rows + 7) / 8, 256, 0, stream>>>(a, p.num_splits, t.part_acc, t.part_ml,
                                                                      t.prefix);
   return cudaGetLastError();
 }
@@ -916,7 +1006,7 @@ bool tc_decode_supported(const DecodeArgs& a) {
   return a.block_size == kBS && a.num_kv_heads >= 1 && a.num_kv_heads <= 8 && (G == 4 || G == 8) && bits_ok && dim_ok;
 }
 
-int tc_warps_per_head(int head_dim) { return head_dim >= 256 ? 1 : 2; }
+int tc_partials_per_sequence_split() { return 1; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
   const int G = a.num_q_heads / a.num_kv_heads;

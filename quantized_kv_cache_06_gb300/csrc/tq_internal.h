@@ -80,7 +80,7 @@ struct DecodeArgs {
 // Tensor-core decode (tq_decode_tc.cu): whether the shapes/bits in `a` have an
 // instantiation, its warps per kv head, and its launch.
 bool tc_decode_supported(const DecodeArgs& a);
-int tc_warps_per_head(int head_dim);
+int tc_partials_per_sequence_split();
 cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 
 // Split plan for the shapes in `a` on a device with `num_sms` SMs.
