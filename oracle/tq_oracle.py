@@ -21,7 +21,9 @@ Sources (TurboQuant documentation pages):
   * "vLLM Reference Audit", section "Feature Checklist": Lloyd-Max codebooks with
     "exact Beta" tests, RHT rotation, 1..5-bit packing.
   * "Architecture", section "Diagnostic vs Serving Paths": the paged decode reads
-    packed pages and reconstructs rows; direct-QK consumes keys compressed.
+    packed pages and reconstructs rows; direct-QK consumes keys compressed; the
+    diagnostic dense reconstruction (the "vLLM Reference Audit" file map's
+    tq4_decompress readback) is ``dequant_slots``.
 
 Readings where the pages are silent (each one is listed in the design notes):
   * signs of the RHT: the i-th output of splitmix64 (Steele, Lea & Flood 2014)
@@ -289,6 +291,29 @@ def dequant_rows(rows: np.ndarray, head_dim: int, bits: int, rot: np.ndarray,
     norms = np.ascontiguousarray(rows[:, nb:nb + 4]).view("<f4").reshape(-1).astype(np.float64)
     rotated = centroids32.astype(np.float64)[idx]
     return norms[:, None] * (rotated @ rot)
+
+
+def dequant_slots(pages: np.ndarray, slots: np.ndarray, signs: np.ndarray, centroids32: np.ndarray,
+                  bits: int) -> np.ndarray:
+    """Dense readback of the rows a write put at ``slots`` ("vLLM Reference Audit", file map:
+    tq4_decompress, diagnostic readback; "Architecture", Diagnostic vs Serving Paths: dense
+    reconstruction from packed bytes).  pages uint8[NB, bs, H, RB]; returns fp64[T, H, D]
+    with nu * R^T c[idx] for every slot >= 0 and a zero row for a negative slot.  A slot
+    at or beyond NB * bs raises SlotOutOfRange, as for the write."""
+    pages = np.asarray(pages, dtype=np.uint8)
+    nblk, bs, nh, _ = pages.shape
+    d = len(signs)
+    slots = np.asarray(slots, dtype=np.int64)
+    if np.any(slots >= nblk * bs):
+        raise SlotOutOfRange("slot outside the allocated pages")
+    rot = rotation_matrix(signs)
+    out = np.zeros((len(slots), nh, d), dtype=np.float64)
+    keep = np.nonzero(slots >= 0)[0]
+    for h in range(nh):
+        rows = pages[slots[keep] // bs, slots[keep] % bs, h]
+        if len(keep):
+            out[keep, h] = dequant_rows(rows, d, bits, rot, centroids32)
+    return out
 
 
 def _gather_rows(pages, block_table_row, seq_len, head):

@@ -371,3 +371,61 @@ def test_decode_skips_out_of_range_block():
     first_only = o.paged_decode(**case2)
     assert np.max(np.abs(bad - first_only)) < 1e-12
     assert np.max(np.abs(bad - good)) > 1e-6
+
+
+# ---------------------------------------------------------------- dense readback (tq4_decompress)
+
+def _fwht_butterfly(x):
+    """Unnormalised Walsh-Hadamard transform of the last axis by in-place butterflies."""
+    y = np.array(x, dtype=np.float64)
+    n = y.shape[-1]
+    hlen = 1
+    while hlen < n:
+        for i in range(0, n, 2 * hlen):
+            a = y[..., i:i + hlen].copy()
+            b = y[..., i + hlen:i + 2 * hlen].copy()
+            y[..., i:i + hlen] = a + b
+            y[..., i + hlen:i + 2 * hlen] = a - b
+        hlen *= 2
+    return y
+
+
+def test_readback_rotates_forward_to_the_centroids():
+    # Applying the encoder's forward rotation R x = H_D (s * x) / sqrt(D) (here by butterfly,
+    # not the oracle's matrix) to the readback of a row must give nu * c[idx].  A transposed
+    # R, a lost sign flip or a wrong bit order in the readback breaks this.
+    rng = np.random.default_rng(11)
+    for d, bits in ((64, 2), (64, 3), (128, 4), (128, 5), (256, 4)):
+        signs = o.splitmix64_signs(d, 42)
+        c32, _ = o.codebook_f32(d, bits)
+        idx = rng.integers(0, 1 << bits, size=(6, d))
+        nu = rng.uniform(0.1, 50.0, size=6).astype(np.float32)
+        pages = o.make_rows(idx, nu, bits).reshape(3, 2, 1, -1)  # 3 blocks x 2 slots x 1 head
+        back = o.dequant_slots(pages, np.arange(6), signs, c32, bits)[:, 0]
+        fwd = _fwht_butterfly(back * signs) / math.sqrt(d)
+        want = nu.astype(np.float64)[:, None] * c32.astype(np.float64)[idx]
+        assert np.max(np.abs(fwd - want)) <= 1e-12 * float(nu.max())
+
+
+def test_readback_norm_and_addressing():
+    rng = np.random.default_rng(12)
+    d, bits, bs, nblk, h = 64, 4, 4, 3, 2
+    signs = o.splitmix64_signs(d, 42)
+    c32, _ = o.codebook_f32(d, bits)
+    idx = rng.integers(0, 16, size=(nblk * bs * h, d))
+    nu = rng.uniform(0.5, 4.0, size=nblk * bs * h).astype(np.float32)
+    pages = o.make_rows(idx, nu, bits).reshape(nblk, bs, h, -1)
+    slots = np.array([7, -1, 0, 11, -3])
+    back = o.dequant_slots(pages, slots, signs, c32, bits)
+    assert back.shape == (5, h, d)
+    assert np.all(back[1] == 0) and np.all(back[4] == 0)  # negative slots: zero rows
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        for hh in range(h):
+            k = (s // bs * bs + s % bs) * h + hh  # slot s, head hh
+            # R is orthogonal: ||nu R^T c[idx]|| = nu ||c[idx]||
+            want = float(nu[k]) * np.linalg.norm(c32.astype(np.float64)[idx[k]])
+            assert np.linalg.norm(back[t, hh]) == pytest.approx(want, rel=1e-12)
+    with pytest.raises(o.SlotOutOfRange):
+        o.dequant_slots(pages, np.array([0, nblk * bs]), signs, c32, bits)
