@@ -395,6 +395,8 @@ def run_gpu(args):
             "write_token_rows_per_s": weak_scaling_rate(world, 2 * w.num_tokens, write_s), "write_gbs_per_gpu": wr_gbs,
             "roofline": dominant, "roofline_decode": roof_dec, "roofline_write": roof_wr,
             "gpu_launches": args.steps * 6, "clocks": clk}
+    line["next_rows"] = {"tq_dequant_rows": dequant_measure(tq, w, dev, kp, slots, signs, ck, flush, stream, peak,
+                                                             peak_kind, world)}
 
     if not args.no_e2e:
         line["e2e"] = e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world)
@@ -408,6 +410,37 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def dequant_measure(tq, w, dev, kp, slots, signs, ck, flush, stream, peak, peak_kind, world, steps=5):
+    """Dense readback of every K row of the workload (tq_dequant_rows, fp16 out), timed
+    apart from the step with CUDA events, an L2 flush before each call."""
+    import torch
+
+    out = torch.empty(w.num_tokens, w.num_kv_heads, w.head_dim, dtype=torch.float16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(2):
+        tq.tq_dequant_rows(kp, slots, signs, ck, out=out, status=st, check=False)
+    times = []
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        tq.tq_dequant_rows(kp, slots, signs, ck, out=out, status=st, check=False)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    tq.raise_for_device_status(st)
+    t_s = max_over_ranks([statistics.mean(times)], world, dev)[0] / 1e3
+    written = int((w.slots >= 0).sum()) * w.num_kv_heads
+    rows = w.num_tokens * w.num_kv_heads
+    nbytes = written * row_bytes(w.head_dim, w.k_bits) + rows * w.head_dim * 2 + w.num_tokens * 8
+    gbs = nbytes / t_s / 1e9
+    return {"workload": f"read back all {rows} K rows (K{w.k_bits} D{w.head_dim}) to fp16", "us": t_s * 1e6,
+            "rows_per_s": weak_scaling_rate(world, rows, t_s), "gbs_per_gpu": gbs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": nbytes},
+            "gpu_launches": steps + 2}
 
 
 def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5):

@@ -150,6 +150,36 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
                           void* workspace, size_t workspace_bytes, int32_t* status_dev,
                           void* stream);
 
+/* Dense readback of packed rows: the inverse addressing of tq_write_kv ("vLLM Reference
+ * Audit", file map: tq4_decompress, the TQ4 unpack kernel for diagnostic readback of
+ * packed index bytes and norms; "Architecture", Diagnostic vs Serving Paths: dense
+ * reconstruction for layout and distortion checks).
+ *
+ * For token t (0 <= t < num_tokens) and kv head h, with s = slots[t]:
+ *   s >= 0:  out[t][h][:] = nu * R^T c[idx], the row pages[s / block_size][s % block_size][h]
+ *            unpacked (LSB-first b-bit indices idx, fp32 norm nu in its last 4 bytes), with
+ *            R^T = diag(signs) H_D / sqrt(D) and c = `centroids`;
+ *   s < 0:   out[t][h][:] = 0;
+ *   s >= num_blocks * block_size: out[t][h][:] = 0 and TQ_ERR_SLOT_OUT_OF_RANGE in status_dev.
+ * A sequence's rows are read back by passing its slots (token i of the sequence sits at
+ * block_table[i / block_size] * block_size + i % block_size, "vLLM Usage", Slot Mapping).
+ *
+ *   pages      device, uint8 [num_blocks][block_size][num_kv_heads][RB(head_dim, bits)],
+ *              16-byte aligned
+ *   slots      device, int64 [num_tokens], 8-byte aligned
+ *   signs      device, fp32 [head_dim] (tq_build_rotation); centroids device, fp32 [2^bits]
+ *              (tq_codebook) -- the ones the rows were written with
+ *   out        device, out_dtype [num_tokens][num_kv_heads][head_dim], 16-byte aligned;
+ *              computed in fp32, rounded once to out_dtype
+ *   status_dev device int32 or NULL; reset to 0 by the call, then set as above
+ *
+ * head_dim must be 32, 64, 128 or 256 and bits 2..5 (TQ_ERR_UNSUPPORTED otherwise).
+ * Reads RB bytes and writes head_dim values per row; no workspace, graph-capturable. */
+tq_status tq_dequant_rows(const uint8_t* pages, int bits, int64_t num_blocks, int block_size, int num_kv_heads,
+                          int head_dim, const int64_t* slots, int64_t num_tokens, const float* signs,
+                          const float* centroids, void* out, tq_dtype out_dtype, int32_t* status_dev,
+                          void* stream);
+
 /* Allocation-free variant of tq_paged_decode.  The TurboQuant pages have no
  * counterpart: it exists for callers that cannot call cudaMalloc -- a plugin whose
  * host framework owns all device memory, a deployment held to a fixed memory

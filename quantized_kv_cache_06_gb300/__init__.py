@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     raise_for_device_status,
     tq_build_rotation,
     tq_codebook,
+    tq_dequant_rows,
     tq_paged_decode,
     tq_paged_decode_static,
     tq_paged_decode_workspace,

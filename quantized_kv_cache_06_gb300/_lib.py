@@ -45,6 +45,8 @@ SIGNATURES = {
     "tq_codebook": (_c_int, [_c_int, _c_int, _c_p, _c_p]),
     "tq_write_kv": (_c_int, [_c_p, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_p, _c_p, _c_i64, _c_int,
                              _c_p, _c_p, _c_p, _c_p]),
+    "tq_dequant_rows": (_c_int, [_c_p, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_p, _c_i64, _c_p, _c_p, _c_p,
+                                 _c_int, _c_p, _c_p]),
     "tq_paged_decode_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "tq_paged_decode": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
                                  _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_int,
@@ -188,6 +190,39 @@ def tq_write_kv(raw: torch.Tensor, pages: torch.Tensor, slots: torch.Tensor, sig
     if check:
         raise_for_device_status(status)
     return status
+
+
+# ---------------------------------------------------------------- readback
+
+def tq_dequant_rows(pages: torch.Tensor, slots: torch.Tensor, signs: torch.Tensor, centroids: torch.Tensor,
+                    out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float16,
+                    status: torch.Tensor | None = None, check: bool = True) -> torch.Tensor:
+    """Dense readback (tq4_decompress) of the rows written at `slots`: out[T, H, D] =
+    nu * R^T c[idx] for slot >= 0, zeros for slot < 0.  pages [NB, bs, H, RB] uint8,
+    slots [T] int64.  With check=True the call synchronises and raises
+    TQError(TQ_ERR_SLOT_OUT_OF_RANGE) when a slot lies past the pages.  Returns `out`."""
+    dev = _need_cuda("tq_dequant_rows", pages, slots, signs, centroids)
+    if pages.dim() != 4 or slots.dim() != 1 or pages.dtype != torch.uint8 or slots.dtype != torch.int64:
+        raise ValueError("tq_dequant_rows: pages uint8 [NB, bs, H, RB] and slots int64 [T] expected")
+    nb, bs, h, rb = pages.shape
+    d = signs.numel()
+    bits = _bits_from_centroids(centroids)
+    if rb != tq_row_bytes(d, bits):
+        raise ValueError(f"tq_dequant_rows: pages row bytes {rb} != RB({d}, {bits})")
+    t = slots.numel()
+    if out is None:
+        out = torch.empty(t, h, d, dtype=out_dtype, device=dev)
+    if tuple(out.shape) != (t, h, d) or out.dtype not in _DTYPES:
+        raise ValueError(f"tq_dequant_rows: out must be [{t}, {h}, {d}] f32/f16/bf16")
+    _need_cuda("tq_dequant_rows", pages, out)
+    if status is None:
+        status = _status_buffer(dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_dequant_rows(_ptr(pages), bits, nb, bs, h, d, _ptr(slots), t, _ptr(signs), _ptr(centroids),
+                                     _ptr(out), _DTYPES[out.dtype], _ptr(status), _stream(dev)))
+    if check:
+        raise_for_device_status(status)
+    return out
 
 
 # ---------------------------------------------------------------- decode

@@ -295,6 +295,33 @@ tq_status tq_write_kv(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, i
   return check_cuda(tq::launch_write(a, static_cast<cudaStream_t>(stream)), "tq_write_kv launch");
 }
 
+tq_status tq_dequant_rows(const uint8_t* pages, int bits, int64_t num_blocks, int block_size, int num_kv_heads,
+                          int head_dim, const int64_t* slots, int64_t num_tokens, const float* signs,
+                          const float* centroids, void* out, tq_dtype out_dtype, int32_t* status_dev,
+                          void* stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 0 || block_size < 1)
+    return fail(TQ_ERR_INVALID_ARG, "tq_dequant_rows: invalid sizes (tokens=%lld, kv_heads=%d, blocks=%lld, block_size=%d)",
+                (long long)num_tokens, num_kv_heads, (long long)num_blocks, block_size);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!bits_ok(bits)) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 2, 3, 4 or 5", bits);
+  if (!dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_dequant_rows: unknown out dtype %d", (int)out_dtype);
+  if (num_tokens > 0 && (!pages || !slots || !signs || !centroids || !out))
+    return fail(TQ_ERR_INVALID_ARG, "tq_dequant_rows: null pointer argument");
+  if (num_tokens > 0 && (!aligned(pages, 16) || !aligned(slots, 8) || !aligned(signs, 4) || !aligned(centroids, 4) ||
+                         !aligned(out, 16) || !aligned(status_dev, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "tq_dequant_rows: pages and out must be 16-byte aligned, slots 8-byte aligned");
+  tq::DequantArgs a{pages, bits, num_blocks, block_size, num_kv_heads, head_dim, slots, num_tokens,
+                    signs, centroids, out, (int)out_dtype, status_dev};
+  if (!tq::dequant_supported(a))
+    return fail(TQ_ERR_UNSUPPORTED, "tq_dequant_rows: head_dim %d with %d bits has no kernel", head_dim, bits);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (status_dev) {
+    tq_status st = check_cuda(cudaMemsetAsync(status_dev, 0, sizeof(int32_t), s), "tq_dequant_rows status reset");
+    if (st != TQ_OK) return st;
+  }
+  return check_cuda(tq::launch_dequant(a, s, current_device_sms()), "tq_dequant_rows launch");
+}
+
 size_t tq_paged_decode_workspace(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                  int max_blocks_per_seq, int block_size) {
   if (decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size) != TQ_OK)

@@ -93,6 +93,27 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t
 
 namespace tq {
 
+// Dense readback of packed rows (tq_dequant.cu).
+struct DequantArgs {
+  const uint8_t* pages;
+  int bits;
+  int64_t num_blocks;
+  int block_size;
+  int num_kv_heads;
+  int head_dim;
+  const int64_t* slots;
+  int64_t num_tokens;
+  const float* signs;
+  const float* centroids;
+  void* out;
+  int out_dtype;
+  int32_t* status;  // may be null
+};
+
+bool dequant_supported(const DequantArgs& a);
+// Enqueues the readback (status must already be reset by the caller).
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t stream, int num_sms);
+
 // Fixed device scratch for tq_paged_decode_static: a file-scope __device__ array in
 // tq_decode.cu.  Returns its device address on the current device (looked up once
 // per device with cudaGetSymbolAddress) and its capacity in bytes.
