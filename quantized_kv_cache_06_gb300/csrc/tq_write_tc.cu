@@ -308,16 +308,21 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
     ss1 += __shfl_xor_sync(kFullMask, ss1, 2);
     // ||x|| = sqrt(ss / D); u = y / sqrt(ss); grid coordinate g = u * q_a + q_b.
     // Every partial sum above only grows, so y^2 <= ss (1 + 2^-23) + 2^-150 for each y of
-    // the row, even when ss is subnormal; adding 2^-149 under the root therefore keeps
-    // |u| <= 1 + 2^-23 and g inside [0, 2 q_a + 1) with no clamp.  It moves ss by at most
-    // one ulp, and only below 2^-124; an all-zero row gets g = q_b, i.e. u = 0.
-    const float nu0 = sqrtf(ss0 * (1.0f / D)), nu1 = sqrtf(ss1 * (1.0f / D));
-    const float ga0 = q_a / sqrtf(ss0 + 0x1p-149f);
-    const float ga1 = q_a / sqrtf(ss1 + 0x1p-149f);
+    // the row, even when ss is subnormal; adding 2^-149 under the root keeps |u| within a
+    // few ulp of 1 and g inside [1/4, 2 q_a + 1/2) with no clamp (it moves ss by at most one
+    // ulp, and only below 2^-124; an all-zero row gets g = q_b, i.e. u = 0).  rsqrtf (2 ulp)
+    // is enough: it moves g by < 1e-4 cell and u by < 1e-6, inside the decision tolerance,
+    // and the stored norm ss * rsqrt(ss) / sqrt(D) by < 1e-6 relative.
+    const float rs0 = rsqrtf(ss0 + 0x1p-149f), rs1 = rsqrtf(ss1 + 0x1p-149f);
+    const float inv_sqrt_d = 1.0f / sqrtf((float)D);
+    float nu0 = ss0 * rs0 * inv_sqrt_d, nu1 = ss1 * rs1 * inv_sqrt_d;
+    const float ga0 = q_a * rs0, ga1 = q_a * rs1;
     // A NaN or infinite input (the only way to a non-finite sum) would give a NaN grid
     // coordinate, whose bits address nothing: such rows are quantised as zero rows.
     if (__any_sync(kFullMask, !(ss0 <= 3.402823466e38f) || !(ss1 <= 3.402823466e38f))) {
       const bool bad0 = !(ss0 <= 3.402823466e38f), bad1 = !(ss1 <= 3.402823466e38f);
+      if (bad0) nu0 = ss0;  // +inf (a sum that overflowed) or NaN, as sqrt would give
+      if (bad1) nu1 = ss1;
 #pragma unroll
       for (int j = 0; j < NB; ++j)
 #pragma unroll
