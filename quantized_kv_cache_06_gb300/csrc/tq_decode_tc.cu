@@ -876,7 +876,11 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 }
 
 // One warp per (sequence, q head): merge the partials of the CTAs that touched the
-// sequence, normalise, apply R^T (FWHT + sign flip) and store.
+// sequence, normalise, apply R^T (FWHT + sign flip) and store.  The (m, l) and the
+// accumulator of up to kCombineBatch partials are loaded together (one round trip);
+// longer spans loop over batches with a running rescale.
+constexpr int kCombineBatch = 4;
+
 template <int E>
 __global__ void __launch_bounds__(256)
 combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc, const float* __restrict__ part_ml,
@@ -894,23 +898,35 @@ combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc
   if (p1 > p0) {
     const long long C = num_ctas;
     const long long f = ((p0 + 1) * C - 1) / N, l = (p1 * C - 1) / N;  // first / last CTA
-    // CTAs whose block range is empty (possible when N < C) wrote nothing
-    auto owns_blocks = [&](long long i) { return N * i / C < N * (i + 1) / C; };
-    float mx = -INFINITY;
-    for (long long i = f; i <= l; ++i)
-      if (owns_blocks(i))
-        mx = fmaxf(mx, part_ml[((i + b) * a.num_q_heads + j) * 2]);
-    float lsum = 0.f;
-    for (long long i = f; i <= l; ++i) {
-      if (!owns_blocks(i)) continue;
-      {
-        const int64_t s = (i + b) * a.num_q_heads + j;
-        const float ms = part_ml[s * 2];
-        const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
-        lsum = fmaf(w, part_ml[s * 2 + 1], lsum);
+    float mx = -INFINITY, lsum = 0.f;
+    for (long long i0 = f; i0 <= l; i0 += kCombineBatch) {
+      float ms[kCombineBatch], ls[kCombineBatch], acc[kCombineBatch][E];
 #pragma unroll
-        for (int k = 0; k < E; ++k) v[k] = fmaf(w, part_acc[s * D + lane * E + k], v[k]);
+      for (int u = 0; u < kCombineBatch; ++u) {
+        const long long i = i0 + u;
+        // CTAs past l, and CTAs whose block range is empty (possible when N < C), wrote nothing
+        const bool live = i <= l && N * i / C < N * (i + 1) / C;
+        const int64_t s = (i + b) * a.num_q_heads + j;
+        ms[u] = live ? part_ml[s * 2] : -INFINITY;
+        ls[u] = live ? part_ml[s * 2 + 1] : 0.f;
+#pragma unroll
+        for (int k = 0; k < E; ++k) acc[u][k] = live ? part_acc[s * D + lane * E + k] : 0.f;
       }
+      float bm = mx;
+#pragma unroll
+      for (int u = 0; u < kCombineBatch; ++u) bm = fmaxf(bm, ms[u]);
+      const float cr = mx == -INFINITY ? 0.f : exp2f(mx - bm);  // rescale of what came before
+      lsum *= cr;
+#pragma unroll
+      for (int k = 0; k < E; ++k) v[k] *= cr;
+#pragma unroll
+      for (int u = 0; u < kCombineBatch; ++u) {
+        const float w = ms[u] == -INFINITY ? 0.f : exp2f(ms[u] - bm);
+        lsum = fmaf(w, ls[u], lsum);
+#pragma unroll
+        for (int k = 0; k < E; ++k) v[k] = fmaf(w, acc[u][k], v[k]);
+      }
+      mx = bm;
     }
     const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
 #pragma unroll
