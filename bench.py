@@ -439,7 +439,8 @@ def dequant_measure(tq, w, dev, kp, slots, signs, ck, flush, stream, peak, peak_
     return {"workload": f"read back all {rows} K rows (K{w.k_bits} D{w.head_dim}) to fp16", "us": t_s * 1e6,
             "rows_per_s": weak_scaling_rate(world, rows, t_s), "gbs_per_gpu": gbs,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": nbytes},
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": nbytes,
+                         "traffic": ncu_traffic("dequant")},
             "gpu_launches": steps + 2}
 
 
