@@ -370,6 +370,24 @@ def paged_decode(q, k_pages, v_pages, k_bits, v_bits, block_table, seq_lens, sig
     return (out, bad_block) if return_flags else out
 
 
+def paged_prefill(q, q_seq, q_len, k_pages, v_pages, k_bits, v_bits, block_table, signs,
+                  k_centroids32, v_centroids32, scale=None, return_flags=False):
+    """Mixed prefill/decode attention over the packed cache ("vLLM Usage", Runtime
+    Dispatch: cache plus mixed prefill/decode reads the packed cache).
+
+    q[T, Hq, D]: query row i belongs to sequence q_seq[i] and sees the first q_len[i]
+    tokens of it (causal: its position + 1); the cache already holds the new tokens.
+    Row i is the decode of one query over block_table[q_seq[i]] with length q_len[i], so
+    a decode batch is the case of one row per sequence.  Returns out[T, Hq, D] (and the
+    bad-block flag of paged_decode).
+    """
+    q_seq = np.asarray(q_seq, dtype=np.int64)
+    q_len = np.asarray(q_len, dtype=np.int64)
+    rows_table = np.asarray(block_table)[q_seq]
+    return paged_decode(q, k_pages, v_pages, k_bits, v_bits, rows_table, q_len, signs, k_centroids32,
+                        v_centroids32, scale=scale, return_flags=return_flags)
+
+
 def paged_decode_rotated(q, k_pages, v_pages, k_bits, v_bits, block_table, seq_lens, signs,
                          k_centroids32, v_centroids32, scale=None):
     """Same attention in rotated space ("Architecture": direct-QK and packed-V):

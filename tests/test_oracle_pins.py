@@ -429,3 +429,82 @@ def test_readback_norm_and_addressing():
             assert np.linalg.norm(back[t, hh]) == pytest.approx(want, rel=1e-12)
     with pytest.raises(o.SlotOutOfRange):
         o.dequant_slots(pages, np.array([0, nblk * bs]), signs, c32, bits)
+
+
+# ---------------------------------------------------------------- mixed prefill / decode
+
+def _prefill_case(seed=21):
+    rng = np.random.default_rng(seed)
+    d, h, hq, kb, vb, bs = 64, 2, 4, 4, 2, 4
+    lens = np.array([9, 6, 1])
+    nblk = int(sum(-(-n // bs) for n in lens))
+    bt = np.zeros((len(lens), 4), dtype=np.int32)
+    perm = rng.permutation(nblk)
+    pos = 0
+    for b, n in enumerate(lens):
+        nb = -(-int(n) // bs)
+        bt[b, :nb] = perm[pos:pos + nb]
+        pos += nb
+    signs = o.splitmix64_signs(d, 42)
+    kc, _ = o.codebook_f32(d, kb)
+    vc, _ = o.codebook_f32(d, vb)
+    kp = np.zeros((nblk, bs, h, o.row_bytes(d, kb)), dtype=np.uint8)
+    vp = np.zeros((nblk, bs, h, o.row_bytes(d, vb)), dtype=np.uint8)
+    for b, n in enumerate(lens):
+        slots = np.array([bt[b, t // bs] * bs + t % bs for t in range(n)])
+        kp = o.write_kv(rng.standard_normal((n, h, d)), kp, slots, signs, kc, kb)
+        vp = o.write_kv(rng.standard_normal((n, h, d)), vp, slots, signs, vc, vb)
+    return dict(d=d, h=h, hq=hq, kb=kb, vb=vb, bs=bs, lens=lens, bt=bt, signs=signs, kc=kc, vc=vc, kp=kp, vp=vp,
+                rng=rng)
+
+
+def test_prefill_rows_equal_per_query_brute_force():
+    # each query row is softmax attention over the dequantised keys up to its position,
+    # computed here directly (dense R built from signs and the Hadamard definition)
+    c = _prefill_case()
+    rng, d, bs = c["rng"], c["d"], c["bs"]
+    # sequence 0: a 3-token chunk at positions 6, 7, 8; sequence 1: 2 tokens at 4, 5; seq 2: decode
+    q_seq = np.array([0, 0, 0, 1, 1, 2])
+    q_len = np.array([7, 8, 9, 5, 6, 1])
+    q = rng.standard_normal((6, c["hq"], d))
+    out = o.paged_prefill(q, q_seq, q_len, c["kp"], c["vp"], c["kb"], c["vb"], c["bt"], c["signs"], c["kc"], c["vc"])
+    rt = (o.hadamard(d) * c["signs"][None, :]).T / math.sqrt(d)  # R^T, R = H diag(s) / sqrt(D)
+    grp = c["hq"] // c["h"]
+    for i in range(6):
+        b, n = q_seq[i], q_len[i]
+        for j in range(c["hq"]):
+            kvh = j // grp
+            keys, vals = [], []
+            for t in range(n):
+                blk, off = c["bt"][b, t // bs], t % bs
+                for pages, bits, cents, dst in ((c["kp"], c["kb"], c["kc"], keys), (c["vp"], c["vb"], c["vc"], vals)):
+                    row = pages[blk, off, kvh]
+                    nb = o.index_bytes(d, bits)
+                    idx = o.unpack_indices(row[None, :nb], d, bits)[0]
+                    nu = float(np.frombuffer(row[nb:nb + 4].tobytes(), dtype="<f4")[0])
+                    dst.append(nu * (rt @ cents.astype(np.float64)[idx]))
+            s = np.array([np.dot(k, q[i, j]) for k in keys]) / math.sqrt(d)
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            want = sum(pi * v for pi, v in zip(p, vals))
+            assert np.allclose(out[i, j], want, rtol=0, atol=1e-12)
+
+
+def test_prefill_is_causal_and_reduces_to_decode():
+    c = _prefill_case(22)
+    rng = c["rng"]
+    q_seq = np.array([0, 0, 1])
+    q_len = np.array([5, 9, 6])
+    q = rng.standard_normal((3, c["hq"], c["d"]))
+    args = (c["kb"], c["vb"], c["bt"], c["signs"], c["kc"], c["vc"])
+    out = o.paged_prefill(q, q_seq, q_len, c["kp"], c["vp"], *args)
+    # tokens past a row's length do not change it: overwrite token 6..8 of sequence 0
+    kp2 = c["kp"].copy()
+    for t in (6, 7, 8):
+        kp2[c["bt"][0, t // c["bs"]], t % c["bs"]] = 0x5A
+    out2 = o.paged_prefill(q, q_seq, q_len, kp2, c["vp"], *args)
+    assert np.array_equal(out[0], out2[0]) and not np.allclose(out[1], out2[1])
+    # one row per sequence at the full length is the decode
+    dec = o.paged_decode(q[[1, 2]], c["kp"], c["vp"], c["kb"], c["vb"], c["bt"][[0, 1]], np.array([9, 6]),
+                         c["signs"], c["kc"], c["vc"])
+    assert np.allclose(out[[1, 2]], dec, rtol=0, atol=1e-13)
