@@ -396,7 +396,9 @@ def run_gpu(args):
             "roofline": dominant, "roofline_decode": roof_dec, "roofline_write": roof_wr,
             "gpu_launches": args.steps * 6, "clocks": clk}
     line["next_rows"] = {"tq_dequant_rows": dequant_measure(tq, w, dev, kp, slots, signs, ck, flush, stream, peak,
-                                                             peak_kind, world)}
+                                                             peak_kind, world),
+                         "tq_paged_prefill": prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream,
+                                                             peak, peak_kind, world)}
 
     if not args.no_e2e:
         line["e2e"] = e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world)
@@ -442,6 +444,52 @@ def dequant_measure(tq, w, dev, kp, slots, signs, ck, flush, stream, peak, peak_
                          "peak_source": peak_kind, "algorithmic_bytes_per_launch": nbytes,
                          "traffic": ncu_traffic("dequant")},
             "gpu_launches": steps + 2}
+
+
+def prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream, peak, peak_kind, world, chunk=16,
+                    steps=5):
+    """Mixed prefill/decode over the workload's cache: a chunk of the last `chunk` tokens of
+    every sequence as query rows (each sees its causal prefix), timed apart from the step."""
+    import numpy as np
+    import torch
+
+    lens = w.seq_lens.astype(np.int64)
+    q_seq = np.repeat(np.arange(w.batch, dtype=np.int32), chunk)
+    q_len = (np.repeat(lens, chunk) - chunk + 1 + np.tile(np.arange(chunk), w.batch)).astype(np.int32)
+    rows = len(q_seq)
+    gen = torch.Generator().manual_seed(7)
+    q = torch.randn(rows, w.num_q_heads, w.head_dim, generator=gen).to(torch.float16).to(dev)
+    dq_seq, dq_len = torch.from_numpy(q_seq).to(dev), torch.from_numpy(q_len).to(dev)
+    out = torch.empty_like(q)
+    need = int(tq.lib().tq_paged_prefill_workspace(rows, w.num_q_heads, w.num_kv_heads, w.head_dim, bt.shape[1],
+                                                  w.block_size))
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(2):
+        tq.tq_paged_prefill(q, dq_seq, dq_len, kp, vp, bt, signs, ck, cv, out=out, workspace=ws, status=st)
+    times = []
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        tq.tq_paged_prefill(q, dq_seq, dq_len, kp, vp, bt, signs, ck, cv, out=out, workspace=ws, status=st)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    tq.raise_for_device_status(st)
+    t_s = max_over_ranks([statistics.mean(times)], world, dev)[0] / 1e3
+    rb = row_bytes(w.head_dim, w.k_bits) + row_bytes(w.head_dim, w.v_bits)
+    unique = int(lens.sum()) * w.num_kv_heads * rb + 2 * rows * w.num_q_heads * w.head_dim * 2
+    streamed = int(q_len.astype(np.int64).sum()) * w.num_kv_heads * rb
+    gbs = unique / t_s / 1e9
+    return {"workload": f"{rows} query rows: the last {chunk} tokens of each of the {w.batch} sequences "
+                        f"(K{w.k_bits}/V{w.v_bits} D{w.head_dim}), each over its causal prefix",
+            "us": t_s * 1e6, "rows_per_s": weak_scaling_rate(world, rows, t_s),
+            "streamed_kv_gbs": streamed / t_s / 1e9, "streamed_kv_bytes": streamed,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": unique,
+                         "traffic": ncu_traffic("prefill")},
+            "gpu_launches": 2 * (steps + 2)}
 
 
 def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5):

@@ -150,6 +150,35 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
                           void* workspace, size_t workspace_bytes, int32_t* status_dev,
                           void* stream);
 
+/* Mixed prefill/decode attention over the packed cache ("vLLM Usage", Runtime Dispatch:
+ * "cache plus mixed prefill/decode" reads the packed cache).
+ *
+ * Query row i (0 <= i < num_q_rows) is one token of sequence q_seq[i] that sees the first
+ * q_len[i] tokens of that sequence (causal: its position + 1; the cache already holds the
+ * new tokens, written by tq_write_kv).  Row i is computed exactly as tq_paged_decode would
+ * compute a one-query sequence with block-table row block_table[q_seq[i]] and length
+ * q_len[i]; a decode batch is the case of one row per sequence at its full length.
+ *
+ *   q            device, q_dtype [num_q_rows][num_q_heads][head_dim]
+ *   block_table  device int32 [num_seqs][max_blocks_per_seq]
+ *   q_seq, q_len device int32 [num_q_rows]
+ *   out          device, out_dtype [num_q_rows][num_q_heads][head_dim]
+ *   workspace    device, >= tq_paged_prefill_workspace(num_q_rows, ...) bytes, 16-byte aligned
+ * Other arguments, the status word and the errors are those of tq_paged_decode; a q_seq
+ * entry outside [0, num_seqs) gives a zero row and TQ_ERR_INVALID_ARG in status_dev.
+ * Rows of one chunk are independent units of the same kernel as the decode: each reads its
+ * own causal prefix of the pages (rows of one sequence are neighbours in the work list, so
+ * their shared blocks tend to be served from L2). */
+size_t tq_paged_prefill_workspace(int num_q_rows, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int max_blocks_per_seq, int block_size);
+tq_status tq_paged_prefill(const void* q, tq_dtype q_dtype, int num_q_rows, int num_q_heads, int num_kv_heads,
+                           int head_dim, const uint8_t* k_pages, int k_bits, const uint8_t* v_pages, int v_bits,
+                           int64_t num_blocks, int block_size, const int32_t* block_table, int num_seqs,
+                           int max_blocks_per_seq, const int32_t* q_seq, const int32_t* q_len, const float* signs,
+                           const float* k_centroids, const float* v_centroids, float scale, void* out,
+                           tq_dtype out_dtype, void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                           void* stream);
+
 /* Dense readback of packed rows: the inverse addressing of tq_write_kv ("vLLM Reference
  * Audit", file map: tq4_decompress, the TQ4 unpack kernel for diagnostic readback of
  * packed index bytes and norms; "Architecture", Diagnostic vs Serving Paths: dense

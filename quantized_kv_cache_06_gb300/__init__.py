@@ -22,6 +22,7 @@ from ._lib import (  # noqa: F401
     tq_paged_decode,
     tq_paged_decode_static,
     tq_paged_decode_workspace,
+    tq_paged_prefill,
     tq_row_bytes,
     tq_write_kv,
 )

@@ -48,6 +48,10 @@ SIGNATURES = {
     "tq_dequant_rows": (_c_int, [_c_p, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_p, _c_i64, _c_p, _c_p, _c_p,
                                  _c_int, _c_p, _c_p]),
     "tq_paged_decode_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tq_paged_prefill_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tq_paged_prefill": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int, _c_i64,
+                                  _c_int, _c_p, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_int,
+                                  _c_p, _c_sz, _c_p, _c_p]),
     "tq_paged_decode": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
                                  _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_int,
                                  _c_p, _c_sz, _c_p, _c_p]),
@@ -264,6 +268,44 @@ def tq_paged_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tenso
                                      _ptr(k_centroids), _ptr(v_centroids), float(scale or 0.0), _ptr(out),
                                      _DTYPES[out.dtype], _ptr(workspace), workspace.numel(), _ptr(status),
                                      _stream(dev)))
+    if check and status is not None:
+        raise_for_device_status(status)
+    return out
+
+
+def tq_paged_prefill(q: torch.Tensor, q_seq: torch.Tensor, q_len: torch.Tensor, k_pages: torch.Tensor,
+                     v_pages: torch.Tensor, block_table: torch.Tensor, signs: torch.Tensor, k_centroids: torch.Tensor,
+                     v_centroids: torch.Tensor, scale: float | None = None, out: torch.Tensor | None = None,
+                     out_dtype: torch.dtype | None = None, workspace: torch.Tensor | None = None,
+                     status: torch.Tensor | None = None, check: bool = False) -> torch.Tensor:
+    """Mixed prefill/decode over the packed pages: row i of q[T, Hq, D] is a query of sequence
+    q_seq[i] that sees that sequence's first q_len[i] tokens (block_table[S, maxblk])."""
+    dev = _need_cuda("tq_paged_prefill", q, q_seq, q_len, k_pages, v_pages, block_table, signs, k_centroids,
+                     v_centroids)
+    if q.dim() != 3 or k_pages.dim() != 4 or v_pages.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("tq_paged_prefill: q [T, Hq, D], pages [NB, bs, H, RB], block_table [S, maxblk] expected")
+    if block_table.dtype != torch.int32 or q_seq.dtype != torch.int32 or q_len.dtype != torch.int32 or \
+            q.dtype not in _DTYPES:
+        raise ValueError("tq_paged_prefill: block_table / q_seq / q_len int32, q f32/f16/bf16 expected")
+    t, hq, d = q.shape
+    nb, bs, h, _ = k_pages.shape
+    kb, vb = _bits_from_centroids(k_centroids), _bits_from_centroids(v_centroids)
+    if k_pages.shape[3] != tq_row_bytes(d, kb) or v_pages.shape[3] != tq_row_bytes(d, vb) or \
+            tuple(v_pages.shape[:3]) != (nb, bs, h) or q_seq.numel() != t or q_len.numel() != t:
+        raise ValueError("tq_paged_prefill: page / row shapes inconsistent with q and the codebooks")
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((t, hq, d), dtype=out_dtype, device=dev)
+    s_rows, maxb = block_table.shape
+    need = int(lib().tq_paged_prefill_workspace(t, hq, h, d, maxb, bs))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_paged_prefill(_ptr(q), _DTYPES[q.dtype], t, hq, h, d, _ptr(k_pages), kb, _ptr(v_pages), vb,
+                                      nb, bs, _ptr(block_table), s_rows, maxb, _ptr(q_seq), _ptr(q_len), _ptr(signs),
+                                      _ptr(k_centroids), _ptr(v_centroids), float(scale or 0.0), _ptr(out),
+                                      _DTYPES[out.dtype], _ptr(workspace), workspace.numel(), _ptr(status),
+                                      _stream(dev)))
     if check and status is not None:
         raise_for_device_status(status)
     return out

@@ -236,6 +236,61 @@ tq::DecodeArgs make_decode_args(int batch, int num_q_heads, int num_kv_heads, in
   return a;
 }
 
+tq_status decode_impl(const char* name, const void* q, tq_dtype q_dtype, int batch, int num_q_heads,
+                          int num_kv_heads, int head_dim, const uint8_t* k_pages, int k_bits,
+                          const uint8_t* v_pages, int v_bits, int64_t num_blocks, int block_size,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, const float* signs, const float* k_centroids,
+                          const float* v_centroids, float scale, void* out, tq_dtype out_dtype,
+                          void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                          void* stream, const int32_t* bt_rows, int bt_num_rows) {
+  tq_status st = decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  if (st != TQ_OK) return st;
+  if (!bits_ok(k_bits) || !bits_ok(v_bits))
+    return fail(TQ_ERR_UNSUPPORTED, "k_bits %d / v_bits %d: must be 2, 3, 4 or 5", k_bits, v_bits);
+  if (!dtype_ok(q_dtype) || !dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "%s: unknown dtype", name);
+  if (num_blocks < 0) return fail(TQ_ERR_INVALID_ARG, "%s: num_blocks < 0", name);
+  if (batch > 0 && (!q || !k_pages || !v_pages || !seq_lens || !signs || !k_centroids || !v_centroids || !out ||
+                    (max_blocks_per_seq > 0 && !block_table)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  if (batch > 0 && (!aligned(q, dtype_size(q_dtype)) || !aligned(out, dtype_size(out_dtype)) ||
+                    !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(block_table, 4) ||
+                    !aligned(seq_lens, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: misaligned pointer (pages need 16-byte alignment)", name);
+  tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  a.q = q;
+  a.q_dtype = (int)q_dtype;
+  a.k_pages = k_pages;
+  a.k_bits = k_bits;
+  a.v_pages = v_pages;
+  a.v_bits = v_bits;
+  a.num_blocks = num_blocks;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.signs = signs;
+  a.k_centroids = k_centroids;
+  a.v_centroids = v_centroids;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = (int)out_dtype;
+  a.workspace = workspace;
+  a.status = status_dev;
+  a.v_alpha = 1.0f;
+  a.k_alpha = 1.0f;
+  a.bt_rows = bt_rows;
+  a.bt_num_rows = bt_num_rows;
+  if (batch > 0 && tq::tc_decode_supported(a)) {
+    a.v_alpha = fp16_scale_for(head_dim, v_bits);
+    a.k_alpha = fp16_scale_for(head_dim, k_bits);
+  }
+  const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());
+  if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: workspace must be >= %zu bytes and 16-byte aligned (got %zu)", name,
+                plan.workspace_bytes, workspace_bytes);
+  return check_cuda(tq::launch_decode(a, plan, static_cast<cudaStream_t>(stream)), name);
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -345,48 +400,31 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
                           const float* v_centroids, float scale, void* out, tq_dtype out_dtype,
                           void* workspace, size_t workspace_bytes, int32_t* status_dev,
                           void* stream) {
-  tq_status st = decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
-  if (st != TQ_OK) return st;
-  if (!bits_ok(k_bits) || !bits_ok(v_bits))
-    return fail(TQ_ERR_UNSUPPORTED, "k_bits %d / v_bits %d: must be 2, 3, 4 or 5", k_bits, v_bits);
-  if (!dtype_ok(q_dtype) || !dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: unknown dtype");
-  if (num_blocks < 0) return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: num_blocks < 0");
-  if (batch > 0 && (!q || !k_pages || !v_pages || !seq_lens || !signs || !k_centroids || !v_centroids || !out ||
-                    (max_blocks_per_seq > 0 && !block_table)))
-    return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: null pointer argument");
-  if (batch > 0 && (!aligned(q, dtype_size(q_dtype)) || !aligned(out, dtype_size(out_dtype)) ||
-                    !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(block_table, 4) ||
-                    !aligned(seq_lens, 4)))
-    return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: misaligned pointer (pages need 16-byte alignment)");
-  tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
-  a.q = q;
-  a.q_dtype = (int)q_dtype;
-  a.k_pages = k_pages;
-  a.k_bits = k_bits;
-  a.v_pages = v_pages;
-  a.v_bits = v_bits;
-  a.num_blocks = num_blocks;
-  a.block_table = block_table;
-  a.seq_lens = seq_lens;
-  a.signs = signs;
-  a.k_centroids = k_centroids;
-  a.v_centroids = v_centroids;
-  a.scale = scale;
-  a.out = out;
-  a.out_dtype = (int)out_dtype;
-  a.workspace = workspace;
-  a.status = status_dev;
-  a.v_alpha = 1.0f;
-  a.k_alpha = 1.0f;
-  if (batch > 0 && tq::tc_decode_supported(a)) {
-    a.v_alpha = fp16_scale_for(head_dim, v_bits);
-    a.k_alpha = fp16_scale_for(head_dim, k_bits);
-  }
-  const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());
-  if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
-    return fail(TQ_ERR_INVALID_ARG, "tq_paged_decode: workspace must be >= %zu bytes and 16-byte aligned (got %zu)",
-                plan.workspace_bytes, workspace_bytes);
-  return check_cuda(tq::launch_decode(a, plan, static_cast<cudaStream_t>(stream)), "tq_paged_decode launch");
+  return decode_impl("tq_paged_decode", q, q_dtype, batch, num_q_heads, num_kv_heads, head_dim, k_pages, k_bits,
+                     v_pages, v_bits, num_blocks, block_size, block_table, max_blocks_per_seq, seq_lens, signs,
+                     k_centroids, v_centroids, scale, out, out_dtype, workspace, workspace_bytes, status_dev, stream,
+                     nullptr, 0);
+}
+
+size_t tq_paged_prefill_workspace(int num_q_rows, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int max_blocks_per_seq, int block_size) {
+  return tq_paged_decode_workspace(num_q_rows, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+}
+
+tq_status tq_paged_prefill(const void* q, tq_dtype q_dtype, int num_q_rows, int num_q_heads, int num_kv_heads,
+                           int head_dim, const uint8_t* k_pages, int k_bits, const uint8_t* v_pages, int v_bits,
+                           int64_t num_blocks, int block_size, const int32_t* block_table, int num_seqs,
+                           int max_blocks_per_seq, const int32_t* q_seq, const int32_t* q_len, const float* signs,
+                           const float* k_centroids, const float* v_centroids, float scale, void* out,
+                           tq_dtype out_dtype, void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                           void* stream) {
+  if (num_seqs < 0) return fail(TQ_ERR_INVALID_ARG, "tq_paged_prefill: num_seqs < 0");
+  if (num_q_rows > 0 && (!q_seq || !q_len || !aligned(q_seq, 4) || !aligned(q_len, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "tq_paged_prefill: q_seq and q_len must be non-null, 4-byte aligned");
+  return decode_impl("tq_paged_prefill", q, q_dtype, num_q_rows, num_q_heads, num_kv_heads, head_dim, k_pages,
+                     k_bits, v_pages, v_bits, num_blocks, block_size, block_table, max_blocks_per_seq, q_len, signs,
+                     k_centroids, v_centroids, scale, out, out_dtype, workspace, workspace_bytes, status_dev, stream,
+                     q_seq, num_seqs);
 }
 
 tq_status tq_paged_decode_static(const void* q, tq_dtype q_dtype, int batch, int num_q_heads,

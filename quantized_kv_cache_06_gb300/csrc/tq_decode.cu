@@ -85,7 +85,7 @@ decode_split_kernel(DecodeArgs a, int num_splits, int blocks_per_split, SplitVie
     len = len < 0 ? 0 : cap;
   }
   const int t_lo = split * blocks_per_split * bs;
-  const int t_hi = min(len, (split + 1) * blocks_per_split * bs);
+  int t_hi = min(len, (split + 1) * blocks_per_split * bs);
 
   const int kib = D * a.k_bits / 8, vib = D * a.v_bits / 8;  // index bytes
   const int64_t krb = kib + 4, vrb = vib + 4;                 // row bytes
@@ -102,8 +102,13 @@ decode_split_kernel(DecodeArgs a, int num_splits, int blocks_per_split, SplitVie
   __syncthreads();
 
   bool bad_block = false;
+  const int bt_row = block_table_row(a, b);
+  if (bt_row < 0) {  // a row map entry outside the table: nothing is read for this row
+    if (threadIdx.x == 0 && a.status) atomicMax(a.status, (int32_t)kInvalidArg);
+    t_hi = t_lo;
+  }
   for (int t = t_lo + warp; t < t_hi; t += kDecodeWarps) {
-    const int bid = __ldg(a.block_table + (int64_t)b * a.max_blocks_per_seq + t / bs);
+    const int bid = __ldg(a.block_table + (int64_t)bt_row * a.max_blocks_per_seq + t / bs);
     if (bid < 0 || (int64_t)bid >= a.num_blocks) {
       bad_block = true;
       continue;

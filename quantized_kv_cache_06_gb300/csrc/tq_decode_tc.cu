@@ -201,6 +201,7 @@ constexpr int kOffL = kOffV2 + 16 * 4;                      // byte K lo table, 
 constexpr int kMiscBytes = (kOffL + 256 * 4 + 127) / 128 * 128;
 
 constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
+constexpr int kNoTableRow = -2;        // block id stand-in for a row map entry outside the table
 // Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored with the fp16-hi key part
 // only.  With the alpha scaling the hi part is within ~1e-4 relative of the fp32
 // centroid, so the score error of such a tile stays far below the output tolerance;
@@ -335,7 +336,9 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       pend_len = __ldg(a.seq_lens + cb);
       pend_m.b = cb;
       pend_m.j = cj;
-      pend_bid = __ldg(a.block_table + (int64_t)cb * a.max_blocks_per_seq + cj);
+      const int bt_row = block_table_row(a, cb);
+      if (bt_row < 0 && a.status) atomicMax(a.status, (int32_t)kInvalidArg);
+      pend_bid = bt_row < 0 ? kNoTableRow : __ldg(a.block_table + (int64_t)bt_row * a.max_blocks_per_seq + cj);
       pend_m.ntok = 1;  // marks a real block until meta_store fills the count
       cursor_advance(WPH);
     }
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       const int len = pend_len < 0 ? 0 : (pend_len > cap ? cap : pend_len);
       m.ntok = min(kBS, len - m.j * kBS);
       m.valid = (pend_bid >= 0 && (int64_t)pend_bid < a.num_blocks);
-      if (!m.valid && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+      if (!m.valid && pend_bid != kNoTableRow && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
       bid = m.valid ? pend_bid : -1;
     }
     meta[slot * WPH + lane] = m;

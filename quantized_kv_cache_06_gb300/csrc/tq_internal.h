@@ -75,7 +75,20 @@ struct DecodeArgs {
   int32_t* status;  // may be null
   float v_alpha;    // fp16 scale of the V centroids (tensor-core decode); 1 when unknown
   float k_alpha;    // fp16 scale of the K centroids (tensor-core decode); 1 when unknown
+  // Mixed prefill/decode: row b of the batch reads block-table row bt_rows[b] (null: row b).
+  // A row outside [0, bt_num_rows) reports kInvalidArg and reads nothing.
+  const int32_t* bt_rows;
+  int bt_num_rows;
 };
+
+#ifdef __CUDACC__
+// Block-table row of batch row b (-1 when the row map points outside the table).
+__device__ __forceinline__ int block_table_row(const DecodeArgs& a, int b) {
+  if (!a.bt_rows) return b;
+  const int r = __ldg(a.bt_rows + b);
+  return (r >= 0 && r < a.bt_num_rows) ? r : -1;
+}
+#endif
 
 // Tensor-core decode (tq_decode_tc.cu): whether the shapes/bits in `a` have an
 // instantiation, its warps per kv head, and its launch.
