@@ -1,0 +1,1050 @@
+// Tensor-core paged decode over packed TurboQuant pages (sm_103a, mma.sync f16 -> f32).
+//
+// TurboQuant docs: "vLLM Usage" (TQ Packed Page Contract: decode_tq4_paged) and
+// "Architecture" (Diagnostic vs Serving Paths: keys consumed compressed, packed-V).
+//
+// Work split.  The blocks of all sequences form one flat list (sequence-major); CTA i
+// of C owns the contiguous range [N*i/C, N*(i+1)/C).  Every CTA is busy for the same
+// number of blocks whatever the length mix, and a CTA emits one split partial per
+// (sequence it touches, warp slot), so the combine pass reads C + B partials at most.
+//
+// Per CTA: WPH warps per kv head (warp w: head w % H, block slot w / H).  A stage holds
+// WPH consecutive blocks; their whole K and V slabs (block_size * H * row_bytes bytes,
+// contiguous in the page tensor) are brought into shared memory by one bulk async copy
+// each, issued by a producer warp (the CTA's last warp, which does no math) and
+// completed on a per-stage "full" mbarrier.  Every consumer warp signals a per-stage
+// "empty" mbarrier when it is done with the stage, and the producer waits on it before
+// it refills the buffers.  No CTA-wide barrier in the main loop.  (A consumer warp that
+// also issues the copies delays them by its own math and serialises copy and compute.)
+//
+// Scores.  For a 16-token tile of one kv head the warp computes S[16 tok x 8 q-heads]
+// = Khat[16 x D] * qrot^T with m16n8k16 MMAs.  The A operand is looked up from the
+// packed bytes: each 2b-bit field (two neighbouring coordinates) indexes a table of
+// (fp16 hi, fp16 lo) centroid pairs, replicated per lane to avoid bank conflicts; the
+// query is split into fp16 hi + lo as well, and hi*hi + lo*hi + hi*lo carries ~22
+// significant bits, so the score keeps fp32-level accuracy even for very large norms.
+// The k order inside a fragment is a fixed permutation of the coordinates; the query
+// fragment follows the same permutation.
+//
+// Values.  Accumulated in rotated space with the contraction over (token, parity):
+// O'[pair][2g + e] += sum_t Vhat[t][2 pair + e] * P'[g][t], so one table entry gives
+// both coordinates of a pair of one token.  V centroids are stored as fp16(alpha * c),
+// alpha chosen on the host so that alpha * c lands near fp16 grid points; 1/alpha is
+// applied when the partial is written.  P' = p * nu_v in fp16.
+//
+// Softmax: online, base 2 (log2 e folded into the query), per q head.  Rows of tokens
+// past the sequence end are masked; blocks with an out-of-range id are skipped and
+// reported through the status word.
+// Tensor-core paged decode kernels, included by tq_decode_tc.cu (plain decode) and
+// tq_prefill_tc.cu (mixed prefill/decode, batch rows mapped to block-table rows): the two
+// instantiation sets compile in parallel.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <type_traits>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kBS = 16;       // tokens per block (the only block size this kernel takes)
+constexpr float kLog2eTc = 1.4426950408889634f;
+
+struct BlockMeta {
+  int b;      // sequence
+  int j;      // block index within the sequence
+  int ntok;   // valid tokens in the block (1..16); 0 = no block in this slot
+  int valid;  // block id inside [0, num_blocks)
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// mbarrier and bulk-copy primitives (shared-window addresses).  Every wait is bounded:
+// after kWaitLimit unsuccessful tries the caller reports kTimeout and stops.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(tx) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `bar` with parity `parity` to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// that completes `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Shared load from an absolute shared-window address.  Not volatile: its address is
+// computed from data read after the stage's wait, which orders it.
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32_off128(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1+128];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld32(const unsigned char* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// 2^x with the hardware approximation (denormal results flush to zero): the softmax
+// weights it produces are relative to the running max, so tiny values do not matter.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D = A * B + D, m16n8k16, A row-major f16, B col-major f16, f32 accumulators.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Split x into fp16 hi + fp16 lo (x ~= hi + lo to ~22 significant bits).
+__device__ __forceinline__ void split_half(float x, __half& hi, __half& lo) {
+  hi = __float2half_rn(x);
+  lo = __float2half_rn(x - __half2float(hi));
+}
+
+template <int D, int KB, int VB, int G, int WPH>
+struct TcCfg {
+  static constexpr int kRBK = D * KB / 8 + 4;          // row bytes
+  static constexpr int kRBV = D * VB / 8 + 4;
+  static constexpr int kWK = D * KB / 32;              // index words per K row
+  static constexpr int kWV = D * VB / 32;
+  static constexpr int kPWK = 16 / KB;                 // pairs per word
+  static constexpr int kPWV = 16 / VB;
+  static constexpr int kKSteps = D / 16;               // score k-steps
+  static constexpr int kMTiles = D / 32;               // value m-tiles
+  static constexpr int kNT = (2 * G + 7) / 8;          // value n-tiles (N = 2G)
+  // Byte-field table T (4-bit indices): 256 entries x 256 bytes, [0, 128) the fp16 hi
+  // parts of the K centroid pairs and [128, 256) the V pairs fp16(alpha c), 32 lane
+  // copies each so lookups are bank conflict free.  T sits at a 64 KB aligned shared
+  // address, so one PRMT of (packed word, T base | lane * 4) yields the absolute
+  // address of an entry.
+  static constexpr bool kHasT = KB == 4 || VB == 4;
+  static constexpr int kTBytes = kHasT ? 256 * 256 : 0;
+  // The small tables (K lo parts of byte fields, read only by tiles that need the exact
+  // score, and the nibble-field tables of 2-bit indices) have one copy each and live in
+  // the fixed part of the shared memory.
+  static_assert(kWK % 4 == 0, "K row must split into 4 interleaved word columns");
+  static_assert(kWV % 8 == 0, "V row must split into 8 interleaved word columns");
+  static_assert(G == 4 || G == 8, "GQA group 4 or 8");
+  static_assert((KB == 2 || KB == 4) && (VB == 2 || VB == 4), "2- or 4-bit indices");
+};
+
+struct TcArgs {
+  DecodeArgs a;
+  int num_ctas;           // C
+  int k_tok_stride;       // smem bytes per token in a K slab (H*RBK + pad)
+  int v_tok_stride;
+  int k_slab_smem;        // bytes of the K part of a block buffer
+  int v_slab_smem;
+  int k_row_copy;         // 1: K copied one token row at a time (padded rows); 0: one slab copy
+  int v_row_copy;
+  float v_alpha;          // V centroid scale
+  float k_alpha;          // K centroid scale
+  int nst;                // pipeline stages (WPH block buffers each), 2..kMaxStages
+  int n_lo;               // block buffers below the T table
+  int buf_lo;             // dynamic-smem offset of buffer 0
+  int buf_hi;             // dynamic-smem offset of buffer n_lo
+  int buf_bytes;          // bytes per block buffer
+  int t_off;              // dynamic-smem offset of T (64 KB aligned shared address)
+  float* part_acc;        // [WPH*(C+B)][Hq][D]
+  float* part_ml;         // [WPH*(C+B)][Hq][2]
+  int* prefix;            // [B+1] block prefix sums (written by CTA 0)
+};
+
+// Fixed part of the dynamic shared memory (offsets from its start).
+constexpr int kMaxStages = 8;
+constexpr int kOffBar = 0;                                  // full[kMaxStages], empty[kMaxStages]
+constexpr int kOffMeta = kOffBar + 2 * kMaxStages * 8;      // BlockMeta[kMaxStages][WPH <= 2]
+constexpr int kOffScan = kOffMeta + kMaxStages * 2 * 16;    // int[36]
+constexpr int kOffK2 = kOffScan + 36 * 4;                   // nibble K table, 16 x 8 bytes
+constexpr int kOffV2 = kOffK2 + 16 * 8;                     // nibble V table, 16 x 4 bytes
+constexpr int kOffL = kOffV2 + 16 * 4;                      // byte K lo table, 256 x 4 bytes
+constexpr int kMiscBytes = (kOffL + 256 * 4 + 127) / 128 * 128;
+
+constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
+constexpr int kNoTableRow = -2;        // block id stand-in for a row map entry outside the table
+// Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored with the fp16-hi key part
+// only.  With the alpha scaling the hi part is within ~1e-4 relative of the fp32
+// centroid, so the score error of such a tile stays far below the output tolerance;
+// tiles above the bound (rows with very large norms) add the fp16-lo part.
+constexpr float kFastScoreBound = 48.0f;
+
+template <int D, int KB, int VB, int G, int WPH, bool ROWMAP>
+__global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
+  using Cfg = TcCfg<D, KB, VB, G, WPH>;
+  const DecodeArgs& a = args.a;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int H = a.num_kv_heads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int ncons = nwarps - 1;  // consumer warps; warp ncons is the producer
+  const int cta = blockIdx.x, C = args.num_ctas;
+  const int B = a.batch;
+  const int cap = a.max_blocks_per_seq * kBS;
+  const int nst = args.nst;
+
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t t_base = smem_base + (uint32_t)args.t_off;
+  if (Cfg::kHasT && (t_base & 0xFFFFu) != 0u) {  // layout computed for another shared window
+    if (tid == 0 && a.status) atomicMax(a.status, (int32_t)kUnsupported);
+    return;
+  }
+  unsigned char* lutT = smem + args.t_off;
+  unsigned char* lutL = smem + kOffL;
+  unsigned char* lutK2 = smem + kOffK2;
+  unsigned char* lutV2 = smem + kOffV2;
+  BlockMeta* meta = reinterpret_cast<BlockMeta*>(smem + kOffMeta);
+  int* scan_tmp = reinterpret_cast<int*>(smem + kOffScan);
+  auto bar_full = [&](int i) -> uint32_t { return smem_base + kOffBar + 8u * i; };
+  auto bar_empty = [&](int i) -> uint32_t { return smem_base + kOffBar + 8u * (kMaxStages + i); };
+  auto buf_off = [&](int slot, int u) -> int {
+    const int idx = slot * WPH + u;
+    return idx < args.n_lo ? args.buf_lo + idx * args.buf_bytes : args.buf_hi + (idx - args.n_lo) * args.buf_bytes;
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), (uint32_t)ncons);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+
+  // ---- flat block list: N, this CTA's range, its first and last sequence ------------
+  auto nblocks_of = [&](int b) -> int {
+    int len = __ldg(a.seq_lens + b);
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    return (len + kBS - 1) / kBS;
+  };
+  int local = 0;
+  bool bad_len = false;
+  for (int b = tid; b < B; b += nthreads) {
+    const int len = __ldg(a.seq_lens + b);
+    bad_len |= (len < 0 || len > cap);
+    local += nblocks_of(b);
+  }
+  if (cta == 0 && a.status && __any_sync(kFullMask, bad_len) && lane == 0) atomicMax(a.status, (int32_t)kInvalidArg);
+  local = (int)__reduce_add_sync(kFullMask, (unsigned)local);
+  if (lane == 0) scan_tmp[warp] = local;
+  __syncthreads();
+  long long N = 0;
+  for (int w = 0; w < nwarps; ++w) N += scan_tmp[w];
+  const long long g_lo = N * cta / C, g_hi = N * (cta + 1) / C;
+  __syncthreads();
+  if (tid == 0) {
+    scan_tmp[32] = -1;
+    scan_tmp[33] = -1;
+    scan_tmp[34] = 0;
+  }
+  int carry = 0;
+  for (int base = 0; base < B; base += nthreads) {
+    const int b = base + tid;
+    const int nb = b < B ? nblocks_of(b) : 0;
+    int incl = nb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += v;
+    }
+    __syncthreads();
+    if (lane == 31) scan_tmp[warp] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      if (w < warp) wbase += scan_tmp[w];
+      total += scan_tmp[w];
+    }
+    const int excl = carry + wbase + incl - nb;
+    if (b < B) {
+      if (cta == 0) args.prefix[b] = excl;
+      if (nb > 0 && excl <= g_lo && g_lo < excl + nb) {
+        scan_tmp[32] = b;
+        scan_tmp[34] = (int)(g_lo - excl);
+      }
+      if (nb > 0 && excl <= g_hi - 1 && g_hi - 1 < excl + nb) scan_tmp[33] = b;
+    }
+    carry += total;
+  }
+  if (cta == 0 && tid == 0) args.prefix[B] = carry;
+  __syncthreads();  // also: barriers initialised
+  if (g_lo >= g_hi) return;  // nothing to do (uniform; no copy was issued)
+  const int b_first = scan_tmp[32], b_last = scan_tmp[33], j_first = scan_tmp[34];
+  const int nstages = (int)((g_hi - g_lo + WPH - 1) / WPH);
+
+  // ---- producer state: block cursor of lane u < WPH, blocks g_lo + WPH*st + u ---------
+  int cb = b_first, cj = j_first, cnb = nblocks_of(b_first);
+  long long cg = g_lo;
+  auto cursor_advance = [&](int steps) {
+    cg += steps;
+    cj += steps;
+    while (cg < g_hi && cj >= cnb) {
+      cj -= cnb;
+      ++cb;
+      cnb = nblocks_of(cb);
+    }
+  };
+  const bool producer = warp == ncons;
+  if (producer && lane < WPH) cursor_advance(lane);
+  // The metadata of a stage is loaded (global reads in flight) one stage before it is
+  // stored, so the producer does not wait on those reads when it issues the copies.
+  BlockMeta pend_m{0, 0, 0, 0};
+  int pend_len = 0, pend_bid = -1;
+  auto meta_load = [&]() {  // producer lanes < WPH: the next stage of this lane's cursor
+    pend_m = BlockMeta{0, 0, 0, 0};
+    pend_bid = -1;
+    pend_len = 0;
+    if (cg < g_hi) {
+      pend_len = __ldg(a.seq_lens + cb);
+      pend_m.b = cb;
+      pend_m.j = cj;
+      if (ROWMAP) {  // mixed prefill/decode: batch row cb reads table row bt_rows[cb]
+        const int bt_row = block_table_row(a, cb);
+        if (bt_row < 0 && a.status) atomicMax(a.status, (int32_t)kInvalidArg);
+        pend_bid = bt_row < 0 ? kNoTableRow : __ldg(a.block_table + (int64_t)bt_row * a.max_blocks_per_seq + cj);
+      } else {
+        pend_bid = __ldg(a.block_table + (int64_t)cb * a.max_blocks_per_seq + cj);
+      }
+      pend_m.ntok = 1;  // marks a real block until meta_store fills the count
+      cursor_advance(WPH);
+    }
+  };
+  // Stores the pending metadata into ring slot `slot`; returns the block id to copy (-1: none).
+  auto meta_store = [&](int slot) -> int {
+    BlockMeta m = pend_m;
+    int bid = -1;
+    if (m.ntok) {
+      const int len = pend_len < 0 ? 0 : (pend_len > cap ? cap : pend_len);
+      m.ntok = min(kBS, len - m.j * kBS);
+      m.valid = (pend_bid >= 0 && (int64_t)pend_bid < a.num_blocks);
+      if (!m.valid && (!ROWMAP || pend_bid != kNoTableRow) && a.status)
+        atomicMax(a.status, (int32_t)kBlockOutOfRange);
+      bid = m.valid ? pend_bid : -1;
+    }
+    meta[slot * WPH + lane] = m;
+    return bid;
+  };
+
+  // ---- copies -------------------------------------------------------------------------
+  const int kraw = H * Cfg::kRBK, vraw = H * Cfg::kRBV;
+  const int k_slab = kBS * kraw, v_slab = kBS * vraw;
+  const uint32_t blk_tx = (uint32_t)(k_slab + v_slab);
+  // Producer step (all lanes of the producer): metadata of the next stage into ring slot `slot`, then
+  // the copies of its valid blocks on full[slot].  The caller has made sure the slot's
+  // buffers are free.
+  auto produce = [&](int slot) {
+    int bid = -1;
+    if (lane < WPH) {
+      bid = meta_store(slot);
+      meta_load();
+    }
+    __syncwarp();
+    int bids[WPH];
+    uint32_t tx = 0;
+#pragma unroll
+    for (int u = 0; u < WPH; ++u) {
+      bids[u] = __shfl_sync(kFullMask, bid, u);
+      if (bids[u] >= 0) tx += blk_tx;
+    }
+    if (lane == 0) mbar_arrive_expect_tx(bar_full(slot), tx);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < WPH; ++u) {
+      if (bids[u] < 0) continue;
+      const unsigned char* ksrc = a.k_pages + (int64_t)bids[u] * k_slab;
+      const unsigned char* vsrc = a.v_pages + (int64_t)bids[u] * v_slab;
+      const uint32_t kdst = smem_base + (uint32_t)buf_off(slot, u);
+      const uint32_t vdst = kdst + (uint32_t)args.k_slab_smem;
+      if (lane < 16) {
+        if (args.k_row_copy)
+          bulk_g2s(kdst + lane * args.k_tok_stride, ksrc + lane * kraw, (uint32_t)kraw, bar_full(slot));
+        else if (lane == 0)
+          bulk_g2s(kdst, ksrc, (uint32_t)k_slab, bar_full(slot));
+      } else {
+        const int t = lane - 16;
+        if (args.v_row_copy)
+          bulk_g2s(vdst + t * args.v_tok_stride, vsrc + t * vraw, (uint32_t)vraw, bar_full(slot));
+        else if (t == 0)
+          bulk_g2s(vdst, vsrc, (uint32_t)v_slab, bar_full(slot));
+      }
+    }
+  };
+
+  // ---- consumer state ----------------------------------------------------------------
+  const int h = warp;  // consumer warp h: kv head h of every block
+  const int r = lane >> 2, c = lane & 3;
+  const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
+  const float qmul = scale * kLog2eTc / sqrtf((float)D);
+  const float inv_alpha_k = 1.0f / args.k_alpha;
+  const int kts = args.k_tok_stride, vts = args.v_tok_stride;
+  const uint32_t t_lane = t_base | (uint32_t)(lane * 4);  // T base (bits 16-31) | lane copy
+  // value-B selectors: the P value goes to the low half when (r & 1) == 0, else the high half
+  const int hsel = (r >> 1) & 1;
+  const uint32_t sel_b = (r & 1) ? (0x0044u | ((2u * hsel) << 8) | ((2u * hsel + 1u) << 12))
+                                 : ((2u * hsel) | ((2u * hsel + 1u) << 4) | 0x4400u);
+
+  // Table lookups for field e of word w.  4-bit fields: one PRMT places byte e of w at
+  // bits 8-15 of (T base | lane * 4), the absolute address of this lane's copy.
+  auto t_addr = [&](uint32_t w, int e) -> uint32_t { return __byte_perm(w, t_lane, 0x7604u | ((uint32_t)e << 4)); };
+  auto k_hi = [&](uint32_t w, int e) -> uint32_t {
+    if (KB == 4) return lds32(t_addr(w, e));
+    return ld32(lutK2 + (((w >> (4 * e)) & 15u) << 3));
+  };
+  auto k_lo = [&](uint32_t w, int e) -> uint32_t {
+    if (KB == 4) return ld32(lutL + (((w >> (8 * e)) & 255u) << 2));
+    return ld32(lutK2 + (((w >> (4 * e)) & 15u) << 3) + 4);
+  };
+  auto v_lookup = [&](uint32_t w, int e) -> uint32_t {
+    if (VB == 4) return lds32_off128(t_addr(w, e));
+    return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 2));
+  };
+
+  // Query B fragments.  G = 4: one set whose columns 0-3 hold the fp16 hi part of the
+  // rotated query and columns 4-7 (the unused half of the n = 8 MMA) its fp16 lo part,
+  // so one MMA yields both products.  G = 8: separate hi and lo sets.
+  constexpr int kQSets = G == 4 ? 1 : 2;
+  uint32_t bq[kQSets][Cfg::kKSteps][2];
+  float qnorm_max = 0.f;  // max over this warp's heads of ||rotated query|| (log2 units)
+  float o_acc[Cfg::kNT][Cfg::kMTiles][4];
+  float m_run[2], l_run[2], m_thr[2];  // running max, sum, and max + kRescaleSlack per head
+  int cur_b = -1;
+
+  auto reset_state = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < Cfg::kNT; ++nt)
+#pragma unroll
+      for (int i = 0; i < Cfg::kMTiles; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o_acc[nt][i][e] = 0.f;
+    m_run[0] = m_run[1] = m_thr[0] = m_thr[1] = -INFINITY;
+    l_run[0] = l_run[1] = 0.f;
+  };
+
+  // Rotated query of sequence b for this warp's G heads -> hi/lo B fragments.
+  auto load_query = [&](int b) {
+    constexpr int E = D / 32;
+    float qr[G][E];
+    qnorm_max = 0.f;
+    // all G*E loads of this lane in flight at once (one dtype branch outside the loops)
+    const int64_t base = ((int64_t)b * a.num_q_heads + (int64_t)h * G) * D + lane * E;
+    if (a.q_dtype == kF16) {
+      const __half* q16 = static_cast<const __half*>(a.q) + base;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < E; ++i) qr[g][i] = __half2float(q16[g * D + i]);
+    } else if (a.q_dtype == kBF16) {
+      const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) + base;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < E; ++i) qr[g][i] = __bfloat162float(qb[g * D + i]);
+    } else {
+      const float* qf = static_cast<const float*>(a.q) + base;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < E; ++i) qr[g][i] = __ldg(qf + g * D + i);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int i = 0; i < E; ++i) qr[g][i] *= __ldg(a.signs + lane * E + i);
+      fwht_warp<E>(qr[g]);
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        qr[g][i] *= qmul;
+        ss = fmaf(qr[g][i], qr[g][i], ss);
+        qr[g][i] *= inv_alpha_k;  // the K tables hold alpha * c
+      }
+      qnorm_max = fmaxf(qnorm_max, sqrtf(warp_sum(ss)));
+    }
+    const int gq = G == 4 ? (r & 3) : r;  // this lane's B column -> q head
+#pragma unroll
+    for (int s = 0; s < Cfg::kKSteps; ++s) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = 2 * s + u;
+        const int jw = q / Cfg::kPWK, e = q % Cfg::kPWK;
+        const int p = Cfg::kPWK * (c + 4 * jw) + e;  // pair index; coordinates 2p, 2p+1
+        const int src = (2 * p) / E;
+        const int off = (2 * p) % E;  // identical on every lane (see the pair layout)
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float v0 = __shfl_sync(kFullMask, qr[g][off], src);
+          const float v1 = __shfl_sync(kFullMask, qr[g][(off + 1) % E], E == 1 ? src + 1 : src);
+          if (g == gq) {
+            x0 = v0;
+            x1 = v1;
+          }
+        }
+        __half h0, l0, h1, l1;
+        split_half(x0, h0, l0);
+        split_half(x1, h1, l1);
+        __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
+        if (G == 4) {
+          bq[0][s][u] = r < 4 ? *reinterpret_cast<uint32_t*>(&hh) : *reinterpret_cast<uint32_t*>(&ll);
+        } else {
+          bq[0][s][u] = *reinterpret_cast<uint32_t*>(&hh);
+          bq[kQSets - 1][s][u] = *reinterpret_cast<uint32_t*>(&ll);
+        }
+      }
+    }
+  };
+
+  const float inv_alpha = 1.0f / args.v_alpha;
+  // Writes this warp's partial for sequence b (empty when `empty`).
+  auto flush = [&](int b, bool empty) {
+    const int64_t slot = (int64_t)cta + b;
+    float lsum[2] = {l_run[0], l_run[1]};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 4);
+      lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 8);
+      lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 16);
+    }
+    if (r == 0) {  // score layout: lane (r, c) holds q heads 2c, 2c+1
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int g = 2 * c + e;
+        if (g < G) {
+          float* ml = args.part_ml + (slot * a.num_q_heads + (int64_t)h * G + g) * 2;
+          ml[0] = empty ? -INFINITY : m_run[e];
+          ml[1] = empty ? 0.f : lsum[e];
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < Cfg::kNT; ++nt) {  // value layout: q head c + 4 nt
+      const int g = c + 4 * nt;
+      if (g < G) {
+        float* acc = args.part_acc + (slot * a.num_q_heads + (int64_t)h * G + g) * D;
+#pragma unroll
+        for (int i = 0; i < Cfg::kMTiles; ++i) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int q = 2 * i + half;
+            const int pv = Cfg::kPWV * (r + 8 * (q / Cfg::kPWV)) + (q % Cfg::kPWV);
+            float2 v;
+            v.x = empty ? 0.f : o_acc[nt][i][2 * half] * inv_alpha;
+            v.y = empty ? 0.f : o_acc[nt][i][2 * half + 1] * inv_alpha;
+            *reinterpret_cast<float2*>(acc + 2 * pv) = v;
+          }
+        }
+      }
+    }
+  };
+
+  // Move this warp to sequence b: close the current one and any non-empty sequences
+  // of this CTA in between (they get empty partials), then load b's query.
+  auto enter_sequence = [&](int b) {
+    const int from = cur_b;
+    if (from >= 0) flush(from, false);
+    for (int x = (from < 0 ? b_first : from + 1); x < b; ++x)
+      if (nblocks_of(x) > 0) flush(x, true);
+    reset_state();
+    cur_b = b;
+    load_query(b);
+  };
+
+  // NTL (1 or 2) consecutive 16-token tiles of this warp's kv head in one sequence:
+  // scores, one joint online-softmax update, values.  Only the last tile may be partial
+  // (ntok_last tokens).  Two tiles give two independent lookup/MMA chains per phase.
+  auto tiles = [&](auto ntl_tag, const unsigned char* kblk0, const unsigned char* kblk1, int ntok_last) {
+    constexpr int NTL = decltype(ntl_tag)::value;
+    const unsigned char* kbase[NTL];
+    const unsigned char* vbase[NTL];
+    kbase[0] = kblk0 + h * Cfg::kRBK;
+    if (NTL == 2) kbase[NTL - 1] = kblk1 + h * Cfg::kRBK;
+    float kn[NTL][2], vn[NTL][2];
+    float kmax = 0.f;
+#pragma unroll
+    for (int t = 0; t < NTL; ++t) {
+      vbase[t] = kbase[t] - h * Cfg::kRBK + args.k_slab_smem + h * Cfg::kRBV;
+      kn[t][0] = __uint_as_float(ld32(kbase[t] + r * kts + Cfg::kWK * 4));
+      kn[t][1] = __uint_as_float(ld32(kbase[t] + (r + 8) * kts + Cfg::kWK * 4));
+      vn[t][0] = __uint_as_float(ld32(vbase[t] + r * vts + Cfg::kWV * 4));
+      vn[t][1] = __uint_as_float(ld32(vbase[t] + (r + 8) * vts + Cfg::kWV * 4));
+      kmax = fmaxf(kmax, fmaxf(fabsf(kn[t][0]), fabsf(kn[t][1])));
+    }
+    // Precision switch: tiles whose largest |score| bound nu_k * ||q|| stays within
+    // kFastScoreBound take the fp16-hi key path (rounding error ~1e-4 relative after the
+    // alpha scaling); otherwise (large-norm rows) the fp16-lo key part is added as well.
+    // Rows past the sequence end hold stale bytes: at worst they select the exact path,
+    // which is correct for any tile.
+    const bool exact = __any_sync(kFullMask, kmax * qnorm_max > kFastScoreBound);
+    float sacc[NTL][4];
+#pragma unroll
+    for (int t = 0; t < NTL; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[t][e] = 0.f;
+    if (!exact) {
+      // G = 4: columns 0-3 get key_hi * q_hi, 4-7 key_hi * q_lo; one tile runs its even and
+      // odd k-steps as two chains.  G = 8: a q_lo chain per tile.
+      float sacc1[NTL][4];
+#pragma unroll
+      for (int t = 0; t < NTL; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc1[t][e] = 0.f;
+#pragma unroll
+      for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
+        uint32_t w0[NTL], w1[NTL];
+#pragma unroll
+        for (int t = 0; t < NTL; ++t) {
+          w0[t] = ld32(kbase[t] + r * kts + (c + 4 * jw) * 4);
+          w1[t] = ld32(kbase[t] + (r + 8) * kts + (c + 4 * jw) * 4);
+        }
+#pragma unroll
+        for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
+          const int s = (jw * Cfg::kPWK + e2) >> 1;
+#pragma unroll
+          for (int t = 0; t < NTL; ++t) {
+            const uint32_t h00 = k_hi(w0[t], e2), h10 = k_hi(w1[t], e2);
+            const uint32_t h01 = k_hi(w0[t], e2 + 1), h11 = k_hi(w1[t], e2 + 1);
+            if (G == 8) {
+              mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+              mma16816(sacc1[t], h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+            } else {
+              mma16816((NTL == 1 && (s & 1)) ? sacc1[t] : sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < NTL; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[t][e] += sacc1[t][e];
+    } else {
+      // adds key_lo * q_hi (G = 4: key_lo * [q_hi | q_lo])
+#pragma unroll
+      for (int t = 0; t < NTL; ++t) {
+        float sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
+          const uint32_t w0 = ld32(kbase[t] + r * kts + (c + 4 * jw) * 4);
+          const uint32_t w1 = ld32(kbase[t] + (r + 8) * kts + (c + 4 * jw) * 4);
+#pragma unroll
+          for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
+            const int s = (jw * Cfg::kPWK + e2) >> 1;
+            const uint32_t h00 = k_hi(w0, e2), h10 = k_hi(w1, e2), h01 = k_hi(w0, e2 + 1), h11 = k_hi(w1, e2 + 1);
+            const uint32_t l00 = k_lo(w0, e2), l10 = k_lo(w1, e2), l01 = k_lo(w0, e2 + 1), l11 = k_lo(w1, e2 + 1);
+            mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+            if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+            mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[t][e] += sacc1[e] + sacc2[e];
+      }
+    }
+    float sc[NTL][4];
+#pragma unroll
+    for (int t = 0; t < NTL; ++t) {
+      if (G == 4) {
+        // fold the q_lo columns (lanes c = 2, 3) onto the q_hi columns (lanes c = 0, 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[t][e] += __shfl_xor_sync(kFullMask, sacc[t][e], 2);
+      }
+      sc[t][0] = sacc[t][0] * kn[t][0];
+      sc[t][1] = sacc[t][1] * kn[t][0];
+      sc[t][2] = sacc[t][2] * kn[t][1];
+      sc[t][3] = sacc[t][3] * kn[t][1];
+    }
+    if (ntok_last < kBS) {  // last block of a sequence: mask the rows past its end
+      if (r >= ntok_last) sc[NTL - 1][0] = sc[NTL - 1][1] = -INFINITY;
+      if (r + 8 >= ntok_last) sc[NTL - 1][2] = sc[NTL - 1][3] = -INFINITY;
+    }
+
+    // --- online softmax (q heads 2c, 2c+1 on this lane).  The running max only moves
+    // when a score passes it by more than kRescaleSlack, so p = 2^(s - m) <= 2^slack.
+    // Most tiles move no max: one compare per score and a vote replace the reduction.
+    float smax[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      smax[e] = fmaxf(sc[0][e], sc[0][2 + e]);
+#pragma unroll
+      for (int t = 1; t < NTL; ++t) smax[e] = fmaxf(smax[e], fmaxf(sc[t][e], sc[t][2 + e]));
+    }
+    if (__any_sync(kFullMask, smax[0] > m_thr[0] || smax[1] > m_thr[1])) {
+      float corr[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mt = smax[e];
+        mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
+        const float mn = mt > m_thr[e] ? mt : m_run[e];
+        corr[e] = fast_exp2(m_run[e] - mn);
+        l_run[e] *= corr[e];
+        m_run[e] = mn;
+        m_thr[e] = mn + kRescaleSlack;
+      }
+#pragma unroll
+      for (int nt = 0; nt < Cfg::kNT; ++nt) {  // value layout holds q head c + 4 nt
+        const int g = c + 4 * nt;
+        const int srcl = (g >> 1) & 3;  // lane (r'=0, c'=g>>1)
+        const float c0 = __shfl_sync(kFullMask, corr[0], srcl);
+        const float c1 = __shfl_sync(kFullMask, corr[1], srcl);
+        const float cg = (g & 1) ? c1 : c0;
+#pragma unroll
+        for (int i = 0; i < Cfg::kMTiles; ++i)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o_acc[nt][i][e] *= cg;
+      }
+    }
+    uint32_t p01[NTL], p23[NTL];
+#pragma unroll
+    for (int t = 0; t < NTL; ++t) {
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float p0 = fast_exp2(sc[t][e] - m_run[e]), p1 = fast_exp2(sc[t][2 + e] - m_run[e]);
+        l_run[e] += p0 + p1;
+        pv[e] = p0 * vn[t][0];
+        pv[2 + e] = p1 * vn[t][1];
+      }
+      p01[t] = pack_half2(pv[0], pv[1]);  // token r:   heads 2c, 2c+1
+      p23[t] = pack_half2(pv[2], pv[3]);  // token r+8: heads 2c, 2c+1
+    }
+
+    // --- values ------------------------------------------------------------------------
+#pragma unroll
+    for (int t = 0; t < NTL; ++t) {
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {  // tokens {c, c+4} (ks=0) and {c+8, c+12} (ks=1)
+        const int t0 = c + 8 * ks, t1 = c + 4 + 8 * ks;
+        uint32_t bv[Cfg::kNT][2];
+#pragma unroll
+        for (int nt = 0; nt < Cfg::kNT; ++nt) {
+          const int cs = 2 * nt + (r >> 2);  // source lane column: q head (4 nt + r/2) / 2
+          const uint32_t src = ks == 0 ? p01[t] : p23[t];
+          const uint32_t x0 = __shfl_sync(kFullMask, src, 4 * c + cs);
+          const uint32_t x1 = __shfl_sync(kFullMask, src, 4 * (c + 4) + cs);
+          bv[nt][0] = __byte_perm(x0, 0u, sel_b);
+          bv[nt][1] = __byte_perm(x1, 0u, sel_b);
+        }
+#pragma unroll
+        for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
+          const uint32_t wa = ld32(vbase[t] + t0 * vts + (r + 8 * jw) * 4);
+          const uint32_t wb = ld32(vbase[t] + t1 * vts + (r + 8 * jw) * 4);
+#pragma unroll
+          for (int e = 0; e < Cfg::kPWV; e += 2) {
+            const int i = (jw * Cfg::kPWV + e) >> 1;  // m-tile: pairs q = 2i (row r), 2i+1 (row r+8)
+            const uint32_t a0 = v_lookup(wa, e), a1 = v_lookup(wa, e + 1);
+            const uint32_t a2 = v_lookup(wb, e), a3 = v_lookup(wb, e + 1);
+#pragma unroll
+            for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+          }
+        }
+      }
+    }
+  };
+  using One = std::integral_constant<int, 1>;
+  using Two = std::integral_constant<int, 2>;
+
+  // ---- main pipeline -----------------------------------------------------------------
+  // Stage st lives in ring slot st % nst; full[slot] completes when its copies landed,
+  // empty[slot] when every consumer warp is done with it.
+  if (producer) {
+    int S = 0;
+    for (; S < nstages; ++S) {
+      const int ps = S % nst;
+      if (S >= nst && !mbar_wait(bar_empty(ps), (uint32_t)(((S / nst) - 1) & 1))) break;
+      if (S == 0 && lane < WPH) meta_load();
+      produce(ps);
+    }
+    if (S < nstages && lane == 0 && a.status) atomicMax(a.status, (int32_t)kTimeout);
+    // let this CTA's copies land before the producer leaves (the consumers normally
+    // have already waited for all of them)
+    for (int s2 = (S > nst ? S - nst : 0); s2 < S; ++s2) mbar_wait(bar_full(s2 % nst), (uint32_t)((s2 / nst) & 1));
+    return;
+  }
+  {
+      // ---- tables (consumer warps; the producer is already streaming) ------------------
+    if (KB == 4) {
+      for (int i = tid; i < 256 * 32; i += 32 * ncons) {
+        const int f = i >> 5, copy = i & 31;
+        __half ha, la, hb, lb;
+        split_half(__ldg(a.k_centroids + (f & 15)) * args.k_alpha, ha, la);
+        split_half(__ldg(a.k_centroids + (f >> 4)) * args.k_alpha, hb, lb);
+        __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
+        *reinterpret_cast<uint32_t*>(lutT + f * 256 + copy * 4) = *reinterpret_cast<uint32_t*>(&hi2);
+        if (copy == 0) *reinterpret_cast<uint32_t*>(lutL + f * 4) = *reinterpret_cast<uint32_t*>(&lo2);
+      }
+    } else {
+      for (int f = tid; f < 16; f += 32 * ncons) {
+        __half ha, la, hb, lb;
+        split_half(__ldg(a.k_centroids + (f & 3)) * args.k_alpha, ha, la);
+        split_half(__ldg(a.k_centroids + (f >> 2)) * args.k_alpha, hb, lb);
+        __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t*>(&hi2);
+        v.y = *reinterpret_cast<uint32_t*>(&lo2);
+        *reinterpret_cast<uint2*>(lutK2 + f * 8) = v;
+      }
+    }
+    if (VB == 4) {
+      for (int i = tid; i < 256 * 32; i += 32 * ncons) {
+        const int f = i >> 5, copy = i & 31;
+        const float ca = __ldg(a.v_centroids + (f & 15)) * args.v_alpha;
+        const float cb = __ldg(a.v_centroids + (f >> 4)) * args.v_alpha;
+        *reinterpret_cast<uint32_t*>(lutT + f * 256 + 128 + copy * 4) = pack_half2(ca, cb);
+      }
+    } else {
+      for (int f = tid; f < 16; f += 32 * ncons) {
+        const float ca = __ldg(a.v_centroids + (f & 3)) * args.v_alpha;
+        const float cb = __ldg(a.v_centroids + (f >> 2)) * args.v_alpha;
+        *reinterpret_cast<uint32_t*>(lutV2 + f * 4) = pack_half2(ca, cb);
+      }
+    }
+  asm volatile("bar.sync 1, %0;\n" ::"r"(32 * ncons) : "memory");  // consumer warps only
+  }
+  // the first block belongs to b_first: its query is read while the first copies land
+  reset_state();
+  cur_b = b_first;
+  load_query(b_first);
+  int slot = 0;
+  uint32_t par = 0;
+  for (int st = 0; st < nstages; ++st) {
+    if (!mbar_wait(bar_full(slot), par)) {
+      if (lane == 0 && a.status) atomicMax(a.status, (int32_t)kTimeout);
+      return;
+    }
+    const BlockMeta m0 = meta[slot * WPH];
+    const BlockMeta m1 = meta[slot * WPH + WPH - 1];
+    if (WPH == 2 && m0.ntok == kBS && m0.valid && m1.ntok != 0 && m1.valid && m1.b == m0.b) {
+      if (m0.b != cur_b) enter_sequence(m0.b);
+      tiles(Two{}, smem + buf_off(slot, 0), smem + buf_off(slot, 1), m1.ntok);
+    } else {
+#pragma unroll
+      for (int u = 0; u < WPH; ++u) {
+        const BlockMeta m = u == 0 ? m0 : m1;
+        if (m.ntok != 0) {
+          if (m.b != cur_b) enter_sequence(m.b);
+          if (m.valid) tiles(One{}, smem + buf_off(slot, u), nullptr, m.ntok);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty(slot));
+    if (++slot == nst) {
+      slot = 0;
+      par ^= 1u;
+    }
+  }
+  // close the last sequence and any later non-empty ones this CTA owns
+  if (cur_b < 0) {
+    for (int x = b_first; x <= b_last; ++x)
+      if (nblocks_of(x) > 0) flush(x, true);
+  } else {
+    flush(cur_b, false);
+    for (int x = cur_b + 1; x <= b_last; ++x)
+      if (nblocks_of(x) > 0) flush(x, true);
+  }
+}
+
+// One warp per (sequence, q head): merge the partials of the CTAs that touched the
+// sequence, normalise, apply R^T (FWHT + sign flip) and store.  The (m, l) and the
+// accumulator of up to kCombineBatch partials are loaded together (one round trip);
+// longer spans loop over batches with a running rescale.
+constexpr int kCombineBatch = 4;
+
+template <int E>
+__global__ void __launch_bounds__(256)
+combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc, const float* __restrict__ part_ml,
+                  const int* __restrict__ prefix) {
+  constexpr int D = 32 * E;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= a.batch * a.num_q_heads) return;
+  const int b = row / a.num_q_heads, j = row - b * a.num_q_heads;
+  const long long N = prefix[a.batch];
+  const long long p0 = prefix[b], p1 = prefix[b + 1];
+  float v[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) v[i] = 0.f;
+  if (p1 > p0) {
+    const long long C = num_ctas;
+    const long long f = ((p0 + 1) * C - 1) / N, l = (p1 * C - 1) / N;  // first / last CTA
+    float mx = -INFINITY, lsum = 0.f;
+    for (long long i0 = f; i0 <= l; i0 += kCombineBatch) {
+      float ms[kCombineBatch], ls[kCombineBatch], acc[kCombineBatch][E];
+#pragma unroll
+      for (int u = 0; u < kCombineBatch; ++u) {
+        const long long i = i0 + u;
+        // CTAs past l, and CTAs whose block range is empty (possible when N < C), wrote nothing
+        const bool live = i <= l && N * i / C < N * (i + 1) / C;
+        const int64_t s = (i + b) * a.num_q_heads + j;
+        ms[u] = live ? part_ml[s * 2] : -INFINITY;
+        ls[u] = live ? part_ml[s * 2 + 1] : 0.f;
+#pragma unroll
+        for (int k = 0; k < E; ++k) acc[u][k] = live ? part_acc[s * D + lane * E + k] : 0.f;
+      }
+      float bm = mx;
+#pragma unroll
+      for (int u = 0; u < kCombineBatch; ++u) bm = fmaxf(bm, ms[u]);
+      const float cr = mx == -INFINITY ? 0.f : exp2f(mx - bm);  // rescale of what came before
+      lsum *= cr;
+#pragma unroll
+      for (int k = 0; k < E; ++k) v[k] *= cr;
+#pragma unroll
+      for (int u = 0; u < kCombineBatch; ++u) {
+        const float w = ms[u] == -INFINITY ? 0.f : exp2f(ms[u] - bm);
+        lsum = fmaf(w, ls[u], lsum);
+#pragma unroll
+        for (int k = 0; k < E; ++k) v[k] = fmaf(w, acc[u][k], v[k]);
+      }
+      mx = bm;
+    }
+    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+#pragma unroll
+    for (int k = 0; k < E; ++k) v[k] *= inv;
+  }
+  fwht_warp<E>(v);
+  const float rs = 1.0f / sqrtf((float)D);
+#pragma unroll
+  for (int k = 0; k < E; ++k)
+    store_from_f32(a.out, (int64_t)row * D + lane * E + k, a.out_dtype, v[k] * __ldg(a.signs + lane * E + k) * rs);
+}
+
+template <int D, int KB, int VB, int G, int WPH, bool ROWMAP>
+cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
+  using Cfg = TcCfg<D, KB, VB, G, WPH>;
+  TcArgs t{};
+  t.a = a;
+  t.num_ctas = p.num_splits;
+  const int H = a.num_kv_heads;
+  const int kraw = H * Cfg::kRBK, vraw = H * Cfg::kRBV;
+  // Each K and V slab arrives as one bulk copy, unpadded.  (Per-token row copies would
+  // allow padded, conflict-free strides, but many small bulk copies do not keep enough
+  // bytes in flight; for 8 heads of 128 4-bit coordinates the unpadded K stride costs a
+  // 2-way conflict on the 8 index-word loads of a tile, the V stride none.)
+  t.k_row_copy = 0;
+  t.v_row_copy = 0;
+  t.k_tok_stride = kraw;
+  t.v_tok_stride = vraw;
+  t.k_slab_smem = (kBS * t.k_tok_stride + 15) / 16 * 16;
+  t.v_slab_smem = (kBS * t.v_tok_stride + 15) / 16 * 16;
+  t.v_alpha = a.v_alpha > 0.f ? a.v_alpha : 1.0f;
+  t.k_alpha = a.k_alpha > 0.f ? a.k_alpha : 1.0f;
+
+  // Shared-memory layout: [misc | buffers ... | T (64 KB, at a 64 KB aligned shared
+  // address) | buffers ...].  Dynamic shared memory starts right after the per-block
+  // reserved bytes in the shared window (the kernel checks the T alignment it gets).
+  int dev = 0, reserved = 0, max_dyn = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&max_dyn, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  t.buf_bytes = (t.k_slab_smem + t.v_slab_smem + 127) / 128 * 128;
+  int total_bufs = 0;
+  t.buf_lo = kMiscBytes;
+  if (Cfg::kHasT) {
+    int t_off = (65536 - reserved % 65536) % 65536;
+    while (t_off < kMiscBytes) t_off += 65536;
+    t.t_off = t_off;
+    t.n_lo = (t_off - kMiscBytes) / t.buf_bytes;
+    t.buf_hi = t_off + Cfg::kTBytes;
+    total_bufs = t.n_lo + std::max(0, (max_dyn - t.buf_hi) / t.buf_bytes);
+  } else {
+    t.t_off = 0;
+    t.n_lo = (max_dyn - kMiscBytes) / t.buf_bytes;
+    t.buf_hi = 0;
+    total_bufs = t.n_lo;
+  }
+  t.nst = std::min(kMaxStages, total_bufs / WPH);
+  if (t.nst < 2) return cudaErrorInvalidConfiguration;
+  const int nbuf = t.nst * WPH;
+  size_t smem = 0;
+  if (Cfg::kHasT) {
+    smem = (size_t)t.t_off + Cfg::kTBytes;
+    if (nbuf > t.n_lo) smem = (size_t)t.buf_hi + (size_t)(nbuf - t.n_lo) * t.buf_bytes;
+  } else {
+    smem = (size_t)kMiscBytes + (size_t)nbuf * t.buf_bytes;
+  }
+
+  const int B = a.batch, Hq = a.num_q_heads;
+  const int64_t slots = (int64_t)p.num_splits + B;
+  t.part_acc = static_cast<float*>(a.workspace);
+  t.part_ml = t.part_acc + slots * Hq * D;
+  t.prefix = reinterpret_cast<int*>(t.part_ml + slots * Hq * 2);
+  auto kern = decode_tc_kernel<D, KB, VB, G, WPH, ROWMAP>;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<p.num_splits, 32 * (H + 1), smem, stream>>>(t);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int rows = B * Hq;
+  combine_tc_kernel<D / 32><<<(rows + 7) / 8, 256, 0, stream>>>(a, p.num_splits, t.part_acc, t.part_ml,
+                                                                     t.prefix);
+  return cudaGetLastError();
+}
+
+
+// Instantiations: D 128 (2 blocks per stage) and 256 (1) x all 2/4-bit combos x G 4/8, and
+// D 64 at 4/4 bits.  ROWMAP: batch rows read block-table rows through a row map.
+template <bool ROWMAP>
+cudaError_t launch_decode_tc_dispatch(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+#define TQ_TC_CASE(D, KB, VB, GG, WPH)                                                    \
+  if (a.head_dim == D && a.k_bits == KB && a.v_bits == VB && G == GG)                     \
+    return launch_tc_typed<D, KB, VB, GG, WPH, ROWMAP>(a, p, stream);
+#define TQ_TC_BITS(D, GG, WPH) \
+  TQ_TC_CASE(D, 4, 4, GG, WPH) TQ_TC_CASE(D, 4, 2, GG, WPH) TQ_TC_CASE(D, 2, 4, GG, WPH) TQ_TC_CASE(D, 2, 2, GG, WPH)
+  TQ_TC_BITS(128, 4, 2)
+  TQ_TC_BITS(128, 8, 2)
+  TQ_TC_BITS(256, 4, 1)
+  TQ_TC_BITS(256, 8, 1)
+  TQ_TC_CASE(64, 4, 4, 4, 2)
+  TQ_TC_CASE(64, 4, 4, 8, 2)
+#undef TQ_TC_BITS
+#undef TQ_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace tq
