@@ -45,6 +45,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--batch", type=int, default=None, help="keep only the first B sequences (profiling runs)")
+    p.add_argument("--workload", type=int, default=WORKLOAD_CFG, help="workload number 1..5 (default 4)")
+    p.add_argument("--sub", type=int, default=0, help="sweep point of workload 3 (0..8)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -118,27 +120,31 @@ def write_bytes(w, raw, slots, bits):
     return raw.size * raw.itemsize + written * row_bytes(w.head_dim, bits) + slots.size * 8
 
 
-def kernel_source_hash():
+def kernel_source_hash(files):
+    """Hash of the kernel source files a traffic figure was taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_kv_cache_06_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for name in sorted(files):
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+        except OSError:
+            return None
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_key):
-    """Per-launch DRAM bytes from the committed ncu summary, if taken on the current sources."""
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
         return None
-    if rec.get("source_hash") != kernel_source_hash():
-        return None
     ent = rec.get("kernels", {}).get(kernel_key)
-    return None if ent is None else ent.get("dram_bytes_per_launch")
+    if ent is None or ent.get("source_hash") != kernel_source_hash(ent.get("sources", [])):
+        return None
+    return ent.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -248,12 +254,22 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
+def write_batch(w):
+    """(K rows, V rows, slots) the step writes: the workload's separate write batch when it has
+    one (workload 5: a prefill-style re-write of sequence 0), else the whole cache."""
+    if w.write_k is not None:
+        return w.write_k, w.write_v, w.write_slots
+    return w.k_raw, w.v_raw, w.slots
+
+
 def workload_config(w, batch_override):
-    return {"workload": f"{w.name}: write {w.num_tokens} tokens K+V, then decode", "batch": w.batch,
+    wk, _, _ = write_batch(w)
+    raw_gb = wk.size * wk.itemsize / 1e9
+    return {"workload": f"{w.name}: write {wk.shape[0]} tokens K+V, then decode", "batch": w.batch,
             "seq_len": int(w.seq_lens.max()), "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "k_bits": w.k_bits, "v_bits": w.v_bits, "block_size": w.block_size,
             "num_blocks": w.num_blocks, "raw_dtype": str(w.k_raw.dtype),
-            "l2": "inputs > L2 (1.07 GB raw per component); 256 MB L2 flush before each decode",
+            "l2": f"256 MB L2 flush before each decode ({raw_gb:.2f} GB raw rows written per component)",
             "batch_override": batch_override}
 
 
@@ -263,8 +279,8 @@ def run_reference(args):
         return
     from quantized_kv_cache_06_gb300.workloads import make_workload
 
-    w = make_workload(WORKLOAD_CFG, batch=args.batch)
-    n_seq, n_write = 2, 4096
+    w = make_workload(args.workload, sub=args.sub, batch=args.batch)
+    n_seq, n_write = min(2, w.batch), 4096
     sampler = OracleSample(w, n_seq, n_write)
     for _ in range(args.warmup):
         sampler.run()
@@ -300,15 +316,17 @@ def run_gpu(args):
     dev = torch.device("cuda", local_rank)
     tq.lib()
 
-    w = make_workload(WORKLOAD_CFG, batch=args.batch, shard=rank)  # each rank its own batch
+    w = make_workload(args.workload, sub=args.sub, batch=args.batch, shard=rank)  # each rank its own batch
     d = w.head_dim
     signs = tq.tq_build_rotation(d, 42, dev)
     ck = tq.tq_codebook(d, w.k_bits, dev)[0]
     cv = tq.tq_codebook(d, w.v_bits, dev)[0]
     rb_k, rb_v = tq.tq_row_bytes(d, w.k_bits), tq.tq_row_bytes(d, w.v_bits)
-    kraw = torch.from_numpy(w.k_raw).to(dev)
-    vraw = torch.from_numpy(w.v_raw).to(dev)
-    slots = torch.from_numpy(w.slots).to(dev)
+    wk_np, wv_np, ws_np = write_batch(w)
+    kraw = torch.from_numpy(wk_np).to(dev)
+    vraw = torch.from_numpy(wv_np).to(dev)
+    slots = torch.from_numpy(ws_np).to(dev)
+    cache_slots = torch.from_numpy(w.slots).to(dev)  # every token of the cache, for the readback
     q = torch.from_numpy(w.q).to(dev)
     bt = torch.from_numpy(w.block_table).to(dev)
     lens = torch.from_numpy(w.seq_lens).to(dev)
@@ -340,6 +358,10 @@ def run_gpu(args):
         if ev is not None:
             ev[4].record(stream)
 
+    if w.write_k is not None:  # the cache the decode reads: every token written once, untimed
+        for raw, pages, cents, st in ((w.k_raw, kp, ck, st_k), (w.v_raw, vp, cv, st_v)):
+            tq.tq_write_kv(torch.from_numpy(raw).to(dev), pages, cache_slots, signs, cents, status=st, check=False)
+        torch.cuda.synchronize()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -369,11 +391,12 @@ def run_gpu(args):
         [total_ms / args.steps, statistics.mean(dec), statistics.mean(wk) + statistics.mean(wv)], world, dev)
 
     dbytes = decode_bytes(w)
-    kbytes = write_bytes(w, w.k_raw, w.slots, w.k_bits)
-    vbytes = write_bytes(w, w.v_raw, w.slots, w.v_bits)
+    kbytes = write_bytes(w, wk_np, ws_np, w.k_bits)
+    vbytes = write_bytes(w, wv_np, ws_np, w.v_bits)
     dec_s = dec_max / 1e3
     value = weak_scaling_rate(world, dbytes, dec_s) / 1e9
-    head_rows = 2 * w.num_tokens * w.num_kv_heads
+    write_tokens = int(ws_np.shape[0])
+    head_rows = 2 * write_tokens * w.num_kv_heads
     write_s = wr_max / 1e3
     peak, peak_kind = peaks()
     dec_gbs = dbytes / dec_s / 1e9
@@ -392,10 +415,10 @@ def run_gpu(args):
             "decode_us": dec_max * 1e3, "decode_gbs_per_gpu": dec_gbs, "decode_frac_of_peak": dec_gbs / peak,
             "decode_seq_per_s": weak_scaling_rate(world, w.batch, dec_s),
             "write_us_per_component": write_s / 2 * 1e6, "write_rows_per_s": weak_scaling_rate(world, head_rows, write_s),
-            "write_token_rows_per_s": weak_scaling_rate(world, 2 * w.num_tokens, write_s), "write_gbs_per_gpu": wr_gbs,
+            "write_token_rows_per_s": weak_scaling_rate(world, 2 * write_tokens, write_s), "write_gbs_per_gpu": wr_gbs,
             "roofline": dominant, "roofline_decode": roof_dec, "roofline_write": roof_wr,
             "gpu_launches": args.steps * 6, "clocks": clk}
-    line["next_rows"] = {"tq_dequant_rows": dequant_measure(tq, w, dev, kp, slots, signs, ck, flush, stream, peak,
+    line["next_rows"] = {"tq_dequant_rows": dequant_measure(tq, w, dev, kp, cache_slots, signs, ck, flush, stream, peak,
                                                              peak_kind, world),
                          "tq_paged_prefill": prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream,
                                                              peak, peak_kind, world)}
@@ -403,10 +426,12 @@ def run_gpu(args):
     if not args.no_e2e:
         line["e2e"] = e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        r = OracleSample(w, 2, 4096).run()
+        sampler = OracleSample(w, min(2, w.batch), 4096)
+        r = sampler.run()
         line["cpu_baseline"] = {"value": r["decode_gbs"], "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
-                                "sample": "oracle decode of 2 sequences (32 q heads, 8192 tokens) and write of "
-                                          "4096 tokens x 8 heads for K and V",
+                                "sample": f"oracle decode of {sampler.n_seq} sequences ({w.num_q_heads} q heads, "
+                                          f"{int(w.seq_lens[:sampler.n_seq].max())} tokens) and write of {sampler.nw} "
+                                          f"tokens x {w.num_kv_heads} heads for K and V",
                                 "decode_seq_per_s": r["decode_seq_per_s"], "write_rows_per_s": r["write_rows_per_s"]}
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -414,7 +439,7 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
 
 
-def dequant_measure(tq, w, dev, kp, slots, signs, ck, flush, stream, peak, peak_kind, world, steps=5):
+def dequant_measure(tq, w, dev, kp, cache_slots, signs, ck, flush, stream, peak, peak_kind, world, steps=5):
     """Dense readback of every K row of the workload (tq_dequant_rows, fp16 out), timed
     apart from the step with CUDA events, an L2 flush before each call."""
     import torch
@@ -422,13 +447,13 @@ def dequant_measure(tq, w, dev, kp, slots, signs, ck, flush, stream, peak, peak_
     out = torch.empty(w.num_tokens, w.num_kv_heads, w.head_dim, dtype=torch.float16, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     for _ in range(2):
-        tq.tq_dequant_rows(kp, slots, signs, ck, out=out, status=st, check=False)
+        tq.tq_dequant_rows(kp, cache_slots, signs, ck, out=out, status=st, check=False)
     times = []
     for i in range(steps):
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        tq.tq_dequant_rows(kp, slots, signs, ck, out=out, status=st, check=False)
+        tq.tq_dequant_rows(kp, cache_slots, signs, ck, out=out, status=st, check=False)
         e1.record(stream)
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
@@ -497,9 +522,10 @@ def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5):
     decode, D2H of the output, all inside the timed region."""
     import torch
 
-    hk = torch.from_numpy(w.k_raw).pin_memory()
-    hv = torch.from_numpy(w.v_raw).pin_memory()
-    hs = torch.from_numpy(w.slots).pin_memory()
+    wk_np, wv_np, ws_np = write_batch(w)
+    hk = torch.from_numpy(wk_np).pin_memory()
+    hv = torch.from_numpy(wv_np).pin_memory()
+    hs = torch.from_numpy(ws_np).pin_memory()
     hq = torch.from_numpy(w.q).pin_memory()
     hbt = torch.from_numpy(w.block_table).pin_memory()
     hl = torch.from_numpy(w.seq_lens).pin_memory()

@@ -72,7 +72,7 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
 
     class Args:
-        batch, steps, warmup, gpus = None, 1, 0, 2
+        batch, steps, warmup, gpus, workload, sub = None, 1, 0, 2, 4, 0
 
     bench.run_reference(Args())
     assert capsys.readouterr().out == ""
