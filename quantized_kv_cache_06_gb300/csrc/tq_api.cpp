@@ -279,6 +279,18 @@ tq_status decode_impl(const char* name, const void* q, tq_dtype q_dtype, int bat
   a.k_alpha = 1.0f;
   a.bt_rows = bt_rows;
   a.bt_num_rows = bt_num_rows;
+  if (bt_rows && tq::prefill_mq_supported(a)) {
+    // mixed prefill/decode: query rows of one sequence share each dequantised key/value tile
+    if (batch > 0) {
+      a.v_alpha = fp16_scale_for(head_dim, v_bits);
+      a.k_alpha = fp16_scale_for(head_dim, k_bits);
+    }
+    const tq::MqPlan plan = tq::plan_prefill_mq(a, current_device_sms());
+    if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
+      return fail(TQ_ERR_INVALID_ARG, "%s: workspace must be >= %zu bytes and 16-byte aligned (got %zu)", name,
+                  plan.workspace_bytes, workspace_bytes);
+    return check_cuda(tq::launch_prefill_mq(a, plan, static_cast<cudaStream_t>(stream)), name);
+  }
   if (batch > 0 && tq::tc_decode_supported(a)) {
     a.v_alpha = fp16_scale_for(head_dim, v_bits);
     a.k_alpha = fp16_scale_for(head_dim, k_bits);
@@ -408,7 +420,15 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
 
 size_t tq_paged_prefill_workspace(int num_q_rows, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_blocks_per_seq, int block_size) {
-  return tq_paged_decode_workspace(num_q_rows, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  // The larger of the row-mapped decode plan and the multi-query plan (which one runs
+  // depends on k_bits / v_bits, which this query does not take).
+  size_t need =
+      tq_paged_decode_workspace(num_q_rows, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  if (need == 0) return 0;
+  tq::DecodeArgs a =
+      make_decode_args(num_q_rows, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  need = std::max(need, tq::plan_prefill_mq(a, current_device_sms()).workspace_bytes);
+  return need;
 }
 
 tq_status tq_paged_prefill(const void* q, tq_dtype q_dtype, int num_q_rows, int num_q_heads, int num_kv_heads,

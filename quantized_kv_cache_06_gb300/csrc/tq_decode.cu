@@ -259,6 +259,23 @@ DecodePlan plan_decode(const DecodeArgs& a, int num_sms) {
   return p;
 }
 
+cudaError_t launch_combine_splits(const float* acc, const float* ml, int rows, int nsplit, int head_dim,
+                                  const float* signs, void* out, int out_dtype, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  SplitView part;
+  part.acc = const_cast<float*>(acc);
+  part.ml = const_cast<float*>(ml);
+  const int grid = (rows + 7) / 8;
+  switch (head_dim) {
+    case 32: combine_kernel<1><<<grid, 256, 0, stream>>>(rows, nsplit, part, signs, out, out_dtype); break;
+    case 64: combine_kernel<2><<<grid, 256, 0, stream>>>(rows, nsplit, part, signs, out, out_dtype); break;
+    case 128: combine_kernel<4><<<grid, 256, 0, stream>>>(rows, nsplit, part, signs, out, out_dtype); break;
+    case 256: combine_kernel<8><<<grid, 256, 0, stream>>>(rows, nsplit, part, signs, out, out_dtype); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
   if (a.status) {
     cudaError_t err = cudaMemsetAsync(a.status, 0, sizeof(int32_t), stream);

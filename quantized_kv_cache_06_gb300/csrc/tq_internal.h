@@ -98,6 +98,25 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStrea
 // The same launch for a batch with a block-table row map (tq_prefill_tc.cu).
 cudaError_t launch_decode_tc_rowmap(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 
+// Multi-query mixed prefill/decode (tq_prefill_mq.cu): windows of query rows against
+// 32-token tiles dequantised once into shared memory, split-K over tokens.
+struct MqPlan {
+  int nsplit;     // token splits per sequence
+  int split_len;  // tokens per split
+  int windows;    // CTAs per (split, kv head)
+  size_t workspace_bytes;
+};
+bool prefill_mq_supported(const DecodeArgs& a);
+MqPlan plan_prefill_mq(const DecodeArgs& a, int num_sms);
+// Enqueues status reset, the multi-query kernel and the split combine.
+cudaError_t launch_prefill_mq(const DecodeArgs& a, const MqPlan& p, cudaStream_t stream);
+
+// Split combine of the SIMT decode (tq_decode.cu): for each of `rows` rows merges
+// `nsplit` partials acc [rows][nsplit][head_dim], ml [rows][nsplit][2] (running max in
+// log2 units, sum), divides by the sum, applies R^T and writes out[rows][head_dim].
+cudaError_t launch_combine_splits(const float* acc, const float* ml, int rows, int nsplit, int head_dim,
+                                  const float* signs, void* out, int out_dtype, cudaStream_t stream);
+
 // Split plan for the shapes in `a` on a device with `num_sms` SMs.
 DecodePlan plan_decode(const DecodeArgs& a, int num_sms);
 

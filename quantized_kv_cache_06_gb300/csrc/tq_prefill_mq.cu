@@ -1,0 +1,691 @@
+// Multi-query mixed prefill/decode attention over packed TurboQuant pages (sm_103a,
+// mma.sync f16 -> f32).
+//
+// TurboQuant docs: "vLLM Usage" (Runtime Dispatch: the cache plus mixed prefill/decode
+// reads the packed cache) and "Architecture" (Diagnostic vs Serving Paths: keys consumed
+// compressed, values accumulated from packed indices).  Query row i is one token of
+// sequence q_seq[i] that attends to the first q_len[i] tokens of that sequence.
+//
+// Rows of one prefill chunk read the same cache blocks.  This kernel dequantises every
+// 32-token tile of one kv head ONCE into shared memory (fp16, rotated space) and runs it
+// against up to 64 (query row, q head) pairs with tensor-core MMAs:
+//   S  = qrot Khat^T          m16n8k16, A = rotated queries, B = key tile (ldmatrix)
+//   causal mask per row (token < q_len), online softmax in base 2
+//   O += P' Vhat               A = P' = p * nu_v (from the S accumulators), B = value tile
+//                              (ldmatrix.trans)
+// Khat holds fp16(alpha_k c[idx]) (+ the fp16 remainder for tiles that need the exact
+// score), Vhat fp16(alpha_v c[idx]); the key norm multiplies the score and the value norm
+// the weight, so nothing of the cache is expanded to a dense row in HBM.  The rotated
+// query is split into fp16 hi + lo, and the score is hi*Khat + lo*Khat (+ hi*Klo when
+// nu_k * ||q|| can exceed kMqFastBound), which keeps it at fp32-level accuracy.
+//
+// Work split.  CTA (window, split, kv head): a window is 64 / G consecutive query rows
+// (64 rows of the MMA: 4 warps x 16), a split a range of split_len tokens of the
+// sequence.  Rows of a window that belong to different sequences form segments, taken one
+// after the other (each streams its own sequence; rows outside the segment are masked).
+// The CTA writes one (m, l, acc[D]) partial per (row, q head, split); the split combine
+// (shared with the SIMT decode) merges them and applies R^T.
+//
+// Per tile: every thread copies the packed words it will dequantise with cp.async into
+// its own slots of a 4-stage ring, three tiles ahead.  For tile it: wait for its own
+// copies -> barrier A (which also votes whether the tile needs the exact key part) ->
+// dequantise into shared memory -> start the copies of tile it + 3 -> barrier B -> MMAs.
+// One tile buffer: barrier A orders its reuse after every warp's math.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr int kMqWarps = 4;
+constexpr int kMqThreads = 32 * kMqWarps;
+constexpr int kMqRows = 16 * kMqWarps;  // MMA rows (query row x q head) per CTA
+constexpr int kMqTile = 32;             // tokens per tile
+constexpr float kMqLog2e = 1.4426950408889634f;
+// Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored without the fp16
+// remainder of the key centroids (same bound as the tensor-core decode).
+constexpr float kMqFastBound = 48.0f;
+constexpr float kMqSlack = 6.0f;  // log2 units the running max may lag behind the scores
+
+constexpr int kMqStages = 4;  // raw-word ring: tiles it .. it + 2 in flight while tile it is used
+
+template <int D, int KB, int VB>
+struct MqSmem {
+  static constexpr int kRow = 2 * D;                  // bytes per fp16 row
+  static constexpr int kTileBytes = kMqTile * kRow;
+  static constexpr int kOffKhi = 0;                   // [32 tokens][D], swizzled
+  static constexpr int kOffKlo = kOffKhi + kTileBytes;
+  static constexpr int kOffV = kOffKlo + kTileBytes;
+  static constexpr int kOffQlo = kOffV + kTileBytes;  // [warp][16 rows][D], swizzled
+  static constexpr int kOffKn = kOffQlo + kMqWarps * 16 * kRow;  // float[32] key norms
+  static constexpr int kOffVn = kOffKn + kMqTile * 4;            // float[32] value norms
+  static constexpr int kOffKadd = kOffVn + kMqTile * 4;          // float[32] 0 / -inf per token
+  static constexpr int kOffSeq = kOffKadd + kMqTile * 4;         // int[64] table row per window row
+  static constexpr int kOffLen = kOffSeq + kMqRows * 4;          // int[64] clamped length
+  static constexpr int kOffQn = kOffLen + kMqRows * 4;           // float[warps] max ||q_rot||
+  // Raw-word ring, private to each thread: per stage and thread, for each of its
+  // dequantisation tasks the index words, the norm, and an "in range" flag; stored
+  // word-major ([stage][word][thread]) so a warp's accesses are conflict free.
+  static constexpr int kTasks = (2 * kMqTile * (D / 32)) / kMqThreads;  // tasks per thread
+  static constexpr int kMaxBits = KB > VB ? KB : VB;
+  static constexpr int kTaskWords = kMaxBits + 2;                       // words, norm, flag
+  static constexpr int kRingWords = kTasks * kTaskWords;                // per thread per stage
+  static constexpr int kOffRing = (kOffQn + kMqWarps * 4 + 15) / 16 * 16;
+  static constexpr int kBytes = kOffRing + kMqStages * kRingWords * kMqThreads * 4;
+  static constexpr int kAlloc = kBytes + 256;  // + the pad that aligns the base to 256 bytes
+  // the query hi parts are staged in the key tiles before the first tile
+  static_assert(2 * kTileBytes == kMqWarps * 16 * kRow, "query staging must fit the key tiles");
+};
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a [rows][D] fp16 tile: the chunk
+// index is XORed with row % 8, so the 8 rows of an ldmatrix hit 8 different bank groups.
+// Region bases are multiples of 1024 bytes and rows are 2D >= 128 bytes, so the chunk
+// bits (4..7) of a row's address are free: for a compile-time step k,
+// swz(row, c ^ k) = swz(row, c) ^ (k << 4), one LOP3 per address.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * (2 * D) + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// D = A * B + D, m16n8k16, A row-major f16, B col-major f16, f32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation (ex2(-inf) = 0)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+
+struct MqArgs {
+  DecodeArgs a;
+  int nsplit;     // token splits per sequence
+  int split_len;  // tokens per split (multiple of 32)
+  int bs_shift;   // log2(block_size) when it is a power of two, else -1
+  int windows;    // ceil(rows / rows_per_window)
+  float* part_acc;  // [rows * Hq][nsplit][D]
+  float* part_ml;   // [rows * Hq][nsplit][2]
+};
+
+// Raw index words of one dequantisation task: 32 consecutive coordinates (BITS whole
+// words) of one token's row, its norm, and whether the token is read at all.
+template <int BITS>
+struct RawTask {
+  uint32_t w[BITS];
+  uint32_t nrm;
+  bool ok;
+};
+
+template <int D, int KB, int VB, int G>
+__global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) {
+  using S = MqSmem<D, KB, VB>;
+  constexpr int P = D / 32;                  // 32-coordinate parts per row
+  constexpr int E = D / 32;                  // query coordinates per lane
+  constexpr int KS = D / 16;                 // score k-steps
+  constexpr int NT = D / 8;                  // value n-tiles
+  constexpr int MQ = kMqRows / G;            // query rows per window
+  constexpr int TASKS = 2 * kMqTile * P;     // K and V tasks of one tile
+  constexpr int TPT = TASKS / kMqThreads;    // tasks per thread
+  constexpr int MAXB = KB > VB ? KB : VB;
+  static_assert(TPT == 1 || TPT == 2, "one or two dequantisation tasks per thread");
+  static_assert(TPT == S::kTasks, "task count");
+  static_assert(TPT == 2 || kMqThreads == 2 * kMqTile * P, "one K and one V task set");
+  static_assert(kMqRows % G == 0, "group must divide the rows of a CTA");
+
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  // region offsets assume a 256-byte aligned base (the XOR addressing needs bits 4..7 free)
+  unsigned char* smem = smem_raw + ((256u - (smem_addr(smem_raw) & 255u)) & 255u);
+  const DecodeArgs& a = args.a;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = a.num_kv_heads, Hq = a.num_q_heads;
+  const int h = blockIdx.x % H;
+  const int split = (blockIdx.x / H) % args.nsplit;
+  const int window = blockIdx.x / (H * args.nsplit);
+  const int i0 = window * MQ;
+  const int nrows = min(MQ, a.batch - i0);
+  const int bs = a.block_size;
+  const int cap = a.max_blocks_per_seq * bs;
+  const uint32_t sbase = smem_addr(smem);
+  int* row_seq = reinterpret_cast<int*>(smem + S::kOffSeq);
+  int* row_len = reinterpret_cast<int*>(smem + S::kOffLen);
+  float* kn_s = reinterpret_cast<float*>(smem + S::kOffKn);
+  float* vn_s = reinterpret_cast<float*>(smem + S::kOffVn);
+  float* kadd_s = reinterpret_cast<float*>(smem + S::kOffKadd);
+  float* qn_s = reinterpret_cast<float*>(smem + S::kOffQn);
+
+  // ---- window rows: table row and clamped length -------------------------------------
+  if (tid < MQ) {
+    int seq = -1, len = 0;
+    if (tid < nrows) {
+      seq = block_table_row(a, i0 + tid);
+      len = __ldg(a.seq_lens + i0 + tid);
+      const bool bad = seq < 0 || len < 0 || len > cap;
+      if (bad && split == 0 && h == 0 && a.status) atomicMax(a.status, (int32_t)kInvalidArg);
+      len = len < 0 ? 0 : (len > cap ? cap : len);
+    }
+    row_seq[tid] = seq;
+    row_len[tid] = len;
+  }
+
+  // ---- rotated queries of this warp's 16 MMA rows -> hi (registers) and lo (smem) ------
+  const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
+  const float qmul = scale * kMqLog2e / sqrtf((float)D);
+  const float inv_alpha_k = 1.0f / a.k_alpha;
+  const uint32_t qhi_base = sbase + S::kOffKhi + warp * 16 * S::kRow;  // staging in the key tiles
+  const uint32_t qlo_base = sbase + S::kOffQlo + warp * 16 * S::kRow;
+  float qn = 0.f;
+  for (int m = 0; m < 16; ++m) {
+    const int mr = warp * 16 + m;
+    const int wrow = mr / G;
+    float v[E];
+    if (wrow < nrows) {
+      const int64_t base = ((int64_t)(i0 + wrow) * Hq + (int64_t)h * G + mr % G) * D + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i) v[i] = load_as_f32(a.q, base + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) v[i] = 0.f;
+    }
+    fwht_warp<E>(v);
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      v[i] *= qmul;
+      ss = fmaf(v[i], v[i], ss);
+      v[i] *= inv_alpha_k;  // the key tile holds alpha_k * c
+    }
+    qn = fmaxf(qn, sqrtf(warp_sum(ss)));
+    uint32_t hi[E / 2], lo[E / 2];
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      const __half h0 = __float2half_rn(v[2 * i]), h1 = __float2half_rn(v[2 * i + 1]);
+      hi[i] = half2_bits(__half2float(h0), __half2float(h1));
+      lo[i] = half2_bits(v[2 * i] - __half2float(h0), v[2 * i + 1] - __half2float(h1));
+    }
+    // lane owns coordinates [lane E, lane E + E): chunk lane E / 8, byte offset (lane E % 8) * 2
+    const uint32_t off = swz<D>(m, (lane * E) >> 3) + (uint32_t)(((lane * E) & 7) * 2);
+    unsigned char* ph = smem + (qhi_base - sbase) + off;
+    unsigned char* pl = smem + (qlo_base - sbase) + off;
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint2*>(ph) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(pl) = make_uint2(lo[0], lo[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(ph) = hi[0];
+      *reinterpret_cast<uint32_t*>(pl) = lo[0];
+    }
+  }
+  if (lane == 0) qn_s[warp] = qn;
+  __syncwarp();
+  const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: this lane addresses row rr of matrix mi
+  // A fragments (16 rows x 16 k): matrix mi = rows (mi & 1) * 8.., k chunk 2 ks + (mi >> 1)
+  const uint32_t qa_lane = swz<D>((mi & 1) * 8 + rr, mi >> 1);
+  uint32_t qh[KS][4];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) ldsm_x4(qh[ks], (qhi_base + qa_lane) ^ (uint32_t)(ks << 5));
+  __syncthreads();  // row metadata and query norms visible; query staging read by every warp
+  float qn_cta = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMqWarps; ++w) qn_cta = fmaxf(qn_cta, qn_s[w]);
+
+  // ---- per-lane softmax state: rows r and r + 8 of this warp's 16 --------------------
+  const int r = lane >> 2, c = lane & 3;
+  float o[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float m_thr[2] = {-INFINITY, -INFINITY};  // m_run + kMqSlack
+
+  // dequantisation centroids: lane l holds entry l mod 2^b (a shuffle reads only the low
+  // 5 bits of its source lane, so a field needs no mask)
+  uint32_t kc_pair, vc_half;
+  {
+    const float ck = __ldg(a.k_centroids + (lane & ((1 << KB) - 1))) * a.k_alpha;
+    const __half hk = __float2half_rn(ck);
+    const __half lk = __float2half_rn(ck - __half2float(hk));
+    kc_pair = (uint32_t)__half_as_ushort(hk) | ((uint32_t)__half_as_ushort(lk) << 16);
+    vc_half = (uint32_t)__half_as_ushort(__float2half_rn(__ldg(a.v_centroids + (lane & ((1 << VB) - 1))) * a.v_alpha));
+  }
+
+  // task j of this thread: component (0 K, 1 V), token t of the tile, part (32
+  // coordinates).  D = 128: task 0 is K and task 1 is V of (t, part) = (tid / 4, tid % 4);
+  // D = 64: warps 0-1 take K tasks and warps 2-3 V tasks (warp-uniform).
+  auto task_comp = [&](int j) -> int { return TPT == 2 ? j : (tid >= kMqTile * P ? 1 : 0); };
+  auto task_rem = [&](int j) -> int { return TPT == 2 ? tid : tid % (kMqTile * P); };
+  auto task_tok = [&](int j) -> int { return task_rem(j) / P; };
+  auto task_part = [&](int j) -> int { return task_rem(j) % P; };
+
+  const uint32_t khi_base = sbase + S::kOffKhi, klo_base = sbase + S::kOffKlo, v_base = sbase + S::kOffV;
+  // ldmatrix lane addresses at k-step / value-tile 0 (the steps are XORed in):
+  // key B fragments: matrix mi = tokens (mi >> 1) * 8.., k chunk 2 ks + (mi & 1);
+  // value B fragments (transposed): tokens (mi & 1) * 8.., value chunk 2 dp + (mi >> 1)
+  const uint32_t kb_lane = khi_base + swz<D>((mi >> 1) * 8 + rr, mi & 1);
+  const uint32_t vb_lane = v_base + swz<D>((mi & 1) * 8 + rr, mi >> 1);
+  const uint32_t ql_lane = qlo_base + qa_lane;
+  // dequantisation stores of task j: chunk part * 4 + q4 of token row t -> base ^ (q4 << 4)
+  uint32_t sts_off[TPT];
+#pragma unroll
+  for (int j = 0; j < TPT; ++j) sts_off[j] = swz<D>(task_tok(j), task_part(j) * 4);
+  const int bs_shift = args.bs_shift;
+  auto blk_of = [&](int T) -> int { return bs_shift >= 0 ? (T >> bs_shift) : T / bs; };
+  auto off_of = [&](int T) -> int { return bs_shift >= 0 ? (T & (bs - 1)) : T % bs; };
+
+  // ---- segments: runs of window rows with one table row ------------------------------
+  int s0 = 0;
+  while (s0 < nrows) {
+    const int seq = row_seq[s0];
+    int s1 = s0 + 1;
+    while (s1 < nrows && row_seq[s1] == seq) ++s1;
+    int seg_len = 0;
+    for (int k = s0; k < s1; ++k) seg_len = max(seg_len, row_len[k]);
+    const int t_beg = split * args.split_len;
+    const int t_end = min(seg_len, t_beg + args.split_len);
+    if (seq >= 0 && t_beg < t_end) {
+      const int32_t* bt = a.block_table + (int64_t)seq * a.max_blocks_per_seq;
+      // lengths of this lane's two rows (0 outside the segment)
+      const int wA = (warp * 16 + r) / G, wB = (warp * 16 + r + 8) / G;
+      const int lenA = (wA >= s0 && wA < s1) ? row_len[wA] : 0;
+      const int lenB = (wB >= s0 && wB < s1) ? row_len[wB] : 0;
+      const int ntiles = (t_end - t_beg + kMqTile - 1) / kMqTile;
+
+      auto load_bid = [&](int tile, int j) -> int {
+        const int T = t_beg + tile * kMqTile + task_tok(j);
+        return (tile < ntiles && T < t_end) ? __ldg(bt + blk_of(T)) : -1;
+      };
+      // ring word w of this thread in stage st
+      auto ring = [&](int st, int w) -> uint32_t {
+        return sbase + S::kOffRing + (uint32_t)(((st * S::kRingWords + w) * kMqThreads + tid) * 4);
+      };
+      // Starts the copies of task j of `tile` (block `bid`) into ring stage tile % kMqStages.
+      auto issue_task = [&](auto bits_tag, int tile, int j, int bid) {
+        constexpr int BITS = decltype(bits_tag)::value;
+        constexpr int RB = D * BITS / 8 + 4;
+        const int st = tile % kMqStages;
+        const int T = t_beg + tile * kMqTile + task_tok(j);
+        const bool in = tile < ntiles && T < t_end;
+        const bool okb = bid >= 0 && (int64_t)bid < a.num_blocks;
+        if (in && !okb && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+        const bool ok = in && okb;
+        sts_u32(ring(st, j * S::kTaskWords + S::kMaxBits + 1), ok ? 1u : 0u);
+        if (ok) {
+          const uint8_t* pages = task_comp(j) == 0 ? a.k_pages : a.v_pages;
+          const uint32_t* row =
+              reinterpret_cast<const uint32_t*>(pages + (((int64_t)bid * bs + off_of(T)) * H + h) * RB);
+#pragma unroll
+          for (int k = 0; k < BITS; ++k) cp_async4(ring(st, j * S::kTaskWords + k), row + task_part(j) * BITS + k);
+          if (task_part(j) == 0) cp_async4(ring(st, j * S::kTaskWords + S::kMaxBits), row + (RB - 4) / 4);
+        }
+      };
+      auto issue_tile = [&](int tile, const int (&bid)[TPT]) {
+#pragma unroll
+        for (int j = 0; j < TPT; ++j) {
+          if (task_comp(j) == 0) issue_task(std::integral_constant<int, KB>{}, tile, j, bid[j]);
+          else issue_task(std::integral_constant<int, VB>{}, tile, j, bid[j]);
+        }
+        cp_async_commit();
+      };
+
+      // prologue: block ids of tiles 0 .. kMqStages - 1, copies of tiles 0 .. kMqStages - 2
+      int bids[kMqStages][TPT];
+#pragma unroll
+      for (int u = 0; u < kMqStages; ++u)
+#pragma unroll
+        for (int j = 0; j < TPT; ++j) bids[u][j] = load_bid(u, j);
+#pragma unroll
+      for (int u = 0; u < kMqStages - 1; ++u) issue_tile(u, bids[u]);
+      int bid_pref[TPT];  // block ids of tile it + kMqStages - 1
+#pragma unroll
+      for (int j = 0; j < TPT; ++j) bid_pref[j] = bids[kMqStages - 1][j];
+
+      for (int it = 0; it < ntiles; ++it) {
+        const int T0 = t_beg + it * kMqTile;
+        // ---- this thread's words of tile it (its own copies: no barrier needed) -------
+        cp_async_wait<kMqStages - 2>();
+        RawTask<MAXB> raw[TPT];
+        {
+          const int st = it % kMqStages;
+#pragma unroll
+          for (int j = 0; j < TPT; ++j) {
+            raw[j].ok = lds_u32(ring(st, j * S::kTaskWords + S::kMaxBits + 1)) != 0u;
+#pragma unroll
+            for (int k = 0; k < MAXB; ++k)
+              raw[j].w[k] = raw[j].ok ? lds_u32(ring(st, j * S::kTaskWords + k)) : 0u;
+            raw[j].nrm = (raw[j].ok && task_part(j) == 0) ? lds_u32(ring(st, j * S::kTaskWords + S::kMaxBits)) : 0u;
+          }
+        }
+        // ---- A: exact-score vote; every warp is done with the previous tile ----------
+        int flag = 0;
+#pragma unroll
+        for (int j = 0; j < TPT; ++j)
+          if (task_comp(j) == 0 && task_part(j) == 0 && raw[j].ok)
+            flag |= fabsf(__uint_as_float(raw[j].nrm)) * qn_cta > kMqFastBound;
+        const bool exact = __syncthreads_or(flag) != 0;
+
+        // ---- dequantise the tile into shared memory --------------------------------
+#pragma unroll
+        for (int j = 0; j < TPT; ++j) {
+          const int t = task_tok(j), part = task_part(j);
+          if (task_comp(j) == 0) {
+            if (part == 0) {
+              kn_s[t] = raw[j].ok ? __uint_as_float(raw[j].nrm) : 0.f;
+              kadd_s[t] = raw[j].ok ? 0.f : -INFINITY;
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {  // 8 coordinates per 16-byte chunk
+              uint32_t val[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int i = q4 * 8 + u;  // coordinate within the part
+                const int bit = i * KB, k = bit >> 5, sh = bit & 31;
+                uint32_t f = raw[j].w[k] >> sh;
+                if (sh + KB > 32) f |= raw[j].w[k + 1] << (32 - sh);
+                val[u] = __shfl_sync(kFullMask, kc_pair, (int)f);
+              }
+              const uint32_t off = sts_off[j] ^ (uint32_t)(q4 << 4);
+              sts_v4(khi_base + off, __byte_perm(val[0], val[1], 0x5410), __byte_perm(val[2], val[3], 0x5410),
+                     __byte_perm(val[4], val[5], 0x5410), __byte_perm(val[6], val[7], 0x5410));
+              if (exact)
+                sts_v4(klo_base + off, __byte_perm(val[0], val[1], 0x7632), __byte_perm(val[2], val[3], 0x7632),
+                       __byte_perm(val[4], val[5], 0x7632), __byte_perm(val[6], val[7], 0x7632));
+            }
+          } else {
+            if (part == 0) vn_s[t] = raw[j].ok ? __uint_as_float(raw[j].nrm) : 0.f;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t vp[4];
+#pragma unroll
+              for (int pr = 0; pr < 4; ++pr) {
+                uint32_t val[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int i = q4 * 8 + pr * 2 + u;
+                  const int bit = i * VB, k = bit >> 5, sh = bit & 31;
+                  uint32_t f = raw[j].w[k] >> sh;
+                  if (sh + VB > 32) f |= raw[j].w[k + 1] << (32 - sh);
+                  val[u] = __shfl_sync(kFullMask, vc_half, (int)f);
+                }
+                vp[pr] = __byte_perm(val[0], val[1], 0x5410);
+              }
+              sts_v4(v_base + (sts_off[j] ^ (uint32_t)(q4 << 4)), vp[0], vp[1], vp[2], vp[3]);
+            }
+          }
+        }
+
+        // ---- copies of tile it + kMqStages - 1 (its stage was read in iteration it - 1) --
+        issue_tile(it + kMqStages - 1, bid_pref);
+#pragma unroll
+        for (int j = 0; j < TPT; ++j) bid_pref[j] = load_bid(it + kMqStages, j);
+        __syncthreads();  // B: the tile is in shared memory
+
+        // ---- math: skipped by a warp whose rows all end before the tile -------------
+        if (!__any_sync(kFullMask, T0 < lenA || T0 < lenB)) continue;  // (its copies are issued)
+        float s[4][4];
+#pragma unroll
+        for (int jn = 0; jn < 4; ++jn)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[jn][e] = 0.f;
+        auto scores = [&](auto exact_tag) {
+          constexpr bool EX = decltype(exact_tag)::value;
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t ql[4];
+            ldsm_x4(ql, ql_lane ^ (uint32_t)(ks << 5));
+            const uint32_t kaddr = kb_lane ^ (uint32_t)(ks << 5);
+#pragma unroll
+            for (int jp = 0; jp < 2; ++jp) {
+              const uint32_t koff = kaddr + (uint32_t)(jp * 16 * S::kRow);  // tokens 16 jp ..
+              uint32_t kb[4];
+              ldsm_x4(kb, koff);
+              mma_f16(s[2 * jp], qh[ks], kb[0], kb[1]);
+              mma_f16(s[2 * jp + 1], qh[ks], kb[2], kb[3]);
+              mma_f16(s[2 * jp], ql, kb[0], kb[1]);
+              mma_f16(s[2 * jp + 1], ql, kb[2], kb[3]);
+              if (EX) {
+                uint32_t kl[4];
+                ldsm_x4(kl, koff + (uint32_t)(S::kOffKlo - S::kOffKhi));
+                mma_f16(s[2 * jp], qh[ks], kl[0], kl[1]);
+                mma_f16(s[2 * jp + 1], qh[ks], kl[2], kl[3]);
+              }
+            }
+          }
+        };
+        if (exact) scores(std::true_type{});
+        else scores(std::false_type{});
+
+        // scores: x nu_k, invalid tokens -inf, causal mask per row
+#pragma unroll
+        for (int jn = 0; jn < 4; ++jn) {
+          const int tok = 8 * jn + 2 * c;
+          const float2 kn = *reinterpret_cast<const float2*>(kn_s + tok);
+          const float2 ka = *reinterpret_cast<const float2*>(kadd_s + tok);
+          s[jn][0] = fmaf(s[jn][0], kn.x, ka.x);
+          s[jn][1] = fmaf(s[jn][1], kn.y, ka.y);
+          s[jn][2] = fmaf(s[jn][2], kn.x, ka.x);
+          s[jn][3] = fmaf(s[jn][3], kn.y, ka.y);
+          if (T0 + tok >= lenA) s[jn][0] = -INFINITY;
+          if (T0 + tok + 1 >= lenA) s[jn][1] = -INFINITY;
+          if (T0 + tok >= lenB) s[jn][2] = -INFINITY;
+          if (T0 + tok + 1 >= lenB) s[jn][3] = -INFINITY;
+        }
+        // online softmax for rows r (e = 0, 1) and r + 8 (e = 2, 3); 4 lanes share a row.
+        // The running max only moves when a score passes it by more than kMqSlack, so
+        // p = 2^(s - m) <= 2^kMqSlack; most tiles move no max and skip the rescale.
+        float mx[2];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          mx[hr] = -INFINITY;
+#pragma unroll
+          for (int jn = 0; jn < 4; ++jn) mx[hr] = fmaxf(mx[hr], fmaxf(s[jn][2 * hr], s[jn][2 * hr + 1]));
+        }
+        if (__any_sync(kFullMask, mx[0] > m_thr[0] || mx[1] > m_thr[1])) {
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            float mt = fmaxf(mx[hr], __shfl_xor_sync(kFullMask, mx[hr], 1));
+            mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 2));
+            const float mn = mt > m_thr[hr] ? mt : m_run[hr];
+            const float corr = mn == -INFINITY ? 1.f : ex2(m_run[hr] - mn);
+            m_run[hr] = mn;
+            m_thr[hr] = mn + kMqSlack;
+            l_run[hr] *= corr;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              o[nt][2 * hr] *= corr;
+              o[nt][2 * hr + 1] *= corr;
+            }
+          }
+        }
+        const float m_use[2] = {m_run[0] == -INFINITY ? 0.f : m_run[0], m_run[1] == -INFINITY ? 0.f : m_run[1]};
+        uint32_t pa[2][4];
+#pragma unroll
+        for (int jn = 0; jn < 4; ++jn) {
+          const int tok = 8 * jn + 2 * c;
+          const float2 vn = *reinterpret_cast<const float2*>(vn_s + tok);
+          float pw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p = ex2(s[jn][e] - m_use[e >> 1]);
+            l_run[e >> 1] += p;
+            pw[e] = p > 0.f ? p * ((e & 1) ? vn.y : vn.x) : 0.f;
+          }
+          pa[jn >> 1][(jn & 1) * 2 + 0] = half2_bits(pw[0], pw[1]);
+          pa[jn >> 1][(jn & 1) * 2 + 1] = half2_bits(pw[2], pw[3]);
+        }
+        // O += P' Vhat: k-step s2 covers tokens 16 s2 .. 16 s2 + 15
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+#pragma unroll
+          for (int dp = 0; dp < NT / 2; ++dp) {
+            uint32_t vb[4];
+            ldsm_x4_t(vb, (vb_lane ^ (uint32_t)(dp << 5)) + (uint32_t)(s2 * 16 * S::kRow));
+            mma_f16(o[2 * dp], pa[s2], vb[0], vb[1]);
+            mma_f16(o[2 * dp + 1], pa[s2], vb[2], vb[3]);
+          }
+        }
+      }
+    }
+    cp_async_wait<0>();  // no copy of this segment outlives it
+    s0 = s1;
+  }
+
+  // ---- partials: (m, l, acc / alpha_v) per (row, q head) of this window and split ------
+  const float inv_alpha_v = 1.0f / a.v_alpha;
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    float l = l_run[hr];
+    l += __shfl_xor_sync(kFullMask, l, 1);
+    l += __shfl_xor_sync(kFullMask, l, 2);
+    const int mr = warp * 16 + r + 8 * hr;
+    const int wrow = mr / G;
+    if (wrow < nrows) {
+      const int64_t slot = ((int64_t)(i0 + wrow) * Hq + (int64_t)h * G + mr % G) * args.nsplit + split;
+      float* acc = args.part_acc + slot * D;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float2*>(acc + 8 * nt + 2 * c) =
+            make_float2(o[nt][2 * hr] * inv_alpha_v, o[nt][2 * hr + 1] * inv_alpha_v);
+      if (c == 0) {
+        args.part_ml[slot * 2 + 0] = m_run[hr];
+        args.part_ml[slot * 2 + 1] = l;
+      }
+    }
+  }
+}
+
+template <int D, int KB, int VB, int G>
+cudaError_t launch_mq_one(const MqArgs& m, int grid, cudaStream_t stream) {
+  constexpr int bytes = MqSmem<D, KB, VB>::kAlloc;
+  auto kern = prefill_mq_kernel<D, KB, VB, G>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kMqThreads, bytes, stream>>>(m);
+  return cudaGetLastError();
+}
+
+template <int D, int KB, int VB>
+cudaError_t launch_mq_g(const MqArgs& m, int grid, cudaStream_t stream) {
+  switch (m.a.num_q_heads / m.a.num_kv_heads) {
+    case 1: return launch_mq_one<D, KB, VB, 1>(m, grid, stream);
+    case 2: return launch_mq_one<D, KB, VB, 2>(m, grid, stream);
+    case 4: return launch_mq_one<D, KB, VB, 4>(m, grid, stream);
+    case 8: return launch_mq_one<D, KB, VB, 8>(m, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int D>
+cudaError_t launch_mq_bits(const MqArgs& m, int grid, cudaStream_t stream) {
+  const int kb = m.a.k_bits, vb = m.a.v_bits;
+  if (kb == 4 && vb == 4) return launch_mq_g<D, 4, 4>(m, grid, stream);
+  if (kb == 4 && vb == 2) return launch_mq_g<D, 4, 2>(m, grid, stream);
+  if (kb == 2 && vb == 4) return launch_mq_g<D, 2, 4>(m, grid, stream);
+  if (kb == 2 && vb == 2) return launch_mq_g<D, 2, 2>(m, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool prefill_mq_supported(const DecodeArgs& a) {
+  const int G = a.num_kv_heads > 0 ? a.num_q_heads / a.num_kv_heads : 0;
+  const bool bits = (a.k_bits == 2 || a.k_bits == 4) && (a.v_bits == 2 || a.v_bits == 4);
+  return (a.head_dim == 64 || a.head_dim == 128) && bits && (G == 1 || G == 2 || G == 4 || G == 8) &&
+         a.block_size >= 1;
+}
+
+MqPlan plan_prefill_mq(const DecodeArgs& a, int num_sms) {
+  MqPlan p{};
+  const int G = std::max(1, a.num_kv_heads > 0 ? a.num_q_heads / a.num_kv_heads : 1);
+  const int rows_per_window = std::max(1, kMqRows / G);
+  p.windows = (std::max(0, a.batch) + rows_per_window - 1) / rows_per_window;
+  const long long cap = (long long)std::max(0, a.max_blocks_per_seq) * std::max(1, a.block_size);
+  const long long units = std::max(1LL, (long long)p.windows * std::max(1, a.num_kv_heads));
+  const long long target = 6LL * num_sms;  // about two waves of three resident CTAs per SM
+  long long nsplit = (target + units - 1) / units;
+  nsplit = std::max(1LL, std::min(nsplit, std::max(1LL, (cap + 1023) / 1024)));  // >= 1024 tokens a split
+  long long len = (cap + nsplit - 1) / nsplit;
+  len = std::max(32LL, (len + 31) / 32 * 32);
+  p.split_len = (int)std::min(len, (long long)1 << 30);
+  p.nsplit = (int)std::max(1LL, (cap + p.split_len - 1) / p.split_len);
+  p.workspace_bytes = (size_t)std::max(0, a.batch) * a.num_q_heads * p.nsplit * (a.head_dim + 2) * sizeof(float) + 16;
+  return p;
+}
+
+cudaError_t launch_prefill_mq(const DecodeArgs& a, const MqPlan& p, cudaStream_t stream) {
+  if (a.status) {
+    cudaError_t err = cudaMemsetAsync(a.status, 0, sizeof(int32_t), stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (a.batch == 0) return cudaSuccess;
+  MqArgs m;
+  m.a = a;
+  m.nsplit = p.nsplit;
+  m.split_len = p.split_len;
+  m.bs_shift = -1;
+  for (int k = 0; k < 31; ++k)
+    if (a.block_size == (1 << k)) m.bs_shift = k;
+  m.windows = p.windows;
+  m.part_acc = static_cast<float*>(a.workspace);
+  m.part_ml = m.part_acc + (size_t)a.batch * a.num_q_heads * p.nsplit * a.head_dim;
+  const long long grid = (long long)p.windows * p.nsplit * a.num_kv_heads;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  cudaError_t err = a.head_dim == 64 ? launch_mq_bits<64>(m, (int)grid, stream)
+                    : a.head_dim == 128 ? launch_mq_bits<128>(m, (int)grid, stream)
+                                        : cudaErrorInvalidValue;
+  if (err != cudaSuccess) return err;
+  return launch_combine_splits(m.part_acc, m.part_ml, a.batch * a.num_q_heads, p.nsplit, a.head_dim, a.signs, a.out,
+                               a.out_dtype, stream);
+}
+
+}  // namespace tq

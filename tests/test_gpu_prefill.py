@@ -121,3 +121,91 @@ def test_prefill_chunk_on_large_cache_sampled():
     pick = rng.choice(len(q_seq), size=24, replace=False)
     want = o.paged_prefill(q[pick], q_seq[pick], q_len[pick], kp, vp, kb, vb, bt, signs, kc, vc)
     _close(got[pick], want)
+
+
+# ---- the multi-query kernel (D 64/128, 2/4-bit K and V, G 1/2/4/8, any block size) ---------
+
+@pytest.mark.parametrize("d,kb,vb,hq,h,bs", [(128, 4, 4, 8, 8, 16), (128, 4, 4, 16, 8, 16), (128, 2, 2, 32, 8, 16),
+                                             (128, 2, 4, 32, 4, 16), (64, 2, 4, 16, 2, 8), (128, 4, 2, 64, 8, 32),
+                                             (64, 4, 4, 8, 8, 5)])
+def test_prefill_multi_query_shapes(d, kb, vb, hq, h, bs):
+    # windows of 64 / G query rows hold rows of several sequences (segments), chunks of
+    # several tokens, decode rows and a whole-sequence chunk
+    tq = _tq()
+    rng = np.random.default_rng(400 + d + 3 * kb + 5 * vb + hq + bs)
+    lens = [37, 16, 1, 70, 5, 130]
+    chunks = [9, 16, 1, 1, 3, 40]
+    bt, signs, kc, vc, kp, vp = _cache(rng, lens, d, h, kb, vb, bs=bs)
+    q_seq, q_len = _rows_for(lens, chunks)
+    q = rng.standard_normal((len(q_seq), hq, d)).astype(np.float32)
+    want = o.paged_prefill(q, q_seq, q_len, kp, vp, kb, vb, bt, signs, kc, vc)
+    _close(_run(tq, q, q_seq, q_len, kp, vp, bt, signs, kc, vc), want)
+
+
+def test_prefill_multi_query_unsorted_rows_and_token_splits():
+    # 3 sequences of up to 3000 tokens in a 4096-token table: the kernel splits the
+    # tokens (several partials per row); query rows in random order, so windows mix
+    # sequences; fp16 query and output
+    tq = _tq()
+    rng = np.random.default_rng(77)
+    d, kb, vb, hq, h = 128, 4, 4, 32, 8
+    lens = [3000, 2100, 1500]
+    bt, signs, kc, vc, kp, vp = _cache(rng, lens, d, h, kb, vb, random_rows=True)
+    bt = np.concatenate([bt, np.zeros((3, 256 - bt.shape[1]), dtype=np.int32)], axis=1)  # 4096-token table
+    q_seq, q_len = _rows_for(lens, [70, 33, 20])
+    perm = rng.permutation(len(q_seq))
+    q_seq, q_len = q_seq[perm], q_len[perm]
+    q = rng.standard_normal((len(q_seq), hq, d)).astype(np.float16)
+    dev = torch.device("cuda")
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)  # noqa: E731
+    out = tq.tq_paged_prefill(t(q), t(q_seq), t(q_len), t(kp), t(vp), t(bt), t(signs.astype(np.float32)), t(kc),
+                              t(vc), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    pick = rng.choice(len(q_seq), size=24, replace=False)
+    want = o.paged_prefill(q[pick].astype(np.float32), q_seq[pick], q_len[pick], kp, vp, kb, vb, bt, signs, kc, vc)
+    _close(got[pick], want)
+
+
+def test_prefill_multi_query_large_norm_rows():
+    # lognormal(0, 1) norms with 2% of rows x 8 and a query x 3: many tiles exceed the
+    # fast-score bound and take the exact key path
+    tq = _tq()
+    rng = np.random.default_rng(12)
+    d, kb, vb, hq, h, bs = 128, 4, 2, 32, 8, 16
+    lens = [300, 77]
+    nblk = sum(-(-n // bs) for n in lens) + 2
+    bt = np.zeros((2, -(-max(lens) // bs)), dtype=np.int32)
+    perm = rng.permutation(nblk).astype(np.int32)
+    bt[0, :-(-lens[0] // bs)] = perm[:-(-lens[0] // bs)]
+    bt[1, :-(-lens[1] // bs)] = perm[-(-lens[0] // bs):-(-lens[0] // bs) + -(-lens[1] // bs)]
+    signs = o.splitmix64_signs(d, 42)
+    kc, _ = o.codebook_f32(d, kb)
+    vc, _ = o.codebook_f32(d, vb)
+    pages = []
+    for bits in (kb, vb):
+        n = nblk * bs * h
+        nu = rng.lognormal(0.0, 1.0, size=n) * np.where(rng.random(n) < 0.02, 8.0, 1.0)
+        pages.append(o.make_rows(rng.integers(0, 1 << bits, size=(n, d)), nu.astype(np.float32), bits)
+                     .reshape(nblk, bs, h, -1))
+    q_seq, q_len = _rows_for(lens, [20, 7])
+    q = 3.0 * rng.standard_normal((len(q_seq), hq, d)).astype(np.float32)
+    want = o.paged_prefill(q, q_seq, q_len, pages[0], pages[1], kb, vb, bt, signs, kc, vc)
+    _close(_run(tq, q, q_seq, q_len, pages[0], pages[1], bt, signs, kc, vc), want)
+
+
+def test_prefill_multi_query_bad_block_is_skipped_and_reported():
+    tq = _tq()
+    rng = np.random.default_rng(31)
+    d, kb, vb, hq, h = 128, 4, 4, 32, 8
+    lens = [90, 40]
+    bt, signs, kc, vc, kp, vp = _cache(rng, lens, d, h, kb, vb)
+    bt[0, 2] = kp.shape[0] + 7  # tokens 32..47 of sequence 0 point outside the pages
+    q_seq, q_len = _rows_for(lens, [12, 5])
+    q = rng.standard_normal((len(q_seq), hq, d)).astype(np.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run(tq, q, q_seq, q_len, kp, vp, bt, signs, kc, vc, status=status)
+    assert int(status.item()) == tq.TQ_ERR_BLOCK_OUT_OF_RANGE
+    want, bad = o.paged_prefill(q, q_seq, q_len, kp, vp, kb, vb, bt, signs, kc, vc, return_flags=True)
+    assert bad
+    _close(got, want)
