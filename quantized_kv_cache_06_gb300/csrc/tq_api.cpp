@@ -224,6 +224,17 @@ tq_status decode_shape_check(int batch, int num_q_heads, int num_kv_heads, int h
   return ok();
 }
 
+// The decode kernel choice also depends on k_bits / v_bits, which the workspace queries do
+// not take: the largest workspace over the SIMT, tensor-core and multi-query plans.
+size_t decode_workspace_any_bits(tq::DecodeArgs a, int sms) {
+  a.k_bits = a.v_bits = 0;
+  size_t need = tq::plan_decode(a, sms).workspace_bytes;  // SIMT plan
+  need = std::max(need, tq::plan_prefill_mq(a, sms, true).workspace_bytes);
+  a.k_bits = a.v_bits = 4;  // the tensor-core plan where the shapes have one, else the multi-query plan
+  need = std::max(need, tq::plan_decode(a, sms).workspace_bytes);
+  return need;
+}
+
 tq::DecodeArgs make_decode_args(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                 int max_blocks_per_seq, int block_size) {
   tq::DecodeArgs a{};
@@ -279,21 +290,17 @@ tq_status decode_impl(const char* name, const void* q, tq_dtype q_dtype, int bat
   a.k_alpha = 1.0f;
   a.bt_rows = bt_rows;
   a.bt_num_rows = bt_num_rows;
+  if (batch > 0 && (tq::tc_decode_supported(a) || tq::prefill_mq_supported(a))) {
+    a.v_alpha = fp16_scale_for(head_dim, v_bits);
+    a.k_alpha = fp16_scale_for(head_dim, k_bits);
+  }
   if (bt_rows && tq::prefill_mq_supported(a)) {
     // mixed prefill/decode: query rows of one sequence share each dequantised key/value tile
-    if (batch > 0) {
-      a.v_alpha = fp16_scale_for(head_dim, v_bits);
-      a.k_alpha = fp16_scale_for(head_dim, k_bits);
-    }
-    const tq::MqPlan plan = tq::plan_prefill_mq(a, current_device_sms());
+    const tq::MqPlan plan = tq::plan_prefill_mq(a, current_device_sms(), false);
     if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
       return fail(TQ_ERR_INVALID_ARG, "%s: workspace must be >= %zu bytes and 16-byte aligned (got %zu)", name,
                   plan.workspace_bytes, workspace_bytes);
     return check_cuda(tq::launch_prefill_mq(a, plan, static_cast<cudaStream_t>(stream)), name);
-  }
-  if (batch > 0 && tq::tc_decode_supported(a)) {
-    a.v_alpha = fp16_scale_for(head_dim, v_bits);
-    a.k_alpha = fp16_scale_for(head_dim, k_bits);
   }
   const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());
   if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
@@ -393,15 +400,8 @@ size_t tq_paged_decode_workspace(int batch, int num_q_heads, int num_kv_heads, i
                                  int max_blocks_per_seq, int block_size) {
   if (decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size) != TQ_OK)
     return 0;
-  // The kernel choice also depends on k_bits / v_bits, which this query does not take:
-  // return the larger of the SIMT plan and the tensor-core plan.
   tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
-  const int sms = current_device_sms();
-  size_t need = tq::plan_decode(a, sms).workspace_bytes;  // k_bits = 0: SIMT plan
-  a.k_bits = 4;
-  a.v_bits = 4;
-  need = std::max(need, tq::plan_decode(a, sms).workspace_bytes);
-  return need;
+  return decode_workspace_any_bits(a, current_device_sms());
 }
 
 tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_heads,
@@ -427,7 +427,7 @@ size_t tq_paged_prefill_workspace(int num_q_rows, int num_q_heads, int num_kv_he
   if (need == 0) return 0;
   tq::DecodeArgs a =
       make_decode_args(num_q_rows, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
-  need = std::max(need, tq::plan_prefill_mq(a, current_device_sms()).workspace_bytes);
+  need = std::max(need, tq::plan_prefill_mq(a, current_device_sms(), false).workspace_bytes);
   return need;
 }
 
@@ -464,7 +464,7 @@ tq_status tq_paged_decode_static(const void* q, tq_dtype q_dtype, int batch, int
   tq_status st = decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
   if (st != TQ_OK) return st;
   tq::DecodeArgs shape = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
-  const size_t need = tq::plan_decode(shape, current_device_sms()).workspace_bytes;
+  const size_t need = decode_workspace_any_bits(shape, current_device_sms());
   if (need > capacity)
     return fail(TQ_ERR_INVALID_ARG,
                 "tq_paged_decode_static: these shapes need %zu bytes of scratch, more than the fixed %zu bytes; "

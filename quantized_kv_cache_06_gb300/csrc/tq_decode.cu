@@ -18,6 +18,9 @@
 //   combine_kernel       one warp per (sequence, q head): merges the splits,
 //                        divides by the softmax sum, applies R^T (in-register FWHT
 //                        and sign flip) and casts to the output dtype.
+// Kernel choice (plan_decode): the tensor-core decode (tq_decode_tc.cu) where it has an
+// instantiation, else the multi-query kernel with one sequence per window
+// (tq_prefill_mq.cu: D 64/128, 2/4-bit or equal 3/5-bit K/V), else the SIMT kernels.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -248,6 +251,15 @@ DecodePlan plan_decode(const DecodeArgs& a, int num_sms) {
     p.workspace_bytes = slots * a.num_q_heads * (a.head_dim + 2) * sizeof(float) + (a.batch + 1) * sizeof(int) + 16;
     return p;
   }
+  if (a.k_bits > 0 && prefill_mq_supported(a)) {
+    // shapes without a tensor-core decode instantiation (3/5-bit rows, block sizes other
+    // than 16, GQA groups 1/2): the multi-query kernel with one sequence per window
+    p.kernel = 3;
+    p.mq = plan_prefill_mq(a, num_sms, true);
+    p.num_splits = p.mq.nsplit;
+    p.workspace_bytes = p.mq.workspace_bytes;
+    return p;
+  }
   p.kernel = 1;
   const int units = std::max(1, a.batch * a.num_kv_heads);
   const int target = num_sms * 8;
@@ -283,6 +295,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t
   }
   if (a.batch == 0) return cudaSuccess;
   if (p.kernel == 2) return launch_decode_tc(a, p, stream);
+  if (p.kernel == 3) return launch_prefill_mq(a, p.mq, stream);
   SplitView part = split_view(a.workspace, a.batch, a.num_q_heads, p.num_splits, a.head_dim);
   switch (a.head_dim) {
     case 32: return launch_split<1>(a, p, part, stream);

@@ -42,11 +42,23 @@ cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream);
 bool write_tc_supported(const WriteArgs& a);
 cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid);
 
+// Multi-query attention (tq_prefill_mq.cu): windows of query rows against 32-token tiles
+// dequantised once into shared memory, split-K over tokens.  Mixed prefill/decode takes
+// windows of 64 / G rows; a plain decode of shapes without a tensor-core decode
+// instantiation takes one row (sequence) per window.
+struct MqPlan {
+  int nsplit;           // token splits per sequence
+  int split_len;        // tokens per split
+  int windows;          // CTAs per (split, kv head)
+  int rows_per_window;  // query rows per CTA
+  size_t workspace_bytes;
+};
 struct DecodePlan {
   int kernel;            // which decode kernel runs (see tq_decode.cu)
   int num_splits;        // split-K factor per sequence
   int blocks_per_split;  // KV blocks per split
   size_t workspace_bytes;
+  MqPlan mq;             // kernel 3: the multi-query kernel, one sequence per window
 };
 
 struct DecodeArgs {
@@ -98,16 +110,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStrea
 // The same launch for a batch with a block-table row map (tq_prefill_tc.cu).
 cudaError_t launch_decode_tc_rowmap(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 
-// Multi-query mixed prefill/decode (tq_prefill_mq.cu): windows of query rows against
-// 32-token tiles dequantised once into shared memory, split-K over tokens.
-struct MqPlan {
-  int nsplit;     // token splits per sequence
-  int split_len;  // tokens per split
-  int windows;    // CTAs per (split, kv head)
-  size_t workspace_bytes;
-};
 bool prefill_mq_supported(const DecodeArgs& a);
-MqPlan plan_prefill_mq(const DecodeArgs& a, int num_sms);
+MqPlan plan_prefill_mq(const DecodeArgs& a, int num_sms, bool one_row_per_window);
 // Enqueues status reset, the multi-query kernel and the split combine.
 cudaError_t launch_prefill_mq(const DecodeArgs& a, const MqPlan& p, cudaStream_t stream);
 

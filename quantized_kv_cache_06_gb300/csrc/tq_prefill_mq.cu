@@ -19,9 +19,11 @@
 // query is split into fp16 hi + lo, and the score is hi*Khat + lo*Khat (+ hi*Klo when
 // nu_k * ||q|| can exceed kMqFastBound), which keeps it at fp32-level accuracy.
 //
-// Work split.  CTA (window, split, kv head): a window is 64 / G consecutive query rows
-// (64 rows of the MMA: 4 warps x 16), a split a range of split_len tokens of the
-// sequence.  Rows of a window that belong to different sequences form segments, taken one
+// Work split.  CTA (window, split, kv head): a window is up to 64 / G consecutive query
+// rows (64 rows of the MMA: 4 warps x 16), a split a range of split_len tokens of the
+// sequence.  tq_paged_prefill takes full windows; tq_paged_decode takes one-row windows
+// for the shapes its tensor-core kernel does not cover (3/5-bit rows, block sizes other
+// than 16, GQA groups 1 and 2).  Rows of a window that belong to different sequences form segments, taken one
 // after the other (each streams its own sequence; rows outside the segment are masked).
 // The CTA writes one (m, l, acc[D]) partial per (row, q head, split); the split combine
 // (shared with the SIMT decode) merges them and applies R^T.
@@ -155,6 +157,7 @@ struct MqArgs {
   int split_len;  // tokens per split (multiple of 32)
   int bs_shift;   // log2(block_size) when it is a power of two, else -1
   int windows;    // ceil(rows / rows_per_window)
+  int rows_per_window;  // query rows per CTA, 1 .. 64 / G (1: a decode batch, one row per sequence)
   float* part_acc;  // [rows * Hq][nsplit][D]
   float* part_ml;   // [rows * Hq][nsplit][2]
 };
@@ -193,8 +196,8 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
   const int h = blockIdx.x % H;
   const int split = (blockIdx.x / H) % args.nsplit;
   const int window = blockIdx.x / (H * args.nsplit);
-  const int i0 = window * MQ;
-  const int nrows = min(MQ, a.batch - i0);
+  const int i0 = window * args.rows_per_window;
+  const int nrows = min(args.rows_per_window, a.batch - i0);
   const int bs = a.block_size;
   const int cap = a.max_blocks_per_seq * bs;
   const uint32_t sbase = smem_addr(smem);
@@ -632,6 +635,8 @@ cudaError_t launch_mq_bits(const MqArgs& m, int grid, cudaStream_t stream) {
   if (kb == 4 && vb == 2) return launch_mq_g<D, 4, 2>(m, grid, stream);
   if (kb == 2 && vb == 4) return launch_mq_g<D, 2, 4>(m, grid, stream);
   if (kb == 2 && vb == 2) return launch_mq_g<D, 2, 2>(m, grid, stream);
+  if (kb == 3 && vb == 3) return launch_mq_g<D, 3, 3>(m, grid, stream);
+  if (kb == 5 && vb == 5) return launch_mq_g<D, 5, 5>(m, grid, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -639,21 +644,26 @@ cudaError_t launch_mq_bits(const MqArgs& m, int grid, cudaStream_t stream) {
 
 bool prefill_mq_supported(const DecodeArgs& a) {
   const int G = a.num_kv_heads > 0 ? a.num_q_heads / a.num_kv_heads : 0;
-  const bool bits = (a.k_bits == 2 || a.k_bits == 4) && (a.v_bits == 2 || a.v_bits == 4);
+  // exactly the instantiations in launch_mq_bits
+  const bool bits = ((a.k_bits == 2 || a.k_bits == 4) && (a.v_bits == 2 || a.v_bits == 4)) ||
+                    (a.k_bits == a.v_bits && (a.k_bits == 3 || a.k_bits == 5));
   return (a.head_dim == 64 || a.head_dim == 128) && bits && (G == 1 || G == 2 || G == 4 || G == 8) &&
          a.block_size >= 1;
 }
 
-MqPlan plan_prefill_mq(const DecodeArgs& a, int num_sms) {
+MqPlan plan_prefill_mq(const DecodeArgs& a, int num_sms, bool one_row_per_window) {
   MqPlan p{};
   const int G = std::max(1, a.num_kv_heads > 0 ? a.num_q_heads / a.num_kv_heads : 1);
-  const int rows_per_window = std::max(1, kMqRows / G);
+  const int rows_per_window = one_row_per_window ? 1 : std::max(1, kMqRows / G);
+  p.rows_per_window = rows_per_window;
   p.windows = (std::max(0, a.batch) + rows_per_window - 1) / rows_per_window;
   const long long cap = (long long)std::max(0, a.max_blocks_per_seq) * std::max(1, a.block_size);
   const long long units = std::max(1LL, (long long)p.windows * std::max(1, a.num_kv_heads));
   const long long target = 6LL * num_sms;  // about two waves of three resident CTAs per SM
   long long nsplit = (target + units - 1) / units;
-  nsplit = std::max(1LL, std::min(nsplit, std::max(1LL, (cap + 1023) / 1024)));  // >= 1024 tokens a split
+  // splits of >= 1024 tokens (>= 256 for one-row windows, whose partials are small)
+  const long long min_len = one_row_per_window ? 256 : 1024;
+  nsplit = std::max(1LL, std::min(nsplit, std::max(1LL, (cap + min_len - 1) / min_len)));
   long long len = (cap + nsplit - 1) / nsplit;
   len = std::max(32LL, (len + 31) / 32 * 32);
   p.split_len = (int)std::min(len, (long long)1 << 30);
@@ -676,6 +686,7 @@ cudaError_t launch_prefill_mq(const DecodeArgs& a, const MqPlan& p, cudaStream_t
   for (int k = 0; k < 31; ++k)
     if (a.block_size == (1 << k)) m.bs_shift = k;
   m.windows = p.windows;
+  m.rows_per_window = p.rows_per_window;
   m.part_acc = static_cast<float*>(a.workspace);
   m.part_ml = m.part_acc + (size_t)a.batch * a.num_q_heads * p.nsplit * a.head_dim;
   const long long grid = (long long)p.windows * p.nsplit * a.num_kv_heads;
