@@ -1,4 +1,4 @@
-// Tensor-core packed-KV row writer (fp16 / bf16 rows, head_dim 64 or 128, 2 or 4 bits).
+// Tensor-core packed-KV row writer (fp16 / bf16 rows, head_dim 64 or 128, 2 to 5 bits).
 //
 // TurboQuant docs: "vLLM Usage" (TQ Byte Layout, Slot Mapping, TQ Packed Page Contract:
 // write_tq4_kv) and "Architecture" (PackedPageCache).
@@ -17,7 +17,10 @@
 //    entries) so the lookups are conflict free.
 //  * Packing.  Bytes are assembled per row in shared memory (LSB-first fields, then the
 //    fp32 norm); a token's H rows are contiguous in the page (H * row_bytes bytes), so the
-//    warp stores whole token slabs with 16-byte stores.
+//    warp stores whole token slabs with 16-byte stores.  4-bit fields fill a byte per
+//    lane pair of coordinates, 2-bit ones a byte per quad; 3- and 5-bit fields cross
+//    bytes, so their index pairs are staged (in the raw tile buffer the MMAs have
+//    consumed) and each lane then packs 32 coordinates of a row into 3 or 5 whole words.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
   };
 
   // chunk i of a tile belongs to token i / d, d = H * RB / 16: a reciprocal multiply,
-  // (i * ceil(2^16 / d)) >> 16, exact for i < 2^16 / d -- here i < RB <= 68 and d <= 68
+  // (i * ceil(2^16 / d)) >> 16, exact for i < 2^16 / d -- here i < RB <= 84 and d <= 84
   const uint32_t cpt = (uint32_t)(H * RB / 16 > 0 ? H * RB / 16 : 1);
   const uint32_t inv_cpt = (65536u + cpt - 1) / cpt;
   int64_t tile = (int64_t)blockIdx.x * kWWarps + warp;
@@ -343,6 +346,10 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
       return lo + (g > __uint_as_float(pt) ? 1u : 0u);
     };
     const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
+    // 3/5 bits: index pairs (2 BITS bits each) of row rr, coordinates 2p, 2p + 1, at
+    // stage[rr * D / 2 + p]; the tile's raw buffer is free once its MMAs have read it
+    uint16_t* stage = reinterpret_cast<uint16_t*>(raw_buf + buf * TILE_BYTES);
+    static_assert(16 * D <= TILE_BYTES, "index staging must fit the raw tile buffer");
 #pragma unroll
     for (int half = 0; half < 2; ++half) {  // row r (half 0) / row r + 8 (half 1)
       const float ga = half ? ga1 : ga0;
@@ -357,7 +364,9 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
           const uint32_t i0 = quant(g.x, m.x);
           const uint32_t i1 = quant(g.y, m.y);
           // columns 16 j + 8 nt + 2c, +1
-          if (BITS == 4) {
+          if (BITS == 3 || BITS == 5) {
+            stage[(r + 8 * half) * (D / 2) + 8 * j + 4 * nt + c] = (uint16_t)(i0 | (i1 << BITS));
+          } else if (BITS == 4) {
             prow[8 * j + 4 * nt + c] = (unsigned char)(i0 + (i1 << 4));
           } else {
             // 2 bits: byte 4 j + 2 nt + c/2 holds columns 16 j + 8 nt + 4 (c/2) .. +3
@@ -370,6 +379,31 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
       if (c == 0) *reinterpret_cast<float*>(prow + IB) = half ? nu1 : nu0;
     }
     __syncwarp();
+    if constexpr (BITS == 3 || BITS == 5) {
+      // group = 32 coordinates (16 pairs) of one row -> BITS words at byte 4 BITS q of the row
+      constexpr int GPR = D / 32;  // groups per row
+#pragma unroll
+      for (int k = 0; k < 16 * GPR / 32; ++k) {
+        const int g = lane + 32 * k, row = g / GPR, q = g % GPR;
+        const uint4* src = reinterpret_cast<const uint4*>(stage + row * (D / 2) + q * 16);
+        const uint4 v0 = src[0], v1 = src[1];
+        const uint32_t w8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t out[BITS];
+#pragma unroll
+        for (int w = 0; w < BITS; ++w) out[w] = 0u;
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {  // pair p: 2 BITS bits at stream bit 2 BITS p
+          const uint32_t pv = (w8[p >> 1] >> (16 * (p & 1))) & ((1u << (2 * BITS)) - 1u);
+          const int bit = 2 * BITS * p, w = bit >> 5, sh = bit & 31;
+          out[w] |= pv << sh;
+          if (sh + 2 * BITS > 32) out[w + 1] |= pv >> (32 - sh);
+        }
+        uint32_t* dst = reinterpret_cast<uint32_t*>(pack_buf + row * RB + q * 4 * BITS);
+#pragma unroll
+        for (int w = 0; w < BITS; ++w) dst[w] = out[w];
+      }
+      __syncwarp();
+    }
 
     // ---- store: token slabs (H rows) or single rows ---------------------------------
     const int64_t row0 = tile * 16;
@@ -410,7 +444,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
 bool write_tc_supported(const WriteArgs& a) {
   const bool dt = a.dtype == kF16 || a.dtype == kBF16;
   const bool hd = a.head_dim == 64 || a.head_dim == 128;
-  const bool bt = a.bits == 2 || a.bits == 4;
+  const bool bt = a.bits >= 2 && a.bits <= 5;
   return dt && hd && bt && a.num_kv_heads >= 1;
 }
 
@@ -428,10 +462,12 @@ cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
     return cudaGetLastError();                                                                                \
   }
   if (a.dtype == kF16) {
-    TQ_WTC(__half, 64, 2) TQ_WTC(__half, 64, 4) TQ_WTC(__half, 128, 2) TQ_WTC(__half, 128, 4)
+    TQ_WTC(__half, 64, 2) TQ_WTC(__half, 64, 3) TQ_WTC(__half, 64, 4) TQ_WTC(__half, 64, 5)
+    TQ_WTC(__half, 128, 2) TQ_WTC(__half, 128, 3) TQ_WTC(__half, 128, 4) TQ_WTC(__half, 128, 5)
   } else if (a.dtype == kBF16) {
-    TQ_WTC(__nv_bfloat16, 64, 2) TQ_WTC(__nv_bfloat16, 64, 4) TQ_WTC(__nv_bfloat16, 128, 2)
-    TQ_WTC(__nv_bfloat16, 128, 4)
+    TQ_WTC(__nv_bfloat16, 64, 2) TQ_WTC(__nv_bfloat16, 64, 3) TQ_WTC(__nv_bfloat16, 64, 4)
+    TQ_WTC(__nv_bfloat16, 64, 5) TQ_WTC(__nv_bfloat16, 128, 2) TQ_WTC(__nv_bfloat16, 128, 3)
+    TQ_WTC(__nv_bfloat16, 128, 4) TQ_WTC(__nv_bfloat16, 128, 5)
   }
 #undef TQ_WTC
   return cudaErrorInvalidValue;

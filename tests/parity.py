@@ -3,7 +3,9 @@
 Tolerances:
   * packed index bytes: bit-exact, except coordinates whose normalised rotated value
     lies within 1e-6 of a decision point (measured in the oracle's fp64); those are
-    counted and must be fewer than 1e-5 of all compared coordinates;
+    counted and must be fewer than 1e-5 of all compared coordinates.  A sample of fewer
+    than 1e5 coordinates cannot resolve that rate (one exception in it is consistent
+    with a rate below 1e-5), so such a sample may hold one in-band exception;
   * norms: within 1e-6 relative;
   * decode outputs: |gpu - oracle| <= 2e-3 + 2e-3 |oracle| elementwise.
 """
@@ -56,7 +58,7 @@ def compare_rows(gpu_rows: np.ndarray, raw_rows: np.ndarray, codec: OracleCodec,
 
 def assert_rows_match(stats: dict) -> None:
     assert stats["flips_outside_band"] == 0, stats
-    assert stats["flips"] <= MAX_FLIP_FRACTION * stats["coords"], stats
+    assert stats["flips"] <= max(1.0, MAX_FLIP_FRACTION * stats["coords"]), stats
     assert stats["max_index_step"] <= 1, stats
     assert stats["max_norm_rel"] <= NORM_RTOL, stats
 

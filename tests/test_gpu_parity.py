@@ -347,10 +347,11 @@ def test_tc_decode_many_short_sequences(tq):
 
 
 # ---------------------------------------------------------------- tensor-core writer shapes
-# (fp16 / bf16 rows, head_dim 64 or 128, 2 or 4 bits; H dividing the 16-row tile or not)
+# (fp16 / bf16 rows, head_dim 64 or 128, 2 to 5 bits; H dividing the 16-row tile or not;
+# 3- and 5-bit fields cross bytes)
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d,bits", [(64, 2), (64, 4), (128, 2), (128, 4)])
+@pytest.mark.parametrize("d,bits", [(64, 2), (64, 3), (64, 4), (64, 5), (128, 2), (128, 3), (128, 4), (128, 5)])
 @pytest.mark.parametrize("h", [1, 3, 8, 16])
 def test_tc_writer_shapes(tq, dtype, d, bits, h):
     rng = np.random.default_rng(d * 7 + bits * 3 + h)
