@@ -251,9 +251,11 @@ DecodePlan plan_decode(const DecodeArgs& a, int num_sms) {
     p.workspace_bytes = slots * a.num_q_heads * (a.head_dim + 2) * sizeof(float) + (a.batch + 1) * sizeof(int) + 16;
     return p;
   }
-  if (a.k_bits > 0 && prefill_mq_supported(a)) {
+  if (a.k_bits > 0 && a.head_dim <= 128 && prefill_mq_supported(a)) {
     // shapes without a tensor-core decode instantiation (3/5-bit rows, block sizes other
-    // than 16, GQA groups 1/2): the multi-query kernel with one sequence per window
+    // than 16, GQA groups 1/2): the multi-query kernel with one sequence per window.  Its
+    // D = 256 form (one 8-warp CTA per SM) is no faster than the SIMT kernel for one row
+    // per window, so D = 256 decodes stay on the SIMT kernel.
     p.kernel = 3;
     p.mq = plan_prefill_mq(a, num_sms, true);
     p.num_splits = p.mq.nsplit;

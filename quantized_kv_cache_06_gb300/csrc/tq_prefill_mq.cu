@@ -22,8 +22,10 @@
 // Work split.  CTA (window, split, kv head): a window is up to 64 / G consecutive query
 // rows (64 rows of the MMA: 4 warps x 16), a split a range of split_len tokens of the
 // sequence.  tq_paged_prefill takes full windows; tq_paged_decode takes one-row windows
-// for the shapes its tensor-core kernel does not cover (3/5-bit rows, block sizes other
-// than 16, GQA groups 1 and 2).  Rows of a window that belong to different sequences form segments, taken one
+// for the D 64/128 shapes its tensor-core kernel does not cover (3/5-bit rows, block
+// sizes other than 16, GQA groups 1 and 2).  D = 256 runs 8 warps: two per row group,
+// each with half of the dimensions (query fragments, score k-steps, value n-tiles); the
+// half scores are summed through shared memory between the pair's two warps.  Rows of a window that belong to different sequences form segments, taken one
 // after the other (each streams its own sequence; rows outside the segment are masked).
 // The CTA writes one (m, l, acc[D]) partial per (row, q head, split); the split combine
 // (shared with the SIMT decode) merges them and applies R^T.
@@ -45,9 +47,8 @@
 namespace tq {
 namespace {
 
-constexpr int kMqWarps = 4;
-constexpr int kMqThreads = 32 * kMqWarps;
-constexpr int kMqRows = 16 * kMqWarps;  // MMA rows (query row x q head) per CTA
+constexpr int kMqGroups = 4;             // 16-row MMA groups per CTA
+constexpr int kMqRows = 16 * kMqGroups;  // MMA rows (query row x q head) per CTA
 constexpr int kMqTile = 32;             // tokens per tile
 constexpr float kMqLog2e = 1.4426950408889634f;
 // Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored without the fp16
@@ -57,6 +58,18 @@ constexpr float kMqSlack = 6.0f;  // log2 units the running max may lag behind t
 
 constexpr int kMqStages = 4;  // raw-word ring: tiles it .. it + 2 in flight while tile it is used
 
+// Warps per CTA.  D <= 128: one warp per 16-row group.  D = 256: two warps per group,
+// each holding the query, the score contraction and the value accumulators of one half of
+// the dimensions; the two half scores are summed through shared memory.
+template <int D>
+struct MqShape {
+  static constexpr bool kSplit = D == 256;
+  static constexpr int kWarps = kSplit ? 2 * kMqGroups : kMqGroups;
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kDh = kSplit ? D / 2 : D;  // dimensions per warp
+  static constexpr int kMinBlocks = kSplit ? 1 : 3;
+};
+
 template <int D, int KB, int VB>
 struct MqSmem {
   static constexpr int kRow = 2 * D;                  // bytes per fp16 row
@@ -64,8 +77,8 @@ struct MqSmem {
   static constexpr int kOffKhi = 0;                   // [32 tokens][D], swizzled
   static constexpr int kOffKlo = kOffKhi + kTileBytes;
   static constexpr int kOffV = kOffKlo + kTileBytes;
-  static constexpr int kOffQlo = kOffV + kTileBytes;  // [warp][16 rows][D], swizzled
-  static constexpr int kOffKn = kOffQlo + kMqWarps * 16 * kRow;  // float[32] key norms
+  static constexpr int kOffQlo = kOffV + kTileBytes;  // [group][16 rows][D], swizzled
+  static constexpr int kOffKn = kOffQlo + kMqGroups * 16 * kRow;  // float[32] key norms
   static constexpr int kOffVn = kOffKn + kMqTile * 4;            // float[32] value norms
   static constexpr int kOffKadd = kOffVn + kMqTile * 4;          // float[32] 0 / -inf per token
   static constexpr int kOffSeq = kOffKadd + kMqTile * 4;         // int[64] table row per window row
@@ -74,21 +87,24 @@ struct MqSmem {
   // Raw-word ring, private to each thread: per stage and thread, for each of its
   // dequantisation tasks the index words, the norm, and an "in range" flag; stored
   // word-major ([stage][word][thread]) so a warp's accesses are conflict free.
-  static constexpr int kTasks = (2 * kMqTile * (D / 32)) / kMqThreads;  // tasks per thread
+  static constexpr int kThreads = MqShape<D>::kThreads;
+  static constexpr int kTasks = (2 * kMqTile * (D / 32)) / kThreads;  // tasks per thread
   static constexpr int kMaxBits = KB > VB ? KB : VB;
   static constexpr int kTaskWords = kMaxBits + 2;                       // words, norm, flag
   static constexpr int kRingWords = kTasks * kTaskWords;                // per thread per stage
-  static constexpr int kOffRing = (kOffQn + kMqWarps * 4 + 15) / 16 * 16;
-  static constexpr int kBytes = kOffRing + kMqStages * kRingWords * kMqThreads * 4;
-  static constexpr int kAlloc = kBytes + 256;  // + the pad that aligns the base to 256 bytes
+  static constexpr int kOffRing = (kOffQn + MqShape<D>::kWarps * 4 + 15) / 16 * 16;
+  // D = 256: per warp and lane the 16 half-score partials exchanged with the partner warp
+  static constexpr int kOffX = kOffRing + kMqStages * kRingWords * kThreads * 4;
+  static constexpr int kBytes = kOffX + (MqShape<D>::kSplit ? MqShape<D>::kWarps * 32 * 16 * 4 : 0);
+  static constexpr int kAlloc = kBytes + 1024;  // + the pad that aligns the base to 1024 bytes
   // the query hi parts are staged in the key tiles before the first tile
-  static_assert(2 * kTileBytes == kMqWarps * 16 * kRow, "query staging must fit the key tiles");
+  static_assert(2 * kTileBytes == kMqGroups * 16 * kRow, "query staging must fit the key tiles");
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a [rows][D] fp16 tile: the chunk
 // index is XORed with row % 8, so the 8 rows of an ldmatrix hit 8 different bank groups.
-// Region bases are multiples of 1024 bytes and rows are 2D >= 128 bytes, so the chunk
-// bits (4..7) of a row's address are free: for a compile-time step k,
+// Region bases are multiples of 1024 bytes and rows are 2D bytes, so the chunk bits
+// (4 .. 3 + log2(D / 8)) of a row's address are free: for a compile-time step k,
 // swz(row, c ^ k) = swz(row, c) ^ (k << 4), one LOP3 per address.
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -147,6 +163,9 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ void bar_pair(int id) {  // the two warps of one row group
+  asm volatile("bar.sync %0, 64;\n" ::"r"(id) : "memory");
+}
 __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
 }
@@ -172,26 +191,31 @@ struct RawTask {
 };
 
 template <int D, int KB, int VB, int G>
-__global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) {
+__global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) prefill_mq_kernel(MqArgs args) {
   using S = MqSmem<D, KB, VB>;
+  using SH = MqShape<D>;
+  constexpr int kThreads = SH::kThreads;
+  constexpr bool SPLIT = SH::kSplit;
   constexpr int P = D / 32;                  // 32-coordinate parts per row
   constexpr int E = D / 32;                  // query coordinates per lane
-  constexpr int KS = D / 16;                 // score k-steps
-  constexpr int NT = D / 8;                  // value n-tiles
+  constexpr int KS = SH::kDh / 16;           // score k-steps of this warp
+  constexpr int NT = SH::kDh / 8;            // value n-tiles of this warp
   constexpr int MQ = kMqRows / G;            // query rows per window
   constexpr int TASKS = 2 * kMqTile * P;     // K and V tasks of one tile
-  constexpr int TPT = TASKS / kMqThreads;    // tasks per thread
+  constexpr int TPT = TASKS / kThreads;      // tasks per thread
   constexpr int MAXB = KB > VB ? KB : VB;
   static_assert(TPT == 1 || TPT == 2, "one or two dequantisation tasks per thread");
   static_assert(TPT == S::kTasks, "task count");
-  static_assert(TPT == 2 || kMqThreads == 2 * kMqTile * P, "one K and one V task set");
+  static_assert(TPT == 2 || kThreads == 2 * kMqTile * P, "one K and one V task set");
   static_assert(kMqRows % G == 0, "group must divide the rows of a CTA");
 
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // region offsets assume a 256-byte aligned base (the XOR addressing needs bits 4..7 free)
-  unsigned char* smem = smem_raw + ((256u - (smem_addr(smem_raw) & 255u)) & 255u);
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const DecodeArgs& a = args.a;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grp = warp % kMqGroups;  // this warp's 16 MMA rows: group grp
+  const int dh = warp / kMqGroups;   // and dimensions [dh Dh, dh Dh + Dh) (D = 256), else 0
   const int H = a.num_kv_heads, Hq = a.num_q_heads;
   const int h = blockIdx.x % H;
   const int split = (blockIdx.x / H) % args.nsplit;
@@ -226,11 +250,11 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kMqLog2e / sqrtf((float)D);
   const float inv_alpha_k = 1.0f / a.k_alpha;
-  const uint32_t qhi_base = sbase + S::kOffKhi + warp * 16 * S::kRow;  // staging in the key tiles
-  const uint32_t qlo_base = sbase + S::kOffQlo + warp * 16 * S::kRow;
+  const uint32_t qhi_base = sbase + S::kOffKhi + grp * 16 * S::kRow;  // staging in the key tiles
+  const uint32_t qlo_base = sbase + S::kOffQlo + grp * 16 * S::kRow;
   float qn = 0.f;
   for (int m = 0; m < 16; ++m) {
-    const int mr = warp * 16 + m;
+    const int mr = grp * 16 + m;
     const int wrow = mr / G;
     float v[E];
     if (wrow < nrows) {
@@ -261,7 +285,11 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
     const uint32_t off = swz<D>(m, (lane * E) >> 3) + (uint32_t)(((lane * E) & 7) * 2);
     unsigned char* ph = smem + (qhi_base - sbase) + off;
     unsigned char* pl = smem + (qlo_base - sbase) + off;
-    if constexpr (E == 4) {
+    if (dh != 0) continue;  // D = 256: the group's first warp writes the staging
+    if constexpr (E == 8) {
+      *reinterpret_cast<uint4*>(ph) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(pl) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    } else if constexpr (E == 4) {
       *reinterpret_cast<uint2*>(ph) = make_uint2(hi[0], hi[1]);
       *reinterpret_cast<uint2*>(pl) = make_uint2(lo[0], lo[1]);
     } else {
@@ -270,17 +298,17 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
     }
   }
   if (lane == 0) qn_s[warp] = qn;
-  __syncwarp();
+  __syncthreads();  // row metadata, query norms and query staging visible
   const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: this lane addresses row rr of matrix mi
-  // A fragments (16 rows x 16 k): matrix mi = rows (mi & 1) * 8.., k chunk 2 ks + (mi >> 1)
+  // A fragments (16 rows x 16 k): matrix mi = rows (mi & 1) * 8.., k chunk 2 ks + (mi >> 1);
+  // this warp's k-steps are dh KS .. dh KS + KS - 1
   const uint32_t qa_lane = swz<D>((mi & 1) * 8 + rr, mi >> 1);
   uint32_t qh[KS][4];
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) ldsm_x4(qh[ks], (qhi_base + qa_lane) ^ (uint32_t)(ks << 5));
-  __syncthreads();  // row metadata and query norms visible; query staging read by every warp
+  for (int ks = 0; ks < KS; ++ks) ldsm_x4(qh[ks], (qhi_base + qa_lane) ^ (uint32_t)((dh * KS + ks) << 5));
   float qn_cta = 0.f;
 #pragma unroll
-  for (int w = 0; w < kMqWarps; ++w) qn_cta = fmaxf(qn_cta, qn_s[w]);
+  for (int w = 0; w < SH::kWarps; ++w) qn_cta = fmaxf(qn_cta, qn_s[w]);
 
   // ---- per-lane softmax state: rows r and r + 8 of this warp's 16 --------------------
   const int r = lane >> 2, c = lane & 3;
@@ -304,8 +332,8 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
   }
 
   // task j of this thread: component (0 K, 1 V), token t of the tile, part (32
-  // coordinates).  D = 128: task 0 is K and task 1 is V of (t, part) = (tid / 4, tid % 4);
-  // D = 64: warps 0-1 take K tasks and warps 2-3 V tasks (warp-uniform).
+  // coordinates).  D = 128 / 256: task 0 is K and task 1 is V of (t, part) =
+  // (tid / P, tid % P); D = 64: warps 0-1 take K tasks and warps 2-3 V tasks (warp-uniform).
   auto task_comp = [&](int j) -> int { return TPT == 2 ? j : (tid >= kMqTile * P ? 1 : 0); };
   auto task_rem = [&](int j) -> int { return TPT == 2 ? tid : tid % (kMqTile * P); };
   auto task_tok = [&](int j) -> int { return task_rem(j) / P; };
@@ -339,7 +367,7 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
     if (seq >= 0 && t_beg < t_end) {
       const int32_t* bt = a.block_table + (int64_t)seq * a.max_blocks_per_seq;
       // lengths of this lane's two rows (0 outside the segment)
-      const int wA = (warp * 16 + r) / G, wB = (warp * 16 + r + 8) / G;
+      const int wA = (grp * 16 + r) / G, wB = (grp * 16 + r + 8) / G;
       const int lenA = (wA >= s0 && wA < s1) ? row_len[wA] : 0;
       const int lenB = (wB >= s0 && wB < s1) ? row_len[wB] : 0;
       const int ntiles = (t_end - t_beg + kMqTile - 1) / kMqTile;
@@ -350,7 +378,7 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
       };
       // ring word w of this thread in stage st
       auto ring = [&](int st, int w) -> uint32_t {
-        return sbase + S::kOffRing + (uint32_t)(((st * S::kRingWords + w) * kMqThreads + tid) * 4);
+        return sbase + S::kOffRing + (uint32_t)(((st * S::kRingWords + w) * kThreads + tid) * 4);
       };
       // Starts the copies of task j of `tile` (block `bid`) into ring stage tile % kMqStages.
       auto issue_task = [&](auto bits_tag, int tile, int j, int bid) {
@@ -485,8 +513,8 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
             uint32_t ql[4];
-            ldsm_x4(ql, ql_lane ^ (uint32_t)(ks << 5));
-            const uint32_t kaddr = kb_lane ^ (uint32_t)(ks << 5);
+            ldsm_x4(ql, ql_lane ^ (uint32_t)((dh * KS + ks) << 5));
+            const uint32_t kaddr = kb_lane ^ (uint32_t)((dh * KS + ks) << 5);
 #pragma unroll
             for (int jp = 0; jp < 2; ++jp) {
               const uint32_t koff = kaddr + (uint32_t)(jp * 16 * S::kRow);  // tokens 16 jp ..
@@ -507,6 +535,21 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
         };
         if (exact) scores(std::true_type{});
         else scores(std::false_type{});
+        if constexpr (SPLIT) {  // sum the two half-dimension scores of the row group
+          float4* xb = reinterpret_cast<float4*>(smem + S::kOffX);
+#pragma unroll
+          for (int jn = 0; jn < 4; ++jn) xb[(warp * 32 + lane) * 4 + jn] = make_float4(s[jn][0], s[jn][1], s[jn][2], s[jn][3]);
+          bar_pair(1 + grp);
+          const int partner = warp ^ kMqGroups;
+#pragma unroll
+          for (int jn = 0; jn < 4; ++jn) {
+            const float4 pv = xb[(partner * 32 + lane) * 4 + jn];
+            s[jn][0] += pv.x;  // fp addition commutes: both warps get the same sums
+            s[jn][1] += pv.y;
+            s[jn][2] += pv.z;
+            s[jn][3] += pv.w;
+          }
+        }
 
         // scores: x nu_k, invalid tokens -inf, causal mask per row
 #pragma unroll
@@ -572,7 +615,7 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
 #pragma unroll
           for (int dp = 0; dp < NT / 2; ++dp) {
             uint32_t vb[4];
-            ldsm_x4_t(vb, (vb_lane ^ (uint32_t)(dp << 5)) + (uint32_t)(s2 * 16 * S::kRow));
+            ldsm_x4_t(vb, (vb_lane ^ (uint32_t)((dh * (NT / 2) + dp) << 5)) + (uint32_t)(s2 * 16 * S::kRow));
             mma_f16(o[2 * dp], pa[s2], vb[0], vb[1]);
             mma_f16(o[2 * dp + 1], pa[s2], vb[2], vb[3]);
           }
@@ -590,16 +633,16 @@ __global__ void __launch_bounds__(kMqThreads, 3) prefill_mq_kernel(MqArgs args) 
     float l = l_run[hr];
     l += __shfl_xor_sync(kFullMask, l, 1);
     l += __shfl_xor_sync(kFullMask, l, 2);
-    const int mr = warp * 16 + r + 8 * hr;
+    const int mr = grp * 16 + r + 8 * hr;
     const int wrow = mr / G;
     if (wrow < nrows) {
       const int64_t slot = ((int64_t)(i0 + wrow) * Hq + (int64_t)h * G + mr % G) * args.nsplit + split;
-      float* acc = args.part_acc + slot * D;
+      float* acc = args.part_acc + slot * D + dh * SH::kDh;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         *reinterpret_cast<float2*>(acc + 8 * nt + 2 * c) =
             make_float2(o[nt][2 * hr] * inv_alpha_v, o[nt][2 * hr + 1] * inv_alpha_v);
-      if (c == 0) {
+      if (c == 0 && dh == 0) {
         args.part_ml[slot * 2 + 0] = m_run[hr];
         args.part_ml[slot * 2 + 1] = l;
       }
@@ -613,7 +656,7 @@ cudaError_t launch_mq_one(const MqArgs& m, int grid, cudaStream_t stream) {
   auto kern = prefill_mq_kernel<D, KB, VB, G>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err != cudaSuccess) return err;
-  kern<<<grid, kMqThreads, bytes, stream>>>(m);
+  kern<<<grid, MqShape<D>::kThreads, bytes, stream>>>(m);
   return cudaGetLastError();
 }
 
@@ -647,7 +690,7 @@ bool prefill_mq_supported(const DecodeArgs& a) {
   // exactly the instantiations in launch_mq_bits
   const bool bits = ((a.k_bits == 2 || a.k_bits == 4) && (a.v_bits == 2 || a.v_bits == 4)) ||
                     (a.k_bits == a.v_bits && (a.k_bits == 3 || a.k_bits == 5));
-  return (a.head_dim == 64 || a.head_dim == 128) && bits && (G == 1 || G == 2 || G == 4 || G == 8) &&
+  return (a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256) && bits && (G == 1 || G == 2 || G == 4 || G == 8) &&
          a.block_size >= 1;
 }
 
@@ -691,8 +734,9 @@ cudaError_t launch_prefill_mq(const DecodeArgs& a, const MqPlan& p, cudaStream_t
   m.part_ml = m.part_acc + (size_t)a.batch * a.num_q_heads * p.nsplit * a.head_dim;
   const long long grid = (long long)p.windows * p.nsplit * a.num_kv_heads;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  cudaError_t err = a.head_dim == 64 ? launch_mq_bits<64>(m, (int)grid, stream)
+  cudaError_t err = a.head_dim == 64    ? launch_mq_bits<64>(m, (int)grid, stream)
                     : a.head_dim == 128 ? launch_mq_bits<128>(m, (int)grid, stream)
+                    : a.head_dim == 256 ? launch_mq_bits<256>(m, (int)grid, stream)
                                         : cudaErrorInvalidValue;
   if (err != cudaSuccess) return err;
   return launch_combine_splits(m.part_acc, m.part_ml, a.batch * a.num_q_heads, p.nsplit, a.head_dim, a.signs, a.out,

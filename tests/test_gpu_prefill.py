@@ -123,11 +123,14 @@ def test_prefill_chunk_on_large_cache_sampled():
     _close(got[pick], want)
 
 
-# ---- the multi-query kernel (D 64/128, 2/4-bit K and V, G 1/2/4/8, any block size) ---------
+# ---- the multi-query kernel (D 64/128/256, 2/4-bit or equal 3/5-bit K and V, G 1/2/4/8, any
+# block size; D 256 splits each row group's dimensions over two warps) ------------------------
 
 @pytest.mark.parametrize("d,kb,vb,hq,h,bs", [(128, 4, 4, 8, 8, 16), (128, 4, 4, 16, 8, 16), (128, 2, 2, 32, 8, 16),
                                              (128, 2, 4, 32, 4, 16), (64, 2, 4, 16, 2, 8), (128, 4, 2, 64, 8, 32),
-                                             (64, 4, 4, 8, 8, 5)])
+                                             (64, 4, 4, 8, 8, 5), (128, 3, 3, 32, 8, 16), (64, 5, 5, 16, 4, 16),
+                                             (256, 4, 4, 32, 8, 16), (256, 3, 3, 16, 4, 16), (256, 5, 5, 8, 8, 8),
+                                             (256, 2, 4, 64, 8, 16)])
 def test_prefill_multi_query_shapes(d, kb, vb, hq, h, bs):
     # windows of 64 / G query rows hold rows of several sequences (segments), chunks of
     # several tokens, decode rows and a whole-sequence chunk
