@@ -38,7 +38,7 @@ struct WriteArgs {
 // Enqueues: status <- 0, slot validation, row write.  Returns the first launch error.
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream);
 
-// Tensor-core writer (tq_write_tc.cu): fp16 / bf16 rows, head_dim 64 or 128, 2 to 5 bits.
+// Tensor-core writer (tq_write_tc.cu): fp16 / bf16 rows, head_dim 64, 128 or 256, 2 to 5 bits.
 bool write_tc_supported(const WriteArgs& a);
 cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid);
 

@@ -1,4 +1,4 @@
-// Tensor-core packed-KV row writer (fp16 / bf16 rows, head_dim 64 or 128, 2 to 5 bits).
+// Tensor-core packed-KV row writer (fp16 / bf16 rows, head_dim 64, 128 or 256, 2 to 5 bits).
 //
 // TurboQuant docs: "vLLM Usage" (TQ Byte Layout, Slot Mapping, TQ Packed Page Contract:
 // write_tq4_kv) and "Architecture" (PackedPageCache).
@@ -8,6 +8,9 @@
 //    y = H_D (s * x) is an m16n8k16 MMA per 16-column block j against
 //    B_j = diag(s_j) H_16 (entries +-1: exact in fp16 / bf16, products exact in the fp32
 //    accumulator), followed by the H_{D/16} butterflies across blocks, in registers.
+//    (D = 256: the signs flip the A operand instead -- an XOR of fp16 sign bits -- and B
+//    is H_16 itself, which keeps 32 sign masks in registers instead of 64 B fragments;
+//    one CTA of 8 warps per SM.)
 //  * Norm.  ||y||^2 = D ||x||^2: a sum of the thread's squares plus two quad shuffles.
 //  * Quantiser.  u = y / sqrt(sum y^2) lies in [-1, 1]; N equal cells cover that range
 //    and each stores (number of decision points below the cell, the first decision point
@@ -126,7 +129,7 @@ __device__ bool choose_grid(const float* b, int m, float& q_a, float& q_b) {
 }
 
 template <typename T, int D, int BITS>
-__global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs args) {
+__global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kernel(WriteTcArgs args) {
   constexpr int NB = D / 16;            // 16-column blocks
   constexpr int RB = D * BITS / 8 + 4;  // row bytes
   constexpr int IB = D * BITS / 8;      // index bytes
@@ -186,17 +189,33 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
 
   // B fragments: B_j[k][n] = s[16 j + k] * (-1)^popcount(k & n); this lane holds
   // k in {2c, 2c+1} (reg 0) and {2c+8, 2c+9} (reg 1) for n = r (+8 for n-tile 1).
-  uint32_t bfr[NB][2][2];
+  // D = 256: the sign flip goes onto the A operand (asgn[j][part]: sign bits of columns
+  // 16 j + 2c + 8 part, +1 in the fp16 / bf16 pair layout) and bfr[0] holds H_16 alone.
+  constexpr bool kSignOnA = D == 256;
+  constexpr int NBF = kSignOnA ? 1 : NB;
+  uint32_t asgn[kSignOnA ? NB : 1][2];
+  if constexpr (kSignOnA) {
 #pragma unroll
-  for (int j = 0; j < NB; ++j) {
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const int k0 = 16 * j + 2 * c + 8 * part;
+        asgn[j][part] = (__ldg(a.signs + k0) < 0.f ? 0x8000u : 0u) | (__ldg(a.signs + k0 + 1) < 0.f ? 0x80000000u : 0u);
+      }
+  }
+  uint32_t bfr[NBF][2][2];
+#pragma unroll
+  for (int j = 0; j < NBF; ++j) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int n = r + 8 * nt;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         const int k0 = 2 * c + 8 * part, k1 = k0 + 1;
-        const bool n0 = (__ldg(a.signs + 16 * j + k0) < 0.f) ^ (__popc(k0 & n) & 1);
-        const bool n1 = (__ldg(a.signs + 16 * j + k1) < 0.f) ^ (__popc(k1 & n) & 1);
+        const bool s0 = kSignOnA ? false : (__ldg(a.signs + 16 * j + k0) < 0.f);
+        const bool s1 = kSignOnA ? false : (__ldg(a.signs + 16 * j + k1) < 0.f);
+        const bool n0 = s0 ^ (__popc(k0 & n) & 1);
+        const bool n1 = s1 ^ (__popc(k1 & n) & 1);
         bfr[j][nt][part] = pm1_pair<T>(n0, n1);
       }
     }
@@ -239,7 +258,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
   };
 
   // chunk i of a tile belongs to token i / d, d = H * RB / 16: a reciprocal multiply,
-  // (i * ceil(2^16 / d)) >> 16, exact for i < 2^16 / d -- here i < RB <= 84 and d <= 84
+  // (i * ceil(2^16 / d)) >> 16, exact for i < 2^16 / d -- here i < RB <= 164 and d <= 164
   const uint32_t cpt = (uint32_t)(H * RB / 16 > 0 ? H * RB / 16 : 1);
   const uint32_t inv_cpt = (65536u + cpt - 1) / cpt;
   int64_t tile = (int64_t)blockIdx.x * kWWarps + warp;
@@ -267,8 +286,15 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
       const int chunk = 2 * j + (lane >> 4);
       uint32_t a0, a1, a2, a3;
       ldmatrix_x4(tbase + row * ROWB + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+      if constexpr (kSignOnA) {  // a0/a1: columns 2c, 2c+1; a2/a3: columns 2c+8, 2c+9 of block j
+        a0 ^= asgn[j][0];
+        a1 ^= asgn[j][0];
+        a2 ^= asgn[j][1];
+        a3 ^= asgn[j][1];
+      }
+      const int jb = kSignOnA ? 0 : j;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) mma_rot<T>(acc[j][nt], a0, a1, a2, a3, bfr[j][nt][0], bfr[j][nt][1]);
+      for (int nt = 0; nt < 2; ++nt) mma_rot<T>(acc[j][nt], a0, a1, a2, a3, bfr[jb][nt][0], bfr[jb][nt][1]);
     }
     const float2 minus1 = make_float2(-1.f, -1.f);
 #pragma unroll
@@ -443,7 +469,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 2) write_tc_kernel(WriteTcArgs a
 
 bool write_tc_supported(const WriteArgs& a) {
   const bool dt = a.dtype == kF16 || a.dtype == kBF16;
-  const bool hd = a.head_dim == 64 || a.head_dim == 128;
+  const bool hd = a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256;
   const bool bt = a.bits >= 2 && a.bits <= 5;
   return dt && hd && bt && a.num_kv_heads >= 1;
 }
@@ -464,10 +490,12 @@ cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
   if (a.dtype == kF16) {
     TQ_WTC(__half, 64, 2) TQ_WTC(__half, 64, 3) TQ_WTC(__half, 64, 4) TQ_WTC(__half, 64, 5)
     TQ_WTC(__half, 128, 2) TQ_WTC(__half, 128, 3) TQ_WTC(__half, 128, 4) TQ_WTC(__half, 128, 5)
+    TQ_WTC(__half, 256, 2) TQ_WTC(__half, 256, 3) TQ_WTC(__half, 256, 4) TQ_WTC(__half, 256, 5)
   } else if (a.dtype == kBF16) {
     TQ_WTC(__nv_bfloat16, 64, 2) TQ_WTC(__nv_bfloat16, 64, 3) TQ_WTC(__nv_bfloat16, 64, 4)
     TQ_WTC(__nv_bfloat16, 64, 5) TQ_WTC(__nv_bfloat16, 128, 2) TQ_WTC(__nv_bfloat16, 128, 3)
-    TQ_WTC(__nv_bfloat16, 128, 4) TQ_WTC(__nv_bfloat16, 128, 5)
+    TQ_WTC(__nv_bfloat16, 128, 4) TQ_WTC(__nv_bfloat16, 128, 5) TQ_WTC(__nv_bfloat16, 256, 2)
+    TQ_WTC(__nv_bfloat16, 256, 3) TQ_WTC(__nv_bfloat16, 256, 4) TQ_WTC(__nv_bfloat16, 256, 5)
   }
 #undef TQ_WTC
   return cudaErrorInvalidValue;

@@ -3,14 +3,19 @@
 Tolerances:
   * packed index bytes: bit-exact, except coordinates whose normalised rotated value
     lies within 1e-6 of a decision point (measured in the oracle's fp64); those are
-    counted and must be fewer than 1e-5 of all compared coordinates.  A sample of fewer
-    than 1e5 coordinates cannot resolve that rate (one exception in it is consistent
-    with a rate below 1e-5), so such a sample may hold one in-band exception;
+    counted and must be fewer than 1e-5 of all compared coordinates.  That is a rate: a
+    sample of n < 1e6 coordinates (expected count below 10 at the rate) cannot resolve
+    it, so there the count is held to what a process at exactly that rate exceeds with
+    probability below 1e-3 (Poisson upper quantile); samples of >= 1e6 coordinates are
+    held to 1e-5 n, and the rate itself is measured at scale by
+    test_index_flip_rate_at_scale (3.4e7 coordinates per shape);
   * norms: within 1e-6 relative;
   * decode outputs: |gpu - oracle| <= 2e-3 + 2e-3 |oracle| elementwise.
 """
 
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -56,9 +61,22 @@ def compare_rows(gpu_rows: np.ndarray, raw_rows: np.ndarray, codec: OracleCodec,
                 max_index_step=int(np.abs(gidx - idx).max()) if idx.size else 0)
 
 
+def allowed_flips(coords: int) -> float:
+    """In-band exceptions a sample of `coords` coordinates may hold (see the tolerances)."""
+    lam = MAX_FLIP_FRACTION * coords
+    if coords >= 1_000_000:
+        return lam
+    k, term, cdf = 0, math.exp(-lam), math.exp(-lam)
+    while 1.0 - cdf >= 1e-3:  # smallest k with P(Poisson(lam) > k) < 1e-3
+        k += 1
+        term *= lam / k
+        cdf += term
+    return float(k)
+
+
 def assert_rows_match(stats: dict) -> None:
     assert stats["flips_outside_band"] == 0, stats
-    assert stats["flips"] <= max(1.0, MAX_FLIP_FRACTION * stats["coords"]), stats
+    assert stats["flips"] <= allowed_flips(stats["coords"]), stats
     assert stats["max_index_step"] <= 1, stats
     assert stats["max_norm_rel"] <= NORM_RTOL, stats
 

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from oracle import tq_oracle as o
-from parity import OracleCodec, assert_decode_close, assert_rows_match, compare_rows
+from parity import MAX_FLIP_FRACTION, OracleCodec, assert_decode_close, assert_rows_match, compare_rows
 from quantized_kv_cache_06_gb300.workloads import SWEEP, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -347,11 +347,12 @@ def test_tc_decode_many_short_sequences(tq):
 
 
 # ---------------------------------------------------------------- tensor-core writer shapes
-# (fp16 / bf16 rows, head_dim 64 or 128, 2 to 5 bits; H dividing the 16-row tile or not;
-# 3- and 5-bit fields cross bytes)
+# (fp16 / bf16 rows, head_dim 64, 128 or 256, 2 to 5 bits; H dividing the 16-row tile or
+# not; 3- and 5-bit fields cross bytes; D 256 puts the signs on the A operand)
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d,bits", [(64, 2), (64, 3), (64, 4), (64, 5), (128, 2), (128, 3), (128, 4), (128, 5)])
+@pytest.mark.parametrize("d,bits", [(64, 2), (64, 3), (64, 4), (64, 5), (128, 2), (128, 3), (128, 4), (128, 5),
+                                    (256, 2), (256, 3), (256, 4), (256, 5)])
 @pytest.mark.parametrize("h", [1, 3, 8, 16])
 def test_tc_writer_shapes(tq, dtype, d, bits, h):
     rng = np.random.default_rng(d * 7 + bits * 3 + h)
@@ -384,3 +385,26 @@ def test_tc_writer_large_values_and_tiny_rows(tq):
                         lib_codebook(tq, 128, 4), check=False)
     assert int(st.item()) == 0
     check_written_rows(pages.cpu().numpy(), raw_t.float().numpy(), slots, 4, OracleCodec(128))
+
+
+@pytest.mark.parametrize("d,bits", [(256, 5), (256, 3), (128, 5), (64, 5)])
+def test_index_flip_rate_at_scale(tq, d, bits):
+    # the index-byte bar measured as a rate: 3.4e7 coordinates of the densest codebooks
+    # (fp16 rows N(0,1) times a lognormal(0, 0.5) scale per (head, channel), 8 heads),
+    # every exception within 1e-6 of a decision point and fewer than 1e-5 of all
+    rng = np.random.default_rng(7 + d + bits)
+    ntok, h = 33_554_432 // (8 * d), 8
+    raw = (rng.standard_normal((ntok, h, d)) * rng.lognormal(0, 0.5, (h, d))).astype(np.float16)
+    slots = np.arange(ntok, dtype=np.int64)
+    pages, st = gpu_write(tq, raw, slots, ntok // 16, 16, bits)
+    assert st == 0
+    rows = pages.cpu().numpy().reshape(ntok * h, -1)
+    flat = raw.reshape(-1, d)
+    codec = OracleCodec(d)
+    tot = dict(coords=0, flips=0, flips_outside_band=0)
+    for s0 in range(0, ntok * h, 16384):
+        part = compare_rows(rows[s0:s0 + 16384], flat[s0:s0 + 16384].astype(np.float64), codec, bits)
+        for k in tot:
+            tot[k] += part[k]
+    assert tot["flips_outside_band"] == 0, tot
+    assert tot["flips"] < MAX_FLIP_FRACTION * tot["coords"], tot
