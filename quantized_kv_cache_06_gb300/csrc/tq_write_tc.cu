@@ -104,25 +104,31 @@ struct WriteTcArgs {
 // least 1/64 cell from a cell edge and no two in one cell.  Deterministic, so every CTA
 // picks the same grid.  Returns false when no pair qualifies (the caller then reports
 // an error instead of writing).
-__device__ bool choose_grid(const float* b, int m, float& q_a, float& q_b) {
+// Run by the 32 lanes of one warp: candidate i = 4 (row of n) + phase, in the order
+// n = kGridMaxA, kGridMaxA - 2, ... and phases {1/2, 1/4, 3/4, 3/8}; lane l tests the
+// candidates l, l + 32, ..., and the first passing candidate in that order wins.
+__device__ bool choose_grid(const float* b, int m, int lane, float& q_a, float& q_b) {
   const float phases[4] = {0.5f, 0.25f, 0.75f, 0.375f};
-  for (int n = kGridMaxA; n >= kGridMaxA / 4; n -= 2) {
-    for (int p = 0; p < 4; ++p) {
-      const float ga = (float)n, gb = (float)n + phases[p];
-      bool ok = true;
-      int prev = -1;
-      for (int k = 0; k < m && ok; ++k) {
-        const float x = fmaf(b[k], ga, gb);
-        const int cell = (int)floorf(x);
-        const float f = x - (float)cell;
-        ok = cell > prev && f >= 1.0f / 64 && f <= 63.0f / 64;
-        prev = cell;
-      }
-      if (ok) {
-        q_a = ga;
-        q_b = gb;
-        return true;
-      }
+  constexpr int kCands = 4 * (kGridMaxA / 2 - kGridMaxA / 8 + 1);
+  for (int base = 0; base < kCands; base += 32) {
+    const int i = base + lane;
+    const int n = kGridMaxA - 2 * (i >> 2);
+    const float ga = (float)n, gb = (float)n + phases[i & 3];
+    bool ok = i < kCands;
+    int prev = -1;
+    for (int k = 0; k < m && ok; ++k) {
+      const float x = fmaf(b[k], ga, gb);
+      const int cell = (int)floorf(x);
+      const float f = x - (float)cell;
+      ok = cell > prev && f >= 1.0f / 64 && f <= 63.0f / 64;
+      prev = cell;
+    }
+    const unsigned hit = __ballot_sync(kFullMask, ok);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      q_a = __shfl_sync(kFullMask, ga, src);
+      q_b = __shfl_sync(kFullMask, gb, src);
+      return true;
     }
   }
   return false;
@@ -155,12 +161,15 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
   __shared__ int grid_ok;
   if (threadIdx.x < NC - 1) bnd[threadIdx.x] = 0.5f * (a.centroids[threadIdx.x] + a.centroids[threadIdx.x + 1]);
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
     float ga = 0.f, gb = 0.f;
-    grid_ok = choose_grid(bnd, NC - 1, ga, gb) ? 1 : 0;
-    grid_a = ga;
-    grid_b = gb;
-    if (!grid_ok && blockIdx.x == 0) atomicMax(a.status, (int32_t)kUnsupported);
+    const bool found = choose_grid(bnd, NC - 1, lane, ga, gb);
+    if (lane == 0) {
+      grid_ok = found ? 1 : 0;
+      grid_a = ga;
+      grid_b = gb;
+      if (!found && blockIdx.x == 0) atomicMax(a.status, (int32_t)kUnsupported);
+    }
   }
   __syncthreads();
   if (!grid_ok || *a.status != kOk) return;  // bad codebook or a slot failed validation: write nothing
@@ -170,9 +179,8 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
   // for g within rounding of an integer, where it may be floor(g) - 1 -- harmless, as no
   // decision point lies within 1/64 cell of a cell edge.  g >= phi >= 1/4 keeps it >= 0.
   const float q_bs = q_b - 0.5f;
-  for (int i = threadIdx.x; i < kQCells * kQCopies; i += blockDim.x) {
+  for (int cell = threadIdx.x; cell < kQCells; cell += blockDim.x) {
     // cell [cell, cell + 1) in grid units: decision points below its start, first one at or above
-    const int cell = i / kQCopies;
     int below = 0;
     float point = INFINITY;
     for (int k = 0; k < NC - 1; ++k) {
@@ -183,7 +191,8 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
     QCell q;
     q.lo = below;
     q.point = point - 0.5f;  // in g' (exact, and +inf stays +inf)
-    qtab[i] = q;
+#pragma unroll
+    for (int copy = 0; copy < kQCopies; ++copy) qtab[cell * kQCopies + copy] = q;
   }
   __syncthreads();
 
