@@ -166,9 +166,11 @@ tq_status tq_paged_decode(const void* q, tq_dtype q_dtype, int batch, int num_q_
  *   workspace    device, >= tq_paged_prefill_workspace(num_q_rows, ...) bytes, 16-byte aligned
  * Other arguments, the status word and the errors are those of tq_paged_decode; a q_seq
  * entry outside [0, num_seqs) gives a zero row and TQ_ERR_INVALID_ARG in status_dev.
- * Rows of one chunk are independent units of the same kernel as the decode: each reads its
- * own causal prefix of the pages (rows of one sequence are neighbours in the work list, so
- * their shared blocks tend to be served from L2). */
+ * For head_dim 64, 128 or 256 with 2/4-bit (or equal 3/5-bit) K and V, up to 64 / G
+ * consecutive rows of one sequence share every dequantised 32-token key/value tile, so a
+ * prefill chunk reads the cache once: keep the rows of a chunk next to each other in
+ * q_seq (rows of several sequences in one window are taken one sequence after the other).
+ * Other shapes run the decode kernels row by row. */
 size_t tq_paged_prefill_workspace(int num_q_rows, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_blocks_per_seq, int block_size);
 tq_status tq_paged_prefill(const void* q, tq_dtype q_dtype, int num_q_rows, int num_q_heads, int num_kv_heads,
