@@ -909,15 +909,21 @@ combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc
   for (int i = 0; i < E; ++i) v[i] = 0.f;
   if (p1 > p0) {
     const long long C = num_ctas;
+    // CTA i owns blocks [N i / C, N (i + 1) / C); block g belongs to CTA ((g + 1) C - 1) / N.
+    // With N >= C every CTA from the owner of p0 to the owner of p1 - 1 wrote a partial for
+    // this sequence; with N < C some ranges are empty, and the writers are exactly the
+    // owners of the sequence's blocks, one each.
+    const bool dense = N >= C;
     const long long f = ((p0 + 1) * C - 1) / N, l = (p1 * C - 1) / N;  // first / last CTA
+    const long long cnt = dense ? l - f + 1 : p1 - p0;                  // partials to merge
     float mx = -INFINITY, lsum = 0.f;
-    for (long long i0 = f; i0 <= l; i0 += kCombineBatch) {
+    for (long long k0 = 0; k0 < cnt; k0 += kCombineBatch) {
       float ms[kCombineBatch], ls[kCombineBatch], acc[kCombineBatch][E];
 #pragma unroll
       for (int u = 0; u < kCombineBatch; ++u) {
-        const long long i = i0 + u;
-        // CTAs past l, and CTAs whose block range is empty (possible when N < C), wrote nothing
-        const bool live = i <= l && N * i / C < N * (i + 1) / C;
+        const long long k = k0 + u;
+        const bool live = k < cnt;
+        const long long i = !live ? 0 : (dense ? f + k : ((p0 + k + 1) * C - 1) / N);
         const int64_t s = (i + b) * a.num_q_heads + j;
         ms[u] = live ? part_ml[s * 2] : -INFINITY;
         ls[u] = live ? part_ml[s * 2 + 1] : 0.f;
