@@ -806,14 +806,17 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   {
       // ---- tables (consumer warps; the producer is already streaming) ------------------
     if (KB == 4) {
+      // lane k of every consumer warp splits centroid k once; the entries then take their
+      // two halves with shuffles instead of global loads in the loop
+      __half k_hi_l, k_lo_l;
+      split_half(__ldg(a.k_centroids + (lane & 15)) * args.k_alpha, k_hi_l, k_lo_l);
+      const uint32_t k_pair_l = (uint32_t)__half_as_ushort(k_hi_l) | ((uint32_t)__half_as_ushort(k_lo_l) << 16);
       for (int i = tid; i < 256 * 32; i += 32 * ncons) {
         const int f = i >> 5, copy = i & 31;
-        __half ha, la, hb, lb;
-        split_half(__ldg(a.k_centroids + (f & 15)) * args.k_alpha, ha, la);
-        split_half(__ldg(a.k_centroids + (f >> 4)) * args.k_alpha, hb, lb);
-        __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
-        *reinterpret_cast<uint32_t*>(lutT + f * 256 + copy * 4) = *reinterpret_cast<uint32_t*>(&hi2);
-        if (copy == 0) *reinterpret_cast<uint32_t*>(lutL + f * 4) = *reinterpret_cast<uint32_t*>(&lo2);
+        const uint32_t pa = __shfl_sync(kFullMask, k_pair_l, f & 15);  // (hi, lo) of c[f & 15]
+        const uint32_t pb = __shfl_sync(kFullMask, k_pair_l, f >> 4);
+        *reinterpret_cast<uint32_t*>(lutT + f * 256 + copy * 4) = __byte_perm(pa, pb, 0x5410);
+        if (copy == 0) *reinterpret_cast<uint32_t*>(lutL + f * 4) = __byte_perm(pa, pb, 0x7632);
       }
     } else {
       for (int f = tid; f < 16; f += 32 * ncons) {
@@ -828,10 +831,11 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       }
     }
     if (VB == 4) {
+      const float v_l = __ldg(a.v_centroids + (lane & 15)) * args.v_alpha;
       for (int i = tid; i < 256 * 32; i += 32 * ncons) {
         const int f = i >> 5, copy = i & 31;
-        const float ca = __ldg(a.v_centroids + (f & 15)) * args.v_alpha;
-        const float cb = __ldg(a.v_centroids + (f >> 4)) * args.v_alpha;
+        const float ca = __shfl_sync(kFullMask, v_l, f & 15);
+        const float cb = __shfl_sync(kFullMask, v_l, f >> 4);
         *reinterpret_cast<uint32_t*>(lutT + f * 256 + 128 + copy * 4) = pack_half2(ca, cb);
       }
     } else {
