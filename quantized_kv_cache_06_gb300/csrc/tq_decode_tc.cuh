@@ -310,6 +310,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   }
   if (cta == 0 && tid == 0) args.prefix[B] = carry;
   __syncthreads();  // also: barriers initialised
+  // the combine grid may be scheduled now; it waits for this grid's completion itself
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if (g_lo >= g_hi) return;  // nothing to do (uniform; no copy was issued)
   const int b_first = scan_tmp[32], b_last = scan_tmp[33], j_first = scan_tmp[34];
   const int nstages = (int)((g_hi - g_lo + WPH - 1) / WPH);
@@ -904,6 +906,9 @@ combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc
   constexpr int D = 32 * E;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  // launched as a programmatic dependent of the split kernel: wait until that grid has
+  // completed and its partials are visible
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (row >= a.batch * a.num_q_heads) return;
   const int b = row / a.num_q_heads, j = row - b * a.num_q_heads;
   const long long N = prefix[a.batch];
@@ -1029,9 +1034,19 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int rows = B * Hq;
-  combine_tc_kernel<D / 32><<<(rows + 7) / 8, 256, 0, stream>>>(a, p.num_splits, t.part_acc, t.part_ml,
-                                                                     t.prefix);
-  return cudaGetLastError();
+  // programmatic dependent launch: the combine's launch overlaps the split kernel's tail
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((rows + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_tc_kernel<D / 32>, a, p.num_splits, (const float*)t.part_acc,
+                            (const float*)t.part_ml, (const int*)t.prefix);
 }
 
 
