@@ -20,6 +20,9 @@ constexpr int kWriteWarps = 8;
 
 __global__ void validate_slots_kernel(const int64_t* __restrict__ slots, int64_t n, int64_t limit,
                                       int32_t* __restrict__ status) {
+  // the tensor-core writer is a programmatic dependent of this kernel: it may be scheduled
+  // now, does its set-up, and waits for this grid before it reads the status word
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   bool bad = false;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     bad |= __ldg(slots + i) >= limit;

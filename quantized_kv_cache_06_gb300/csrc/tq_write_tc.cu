@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
     }
   }
   __syncthreads();
-  if (!grid_ok || *a.status != kOk) return;  // bad codebook or a slot failed validation: write nothing
+  if (!grid_ok) return;  // bad codebook: write nothing
   const float q_a = grid_a, q_b = grid_b;  // grid coordinate g = u * q_a + q_b, cell = floor(g)
   // The loop works in g' = g - 1/2 (exact: q_b is a small multiple of 1/8): adding
   // 1.5 * 2^23 to g' leaves round(g') in the low mantissa bits, which is floor(g) but
@@ -233,6 +233,11 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
   constexpr uint32_t kMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
   const uint32_t q_addr_bias =
       smem_addr(qtab) + (uint32_t)((lane & 15) * sizeof(QCell)) - kMagicBits * (uint32_t)(kQCopies * sizeof(QCell));
+
+  // launched as a programmatic dependent of the slot validation: the set-up above overlaps
+  // it; the status word is read once that grid has completed
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  if (*a.status != kOk) return;  // a slot failed validation: write nothing
 
   const int64_t num_rows = a.num_tokens * H;
   const int64_t num_tiles = (num_rows + 15) / 16;
@@ -483,6 +488,23 @@ bool write_tc_supported(const WriteArgs& a) {
   return dt && hd && bt && a.num_kv_heads >= 1;
 }
 
+// Launches `kern` as a programmatic dependent of the previous kernel on `stream` (the slot
+// validation): it may start before that kernel completes and waits for it itself.
+template <typename K>
+cudaError_t launch_dependent(K kern, int grid, size_t smem, cudaStream_t stream, const WriteTcArgs& t) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kWWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, t);
+}
+
 cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
   WriteTcArgs t;
   t.a = a;
@@ -493,8 +515,7 @@ cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
     auto kern = write_tc_kernel<T, D, BITS>;                                                                  \
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
     if (err != cudaSuccess) return err;                                                                       \
-    kern<<<grid, kWWarps * 32, smem, stream>>>(t);                                                            \
-    return cudaGetLastError();                                                                                \
+    return launch_dependent(kern, grid, smem, stream, t);                                                     \
   }
   if (a.dtype == kF16) {
     TQ_WTC(__half, 64, 2) TQ_WTC(__half, 64, 3) TQ_WTC(__half, 64, 4) TQ_WTC(__half, 64, 5)
