@@ -15,8 +15,10 @@ bool tc_decode_supported(const DecodeArgs& a) {
 int tc_partials_per_sequence_split() { return 1; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
-  if (a.bt_rows) return launch_decode_tc_rowmap(a, p, stream);
-  return launch_decode_tc_dispatch<false>(a, p, stream);
+  // Batches with a block-table row map (tq_paged_prefill) never come here: every shape this
+  // kernel covers is also covered by the multi-query kernel, which takes them.
+  if (a.bt_rows) return cudaErrorInvalidValue;
+  return launch_decode_tc_dispatch(a, p, stream);
 }
 
 }  // namespace tq

@@ -35,9 +35,7 @@
 // Softmax: online, base 2 (log2 e folded into the query), per q head.  Rows of tokens
 // past the sequence end are masked; blocks with an out-of-range id are skipped and
 // reported through the status word.
-// Tensor-core paged decode kernels, included by tq_decode_tc.cu (plain decode) and
-// tq_prefill_tc.cu (mixed prefill/decode, batch rows mapped to block-table rows): the two
-// instantiation sets compile in parallel.
+// The kernels are instantiated and launched by tq_decode_tc.cu.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -205,14 +203,13 @@ constexpr int kOffL = kOffV2 + 16 * 4;                      // byte K lo table, 
 constexpr int kMiscBytes = (kOffL + 256 * 4 + 127) / 128 * 128;
 
 constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
-constexpr int kNoTableRow = -2;        // block id stand-in for a row map entry outside the table
 // Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored with the fp16-hi key part
 // only.  With the alpha scaling the hi part is within ~1e-4 relative of the fp32
 // centroid, so the score error of such a tile stays far below the output tolerance;
 // tiles above the bound (rows with very large norms) add the fp16-lo part.
 constexpr float kFastScoreBound = 48.0f;
 
-template <int D, int KB, int VB, int G, int WPH, bool ROWMAP>
+template <int D, int KB, int VB, int G, int WPH>
 __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   using Cfg = TcCfg<D, KB, VB, G, WPH>;
   const DecodeArgs& a = args.a;
@@ -342,13 +339,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       pend_len = __ldg(a.seq_lens + cb);
       pend_m.b = cb;
       pend_m.j = cj;
-      if (ROWMAP) {  // mixed prefill/decode: batch row cb reads table row bt_rows[cb]
-        const int bt_row = block_table_row(a, cb);
-        if (bt_row < 0 && a.status) atomicMax(a.status, (int32_t)kInvalidArg);
-        pend_bid = bt_row < 0 ? kNoTableRow : __ldg(a.block_table + (int64_t)bt_row * a.max_blocks_per_seq + cj);
-      } else {
-        pend_bid = __ldg(a.block_table + (int64_t)cb * a.max_blocks_per_seq + cj);
-      }
+      pend_bid = __ldg(a.block_table + (int64_t)cb * a.max_blocks_per_seq + cj);
       pend_m.ntok = 1;  // marks a real block until meta_store fills the count
       cursor_advance(WPH);
     }
@@ -361,7 +352,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       const int len = pend_len < 0 ? 0 : (pend_len > cap ? cap : pend_len);
       m.ntok = min(kBS, len - m.j * kBS);
       m.valid = (pend_bid >= 0 && (int64_t)pend_bid < a.num_blocks);
-      if (!m.valid && (!ROWMAP || pend_bid != kNoTableRow) && a.status)
+      if (!m.valid && a.status)
         atomicMax(a.status, (int32_t)kBlockOutOfRange);
       bid = m.valid ? pend_bid : -1;
     }
@@ -966,7 +957,7 @@ combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc
     store_from_f32(a.out, (int64_t)row * D + lane * E + k, a.out_dtype, v[k] * __ldg(a.signs + lane * E + k) * rs);
 }
 
-template <int D, int KB, int VB, int G, int WPH, bool ROWMAP>
+template <int D, int KB, int VB, int G, int WPH>
 cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
   using Cfg = TcCfg<D, KB, VB, G, WPH>;
   TcArgs t{};
@@ -1027,7 +1018,7 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   t.part_acc = static_cast<float*>(a.workspace);
   t.part_ml = t.part_acc + slots * Hq * D;
   t.prefix = reinterpret_cast<int*>(t.part_ml + slots * Hq * 2);
-  auto kern = decode_tc_kernel<D, KB, VB, G, WPH, ROWMAP>;
+  auto kern = decode_tc_kernel<D, KB, VB, G, WPH>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   kern<<<p.num_splits, 32 * (H + 1), smem, stream>>>(t);
@@ -1051,13 +1042,12 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
 
 
 // Instantiations: D 128 (2 blocks per stage) and 256 (1) x all 2/4-bit combos x G 4/8, and
-// D 64 at 4/4 bits.  ROWMAP: batch rows read block-table rows through a row map.
-template <bool ROWMAP>
+// D 64 at 4/4 bits.
 cudaError_t launch_decode_tc_dispatch(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
   const int G = a.num_q_heads / a.num_kv_heads;
 #define TQ_TC_CASE(D, KB, VB, GG, WPH)                                                    \
   if (a.head_dim == D && a.k_bits == KB && a.v_bits == VB && G == GG)                     \
-    return launch_tc_typed<D, KB, VB, GG, WPH, ROWMAP>(a, p, stream);
+    return launch_tc_typed<D, KB, VB, GG, WPH>(a, p, stream);
 #define TQ_TC_BITS(D, GG, WPH) \
   TQ_TC_CASE(D, 4, 4, GG, WPH) TQ_TC_CASE(D, 4, 2, GG, WPH) TQ_TC_CASE(D, 2, 4, GG, WPH) TQ_TC_CASE(D, 2, 2, GG, WPH)
   TQ_TC_BITS(128, 4, 2)

@@ -107,8 +107,6 @@ __device__ __forceinline__ int block_table_row(const DecodeArgs& a, int b) {
 bool tc_decode_supported(const DecodeArgs& a);
 int tc_partials_per_sequence_split();
 cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
-// The same launch for a batch with a block-table row map (tq_prefill_tc.cu).
-cudaError_t launch_decode_tc_rowmap(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 
 bool prefill_mq_supported(const DecodeArgs& a);
 MqPlan plan_prefill_mq(const DecodeArgs& a, int num_sms, bool one_row_per_window);
