@@ -110,3 +110,17 @@ def test_host_argument_errors(tq):
     assert lib.tq_paged_decode(*args(48, 3, 4)) == tq.TQ_ERR_UNSUPPORTED
     assert lib.tq_paged_decode(*args(32, 8, 7)) == tq.TQ_ERR_UNSUPPORTED
     assert lib.tq_paged_decode_workspace(2, 12, 8, 128, 4, 16) == 0
+
+
+def test_workspace_queries_cover_every_plan(tq):
+    # the queries take no bit widths, so they return the largest workspace over the kernels a
+    # call may pick: the prefill query covers the decode query for the same shapes, and both
+    # cover at least one split partial (D accumulators + max + sum) per (row, q head)
+    lib = tq.lib()
+    for r, hq, h, d, maxb, bs in [(64, 32, 8, 128, 512, 16), (1024, 32, 8, 128, 512, 16), (4, 64, 8, 128, 8192, 16),
+                                  (16, 32, 8, 256, 256, 16), (5, 8, 8, 64, 3, 5), (3, 4, 4, 32, 2, 16)]:
+        dec = lib.tq_paged_decode_workspace(r, hq, h, d, maxb, bs)
+        pre = lib.tq_paged_prefill_workspace(r, hq, h, d, maxb, bs)
+        assert dec >= r * hq * (d + 2) * 4
+        assert pre >= dec
+    assert lib.tq_paged_prefill_workspace(2, 12, 8, 128, 4, 16) == 0  # group does not divide
