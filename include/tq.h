@@ -238,6 +238,65 @@ tq_status tq_paged_decode_static(const void* q, tq_dtype q_dtype, int batch, int
                                  const float* v_centroids, float scale, void* out, tq_dtype out_dtype,
                                  int32_t* status_dev, void* stream);
 
+/* ---------------------------------------------------------------------------------
+ * Product-quantised ("QJL residual") key rows ("vLLM Reference Audit": File Map, the
+ * quantizer's "MSE and QJL codecs" with indices, norms and signs, TurboQuantMSE /
+ * TurboQuantProd; Feature Checklist, "QJL residual").  The pages name the codec but not
+ * its arithmetic or layout; the readings below follow the product quantiser that
+ * TurboQuantProd names: a (b-1)-bit MSE row plus a one-bit Johnson-Lindenstrauss sketch
+ * of its residual, which makes the score an unbiased estimate of <q, k>.
+ *
+ * Key row at b bits (b in {2..5} for the layout): the (b-1)-bit MSE indices of y = R x/nu
+ * (LSB-first, as in the MSE rows), then D sign bits z_i = [(S r)_i >= 0] with r = y -
+ * c[idx] the rotated residual (bit i = bit i%8 of byte i/8), then nu = ||x|| and gamma =
+ * ||r|| as little-endian fp32: RBP(D, b) = D (b-1)/8 + D/8 + 8.  S is a D x D matrix of
+ * N(0, 1) numbers (tq_build_qjl_matrix).  Values keep the MSE rows of tq_write_kv.
+ * --------------------------------------------------------------------------------- */
+
+/* RBP(head_dim, bits); -1 when head_dim is not a power of two in [32, 256] or bits is
+ * outside 2..5. */
+int64_t tq_prod_row_bytes(int head_dim, int bits);
+
+/* The sketch matrix S, row-major fp32 [head_dim][head_dim], written to s_host: entry
+ * (i, j) is normal number i*D + j of the stream seeded with `seed` -- splitmix64 outputs
+ * taken in pairs (z1, z2), u1 = ((z1 >> 11) + 1) 2^-53, u2 = (z2 >> 11) 2^-53, and the
+ * Box-Muller pair sqrt(-2 ln u1) (cos 2 pi u2, sin 2 pi u2) in that order, computed in
+ * fp64 and rounded once (a reading: the pages fix no generator).  Host only; errors:
+ * TQ_ERR_INVALID_ARG (null), TQ_ERR_UNSUPPORTED (head_dim). */
+tq_status tq_build_qjl_matrix(int head_dim, uint64_t seed, float* s_host);
+
+/* Key writer for product-quantised rows: tq_write_kv's contract (raw, slots, pages,
+ * status_dev and its errors) with rows of RBP(D, bits) bytes.
+ *   mse_centroids  device, float[2^(bits-1)] from tq_codebook(head_dim, bits - 1)
+ *   qjl_matrix     device, float[head_dim][head_dim] from tq_build_qjl_matrix
+ * Per row (fp32): nu, y and the indices exactly as tq_write_kv at bits - 1; r = y -
+ * c[idx]; gamma = ||r||; z_i = [sum_j S[i][j] r_j >= 0].  head_dim 64 or 128 and bits
+ * 3..5 (TQ_ERR_UNSUPPORTED otherwise). */
+tq_status tq_write_kv_prod(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, int num_kv_heads,
+                           int head_dim, int bits, const int64_t* slots, uint8_t* pages, int64_t num_blocks,
+                           int block_size, const float* signs, const float* mse_centroids,
+                           const float* qjl_matrix, int32_t* status_dev, void* stream);
+
+/* Workspace bytes of tq_paged_decode_prod for these shapes (split-K partials and the
+ * projected queries S R q); 0 when the arguments are invalid. */
+size_t tq_paged_decode_prod_workspace(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                      int max_blocks_per_seq, int block_size);
+
+/* Paged decode with product-quantised keys (k_bits = b in 3..5, rows of RBP(D, b)
+ * bytes, k_mse_centroids float[2^(b-1)]) and MSE value rows (v_bits 2..5, RB(D, v_bits),
+ * v_centroids float[2^v_bits]).  Every other argument, the status word and the errors
+ * are those of tq_paged_decode.  The score of key row (idx, z, nu, gamma) is
+ *   scale * nu * (<R q, c[idx]> + gamma sqrt(pi/2) / D * <S R q, 2z - 1>);
+ * S R q is computed once per (sequence, q head) into the workspace.  head_dim 64 or 128
+ * (TQ_ERR_UNSUPPORTED otherwise). */
+tq_status tq_paged_decode_prod(const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int num_kv_heads,
+                               int head_dim, const uint8_t* k_pages, int k_bits, const uint8_t* v_pages,
+                               int v_bits, int64_t num_blocks, int block_size, const int32_t* block_table,
+                               int max_blocks_per_seq, const int32_t* seq_lens, const float* signs,
+                               const float* k_mse_centroids, const float* v_centroids, const float* qjl_matrix,
+                               float scale, void* out, tq_dtype out_dtype, void* workspace,
+                               size_t workspace_bytes, int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

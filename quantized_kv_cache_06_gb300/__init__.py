@@ -16,13 +16,17 @@ from ._lib import (  # noqa: F401
     TQError,
     lib,
     raise_for_device_status,
+    tq_build_qjl_matrix,
     tq_build_rotation,
     tq_codebook,
     tq_dequant_rows,
     tq_paged_decode,
+    tq_paged_decode_prod,
     tq_paged_decode_static,
     tq_paged_decode_workspace,
     tq_paged_prefill,
+    tq_prod_row_bytes,
     tq_row_bytes,
     tq_write_kv,
+    tq_write_kv_prod,
 )

@@ -58,6 +58,14 @@ SIGNATURES = {
     "tq_paged_decode_static": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p,
                                         _c_int, _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_f,
                                         _c_p, _c_int, _c_p, _c_p]),
+    "tq_prod_row_bytes": (_c_i64, [_c_int, _c_int]),
+    "tq_build_qjl_matrix": (_c_int, [_c_int, _c_u64, _c_p]),
+    "tq_write_kv_prod": (_c_int, [_c_p, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_p, _c_p, _c_i64, _c_int,
+                                  _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "tq_paged_decode_prod_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tq_paged_decode_prod": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
+                                      _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p,
+                                      _c_int, _c_p, _c_sz, _c_p, _c_p]),
 }
 
 _lib = None
@@ -331,4 +339,92 @@ def tq_paged_decode_static(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
                                             _ptr(seq_lens), _ptr(signs), _ptr(k_centroids), _ptr(v_centroids),
                                             float(scale or 0.0), _ptr(out), _DTYPES[out.dtype], _ptr(status),
                                             _stream(dev)))
+    return out
+
+
+# ---------------------------------------------------------------- product-quantised keys
+
+def tq_prod_row_bytes(head_dim: int, bits: int) -> int:
+    """Bytes of one product-quantised key row: (bits-1)-bit indices, D sign bits, nu, gamma."""
+    n = lib().tq_prod_row_bytes(int(head_dim), int(bits))
+    if n < 0:
+        raise TQError(TQ_ERR_UNSUPPORTED, f"head_dim {head_dim} / bits {bits} unsupported")
+    return int(n)
+
+
+def tq_build_qjl_matrix(head_dim: int, seed: int, device=None) -> torch.Tensor:
+    """The N(0, 1) sketch matrix S, float32 [head_dim, head_dim] (host, or moved to `device`)."""
+    out = torch.empty(int(head_dim), int(head_dim), dtype=torch.float32)
+    _check(lib().tq_build_qjl_matrix(int(head_dim), int(seed) & ((1 << 64) - 1), out.data_ptr()))
+    return out if device is None else out.to(device)
+
+
+def tq_write_kv_prod(raw: torch.Tensor, pages: torch.Tensor, slots: torch.Tensor, signs: torch.Tensor,
+                     mse_centroids: torch.Tensor, qjl_matrix: torch.Tensor, status: torch.Tensor | None = None,
+                     check: bool = True) -> torch.Tensor:
+    """Product-quantised key rows: encode raw[T, H, D] into pages[NB, bs, H, RBP] at
+    bits = log2(len(mse_centroids)) + 1.  Same slot rules and status as tq_write_kv."""
+    dev = _need_cuda("tq_write_kv_prod", raw, pages, slots, signs, mse_centroids, qjl_matrix)
+    if raw.dim() != 3 or pages.dim() != 4 or slots.dim() != 1 or slots.numel() != raw.shape[0]:
+        raise ValueError("tq_write_kv_prod: raw [T, H, D], pages [NB, bs, H, RBP], slots [T] expected")
+    if raw.dtype not in _DTYPES or pages.dtype != torch.uint8 or slots.dtype != torch.int64 or \
+            qjl_matrix.dtype != torch.float32:
+        raise ValueError("tq_write_kv_prod: raw f32/f16/bf16, pages uint8, slots int64, qjl_matrix f32 expected")
+    t, h, d = raw.shape
+    n = mse_centroids.numel()
+    bits = n.bit_length()
+    if n < 2 or (1 << (bits - 1)) != n:
+        raise ValueError(f"tq_write_kv_prod: mse_centroids must hold 2^(bits-1) values, got {n}")
+    if tuple(qjl_matrix.shape) != (d, d):
+        raise ValueError(f"tq_write_kv_prod: qjl_matrix must be [{d}, {d}]")
+    if pages.shape[2] != h or pages.shape[3] != tq_prod_row_bytes(d, bits):
+        raise ValueError(f"tq_write_kv_prod: pages {tuple(pages.shape)} do not match H={h}, "
+                         f"RBP={tq_prod_row_bytes(d, bits)}")
+    if status is None:
+        status = _status_buffer(dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_write_kv_prod(_ptr(raw), _DTYPES[raw.dtype], t, h, d, bits, _ptr(slots), _ptr(pages),
+                                      pages.shape[0], pages.shape[1], _ptr(signs), _ptr(mse_centroids),
+                                      _ptr(qjl_matrix), _ptr(status), _stream(dev)))
+    if check:
+        raise_for_device_status(status)
+    return status
+
+
+def tq_paged_decode_prod(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                         seq_lens: torch.Tensor, signs: torch.Tensor, k_mse_centroids: torch.Tensor,
+                         v_centroids: torch.Tensor, qjl_matrix: torch.Tensor, scale: float | None = None,
+                         out: torch.Tensor | None = None, out_dtype: torch.dtype | None = None,
+                         workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                         check: bool = False) -> torch.Tensor:
+    """tq_paged_decode with product-quantised key pages (k_bits = log2(len(k_mse_centroids)) + 1)."""
+    dev = _need_cuda("tq_paged_decode_prod", q, k_pages, v_pages, block_table, seq_lens, signs, k_mse_centroids,
+                     v_centroids, qjl_matrix)
+    if q.dim() != 3 or k_pages.dim() != 4 or v_pages.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("tq_paged_decode_prod: q [B, Hq, D], pages [NB, bs, H, RB], block_table [B, maxblk] expected")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32 or q.dtype not in _DTYPES:
+        raise ValueError("tq_paged_decode_prod: block_table / seq_lens int32, q f32/f16/bf16 expected")
+    b, hq, d = q.shape
+    nb, bs, h, _ = k_pages.shape
+    kb = k_mse_centroids.numel().bit_length()
+    vb = _bits_from_centroids(v_centroids)
+    if k_pages.shape[3] != tq_prod_row_bytes(d, kb) or v_pages.shape[3] != tq_row_bytes(d, vb) or \
+            tuple(v_pages.shape[:3]) != (nb, bs, h) or block_table.shape[0] != b or seq_lens.numel() != b or \
+            tuple(qjl_matrix.shape) != (d, d):
+        raise ValueError("tq_paged_decode_prod: page / table / matrix shapes inconsistent with q and the codebooks")
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=out_dtype, device=dev)
+    maxb = block_table.shape[1]
+    need = int(lib().tq_paged_decode_prod_workspace(b, hq, h, d, maxb, bs))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_paged_decode_prod(_ptr(q), _DTYPES[q.dtype], b, hq, h, d, _ptr(k_pages), kb, _ptr(v_pages),
+                                          vb, nb, bs, _ptr(block_table), maxb, _ptr(seq_lens), _ptr(signs),
+                                          _ptr(k_mse_centroids), _ptr(v_centroids), _ptr(qjl_matrix),
+                                          float(scale or 0.0), _ptr(out), _DTYPES[out.dtype], _ptr(workspace),
+                                          workspace.numel(), _ptr(status), _stream(dev)))
+    if check and status is not None:
+        raise_for_device_status(status)
     return out

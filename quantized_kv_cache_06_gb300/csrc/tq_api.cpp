@@ -474,4 +474,116 @@ tq_status tq_paged_decode_static(const void* q, tq_dtype q_dtype, int batch, int
                          v_centroids, scale, out, out_dtype, scratch, capacity, status_dev, stream);
 }
 
+// ---------------------------------------------------------------- product-quantised keys
+
+int64_t tq_prod_row_bytes(int head_dim, int bits) {
+  if (!pow2_dim_ok(head_dim) || !bits_ok(bits)) return -1;
+  return ((int64_t)head_dim * (bits - 1) + 7) / 8 + (head_dim + 7) / 8 + 8;
+}
+
+tq_status tq_build_qjl_matrix(int head_dim, uint64_t seed, float* s_host) {
+  if (!s_host) return fail(TQ_ERR_INVALID_ARG, "tq_build_qjl_matrix: s_host is NULL");
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  // splitmix64 (Steele, Lea & Flood 2014), outputs in pairs through Box-Muller (1958)
+  uint64_t state = seed;
+  auto next = [&state]() {
+    state += 0x9E3779B97F4A7C15ull;
+    uint64_t z = state;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+  };
+  const int64_t n = (int64_t)head_dim * head_dim;  // even
+  for (int64_t k = 0; k < n; k += 2) {
+    const uint64_t z1 = next(), z2 = next();
+    const double u1 = (double)((z1 >> 11) + 1) * 0x1p-53;  // (0, 1]
+    const double u2 = (double)(z2 >> 11) * 0x1p-53;        // [0, 1)
+    const double rad = std::sqrt(-2.0 * std::log(u1));
+    s_host[k] = (float)(rad * std::cos(2.0 * M_PI * u2));
+    s_host[k + 1] = (float)(rad * std::sin(2.0 * M_PI * u2));
+  }
+  return ok();
+}
+
+tq_status tq_write_kv_prod(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, int num_kv_heads,
+                           int head_dim, int bits, const int64_t* slots, uint8_t* pages, int64_t num_blocks,
+                           int block_size, const float* signs, const float* mse_centroids,
+                           const float* qjl_matrix, int32_t* status_dev, void* stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 0 || block_size < 1)
+    return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: invalid sizes (tokens=%lld, kv_heads=%d, blocks=%lld, block_size=%d)",
+                (long long)num_tokens, num_kv_heads, (long long)num_blocks, block_size);
+  if (!tq::prod_supported(head_dim, bits))
+    return fail(TQ_ERR_UNSUPPORTED, "tq_write_kv_prod: head_dim %d / bits %d: needs head_dim 64 or 128 and bits 3..5",
+                head_dim, bits);
+  if (!dtype_ok(raw_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: unknown raw dtype %d", (int)raw_dtype);
+  if (!status_dev) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: status_dev is required");
+  if (num_tokens > 0 && (!raw || !slots || !pages || !signs || !mse_centroids || !qjl_matrix))
+    return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: null pointer argument");
+  if (num_tokens > 0 && (!aligned(raw, 16) || !aligned(pages, 16) || !aligned(slots, 8) || !aligned(signs, 4) ||
+                         !aligned(mse_centroids, 4) || !aligned(qjl_matrix, 4) || !aligned(status_dev, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: raw and pages must be 16-byte aligned, slots 8-byte aligned");
+  tq::WriteArgs a{raw, (int)raw_dtype, num_tokens, num_kv_heads, head_dim, bits, slots, pages,
+                  num_blocks, block_size, signs, mse_centroids, status_dev};
+  return check_cuda(tq::launch_write_prod(a, qjl_matrix, static_cast<cudaStream_t>(stream), current_device_sms()),
+                    "tq_write_kv_prod launch");
+}
+
+size_t tq_paged_decode_prod_workspace(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                      int max_blocks_per_seq, int block_size) {
+  if (decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size) != TQ_OK)
+    return 0;
+  tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  a.k_bits = a.v_bits = 0;  // the SIMT split plan
+  return tq::prod_decode_workspace(a, tq::plan_decode(a, current_device_sms()));
+}
+
+tq_status tq_paged_decode_prod(const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int num_kv_heads,
+                               int head_dim, const uint8_t* k_pages, int k_bits, const uint8_t* v_pages,
+                               int v_bits, int64_t num_blocks, int block_size, const int32_t* block_table,
+                               int max_blocks_per_seq, const int32_t* seq_lens, const float* signs,
+                               const float* k_mse_centroids, const float* v_centroids, const float* qjl_matrix,
+                               float scale, void* out, tq_dtype out_dtype, void* workspace,
+                               size_t workspace_bytes, int32_t* status_dev, void* stream) {
+  const char* name = "tq_paged_decode_prod";
+  tq_status st = decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  if (st != TQ_OK) return st;
+  if (!tq::prod_supported(head_dim, k_bits) || !bits_ok(v_bits))
+    return fail(TQ_ERR_UNSUPPORTED, "%s: head_dim %d, k_bits %d, v_bits %d: needs head_dim 64 or 128, k_bits 3..5, "
+                "v_bits 2..5", name, head_dim, k_bits, v_bits);
+  if (!dtype_ok(q_dtype) || !dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "%s: unknown dtype", name);
+  if (num_blocks < 0) return fail(TQ_ERR_INVALID_ARG, "%s: num_blocks < 0", name);
+  if (batch > 0 && (!q || !k_pages || !v_pages || !seq_lens || !signs || !k_mse_centroids || !v_centroids ||
+                    !qjl_matrix || !out || (max_blocks_per_seq > 0 && !block_table)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  if (batch > 0 && (!aligned(q, dtype_size(q_dtype)) || !aligned(out, dtype_size(out_dtype)) ||
+                    !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(block_table, 4) ||
+                    !aligned(seq_lens, 4) || !aligned(qjl_matrix, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: misaligned pointer (pages need 16-byte alignment)", name);
+  tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());  // SIMT split plan (k_bits 0)
+  const size_t need = tq::prod_decode_workspace(a, plan);
+  if (batch > 0 && (workspace_bytes < need || !workspace || !aligned(workspace, 16)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: workspace must be >= %zu bytes and 16-byte aligned (got %zu)", name, need,
+                workspace_bytes);
+  a.q = q;
+  a.q_dtype = (int)q_dtype;
+  a.k_pages = k_pages;
+  a.k_bits = k_bits;
+  a.v_pages = v_pages;
+  a.v_bits = v_bits;
+  a.num_blocks = num_blocks;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.signs = signs;
+  a.k_centroids = k_mse_centroids;
+  a.v_centroids = v_centroids;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = (int)out_dtype;
+  a.workspace = workspace;
+  a.status = status_dev;
+  a.v_alpha = a.k_alpha = 1.0f;
+  return check_cuda(tq::launch_decode_prod(a, qjl_matrix, plan, static_cast<cudaStream_t>(stream)), name);
+}
+
 }  // extern "C"

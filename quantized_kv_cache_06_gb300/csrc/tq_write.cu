@@ -124,14 +124,18 @@ cudaError_t launch_write_typed(const WriteArgs& a, cudaStream_t stream, int grid
 
 }  // namespace
 
+cudaError_t launch_validate_slots(const WriteArgs& a, cudaStream_t stream, int num_sms) {
+  const int vgrid = (int)std::min<int64_t>((a.num_tokens + 255) / 256, (int64_t)num_sms * 4);
+  validate_slots_kernel<<<vgrid, 256, 0, stream>>>(a.slots, a.num_tokens, a.num_blocks * a.block_size, a.status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream) {
   cudaError_t err = cudaMemsetAsync(a.status, 0, sizeof(int32_t), stream);
   if (err != cudaSuccess) return err;
   if (a.num_tokens == 0) return cudaSuccess;
   const int sms = device_sms();
-  const int vgrid = (int)std::min<int64_t>((a.num_tokens + 255) / 256, (int64_t)sms * 4);
-  validate_slots_kernel<<<vgrid, 256, 0, stream>>>(a.slots, a.num_tokens, a.num_blocks * a.block_size, a.status);
-  err = cudaGetLastError();
+  err = launch_validate_slots(a, stream, sms);
   if (err != cudaSuccess) return err;
   const int64_t rows = a.num_tokens * a.num_kv_heads;
   if (write_tc_supported(a)) {

@@ -124,3 +124,36 @@ def test_workspace_queries_cover_every_plan(tq):
         assert dec >= r * hq * (d + 2) * 4
         assert pre >= dec
     assert lib.tq_paged_prefill_workspace(2, 12, 8, 128, 4, 16) == 0  # group does not divide
+
+
+def test_prod_row_bytes_and_sketch_matrix_match_oracle(tq):
+    from oracle import qjl_oracle as qo
+
+    for d in (32, 64, 128, 256):
+        for b in (2, 3, 4, 5):
+            assert tq.tq_prod_row_bytes(d, b) == qo.prod_row_bytes(d, b)
+    assert tq.lib().tq_prod_row_bytes(128, 1) == -1
+    assert tq.lib().tq_prod_row_bytes(96, 4) == -1
+    # the library draws S in fp64 and rounds once: equal to the oracle's S rounded to fp32
+    for d, seed in [(64, 43), (128, 7), (32, 2**64 - 1)]:
+        got = tq.tq_build_qjl_matrix(d, seed).numpy()
+        assert np.array_equal(got, qo.normal_matrix(d, d, seed).astype(np.float32))
+
+
+def test_prod_host_argument_errors(tq):
+    lib = tq.lib()
+    dummy = 1 << 20
+    assert lib.tq_build_qjl_matrix(64, 1, None) == tq.TQ_ERR_INVALID_ARG
+    w = lambda d, b, status: (dummy, 1, 4, 2, d, b, dummy, dummy, 4, 16, dummy, dummy, dummy, status, None)
+    assert lib.tq_write_kv_prod(*w(256, 4, dummy)) == tq.TQ_ERR_UNSUPPORTED  # the kernels take D 64 / 128
+    assert lib.tq_write_kv_prod(*w(128, 2, dummy)) == tq.TQ_ERR_UNSUPPORTED  # and 3..5 bits
+    assert lib.tq_write_kv_prod(*w(128, 4, None)) == tq.TQ_ERR_INVALID_ARG
+    dec = lambda d, kb, vb, ws: (dummy, 1, 2, 32, 8, d, dummy, kb, dummy, vb, 8, 16, dummy, 4, dummy, dummy, dummy,
+                                 dummy, dummy, 0.0, dummy, 1, dummy, ws, None, None)
+    assert lib.tq_paged_decode_prod(*dec(256, 4, 4, 1 << 30)) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_paged_decode_prod(*dec(128, 6, 4, 1 << 30)) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_paged_decode_prod(*dec(128, 4, 4, 16)) == tq.TQ_ERR_INVALID_ARG  # workspace too small
+    for r, hq, h, d, maxb, bs in [(64, 32, 8, 128, 512, 16), (5, 8, 8, 64, 3, 5)]:
+        # partials per (row, q head) plus the projected query S R q
+        assert lib.tq_paged_decode_prod_workspace(r, hq, h, d, maxb, bs) >= r * hq * (2 * d + 2) * 4
+    assert lib.tq_paged_decode_prod_workspace(2, 12, 8, 128, 4, 16) == 0
