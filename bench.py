@@ -421,7 +421,9 @@ def run_gpu(args):
     line["next_rows"] = {"tq_dequant_rows": dequant_measure(tq, w, dev, kp, cache_slots, signs, ck, flush, stream, peak,
                                                              peak_kind, world),
                          "tq_paged_prefill": prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream,
-                                                             peak, peak_kind, world)}
+                                                             peak, peak_kind, world),
+                         "qjl_residual_keys": qjl_measure(tq, w, dev, kraw, slots, ws_np, vp, bt, lens, q, signs, cv,
+                                                          flush, stream, peak, peak_kind, world)}
 
     if not args.no_e2e:
         line["e2e"] = e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world)
@@ -515,6 +517,59 @@ def prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream, peak, 
                          "peak_source": peak_kind, "algorithmic_bytes_per_launch": unique,
                          "traffic": ncu_traffic("prefill")},
             "gpu_launches": 2 * (steps + 2)}
+
+
+def qjl_measure(tq, w, dev, kraw, slots, slots_np, vp, bt, lens, q, signs, cv, flush, stream, peak, peak_kind,
+                world, steps=3):
+    """Product-quantised (QJL residual) keys at the workload's key width: the step's K rows
+    written as product rows (tq_write_kv_prod), then the decode over them with the MSE value
+    pages (tq_paged_decode_prod); each timed apart with CUDA events, an L2 flush before
+    each call."""
+    import torch
+
+    d, kb = w.head_dim, w.k_bits
+    if d not in (64, 128) or not 3 <= kb <= 5:
+        return {"skipped": f"product-key kernels take head_dim 64/128 and 3..5 key bits (D{d}, K{kb})"}
+    rbp = tq.tq_prod_row_bytes(d, kb)
+    kmse = tq.tq_codebook(d, kb - 1, dev)[0]
+    smat = tq.tq_build_qjl_matrix(d, 43, dev)
+    kpp = torch.zeros(w.num_blocks, w.block_size, w.num_kv_heads, rbp, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    need = int(tq.lib().tq_paged_decode_prod_workspace(w.batch, w.num_q_heads, w.num_kv_heads, d, bt.shape[1],
+                                                       w.block_size))
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        fn()
+        times = []
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        tq.raise_for_device_status(st)
+        return max_over_ranks([statistics.mean(times)], world, dev)[0] / 1e3
+
+    wr_s = timed(lambda: tq.tq_write_kv_prod(kraw, kpp, slots, signs, kmse, smat, status=st, check=False))
+    dec_s = timed(lambda: tq.tq_paged_decode_prod(q, kpp, vp, bt, lens, signs, kmse, cv, smat, out=out, workspace=ws,
+                                                  status=st))
+    rows = int((slots_np >= 0).sum()) * w.num_kv_heads
+    wr_bytes = kraw.numel() * kraw.element_size() + rows * rbp + slots_np.size * 8
+    dec_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * (rbp + row_bytes(d, w.v_bits)) + \
+        2 * q.numel() * q.element_size()
+    wr_gbs, dec_gbs = wr_bytes / wr_s / 1e9, dec_bytes / dec_s / 1e9
+    return {"workload": f"{rows} K rows written as product rows (K{kb} = {kb - 1}-bit MSE + 1 sign bit, D{d}), "
+                        f"then the decode of the {w.batch} sequences over them with the V{w.v_bits} pages",
+            "write_us": wr_s * 1e6, "write_rows_per_s": weak_scaling_rate(world, rows, wr_s), "write_gbs": wr_gbs,
+            "write_frac_of_hbm": wr_gbs / peak, "sketch_tflops": rows * 2.0 * d * d / wr_s / 1e12,
+            "decode_us": dec_s * 1e6, "decode_gbs": dec_gbs, "decode_frac_of_hbm": dec_gbs / peak,
+            "algorithmic_bytes": {"write": wr_bytes, "decode": dec_bytes}, "peak": peak, "peak_source": peak_kind,
+            "kernels": "SIMT (write_prod_kernel; qjl_project_kernel + decode_prod_split_kernel + combine)",
+            "gpu_launches": 2 * (steps + 1) + 3 * (steps + 1)}
 
 
 def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5, chunks=8):

@@ -19,6 +19,7 @@
 
 #include "tq.h"
 #include "tq_internal.h"
+#include "tq_qjl.h"
 
 namespace {
 

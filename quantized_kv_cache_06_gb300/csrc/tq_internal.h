@@ -37,8 +37,6 @@ struct WriteArgs {
 
 // Enqueues: status <- 0, slot validation, row write.  Returns the first launch error.
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream);
-// Enqueues the slot check alone: status <- kSlotOutOfRange if a slot is past the pages.
-cudaError_t launch_validate_slots(const WriteArgs& a, cudaStream_t stream, int num_sms);
 
 // Tensor-core writer (tq_write_tc.cu): fp16 / bf16 rows, head_dim 64, 128 or 256, 2 to 5 bits.
 bool write_tc_supported(const WriteArgs& a);
@@ -123,15 +121,6 @@ cudaError_t launch_combine_splits(const float* acc, const float* ml, int rows, i
 
 // Split plan for the shapes in `a` on a device with `num_sms` SMs.
 DecodePlan plan_decode(const DecodeArgs& a, int num_sms);
-
-// Product-quantised key rows (tq_qjl.cu).  WriteArgs.bits and DecodeArgs.k_bits are the
-// total key bits b (MSE indices at b - 1 bits plus one sign bit); the centroids passed
-// for the keys are the (b - 1)-bit MSE codebook; smat is S, fp32 [D][D] row-major.
-bool prod_supported(int head_dim, int bits);
-cudaError_t launch_write_prod(const WriteArgs& a, const float* smat, cudaStream_t stream, int num_sms);
-// Workspace of the product-key decode for split plan p (a SIMT plan of plan_decode).
-size_t prod_decode_workspace(const DecodeArgs& a, const DecodePlan& p);
-cudaError_t launch_decode_prod(const DecodeArgs& a, const float* smat, const DecodePlan& p, cudaStream_t stream);
 
 // Enqueues the decode for plan `p`.  Returns the first launch error.
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);

@@ -27,7 +27,7 @@
 #include <cmath>
 
 #include "tq_device.cuh"
-#include "tq_internal.h"
+#include "tq_qjl.h"
 
 namespace tq {
 namespace {

@@ -12,6 +12,7 @@
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
+#include "tq_qjl.h"
 
 namespace tq {
 namespace {
