@@ -12,7 +12,15 @@
  *                    Diagnostic vs Serving Paths, direct-QK and packed-V).
  *
  * plus the host-side set-up the contract call needs (rotation signs, Lloyd-Max
- * codebook, row size).
+ * codebook, row size), and the calls that widen the path over the same pages:
+ *
+ *   tq_paged_decode_static  the decode without a caller workspace (fixed scratch).
+ *   tq_paged_prefill        mixed prefill/decode: query rows of one sequence share each
+ *                           dequantised key/value tile ("vLLM Usage", Runtime Dispatch).
+ *   tq_dequant_rows         dense readback of packed rows ("vLLM Reference Audit",
+ *                           tq4_decompress).
+ *   tq_write_kv_prod,       product-quantised ("QJL residual") key rows and the decode
+ *   tq_paged_decode_prod    over them ("vLLM Reference Audit", MSE and QJL codecs).
  *
  * Conventions shared by every entry point:
  *   - Every buffer is owned by the caller.  "device" pointers must point to memory of
