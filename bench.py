@@ -239,6 +239,76 @@ class OracleSample:
                 "write_rows_per_s": 2 * nw * w.num_kv_heads / t_write, "t_decode_s": t_dec, "t_write_s": t_write}
 
 
+def next_rows_cpu_baselines(w, n_write_tokens=2048, chunk=4):
+    """The oracle (as it stands) timed on bounded samples of the next rows' work, on this host's
+    cores, in the units of each row's GPU figure: the readback of sequence 0's K rows, a
+    `chunk`-row prefill chunk at the end of sequence 0, and for product-quantised keys the
+    write of `n_write_tokens` tokens' K rows plus the decode of sequence 0 over them.  The
+    pages hold sequence 0 only (its tokens at slots 0..n-1), written by the oracle, untimed."""
+    from oracle import qjl_oracle as qo
+    from oracle import tq_oracle as o
+
+    d, h, bs, hq = w.head_dim, w.num_kv_heads, w.block_size, w.num_q_heads
+    n0 = int(w.seq_lens[0])
+    nblk = max(1, -(-n0 // bs))
+    bt = np.arange(nblk, dtype=np.int32)[None]
+    slots = np.arange(n0, dtype=np.int64)
+    signs = o.splitmix64_signs(d, 42)
+    ck, cv = o.codebook_f32(d, w.k_bits)[0], o.codebook_f32(d, w.v_bits)[0]
+    rb_k, rb_v = row_bytes(d, w.k_bits), row_bytes(d, w.v_bits)
+    kraw, vraw = w.k_raw[:n0], w.v_raw[:n0]
+    kp = o.write_kv(kraw, np.zeros((nblk, bs, h, rb_k), np.uint8), slots, signs, ck, w.k_bits)
+    vp = o.write_kv(vraw, np.zeros((nblk, bs, h, rb_v), np.uint8), slots, signs, cv, w.v_bits)
+    cores = blas_threads()
+
+    def entry(value, sample):
+        return {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    out = {}
+    t0 = time.perf_counter()
+    o.dequant_slots(kp, slots, signs, ck, w.k_bits)
+    t = time.perf_counter() - t0
+    out["tq_dequant_rows"] = entry((n0 * h * (rb_k + 2 * d) + n0 * 8) / t / 1e9,
+                                   f"readback of the {n0 * h} K rows of sequence 0 (fp64 out)")
+
+    c = min(chunk, n0)
+    q = np.random.default_rng(7).standard_normal((c, hq, d)).astype(np.float16)
+    q_len = (n0 - c + 1 + np.arange(c)).astype(np.int64)
+    t0 = time.perf_counter()
+    o.paged_prefill(q, np.zeros(c, np.int64), q_len, kp, vp, w.k_bits, w.v_bits, bt, signs, ck, cv)
+    t = time.perf_counter() - t0
+    unique = n0 * h * (rb_k + rb_v) + 2 * q.size * 2
+    out["tq_paged_prefill"] = entry(unique / t / 1e9, f"{c} query rows at the end of sequence 0 ({n0} tokens), "
+                                                      "GB/s of unique bytes")
+
+    kb = w.k_bits
+    if d in (64, 128) and 3 <= kb <= 5:
+        rot = o.rotation_matrix(signs)
+        kc = o.codebook_f32(d, kb - 1)[0]
+        smat = qo.normal_matrix(d, d, 43).astype(np.float32).astype(np.float64)
+        rbp = qo.prod_row_bytes(d, kb)
+        nw = min(n_write_tokens, n0)
+        x = np.asarray(kraw[:nw], dtype=np.float64).reshape(-1, d)
+        t0 = time.perf_counter()
+        enc = qo.encode_prod(x, rot, kc, smat)
+        qo.pack_prod_rows(enc["idx"], enc["z"], enc["nu"], enc["gamma"], kb)
+        t_w = time.perf_counter() - t0
+        enc = qo.encode_prod(np.asarray(kraw, dtype=np.float64).reshape(-1, d), rot, kc, smat)
+        rows = qo.pack_prod_rows(enc["idx"], enc["z"], enc["nu"], enc["gamma"], kb).reshape(n0, h, rbp)
+        kpp = np.zeros((nblk * bs, h, rbp), np.uint8)
+        kpp[:n0] = rows
+        kpp = kpp.reshape(nblk, bs, h, rbp)
+        t0 = time.perf_counter()
+        qo.paged_decode_prod_keys(w.q[:1], kpp, vp, kb, w.v_bits, bt, np.array([n0]), signs, kc, cv, smat)
+        t_d = time.perf_counter() - t0
+        wr_bytes = nw * h * (d * kraw.itemsize + rbp) + nw * 8
+        dec_bytes = n0 * h * (rbp + rb_v) + 2 * w.q[:1].size * w.q.itemsize
+        out["qjl_residual_keys"] = {
+            "write": entry(wr_bytes / t_w / 1e9, f"product-key write of {nw} tokens x {h} K rows"),
+            "decode": entry(dec_bytes / t_d / 1e9, f"decode of sequence 0 ({n0} tokens) over product keys")}
+    return out
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -435,6 +505,9 @@ def run_gpu(args):
                                           f"{int(w.seq_lens[:sampler.n_seq].max())} tokens) and write of {sampler.nw} "
                                           f"tokens x {w.num_kv_heads} heads for K and V",
                                 "decode_seq_per_s": r["decode_seq_per_s"], "write_rows_per_s": r["write_rows_per_s"]}
+        for key, base in next_rows_cpu_baselines(w).items():
+            if key in line["next_rows"]:
+                line["next_rows"][key]["cpu_baseline"] = base
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:

@@ -76,3 +76,13 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 
     bench.run_reference(Args())
     assert capsys.readouterr().out == ""
+
+
+def test_next_rows_cpu_baselines_cover_each_row():
+    # the oracle timed beside each next row, on the tiny workload: every row present, in the
+    # unit of its GPU figure, positive, and labelled as the oracle
+    base = bench.next_rows_cpu_baselines(make_workload(1))
+    assert set(base) == {"tq_dequant_rows", "tq_paged_prefill", "qjl_residual_keys"}
+    entries = [base["tq_dequant_rows"], base["tq_paged_prefill"], *base["qjl_residual_keys"].values()]
+    for e in entries:
+        assert e["kind"] == "oracle" and e["unit"] == "GB/s" and e["value"] > 0 and e["cores"] >= 1
