@@ -406,7 +406,10 @@ def tq_paged_decode_prod(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.
         raise ValueError("tq_paged_decode_prod: block_table / seq_lens int32, q f32/f16/bf16 expected")
     b, hq, d = q.shape
     nb, bs, h, _ = k_pages.shape
-    kb = k_mse_centroids.numel().bit_length()
+    n = k_mse_centroids.numel()
+    kb = n.bit_length()
+    if n < 2 or (1 << (kb - 1)) != n:
+        raise ValueError(f"tq_paged_decode_prod: k_mse_centroids must hold 2^(k_bits-1) values, got {n}")
     vb = _bits_from_centroids(v_centroids)
     if k_pages.shape[3] != tq_prod_row_bytes(d, kb) or v_pages.shape[3] != tq_row_bytes(d, vb) or \
             tuple(v_pages.shape[:3]) != (nb, bs, h) or block_table.shape[0] != b or seq_lens.numel() != b or \
