@@ -166,6 +166,17 @@ def tq_codebook(head_dim: int, bits: int, device=None):
     return c, b
 
 
+def _need_f32(name: str, head_dim: int, signs: torch.Tensor, *others: torch.Tensor) -> None:
+    """The rotation signs, codebooks and sketch matrix are read by the kernels as fp32 arrays
+    of known length: another dtype, or fewer than head_dim signs, would make them read past
+    the buffer."""
+    for t in (signs, *others):
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name}: signs, codebooks and the sketch matrix must be float32, got {t.dtype}")
+    if signs.numel() != head_dim:
+        raise ValueError(f"{name}: signs must hold head_dim = {head_dim} values, got {signs.numel()}")
+
+
 def _bits_from_centroids(centroids: torch.Tensor) -> int:
     n = centroids.numel()
     bits = n.bit_length() - 1
@@ -191,6 +202,7 @@ def tq_write_kv(raw: torch.Tensor, pages: torch.Tensor, slots: torch.Tensor, sig
         raise ValueError("tq_write_kv: raw f32/f16/bf16, pages uint8, slots int64 expected")
     t, h, d = raw.shape
     bits = _bits_from_centroids(centroids)
+    _need_f32("tq_write_kv", d, signs, centroids)
     if pages.shape[2] != h or pages.shape[3] != tq_row_bytes(d, bits):
         raise ValueError(f"tq_write_kv: pages {tuple(pages.shape)} do not match H={h}, RB={tq_row_bytes(d, bits)}")
     if status is None:
@@ -219,6 +231,7 @@ def tq_dequant_rows(pages: torch.Tensor, slots: torch.Tensor, signs: torch.Tenso
     nb, bs, h, rb = pages.shape
     d = signs.numel()
     bits = _bits_from_centroids(centroids)
+    _need_f32("tq_dequant_rows", d, signs, centroids)
     if rb != tq_row_bytes(d, bits):
         raise ValueError(f"tq_dequant_rows: pages row bytes {rb} != RB({d}, {bits})")
     t = slots.numel()
@@ -260,6 +273,7 @@ def tq_paged_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tenso
     b, hq, d = q.shape
     nb, bs, h, _ = k_pages.shape
     kb, vb = _bits_from_centroids(k_centroids), _bits_from_centroids(v_centroids)
+    _need_f32("tq_paged_decode", d, signs, k_centroids, v_centroids)
     if k_pages.shape[3] != tq_row_bytes(d, kb) or v_pages.shape[3] != tq_row_bytes(d, vb) or \
             tuple(v_pages.shape[:3]) != (nb, bs, h) or block_table.shape[0] != b or seq_lens.numel() != b:
         raise ValueError("tq_paged_decode: page / table shapes inconsistent with q and the codebooks")
@@ -298,6 +312,7 @@ def tq_paged_prefill(q: torch.Tensor, q_seq: torch.Tensor, q_len: torch.Tensor, 
     t, hq, d = q.shape
     nb, bs, h, _ = k_pages.shape
     kb, vb = _bits_from_centroids(k_centroids), _bits_from_centroids(v_centroids)
+    _need_f32("tq_paged_prefill", d, signs, k_centroids, v_centroids)
     if k_pages.shape[3] != tq_row_bytes(d, kb) or v_pages.shape[3] != tq_row_bytes(d, vb) or \
             tuple(v_pages.shape[:3]) != (nb, bs, h) or q_seq.numel() != t or q_len.numel() != t:
         raise ValueError("tq_paged_prefill: page / row shapes inconsistent with q and the codebooks")
@@ -331,6 +346,7 @@ def tq_paged_decode_static(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
     b, hq, d = q.shape
     nb, bs, h, _ = k_pages.shape
     kb, vb = _bits_from_centroids(k_centroids), _bits_from_centroids(v_centroids)
+    _need_f32("tq_paged_decode_static", d, signs, k_centroids, v_centroids)
     if out.shape != q.shape or out.dtype not in _DTYPES:
         raise ValueError("tq_paged_decode_static: out must be [B, Hq, D] f32/f16/bf16")
     with torch.cuda.device(dev):
@@ -377,6 +393,7 @@ def tq_write_kv_prod(raw: torch.Tensor, pages: torch.Tensor, slots: torch.Tensor
         raise ValueError(f"tq_write_kv_prod: mse_centroids must hold 2^(bits-1) values, got {n}")
     if tuple(qjl_matrix.shape) != (d, d):
         raise ValueError(f"tq_write_kv_prod: qjl_matrix must be [{d}, {d}]")
+    _need_f32("tq_write_kv_prod", d, signs, mse_centroids)
     if pages.shape[2] != h or pages.shape[3] != tq_prod_row_bytes(d, bits):
         raise ValueError(f"tq_write_kv_prod: pages {tuple(pages.shape)} do not match H={h}, "
                          f"RBP={tq_prod_row_bytes(d, bits)}")
@@ -411,6 +428,7 @@ def tq_paged_decode_prod(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.
     if n < 2 or (1 << (kb - 1)) != n:
         raise ValueError(f"tq_paged_decode_prod: k_mse_centroids must hold 2^(k_bits-1) values, got {n}")
     vb = _bits_from_centroids(v_centroids)
+    _need_f32("tq_paged_decode_prod", d, signs, k_mse_centroids, v_centroids, qjl_matrix)
     if k_pages.shape[3] != tq_prod_row_bytes(d, kb) or v_pages.shape[3] != tq_row_bytes(d, vb) or \
             tuple(v_pages.shape[:3]) != (nb, bs, h) or block_table.shape[0] != b or seq_lens.numel() != b or \
             tuple(qjl_matrix.shape) != (d, d):

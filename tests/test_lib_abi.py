@@ -157,3 +157,19 @@ def test_prod_host_argument_errors(tq):
         # partials per (row, q head) plus the projected query S R q
         assert lib.tq_paged_decode_prod_workspace(r, hq, h, d, maxb, bs) >= r * hq * (2 * d + 2) * 4
     assert lib.tq_paged_decode_prod_workspace(2, 12, 8, 128, 4, 16) == 0
+
+
+def test_binding_refuses_float_buffers_the_kernels_would_overread(tq):
+    # signs, codebooks and the sketch matrix are fp32 arrays of known length on the device side
+    import torch
+
+    from quantized_kv_cache_06_gb300 import _lib
+
+    f32 = torch.zeros(128, dtype=torch.float32)
+    _lib._need_f32("x", 128, f32, torch.zeros(16), torch.zeros(128, 128))
+    with pytest.raises(ValueError, match="float32"):
+        _lib._need_f32("x", 128, f32.half(), torch.zeros(16))
+    with pytest.raises(ValueError, match="float32"):
+        _lib._need_f32("x", 128, f32, torch.zeros(128, 128, dtype=torch.float16))
+    with pytest.raises(ValueError, match="head_dim"):
+        _lib._need_f32("x", 128, torch.zeros(64), torch.zeros(16))
