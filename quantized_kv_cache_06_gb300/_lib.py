@@ -177,6 +177,24 @@ def _need_f32(name: str, head_dim: int, signs: torch.Tensor, *others: torch.Tens
         raise ValueError(f"{name}: signs must hold head_dim = {head_dim} values, got {signs.numel()}")
 
 
+def _need_out(name: str, out: torch.Tensor, shape: tuple, device: torch.device) -> None:
+    """A caller-supplied output must have exactly the rows the kernels write."""
+    if tuple(out.shape) != tuple(shape) or out.dtype not in _DTYPES:
+        raise ValueError(f"{name}: out must be {list(shape)} f32/f16/bf16, got {list(out.shape)} {out.dtype}")
+    _need_cuda(name, out)
+    if out.device != device:
+        raise ValueError(f"{name}: out must be on {device}")
+
+
+def _need_status(name: str, status: torch.Tensor | None, device: torch.device | None = None) -> None:
+    """A caller-supplied status word: one int32 (at least) on the call's device."""
+    if status is None:
+        return
+    if status.dtype != torch.int32 or status.numel() < 1 or status.device.type != "cuda" or \
+            (device is not None and status.device != device):
+        raise ValueError(f"{name}: status must be an int32 tensor of at least one element on the call's device")
+
+
 def _bits_from_centroids(centroids: torch.Tensor) -> int:
     n = centroids.numel()
     bits = n.bit_length() - 1
@@ -205,6 +223,7 @@ def tq_write_kv(raw: torch.Tensor, pages: torch.Tensor, slots: torch.Tensor, sig
     _need_f32("tq_write_kv", d, signs, centroids)
     if pages.shape[2] != h or pages.shape[3] != tq_row_bytes(d, bits):
         raise ValueError(f"tq_write_kv: pages {tuple(pages.shape)} do not match H={h}, RB={tq_row_bytes(d, bits)}")
+    _need_status("tq_write_kv", status, dev)
     if status is None:
         status = _status_buffer(dev)
     with torch.cuda.device(dev):
@@ -240,6 +259,7 @@ def tq_dequant_rows(pages: torch.Tensor, slots: torch.Tensor, signs: torch.Tenso
     if tuple(out.shape) != (t, h, d) or out.dtype not in _DTYPES:
         raise ValueError(f"tq_dequant_rows: out must be [{t}, {h}, {d}] f32/f16/bf16")
     _need_cuda("tq_dequant_rows", pages, out)
+    _need_status("tq_dequant_rows", status, dev)
     if status is None:
         status = _status_buffer(dev)
     with torch.cuda.device(dev):
@@ -280,6 +300,8 @@ def tq_paged_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tenso
     out_dtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty((b, hq, d), dtype=out_dtype, device=dev)
+    _need_out("tq_paged_decode", out, (b, hq, d), dev)
+    _need_status("tq_paged_decode", status, dev)
     maxb = block_table.shape[1]
     need = tq_paged_decode_workspace(b, hq, h, d, maxb, bs)
     if workspace is None or workspace.numel() < need:
@@ -319,6 +341,8 @@ def tq_paged_prefill(q: torch.Tensor, q_seq: torch.Tensor, q_len: torch.Tensor, 
     out_dtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty((t, hq, d), dtype=out_dtype, device=dev)
+    _need_out("tq_paged_prefill", out, (t, hq, d), dev)
+    _need_status("tq_paged_prefill", status, dev)
     s_rows, maxb = block_table.shape
     need = int(lib().tq_paged_prefill_workspace(t, hq, h, d, maxb, bs))
     if workspace is None or workspace.numel() < need:
@@ -349,6 +373,7 @@ def tq_paged_decode_static(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
     _need_f32("tq_paged_decode_static", d, signs, k_centroids, v_centroids)
     if out.shape != q.shape or out.dtype not in _DTYPES:
         raise ValueError("tq_paged_decode_static: out must be [B, Hq, D] f32/f16/bf16")
+    _need_status("tq_paged_decode_static", status, dev)
     with torch.cuda.device(dev):
         _check(lib().tq_paged_decode_static(_ptr(q), _DTYPES[q.dtype], b, hq, h, d, _ptr(k_pages), kb,
                                             _ptr(v_pages), vb, nb, bs, _ptr(block_table), block_table.shape[1],
@@ -397,6 +422,7 @@ def tq_write_kv_prod(raw: torch.Tensor, pages: torch.Tensor, slots: torch.Tensor
     if pages.shape[2] != h or pages.shape[3] != tq_prod_row_bytes(d, bits):
         raise ValueError(f"tq_write_kv_prod: pages {tuple(pages.shape)} do not match H={h}, "
                          f"RBP={tq_prod_row_bytes(d, bits)}")
+    _need_status("tq_write_kv_prod", status, dev)
     if status is None:
         status = _status_buffer(dev)
     with torch.cuda.device(dev):
@@ -436,6 +462,8 @@ def tq_paged_decode_prod(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.
     out_dtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty((b, hq, d), dtype=out_dtype, device=dev)
+    _need_out("tq_paged_decode_prod", out, (b, hq, d), dev)
+    _need_status("tq_paged_decode_prod", status, dev)
     maxb = block_table.shape[1]
     need = int(lib().tq_paged_decode_prod_workspace(b, hq, h, d, maxb, bs))
     if workspace is None or workspace.numel() < need:

@@ -173,3 +173,18 @@ def test_binding_refuses_float_buffers_the_kernels_would_overread(tq):
         _lib._need_f32("x", 128, f32, torch.zeros(128, 128, dtype=torch.float16))
     with pytest.raises(ValueError, match="head_dim"):
         _lib._need_f32("x", 128, torch.zeros(64), torch.zeros(16))
+
+
+def test_binding_refuses_outputs_and_status_words_the_kernels_would_overrun(tq):
+    import torch
+
+    from quantized_kv_cache_06_gb300 import _lib
+
+    with pytest.raises(ValueError, match="out must be"):
+        _lib._need_out("x", torch.zeros(2, 4, 64), (2, 4, 128), torch.device("cpu"))
+    with pytest.raises(ValueError, match="out must be"):
+        _lib._need_out("x", torch.zeros(2, 4, 128, dtype=torch.int32), (2, 4, 128), torch.device("cpu"))
+    _lib._need_status("x", None)
+    for bad in (torch.zeros(1, dtype=torch.int64), torch.zeros(0, dtype=torch.int32), torch.zeros(1, dtype=torch.int32)):
+        with pytest.raises(ValueError, match="status"):
+            _lib._need_status("x", bad)  # wrong dtype, empty, or not on a CUDA device
