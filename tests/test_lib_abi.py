@@ -188,3 +188,12 @@ def test_binding_refuses_outputs_and_status_words_the_kernels_would_overrun(tq):
     for bad in (torch.zeros(1, dtype=torch.int64), torch.zeros(0, dtype=torch.int32), torch.zeros(1, dtype=torch.int32)):
         with pytest.raises(ValueError, match="status"):
             _lib._need_status("x", bad)  # wrong dtype, empty, or not on a CUDA device
+
+
+def test_build_compiles_every_source_file():
+    # a translation unit left out of the build list would be missing from the library on a
+    # machine that builds from source
+    from quantized_kv_cache_06_gb300 import build
+
+    on_disk = {f for f in os.listdir(build.CSRC) if f.endswith((".cu", ".cpp"))}
+    assert set(build.SOURCES) == on_disk
