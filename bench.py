@@ -35,6 +35,13 @@ if ROOT not in sys.path:
 
 METRIC = "TQ paged decode KV GB/s (% of HBM peak) and seq/s; tq_write_kv rows/s"
 WORKLOAD_CFG = 4
+# What "dtype" stands for: the arithmetic of the path, kernel by kernel.
+DTYPE_NOTE = ("writer: fp16/bf16 raw rows rotated by m16n8k16 MMAs with fp32 accumulation (fp32 rows on the "
+              "SIMT writer), norms and quantiser decisions in fp32; decode: m16n8k16 fp16 MMA operands with fp32 "
+              "accumulation (query split into fp16 hi + lo, fp16 centroid table entries, fp16 value weights; the "
+              "fp16 remainders of keys and values added on tiles of large norm), softmax and split-K merge in fp32")
+THREADS_NOTE = ("cores = the BLAS threads the oracle's matrix products use; its unpacking, gathers and softmax "
+                "run in one thread; host_cores = os.cpu_count()")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -367,7 +374,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w, args.batch),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "host_cores": os.cpu_count(),
+                             "threads_note": THREADS_NOTE, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -446,13 +454,17 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = tq.tq_launch_count()
     t0.record(stream)
     for i in range(args.steps):
         step(events[i])
     t1.record(stream)
     torch.cuda.synchronize()
+    launches = tq.tq_launch_count() - launches0
     barrier(world)
     clk = clocks.stop()
+    for s in (st_k, st_v, st_d):  # the status words of the last timed step
+        tq.raise_for_device_status(s)
     total_ms = t0.elapsed_time(t1)
     wk = [e[0].elapsed_time(e[1]) for e in events]
     wv = [e[1].elapsed_time(e[2]) for e in events]
@@ -481,13 +493,14 @@ def run_gpu(args):
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(w, args.batch),
+            "vs_baseline": None, "dtype": "f16/f32", "dtype_note": DTYPE_NOTE, "data": "synthetic",
+            "config": workload_config(w, args.batch),
             "decode_us": dec_max * 1e3, "decode_gbs_per_gpu": dec_gbs, "decode_frac_of_peak": dec_gbs / peak,
             "decode_seq_per_s": weak_scaling_rate(world, w.batch, dec_s),
             "write_us_per_component": write_s / 2 * 1e6, "write_rows_per_s": weak_scaling_rate(world, head_rows, write_s),
             "write_token_rows_per_s": weak_scaling_rate(world, 2 * write_tokens, write_s), "write_gbs_per_gpu": wr_gbs,
             "roofline": dominant, "roofline_decode": roof_dec, "roofline_write": roof_wr,
-            "gpu_launches": args.steps * 6, "clocks": clk}
+            "gpu_launches": launches, "clocks": clk}
     line["next_rows"] = {"tq_dequant_rows": dequant_measure(tq, w, dev, kp, cache_slots, signs, ck, flush, stream, peak,
                                                              peak_kind, world),
                          "tq_paged_prefill": prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream,
@@ -500,7 +513,8 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         sampler = OracleSample(w, min(2, w.batch), 4096)
         r = sampler.run()
-        line["cpu_baseline"] = {"value": r["decode_gbs"], "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+        line["cpu_baseline"] = {"value": r["decode_gbs"], "unit": "GB/s", "cores": blas_threads(),
+                                "host_cores": os.cpu_count(), "threads_note": THREADS_NOTE, "kind": "oracle",
                                 "sample": f"oracle decode of {sampler.n_seq} sequences ({w.num_q_heads} q heads, "
                                           f"{int(w.seq_lens[:sampler.n_seq].max())} tokens) and write of {sampler.nw} "
                                           f"tokens x {w.num_kv_heads} heads for K and V",

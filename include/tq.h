@@ -21,6 +21,10 @@
  *                           tq4_decompress).
  *   tq_write_kv_prod,       product-quantised ("QJL residual") key rows and the decode
  *   tq_paged_decode_prod    over them ("vLLM Reference Audit", MSE and QJL codecs).
+ *   tq_write_kv_recipe,     the recipe cache modes turboquant25 / turboquant35: grouped
+ *   tq_paged_decode_recipe  product-quantised K and V rows ("vLLM Usage", Cache Dtypes;
+ *                           "Architecture", vLLM Runtime Mapping), with the metadata
+ *                           helpers tq_recipe_channel_order and tq_recipe_calibrate.
  *
  * Conventions shared by every entry point:
  *   - Every buffer is owned by the caller.  "device" pointers must point to memory of
@@ -73,9 +77,29 @@ typedef enum tq_dtype { TQ_F32 = 0, TQ_F16 = 1, TQ_BF16 = 2 } tq_dtype;
  * The pointer stays valid until the next library call on that thread. */
 const char* tq_last_error(void);
 
+/* Failure-path testing hook (the pages have no counterpart).  Every device-side wait of
+ * the tensor-core decode is bounded: after a number of tries it gives up, the kernel
+ * records TQ_ERR_TIMEOUT in status_dev and returns (its copies in flight drained first),
+ * so a wait that cannot end never hangs the GPU.  This sets the number of tries of the
+ * pipeline waits of launches made after the call: `tries` >= 0 sets it (0: every such
+ * wait gives up at once, so a decode with at least one block reports TQ_ERR_TIMEOUT and
+ * leaves its output incomplete), `tries` < 0 restores the default.  Returns the previous
+ * value.  Process-wide; meant for tests that check the timeout is reported and that the
+ * next call with the default is correct, not for production use. */
+int64_t tq_set_wait_limit(int64_t tries);
+
+/* Number of kernel launches the library has enqueued in this process, all devices and
+ * streams together (each launch counted once its launch call returned without error).
+ * For measurement: the difference over a timed region is the number of the library's own
+ * kernels that region ran. */
+uint64_t tq_launch_count(void);
+
 /* Row size in bytes for one component, one token and one KV head: ceil(D*b/8) + 4
  * ("vLLM Usage", TQ Byte Layout).  Returns -1 when head_dim or bits is unsupported. */
 int64_t tq_row_bytes(int head_dim, int bits);
+
+/* Lloyd-Max codebooks exist for bits 1..5 (tq_codebook); rows and kernels take 2..5, the
+ * 1-bit codebook serves the MSE part of 2-bit recipe groups. */
 
 /* RHT signs for build_rotation(dim, RHT, seed) ("vLLM Usage", TQ Packed Page Contract).
  * Writes head_dim values in {-1.0f, +1.0f} to signs_host[0..D): sign i is -1 when the
@@ -104,16 +128,23 @@ tq_status tq_codebook(int head_dim, int bits, float* centroids_host, float* boun
  *   pages      device, uint8[num_blocks][block_size][num_kv_heads][RB(D, bits)].
  *   signs      device, float[head_dim] from tq_build_rotation.
  *   centroids  device, float[2^bits] ascending, from tq_codebook.
- *   status_dev device int32, required: set to 0 at the start of the call, then to
- *              TQ_ERR_SLOT_OUT_OF_RANGE if any slot >= num_blocks * block_size -- in
- *              that case NO row is written (validation runs before the write).
+ *   status_dev device int32 or NULL.  If not NULL: set to 0 at the start of the call,
+ *              then to TQ_ERR_SLOT_OUT_OF_RANGE if any slot >= num_blocks * block_size
+ *              -- in that case NO row is written (validation runs before the write) --
+ *              and the call stays asynchronous (it can be captured in a CUDA graph; the
+ *              caller reads the word later).  If NULL ("Slot Mapping": a slot outside
+ *              the allocated pages raises): the call uses a status word of the library
+ *              (one per device, shared by such calls, which the library serialises),
+ *              synchronises `stream` and returns TQ_ERR_SLOT_OUT_OF_RANGE itself when a
+ *              slot was out of range (nothing written) or TQ_OK.  That form cannot be
+ *              captured in a CUDA graph (its synchronisation fails with TQ_ERR_CUDA).
  *
  * Each row x is encoded as: nu = ||x||_2 (fp32), u = x / nu (0 if nu == 0),
  * y = R u (fp32, in-register FWHT), index_j = #{k : boundary_k < y_j} (the nearest
  * centroid, ties to the lower index), packed LSB-first, norm appended.  Rows of
  * skipped tokens keep their previous bytes.  Duplicate non-negative slots: which
- * token's row survives is unspecified.  Asynchronous; errors detected on the host:
- * TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA. */
+ * token's row survives is unspecified.  Asynchronous unless status_dev is NULL; errors
+ * detected on the host: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA. */
 tq_status tq_write_kv(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, int num_kv_heads,
                       int head_dim, int bits, const int64_t* slots, uint8_t* pages,
                       int64_t num_blocks, int block_size, const float* signs,
@@ -274,7 +305,7 @@ int64_t tq_prod_row_bytes(int head_dim, int bits);
 tq_status tq_build_qjl_matrix(int head_dim, uint64_t seed, float* s_host);
 
 /* Key writer for product-quantised rows: tq_write_kv's contract (raw, slots, pages,
- * status_dev and its errors) with rows of RBP(D, bits) bytes.
+ * status_dev -- NULL included -- and its errors) with rows of RBP(D, bits) bytes.
  *   mse_centroids  device, float[2^(bits-1)] from tq_codebook(head_dim, bits - 1)
  *   qjl_matrix     device, float[head_dim][head_dim] from tq_build_qjl_matrix
  * Per row (fp32): nu, y and the indices exactly as tq_write_kv at bits - 1; r = y -
@@ -304,6 +335,79 @@ tq_status tq_paged_decode_prod(const void* q, tq_dtype q_dtype, int batch, int n
                                const float* k_mse_centroids, const float* v_centroids, const float* qjl_matrix,
                                float scale, void* out, tq_dtype out_dtype, void* workspace,
                                size_t workspace_bytes, int32_t* status_dev, void* stream);
+
+/* ---------------------------------------------------------------- recipe cache modes
+ *
+ * turboquant25 / turboquant35 ("vLLM Usage": Cache Dtypes -- recipe modes require
+ * metadata; Metadata Validation Rules; Page Geometry -- recipe row-byte overrides;
+ * "Architecture", vLLM Runtime Mapping: channels selected by energy, grouped MSE+QJL rows).
+ * The pages give no numbers; the readings: the recipe name is the mean bits per channel.
+ * A row's D channels form a high and a low group of d = D/2 channels each, coded at 3 and 2
+ * bits (turboquant25) or 4 and 3 bits (turboquant35).  Each group is a product-quantised
+ * vector of dimension d (tq_write_kv_prod's codec at head_dim d: (b-1)-bit MSE indices of
+ * R_d x_g/||x_g||, d sign bits of S_d r, fp32 nu and gamma), R_d the RHT of dimension d and
+ * seed 42 (tq_build_rotation(d, 42)), S_d = tq_build_qjl_matrix(d, 43), the MSE codebooks
+ * tq_codebook(d, b - 1).  The row holds the high group's bytes, then the low group's.  K and
+ * V both use recipe rows.  head_dim 64 or 128. */
+typedef enum tq_recipe { TQ_RECIPE_TURBOQUANT25 = 25, TQ_RECIPE_TURBOQUANT35 = 35 } tq_recipe;
+
+/* Bytes of one recipe row (56 / 72 at head_dim 128 for turboquant25 / 35); -1 when the recipe
+ * or head_dim is unsupported. */
+int64_t tq_recipe_row_bytes(int recipe, int head_dim);
+
+/* The metadata check ("Metadata Validation Rules": sorted unique high-group indices, inside
+ * the head, as many as the recipe expects -- D/2, fixed by the array shape) and the channel
+ * order the kernels take.
+ *   high_host   host int32[num_kv_heads][head_dim / 2]: each kv head's high-group channels.
+ *   order_host  host int32[num_kv_heads][head_dim]: the high group, then the low group (the
+ *               other channels, ascending).
+ * Errors: TQ_ERR_INVALID_ARG naming the broken rule (an index outside [0, head_dim), not
+ * sorted or repeated), an unknown recipe or an odd head_dim. */
+tq_status tq_recipe_channel_order(int recipe, int head_dim, int num_kv_heads, const int32_t* high_host,
+                                  int32_t* order_host);
+
+/* Calibration ("Architecture": channels selected by energy): per kv head, the head_dim / 2
+ * channels of largest energy sum_t x[t][h][c]^2 (fp64 sums; ties to the lower channel),
+ * ascending.
+ *   samples_host  host float[num_samples][num_kv_heads][head_dim]
+ *   high_host     host int32[num_kv_heads][head_dim / 2], written. */
+tq_status tq_recipe_calibrate(int recipe, int head_dim, int num_kv_heads, const float* samples_host,
+                              int64_t num_samples, int32_t* high_host);
+
+/* Recipe row writer: tq_write_kv's contract (raw, slots -- negative skipped, out of range an
+ * error with nothing written --, pages of RB = tq_recipe_row_bytes, status_dev NULL or not)
+ * for K or V.
+ *   channel_order  device int32[num_kv_heads][head_dim] from tq_recipe_channel_order
+ *   group_signs    device float[head_dim / 2] = tq_build_rotation(head_dim / 2, 42)
+ *   mse_high       device float[2^(b_high - 1)] = tq_codebook(head_dim / 2, b_high - 1)
+ *   mse_low        device float[2^(b_low - 1)]
+ *   qjl_matrix     device float[head_dim / 2][head_dim / 2] = tq_build_qjl_matrix(head_dim / 2, 43)
+ * Per group (fp32): the gathered channels x_g, nu = ||x_g||, y = R_d x_g / nu, the nearest
+ * centroid indices, r = y - c[idx], gamma = ||r||, z_i = [(S_d r)_i >= 0]. */
+tq_status tq_write_kv_recipe(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, int num_kv_heads, int head_dim,
+                             int recipe, const int64_t* slots, uint8_t* pages, int64_t num_blocks, int block_size,
+                             const int32_t* channel_order, const float* group_signs, const float* mse_high,
+                             const float* mse_low, const float* qjl_matrix, int32_t* status_dev, void* stream);
+
+/* Workspace bytes of tq_paged_decode_recipe (split partials with two accumulators per group,
+ * and the projected queries); 0 when the arguments are invalid. */
+size_t tq_paged_decode_recipe_workspace(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int max_blocks_per_seq, int block_size);
+
+/* Paged decode over recipe K and V pages (both of tq_recipe_row_bytes(recipe, head_dim)
+ * bytes per row).  Every other argument, the status word and the errors are those of
+ * tq_paged_decode; the codec arguments are those of tq_write_kv_recipe.  The score of key
+ * row k is scale * sum_g nu_g (<R_d q_g, c_g[idx]> + gamma_g sqrt(pi/2)/d <S_d R_d q_g, 2z - 1>)
+ * with q_g the query's channels of group g; the value of row v is, per group,
+ * nu_g R_d^T (c_g[idx] + gamma_g sqrt(pi/2)/d S_d^T (2z - 1)) put back at the group's
+ * channels. */
+tq_status tq_paged_decode_recipe(const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int num_kv_heads,
+                                 int head_dim, const uint8_t* k_pages, const uint8_t* v_pages, int recipe,
+                                 int64_t num_blocks, int block_size, const int32_t* block_table, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, const int32_t* channel_order, const float* group_signs,
+                                 const float* mse_high, const float* mse_low, const float* qjl_matrix, float scale,
+                                 void* out, tq_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                 int32_t* status_dev, void* stream);
 
 #ifdef __cplusplus
 }

@@ -13,6 +13,9 @@ from ._lib import (  # noqa: F401
     TQ_ERR_TIMEOUT,
     TQ_ERR_UNSUPPORTED,
     TQ_OK,
+    TQ_RECIPE_TURBOQUANT25,
+    TQ_RECIPE_TURBOQUANT35,
+    RecipeCodec,
     TQError,
     lib,
     raise_for_device_status,
@@ -20,13 +23,20 @@ from ._lib import (  # noqa: F401
     tq_build_rotation,
     tq_codebook,
     tq_dequant_rows,
+    tq_launch_count,
     tq_paged_decode,
     tq_paged_decode_prod,
+    tq_paged_decode_recipe,
     tq_paged_decode_static,
     tq_paged_decode_workspace,
     tq_paged_prefill,
     tq_prod_row_bytes,
+    tq_recipe_calibrate,
+    tq_recipe_channel_order,
+    tq_recipe_row_bytes,
     tq_row_bytes,
+    tq_set_wait_limit,
     tq_write_kv,
     tq_write_kv_prod,
+    tq_write_kv_recipe,
 )

@@ -35,11 +35,19 @@ STATUS_NAMES = {
 
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
+TQ_RECIPE_TURBOQUANT25 = 25
+TQ_RECIPE_TURBOQUANT35 = 35
+RECIPES = {"turboquant25": TQ_RECIPE_TURBOQUANT25, "turboquant35": TQ_RECIPE_TURBOQUANT35}
+RECIPE_ROTATION_SEED = 42
+RECIPE_SKETCH_SEED = 43
+
 # Every symbol include/tq.h declares, with (restype, argtypes).
 _c_int, _c_i64, _c_u64, _c_f, _c_p, _c_sz = (ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float,
                                             ctypes.c_void_p, ctypes.c_size_t)
 SIGNATURES = {
     "tq_last_error": (ctypes.c_char_p, []),
+    "tq_set_wait_limit": (_c_i64, [_c_i64]),
+    "tq_launch_count": (ctypes.c_uint64, []),
     "tq_row_bytes": (_c_i64, [_c_int, _c_int]),
     "tq_build_rotation": (_c_int, [_c_int, _c_u64, _c_p]),
     "tq_codebook": (_c_int, [_c_int, _c_int, _c_p, _c_p]),
@@ -66,6 +74,15 @@ SIGNATURES = {
     "tq_paged_decode_prod": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
                                       _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p,
                                       _c_int, _c_p, _c_sz, _c_p, _c_p]),
+    "tq_recipe_row_bytes": (_c_i64, [_c_int, _c_int]),
+    "tq_recipe_channel_order": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p]),
+    "tq_recipe_calibrate": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_p]),
+    "tq_write_kv_recipe": (_c_int, [_c_p, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_p, _c_p, _c_i64, _c_int, _c_p,
+                                    _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "tq_paged_decode_recipe_workspace": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tq_paged_decode_recipe": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_int, _c_i64,
+                                        _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_int,
+                                        _c_p, _c_sz, _c_p, _c_p]),
 }
 
 _lib = None
@@ -140,6 +157,17 @@ def raise_for_device_status(status: torch.Tensor) -> None:
 
 
 # ---------------------------------------------------------------- host set-up
+
+def tq_set_wait_limit(tries: int) -> int:
+    """Failure-path testing hook: tries of the decode's bounded device waits for later
+    launches (>= 0), or the default (< 0).  Returns the previous value."""
+    return int(lib().tq_set_wait_limit(int(tries)))
+
+
+def tq_launch_count() -> int:
+    """Kernel launches the library has enqueued in this process so far."""
+    return int(lib().tq_launch_count())
+
 
 def tq_row_bytes(head_dim: int, bits: int) -> int:
     n = lib().tq_row_bytes(int(head_dim), int(bits))
@@ -474,6 +502,134 @@ def tq_paged_decode_prod(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.
                                           _ptr(k_mse_centroids), _ptr(v_centroids), _ptr(qjl_matrix),
                                           float(scale or 0.0), _ptr(out), _DTYPES[out.dtype], _ptr(workspace),
                                           workspace.numel(), _ptr(status), _stream(dev)))
+    if check and status is not None:
+        raise_for_device_status(status)
+    return out
+
+
+# ---------------------------------------------------------------- recipe modes
+
+def _recipe_id(recipe) -> int:
+    if isinstance(recipe, str):
+        if recipe not in RECIPES:
+            raise ValueError(f"unknown recipe {recipe!r}")
+        return RECIPES[recipe]
+    return int(recipe)
+
+
+def tq_recipe_row_bytes(recipe, head_dim: int) -> int:
+    rb = int(lib().tq_recipe_row_bytes(_recipe_id(recipe), int(head_dim)))
+    if rb < 0:
+        raise ValueError(f"recipe {recipe!r} at head_dim {head_dim} is not supported")
+    return rb
+
+
+def tq_recipe_channel_order(recipe, head_dim: int, high) -> torch.Tensor:
+    """Checks the metadata's high groups [H, head_dim / 2] and returns the channel order
+    int32 [H, head_dim] (high group, then the rest ascending) on the host."""
+    high = torch.as_tensor(high).to(torch.int32).contiguous().cpu()
+    if high.dim() != 2 or high.shape[1] * 2 != int(head_dim):
+        raise ValueError(f"tq_recipe_channel_order: high groups must be [H, {int(head_dim) // 2}], got "
+                         f"{tuple(high.shape)}")
+    order = torch.empty(high.shape[0], int(head_dim), dtype=torch.int32)
+    _check(lib().tq_recipe_channel_order(_recipe_id(recipe), int(head_dim), high.shape[0], high.data_ptr(),
+                                         order.data_ptr()))
+    return order
+
+
+def tq_recipe_calibrate(recipe, samples) -> torch.Tensor:
+    """High groups int32 [H, D / 2] from calibration rows samples[N, H, D] (host)."""
+    x = torch.as_tensor(samples).to(torch.float32).contiguous().cpu()
+    if x.dim() != 3:
+        raise ValueError("tq_recipe_calibrate: samples must be [N, H, D]")
+    n, h, d = x.shape
+    high = torch.empty(h, d // 2, dtype=torch.int32)
+    _check(lib().tq_recipe_calibrate(_recipe_id(recipe), d, h, x.data_ptr(), n, high.data_ptr()))
+    return high
+
+
+class RecipeCodec:
+    """The shared group codec of a recipe at one head_dim, on a device: the signs of R_d
+    (seed 42), the MSE codebooks of both groups and S_d (seed 43), d = head_dim / 2."""
+
+    def __init__(self, recipe, head_dim: int, device=None):
+        rid = _recipe_id(recipe)
+        bits = {TQ_RECIPE_TURBOQUANT25: (3, 2), TQ_RECIPE_TURBOQUANT35: (4, 3)}.get(rid)
+        if bits is None:
+            raise ValueError(f"unknown recipe {recipe!r}")
+        self.recipe, self.head_dim, self.d, self.bits = rid, int(head_dim), int(head_dim) // 2, bits
+        self.row_bytes = tq_recipe_row_bytes(rid, head_dim)
+        self.signs = tq_build_rotation(self.d, RECIPE_ROTATION_SEED, device)
+        self.mse_high = tq_codebook(self.d, bits[0] - 1, device)[0]
+        self.mse_low = tq_codebook(self.d, bits[1] - 1, device)[0]
+        self.smat = tq_build_qjl_matrix(self.d, RECIPE_SKETCH_SEED, device)
+
+
+def _need_order(name: str, order: torch.Tensor, h: int, d: int, device) -> None:
+    if order.dtype != torch.int32 or tuple(order.shape) != (h, d) or not order.is_contiguous() or \
+            order.device != device:
+        raise ValueError(f"{name}: channel order must be contiguous int32 [{h}, {d}] on {device}")
+
+
+def tq_write_kv_recipe(raw: torch.Tensor, pages: torch.Tensor, slots: torch.Tensor, order: torch.Tensor,
+                       codec: RecipeCodec, status: torch.Tensor | None = None, check: bool = True) -> torch.Tensor:
+    """Encode raw[T, H, D] into recipe pages[NB, bs, H, RB] (tq_write_kv's slot rules)."""
+    dev = _need_cuda("tq_write_kv_recipe", raw, pages, slots, order, codec.signs, codec.smat)
+    if raw.dim() != 3 or pages.dim() != 4 or slots.dim() != 1 or slots.numel() != raw.shape[0]:
+        raise ValueError("tq_write_kv_recipe: raw [T, H, D], pages [NB, bs, H, RB], slots [T] expected")
+    if raw.dtype not in _DTYPES or pages.dtype != torch.uint8 or slots.dtype != torch.int64:
+        raise ValueError("tq_write_kv_recipe: raw f32/f16/bf16, pages uint8, slots int64 expected")
+    t, h, d = raw.shape
+    if d != codec.head_dim or pages.shape[2] != h or pages.shape[3] != codec.row_bytes:
+        raise ValueError("tq_write_kv_recipe: raw / pages do not match the codec's head_dim and row bytes")
+    _need_order("tq_write_kv_recipe", order, h, d, dev)
+    _need_status("tq_write_kv_recipe", status, dev)
+    if status is None:
+        status = _status_buffer(dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_write_kv_recipe(_ptr(raw), _DTYPES[raw.dtype], t, h, d, codec.recipe, _ptr(slots),
+                                        _ptr(pages), pages.shape[0], pages.shape[1], _ptr(order), _ptr(codec.signs),
+                                        _ptr(codec.mse_high), _ptr(codec.mse_low), _ptr(codec.smat), _ptr(status),
+                                        _stream(dev)))
+    if check:
+        raise_for_device_status(status)
+    return status
+
+
+def tq_paged_decode_recipe(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                           seq_lens: torch.Tensor, order: torch.Tensor, codec: RecipeCodec,
+                           scale: float | None = None, out: torch.Tensor | None = None,
+                           out_dtype: torch.dtype | None = None, workspace: torch.Tensor | None = None,
+                           status: torch.Tensor | None = None, check: bool = False) -> torch.Tensor:
+    """tq_paged_decode over recipe K and V pages."""
+    dev = _need_cuda("tq_paged_decode_recipe", q, k_pages, v_pages, block_table, seq_lens, order, codec.signs)
+    if q.dim() != 3 or k_pages.dim() != 4 or v_pages.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("tq_paged_decode_recipe: q [B, Hq, D], pages [NB, bs, H, RB], block_table [B, maxblk] "
+                         "expected")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32 or q.dtype not in _DTYPES:
+        raise ValueError("tq_paged_decode_recipe: block_table / seq_lens int32, q f32/f16/bf16 expected")
+    b, hq, d = q.shape
+    nb, bs, h, rb = k_pages.shape
+    if d != codec.head_dim or rb != codec.row_bytes or tuple(v_pages.shape) != tuple(k_pages.shape) or \
+            block_table.shape[0] != b or seq_lens.numel() != b:
+        raise ValueError("tq_paged_decode_recipe: page / table shapes inconsistent with q and the codec")
+    _need_order("tq_paged_decode_recipe", order, h, d, dev)
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=out_dtype, device=dev)
+    _need_out("tq_paged_decode_recipe", out, (b, hq, d), dev)
+    _need_status("tq_paged_decode_recipe", status, dev)
+    maxb = block_table.shape[1]
+    need = int(lib().tq_paged_decode_recipe_workspace(b, hq, h, d, maxb, bs))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_paged_decode_recipe(_ptr(q), _DTYPES[q.dtype], b, hq, h, d, _ptr(k_pages), _ptr(v_pages),
+                                            codec.recipe, nb, bs, _ptr(block_table), maxb, _ptr(seq_lens),
+                                            _ptr(order), _ptr(codec.signs), _ptr(codec.mse_high),
+                                            _ptr(codec.mse_low), _ptr(codec.smat), float(scale or 0.0), _ptr(out),
+                                            _DTYPES[out.dtype], _ptr(workspace), workspace.numel(), _ptr(status),
+                                            _stream(dev)))
     if check and status is not None:
         raise_for_device_status(status)
     return out

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -20,6 +21,7 @@
 #include "tq.h"
 #include "tq_internal.h"
 #include "tq_qjl.h"
+#include "tq_recipe.h"
 
 namespace {
 
@@ -311,11 +313,57 @@ tq_status decode_impl(const char* name, const void* q, tq_dtype q_dtype, int bat
 }
 
 
+// Tries of a bounded device wait for the next launches; < 0 means the default.
+std::atomic<int64_t> g_wait_limit{-1};
+
+// A write called with status_dev == NULL: runs `launch` with the library's own status word
+// (one per device, shared, so these calls are serialised), waits for the stream and
+// returns the code the kernels left there.
+std::mutex g_sync_write_mutex;
+
+template <typename Launch>
+tq_status write_with_own_status(const char* name, cudaStream_t stream, Launch launch) {
+  std::lock_guard<std::mutex> lock(g_sync_write_mutex);
+  int32_t* st = nullptr;
+  tq_status r = check_cuda(tq::internal_write_status(&st), name);
+  if (r != TQ_OK) return r;
+  r = check_cuda(launch(st), name);
+  if (r != TQ_OK) return r;
+  int32_t code = 0;
+  r = check_cuda(cudaMemcpyAsync(&code, st, sizeof(code), cudaMemcpyDeviceToHost, stream), name);
+  if (r != TQ_OK) return r;
+  r = check_cuda(cudaStreamSynchronize(stream), name);
+  if (r != TQ_OK) return r;
+  if (code == TQ_ERR_SLOT_OUT_OF_RANGE)
+    return fail(TQ_ERR_SLOT_OUT_OF_RANGE, "%s: a slot is >= num_blocks * block_size; no row was written", name);
+  if (code != TQ_OK) return fail((tq_status)code, "%s: device status %d", name, (int)code);
+  return ok();
+}
+
 }  // namespace
+
+namespace tq {
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+uint32_t wait_tries() {
+  const int64_t v = g_wait_limit.load(std::memory_order_relaxed);
+  if (v < 0) return kDefaultWaitTries;
+  return v > (int64_t)kDefaultWaitTries ? kDefaultWaitTries : (uint32_t)v;
+}
+}  // namespace tq
 
 extern "C" {
 
 const char* tq_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t tq_launch_count(void) { return tq::g_launches.load(std::memory_order_relaxed); }
+
+int64_t tq_set_wait_limit(int64_t tries) {
+  const int64_t prev = g_wait_limit.exchange(tries < 0 ? -1 : tries);
+  return prev < 0 ? (int64_t)tq::kDefaultWaitTries : prev;
+}
 
 int64_t tq_row_bytes(int head_dim, int bits) {
   if (!pow2_dim_ok(head_dim) || !bits_ok(bits)) return -1;
@@ -340,7 +388,8 @@ tq_status tq_build_rotation(int head_dim, uint64_t seed, float* signs_host) {
 tq_status tq_codebook(int head_dim, int bits, float* centroids_host, float* boundaries_host) {
   if (!centroids_host) return fail(TQ_ERR_INVALID_ARG, "tq_codebook: centroids_host is NULL");
   if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
-  if (!bits_ok(bits)) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 2, 3, 4 or 5", bits);
+  // 1 bit: the MSE part of the 2-bit groups of the recipe rows
+  if (bits < 1 || bits > 5) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 1 .. 5", bits);
   const std::vector<float>& c = codebook_f32(head_dim, bits);
   std::memcpy(centroids_host, c.data(), c.size() * sizeof(float));
   if (boundaries_host)
@@ -359,7 +408,6 @@ tq_status tq_write_kv(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, i
   if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
   if (!bits_ok(bits)) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 2, 3, 4 or 5", bits);
   if (!dtype_ok(raw_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: unknown raw dtype %d", (int)raw_dtype);
-  if (!status_dev) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: status_dev is required");
   if (num_tokens > 0 && (!raw || !slots || !pages || !signs || !centroids))
     return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: null pointer argument");
   if (num_tokens > 0 && (!aligned(raw, 16) || !aligned(pages, 16) || !aligned(slots, 8) || !aligned(signs, 4) ||
@@ -367,7 +415,13 @@ tq_status tq_write_kv(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, i
     return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: raw and pages must be 16-byte aligned, slots 8-byte aligned");
   tq::WriteArgs a{raw, (int)raw_dtype, num_tokens, num_kv_heads, head_dim, bits, slots, pages,
                   num_blocks, block_size, signs, centroids, status_dev};
-  return check_cuda(tq::launch_write(a, static_cast<cudaStream_t>(stream)), "tq_write_kv launch");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!status_dev)
+    return write_with_own_status("tq_write_kv", s, [&](int32_t* st) {
+      a.status = st;
+      return tq::launch_write(a, s);
+    });
+  return check_cuda(tq::launch_write(a, s), "tq_write_kv launch");
 }
 
 tq_status tq_dequant_rows(const uint8_t* pages, int bits, int64_t num_blocks, int block_size, int num_kv_heads,
@@ -517,7 +571,6 @@ tq_status tq_write_kv_prod(const void* raw, tq_dtype raw_dtype, int64_t num_toke
     return fail(TQ_ERR_UNSUPPORTED, "tq_write_kv_prod: head_dim %d / bits %d: needs head_dim 64 or 128 and bits 3..5",
                 head_dim, bits);
   if (!dtype_ok(raw_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: unknown raw dtype %d", (int)raw_dtype);
-  if (!status_dev) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: status_dev is required");
   if (num_tokens > 0 && (!raw || !slots || !pages || !signs || !mse_centroids || !qjl_matrix))
     return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: null pointer argument");
   if (num_tokens > 0 && (!aligned(raw, 16) || !aligned(pages, 16) || !aligned(slots, 8) || !aligned(signs, 4) ||
@@ -525,8 +578,13 @@ tq_status tq_write_kv_prod(const void* raw, tq_dtype raw_dtype, int64_t num_toke
     return fail(TQ_ERR_INVALID_ARG, "tq_write_kv_prod: raw and pages must be 16-byte aligned, slots 8-byte aligned");
   tq::WriteArgs a{raw, (int)raw_dtype, num_tokens, num_kv_heads, head_dim, bits, slots, pages,
                   num_blocks, block_size, signs, mse_centroids, status_dev};
-  return check_cuda(tq::launch_write_prod(a, qjl_matrix, static_cast<cudaStream_t>(stream), current_device_sms()),
-                    "tq_write_kv_prod launch");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!status_dev)
+    return write_with_own_status("tq_write_kv_prod", s, [&](int32_t* st) {
+      a.status = st;
+      return tq::launch_write_prod(a, qjl_matrix, s, current_device_sms());
+    });
+  return check_cuda(tq::launch_write_prod(a, qjl_matrix, s, current_device_sms()), "tq_write_kv_prod launch");
 }
 
 size_t tq_paged_decode_prod_workspace(int batch, int num_q_heads, int num_kv_heads, int head_dim,
@@ -585,6 +643,201 @@ tq_status tq_paged_decode_prod(const void* q, tq_dtype q_dtype, int batch, int n
   a.status = status_dev;
   a.v_alpha = a.k_alpha = 1.0f;
   return check_cuda(tq::launch_decode_prod(a, qjl_matrix, plan, static_cast<cudaStream_t>(stream)), name);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- recipe modes
+
+namespace {
+
+// (high-group bits, low-group bits) of a recipe; false for an unknown one.
+bool recipe_bits(int recipe, int* hi, int* lo) {
+  if (recipe == TQ_RECIPE_TURBOQUANT25) {
+    *hi = 3;
+    *lo = 2;
+    return true;
+  }
+  if (recipe == TQ_RECIPE_TURBOQUANT35) {
+    *hi = 4;
+    *lo = 3;
+    return true;
+  }
+  return false;
+}
+
+tq_status recipe_codec_check(const char* name, int recipe, int head_dim, tq::RecipeArgs* rc) {
+  int hi = 0, lo = 0;
+  if (!recipe_bits(recipe, &hi, &lo)) return fail(TQ_ERR_INVALID_ARG, "%s: unknown recipe %d", name, recipe);
+  if (!tq::recipe_supported(head_dim))
+    return fail(TQ_ERR_UNSUPPORTED, "%s: head_dim %d: the recipe kernels take 64 or 128", name, head_dim);
+  rc->bits_hi = hi;
+  rc->bits_lo = lo;
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t tq_recipe_row_bytes(int recipe, int head_dim) {
+  int hi = 0, lo = 0;
+  if (!recipe_bits(recipe, &hi, &lo) || !tq::recipe_supported(head_dim)) return -1;
+  return tq::recipe_row_bytes(head_dim, hi, lo);
+}
+
+tq_status tq_recipe_channel_order(int recipe, int head_dim, int num_kv_heads, const int32_t* high_host,
+                                  int32_t* order_host) {
+  int hi = 0, lo = 0;
+  if (!recipe_bits(recipe, &hi, &lo)) return fail(TQ_ERR_INVALID_ARG, "tq_recipe_channel_order: unknown recipe %d", recipe);
+  if (head_dim < 4 || head_dim % 2 || head_dim > 4096)
+    return fail(TQ_ERR_INVALID_ARG, "tq_recipe_channel_order: head_dim %d cannot be split in two groups", head_dim);
+  if (num_kv_heads < 1 || !high_host || !order_host)
+    return fail(TQ_ERR_INVALID_ARG, "tq_recipe_channel_order: num_kv_heads < 1 or a NULL array");
+  const int n = head_dim / 2;
+  std::vector<char> used(head_dim);
+  for (int h = 0; h < num_kv_heads; ++h) {
+    const int32_t* row = high_host + (int64_t)h * n;
+    std::fill(used.begin(), used.end(), 0);
+    for (int k = 0; k < n; ++k) {
+      if (row[k] < 0 || row[k] >= head_dim)
+        return fail(TQ_ERR_INVALID_ARG, "tq_recipe_channel_order: kv head %d: high-group index %d outside [0, %d)", h,
+                    (int)row[k], head_dim);
+      if (k > 0 && row[k] <= row[k - 1])
+        return fail(TQ_ERR_INVALID_ARG, "tq_recipe_channel_order: kv head %d: high-group indices must be sorted and unique",
+                    h);
+      used[row[k]] = 1;
+    }
+    int32_t* out = order_host + (int64_t)h * head_dim;
+    std::copy(row, row + n, out);
+    int w = n;
+    for (int c = 0; c < head_dim; ++c)
+      if (!used[c]) out[w++] = c;
+  }
+  return ok();
+}
+
+tq_status tq_recipe_calibrate(int recipe, int head_dim, int num_kv_heads, const float* samples_host,
+                              int64_t num_samples, int32_t* high_host) {
+  int hi = 0, lo = 0;
+  if (!recipe_bits(recipe, &hi, &lo)) return fail(TQ_ERR_INVALID_ARG, "tq_recipe_calibrate: unknown recipe %d", recipe);
+  if (head_dim < 4 || head_dim % 2 || head_dim > 4096 || num_kv_heads < 1 || num_samples < 0 || !high_host ||
+      (num_samples > 0 && !samples_host))
+    return fail(TQ_ERR_INVALID_ARG, "tq_recipe_calibrate: invalid sizes or a NULL array");
+  const int n = head_dim / 2;
+  std::vector<double> energy((size_t)num_kv_heads * head_dim, 0.0);
+  for (int64_t t = 0; t < num_samples; ++t)
+    for (int h = 0; h < num_kv_heads; ++h)
+      for (int c = 0; c < head_dim; ++c) {
+        const double x = samples_host[(t * num_kv_heads + h) * head_dim + c];
+        energy[(size_t)h * head_dim + c] += x * x;
+      }
+  std::vector<int> chans(head_dim);
+  for (int h = 0; h < num_kv_heads; ++h) {
+    const double* e = energy.data() + (size_t)h * head_dim;
+    for (int c = 0; c < head_dim; ++c) chans[c] = c;
+    // largest energy first, ties to the lower channel
+    std::stable_sort(chans.begin(), chans.end(), [e](int a, int b) { return e[a] > e[b]; });
+    std::sort(chans.begin(), chans.begin() + n);
+    std::copy(chans.begin(), chans.begin() + n, high_host + (int64_t)h * n);
+  }
+  return ok();
+}
+
+tq_status tq_write_kv_recipe(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, int num_kv_heads, int head_dim,
+                             int recipe, const int64_t* slots, uint8_t* pages, int64_t num_blocks, int block_size,
+                             const int32_t* channel_order, const float* group_signs, const float* mse_high,
+                             const float* mse_low, const float* qjl_matrix, int32_t* status_dev, void* stream) {
+  const char* name = "tq_write_kv_recipe";
+  if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 0 || block_size < 1)
+    return fail(TQ_ERR_INVALID_ARG, "%s: invalid sizes (tokens=%lld, kv_heads=%d, blocks=%lld, block_size=%d)", name,
+                (long long)num_tokens, num_kv_heads, (long long)num_blocks, block_size);
+  tq::RecipeArgs rc{};
+  tq_status st = recipe_codec_check(name, recipe, head_dim, &rc);
+  if (st != TQ_OK) return st;
+  if (!dtype_ok(raw_dtype)) return fail(TQ_ERR_INVALID_ARG, "%s: unknown raw dtype %d", name, (int)raw_dtype);
+  if (num_tokens > 0 && (!raw || !slots || !pages || !channel_order || !group_signs || !mse_high || !mse_low ||
+                         !qjl_matrix))
+    return fail(TQ_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  if (num_tokens > 0 && (!aligned(raw, dtype_size(raw_dtype)) || !aligned(pages, 16) || !aligned(slots, 8) ||
+                         !aligned(channel_order, 4) || !aligned(group_signs, 4) || !aligned(mse_high, 4) ||
+                         !aligned(mse_low, 4) || !aligned(qjl_matrix, 4) || !aligned(status_dev, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: misaligned pointer (pages need 16 bytes, slots 8)", name);
+  rc.order = channel_order;
+  rc.mse_hi = mse_high;
+  rc.mse_lo = mse_low;
+  rc.smat = qjl_matrix;
+  tq::WriteArgs a{raw, (int)raw_dtype, num_tokens, num_kv_heads, head_dim, 0, slots, pages,
+                  num_blocks, block_size, group_signs, nullptr, status_dev};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!status_dev)
+    return write_with_own_status(name, s, [&](int32_t* w) {
+      a.status = w;
+      return tq::launch_write_recipe(a, rc, s, current_device_sms());
+    });
+  return check_cuda(tq::launch_write_recipe(a, rc, s, current_device_sms()), name);
+}
+
+size_t tq_paged_decode_recipe_workspace(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int max_blocks_per_seq, int block_size) {
+  if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 0 || block_size < 1 ||
+      num_q_heads % num_kv_heads || !tq::recipe_supported(head_dim))
+    return 0;
+  const int g = num_q_heads / num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return 0;
+  tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  a.k_bits = a.v_bits = 0;  // the SIMT split plan
+  return tq::recipe_decode_workspace(a, tq::plan_decode(a, current_device_sms()));
+}
+
+tq_status tq_paged_decode_recipe(const void* q, tq_dtype q_dtype, int batch, int num_q_heads, int num_kv_heads,
+                                 int head_dim, const uint8_t* k_pages, const uint8_t* v_pages, int recipe,
+                                 int64_t num_blocks, int block_size, const int32_t* block_table, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, const int32_t* channel_order, const float* group_signs,
+                                 const float* mse_high, const float* mse_low, const float* qjl_matrix, float scale,
+                                 void* out, tq_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                 int32_t* status_dev, void* stream) {
+  const char* name = "tq_paged_decode_recipe";
+  tq::RecipeArgs rc{};
+  tq_status st = recipe_codec_check(name, recipe, head_dim, &rc);
+  if (st != TQ_OK) return st;
+  st = decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  if (st != TQ_OK) return st;
+  if (!dtype_ok(q_dtype) || !dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "%s: unknown dtype", name);
+  if (num_blocks < 0) return fail(TQ_ERR_INVALID_ARG, "%s: num_blocks < 0", name);
+  if (batch > 0 && (!q || !k_pages || !v_pages || !seq_lens || !channel_order || !group_signs || !mse_high ||
+                    !mse_low || !qjl_matrix || !out || (max_blocks_per_seq > 0 && !block_table)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  if (batch > 0 && (!aligned(q, dtype_size(q_dtype)) || !aligned(out, dtype_size(out_dtype)) ||
+                    !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(block_table, 4) ||
+                    !aligned(seq_lens, 4) || !aligned(channel_order, 4) || !aligned(qjl_matrix, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: misaligned pointer (pages need 16-byte alignment)", name);
+  tq::DecodeArgs a = make_decode_args(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
+  const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());  // SIMT split plan (k_bits 0)
+  const size_t need = tq::recipe_decode_workspace(a, plan);
+  if (batch > 0 && (workspace_bytes < need || !workspace || !aligned(workspace, 16)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: workspace must be >= %zu bytes and 16-byte aligned (got %zu)", name, need,
+                workspace_bytes);
+  rc.order = channel_order;
+  rc.mse_hi = mse_high;
+  rc.mse_lo = mse_low;
+  rc.smat = qjl_matrix;
+  a.q = q;
+  a.q_dtype = (int)q_dtype;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.k_bits = a.v_bits = 0;
+  a.num_blocks = num_blocks;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.signs = group_signs;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = (int)out_dtype;
+  a.workspace = workspace;
+  a.status = status_dev;
+  a.v_alpha = a.k_alpha = 1.0f;
+  return check_cuda(tq::launch_decode_recipe(a, rc, plan, static_cast<cudaStream_t>(stream)), name);
 }
 
 }  // extern "C"

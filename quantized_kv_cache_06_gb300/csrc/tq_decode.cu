@@ -232,9 +232,12 @@ cudaError_t launch_split(const DecodeArgs& a, const DecodePlan& p, SplitView par
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  count_launches(1);
   const int rows = a.batch * a.num_q_heads;
   combine_kernel<E><<<(rows + 7) / 8, 256, 0, stream>>>(rows, p.num_splits, part, a.signs, a.out, a.out_dtype);
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
 }
 
 }  // namespace
@@ -287,7 +290,9 @@ cudaError_t launch_combine_splits(const float* acc, const float* ml, int rows, i
     case 256: combine_kernel<8><<<grid, 256, 0, stream>>>(rows, nsplit, part, signs, out, out_dtype); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {

@@ -30,11 +30,21 @@
 // O'[pair][2g + e] += sum_t Vhat[t][2 pair + e] * P'[g][t], so one table entry gives
 // both coordinates of a pair of one token.  V centroids are stored as fp16(alpha * c),
 // alpha chosen on the host so that alpha * c lands near fp16 grid points; 1/alpha is
-// applied when the partial is written.  P' = p * nu_v in fp16.
+// applied when the partial is written.
+//
+// Value frame.  The value weight p * nu_v has no bound (nu_v is the norm of an arbitrary
+// raw row), so it is not rounded to fp16 as it stands.  Each q head keeps a second,
+// lazily moved exponent mv next to the score max m: the value accumulator holds
+// sum_t 2^(s_t - mv) nu_v,t c[idx_v,t], and P' = p * 2^(m - mv) * nu_v.  mv is raised
+// whenever a tile's bound on P' would pass the fp16 range (then to the tile's largest
+// s_t + log2 nu_v,t), and never falls more than kFrameGap below m, so P' stays inside the
+// fp16 range for every finite norm and keeps fp16's relative precision for the terms
+// that matter.  The partial is converted back to the score frame (times 2^(mv - m)) when
+// it is written, so the combine pass is unchanged.
 //
 // Softmax: online, base 2 (log2 e folded into the query), per q head.  Rows of tokens
-// past the sequence end are masked; blocks with an out-of-range id are skipped and
-// reported through the status word.
+// past the sequence end are masked (score -inf, value norm 0: their bytes are stale);
+// blocks with an out-of-range id are skipped and reported through the status word.
 // The kernels are instantiated and launched by tq_decode_tc.cu.
 #pragma once
 #include <cuda_bf16.h>
@@ -65,8 +75,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // mbarrier and bulk-copy primitives (shared-window addresses).  Every wait is bounded:
-// after kWaitLimit unsuccessful tries the caller reports kTimeout and stops.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// after `tries` unsuccessful tries the caller reports kTimeout and stops.  The waits of the
+// pipeline take TcArgs::wait_tries (normally kDefaultWaitTries); the producer's final
+// drain of its own copies always takes kDefaultWaitTries, so no copy is in flight when
+// the CTA exits.
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
@@ -87,8 +99,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase of `bar` with parity `parity` to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t tries) {
+  for (uint32_t i = 0; i < tries; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -119,6 +131,13 @@ __device__ __forceinline__ uint32_t ld32(const unsigned char* p) { return *reint
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+// log2(x) with the hardware approximation (log2(0) = -inf); used only to place the
+// value frame, where an error of a few ulps moves nothing that matters.
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -187,6 +206,7 @@ struct TcArgs {
   int buf_hi;             // dynamic-smem offset of buffer n_lo
   int buf_bytes;          // bytes per block buffer
   int t_off;              // dynamic-smem offset of T (64 KB aligned shared address)
+  uint32_t wait_tries;    // tries of a pipeline wait before it reports kTimeout
   float* part_acc;        // [WPH*(C+B)][Hq][D]
   float* part_ml;         // [WPH*(C+B)][Hq][2]
   int* prefix;            // [B+1] block prefix sums (written by CTA 0)
@@ -198,16 +218,30 @@ constexpr int kOffBar = 0;                                  // full[kMaxStages],
 constexpr int kOffMeta = kOffBar + 2 * kMaxStages * 8;      // BlockMeta[kMaxStages][WPH <= 2]
 constexpr int kOffScan = kOffMeta + kMaxStages * 2 * 16;    // int[36]
 constexpr int kOffK2 = kOffScan + 36 * 4;                   // nibble K table, 16 x 8 bytes
-constexpr int kOffV2 = kOffK2 + 16 * 8;                     // nibble V table, 16 x 4 bytes
-constexpr int kOffL = kOffV2 + 16 * 4;                      // byte K lo table, 256 x 4 bytes
-constexpr int kMiscBytes = (kOffL + 256 * 4 + 127) / 128 * 128;
+constexpr int kOffV2 = kOffK2 + 16 * 8;                     // nibble V table (hi, lo), 16 x 8 bytes
+constexpr int kOffL = kOffV2 + 16 * 8;                      // byte K lo table, 256 x 4 bytes
+constexpr int kOffVL = kOffL + 256 * 4;                     // byte V lo table, 256 x 4 bytes
+constexpr int kMiscBytes = (kOffVL + 256 * 4 + 127) / 128 * 128;
 
 constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
+// Value frame (see the file comment): a tile whose largest nu_v * 2^(m - mv) passes
+// kValueBound raises the frame, so P' <= 2^kRescaleSlack * kValueBound = 2^15 (fp16 holds
+// 65504); the frame never lags the score max by more than kFrameGap log2 units (so
+// 2^(m - mv) <= 2^64 and p * 2^(m - mv) stays finite).
+constexpr float kValueBound = 512.0f;
+constexpr float kFrameGap = 64.0f;
 // Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored with the fp16-hi key part
 // only.  With the alpha scaling the hi part is within ~1e-4 relative of the fp32
 // centroid, so the score error of such a tile stays far below the output tolerance;
 // tiles above the bound (rows with very large norms) add the fp16-lo part.
 constexpr float kFastScoreBound = 48.0f;
+// Largest value norm of a tile whose values take the fp16 path (P' and the value table
+// each rounded once to fp16, ~2^-12 relative): there the output error stays far below
+// the 2e-3 + 2e-3 |o| tolerance.  Tiles with a larger norm add the fp16 remainders of
+// both (V_hi P'_hi + V_lo P'_hi + V_hi P'_lo, ~2^-22 relative), since a rounding error
+// proportional to a large norm can exceed the absolute part of the tolerance wherever
+// the output element itself is small.
+constexpr float kFastValueNorm = 32.0f;
 
 template <int D, int KB, int VB, int G, int WPH>
 __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
@@ -233,6 +267,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   unsigned char* lutL = smem + kOffL;
   unsigned char* lutK2 = smem + kOffK2;
   unsigned char* lutV2 = smem + kOffV2;
+  unsigned char* lutVL = smem + kOffVL;
   BlockMeta* meta = reinterpret_cast<BlockMeta*>(smem + kOffMeta);
   int* scan_tmp = reinterpret_cast<int*>(smem + kOffScan);
   auto bar_full = [&](int i) -> uint32_t { return smem_base + kOffBar + 8u * i; };
@@ -431,7 +466,11 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   };
   auto v_lookup = [&](uint32_t w, int e) -> uint32_t {
     if (VB == 4) return lds32_off128(t_addr(w, e));
-    return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 2));
+    return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 3));
+  };
+  auto v_lookup_lo = [&](uint32_t w, int e) -> uint32_t {  // fp16 remainders of the same pair
+    if (VB == 4) return ld32(lutVL + (((w >> (8 * e)) & 255u) << 2));
+    return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 3) + 4);
   };
 
   // Query B fragments.  G = 4: one set whose columns 0-3 hold the fp16 hi part of the
@@ -442,6 +481,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   float qnorm_max = 0.f;  // max over this warp's heads of ||rotated query|| (log2 units)
   float o_acc[Cfg::kNT][Cfg::kMTiles][4];
   float m_run[2], l_run[2], m_thr[2];  // running max, sum, and max + kRescaleSlack per head
+  float mv[2], fr[2];                  // value frame exponent and 2^(m_run - mv) per head
   int cur_b = -1;
 
   auto reset_state = [&]() {
@@ -453,6 +493,24 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         for (int e = 0; e < 4; ++e) o_acc[nt][i][e] = 0.f;
     m_run[0] = m_run[1] = m_thr[0] = m_thr[1] = -INFINITY;
     l_run[0] = l_run[1] = 0.f;
+    mv[0] = mv[1] = -INFINITY;
+    fr[0] = fr[1] = 0.f;
+  };
+  // Multiplies the value accumulators of each q head by its factor cv[e] (held by the
+  // score-layout lanes: lane (r, c) has heads 2c, 2c+1; the value layout has head c + 4 nt).
+  auto rescale_values = [&](const float (&cv)[2]) {
+#pragma unroll
+    for (int nt = 0; nt < Cfg::kNT; ++nt) {
+      const int g = c + 4 * nt;
+      const int srcl = (g >> 1) & 3;  // lane (r'=0, c'=g>>1)
+      const float c0 = __shfl_sync(kFullMask, cv[0], srcl);
+      const float c1 = __shfl_sync(kFullMask, cv[1], srcl);
+      const float cg = (g & 1) ? c1 : c0;
+#pragma unroll
+      for (int i = 0; i < Cfg::kMTiles; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o_acc[nt][i][e] *= cg;
+    }
   };
 
   // Rotated query of sequence b for this warp's G heads -> hi/lo B fragments.
@@ -530,10 +588,15 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   };
 
   const float inv_alpha = 1.0f / args.v_alpha;
-  // Writes this warp's partial for sequence b (empty when `empty`).
+  // Writes this warp's partial for sequence b (empty when `empty`).  The value
+  // accumulators go back from the value frame to the score frame: times 2^(mv - m).
   auto flush = [&](int b, bool empty) {
     const int64_t slot = (int64_t)cta + b;
     float lsum[2] = {l_run[0], l_run[1]};
+    float to_m[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      to_m[e] = (empty || m_run[e] == -INFINITY || mv[e] == -INFINITY) ? 0.f : fast_exp2(mv[e] - m_run[e]) * inv_alpha;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 4);
@@ -554,6 +617,10 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
     for (int nt = 0; nt < Cfg::kNT; ++nt) {  // value layout: q head c + 4 nt
       const int g = c + 4 * nt;
+      const int srcl = (g >> 1) & 3;
+      const float f0 = __shfl_sync(kFullMask, to_m[0], srcl);
+      const float f1 = __shfl_sync(kFullMask, to_m[1], srcl);
+      const float fg = (g & 1) ? f1 : f0;
       if (g < G) {
         float* acc = args.part_acc + (slot * a.num_q_heads + (int64_t)h * G + g) * D;
 #pragma unroll
@@ -563,8 +630,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
             const int q = 2 * i + half;
             const int pv = Cfg::kPWV * (r + 8 * (q / Cfg::kPWV)) + (q % Cfg::kPWV);
             float2 v;
-            v.x = empty ? 0.f : o_acc[nt][i][2 * half] * inv_alpha;
-            v.y = empty ? 0.f : o_acc[nt][i][2 * half + 1] * inv_alpha;
+            v.x = fg == 0.f ? 0.f : o_acc[nt][i][2 * half] * fg;
+            v.y = fg == 0.f ? 0.f : o_acc[nt][i][2 * half + 1] * fg;
             *reinterpret_cast<float2*>(acc + 2 * pv) = v;
           }
         }
@@ -688,8 +755,15 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       sc[t][3] = sacc[t][3] * kn[t][1];
     }
     if (ntok_last < kBS) {  // last block of a sequence: mask the rows past its end
-      if (r >= ntok_last) sc[NTL - 1][0] = sc[NTL - 1][1] = -INFINITY;
-      if (r + 8 >= ntok_last) sc[NTL - 1][2] = sc[NTL - 1][3] = -INFINITY;
+      // (their bytes are stale: the value norm may hold any bit pattern, NaN included)
+      if (r >= ntok_last) {
+        sc[NTL - 1][0] = sc[NTL - 1][1] = -INFINITY;
+        vn[NTL - 1][0] = 0.f;
+      }
+      if (r + 8 >= ntok_last) {
+        sc[NTL - 1][2] = sc[NTL - 1][3] = -INFINITY;
+        vn[NTL - 1][1] = 0.f;
+      }
     }
 
     // --- online softmax (q heads 2c, 2c+1 on this lane).  The running max only moves
@@ -703,7 +777,9 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       for (int t = 1; t < NTL; ++t) smax[e] = fmaxf(smax[e], fmaxf(sc[t][e], sc[t][2 + e]));
     }
     if (__any_sync(kFullMask, smax[0] > m_thr[0] || smax[1] > m_thr[1])) {
-      float corr[2];
+      // the sums follow the score max; the value frame moves only when it would lag the
+      // score max by more than kFrameGap (always at the first tile of a sequence)
+      float cv[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         float mt = smax[e];
@@ -711,70 +787,119 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
         const float mn = mt > m_thr[e] ? mt : m_run[e];
-        corr[e] = fast_exp2(m_run[e] - mn);
-        l_run[e] *= corr[e];
+        l_run[e] *= m_run[e] == mn ? 1.f : fast_exp2(m_run[e] - mn);
         m_run[e] = mn;
         m_thr[e] = mn + kRescaleSlack;
+        const float mvn = fmaxf(mv[e], mn - kFrameGap);
+        cv[e] = mvn == mv[e] ? 1.f : fast_exp2(mv[e] - mvn);
+        mv[e] = mvn;
+        fr[e] = mn == -INFINITY ? 0.f : fast_exp2(mn - mvn);
       }
-#pragma unroll
-      for (int nt = 0; nt < Cfg::kNT; ++nt) {  // value layout holds q head c + 4 nt
-        const int g = c + 4 * nt;
-        const int srcl = (g >> 1) & 3;  // lane (r'=0, c'=g>>1)
-        const float c0 = __shfl_sync(kFullMask, corr[0], srcl);
-        const float c1 = __shfl_sync(kFullMask, corr[1], srcl);
-        const float cg = (g & 1) ? c1 : c0;
-#pragma unroll
-        for (int i = 0; i < Cfg::kMTiles; ++i)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o_acc[nt][i][e] *= cg;
-      }
+      if (__any_sync(kFullMask, cv[0] != 1.f || cv[1] != 1.f)) rescale_values(cv);
     }
-    uint32_t p01[NTL], p23[NTL];
+    // Value frame check, before any weight is formed: p <= 2^kRescaleSlack, so every P' of
+    // this tile is at most 2^6 * 2^(m - mv) * max nu_v.  Where that bound passes kValueBound
+    // (the first tile of a sequence, rows of very large norm) the frame of each head is
+    // raised to the tile's largest s_t + log2 nu_v,t (then every P' here is at most ~1).
+    float vmax = 0.f;
+#pragma unroll
+    for (int t = 0; t < NTL; ++t) vmax = fmaxf(vmax, fmaxf(vn[t][0], vn[t][1]));
+    if (__any_sync(kFullMask, vmax * fr[0] > kValueBound || vmax * fr[1] > kValueBound)) {
+      float cv[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float sv = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < NTL; ++t)
+          sv = fmaxf(sv, fmaxf(sc[t][e] + fast_log2(vn[t][0]), sc[t][2 + e] + fast_log2(vn[t][1])));
+        sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 4));
+        sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 8));
+        sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 16));
+        const float mvn = fmaxf(mv[e], sv);
+        cv[e] = mvn == mv[e] ? 1.f : fast_exp2(mv[e] - mvn);
+        mv[e] = mvn;
+        fr[e] = (m_run[e] == -INFINITY || mvn == -INFINITY) ? 0.f : fast_exp2(m_run[e] - mvn);
+      }
+      if (__any_sync(kFullMask, cv[0] != 1.f || cv[1] != 1.f)) rescale_values(cv);
+    }
+    float pvf[NTL][4];  // P' = p 2^(m - mv) nu_v: [t][e] token r, [t][2 + e] token r + 8 (heads 2c, 2c+1)
 #pragma unroll
     for (int t = 0; t < NTL; ++t) {
-      float pv[4];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float p0 = fast_exp2(sc[t][e] - m_run[e]), p1 = fast_exp2(sc[t][2 + e] - m_run[e]);
         l_run[e] += p0 + p1;
-        pv[e] = p0 * vn[t][0];
-        pv[2 + e] = p1 * vn[t][1];
+        pvf[t][e] = (p0 * fr[e]) * vn[t][0];
+        pvf[t][2 + e] = (p1 * fr[e]) * vn[t][1];
       }
-      p01[t] = pack_half2(pv[0], pv[1]);  // token r:   heads 2c, 2c+1
-      p23[t] = pack_half2(pv[2], pv[3]);  // token r+8: heads 2c, 2c+1
     }
 
     // --- values ------------------------------------------------------------------------
+    // EXV: tiles with a value norm above kFastValueNorm add the fp16 remainders of the
+    // table entries and of P'.
+    auto values = [&](auto exv_tag) {
+      constexpr bool EXV = decltype(exv_tag)::value;
+      uint32_t p01[NTL], p23[NTL], q01[NTL], q23[NTL];
 #pragma unroll
-    for (int t = 0; t < NTL; ++t) {
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {  // tokens {c, c+4} (ks=0) and {c+8, c+12} (ks=1)
-        const int t0 = c + 8 * ks, t1 = c + 4 + 8 * ks;
-        uint32_t bv[Cfg::kNT][2];
-#pragma unroll
-        for (int nt = 0; nt < Cfg::kNT; ++nt) {
-          const int cs = 2 * nt + (r >> 2);  // source lane column: q head (4 nt + r/2) / 2
-          const uint32_t src = ks == 0 ? p01[t] : p23[t];
-          const uint32_t x0 = __shfl_sync(kFullMask, src, 4 * c + cs);
-          const uint32_t x1 = __shfl_sync(kFullMask, src, 4 * (c + 4) + cs);
-          bv[nt][0] = __byte_perm(x0, 0u, sel_b);
-          bv[nt][1] = __byte_perm(x1, 0u, sel_b);
+      for (int t = 0; t < NTL; ++t) {
+        p01[t] = pack_half2(pvf[t][0], pvf[t][1]);  // token r:   heads 2c, 2c+1
+        p23[t] = pack_half2(pvf[t][2], pvf[t][3]);  // token r+8: heads 2c, 2c+1
+        if (EXV) {
+          const __half2 h01 = *reinterpret_cast<const __half2*>(&p01[t]);
+          const __half2 h23 = *reinterpret_cast<const __half2*>(&p23[t]);
+          q01[t] = pack_half2(pvf[t][0] - __low2float(h01), pvf[t][1] - __high2float(h01));
+          q23[t] = pack_half2(pvf[t][2] - __low2float(h23), pvf[t][3] - __high2float(h23));
         }
+      }
 #pragma unroll
-        for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
-          const uint32_t wa = ld32(vbase[t] + t0 * vts + (r + 8 * jw) * 4);
-          const uint32_t wb = ld32(vbase[t] + t1 * vts + (r + 8 * jw) * 4);
+      for (int t = 0; t < NTL; ++t) {
 #pragma unroll
-          for (int e = 0; e < Cfg::kPWV; e += 2) {
-            const int i = (jw * Cfg::kPWV + e) >> 1;  // m-tile: pairs q = 2i (row r), 2i+1 (row r+8)
-            const uint32_t a0 = v_lookup(wa, e), a1 = v_lookup(wa, e + 1);
-            const uint32_t a2 = v_lookup(wb, e), a3 = v_lookup(wb, e + 1);
+        for (int ks = 0; ks < 2; ++ks) {  // tokens {c, c+4} (ks=0) and {c+8, c+12} (ks=1)
+          const int t0 = c + 8 * ks, t1 = c + 4 + 8 * ks;
+          uint32_t bv[Cfg::kNT][2], bl[Cfg::kNT][2];
 #pragma unroll
-            for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+          for (int nt = 0; nt < Cfg::kNT; ++nt) {
+            const int cs = 2 * nt + (r >> 2);  // source lane column: q head (4 nt + r/2) / 2
+            const uint32_t src = ks == 0 ? p01[t] : p23[t];
+            const uint32_t x0 = __shfl_sync(kFullMask, src, 4 * c + cs);
+            const uint32_t x1 = __shfl_sync(kFullMask, src, 4 * (c + 4) + cs);
+            bv[nt][0] = __byte_perm(x0, 0u, sel_b);
+            bv[nt][1] = __byte_perm(x1, 0u, sel_b);
+            if (EXV) {
+              const uint32_t srcl = ks == 0 ? q01[t] : q23[t];
+              const uint32_t y0 = __shfl_sync(kFullMask, srcl, 4 * c + cs);
+              const uint32_t y1 = __shfl_sync(kFullMask, srcl, 4 * (c + 4) + cs);
+              bl[nt][0] = __byte_perm(y0, 0u, sel_b);
+              bl[nt][1] = __byte_perm(y1, 0u, sel_b);
+            }
+          }
+#pragma unroll
+          for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
+            const uint32_t wa = ld32(vbase[t] + t0 * vts + (r + 8 * jw) * 4);
+            const uint32_t wb = ld32(vbase[t] + t1 * vts + (r + 8 * jw) * 4);
+#pragma unroll
+            for (int e = 0; e < Cfg::kPWV; e += 2) {
+              const int i = (jw * Cfg::kPWV + e) >> 1;  // m-tile: pairs q = 2i (row r), 2i+1 (row r+8)
+              const uint32_t a0 = v_lookup(wa, e), a1 = v_lookup(wa, e + 1);
+              const uint32_t a2 = v_lookup(wb, e), a3 = v_lookup(wb, e + 1);
+#pragma unroll
+              for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+              if (EXV) {
+                const uint32_t l0 = v_lookup_lo(wa, e), l1 = v_lookup_lo(wa, e + 1);
+                const uint32_t l2 = v_lookup_lo(wb, e), l3 = v_lookup_lo(wb, e + 1);
+#pragma unroll
+                for (int nt = 0; nt < Cfg::kNT; ++nt) {
+                  mma16816(o_acc[nt][i], l0, l1, l2, l3, bv[nt][0], bv[nt][1]);
+                  mma16816(o_acc[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                }
+              }
+            }
           }
         }
       }
-    }
+    };
+    if (__any_sync(kFullMask, vmax > kFastValueNorm)) values(std::true_type{});
+    else values(std::false_type{});
   };
   using One = std::integral_constant<int, 1>;
   using Two = std::integral_constant<int, 2>;
@@ -786,14 +911,15 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
     int S = 0;
     for (; S < nstages; ++S) {
       const int ps = S % nst;
-      if (S >= nst && !mbar_wait(bar_empty(ps), (uint32_t)(((S / nst) - 1) & 1))) break;
+      if (S >= nst && !mbar_wait(bar_empty(ps), (uint32_t)(((S / nst) - 1) & 1), args.wait_tries)) break;
       if (S == 0 && lane < WPH) meta_load();
       produce(ps);
     }
     if (S < nstages && lane == 0 && a.status) atomicMax(a.status, (int32_t)kTimeout);
     // let this CTA's copies land before the producer leaves (the consumers normally
     // have already waited for all of them)
-    for (int s2 = (S > nst ? S - nst : 0); s2 < S; ++s2) mbar_wait(bar_full(s2 % nst), (uint32_t)((s2 / nst) & 1));
+    for (int s2 = (S > nst ? S - nst : 0); s2 < S; ++s2)
+      mbar_wait(bar_full(s2 % nst), (uint32_t)((s2 / nst) & 1), kDefaultWaitTries);
     return;
   }
   {
@@ -824,18 +950,26 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       }
     }
     if (VB == 4) {
-      const float v_l = __ldg(a.v_centroids + (lane & 15)) * args.v_alpha;
+      __half v_hi_l, v_lo_l;
+      split_half(__ldg(a.v_centroids + (lane & 15)) * args.v_alpha, v_hi_l, v_lo_l);
+      const uint32_t v_pair_l = (uint32_t)__half_as_ushort(v_hi_l) | ((uint32_t)__half_as_ushort(v_lo_l) << 16);
       for (int i = tid; i < 256 * 32; i += 32 * ncons) {
         const int f = i >> 5, copy = i & 31;
-        const float ca = __shfl_sync(kFullMask, v_l, f & 15);
-        const float cb = __shfl_sync(kFullMask, v_l, f >> 4);
-        *reinterpret_cast<uint32_t*>(lutT + f * 256 + 128 + copy * 4) = pack_half2(ca, cb);
+        const uint32_t pa = __shfl_sync(kFullMask, v_pair_l, f & 15);  // (hi, lo) of c[f & 15]
+        const uint32_t pb = __shfl_sync(kFullMask, v_pair_l, f >> 4);
+        *reinterpret_cast<uint32_t*>(lutT + f * 256 + 128 + copy * 4) = __byte_perm(pa, pb, 0x5410);
+        if (copy == 0) *reinterpret_cast<uint32_t*>(lutVL + f * 4) = __byte_perm(pa, pb, 0x7632);
       }
     } else {
       for (int f = tid; f < 16; f += 32 * ncons) {
-        const float ca = __ldg(a.v_centroids + (f & 3)) * args.v_alpha;
-        const float cb = __ldg(a.v_centroids + (f >> 2)) * args.v_alpha;
-        *reinterpret_cast<uint32_t*>(lutV2 + f * 4) = pack_half2(ca, cb);
+        __half ha, la, hb, lb;
+        split_half(__ldg(a.v_centroids + (f & 3)) * args.v_alpha, ha, la);
+        split_half(__ldg(a.v_centroids + (f >> 2)) * args.v_alpha, hb, lb);
+        __half2 hi2 = __halves2half2(ha, hb), lo2 = __halves2half2(la, lb);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t*>(&hi2);
+        v.y = *reinterpret_cast<uint32_t*>(&lo2);
+        *reinterpret_cast<uint2*>(lutV2 + f * 8) = v;
       }
     }
   asm volatile("bar.sync 1, %0;\n" ::"r"(32 * ncons) : "memory");  // consumer warps only
@@ -847,7 +981,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   int slot = 0;
   uint32_t par = 0;
   for (int st = 0; st < nstages; ++st) {
-    if (!mbar_wait(bar_full(slot), par)) {
+    if (!mbar_wait(bar_full(slot), par, args.wait_tries)) {
       if (lane == 0 && a.status) atomicMax(a.status, (int32_t)kTimeout);
       return;
     }
@@ -977,6 +1111,7 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   t.v_slab_smem = (kBS * t.v_tok_stride + 15) / 16 * 16;
   t.v_alpha = a.v_alpha > 0.f ? a.v_alpha : 1.0f;
   t.k_alpha = a.k_alpha > 0.f ? a.k_alpha : 1.0f;
+  t.wait_tries = wait_tries();
 
   // Shared-memory layout: [misc | buffers ... | T (64 KB, at a 64 KB aligned shared
   // address) | buffers ...].  Dynamic shared memory starts right after the per-block
@@ -1024,6 +1159,7 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   kern<<<p.num_splits, 32 * (H + 1), smem, stream>>>(t);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  count_launches(1);
   const int rows = B * Hq;
   // programmatic dependent launch: the combine's launch overlaps the split kernel's tail
   cudaLaunchConfig_t cfg{};
@@ -1036,8 +1172,10 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_tc_kernel<D / 32>, a, p.num_splits, (const float*)t.part_acc,
-                            (const float*)t.part_ml, (const int*)t.prefix);
+  err = cudaLaunchKernelEx(&cfg, combine_tc_kernel<D / 32>, a, p.num_splits, (const float*)t.part_acc,
+                           (const float*)t.part_ml, (const int*)t.prefix);
+  if (err == cudaSuccess) count_launches(1);
+  return err;
 }
 
 

@@ -168,7 +168,9 @@ cudaError_t launch_bits(const DequantArgs& a, cudaStream_t stream, int grid) {
     case 5: dequant_rows_kernel<T, D, 5><<<grid, 256, 0, stream>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
 }
 
 template <typename T>

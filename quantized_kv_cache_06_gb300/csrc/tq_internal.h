@@ -19,6 +19,16 @@ enum : int32_t {
 
 enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
+// Tries of one bounded mbarrier wait before it gives up and reports kTimeout (seconds at
+// most with the hardware's own suspend time per try), and the number the next launches
+// use: the default unless a failure-path test set another with tq_set_wait_limit.
+constexpr uint32_t kDefaultWaitTries = 1u << 22;
+uint32_t wait_tries();
+
+// Process-wide count of kernel launches the library has enqueued (tq_launch_count): every
+// launch site adds its launches once the launch call has returned without error.
+void count_launches(int n);
+
 struct WriteArgs {
   const void* raw;
   int dtype;
@@ -37,6 +47,10 @@ struct WriteArgs {
 
 // Enqueues: status <- 0, slot validation, row write.  Returns the first launch error.
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream);
+
+// Device address (current device) of the library's own status word, used by the writes
+// called without one (tq_write.cu).
+cudaError_t internal_write_status(int32_t** ptr);
 
 // Tensor-core writer (tq_write_tc.cu): fp16 / bf16 rows, head_dim 64, 128 or 256, 2 to 5 bits.
 bool write_tc_supported(const WriteArgs& a);

@@ -11,8 +11,12 @@
 // against up to 64 (query row, q head) pairs with tensor-core MMAs:
 //   S  = qrot Khat^T          m16n8k16, A = rotated queries, B = key tile (ldmatrix)
 //   causal mask per row (token < q_len), online softmax in base 2
-//   O += P' Vhat               A = P' = p * nu_v (from the S accumulators), B = value tile
-//                              (ldmatrix.trans)
+//   O += P' Vhat               A = P' = p 2^(m - mv) nu_v (from the S accumulators), B =
+//                              value tile (ldmatrix.trans); mv is a per-row value frame that
+//                              keeps P' inside the fp16 range for any value norm (it is
+//                              raised when a tile's bound on P' would pass the fp16 range,
+//                              and O is turned back to the score frame when the partial
+//                              is written)
 // Khat holds fp16(alpha_k c[idx]) (+ the fp16 remainder for tiles that need the exact
 // score), Vhat fp16(alpha_v c[idx]); the key norm multiplies the score and the value norm
 // the weight, so nothing of the cache is expanded to a dense row in HBM.  The rotated
@@ -55,6 +59,16 @@ constexpr float kMqLog2e = 1.4426950408889634f;
 // remainder of the key centroids (same bound as the tensor-core decode).
 constexpr float kMqFastBound = 48.0f;
 constexpr float kMqSlack = 6.0f;  // log2 units the running max may lag behind the scores
+// Value frame (as in the tensor-core decode): the value weights P' = p 2^(m - mv) nu_v stay
+// below 2^kMqSlack * kMqValueBound = 2^15 by raising mv, and mv never lags m by more than
+// kMqFrameGap.
+constexpr float kMqValueBound = 512.0f;
+constexpr float kMqFrameGap = 64.0f;
+// Largest value norm of a tile whose values take the fp16 path (P' and the value tile each
+// rounded once to fp16); tiles above it add both fp16 remainders (same rule as the
+// tensor-core decode: an error proportional to a large norm can pass the absolute part of
+// the 2e-3 + 2e-3 |o| tolerance where the output element is small).
+constexpr float kMqFastValueNorm = 32.0f;
 
 constexpr int kMqStages = 4;  // raw-word ring: tiles it .. it + 2 in flight while tile it is used
 
@@ -142,6 +156,11 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
 __device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation (ex2(-inf) = 0)
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {  // log2(x), hardware approximation (lg2(0) = -inf)
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -319,16 +338,21 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
     for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float m_thr[2] = {-INFINITY, -INFINITY};  // m_run + kMqSlack
+  // value frame: o holds sum_t 2^(s_t - mv) nu_v,t c[idx_v,t]; fr = 2^(m_run - mv)
+  float mv[2] = {-INFINITY, -INFINITY}, fr[2] = {0.f, 0.f};
 
   // dequantisation centroids: lane l holds entry l mod 2^b (a shuffle reads only the low
   // 5 bits of its source lane, so a field needs no mask)
-  uint32_t kc_pair, vc_half;
+  uint32_t kc_pair, vc_pair;  // (fp16 hi, fp16 lo) of alpha c
   {
     const float ck = __ldg(a.k_centroids + (lane & ((1 << KB) - 1))) * a.k_alpha;
     const __half hk = __float2half_rn(ck);
     const __half lk = __float2half_rn(ck - __half2float(hk));
     kc_pair = (uint32_t)__half_as_ushort(hk) | ((uint32_t)__half_as_ushort(lk) << 16);
-    vc_half = (uint32_t)__half_as_ushort(__float2half_rn(__ldg(a.v_centroids + (lane & ((1 << VB) - 1))) * a.v_alpha));
+    const float cv = __ldg(a.v_centroids + (lane & ((1 << VB) - 1))) * a.v_alpha;
+    const __half hv = __float2half_rn(cv);
+    const __half lv = __float2half_rn(cv - __half2float(hv));
+    vc_pair = (uint32_t)__half_as_ushort(hv) | ((uint32_t)__half_as_ushort(lv) << 16);
   }
 
   // task j of this thread: component (0 K, 1 V), token t of the tile, part (32
@@ -437,13 +461,21 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
             raw[j].nrm = (raw[j].ok && task_part(j) == 0) ? lds_u32(ring(st, j * S::kTaskWords + S::kMaxBits)) : 0u;
           }
         }
-        // ---- A: exact-score vote; every warp is done with the previous tile ----------
-        int flag = 0;
+        // ---- A: exact-score and exact-value votes; every warp is done with the previous
+        // tile.  One barrier votes on both; only a tile that needs either (rare) takes two
+        // more to tell them apart.
+        int kflag = 0, vflag = 0;
 #pragma unroll
-        for (int j = 0; j < TPT; ++j)
-          if (task_comp(j) == 0 && task_part(j) == 0 && raw[j].ok)
-            flag |= fabsf(__uint_as_float(raw[j].nrm)) * qn_cta > kMqFastBound;
-        const bool exact = __syncthreads_or(flag) != 0;
+        for (int j = 0; j < TPT; ++j) {
+          if (task_part(j) != 0 || !raw[j].ok) continue;
+          if (task_comp(j) == 0) kflag |= fabsf(__uint_as_float(raw[j].nrm)) * qn_cta > kMqFastBound;
+          else vflag |= fabsf(__uint_as_float(raw[j].nrm)) > kMqFastValueNorm;
+        }
+        bool exact = false, exact_v = false;
+        if (__syncthreads_or(kflag | vflag)) {
+          exact = __syncthreads_or(kflag) != 0;
+          exact_v = __syncthreads_or(vflag) != 0;
+        }
 
         // ---- dequantise the tile into shared memory --------------------------------
 #pragma unroll
@@ -486,7 +518,7 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
                   const int bit = i * VB, k = bit >> 5, sh = bit & 31;
                   uint32_t f = raw[j].w[k] >> sh;
                   if (sh + VB > 32) f |= raw[j].w[k + 1] << (32 - sh);
-                  val[u] = __shfl_sync(kFullMask, vc_half, (int)f);
+                  val[u] = __shfl_sync(kFullMask, vc_pair, (int)f);
                 }
                 vp[pr] = __byte_perm(val[0], val[1], 0x5410);
               }
@@ -501,8 +533,48 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
         for (int j = 0; j < TPT; ++j) bid_pref[j] = load_bid(it + kMqStages, j);
         __syncthreads();  // B: the tile is in shared memory
 
-        // ---- math: skipped by a warp whose rows all end before the tile -------------
-        if (!__any_sync(kFullMask, T0 < lenA || T0 < lenB)) continue;  // (its copies are issued)
+        // ---- math: skipped by a warp whose rows all end before the tile (such a warp
+        // still takes part in an exact-value tile's barriers and remainder tile) ---------
+        const bool live = __any_sync(kFullMask, T0 < lenA || T0 < lenB);
+        if (!live && !exact_v) continue;  // (its copies are issued)
+        // Exact-value tiles: once every warp's scores are done (barrier C), the key tile
+        // is free; the fp16 remainders of the value tile go there (re-read from this
+        // thread's ring words of the tile), visible after barrier D.
+        auto value_remainders = [&]() {
+          __syncthreads();  // C
+          const int st = it % kMqStages;
+#pragma unroll
+          for (int j = 0; j < TPT; ++j) {
+            if (task_comp(j) != 1) continue;
+            const bool ok = lds_u32(ring(st, j * S::kTaskWords + S::kMaxBits + 1)) != 0u;
+            uint32_t w[MAXB];
+#pragma unroll
+            for (int k = 0; k < MAXB; ++k) w[k] = ok ? lds_u32(ring(st, j * S::kTaskWords + k)) : 0u;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t vp[4];
+#pragma unroll
+              for (int pr = 0; pr < 4; ++pr) {
+                uint32_t val[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int i = q4 * 8 + pr * 2 + u;
+                  const int bit = i * VB, k = bit >> 5, sh = bit & 31;
+                  uint32_t f = w[k] >> sh;
+                  if (sh + VB > 32) f |= w[k + 1] << (32 - sh);
+                  val[u] = __shfl_sync(kFullMask, vc_pair, (int)f);
+                }
+                vp[pr] = __byte_perm(val[0], val[1], 0x7632);
+              }
+              sts_v4(khi_base + (sts_off[j] ^ (uint32_t)(q4 << 4)), vp[0], vp[1], vp[2], vp[3]);
+            }
+          }
+          __syncthreads();  // D
+        };
+        if (!live) {
+          value_remainders();
+          continue;
+        }
         float s[4][4];
 #pragma unroll
         for (int jn = 0; jn < 4; ++jn)
@@ -551,6 +623,8 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
           }
         }
 
+        if (exact_v) value_remainders();
+
         // scores: x nu_k, invalid tokens -inf, causal mask per row
 #pragma unroll
         for (int jn = 0; jn < 4; ++jn) {
@@ -576,57 +650,121 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
 #pragma unroll
           for (int jn = 0; jn < 4; ++jn) mx[hr] = fmaxf(mx[hr], fmaxf(s[jn][2 * hr], s[jn][2 * hr + 1]));
         }
+        // The sums follow the score max; the value frame moves only when it would lag the
+        // score max by more than kMqFrameGap (always at a row's first live tile).
         if (__any_sync(kFullMask, mx[0] > m_thr[0] || mx[1] > m_thr[1])) {
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             float mt = fmaxf(mx[hr], __shfl_xor_sync(kFullMask, mx[hr], 1));
             mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 2));
             const float mn = mt > m_thr[hr] ? mt : m_run[hr];
-            const float corr = mn == -INFINITY ? 1.f : ex2(m_run[hr] - mn);
+            const float corr = mn == m_run[hr] ? 1.f : ex2(m_run[hr] - mn);
             m_run[hr] = mn;
             m_thr[hr] = mn + kMqSlack;
             l_run[hr] *= corr;
+            const float mvn = fmaxf(mv[hr], mn - kMqFrameGap);
+            if (mvn != mv[hr]) {
+              const float cv = ex2(mv[hr] - mvn);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              o[nt][2 * hr] *= corr;
-              o[nt][2 * hr + 1] *= corr;
+              for (int nt = 0; nt < NT; ++nt) {
+                o[nt][2 * hr] *= cv;
+                o[nt][2 * hr + 1] *= cv;
+              }
+              mv[hr] = mvn;
+            }
+            fr[hr] = mn == -INFINITY ? 0.f : ex2(mn - mv[hr]);
+          }
+        }
+        // Value frame check before any weight is formed: p <= 2^kMqSlack, so every P' of a
+        // row is at most 2^6 * 2^(m - mv) * max nu_v.  Where that passes kMqValueBound (a
+        // row's first live tile, rows of very large norm) the row's frame is raised to the
+        // tile's largest s_t + log2 nu_v,t, so its P' here are at most ~1.
+        float vmax = 0.f;
+#pragma unroll
+        for (int jn = 0; jn < 4; ++jn) {
+          const float2 vn = *reinterpret_cast<const float2*>(vn_s + 8 * jn + 2 * c);
+          vmax = fmaxf(vmax, fmaxf(vn.x, vn.y));
+        }
+        if (__any_sync(kFullMask, vmax * fr[0] > kMqValueBound || vmax * fr[1] > kMqValueBound)) {
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            float sv = -INFINITY;
+#pragma unroll
+            for (int jn = 0; jn < 4; ++jn) {
+              const float2 vn = *reinterpret_cast<const float2*>(vn_s + 8 * jn + 2 * c);
+              sv = fmaxf(sv, fmaxf(s[jn][2 * hr] + lg2(vn.x), s[jn][2 * hr + 1] + lg2(vn.y)));
+            }
+            sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 1));
+            sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 2));
+            if (sv > mv[hr]) {
+              const float cv = ex2(mv[hr] - sv);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                o[nt][2 * hr] *= cv;
+                o[nt][2 * hr + 1] *= cv;
+              }
+              mv[hr] = sv;
+              fr[hr] = m_run[hr] == -INFINITY ? 0.f : ex2(m_run[hr] - sv);
             }
           }
         }
         const float m_use[2] = {m_run[0] == -INFINITY ? 0.f : m_run[0], m_run[1] == -INFINITY ? 0.f : m_run[1]};
-        uint32_t pa[2][4];
+        // O += P' Vhat: k-step s2 covers tokens 16 s2 .. 16 s2 + 15.  EXV adds P'_lo Vhat_hi
+        // and P'_hi Vhat_lo (the remainders sit in the key tile's space).
+        auto values = [&](auto exv_tag) {
+          constexpr bool EXV = decltype(exv_tag)::value;
+          uint32_t pa[2][4], pl[2][4];
 #pragma unroll
-        for (int jn = 0; jn < 4; ++jn) {
-          const int tok = 8 * jn + 2 * c;
-          const float2 vn = *reinterpret_cast<const float2*>(vn_s + tok);
-          float pw[4];
+          for (int jn = 0; jn < 4; ++jn) {
+            const int tok = 8 * jn + 2 * c;
+            const float2 vn = *reinterpret_cast<const float2*>(vn_s + tok);
+            float pw[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p = ex2(s[jn][e] - m_use[e >> 1]);
-            l_run[e >> 1] += p;
-            pw[e] = p > 0.f ? p * ((e & 1) ? vn.y : vn.x) : 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const float p = ex2(s[jn][e] - m_use[e >> 1]);
+              l_run[e >> 1] += p;
+              pw[e] = p > 0.f ? (p * fr[e >> 1]) * ((e & 1) ? vn.y : vn.x) : 0.f;  // P' = p 2^(m - mv) nu_v
+            }
+            const uint32_t h01 = half2_bits(pw[0], pw[1]), h23 = half2_bits(pw[2], pw[3]);
+            pa[jn >> 1][(jn & 1) * 2 + 0] = h01;
+            pa[jn >> 1][(jn & 1) * 2 + 1] = h23;
+            if (EXV) {
+              const __half2 x01 = *reinterpret_cast<const __half2*>(&h01);
+              const __half2 x23 = *reinterpret_cast<const __half2*>(&h23);
+              pl[jn >> 1][(jn & 1) * 2 + 0] = half2_bits(pw[0] - __low2float(x01), pw[1] - __high2float(x01));
+              pl[jn >> 1][(jn & 1) * 2 + 1] = half2_bits(pw[2] - __low2float(x23), pw[3] - __high2float(x23));
+            }
           }
-          pa[jn >> 1][(jn & 1) * 2 + 0] = half2_bits(pw[0], pw[1]);
-          pa[jn >> 1][(jn & 1) * 2 + 1] = half2_bits(pw[2], pw[3]);
-        }
-        // O += P' Vhat: k-step s2 covers tokens 16 s2 .. 16 s2 + 15
 #pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
+          for (int s2 = 0; s2 < 2; ++s2) {
 #pragma unroll
-          for (int dp = 0; dp < NT / 2; ++dp) {
-            uint32_t vb[4];
-            ldsm_x4_t(vb, (vb_lane ^ (uint32_t)((dh * (NT / 2) + dp) << 5)) + (uint32_t)(s2 * 16 * S::kRow));
-            mma_f16(o[2 * dp], pa[s2], vb[0], vb[1]);
-            mma_f16(o[2 * dp + 1], pa[s2], vb[2], vb[3]);
+            for (int dp = 0; dp < NT / 2; ++dp) {
+              const uint32_t vaddr = (vb_lane ^ (uint32_t)((dh * (NT / 2) + dp) << 5)) + (uint32_t)(s2 * 16 * S::kRow);
+              uint32_t vb[4];
+              ldsm_x4_t(vb, vaddr);
+              mma_f16(o[2 * dp], pa[s2], vb[0], vb[1]);
+              mma_f16(o[2 * dp + 1], pa[s2], vb[2], vb[3]);
+              if (EXV) {
+                uint32_t vl[4];
+                ldsm_x4_t(vl, vaddr - v_base + khi_base);
+                mma_f16(o[2 * dp], pl[s2], vb[0], vb[1]);
+                mma_f16(o[2 * dp + 1], pl[s2], vb[2], vb[3]);
+                mma_f16(o[2 * dp], pa[s2], vl[0], vl[1]);
+                mma_f16(o[2 * dp + 1], pa[s2], vl[2], vl[3]);
+              }
+            }
           }
-        }
+        };
+        if (exact_v) values(std::true_type{});
+        else values(std::false_type{});
       }
     }
     cp_async_wait<0>();  // no copy of this segment outlives it
     s0 = s1;
   }
 
-  // ---- partials: (m, l, acc / alpha_v) per (row, q head) of this window and split ------
+  // ---- partials: (m, l, acc / alpha_v) per (row, q head) of this window and split; the
+  // accumulator goes back from the value frame to the score frame (times 2^(mv - m)) ----
   const float inv_alpha_v = 1.0f / a.v_alpha;
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
@@ -638,10 +776,12 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
     if (wrow < nrows) {
       const int64_t slot = ((int64_t)(i0 + wrow) * Hq + (int64_t)h * G + mr % G) * args.nsplit + split;
       float* acc = args.part_acc + slot * D + dh * SH::kDh;
+      const float to_m =
+          (m_run[hr] == -INFINITY || mv[hr] == -INFINITY) ? 0.f : ex2(mv[hr] - m_run[hr]) * inv_alpha_v;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         *reinterpret_cast<float2*>(acc + 8 * nt + 2 * c) =
-            make_float2(o[nt][2 * hr] * inv_alpha_v, o[nt][2 * hr + 1] * inv_alpha_v);
+            to_m == 0.f ? make_float2(0.f, 0.f) : make_float2(o[nt][2 * hr] * to_m, o[nt][2 * hr + 1] * to_m);
       if (c == 0 && dh == 0) {
         args.part_ml[slot * 2 + 0] = m_run[hr];
         args.part_ml[slot * 2 + 1] = l;
@@ -657,7 +797,9 @@ cudaError_t launch_mq_one(const MqArgs& m, int grid, cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err != cudaSuccess) return err;
   kern<<<grid, MqShape<D>::kThreads, bytes, stream>>>(m);
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
 }
 
 template <int D, int KB, int VB>

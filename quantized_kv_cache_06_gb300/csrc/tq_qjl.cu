@@ -319,6 +319,7 @@ cudaError_t launch_prod_decode_e(const DecodeArgs& a, const float* smat, const D
   qjl_project_kernel<E><<<(unsigned)((qrows + 7) / 8), 256, 0, stream>>>(a, smat, p_all);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  count_launches(1);
   const int G = a.num_q_heads / a.num_kv_heads;
   dim3 grid(p.num_splits, a.num_kv_heads, a.batch);
   switch (G) {
@@ -330,6 +331,7 @@ cudaError_t launch_prod_decode_e(const DecodeArgs& a, const float* smat, const D
   }
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  count_launches(1);
   return launch_combine_splits(part.acc, part.ml, (int)qrows, p.num_splits, D, a.signs, a.out, a.out_dtype, stream);
 }
 
@@ -358,7 +360,9 @@ cudaError_t launch_write_prod(const WriteArgs& a, const float* smat, cudaStream_
     if (err != cudaSuccess) return err;                                                                       \
     kern<<<grid, kProdWarps * 32, smem, stream>>>(static_cast<const T*>(a.raw), rows, a.num_kv_heads, a.bits, \
                                                   a.slots, a.pages, a.signs, a.centroids, smat, a.status);    \
-    return cudaGetLastError();                                                                                \
+    err = cudaGetLastError();                                                                                 \
+    if (err == cudaSuccess) count_launches(1);                                                                \
+    return err;                                                                                               \
   }
   const int E = a.head_dim / 32;
   if (a.dtype == kF16) {

@@ -1,0 +1,538 @@
+// Recipe cache modes turboquant25 / turboquant35: grouped product-quantised rows, writer
+// and paged decode (sm_103a, SIMT).
+//
+// TurboQuant docs: "vLLM Usage" (Cache Dtypes: turboquant25 and turboquant35, recipe
+// modes require metadata; Metadata Validation Rules; Page Geometry: recipe row bytes) and
+// "Architecture" (vLLM Runtime Mapping: channels selected by energy, recipe vector rows
+// pack and unpack grouped MSE+QJL rows); "vLLM Reference Audit" lists the recipe update
+// and decode kernels as missing.
+//
+// Row (a reading: the pages name the parts, not the numbers).  A row's D channels form a
+// high group and a low group of d = D / 2 channels; order[h][0, D) lists kv head h's high
+// group (sorted), then its low group (the complement, ascending).  Group g is one
+// product-quantised vector of dimension d at bits_g (turboquant25: 3 and 2, turboquant35:
+// 4 and 3 -- the recipe name is the mean bits per channel): the (bits_g - 1)-bit MSE
+// indices of y = R_d x_g / ||x_g|| (LSB first), one sign bit per coordinate of S_d r
+// (r = y - c[idx], bit = 1 for a non-negative projection), then nu_g = ||x_g|| and
+// gamma_g = ||r|| as fp32.  The row holds the high group's bytes, then the low group's.
+// R_d (RHT of dimension d) and S_d (d x d standard normal) are shared by both groups and
+// by K and V, which both use recipe rows.
+//
+// Kernels:
+//   write_recipe_kernel        one warp per (token, head, group): channel gather, norm,
+//                              rotation (warp FWHT), indices, residual, and the sketch
+//                              signs from S_d^T staged in shared memory (output i = lane
+//                              + 32 e, so one ballot per e is sign word e).
+//   recipe_project_kernel      one warp per (sequence, q head): per group the rotated
+//                              gathered query q_g = R_d q[order_g] (times the softmax scale
+//                              and log2 e) and its projection p_g = S_d q_g.
+//   decode_recipe_split_kernel the SIMT split decode.  Score of key row k:
+//                                sum_g nu_g (<q_g, c_g[idx]> + gamma_g kappa <p_g, 2z - 1>),
+//                              kappa = sqrt(pi / 2) / d.  The value reconstruction
+//                              nu R_d^T (c[idx] + gamma kappa S_d^T (2z - 1)) is linear, so
+//                              the kernel keeps two accumulators per group,
+//                              sum p nu c[idx] and sum p nu gamma kappa (2z - 1), and no
+//                              per-token S_d^T product is needed.
+//   combine_recipe_kernel      one warp per (sequence, q head): merges the splits, then per
+//                              group w = acc_c + S_d^T acc_z, R_d^T w / l, scattered back to
+//                              the group's channels.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "tq_device.cuh"
+#include "tq_recipe.h"
+
+namespace tq {
+namespace {
+
+constexpr int kRecWarps = 8;
+constexpr int kRecDecodeWarps = 4;
+constexpr float kRecLog2e = 1.4426950408889634f;
+constexpr float kRecSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi / 2)
+
+// 32-bit words of group g's part of a row: d (b - 1) / 32 index words, d / 32 sign words,
+// nu, gamma.
+__host__ __device__ constexpr int group_words(int d, int bits) { return d * (bits - 1) / 32 + d / 32 + 2; }
+
+template <typename T, int E>
+__global__ void __launch_bounds__(kRecWarps * 32)
+write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads, const int64_t* __restrict__ slots,
+                    uint8_t* __restrict__ pages, RecipeArgs rc, const float* __restrict__ signs,
+                    const int32_t* __restrict__ status) {
+  constexpr int d = 32 * E, D = 2 * d;
+  extern __shared__ float s_t[];  // S_d^T, padded: s_t[j * (d + 1) + i] = S[i][j]
+  __shared__ float bnd[2][8], cen[2][8];
+  __shared__ float rbuf[kRecWarps][d];
+  __shared__ uint32_t rowbuf[kRecWarps][3 * E + E + 2];
+
+  const int tid = threadIdx.x;
+  const int mb0 = rc.bits_hi - 1, mb1 = rc.bits_lo - 1;
+  const int nc0 = 1 << mb0, nc1 = 1 << mb1;
+  if (tid < nc0 - 1) bnd[0][tid] = 0.5f * (rc.mse_hi[tid] + rc.mse_hi[tid + 1]);
+  if (tid < nc0) cen[0][tid] = rc.mse_hi[tid];
+  if (tid < nc1 - 1) bnd[1][tid] = 0.5f * (rc.mse_lo[tid] + rc.mse_lo[tid + 1]);
+  if (tid < nc1) cen[1][tid] = rc.mse_lo[tid];
+  for (int k = tid; k < d * d; k += blockDim.x) {  // coalesced reads, conflict-free stores
+    const int i = k / d, j = k - i * d;
+    s_t[j * (d + 1) + i] = __ldg(rc.smat + k);
+  }
+  __syncthreads();
+  if (*status != kOk) return;  // a slot failed validation: write nothing
+
+  const int warp = tid >> 5, lane = tid & 31;
+  const int row_words = group_words(d, rc.bits_hi) + group_words(d, rc.bits_lo);
+  const float inv_sqrt_d = 1.0f / sqrtf((float)d);
+  float sg[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) sg[i] = __ldg(signs + lane * E + i);
+  uint32_t* buf = rowbuf[warp];
+  float* res = rbuf[warp];
+
+  const int64_t units = 2 * num_rows;
+  for (int64_t u = (int64_t)blockIdx.x * kRecWarps + warp; u < units; u += (int64_t)gridDim.x * kRecWarps) {
+    const int64_t r = u >> 1;
+    const int g = (int)(u & 1);
+    const int64_t t = r / num_kv_heads;
+    const int h = (int)(r - t * num_kv_heads);
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;  // "Slot Mapping": negative slots are ignored
+    const int mb = g ? mb1 : mb0, nc = g ? nc1 : nc0;
+
+    float v[E];
+    const int32_t* ord = rc.order + (int64_t)h * D + g * d + lane * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) v[i] = to_f32<T>(raw[r * D + __ldg(ord + i)]);
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) ss = fmaf(v[i], v[i], ss);
+    const float nu = sqrtf(warp_sum(ss));
+#pragma unroll
+    for (int i = 0; i < E; ++i) v[i] *= sg[i];
+    fwht_warp<E>(v);
+    const float inv = nu > 0.f ? inv_sqrt_d / nu : 0.f;  // y = H(s*x)/(sqrt(d) nu)
+
+    const int index_words = d * mb / 32;
+    const int gw = index_words + E + 2;
+    for (int w = lane; w < gw; w += 32) buf[w] = 0u;
+    __syncwarp();
+    float rs = 0.f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float y = v[i] * inv;
+      int idx = 0;  // #{k : boundary_k < y}
+      for (int s = nc >> 1; s > 0; s >>= 1)
+        if (y > bnd[g][idx + s - 1]) idx += s;
+      const int bit = (lane * E + i) * mb;
+      const int w = bit >> 5, o = bit & 31;
+      atomicOr(&buf[w], (uint32_t)idx << o);
+      if (o + mb > 32) atomicOr(&buf[w + 1], (uint32_t)idx >> (32 - o));
+      const float dr = y - cen[g][idx];
+      res[lane * E + i] = dr;
+      rs = fmaf(dr, dr, rs);
+    }
+    const float gamma = sqrtf(warp_sum(rs));
+    __syncwarp();
+    // sign word e: bit `lane` is [(S r)_(lane + 32 e) >= 0]
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = lane + 32 * e;
+      float acc = 0.f;
+      for (int j = 0; j < d; ++j) acc = fmaf(s_t[j * (d + 1) + i], res[j], acc);
+      const uint32_t mask = __ballot_sync(kFullMask, acc >= 0.f);
+      if (lane == 0) buf[index_words + e] = mask;
+    }
+    if (lane == 0) {
+      buf[index_words + E] = __float_as_uint(nu);
+      buf[index_words + E + 1] = __float_as_uint(gamma);
+    }
+    __syncwarp();
+    uint32_t* dst = reinterpret_cast<uint32_t*>(pages + (slot * num_kv_heads + h) * (int64_t)(row_words * 4)) +
+                    (g ? group_words(d, rc.bits_hi) : 0);
+    for (int w = lane; w < gw; w += 32) dst[w] = buf[w];
+    __syncwarp();
+  }
+}
+
+// p[row][g][i] = sum_j S[i][j] q_g[j], q_g = R_d q[row][order_g] times the softmax scale
+// and log2(e) (the decode's own rotated query), row = (sequence, q head).
+template <int E>
+__global__ void __launch_bounds__(256)
+recipe_project_kernel(DecodeArgs a, RecipeArgs rc, float* __restrict__ p_out) {
+  constexpr int d = 32 * E, D = 2 * d;
+  __shared__ float qs[8][2][d];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;
+  if (row >= (int64_t)a.batch * a.num_q_heads) return;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const int h = (int)(row % a.num_q_heads) / G;
+  const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
+  const float qmul = scale * kRecLog2e / sqrtf((float)d);
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    float qr[E];
+    const int32_t* ord = rc.order + (int64_t)h * D + g * d + lane * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i) qr[i] = load_as_f32(a.q, row * D + __ldg(ord + i), a.q_dtype) * __ldg(a.signs + lane * E + i);
+    fwht_warp<E>(qr);
+#pragma unroll
+    for (int i = 0; i < E; ++i) qs[warp][g][lane * E + i] = qr[i] * qmul;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = lane + 32 * e;
+      float acc = 0.f;
+      for (int j = 0; j < d; ++j) acc = fmaf(__ldg(rc.smat + (int64_t)i * d + j), qs[warp][g][j], acc);
+      p_out[(row * 2 + g) * d + i] = acc;
+    }
+}
+
+struct RecipeSplitView {
+  float* acc;  // [rows][nsplit][2 D]: acc_c (group-major, coordinate j), then acc_z (coordinate i)
+  float* ml;   // [rows][nsplit][2]  (running max in log2 units, sum)
+};
+
+__device__ __forceinline__ int rfield(uint64_t win, int bitpos, int bits) {
+  return (int)((win >> bitpos) & ((1u << bits) - 1u));
+}
+
+// One group of one packed row, as this lane needs it: the MSE indices of coordinates
+// lane E + i, the sign words (bit `lane` of word e: coordinate lane + 32 e), nu, gamma.
+template <int E>
+struct GroupView {
+  int idx[E];
+  uint32_t zw[E];
+  float nu, gamma;
+};
+
+template <int E>
+__device__ __forceinline__ GroupView<E> read_group(const uint32_t* __restrict__ gw, int mb, int lane) {
+  constexpr int d = 32 * E;
+  GroupView<E> v;
+  const int bit0 = lane * E * mb;
+  const uint64_t win = (uint64_t)__ldg(gw + (bit0 >> 5)) | ((uint64_t)__ldg(gw + (bit0 >> 5) + 1) << 32);
+#pragma unroll
+  for (int i = 0; i < E; ++i) v.idx[i] = rfield(win, (bit0 & 31) + i * mb, mb);
+  const int iw = d * mb / 32;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v.zw[e] = __ldg(gw + iw + e);
+  v.nu = __uint_as_float(__ldg(gw + iw + E));
+  v.gamma = __uint_as_float(__ldg(gw + iw + E + 1));
+  return v;
+}
+
+template <int E, int G>
+__global__ void __launch_bounds__(kRecDecodeWarps * 32)
+decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p_all, int num_splits,
+                           int blocks_per_split, RecipeSplitView part) {
+  constexpr int d = 32 * E, D = 2 * d;
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.num_kv_heads, bs = a.block_size;
+  const int mb[2] = {rc.bits_hi - 1, rc.bits_lo - 1};
+  const int w_hi = group_words(d, rc.bits_hi);
+  const int rb = 4 * (w_hi + group_words(d, rc.bits_lo));
+
+  __shared__ float cent[2][8];
+  __shared__ float red_ml[kRecDecodeWarps][G][2];
+  __shared__ float red_acc[kRecDecodeWarps][G][2 * D];
+  if (threadIdx.x < (1 << mb[0])) cent[0][threadIdx.x] = rc.mse_hi[threadIdx.x];
+  if (threadIdx.x < (1 << mb[1])) cent[1][threadIdx.x] = rc.mse_lo[threadIdx.x];
+
+  const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
+  const float qmul = scale * kRecLog2e / sqrtf((float)d);
+  const float kappa = kRecSqrtHalfPi / (float)d;
+  float qr[G][2][E], pp[G][2][E];  // rotated query (coordinates lane E + i), projection (lane + 32 e)
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int64_t qrow = (int64_t)b * a.num_q_heads + (int64_t)h * G + g;
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const int32_t* ord = rc.order + (int64_t)h * D + grp * d + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        qr[g][grp][i] = load_as_f32(a.q, qrow * D + __ldg(ord + i), a.q_dtype) * __ldg(a.signs + lane * E + i);
+      fwht_warp<E>(qr[g][grp]);
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        qr[g][grp][i] *= qmul;
+        pp[g][grp][i] = __ldg(p_all + (qrow * 2 + grp) * d + lane + 32 * i);
+      }
+    }
+  }
+
+  int len = __ldg(a.seq_lens + b);
+  const int cap = a.max_blocks_per_seq * bs;
+  if (len < 0 || len > cap) {
+    if (threadIdx.x == 0 && split == 0 && h == 0 && a.status) atomicMax(a.status, (int32_t)kInvalidArg);
+    len = len < 0 ? 0 : cap;
+  }
+  const int t_lo = split * blocks_per_split * bs;
+  const int t_hi = min(len, (split + 1) * blocks_per_split * bs);
+
+  float m[G], l[G], acc_c[G][2][E], acc_z[G][2][E];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+      for (int i = 0; i < E; ++i) acc_c[g][grp][i] = acc_z[g][grp][i] = 0.f;
+  }
+  __syncthreads();
+
+  bool bad_block = false;
+  for (int t = t_lo + warp; t < t_hi; t += kRecDecodeWarps) {
+    const int bid = __ldg(a.block_table + (int64_t)b * a.max_blocks_per_seq + t / bs);
+    if (bid < 0 || (int64_t)bid >= a.num_blocks) {
+      bad_block = true;
+      continue;
+    }
+    const int64_t row = ((int64_t)bid * bs + t % bs) * H + h;
+    const uint32_t* kr = reinterpret_cast<const uint32_t*>(a.k_pages + row * rb);
+    const uint32_t* vr = reinterpret_cast<const uint32_t*>(a.v_pages + row * rb);
+    float s[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) s[g] = 0.f;
+    float vc[2][E], vz[2][E];  // this token's value terms: nu c[idx] and nu gamma kappa (2z - 1)
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const GroupView<E> k = read_group<E>(kr + (grp ? w_hi : 0), mb[grp], lane);
+      const GroupView<E> v = read_group<E>(vr + (grp ? w_hi : 0), mb[grp], lane);
+      const float kz = k.gamma * kappa;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float sm = 0.f, sz = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          sm = fmaf(qr[g][grp][i], cent[grp][k.idx[i]], sm);
+          sz = fmaf(pp[g][grp][i], ((k.zw[i] >> lane) & 1u) ? 1.f : -1.f, sz);
+        }
+        s[g] = fmaf(k.nu, fmaf(kz, sz, sm), s[g]);
+      }
+      const float vzs = v.nu * v.gamma * kappa;
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        vc[grp][i] = v.nu * cent[grp][v.idx[i]];
+        vz[grp][i] = ((v.zw[i] >> lane) & 1u) ? vzs : -vzs;
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float sc = warp_sum(s[g]);
+      const float mn = fmaxf(m[g], sc);
+      const float corr = exp2f(m[g] - mn);
+      const float p = exp2f(sc - mn);
+      l[g] = l[g] * corr + p;
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          acc_c[g][grp][i] = fmaf(p, vc[grp][i], acc_c[g][grp][i] * corr);
+          acc_z[g][grp][i] = fmaf(p, vz[grp][i], acc_z[g][grp][i] * corr);
+        }
+      m[g] = mn;
+    }
+  }
+  if (__any_sync(kFullMask, bad_block) && lane == 0 && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+
+  // merge the warps of this CTA, then write the split partial
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (lane == 0) {
+      red_ml[warp][g][0] = m[g];
+      red_ml[warp][g][1] = l[g];
+    }
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        red_acc[warp][g][grp * d + lane * E + i] = acc_c[g][grp][i];
+        red_acc[warp][g][D + grp * d + lane + 32 * i] = acc_z[g][grp][i];
+      }
+  }
+  __syncthreads();
+  for (int g = warp; g < G; g += kRecDecodeWarps) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kRecDecodeWarps; ++w) mx = fmaxf(mx, red_ml[w][g][0]);
+    float wt[kRecDecodeWarps], lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRecDecodeWarps; ++w) {
+      wt[w] = red_ml[w][g][0] == -INFINITY ? 0.f : exp2f(red_ml[w][g][0] - mx);
+      lsum = fmaf(wt[w], red_ml[w][g][1], lsum);
+    }
+    const int64_t slot = ((int64_t)b * a.num_q_heads + (int64_t)h * G + g) * num_splits + split;
+    for (int k = lane; k < 2 * D; k += 32) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRecDecodeWarps; ++w) sum = fmaf(wt[w], red_acc[w][g][k], sum);
+      part.acc[slot * 2 * D + k] = sum;
+    }
+    if (lane == 0) {
+      part.ml[slot * 2 + 0] = mx;
+      part.ml[slot * 2 + 1] = lsum;
+    }
+  }
+}
+
+template <int E>
+__global__ void __launch_bounds__(256)
+combine_recipe_kernel(DecodeArgs a, RecipeArgs rc, int num_splits, RecipeSplitView part) {
+  constexpr int d = 32 * E, D = 2 * d;
+  __shared__ float zs[8][d];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;
+  if (row >= (int64_t)a.batch * a.num_q_heads) return;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const int h = (int)(row % a.num_q_heads) / G;
+  const float* ml = part.ml + row * num_splits * 2;
+  const float* acc = part.acc + row * num_splits * 2 * D;
+  float mx = -INFINITY;
+  for (int s = 0; s < num_splits; ++s) mx = fmaxf(mx, ml[2 * s]);
+  float vc[2][E], vz[2][E], lsum = 0.f;
+#pragma unroll
+  for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+    for (int i = 0; i < E; ++i) vc[grp][i] = vz[grp][i] = 0.f;
+  for (int s = 0; s < num_splits; ++s) {
+    const float ms = ml[2 * s];
+    const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+    lsum = fmaf(w, ml[2 * s + 1], lsum);
+    const float* as = acc + (int64_t)s * 2 * D;
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        vc[grp][i] = fmaf(w, as[grp * d + lane * E + i], vc[grp][i]);
+        vz[grp][i] = fmaf(w, as[D + grp * d + lane + 32 * i], vz[grp][i]);
+      }
+  }
+  const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+  const float rs = 1.0f / sqrtf((float)d);
+#pragma unroll
+  for (int grp = 0; grp < 2; ++grp) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) zs[warp][lane + 32 * i] = vz[grp][i];
+    __syncwarp();
+    float w[E];  // acc_c + S^T acc_z at coordinates lane E + i
+#pragma unroll
+    for (int i = 0; i < E; ++i) w[i] = vc[grp][i];
+    for (int k = 0; k < d; ++k) {
+      const float z = zs[warp][k];
+#pragma unroll
+      for (int i = 0; i < E; ++i) w[i] = fmaf(__ldg(rc.smat + (int64_t)k * d + lane * E + i), z, w[i]);
+    }
+    __syncwarp();  // zs is rewritten for the next group
+#pragma unroll
+    for (int i = 0; i < E; ++i) w[i] *= inv;
+    fwht_warp<E>(w);  // R_d^T w = diag(s) H w / sqrt(d)
+    const int32_t* ord = rc.order + (int64_t)h * D + grp * d + lane * E;
+#pragma unroll
+    for (int i = 0; i < E; ++i)
+      store_from_f32(a.out, row * D + __ldg(ord + i), a.out_dtype, w[i] * __ldg(a.signs + lane * E + i) * rs);
+  }
+}
+
+template <typename T, int E>
+cudaError_t launch_write_recipe_typed(const WriteArgs& a, const RecipeArgs& rc, cudaStream_t stream, int num_sms) {
+  constexpr int d = 32 * E;
+  const int64_t units = 2 * a.num_tokens * a.num_kv_heads;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((units + kRecWarps - 1) / kRecWarps, (int64_t)num_sms * 4));
+  const size_t smem = (size_t)d * (d + 1) * sizeof(float);
+  auto kern = write_recipe_kernel<T, E>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kRecWarps * 32, smem, stream>>>(static_cast<const T*>(a.raw), a.num_tokens * a.num_kv_heads,
+                                               a.num_kv_heads, a.slots, a.pages, rc, a.signs, a.status);
+  err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
+}
+
+template <typename T>
+cudaError_t launch_write_recipe_dim(const WriteArgs& a, const RecipeArgs& rc, cudaStream_t stream, int num_sms) {
+  if (a.head_dim == 64) return launch_write_recipe_typed<T, 1>(a, rc, stream, num_sms);
+  if (a.head_dim == 128) return launch_write_recipe_typed<T, 2>(a, rc, stream, num_sms);
+  return cudaErrorInvalidValue;
+}
+
+template <int E>
+cudaError_t launch_decode_recipe_e(const DecodeArgs& a, const RecipeArgs& rc, const DecodePlan& p,
+                                   cudaStream_t stream) {
+  constexpr int D = 64 * E;
+  const int64_t qrows = (int64_t)a.batch * a.num_q_heads;
+  RecipeSplitView part;
+  part.acc = static_cast<float*>(a.workspace);
+  part.ml = part.acc + (size_t)qrows * p.num_splits * 2 * D;
+  float* p_all = part.ml + (size_t)qrows * p.num_splits * 2;
+  const unsigned rgrid = (unsigned)((qrows + 7) / 8);
+  recipe_project_kernel<E><<<rgrid, 256, 0, stream>>>(a, rc, p_all);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  count_launches(1);
+  const int G = a.num_q_heads / a.num_kv_heads;
+  dim3 grid(p.num_splits, a.num_kv_heads, a.batch);
+  switch (G) {
+    case 1: decode_recipe_split_kernel<E, 1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    case 2: decode_recipe_split_kernel<E, 2><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    case 4: decode_recipe_split_kernel<E, 4><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    case 8: decode_recipe_split_kernel<E, 8><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    default: return cudaErrorInvalidValue;
+  }
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  count_launches(1);
+  combine_recipe_kernel<E><<<rgrid, 256, 0, stream>>>(a, rc, p.num_splits, part);
+  err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
+}
+
+}  // namespace
+
+bool recipe_supported(int head_dim) { return head_dim == 64 || head_dim == 128; }
+
+int recipe_row_bytes(int head_dim, int bits_hi, int bits_lo) {
+  const int d = head_dim / 2;
+  return 4 * (group_words(d, bits_hi) + group_words(d, bits_lo));
+}
+
+size_t recipe_decode_workspace(const DecodeArgs& a, const DecodePlan& p) {
+  const size_t qrows = (size_t)std::max(0, a.batch) * a.num_q_heads;
+  return qrows * p.num_splits * (2 * a.head_dim + 2) * sizeof(float) + qrows * a.head_dim * sizeof(float) + 16;
+}
+
+cudaError_t launch_write_recipe(const WriteArgs& a, const RecipeArgs& rc, cudaStream_t stream, int num_sms) {
+  cudaError_t err = cudaMemsetAsync(a.status, 0, sizeof(int32_t), stream);
+  if (err != cudaSuccess) return err;
+  if (a.num_tokens == 0) return cudaSuccess;
+  err = launch_validate_slots(a, stream, num_sms);
+  if (err != cudaSuccess) return err;
+  switch (a.dtype) {
+    case kF32: return launch_write_recipe_dim<float>(a, rc, stream, num_sms);
+    case kF16: return launch_write_recipe_dim<__half>(a, rc, stream, num_sms);
+    case kBF16: return launch_write_recipe_dim<__nv_bfloat16>(a, rc, stream, num_sms);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_recipe(const DecodeArgs& a, const RecipeArgs& rc, const DecodePlan& p, cudaStream_t stream) {
+  if (a.status) {
+    cudaError_t err = cudaMemsetAsync(a.status, 0, sizeof(int32_t), stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (a.batch == 0) return cudaSuccess;
+  if (a.head_dim == 64) return launch_decode_recipe_e<1>(a, rc, p, stream);
+  if (a.head_dim == 128) return launch_decode_recipe_e<2>(a, rc, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tq

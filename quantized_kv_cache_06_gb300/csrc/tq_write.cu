@@ -9,6 +9,7 @@
 // shuffles.  The packed row is assembled in shared memory and written back as
 // 32-bit words (rows are 4-byte aligned for D >= 32).
 #include <algorithm>
+#include <mutex>
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
@@ -120,7 +121,9 @@ cudaError_t launch_write_typed(const WriteArgs& a, cudaStream_t stream, int grid
       return cudaErrorInvalidValue;
   }
 #undef TQ_WRITE_CASE
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
 }
 
 }  // namespace
@@ -128,7 +131,34 @@ cudaError_t launch_write_typed(const WriteArgs& a, cudaStream_t stream, int grid
 cudaError_t launch_validate_slots(const WriteArgs& a, cudaStream_t stream, int num_sms) {
   const int vgrid = (int)std::min<int64_t>((a.num_tokens + 255) / 256, (int64_t)num_sms * 4);
   validate_slots_kernel<<<vgrid, 256, 0, stream>>>(a.slots, a.num_tokens, a.num_blocks * a.block_size, a.status);
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
+}
+
+// Status word of the writes called without a caller status word (tq_write_kv /
+// tq_write_kv_prod with status_dev == NULL): one file-scope device int per device, its
+// address looked up once per device with that device current.
+namespace {
+__device__ int32_t g_internal_write_status;
+std::mutex g_internal_status_mutex;
+int32_t* g_internal_status_ptr[128] = {};
+}  // namespace
+
+cudaError_t internal_write_status(int32_t** ptr) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_internal_status_mutex);
+  if (g_internal_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_internal_write_status);
+    if (err != cudaSuccess) return err;
+    g_internal_status_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *ptr = g_internal_status_ptr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream) {

@@ -502,7 +502,9 @@ cudaError_t launch_dependent(K kern, int grid, size_t smem, cudaStream_t stream,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, t);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, t);
+  if (err == cudaSuccess) count_launches(1);
+  return err;
 }
 
 cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {

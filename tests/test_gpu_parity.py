@@ -126,24 +126,28 @@ def test_workload2_mixed_bits(tq):
     run_workload(tq, w)
 
 
+# Full-size workloads: every (sequence, q head) output is compared with the oracle (the
+# oracle's cost is per (sequence, kv head), the same for one q head or all of them).  The
+# writer is checked on sampled tokens: >= 1e7 coordinates per component for workloads 4
+# and 5, where the in-band flip count is held to the strict 1e-5 n.
+
 @pytest.mark.parametrize("sub", range(len(SWEEP)), ids=[f"b{b}_d{d}" for b, d in SWEEP])
 def test_workload3_sweep(tq, sub):
     w = make_workload(3, sub=sub)
-    heads = [(b, j) for b in (0, 7, 15) for j in range(0, 32, 5)]
-    run_workload(tq, w, sample_tokens=3000, heads=heads)
+    run_workload(tq, w, sample_tokens=3000)
 
 
 def test_workload4_full_size(tq):
     w = make_workload(4)
-    heads = [(b, j) for b in (0, 21, 63) for j in (0, 5, 17, 31)]
-    run_workload(tq, w, sample_tokens=4000, heads=heads)
+    ks, vs, _ = run_workload(tq, w, sample_tokens=10000)
+    assert ks["coords"] >= 10_000_000 and vs["coords"] >= 10_000_000
 
 
 def test_workload5_full_size_with_prefill_write(tq):
     w = make_workload(5)
-    heads = [(b, j) for b in range(4) for j in (0, 13, 63)]
     codec = OracleCodec(w.head_dim)
-    ks, vs, _ = run_workload(tq, w, sample_tokens=3000, heads=heads)
+    ks, vs, _ = run_workload(tq, w, sample_tokens=10000)
+    assert ks["coords"] >= 10_000_000 and vs["coords"] >= 10_000_000
     # prefill-style re-write of sequence 0 with 5% negative slots: the skipped rows keep the
     # bytes of the first write, the others hold the new rows
     kp, _ = gpu_write(tq, w.k_raw, w.slots, w.num_blocks, w.block_size, w.k_bits)
@@ -155,7 +159,8 @@ def test_workload5_full_size_with_prefill_write(tq):
     flat_b = before.reshape(-1, before.shape[2], before.shape[3])
     flat_a = after.reshape(-1, after.shape[2], after.shape[3])
     assert np.array_equal(flat_a[skipped], flat_b[skipped])
-    check_written_rows(after, w.write_k, w.write_slots, w.k_bits, codec, sample_tokens=3000)
+    st = check_written_rows(after, w.write_k, w.write_slots, w.k_bits, codec, sample_tokens=10000)
+    assert st["coords"] >= 10_000_000
 
 
 # ---------------------------------------------------------------- writer edge cases

@@ -90,13 +90,17 @@ def test_host_argument_errors(tq):
     assert lib.tq_build_rotation(100, 1, ctypes.addressof(buf)) == tq.TQ_ERR_UNSUPPORTED
     assert lib.tq_build_rotation(64, 1, None) == tq.TQ_ERR_INVALID_ARG
     assert "NULL" in lib.tq_last_error().decode()
-    assert lib.tq_codebook(128, 1, ctypes.addressof(buf), None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_codebook(128, 6, ctypes.addressof(buf), None) == tq.TQ_ERR_UNSUPPORTED
+    assert lib.tq_codebook(128, 0, ctypes.addressof(buf), None) == tq.TQ_ERR_UNSUPPORTED
     assert lib.tq_codebook(128, 4, ctypes.addressof(buf), None) == tq.TQ_OK
     assert lib.tq_last_error().decode() == ""
-    # writer: missing status word, bad bits, bad head_dim -- all rejected on the host
+    # writer: bad sizes, bad bits, bad head_dim, misalignment -- all rejected on the host, with
+    # or without a status word (a NULL one makes a valid call synchronous, not invalid)
     dummy = 1 << 20
-    assert lib.tq_write_kv(dummy, 1, 4, 2, 128, 4, dummy, dummy, 4, 16, dummy, dummy, None, None) == \
+    assert lib.tq_write_kv(dummy, 1, -4, 2, 128, 4, dummy, dummy, 4, 16, dummy, dummy, None, None) == \
         tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_write_kv(dummy, 1, 4, 2, 128, 6, dummy, dummy, 4, 16, dummy, dummy, None, None) == \
+        tq.TQ_ERR_UNSUPPORTED
     assert lib.tq_write_kv(dummy, 1, 4, 2, 128, 6, dummy, dummy, 4, 16, dummy, dummy, dummy, None) == \
         tq.TQ_ERR_UNSUPPORTED
     assert lib.tq_write_kv(dummy, 1, 4, 2, 96, 4, dummy, dummy, 4, 16, dummy, dummy, dummy, None) == \
@@ -147,7 +151,7 @@ def test_prod_host_argument_errors(tq):
     w = lambda d, b, status: (dummy, 1, 4, 2, d, b, dummy, dummy, 4, 16, dummy, dummy, dummy, status, None)
     assert lib.tq_write_kv_prod(*w(256, 4, dummy)) == tq.TQ_ERR_UNSUPPORTED  # the kernels take D 64 / 128
     assert lib.tq_write_kv_prod(*w(128, 2, dummy)) == tq.TQ_ERR_UNSUPPORTED  # and 3..5 bits
-    assert lib.tq_write_kv_prod(*w(128, 4, None)) == tq.TQ_ERR_INVALID_ARG
+    assert lib.tq_write_kv_prod(*w(128, 2, None)) == tq.TQ_ERR_UNSUPPORTED  # NULL status: checked all the same
     dec = lambda d, kb, vb, ws: (dummy, 1, 2, 32, 8, d, dummy, kb, dummy, vb, 8, 16, dummy, 4, dummy, dummy, dummy,
                                  dummy, dummy, 0.0, dummy, 1, dummy, ws, None, None)
     assert lib.tq_paged_decode_prod(*dec(256, 4, 4, 1 << 30)) == tq.TQ_ERR_UNSUPPORTED
@@ -197,3 +201,14 @@ def test_build_compiles_every_source_file():
 
     on_disk = {f for f in os.listdir(build.CSRC) if f.endswith((".cu", ".cpp"))}
     assert set(build.SOURCES) == on_disk
+
+
+def test_wait_limit_hook_round_trips(tq):
+    # host-only: the value later decode launches take for their bounded waits
+    lib = tq.lib()
+    default = lib.tq_set_wait_limit(-1)
+    assert default > 0
+    assert lib.tq_set_wait_limit(5) == default
+    assert lib.tq_set_wait_limit(0) == 5
+    assert lib.tq_set_wait_limit(-7) == 0
+    assert lib.tq_set_wait_limit(-1) == default
