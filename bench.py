@@ -313,6 +313,42 @@ def next_rows_cpu_baselines(w, n_write_tokens=2048, chunk=4):
         out["qjl_residual_keys"] = {
             "write": entry(wr_bytes / t_w / 1e9, f"product-key write of {nw} tokens x {h} K rows"),
             "decode": entry(dec_bytes / t_d / 1e9, f"decode of sequence 0 ({n0} tokens) over product keys")}
+
+    # INT8-query prefill: the same chunk as the float prefill, on int8 codes and scales
+    from oracle import int8q_oracle as iq
+    codes, scales = iq.quantize_queries_int8(q)
+    t0 = time.perf_counter()
+    iq.paged_prefill_int8q(codes, scales, np.zeros(c, np.int64), q_len, kp, vp, w.k_bits, w.v_bits, bt, signs, ck, cv)
+    t = time.perf_counter() - t0
+    out["int8q_prefill"] = entry((n0 * h * (rb_k + rb_v) + codes.size + 4 * scales.size + 2 * q.size) / t / 1e9,
+                                 f"{c} int8 query rows at the end of sequence 0 ({n0} tokens), GB/s of unique bytes")
+
+    # recipe modes: the recipe write of n_write_tokens tokens' K rows, and the decode of
+    # sequence 0 over K and V recipe pages (channel groups calibrated on those K rows)
+    if d in (64, 128):
+        from oracle import recipe_oracle as ro
+        nw = min(n_write_tokens, n0)
+        rec = {}
+        for recipe in ("turboquant25", "turboquant35"):
+            smat = qo.normal_matrix(d // 2, d // 2, ro.SKETCH_SEED).astype(np.float32).astype(np.float64)
+            codec = ro.RecipeCodec(recipe, d, smat=smat)
+            rb = ro.recipe_row_bytes(recipe, d)
+            high = ro.calibrate_high_groups(np.asarray(kraw[:nw], dtype=np.float64), recipe)
+            pages = np.zeros((nblk, bs, h, rb), np.uint8)
+            t0 = time.perf_counter()
+            ro.write_recipe_kv(kraw[:nw], pages, slots[:nw], high, codec)
+            t_w = time.perf_counter() - t0
+            kpr = ro.write_recipe_kv(kraw, pages, slots, high, codec)
+            vpr = ro.write_recipe_kv(vraw, pages, slots, high, codec)
+            t0 = time.perf_counter()
+            ro.paged_decode_recipe(w.q[:1], kpr, vpr, bt, np.array([n0]), high, codec)
+            t_d = time.perf_counter() - t0
+            rec[recipe] = {
+                "write": entry((nw * h * (d * kraw.itemsize + rb) + nw * 8) / t_w / 1e9,
+                               f"recipe write of {nw} tokens x {h} K rows"),
+                "decode": entry((n0 * h * 2 * rb + 2 * w.q[:1].size * w.q.itemsize) / t_d / 1e9,
+                                f"decode of sequence 0 ({n0} tokens) over K and V recipe pages")}
+        out["recipe_modes"] = rec
     return out
 
 
@@ -506,7 +542,11 @@ def run_gpu(args):
                          "tq_paged_prefill": prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream,
                                                              peak, peak_kind, world),
                          "qjl_residual_keys": qjl_measure(tq, w, dev, kraw, slots, ws_np, vp, bt, lens, q, signs, cv,
-                                                          flush, stream, peak, peak_kind, world)}
+                                                          flush, stream, peak, peak_kind, world),
+                         "int8q_prefill": int8q_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream, peak,
+                                                        peak_kind, world),
+                         "recipe_modes": recipe_measure(tq, w, dev, kraw, vraw, slots, ws_np, bt, lens, q, flush,
+                                                        stream, peak, peak_kind, world)}
 
     if not args.no_e2e:
         line["e2e"] = e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world)
@@ -581,6 +621,7 @@ def prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream, peak, 
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     for _ in range(2):
         tq.tq_paged_prefill(q, dq_seq, dq_len, kp, vp, bt, signs, ck, cv, out=out, workspace=ws, status=st)
+    launches0 = tq.tq_launch_count()
     times = []
     for i in range(steps):
         flush.fill_(i & 0xFF)
@@ -591,6 +632,7 @@ def prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream, peak, 
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
     tq.raise_for_device_status(st)
+    launches = tq.tq_launch_count() - launches0
     t_s = max_over_ranks([statistics.mean(times)], world, dev)[0] / 1e3
     rb = row_bytes(w.head_dim, w.k_bits) + row_bytes(w.head_dim, w.v_bits)
     unique = int(lens.sum()) * w.num_kv_heads * rb + 2 * rows * w.num_q_heads * w.head_dim * 2
@@ -603,7 +645,7 @@ def prefill_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream, peak, 
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "peak_source": peak_kind, "algorithmic_bytes_per_launch": unique,
                          "traffic": ncu_traffic("prefill")},
-            "gpu_launches": 2 * (steps + 2)}
+            "gpu_launches": launches}
 
 
 def qjl_measure(tq, w, dev, kraw, slots, slots_np, vp, bt, lens, q, signs, cv, flush, stream, peak, peak_kind,
@@ -641,6 +683,7 @@ def qjl_measure(tq, w, dev, kraw, slots, slots_np, vp, bt, lens, q, signs, cv, f
         tq.raise_for_device_status(st)
         return max_over_ranks([statistics.mean(times)], world, dev)[0] / 1e3
 
+    launches0 = tq.tq_launch_count()
     wr_s = timed(lambda: tq.tq_write_kv_prod(kraw, kpp, slots, signs, kmse, smat, status=st, check=False))
     dec_s = timed(lambda: tq.tq_paged_decode_prod(q, kpp, vp, bt, lens, signs, kmse, cv, smat, out=out, workspace=ws,
                                                   status=st))
@@ -656,7 +699,119 @@ def qjl_measure(tq, w, dev, kraw, slots, slots_np, vp, bt, lens, q, signs, cv, f
             "decode_us": dec_s * 1e6, "decode_gbs": dec_gbs, "decode_frac_of_hbm": dec_gbs / peak,
             "algorithmic_bytes": {"write": wr_bytes, "decode": dec_bytes}, "peak": peak, "peak_source": peak_kind,
             "kernels": "SIMT (write_prod_kernel; qjl_project_kernel + decode_prod_split_kernel + combine)",
-            "gpu_launches": 2 * (steps + 1) + 3 * (steps + 1)}
+            "gpu_launches": tq.tq_launch_count() - launches0}
+
+
+def recipe_measure(tq, w, dev, kraw, vraw, slots, slots_np, bt, lens, q, flush, stream, peak, peak_kind, world,
+                   steps=3):
+    """Recipe cache modes turboquant25 / turboquant35 on the workload's cache: the step's K and
+    V rows written as recipe rows (channel groups calibrated on the first 4096 tokens' K rows),
+    then the decode of the batch over them; each call timed apart with CUDA events, an L2
+    flush before each."""
+    import torch
+
+    d = w.head_dim
+    if d not in (64, 128):
+        return {"skipped": f"recipe kernels take head_dim 64/128 (D{d})"}
+    out = {}
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = torch.empty_like(q)
+
+    def timed(fn):
+        fn()
+        times = []
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        tq.raise_for_device_status(st)
+        return max_over_ranks([statistics.mean(times)], world, dev)[0] / 1e3
+
+    for recipe in ("turboquant25", "turboquant35"):
+        codec = tq.RecipeCodec(recipe, d, dev)
+        high = tq.tq_recipe_calibrate(recipe, kraw[:4096].float().cpu())
+        order = tq.tq_recipe_channel_order(recipe, d, high).to(dev)
+        kp = torch.zeros(w.num_blocks, w.block_size, w.num_kv_heads, codec.row_bytes, dtype=torch.uint8, device=dev)
+        vp = torch.zeros_like(kp)
+        tq.tq_write_kv_recipe(vraw, vp, slots, order, codec, status=st, check=False)
+        need = int(tq.lib().tq_paged_decode_recipe_workspace(w.batch, w.num_q_heads, w.num_kv_heads, d, bt.shape[1],
+                                                             w.block_size))
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        launches0 = tq.tq_launch_count()
+        wr_s = timed(lambda: tq.tq_write_kv_recipe(kraw, kp, slots, order, codec, status=st, check=False))
+        dec_s = timed(lambda: tq.tq_paged_decode_recipe(q, kp, vp, bt, lens, order, codec, out=res, workspace=ws,
+                                                        status=st))
+        launches = tq.tq_launch_count() - launches0
+        rows = int((slots_np >= 0).sum()) * w.num_kv_heads
+        wr_bytes = kraw.numel() * kraw.element_size() + rows * codec.row_bytes + slots_np.size * 8
+        dec_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * 2 * codec.row_bytes + \
+            2 * q.numel() * q.element_size()
+        wr_gbs, dec_gbs = wr_bytes / wr_s / 1e9, dec_bytes / dec_s / 1e9
+        out[recipe] = {"row_bytes": codec.row_bytes, "write_us": wr_s * 1e6,
+                       "write_rows_per_s": weak_scaling_rate(world, rows, wr_s), "write_gbs": wr_gbs,
+                       "write_frac_of_hbm": wr_gbs / peak, "decode_us": dec_s * 1e6, "decode_gbs": dec_gbs,
+                       "decode_frac_of_hbm": dec_gbs / peak,
+                       "algorithmic_bytes": {"write": wr_bytes, "decode": dec_bytes}, "gpu_launches": launches}
+    out.update({"workload": f"the step's {int((slots_np >= 0).sum()) * w.num_kv_heads} K rows (and V rows, untimed) "
+                            f"as recipe rows at D{d}, then the decode of the {w.batch} sequences over K and V recipe "
+                            "pages", "peak": peak, "peak_source": peak_kind,
+                "kernels": "SIMT (write_recipe_kernel; recipe_project_kernel + decode_recipe_split_kernel + "
+                           "combine_recipe_kernel)"})
+    return out
+
+
+def int8q_measure(tq, w, dev, kp, vp, bt, signs, ck, cv, flush, stream, peak, peak_kind, world, chunk=16, steps=5):
+    """The INT8-query prefill on the prefill chunk of prefill_measure: the queries quantised to
+    int8 codes and scales once (untimed), then tq_paged_prefill_int8q timed with CUDA events,
+    an L2 flush before each call."""
+    import torch
+
+    lens = w.seq_lens.astype(np.int64)
+    q_seq = np.repeat(np.arange(w.batch, dtype=np.int32), chunk)
+    q_len = (np.repeat(lens, chunk) - chunk + 1 + np.tile(np.arange(chunk), w.batch)).astype(np.int32)
+    rows = len(q_seq)
+    gen = torch.Generator().manual_seed(7)
+    q = torch.randn(rows, w.num_q_heads, w.head_dim, generator=gen).to(torch.float16).to(dev)
+    codes, scales = tq.tq_quantize_queries_int8(q)
+    dq_seq, dq_len = torch.from_numpy(q_seq).to(dev), torch.from_numpy(q_len).to(dev)
+    out = torch.empty_like(q)
+    need = int(tq.lib().tq_paged_prefill_workspace(rows, w.num_q_heads, w.num_kv_heads, w.head_dim, bt.shape[1],
+                                                  w.block_size))
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        tq.tq_paged_prefill_int8q(codes, scales, dq_seq, dq_len, kp, vp, bt, signs, ck, cv, out=out, workspace=ws,
+                                  status=st)
+
+    for _ in range(2):
+        call()
+    launches0 = tq.tq_launch_count()
+    times = []
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    tq.raise_for_device_status(st)
+    launches = tq.tq_launch_count() - launches0
+    t_s = max_over_ranks([statistics.mean(times)], world, dev)[0] / 1e3
+    rb = row_bytes(w.head_dim, w.k_bits) + row_bytes(w.head_dim, w.v_bits)
+    unique = int(lens.sum()) * w.num_kv_heads * rb + codes.numel() + scales.numel() * 4 + out.numel() * 2
+    gbs = unique / t_s / 1e9
+    return {"workload": f"{rows} int8 query rows (one scale per row and q head): the last {chunk} tokens of each of "
+                        f"the {w.batch} sequences, each over its causal prefix",
+            "us": t_s * 1e6, "rows_per_s": weak_scaling_rate(world, rows, t_s),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": unique, "traffic": None},
+            "gpu_launches": launches}
 
 
 def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5, chunks=8):

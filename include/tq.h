@@ -16,7 +16,9 @@
  *
  *   tq_paged_decode_static  the decode without a caller workspace (fixed scratch).
  *   tq_paged_prefill        mixed prefill/decode: query rows of one sequence share each
- *                           dequantised key/value tile ("vLLM Usage", Runtime Dispatch).
+ *                           dequantised key/value tile ("vLLM Usage", Runtime Dispatch);
+ *                           tq_paged_prefill_int8q takes int8 query codes and scales
+ *                           (tq_quantize_queries_int8 makes them).
  *   tq_dequant_rows         dense readback of packed rows ("vLLM Reference Audit",
  *                           tq4_decompress).
  *   tq_write_kv_prod,       product-quantised ("QJL residual") key rows and the decode
@@ -38,7 +40,7 @@
  *     ids, sequence lengths) are reported through `status_dev`, a device int32 the
  *     caller reads after the stream reaches it: 0 = OK, otherwise a tq_status code
  *     (the largest one when several kinds occur).  No kernel traps or asserts.
- *   - Geometry: head_dim D is a power of two in [32, 256]; bits b in {2, 3, 4, 5};
+ *   - Geometry: head_dim D is a power of two in [16, 256]; bits b in {2, 3, 4, 5};
  *     row_bytes RB(D, b) = ceil(D*b/8) + 4.  A page tensor is
  *     uint8[num_blocks][block_size][num_kv_heads][RB], contiguous, no padding, one
  *     tensor per component (K and V are independent and may use different bits).
@@ -220,6 +222,29 @@ tq_status tq_paged_prefill(const void* q, tq_dtype q_dtype, int num_q_rows, int 
                            tq_dtype out_dtype, void* workspace, size_t workspace_bytes, int32_t* status_dev,
                            void* stream);
 
+/* INT8-query prefill ("vLLM Usage", Runtime Dispatch: cache plus the INT8 prefill gate
+ * takes the int8 query path; "vLLM Reference Audit", File Map: INT8-Q prefill, int8 query
+ * scale over packed pages).  The pages give no quantiser; the reading: one symmetric scale
+ * per (query row, q head), s = amax / 127, code = round-half-even(q / s) in [-127, 127],
+ * both divisions correctly rounded fp32; a zero row has s = 0 and codes 0.
+ *
+ * tq_quantize_queries_int8: q device q_dtype [num_q_rows][num_q_heads][head_dim] ->
+ *   q_codes device int8 [num_q_rows][num_q_heads][head_dim] and q_scales device float
+ *   [num_q_rows][num_q_heads].  Asynchronous; errors TQ_ERR_INVALID_ARG / UNSUPPORTED.
+ * tq_paged_prefill_int8q: tq_paged_prefill with int8 query codes and their scales in place
+ *   of q / q_dtype: row i attends with the query q_scales[i][h] * q_codes[i][h][:] (the
+ *   kernels take the codes and scales as they are; out_dtype gives the output type).  The
+ *   workspace is tq_paged_prefill_workspace's. */
+tq_status tq_quantize_queries_int8(const void* q, tq_dtype q_dtype, int64_t num_q_rows, int num_q_heads, int head_dim,
+                                   int8_t* q_codes, float* q_scales, void* stream);
+tq_status tq_paged_prefill_int8q(const int8_t* q_codes, const float* q_scales, int num_q_rows, int num_q_heads,
+                                 int num_kv_heads, int head_dim, const uint8_t* k_pages, int k_bits,
+                                 const uint8_t* v_pages, int v_bits, int64_t num_blocks, int block_size,
+                                 const int32_t* block_table, int num_seqs, int max_blocks_per_seq, const int32_t* q_seq,
+                                 const int32_t* q_len, const float* signs, const float* k_centroids,
+                                 const float* v_centroids, float scale, void* out, tq_dtype out_dtype, void* workspace,
+                                 size_t workspace_bytes, int32_t* status_dev, void* stream);
+
 /* Dense readback of packed rows: the inverse addressing of tq_write_kv ("vLLM Reference
  * Audit", file map: tq4_decompress, the TQ4 unpack kernel for diagnostic readback of
  * packed index bytes and norms; "Architecture", Diagnostic vs Serving Paths: dense
@@ -292,7 +317,7 @@ tq_status tq_paged_decode_static(const void* q, tq_dtype q_dtype, int batch, int
  * N(0, 1) numbers (tq_build_qjl_matrix).  Values keep the MSE rows of tq_write_kv.
  * --------------------------------------------------------------------------------- */
 
-/* RBP(head_dim, bits); -1 when head_dim is not a power of two in [32, 256] or bits is
+/* RBP(head_dim, bits); -1 when head_dim is not a power of two in [16, 256] or bits is
  * outside 2..5. */
 int64_t tq_prod_row_bytes(int head_dim, int bits);
 

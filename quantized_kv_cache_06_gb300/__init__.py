@@ -30,7 +30,9 @@ from ._lib import (  # noqa: F401
     tq_paged_decode_static,
     tq_paged_decode_workspace,
     tq_paged_prefill,
+    tq_paged_prefill_int8q,
     tq_prod_row_bytes,
+    tq_quantize_queries_int8,
     tq_recipe_calibrate,
     tq_recipe_channel_order,
     tq_recipe_row_bytes,

@@ -74,6 +74,10 @@ SIGNATURES = {
     "tq_paged_decode_prod": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
                                       _c_i64, _c_int, _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p,
                                       _c_int, _c_p, _c_sz, _c_p, _c_p]),
+    "tq_quantize_queries_int8": (_c_int, [_c_p, _c_int, _c_i64, _c_int, _c_int, _c_p, _c_p, _c_p]),
+    "tq_paged_prefill_int8q": (_c_int, [_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
+                                        _c_i64, _c_int, _c_p, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_f,
+                                        _c_p, _c_int, _c_p, _c_sz, _c_p, _c_p]),
     "tq_recipe_row_bytes": (_c_i64, [_c_int, _c_int]),
     "tq_recipe_channel_order": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p]),
     "tq_recipe_calibrate": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_i64, _c_p]),
@@ -381,6 +385,63 @@ def tq_paged_prefill(q: torch.Tensor, q_seq: torch.Tensor, q_len: torch.Tensor, 
                                       _ptr(k_centroids), _ptr(v_centroids), float(scale or 0.0), _ptr(out),
                                       _DTYPES[out.dtype], _ptr(workspace), workspace.numel(), _ptr(status),
                                       _stream(dev)))
+    if check and status is not None:
+        raise_for_device_status(status)
+    return out
+
+
+def tq_quantize_queries_int8(q: torch.Tensor):
+    """int8 codes [T, Hq, D] and fp32 scales [T, Hq] of queries q[T, Hq, D] (one symmetric
+    scale per (row, q head))."""
+    dev = _need_cuda("tq_quantize_queries_int8", q)
+    if q.dim() != 3 or q.dtype not in _DTYPES or not q.is_contiguous():
+        raise ValueError("tq_quantize_queries_int8: contiguous q [T, Hq, D] f32/f16/bf16 expected")
+    t, hq, d = q.shape
+    codes = torch.empty((t, hq, d), dtype=torch.int8, device=dev)
+    scales = torch.empty((t, hq), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_quantize_queries_int8(_ptr(q), _DTYPES[q.dtype], t, hq, d, _ptr(codes), _ptr(scales),
+                                              _stream(dev)))
+    return codes, scales
+
+
+def tq_paged_prefill_int8q(q_codes: torch.Tensor, q_scales: torch.Tensor, q_seq: torch.Tensor, q_len: torch.Tensor,
+                           k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                           signs: torch.Tensor, k_centroids: torch.Tensor, v_centroids: torch.Tensor,
+                           scale: float | None = None, out: torch.Tensor | None = None,
+                           out_dtype: torch.dtype = torch.float16, workspace: torch.Tensor | None = None,
+                           status: torch.Tensor | None = None, check: bool = False) -> torch.Tensor:
+    """tq_paged_prefill with int8 query codes [T, Hq, D] and their fp32 scales [T, Hq]."""
+    dev = _need_cuda("tq_paged_prefill_int8q", q_codes, q_scales, q_seq, q_len, k_pages, v_pages, block_table, signs,
+                     k_centroids, v_centroids)
+    if q_codes.dim() != 3 or q_codes.dtype != torch.int8 or q_scales.dtype != torch.float32 or \
+            tuple(q_scales.shape) != tuple(q_codes.shape[:2]) or not q_codes.is_contiguous() or \
+            not q_scales.is_contiguous():
+        raise ValueError("tq_paged_prefill_int8q: contiguous int8 codes [T, Hq, D] and float32 scales [T, Hq] "
+                         "expected")
+    if block_table.dtype != torch.int32 or q_seq.dtype != torch.int32 or q_len.dtype != torch.int32:
+        raise ValueError("tq_paged_prefill_int8q: block_table / q_seq / q_len int32 expected")
+    t, hq, d = q_codes.shape
+    nb, bs, h, _ = k_pages.shape
+    kb, vb = _bits_from_centroids(k_centroids), _bits_from_centroids(v_centroids)
+    _need_f32("tq_paged_prefill_int8q", d, signs, k_centroids, v_centroids)
+    if k_pages.shape[3] != tq_row_bytes(d, kb) or v_pages.shape[3] != tq_row_bytes(d, vb) or \
+            tuple(v_pages.shape[:3]) != (nb, bs, h) or q_seq.numel() != t or q_len.numel() != t:
+        raise ValueError("tq_paged_prefill_int8q: page / row shapes inconsistent with q and the codebooks")
+    if out is None:
+        out = torch.empty((t, hq, d), dtype=out_dtype, device=dev)
+    _need_out("tq_paged_prefill_int8q", out, (t, hq, d), dev)
+    _need_status("tq_paged_prefill_int8q", status, dev)
+    s_rows, maxb = block_table.shape
+    need = int(lib().tq_paged_prefill_workspace(t, hq, h, d, maxb, bs))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().tq_paged_prefill_int8q(_ptr(q_codes), _ptr(q_scales), t, hq, h, d, _ptr(k_pages), kb,
+                                            _ptr(v_pages), vb, nb, bs, _ptr(block_table), s_rows, maxb, _ptr(q_seq),
+                                            _ptr(q_len), _ptr(signs), _ptr(k_centroids), _ptr(v_centroids),
+                                            float(scale or 0.0), _ptr(out), _DTYPES[out.dtype], _ptr(workspace),
+                                            workspace.numel(), _ptr(status), _stream(dev)))
     if check and status is not None:
         raise_for_device_status(status)
     return out

@@ -42,7 +42,7 @@ tq_status ok() {
   return TQ_OK;
 }
 
-bool pow2_dim_ok(int d) { return d >= 32 && d <= 256 && (d & (d - 1)) == 0; }
+bool pow2_dim_ok(int d) { return d >= 16 && d <= 256 && (d & (d - 1)) == 0; }
 bool bits_ok(int b) { return b >= 2 && b <= 5; }
 bool dtype_ok(int t) { return t == TQ_F32 || t == TQ_F16 || t == TQ_BF16; }
 size_t dtype_size(int t) { return t == TQ_F32 ? 4 : 2; }
@@ -220,7 +220,7 @@ tq_status decode_shape_check(int batch, int num_q_heads, int num_kv_heads, int h
                 batch, num_q_heads, num_kv_heads, max_blocks_per_seq, block_size);
   if (num_q_heads % num_kv_heads != 0)
     return fail(TQ_ERR_INVALID_ARG, "decode: num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads, num_kv_heads);
-  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [16, 256]", head_dim);
   const int g = num_q_heads / num_kv_heads;
   if (g != 1 && g != 2 && g != 4 && g != 8)
     return fail(TQ_ERR_UNSUPPORTED, "decode: GQA group %d not supported (1, 2, 4 or 8)", g);
@@ -257,17 +257,20 @@ tq_status decode_impl(const char* name, const void* q, tq_dtype q_dtype, int bat
                           const int32_t* seq_lens, const float* signs, const float* k_centroids,
                           const float* v_centroids, float scale, void* out, tq_dtype out_dtype,
                           void* workspace, size_t workspace_bytes, int32_t* status_dev,
-                          void* stream, const int32_t* bt_rows, int bt_num_rows) {
+                          void* stream, const int32_t* bt_rows, int bt_num_rows, const float* q_scale = nullptr) {
   tq_status st = decode_shape_check(batch, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size);
   if (st != TQ_OK) return st;
   if (!bits_ok(k_bits) || !bits_ok(v_bits))
     return fail(TQ_ERR_UNSUPPORTED, "k_bits %d / v_bits %d: must be 2, 3, 4 or 5", k_bits, v_bits);
-  if (!dtype_ok(q_dtype) || !dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "%s: unknown dtype", name);
+  // int8 query codes (q_dtype 3) only come with their scales, from tq_paged_prefill_int8q
+  const bool int8q = q_scale != nullptr && (int)q_dtype == tq::kI8;
+  if ((!dtype_ok(q_dtype) && !int8q) || !dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "%s: unknown dtype", name);
   if (num_blocks < 0) return fail(TQ_ERR_INVALID_ARG, "%s: num_blocks < 0", name);
   if (batch > 0 && (!q || !k_pages || !v_pages || !seq_lens || !signs || !k_centroids || !v_centroids || !out ||
                     (max_blocks_per_seq > 0 && !block_table)))
     return fail(TQ_ERR_INVALID_ARG, "%s: null pointer argument", name);
-  if (batch > 0 && (!aligned(q, dtype_size(q_dtype)) || !aligned(out, dtype_size(out_dtype)) ||
+  if (batch > 0 && int8q && !aligned(q_scale, 4)) return fail(TQ_ERR_INVALID_ARG, "%s: misaligned q_scales", name);
+  if (batch > 0 && (!aligned(q, int8q ? 1 : dtype_size(q_dtype)) || !aligned(out, dtype_size(out_dtype)) ||
                     !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(block_table, 4) ||
                     !aligned(seq_lens, 4)))
     return fail(TQ_ERR_INVALID_ARG, "%s: misaligned pointer (pages need 16-byte alignment)", name);
@@ -293,6 +296,7 @@ tq_status decode_impl(const char* name, const void* q, tq_dtype q_dtype, int bat
   a.k_alpha = 1.0f;
   a.bt_rows = bt_rows;
   a.bt_num_rows = bt_num_rows;
+  a.q_scale = int8q ? q_scale : nullptr;
   if (batch > 0 && (tq::tc_decode_supported(a) || tq::prefill_mq_supported(a))) {
     a.v_alpha = fp16_scale_for(head_dim, v_bits);
     a.k_alpha = fp16_scale_for(head_dim, k_bits);
@@ -305,7 +309,14 @@ tq_status decode_impl(const char* name, const void* q, tq_dtype q_dtype, int bat
                   plan.workspace_bytes, workspace_bytes);
     return check_cuda(tq::launch_prefill_mq(a, plan, static_cast<cudaStream_t>(stream)), name);
   }
-  const tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());
+  tq::DecodePlan plan = tq::plan_decode(a, current_device_sms());
+  if (int8q && plan.kernel != 1) {
+    // int8 query codes are read by the multi-query kernel (taken above for every shape it
+    // covers) and the SIMT kernels; any other shape runs the SIMT plan
+    tq::DecodeArgs s = a;
+    s.k_bits = s.v_bits = 0;
+    plan = tq::plan_decode(s, current_device_sms());
+  }
   if (batch > 0 && (workspace_bytes < plan.workspace_bytes || !workspace || !aligned(workspace, 16)))
     return fail(TQ_ERR_INVALID_ARG, "%s: workspace must be >= %zu bytes and 16-byte aligned (got %zu)", name,
                 plan.workspace_bytes, workspace_bytes);
@@ -372,7 +383,7 @@ int64_t tq_row_bytes(int head_dim, int bits) {
 
 tq_status tq_build_rotation(int head_dim, uint64_t seed, float* signs_host) {
   if (!signs_host) return fail(TQ_ERR_INVALID_ARG, "tq_build_rotation: signs_host is NULL");
-  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [16, 256]", head_dim);
   uint64_t state = seed;
   for (int i = 0; i < head_dim; ++i) {
     state += 0x9E3779B97F4A7C15ull;  // splitmix64 (Steele, Lea & Flood 2014)
@@ -387,7 +398,7 @@ tq_status tq_build_rotation(int head_dim, uint64_t seed, float* signs_host) {
 
 tq_status tq_codebook(int head_dim, int bits, float* centroids_host, float* boundaries_host) {
   if (!centroids_host) return fail(TQ_ERR_INVALID_ARG, "tq_codebook: centroids_host is NULL");
-  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [16, 256]", head_dim);
   // 1 bit: the MSE part of the 2-bit groups of the recipe rows
   if (bits < 1 || bits > 5) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 1 .. 5", bits);
   const std::vector<float>& c = codebook_f32(head_dim, bits);
@@ -405,7 +416,7 @@ tq_status tq_write_kv(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, i
   if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 0 || block_size < 1)
     return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: invalid sizes (tokens=%lld, kv_heads=%d, blocks=%lld, block_size=%d)",
                 (long long)num_tokens, num_kv_heads, (long long)num_blocks, block_size);
-  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [16, 256]", head_dim);
   if (!bits_ok(bits)) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 2, 3, 4 or 5", bits);
   if (!dtype_ok(raw_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_write_kv: unknown raw dtype %d", (int)raw_dtype);
   if (num_tokens > 0 && (!raw || !slots || !pages || !signs || !centroids))
@@ -431,7 +442,7 @@ tq_status tq_dequant_rows(const uint8_t* pages, int bits, int64_t num_blocks, in
   if (num_tokens < 0 || num_kv_heads < 1 || num_blocks < 0 || block_size < 1)
     return fail(TQ_ERR_INVALID_ARG, "tq_dequant_rows: invalid sizes (tokens=%lld, kv_heads=%d, blocks=%lld, block_size=%d)",
                 (long long)num_tokens, num_kv_heads, (long long)num_blocks, block_size);
-  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [16, 256]", head_dim);
   if (!bits_ok(bits)) return fail(TQ_ERR_UNSUPPORTED, "bits %d: must be 2, 3, 4 or 5", bits);
   if (!dtype_ok(out_dtype)) return fail(TQ_ERR_INVALID_ARG, "tq_dequant_rows: unknown out dtype %d", (int)out_dtype);
   if (num_tokens > 0 && (!pages || !slots || !signs || !centroids || !out))
@@ -502,6 +513,40 @@ tq_status tq_paged_prefill(const void* q, tq_dtype q_dtype, int num_q_rows, int 
                      q_seq, num_seqs);
 }
 
+tq_status tq_quantize_queries_int8(const void* q, tq_dtype q_dtype, int64_t num_q_rows, int num_q_heads, int head_dim,
+                                   int8_t* q_codes, float* q_scales, void* stream) {
+  const char* name = "tq_quantize_queries_int8";
+  if (num_q_rows < 0 || num_q_heads < 1) return fail(TQ_ERR_INVALID_ARG, "%s: invalid sizes", name);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [16, 256]", head_dim);
+  if (!dtype_ok(q_dtype)) return fail(TQ_ERR_INVALID_ARG, "%s: unknown dtype %d", name, (int)q_dtype);
+  if (num_q_rows > 0 && (!q || !q_codes || !q_scales)) return fail(TQ_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  if (num_q_rows > 0 && (!aligned(q, dtype_size(q_dtype)) || !aligned(q_scales, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: misaligned pointer", name);
+  return check_cuda(tq::launch_quantize_queries(q, (int)q_dtype, num_q_rows * num_q_heads, head_dim, q_codes, q_scales,
+                                                static_cast<cudaStream_t>(stream)),
+                    name);
+}
+
+tq_status tq_paged_prefill_int8q(const int8_t* q_codes, const float* q_scales, int num_q_rows, int num_q_heads,
+                                 int num_kv_heads, int head_dim, const uint8_t* k_pages, int k_bits,
+                                 const uint8_t* v_pages, int v_bits, int64_t num_blocks, int block_size,
+                                 const int32_t* block_table, int num_seqs, int max_blocks_per_seq, const int32_t* q_seq,
+                                 const int32_t* q_len, const float* signs, const float* k_centroids,
+                                 const float* v_centroids, float scale, void* out, tq_dtype out_dtype, void* workspace,
+                                 size_t workspace_bytes, int32_t* status_dev, void* stream) {
+  const char* name = "tq_paged_prefill_int8q";
+  if (num_seqs < 0) return fail(TQ_ERR_INVALID_ARG, "%s: num_seqs < 0", name);
+  if (num_q_rows > 0 && (!q_seq || !q_len || !aligned(q_seq, 4) || !aligned(q_len, 4)))
+    return fail(TQ_ERR_INVALID_ARG, "%s: q_seq and q_len must be non-null, 4-byte aligned", name);
+  if (num_q_rows > 0 && !q_scales) return fail(TQ_ERR_INVALID_ARG, "%s: q_scales is NULL", name);
+  // a non-null scale array marks the int8 codes (an empty batch needs none)
+  static const float kNoRows = 0.f;
+  return decode_impl(name, q_codes, (tq_dtype)tq::kI8, num_q_rows, num_q_heads, num_kv_heads, head_dim, k_pages,
+                     k_bits, v_pages, v_bits, num_blocks, block_size, block_table, max_blocks_per_seq, q_len, signs,
+                     k_centroids, v_centroids, scale, out, out_dtype, workspace, workspace_bytes, status_dev, stream,
+                     q_seq, num_seqs, q_scales ? q_scales : &kNoRows);
+}
+
 tq_status tq_paged_decode_static(const void* q, tq_dtype q_dtype, int batch, int num_q_heads,
                                  int num_kv_heads, int head_dim, const uint8_t* k_pages, int k_bits,
                                  const uint8_t* v_pages, int v_bits, int64_t num_blocks, int block_size,
@@ -538,7 +583,7 @@ int64_t tq_prod_row_bytes(int head_dim, int bits) {
 
 tq_status tq_build_qjl_matrix(int head_dim, uint64_t seed, float* s_host) {
   if (!s_host) return fail(TQ_ERR_INVALID_ARG, "tq_build_qjl_matrix: s_host is NULL");
-  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [32, 256]", head_dim);
+  if (!pow2_dim_ok(head_dim)) return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: must be a power of two in [16, 256]", head_dim);
   // splitmix64 (Steele, Lea & Flood 2014), outputs in pairs through Box-Muller (1958)
   uint64_t state = seed;
   auto next = [&state]() {

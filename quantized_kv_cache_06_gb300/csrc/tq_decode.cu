@@ -73,9 +73,11 @@ decode_split_kernel(DecodeArgs a, int num_splits, int blocks_per_split, SplitVie
   float qr[G][E];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    const int64_t base = ((int64_t)b * a.num_q_heads + (int64_t)h * G + g) * D + lane * E;
+    const int64_t qrow = (int64_t)b * a.num_q_heads + (int64_t)h * G + g;  // (row, q head)
+    const int64_t base = qrow * D + lane * E;
 #pragma unroll
-    for (int i = 0; i < E; ++i) qr[g][i] = load_as_f32(a.q, base + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
+    for (int i = 0; i < E; ++i)
+      qr[g][i] = load_query_f32(a.q, a.q_scale, qrow, base + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
     fwht_warp<E>(qr[g]);
 #pragma unroll
     for (int i = 0; i < E; ++i) qr[g][i] *= qmul;
@@ -303,6 +305,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, cudaStream_t
   if (a.batch == 0) return cudaSuccess;
   if (p.kernel == 2) return launch_decode_tc(a, p, stream);
   if (p.kernel == 3) return launch_prefill_mq(a, p.mq, stream);
+  if (a.head_dim == 16) return launch_decode_d16(a, stream);
   SplitView part = split_view(a.workspace, a.batch, a.num_q_heads, p.num_splits, a.head_dim);
   switch (a.head_dim) {
     case 32: return launch_split<1>(a, p, part, stream);

@@ -32,15 +32,15 @@
 // alpha chosen on the host so that alpha * c lands near fp16 grid points; 1/alpha is
 // applied when the partial is written.
 //
-// Value frame.  The value weight p * nu_v has no bound (nu_v is the norm of an arbitrary
-// raw row), so it is not rounded to fp16 as it stands.  Each q head keeps a second,
-// lazily moved exponent mv next to the score max m: the value accumulator holds
-// sum_t 2^(s_t - mv) nu_v,t c[idx_v,t], and P' = p * 2^(m - mv) * nu_v.  mv is raised
-// whenever a tile's bound on P' would pass the fp16 range (then to the tile's largest
-// s_t + log2 nu_v,t), and never falls more than kFrameGap below m, so P' stays inside the
-// fp16 range for every finite norm and keeps fp16's relative precision for the terms
-// that matter.  The partial is converted back to the score frame (times 2^(mv - m)) when
-// it is written, so the combine pass is unchanged.
+// Large norms.  Nothing bounds a row's norm (the writer takes any raw row), so tiles whose
+// largest value norm passes kFastValueNorm take an exact path: the value weights
+// P' = p * nu_v of each q head are scaled by a power of two that puts their largest near
+// 2^12 (the accumulators scaled by the same power before the tile and back after it, both
+// exact), then split into fp16 hi + lo, with the value table entries split the same way:
+// V_hi P'_hi + V_lo P'_hi + V_hi P'_lo carries ~22 significant bits for every weight the
+// output can feel.  Such tiles also take the exact key path (the error of the hi-only key
+// scores, ~1e-3 of p at the fast bound, would otherwise be multiplied by the large norm).
+// Other tiles have P' <= 2^kRescaleSlack * kFastValueNorm = 2048, well inside fp16.
 //
 // Softmax: online, base 2 (log2 e folded into the query), per q head.  Rows of tokens
 // past the sequence end are masked (score -inf, value norm 0: their bytes are stale);
@@ -133,12 +133,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
-// log2(x) with the hardware approximation (log2(0) = -inf); used only to place the
-// value frame, where an error of a few ulps moves nothing that matters.
-__device__ __forceinline__ float fast_log2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
+// Power-of-two scale (and its inverse) that brings a positive x to [2^11, 2^12): both
+// exact; 1 and 1 for x = 0 or subnormal (nothing there that could reach the output).
+__device__ __forceinline__ void tile_scale(float x, float& f, float& inv_f) {
+  int e = (int)((__float_as_uint(x) >> 23) & 0xffu);  // biased exponent of x (x >= 0)
+  if (e == 0) {
+    f = inv_f = 1.f;
+    return;
+  }
+  e = max(12, e);  // x < 2^-115: clamp, its terms are far below anything the output feels
+  f = __uint_as_float((uint32_t)(265 - e) << 23);   // 2^(138 - e)
+  inv_f = __uint_as_float((uint32_t)(e - 11) << 23);  // 2^(e - 138)
 }
 
 // D = A * B + D, m16n8k16, A row-major f16, B col-major f16, f32 accumulators.
@@ -156,10 +161,16 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Split x into fp16 hi + fp16 lo (x ~= hi + lo to ~22 significant bits).
+// Split x into fp16 hi + fp16 lo with the remainder scaled by 2^kLoShift:
+// x ~= hi + lo * 2^-kLoShift to ~22 significant bits.  (The remainder of a value below 1/4
+// would fall into fp16's subnormal range, where only 2^-25 of absolute precision is left;
+// the products with lo parts are multiplied by 2^-kLoShift when they are summed, exactly.)
+constexpr int kLoShift = 12;
+constexpr float kLoScale = 4096.0f;        // 2^kLoShift
+constexpr float kLoUnscale = 1.0f / 4096;  // 2^-kLoShift
 __device__ __forceinline__ void split_half(float x, __half& hi, __half& lo) {
   hi = __float2half_rn(x);
-  lo = __float2half_rn(x - __half2float(hi));
+  lo = __float2half_rn((x - __half2float(hi)) * kLoScale);
 }
 
 template <int D, int KB, int VB, int G, int WPH>
@@ -224,12 +235,6 @@ constexpr int kOffVL = kOffL + 256 * 4;                     // byte V lo table, 
 constexpr int kMiscBytes = (kOffVL + 256 * 4 + 127) / 128 * 128;
 
 constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
-// Value frame (see the file comment): a tile whose largest nu_v * 2^(m - mv) passes
-// kValueBound raises the frame, so P' <= 2^kRescaleSlack * kValueBound = 2^15 (fp16 holds
-// 65504); the frame never lags the score max by more than kFrameGap log2 units (so
-// 2^(m - mv) <= 2^64 and p * 2^(m - mv) stays finite).
-constexpr float kValueBound = 512.0f;
-constexpr float kFrameGap = 64.0f;
 // Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored with the fp16-hi key part
 // only.  With the alpha scaling the hi part is within ~1e-4 relative of the fp32
 // centroid, so the score error of such a tile stays far below the output tolerance;
@@ -481,7 +486,6 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   float qnorm_max = 0.f;  // max over this warp's heads of ||rotated query|| (log2 units)
   float o_acc[Cfg::kNT][Cfg::kMTiles][4];
   float m_run[2], l_run[2], m_thr[2];  // running max, sum, and max + kRescaleSlack per head
-  float mv[2], fr[2];                  // value frame exponent and 2^(m_run - mv) per head
   int cur_b = -1;
 
   auto reset_state = [&]() {
@@ -493,8 +497,6 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         for (int e = 0; e < 4; ++e) o_acc[nt][i][e] = 0.f;
     m_run[0] = m_run[1] = m_thr[0] = m_thr[1] = -INFINITY;
     l_run[0] = l_run[1] = 0.f;
-    mv[0] = mv[1] = -INFINITY;
-    fr[0] = fr[1] = 0.f;
   };
   // Multiplies the value accumulators of each q head by its factor cv[e] (held by the
   // score-layout lanes: lane (r, c) has heads 2c, 2c+1; the value layout has head c + 4 nt).
@@ -588,15 +590,10 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   };
 
   const float inv_alpha = 1.0f / args.v_alpha;
-  // Writes this warp's partial for sequence b (empty when `empty`).  The value
-  // accumulators go back from the value frame to the score frame: times 2^(mv - m).
+  // Writes this warp's partial for sequence b (empty when `empty`).
   auto flush = [&](int b, bool empty) {
     const int64_t slot = (int64_t)cta + b;
     float lsum[2] = {l_run[0], l_run[1]};
-    float to_m[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-      to_m[e] = (empty || m_run[e] == -INFINITY || mv[e] == -INFINITY) ? 0.f : fast_exp2(mv[e] - m_run[e]) * inv_alpha;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       lsum[e] += __shfl_xor_sync(kFullMask, lsum[e], 4);
@@ -617,10 +614,6 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
     for (int nt = 0; nt < Cfg::kNT; ++nt) {  // value layout: q head c + 4 nt
       const int g = c + 4 * nt;
-      const int srcl = (g >> 1) & 3;
-      const float f0 = __shfl_sync(kFullMask, to_m[0], srcl);
-      const float f1 = __shfl_sync(kFullMask, to_m[1], srcl);
-      const float fg = (g & 1) ? f1 : f0;
       if (g < G) {
         float* acc = args.part_acc + (slot * a.num_q_heads + (int64_t)h * G + g) * D;
 #pragma unroll
@@ -630,8 +623,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
             const int q = 2 * i + half;
             const int pv = Cfg::kPWV * (r + 8 * (q / Cfg::kPWV)) + (q % Cfg::kPWV);
             float2 v;
-            v.x = fg == 0.f ? 0.f : o_acc[nt][i][2 * half] * fg;
-            v.y = fg == 0.f ? 0.f : o_acc[nt][i][2 * half + 1] * fg;
+            v.x = empty ? 0.f : o_acc[nt][i][2 * half] * inv_alpha;
+            v.y = empty ? 0.f : o_acc[nt][i][2 * half + 1] * inv_alpha;
             *reinterpret_cast<float2*>(acc + 2 * pv) = v;
           }
         }
@@ -671,12 +664,26 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       vn[t][1] = __uint_as_float(ld32(vbase[t] + (r + 8) * vts + Cfg::kWV * 4));
       kmax = fmaxf(kmax, fmaxf(fabsf(kn[t][0]), fabsf(kn[t][1])));
     }
+    // Rows past the sequence end hold stale bytes (a NaN norm, say): their value norm is 0
+    // before any arithmetic sees it (their scores are masked below).
+    if (ntok_last < kBS) {
+      if (r >= ntok_last) vn[NTL - 1][0] = 0.f;
+      if (r + 8 >= ntok_last) vn[NTL - 1][1] = 0.f;
+    }
+    float vmax = 0.f;
+#pragma unroll
+    for (int t = 0; t < NTL; ++t) vmax = fmaxf(vmax, fmaxf(vn[t][0], vn[t][1]));
     // Precision switch: tiles whose largest |score| bound nu_k * ||q|| stays within
     // kFastScoreBound take the fp16-hi key path (rounding error ~1e-4 relative after the
-    // alpha scaling); otherwise (large-norm rows) the fp16-lo key part is added as well.
-    // Rows past the sequence end hold stale bytes: at worst they select the exact path,
-    // which is correct for any tile.
-    const bool exact = __any_sync(kFullMask, kmax * qnorm_max > kFastScoreBound);
+    // alpha scaling); otherwise (large-norm rows), and in every exact-value tile, the
+    // fp16-lo key part is added as well.  Stale rows past the sequence end can only select
+    // the exact path, which is correct for any tile.  One vote in the common case.
+    const bool pv = vmax > kFastValueNorm;
+    bool exact = false, exact_v = false;
+    if (__any_sync(kFullMask, pv || kmax * qnorm_max > kFastScoreBound)) {
+      exact = true;
+      exact_v = __any_sync(kFullMask, pv);
+    }
     float sacc[NTL][4];
 #pragma unroll
     for (int t = 0; t < NTL; ++t)
@@ -714,10 +721,12 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
           }
         }
       }
+      // G = 8: sacc1 holds key_hi * q_lo (q_lo scaled by 2^12); G = 4: the odd k-steps, same
+      // column scales as sacc
 #pragma unroll
       for (int t = 0; t < NTL; ++t)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[t][e] += sacc1[t][e];
+        for (int e = 0; e < 4; ++e) sacc[t][e] = G == 8 ? fmaf(sacc1[t][e], kLoUnscale, sacc[t][e]) : sacc[t][e] + sacc1[t][e];
     } else {
       // adds key_lo * q_hi (G = 4: key_lo * [q_hi | q_lo])
 #pragma unroll
@@ -737,17 +746,19 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
             mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
           }
         }
+        // sacc1 (key_hi * q_lo) and sacc2 (key_lo * q) each carry one 2^12 scale
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[t][e] += sacc1[e] + sacc2[e];
+        for (int e = 0; e < 4; ++e) sacc[t][e] = fmaf(sacc1[e] + sacc2[e], kLoUnscale, sacc[t][e]);
       }
     }
     float sc[NTL][4];
 #pragma unroll
     for (int t = 0; t < NTL; ++t) {
       if (G == 4) {
-        // fold the q_lo columns (lanes c = 2, 3) onto the q_hi columns (lanes c = 0, 1)
+        // fold the q_lo columns (lanes c = 2, 3; q_lo scaled by 2^12) onto the q_hi columns
+        // (lanes c = 0, 1)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[t][e] += __shfl_xor_sync(kFullMask, sacc[t][e], 2);
+        for (int e = 0; e < 4; ++e) sacc[t][e] = fmaf(__shfl_xor_sync(kFullMask, sacc[t][e], 2), kLoUnscale, sacc[t][e]);
       }
       sc[t][0] = sacc[t][0] * kn[t][0];
       sc[t][1] = sacc[t][1] * kn[t][0];
@@ -755,15 +766,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       sc[t][3] = sacc[t][3] * kn[t][1];
     }
     if (ntok_last < kBS) {  // last block of a sequence: mask the rows past its end
-      // (their bytes are stale: the value norm may hold any bit pattern, NaN included)
-      if (r >= ntok_last) {
-        sc[NTL - 1][0] = sc[NTL - 1][1] = -INFINITY;
-        vn[NTL - 1][0] = 0.f;
-      }
-      if (r + 8 >= ntok_last) {
-        sc[NTL - 1][2] = sc[NTL - 1][3] = -INFINITY;
-        vn[NTL - 1][1] = 0.f;
-      }
+      if (r >= ntok_last) sc[NTL - 1][0] = sc[NTL - 1][1] = -INFINITY;
+      if (r + 8 >= ntok_last) sc[NTL - 1][2] = sc[NTL - 1][3] = -INFINITY;
     }
 
     // --- online softmax (q heads 2c, 2c+1 on this lane).  The running max only moves
@@ -777,9 +781,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       for (int t = 1; t < NTL; ++t) smax[e] = fmaxf(smax[e], fmaxf(sc[t][e], sc[t][2 + e]));
     }
     if (__any_sync(kFullMask, smax[0] > m_thr[0] || smax[1] > m_thr[1])) {
-      // the sums follow the score max; the value frame moves only when it would lag the
-      // score max by more than kFrameGap (always at the first tile of a sequence)
-      float cv[2];
+      float corr[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         float mt = smax[e];
@@ -787,50 +789,22 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
         const float mn = mt > m_thr[e] ? mt : m_run[e];
-        l_run[e] *= m_run[e] == mn ? 1.f : fast_exp2(m_run[e] - mn);
+        corr[e] = m_run[e] == mn ? 1.f : fast_exp2(m_run[e] - mn);
+        l_run[e] *= corr[e];
         m_run[e] = mn;
         m_thr[e] = mn + kRescaleSlack;
-        const float mvn = fmaxf(mv[e], mn - kFrameGap);
-        cv[e] = mvn == mv[e] ? 1.f : fast_exp2(mv[e] - mvn);
-        mv[e] = mvn;
-        fr[e] = mn == -INFINITY ? 0.f : fast_exp2(mn - mvn);
       }
-      if (__any_sync(kFullMask, cv[0] != 1.f || cv[1] != 1.f)) rescale_values(cv);
+      rescale_values(corr);
     }
-    // Value frame check, before any weight is formed: p <= 2^kRescaleSlack, so every P' of
-    // this tile is at most 2^6 * 2^(m - mv) * max nu_v.  Where that bound passes kValueBound
-    // (the first tile of a sequence, rows of very large norm) the frame of each head is
-    // raised to the tile's largest s_t + log2 nu_v,t (then every P' here is at most ~1).
-    float vmax = 0.f;
-#pragma unroll
-    for (int t = 0; t < NTL; ++t) vmax = fmaxf(vmax, fmaxf(vn[t][0], vn[t][1]));
-    if (__any_sync(kFullMask, vmax * fr[0] > kValueBound || vmax * fr[1] > kValueBound)) {
-      float cv[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float sv = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < NTL; ++t)
-          sv = fmaxf(sv, fmaxf(sc[t][e] + fast_log2(vn[t][0]), sc[t][2 + e] + fast_log2(vn[t][1])));
-        sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 4));
-        sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 8));
-        sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 16));
-        const float mvn = fmaxf(mv[e], sv);
-        cv[e] = mvn == mv[e] ? 1.f : fast_exp2(mv[e] - mvn);
-        mv[e] = mvn;
-        fr[e] = (m_run[e] == -INFINITY || mvn == -INFINITY) ? 0.f : fast_exp2(m_run[e] - mvn);
-      }
-      if (__any_sync(kFullMask, cv[0] != 1.f || cv[1] != 1.f)) rescale_values(cv);
-    }
-    float pvf[NTL][4];  // P' = p 2^(m - mv) nu_v: [t][e] token r, [t][2 + e] token r + 8 (heads 2c, 2c+1)
+    float pvf[NTL][4];  // P' = p nu_v: [t][e] token r, [t][2 + e] token r + 8 (heads 2c, 2c+1)
 #pragma unroll
     for (int t = 0; t < NTL; ++t) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float p0 = fast_exp2(sc[t][e] - m_run[e]), p1 = fast_exp2(sc[t][2 + e] - m_run[e]);
         l_run[e] += p0 + p1;
-        pvf[t][e] = (p0 * fr[e]) * vn[t][0];
-        pvf[t][2 + e] = (p1 * fr[e]) * vn[t][1];
+        pvf[t][e] = p0 * vn[t][0];
+        pvf[t][2 + e] = p1 * vn[t][1];
       }
     }
 
@@ -839,7 +813,9 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
     // table entries and of P'.
     auto values = [&](auto exv_tag) {
       constexpr bool EXV = decltype(exv_tag)::value;
-      uint32_t p01[NTL], p23[NTL], q01[NTL], q23[NTL];
+      // EXV: q = fp16 remainders of P' (P'_lo), u = P' 2^-12 (pairs with the V_lo entries,
+      // which carry 2^12)
+      uint32_t p01[NTL], p23[NTL], q01[NTL], q23[NTL], u01[NTL], u23[NTL];
 #pragma unroll
       for (int t = 0; t < NTL; ++t) {
         p01[t] = pack_half2(pvf[t][0], pvf[t][1]);  // token r:   heads 2c, 2c+1
@@ -849,6 +825,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
           const __half2 h23 = *reinterpret_cast<const __half2*>(&p23[t]);
           q01[t] = pack_half2(pvf[t][0] - __low2float(h01), pvf[t][1] - __high2float(h01));
           q23[t] = pack_half2(pvf[t][2] - __low2float(h23), pvf[t][3] - __high2float(h23));
+          u01[t] = pack_half2(pvf[t][0] * kLoUnscale, pvf[t][1] * kLoUnscale);
+          u23[t] = pack_half2(pvf[t][2] * kLoUnscale, pvf[t][3] * kLoUnscale);
         }
       }
 #pragma unroll
@@ -856,7 +834,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {  // tokens {c, c+4} (ks=0) and {c+8, c+12} (ks=1)
           const int t0 = c + 8 * ks, t1 = c + 4 + 8 * ks;
-          uint32_t bv[Cfg::kNT][2], bl[Cfg::kNT][2];
+          uint32_t bv[Cfg::kNT][2], bl[Cfg::kNT][2], bu[Cfg::kNT][2];
 #pragma unroll
           for (int nt = 0; nt < Cfg::kNT; ++nt) {
             const int cs = 2 * nt + (r >> 2);  // source lane column: q head (4 nt + r/2) / 2
@@ -871,6 +849,11 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
               const uint32_t y1 = __shfl_sync(kFullMask, srcl, 4 * (c + 4) + cs);
               bl[nt][0] = __byte_perm(y0, 0u, sel_b);
               bl[nt][1] = __byte_perm(y1, 0u, sel_b);
+              const uint32_t srcu = ks == 0 ? u01[t] : u23[t];
+              const uint32_t z0 = __shfl_sync(kFullMask, srcu, 4 * c + cs);
+              const uint32_t z1 = __shfl_sync(kFullMask, srcu, 4 * (c + 4) + cs);
+              bu[nt][0] = __byte_perm(z0, 0u, sel_b);
+              bu[nt][1] = __byte_perm(z1, 0u, sel_b);
             }
           }
 #pragma unroll
@@ -889,8 +872,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
                 const uint32_t l2 = v_lookup_lo(wb, e), l3 = v_lookup_lo(wb, e + 1);
 #pragma unroll
                 for (int nt = 0; nt < Cfg::kNT; ++nt) {
-                  mma16816(o_acc[nt][i], l0, l1, l2, l3, bv[nt][0], bv[nt][1]);
-                  mma16816(o_acc[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                  mma16816(o_acc[nt][i], l0, l1, l2, l3, bu[nt][0], bu[nt][1]);  // V_lo 2^12 * P' 2^-12
+                  mma16816(o_acc[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);  // V_hi * P'_lo
                 }
               }
             }
@@ -898,8 +881,31 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         }
       }
     };
-    if (__any_sync(kFullMask, vmax > kFastValueNorm)) values(std::true_type{});
-    else values(std::false_type{});
+    if (exact_v) {
+      // per q head, scale the weights so that the largest lands in [2^11, 2^12) and the
+      // accumulators by the same power of two, exactly; undone after the tile
+      float f[2], inv_f[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float pm = 0.f;
+#pragma unroll
+        for (int t = 0; t < NTL; ++t) pm = fmaxf(pm, fmaxf(pvf[t][e], pvf[t][2 + e]));
+        pm = fmaxf(pm, __shfl_xor_sync(kFullMask, pm, 4));
+        pm = fmaxf(pm, __shfl_xor_sync(kFullMask, pm, 8));
+        pm = fmaxf(pm, __shfl_xor_sync(kFullMask, pm, 16));
+        tile_scale(pm, f[e], inv_f[e]);
+#pragma unroll
+        for (int t = 0; t < NTL; ++t) {
+          pvf[t][e] *= f[e];
+          pvf[t][2 + e] *= f[e];
+        }
+      }
+      rescale_values(f);
+      values(std::true_type{});
+      rescale_values(inv_f);
+    } else {
+      values(std::false_type{});
+    }
   };
   using One = std::integral_constant<int, 1>;
   using Two = std::integral_constant<int, 2>;

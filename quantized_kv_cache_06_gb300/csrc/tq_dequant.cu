@@ -187,12 +187,13 @@ cudaError_t launch_dim(const DequantArgs& a, cudaStream_t stream, int grid) {
 }  // namespace
 
 bool dequant_supported(const DequantArgs& a) {
-  const bool dim = a.head_dim == 32 || a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256;
+  const bool dim = a.head_dim == 16 || a.head_dim == 32 || a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256;
   return dim && a.bits >= 2 && a.bits <= 5;
 }
 
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t stream, int num_sms) {
   if (a.num_tokens <= 0) return cudaSuccess;
+  if (a.head_dim == 16) return launch_dequant_d16(a, stream);
   const int64_t rows_per_warp = 32 / (a.head_dim / 32);
   const int64_t warps_wanted = (a.num_tokens * a.num_kv_heads + rows_per_warp - 1) / rows_per_warp;
   const int64_t blocks = (warps_wanted + 7) / 8;

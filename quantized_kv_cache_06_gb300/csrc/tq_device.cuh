@@ -62,6 +62,14 @@ __device__ __forceinline__ float load_as_f32(const void* base, int64_t i, int dt
   return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
 }
 
+// Element i of query (row, q head) r: q_dtype 0/1/2 as load_as_f32, 3 = int8 code times
+// the (row, q head) scale q_scale[r].
+__device__ __forceinline__ float load_query_f32(const void* q, const float* q_scale, int64_t r, int64_t i,
+                                                int dtype) {
+  if (dtype == 3) return (float)reinterpret_cast<const int8_t*>(q)[i] * __ldg(q_scale + r);
+  return load_as_f32(q, i, dtype);
+}
+
 __device__ __forceinline__ void store_from_f32(void* base, int64_t i, int dtype, float v) {
   if (dtype == 0) reinterpret_cast<float*>(base)[i] = v;
   else if (dtype == 1) reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);

@@ -17,7 +17,9 @@ enum : int32_t {
   kTimeout = 6,
 };
 
-enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+// kI8: int8 query codes with one fp32 scale per (query row, q head) (the INT8-query
+// prefill); queries only.
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2, kI8 = 3 };
 
 // Tries of one bounded mbarrier wait before it gives up and reports kTimeout (seconds at
 // most with the hardware's own suspend time per try), and the number the next launches
@@ -105,6 +107,8 @@ struct DecodeArgs {
   // A row outside [0, bt_num_rows) reports kInvalidArg and reads nothing.
   const int32_t* bt_rows;
   int bt_num_rows;
+  // q_dtype == kI8: scale of query (row, q head) r at q_scale[r] (null otherwise).
+  const float* q_scale;
 };
 
 #ifdef __CUDACC__
@@ -115,6 +119,20 @@ __device__ __forceinline__ int block_table_row(const DecodeArgs& a, int b) {
   return (r >= 0 && r < a.bt_num_rows) ? r : -1;
 }
 #endif
+
+// head_dim 16 (tq_small.cu): rows of 8 to 14 bytes, taken byte by byte.  The writer runs
+// after the slot validation; the decode handles row maps (prefill) and int8 queries.
+struct DequantArgs;
+cudaError_t launch_write_d16(const WriteArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_d16(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_dequant_d16(const DequantArgs& a, cudaStream_t stream);
+cudaError_t launch_quantize_d16(const void* q, int q_dtype, int64_t rows, int8_t* codes, float* scales,
+                                cudaStream_t stream);
+
+// Int8 query codes -> codes and scales (tq_query.cu): one warp per (row, q head) of
+// rows = num_q_rows * num_q_heads, D = head_dim.
+cudaError_t launch_quantize_queries(const void* q, int q_dtype, int64_t rows, int head_dim, int8_t* codes,
+                                    float* scales, cudaStream_t stream);
 
 // Tensor-core decode (tq_decode_tc.cu): whether the shapes/bits in `a` have an
 // instantiation, its warps per kv head, and its launch.

@@ -11,12 +11,12 @@
 // against up to 64 (query row, q head) pairs with tensor-core MMAs:
 //   S  = qrot Khat^T          m16n8k16, A = rotated queries, B = key tile (ldmatrix)
 //   causal mask per row (token < q_len), online softmax in base 2
-//   O += P' Vhat               A = P' = p 2^(m - mv) nu_v (from the S accumulators), B =
-//                              value tile (ldmatrix.trans); mv is a per-row value frame that
-//                              keeps P' inside the fp16 range for any value norm (it is
-//                              raised when a tile's bound on P' would pass the fp16 range,
-//                              and O is turned back to the score frame when the partial
-//                              is written)
+//   O += P' Vhat               A = P' = p * nu_v (from the S accumulators), B = value tile
+//                              (ldmatrix.trans).  A tile whose largest value norm passes
+//                              kMqFastValueNorm scales each row's P' by a power of two that
+//                              puts its largest near 2^12 (O scaled by it before the tile and
+//                              back after, both exact) and adds the fp16 remainders of P'
+//                              and of the value tile; it also takes the exact key path.
 // Khat holds fp16(alpha_k c[idx]) (+ the fp16 remainder for tiles that need the exact
 // score), Vhat fp16(alpha_v c[idx]); the key norm multiplies the score and the value norm
 // the weight, so nothing of the cache is expanded to a dense row in HBM.  The rotated
@@ -59,16 +59,17 @@ constexpr float kMqLog2e = 1.4426950408889634f;
 // remainder of the key centroids (same bound as the tensor-core decode).
 constexpr float kMqFastBound = 48.0f;
 constexpr float kMqSlack = 6.0f;  // log2 units the running max may lag behind the scores
-// Value frame (as in the tensor-core decode): the value weights P' = p 2^(m - mv) nu_v stay
-// below 2^kMqSlack * kMqValueBound = 2^15 by raising mv, and mv never lags m by more than
-// kMqFrameGap.
-constexpr float kMqValueBound = 512.0f;
-constexpr float kMqFrameGap = 64.0f;
-// Largest value norm of a tile whose values take the fp16 path (P' and the value tile each
-// rounded once to fp16); tiles above it add both fp16 remainders (same rule as the
-// tensor-core decode: an error proportional to a large norm can pass the absolute part of
-// the 2e-3 + 2e-3 |o| tolerance where the output element is small).
+// Largest value norm of a tile whose values take the fp16 path (P' = p nu_v <= 2^6 * 32,
+// rounded once to fp16, and the fp16 value tile); tiles above it scale P', add both fp16
+// remainders and take the exact key path (same rule as the tensor-core decode: an error
+// proportional to a large norm can pass the absolute part of the 2e-3 + 2e-3 |o|
+// tolerance where the output element is small).
 constexpr float kMqFastValueNorm = 32.0f;
+// The fp16 remainders of the key and value tiles are stored times 2^12: a remainder of a
+// value below 1/4 would otherwise be an fp16 subnormal (2^-25 of absolute precision); the
+// products with them are scaled back by 2^-12, exactly.
+constexpr float kMqLoScale = 4096.0f;
+constexpr float kMqLoUnscale = 1.0f / 4096;
 
 constexpr int kMqStages = 4;  // raw-word ring: tiles it .. it + 2 in flight while tile it is used
 
@@ -158,10 +159,17 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation 
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float lg2(float x) {  // log2(x), hardware approximation (lg2(0) = -inf)
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
+// Power-of-two scale (and its inverse) that brings a positive x to [2^11, 2^12): both exact;
+// 1 and 1 for x = 0 or subnormal.
+__device__ __forceinline__ void mq_tile_scale(float x, float& f, float& inv_f) {
+  int e = (int)((__float_as_uint(x) >> 23) & 0xffu);
+  if (e == 0) {
+    f = inv_f = 1.f;
+    return;
+  }
+  e = max(12, e);
+  f = __uint_as_float((uint32_t)(265 - e) << 23);   // 2^(138 - e)
+  inv_f = __uint_as_float((uint32_t)(e - 11) << 23);  // 2^(e - 138)
 }
 
 __device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
@@ -187,6 +195,46 @@ __device__ __forceinline__ void bar_pair(int id) {  // the two warps of one row 
 }
 __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+
+// The value remainders of one tile (an exact-value tile, rare): this thread's value tasks
+// re-read from its ring words and expanded into the key tile's space (fp16 (alpha c - hi)
+// times 2^12), between barrier C (every warp's scores done) and barrier D.  Not inlined, so
+// the registers of this path do not weigh on the main loop's.
+template <int VB, int MAXB, int TPT, int kTaskWords, int kMaxBits, int kThreads, int kRingWords>
+__device__ __noinline__ void mq_value_remainders(uint32_t ring_base, int tid, int st, const int* comps,
+                                                 const uint32_t* sts_offs, uint32_t khi_base, uint32_t vc_pair) {
+  __syncthreads();  // C
+#pragma unroll
+  for (int j = 0; j < TPT; ++j) {
+    if (comps[j] != 1) continue;
+    auto ring = [&](int w) -> uint32_t {
+      return ring_base + (uint32_t)(((st * kRingWords + j * kTaskWords + w) * kThreads + tid) * 4);
+    };
+    const bool ok = lds_u32(ring(kMaxBits + 1)) != 0u;
+    uint32_t w[MAXB];
+#pragma unroll
+    for (int k = 0; k < MAXB; ++k) w[k] = ok ? lds_u32(ring(k)) : 0u;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t vp[4];
+#pragma unroll
+      for (int pr = 0; pr < 4; ++pr) {
+        uint32_t val[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = q4 * 8 + pr * 2 + u;
+          const int bit = i * VB, k = bit >> 5, sh = bit & 31;
+          uint32_t f = w[k] >> sh;
+          if (sh + VB > 32) f |= w[k + 1] << (32 - sh);
+          val[u] = __shfl_sync(kFullMask, vc_pair, (int)f);
+        }
+        vp[pr] = __byte_perm(val[0], val[1], 0x7632);
+      }
+      sts_v4(khi_base + (sts_offs[j] ^ (uint32_t)(q4 << 4)), vp[0], vp[1], vp[2], vp[3]);
+    }
+  }
+  __syncthreads();  // D
 }
 
 struct MqArgs {
@@ -277,9 +325,11 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
     const int wrow = mr / G;
     float v[E];
     if (wrow < nrows) {
-      const int64_t base = ((int64_t)(i0 + wrow) * Hq + (int64_t)h * G + mr % G) * D + lane * E;
+      const int64_t qr = (int64_t)(i0 + wrow) * Hq + (int64_t)h * G + mr % G;  // (row, q head)
+      const int64_t base = qr * D + lane * E;
 #pragma unroll
-      for (int i = 0; i < E; ++i) v[i] = load_as_f32(a.q, base + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
+      for (int i = 0; i < E; ++i)
+        v[i] = load_query_f32(a.q, a.q_scale, qr, base + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
     } else {
 #pragma unroll
       for (int i = 0; i < E; ++i) v[i] = 0.f;
@@ -338,20 +388,18 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
     for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float m_thr[2] = {-INFINITY, -INFINITY};  // m_run + kMqSlack
-  // value frame: o holds sum_t 2^(s_t - mv) nu_v,t c[idx_v,t]; fr = 2^(m_run - mv)
-  float mv[2] = {-INFINITY, -INFINITY}, fr[2] = {0.f, 0.f};
 
   // dequantisation centroids: lane l holds entry l mod 2^b (a shuffle reads only the low
   // 5 bits of its source lane, so a field needs no mask)
-  uint32_t kc_pair, vc_pair;  // (fp16 hi, fp16 lo) of alpha c
+  uint32_t kc_pair, vc_pair;  // (fp16 hi, fp16 lo * 2^12) of alpha c
   {
     const float ck = __ldg(a.k_centroids + (lane & ((1 << KB) - 1))) * a.k_alpha;
     const __half hk = __float2half_rn(ck);
-    const __half lk = __float2half_rn(ck - __half2float(hk));
+    const __half lk = __float2half_rn((ck - __half2float(hk)) * kMqLoScale);
     kc_pair = (uint32_t)__half_as_ushort(hk) | ((uint32_t)__half_as_ushort(lk) << 16);
     const float cv = __ldg(a.v_centroids + (lane & ((1 << VB) - 1))) * a.v_alpha;
     const __half hv = __float2half_rn(cv);
-    const __half lv = __float2half_rn(cv - __half2float(hv));
+    const __half lv = __float2half_rn((cv - __half2float(hv)) * kMqLoScale);
     vc_pair = (uint32_t)__half_as_ushort(hv) | ((uint32_t)__half_as_ushort(lv) << 16);
   }
 
@@ -462,7 +510,7 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
           }
         }
         // ---- A: exact-score and exact-value votes; every warp is done with the previous
-        // tile.  One barrier votes on both; only a tile that needs either (rare) takes two
+        // tile.  One barrier votes on both; only a tile that needs either (rare) takes one
         // more to tell them apart.
         int kflag = 0, vflag = 0;
 #pragma unroll
@@ -471,9 +519,10 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
           if (task_comp(j) == 0) kflag |= fabsf(__uint_as_float(raw[j].nrm)) * qn_cta > kMqFastBound;
           else vflag |= fabsf(__uint_as_float(raw[j].nrm)) > kMqFastValueNorm;
         }
+        // an exact-value tile also takes the exact key path
         bool exact = false, exact_v = false;
         if (__syncthreads_or(kflag | vflag)) {
-          exact = __syncthreads_or(kflag) != 0;
+          exact = true;
           exact_v = __syncthreads_or(vflag) != 0;
         }
 
@@ -541,40 +590,12 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
         // is free; the fp16 remainders of the value tile go there (re-read from this
         // thread's ring words of the tile), visible after barrier D.
         auto value_remainders = [&]() {
-          __syncthreads();  // C
-          const int st = it % kMqStages;
+          int comps[TPT];
 #pragma unroll
-          for (int j = 0; j < TPT; ++j) {
-            if (task_comp(j) != 1) continue;
-            const bool ok = lds_u32(ring(st, j * S::kTaskWords + S::kMaxBits + 1)) != 0u;
-            uint32_t w[MAXB];
-#pragma unroll
-            for (int k = 0; k < MAXB; ++k) w[k] = ok ? lds_u32(ring(st, j * S::kTaskWords + k)) : 0u;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint32_t vp[4];
-#pragma unroll
-              for (int pr = 0; pr < 4; ++pr) {
-                uint32_t val[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int i = q4 * 8 + pr * 2 + u;
-                  const int bit = i * VB, k = bit >> 5, sh = bit & 31;
-                  uint32_t f = w[k] >> sh;
-                  if (sh + VB > 32) f |= w[k + 1] << (32 - sh);
-                  val[u] = __shfl_sync(kFullMask, vc_pair, (int)f);
-                }
-                vp[pr] = __byte_perm(val[0], val[1], 0x7632);
-              }
-              sts_v4(khi_base + (sts_off[j] ^ (uint32_t)(q4 << 4)), vp[0], vp[1], vp[2], vp[3]);
-            }
-          }
-          __syncthreads();  // D
+          for (int j = 0; j < TPT; ++j) comps[j] = task_comp(j);
+          mq_value_remainders<VB, MAXB, TPT, S::kTaskWords, S::kMaxBits, kThreads, S::kRingWords>(
+              sbase + S::kOffRing, tid, it % kMqStages, comps, sts_off, khi_base, vc_pair);
         };
-        if (!live) {
-          value_remainders();
-          continue;
-        }
         float s[4][4];
 #pragma unroll
         for (int jn = 0; jn < 4; ++jn)
@@ -582,6 +603,24 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
           for (int e = 0; e < 4; ++e) s[jn][e] = 0.f;
         auto scores = [&](auto exact_tag) {
           constexpr bool EX = decltype(exact_tag)::value;
+          if (EX) {
+            // q_hi * key_lo first (key_lo carries 2^12), scaled back before the main products
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              const uint32_t kaddr = kb_lane ^ (uint32_t)((dh * KS + ks) << 5);
+#pragma unroll
+              for (int jp = 0; jp < 2; ++jp) {
+                uint32_t kl[4];
+                ldsm_x4(kl, kaddr + (uint32_t)(jp * 16 * S::kRow) + (uint32_t)(S::kOffKlo - S::kOffKhi));
+                mma_f16(s[2 * jp], qh[ks], kl[0], kl[1]);
+                mma_f16(s[2 * jp + 1], qh[ks], kl[2], kl[3]);
+              }
+            }
+#pragma unroll
+            for (int jn = 0; jn < 4; ++jn)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) s[jn][e] *= kMqLoUnscale;
+          }
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
             uint32_t ql[4];
@@ -596,15 +635,10 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
               mma_f16(s[2 * jp + 1], qh[ks], kb[2], kb[3]);
               mma_f16(s[2 * jp], ql, kb[0], kb[1]);
               mma_f16(s[2 * jp + 1], ql, kb[2], kb[3]);
-              if (EX) {
-                uint32_t kl[4];
-                ldsm_x4(kl, koff + (uint32_t)(S::kOffKlo - S::kOffKhi));
-                mma_f16(s[2 * jp], qh[ks], kl[0], kl[1]);
-                mma_f16(s[2 * jp + 1], qh[ks], kl[2], kl[3]);
-              }
             }
           }
         };
+        if (live) {
         if (exact) scores(std::true_type{});
         else scores(std::false_type{});
         if constexpr (SPLIT) {  // sum the two half-dimension scores of the row group
@@ -622,8 +656,10 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
             s[jn][3] += pv.w;
           }
         }
+        }  // live
 
         if (exact_v) value_remainders();
+        if (!live) continue;
 
         // scores: x nu_k, invalid tokens -inf, causal mask per row
 #pragma unroll
@@ -650,8 +686,6 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
 #pragma unroll
           for (int jn = 0; jn < 4; ++jn) mx[hr] = fmaxf(mx[hr], fmaxf(s[jn][2 * hr], s[jn][2 * hr + 1]));
         }
-        // The sums follow the score max; the value frame moves only when it would lag the
-        // score max by more than kMqFrameGap (always at a row's first live tile).
         if (__any_sync(kFullMask, mx[0] > m_thr[0] || mx[1] > m_thr[1])) {
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
@@ -662,49 +696,10 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
             m_run[hr] = mn;
             m_thr[hr] = mn + kMqSlack;
             l_run[hr] *= corr;
-            const float mvn = fmaxf(mv[hr], mn - kMqFrameGap);
-            if (mvn != mv[hr]) {
-              const float cv = ex2(mv[hr] - mvn);
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                o[nt][2 * hr] *= cv;
-                o[nt][2 * hr + 1] *= cv;
-              }
-              mv[hr] = mvn;
-            }
-            fr[hr] = mn == -INFINITY ? 0.f : ex2(mn - mv[hr]);
-          }
-        }
-        // Value frame check before any weight is formed: p <= 2^kMqSlack, so every P' of a
-        // row is at most 2^6 * 2^(m - mv) * max nu_v.  Where that passes kMqValueBound (a
-        // row's first live tile, rows of very large norm) the row's frame is raised to the
-        // tile's largest s_t + log2 nu_v,t, so its P' here are at most ~1.
-        float vmax = 0.f;
-#pragma unroll
-        for (int jn = 0; jn < 4; ++jn) {
-          const float2 vn = *reinterpret_cast<const float2*>(vn_s + 8 * jn + 2 * c);
-          vmax = fmaxf(vmax, fmaxf(vn.x, vn.y));
-        }
-        if (__any_sync(kFullMask, vmax * fr[0] > kMqValueBound || vmax * fr[1] > kMqValueBound)) {
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            float sv = -INFINITY;
-#pragma unroll
-            for (int jn = 0; jn < 4; ++jn) {
-              const float2 vn = *reinterpret_cast<const float2*>(vn_s + 8 * jn + 2 * c);
-              sv = fmaxf(sv, fmaxf(s[jn][2 * hr] + lg2(vn.x), s[jn][2 * hr + 1] + lg2(vn.y)));
-            }
-            sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 1));
-            sv = fmaxf(sv, __shfl_xor_sync(kFullMask, sv, 2));
-            if (sv > mv[hr]) {
-              const float cv = ex2(mv[hr] - sv);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                o[nt][2 * hr] *= cv;
-                o[nt][2 * hr + 1] *= cv;
-              }
-              mv[hr] = sv;
-              fr[hr] = m_run[hr] == -INFINITY ? 0.f : ex2(m_run[hr] - sv);
+            for (int nt = 0; nt < NT; ++nt) {
+              o[nt][2 * hr] *= corr;
+              o[nt][2 * hr + 1] *= corr;
             }
           }
         }
@@ -713,26 +708,56 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
         // and P'_hi Vhat_lo (the remainders sit in the key tile's space).
         auto values = [&](auto exv_tag) {
           constexpr bool EXV = decltype(exv_tag)::value;
+          float pw[4][4];  // P' = p nu_v (the fast path packs each column group at once)
           uint32_t pa[2][4], pl[2][4];
 #pragma unroll
           for (int jn = 0; jn < 4; ++jn) {
-            const int tok = 8 * jn + 2 * c;
-            const float2 vn = *reinterpret_cast<const float2*>(vn_s + tok);
-            float pw[4];
+            const float2 vn = *reinterpret_cast<const float2*>(vn_s + 8 * jn + 2 * c);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float p = ex2(s[jn][e] - m_use[e >> 1]);
               l_run[e >> 1] += p;
-              pw[e] = p > 0.f ? (p * fr[e >> 1]) * ((e & 1) ? vn.y : vn.x) : 0.f;  // P' = p 2^(m - mv) nu_v
+              pw[jn][e] = p > 0.f ? p * ((e & 1) ? vn.y : vn.x) : 0.f;
             }
-            const uint32_t h01 = half2_bits(pw[0], pw[1]), h23 = half2_bits(pw[2], pw[3]);
+            if (!EXV) {
+              pa[jn >> 1][(jn & 1) * 2 + 0] = half2_bits(pw[jn][0], pw[jn][1]);
+              pa[jn >> 1][(jn & 1) * 2 + 1] = half2_bits(pw[jn][2], pw[jn][3]);
+            }
+          }
+          float inv_f[2] = {1.f, 1.f};
+          if (EXV) {  // per row: the largest P' to [2^11, 2^12), O by the same power of two
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+              float pm = 0.f;
+#pragma unroll
+              for (int jn = 0; jn < 4; ++jn) pm = fmaxf(pm, fmaxf(pw[jn][2 * hr], pw[jn][2 * hr + 1]));
+              pm = fmaxf(pm, __shfl_xor_sync(kFullMask, pm, 1));
+              pm = fmaxf(pm, __shfl_xor_sync(kFullMask, pm, 2));
+              float f;
+              mq_tile_scale(pm, f, inv_f[hr]);
+#pragma unroll
+              for (int jn = 0; jn < 4; ++jn) {
+                pw[jn][2 * hr] *= f;
+                pw[jn][2 * hr + 1] *= f;
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                o[nt][2 * hr] *= f;
+                o[nt][2 * hr + 1] *= f;
+              }
+            }
+          }
+          // EXV: pa = fp16 P' (scaled), pl = its fp16 remainders
+#pragma unroll
+          for (int jn = 0; jn < 4 && EXV; ++jn) {
+            const uint32_t h01 = half2_bits(pw[jn][0], pw[jn][1]), h23 = half2_bits(pw[jn][2], pw[jn][3]);
             pa[jn >> 1][(jn & 1) * 2 + 0] = h01;
             pa[jn >> 1][(jn & 1) * 2 + 1] = h23;
-            if (EXV) {
+            {
               const __half2 x01 = *reinterpret_cast<const __half2*>(&h01);
               const __half2 x23 = *reinterpret_cast<const __half2*>(&h23);
-              pl[jn >> 1][(jn & 1) * 2 + 0] = half2_bits(pw[0] - __low2float(x01), pw[1] - __high2float(x01));
-              pl[jn >> 1][(jn & 1) * 2 + 1] = half2_bits(pw[2] - __low2float(x23), pw[3] - __high2float(x23));
+              pl[jn >> 1][(jn & 1) * 2 + 0] = half2_bits(pw[jn][0] - __low2float(x01), pw[jn][1] - __high2float(x01));
+              pl[jn >> 1][(jn & 1) * 2 + 1] = half2_bits(pw[jn][2] - __low2float(x23), pw[jn][3] - __high2float(x23));
             }
           }
 #pragma unroll
@@ -745,13 +770,43 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
               mma_f16(o[2 * dp], pa[s2], vb[0], vb[1]);
               mma_f16(o[2 * dp + 1], pa[s2], vb[2], vb[3]);
               if (EXV) {
-                uint32_t vl[4];
-                ldsm_x4_t(vl, vaddr - v_base + khi_base);
                 mma_f16(o[2 * dp], pl[s2], vb[0], vb[1]);
                 mma_f16(o[2 * dp + 1], pl[s2], vb[2], vb[3]);
+              }
+            }
+          }
+          if (EXV) {
+            // value remainders (stored x 2^12, in the key tile's space) against P'_hi 2^-12:
+            // scaling an fp16 by a power of two is exact while it stays normal, and the
+            // weights that leave the normal range are 2^-13 of the tile's largest or less
+            const __half2 unscale = __float2half2_rn(kMqLoUnscale);
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                __half2 x = *reinterpret_cast<const __half2*>(&pa[s2][k]);
+                x = __hmul2(x, unscale);
+                pa[s2][k] = *reinterpret_cast<const uint32_t*>(&x);
+              }
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+#pragma unroll
+              for (int dp = 0; dp < NT / 2; ++dp) {
+                const uint32_t vaddr = (vb_lane ^ (uint32_t)((dh * (NT / 2) + dp) << 5)) + (uint32_t)(s2 * 16 * S::kRow);
+                uint32_t vl[4];
+                ldsm_x4_t(vl, vaddr - v_base + khi_base);
                 mma_f16(o[2 * dp], pa[s2], vl[0], vl[1]);
                 mma_f16(o[2 * dp + 1], pa[s2], vl[2], vl[3]);
               }
+            }
+          }
+          if (EXV) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              o[nt][0] *= inv_f[0];
+              o[nt][1] *= inv_f[0];
+              o[nt][2] *= inv_f[1];
+              o[nt][3] *= inv_f[1];
             }
           }
         };
@@ -763,8 +818,7 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
     s0 = s1;
   }
 
-  // ---- partials: (m, l, acc / alpha_v) per (row, q head) of this window and split; the
-  // accumulator goes back from the value frame to the score frame (times 2^(mv - m)) ----
+  // ---- partials: (m, l, acc / alpha_v) per (row, q head) of this window and split ------
   const float inv_alpha_v = 1.0f / a.v_alpha;
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
@@ -776,12 +830,10 @@ __global__ void __launch_bounds__(MqShape<D>::kThreads, MqShape<D>::kMinBlocks) 
     if (wrow < nrows) {
       const int64_t slot = ((int64_t)(i0 + wrow) * Hq + (int64_t)h * G + mr % G) * args.nsplit + split;
       float* acc = args.part_acc + slot * D + dh * SH::kDh;
-      const float to_m =
-          (m_run[hr] == -INFINITY || mv[hr] == -INFINITY) ? 0.f : ex2(mv[hr] - m_run[hr]) * inv_alpha_v;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         *reinterpret_cast<float2*>(acc + 8 * nt + 2 * c) =
-            to_m == 0.f ? make_float2(0.f, 0.f) : make_float2(o[nt][2 * hr] * to_m, o[nt][2 * hr + 1] * to_m);
+            make_float2(o[nt][2 * hr] * inv_alpha_v, o[nt][2 * hr + 1] * inv_alpha_v);
       if (c == 0 && dh == 0) {
         args.part_ml[slot * 2 + 0] = m_run[hr];
         args.part_ml[slot * 2 + 1] = l;

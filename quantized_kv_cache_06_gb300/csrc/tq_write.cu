@@ -169,6 +169,7 @@ cudaError_t launch_write(const WriteArgs& a, cudaStream_t stream) {
   err = launch_validate_slots(a, stream, sms);
   if (err != cudaSuccess) return err;
   const int64_t rows = a.num_tokens * a.num_kv_heads;
+  if (a.head_dim == 16) return launch_write_d16(a, stream);
   if (write_tc_supported(a)) {
     // 16-row tiles, 8 warps per CTA, two CTAs per SM resident
     const int64_t tiles = (rows + 15) / 16;

@@ -82,7 +82,10 @@ def test_next_rows_cpu_baselines_cover_each_row():
     # the oracle timed beside each next row, on the tiny workload: every row present, in the
     # unit of its GPU figure, positive, and labelled as the oracle
     base = bench.next_rows_cpu_baselines(make_workload(1))
-    assert set(base) == {"tq_dequant_rows", "tq_paged_prefill", "qjl_residual_keys"}
-    entries = [base["tq_dequant_rows"], base["tq_paged_prefill"], *base["qjl_residual_keys"].values()]
+    assert set(base) == {"tq_dequant_rows", "tq_paged_prefill", "qjl_residual_keys", "int8q_prefill", "recipe_modes"}
+    entries = [base["tq_dequant_rows"], base["tq_paged_prefill"], base["int8q_prefill"],
+               *base["qjl_residual_keys"].values()]
+    for rec in ("turboquant25", "turboquant35"):
+        entries += list(base["recipe_modes"][rec].values())
     for e in entries:
         assert e["kind"] == "oracle" and e["unit"] == "GB/s" and e["value"] > 0 and e["cores"] >= 1

@@ -107,11 +107,9 @@ def test_dequant_zero_tokens_and_unsupported_dim():
     c32 = torch.from_numpy(o.codebook_f32(d, bits)[0]).to(dev)
     out = tq.tq_dequant_rows(pages, torch.zeros(0, dtype=torch.int64, device=dev), signs, c32)
     assert out.shape == (0, 1, d)
-    d16 = 16
-    pages16 = torch.zeros(2, 16, 1, o.row_bytes(d16, bits), dtype=torch.uint8, device=dev)
-    with pytest.raises(tq.TQError):
-        tq.tq_dequant_rows(pages16, torch.zeros(3, dtype=torch.int64, device=dev),
-                           torch.ones(d16, device=dev), c32)
+    # head_dim 8 is below the boundary's range (16 .. 256): refused on the host
+    assert tq.lib().tq_dequant_rows(pages.data_ptr(), bits, 2, 16, 1, 8, pages.data_ptr(), 3, signs.data_ptr(),
+                                    c32.data_ptr(), pages.data_ptr(), 1, None, None) == tq.TQ_ERR_UNSUPPORTED
 
 
 def test_dequant_round_trip_of_oracle_written_rows():

@@ -52,21 +52,22 @@ def test_row_bytes_matches_pages_table(tq):
     for line in read_golden_rows("row_bytes_d128.txt"):
         d, b, _, rb = map(int, line.split())
         assert tq.tq_row_bytes(d, b) == rb
-    for d in (32, 64, 128, 256):
+    for d in (16, 32, 64, 128, 256):
         for b in (2, 3, 4, 5):
             assert tq.tq_row_bytes(d, b) == o.row_bytes(d, b)
     assert tq.lib().tq_row_bytes(48, 4) == -1
+    assert tq.lib().tq_row_bytes(8, 4) == -1  # head_dim below 16
     assert tq.lib().tq_row_bytes(128, 6) == -1
 
 
-@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("d", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("seed", [0, 42, 2**63 + 5])
 def test_rotation_signs_match_oracle(tq, d, seed):
     got = tq.tq_build_rotation(d, seed).numpy()
     assert np.array_equal(got.astype(np.float64), o.splitmix64_signs(d, seed))
 
 
-@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("d", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("bits", [2, 3, 4, 5])
 def test_codebook_matches_oracle(tq, d, bits):
     c_lib, b_lib = tq.tq_codebook(d, bits)
