@@ -257,8 +257,8 @@ DecodePlan plan_decode(const DecodeArgs& a, int num_sms) {
     return p;
   }
   if (a.k_bits > 0 && a.head_dim <= 128 && prefill_mq_supported(a)) {
-    // shapes without a tensor-core decode instantiation (3/5-bit rows, block sizes other
-    // than 16, GQA groups 1/2): the multi-query kernel with one sequence per window.  Its
+    // shapes without a tensor-core decode instantiation (5-bit rows, 3-bit rows paired with
+    // other widths, block sizes other than 16, GQA groups 1/2): the multi-query kernel with one sequence per window.  Its
     // D = 256 form (one 8-warp CTA per SM) is no faster than the SIMT kernel for one row
     // per window, so D = 256 decodes stay on the SIMT kernel.
     p.kernel = 3;

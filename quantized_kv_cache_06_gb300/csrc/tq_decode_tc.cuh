@@ -24,7 +24,10 @@
 // query is split into fp16 hi + lo as well, and hi*hi + lo*hi + hi*lo carries ~22
 // significant bits, so the score keeps fp32-level accuracy even for very large norms.
 // The k order inside a fragment is a fixed permutation of the coordinates; the query
-// fragment follows the same permutation.
+// fragment follows the same permutation.  3- and 5-bit rows have fields that cross word
+// boundaries: each lane takes a contiguous window of whole fields and extracts them with
+// shifts (funnel shifts across words) into the address of its own table copy; 3-bit rows
+// look up a pair of coordinates per 6-bit field, 5-bit rows one coordinate per field.
 //
 // Values.  Accumulated in rotated space with the contraction over (token, parity):
 // O'[pair][2g + e] += sum_t Vhat[t][2 pair + e] * P'[g][t], so one table entry gives
@@ -173,14 +176,32 @@ __device__ __forceinline__ void split_half(float x, __half& hi, __half& lo) {
   lo = __float2half_rn((x - __half2float(hi)) * kLoScale);
 }
 
+// Field i of width W (bits [W i, W i + W)) of a window of words w (i compile-time).
+template <int W>
+__device__ __forceinline__ uint32_t win_field(const uint32_t* w, int i) {
+  const int bit = W * i, wi = bit >> 5, sh = bit & 31;
+  return (sh <= 32 - W ? (w[wi] >> sh) : __funnelshift_r(w[wi], w[wi + 1], sh)) & ((1u << W) - 1u);
+}
+// The same field shifted to bits [7, 7 + W) and OR'd into `lane_base`: the shared address
+// of entry `field` of a per-lane replicated table of 128-byte entries.
+template <int W>
+__device__ __forceinline__ uint32_t win_addr(const uint32_t* w, int i, uint32_t lane_base) {
+  const int bit = W * i, wi = bit >> 5, sh = bit & 31;
+  uint32_t x;
+  if (sh <= 32 - W) x = sh >= 7 ? (w[wi] >> (sh - 7)) : (w[wi] << (7 - sh));
+  else x = __funnelshift_r(w[wi], w[wi + 1], sh - 7);
+  return (x & (((1u << W) - 1u) << 7)) | lane_base;
+}
+
 template <int D, int KB, int VB, int G, int WPH>
 struct TcCfg {
   static constexpr int kRBK = D * KB / 8 + 4;          // row bytes
   static constexpr int kRBV = D * VB / 8 + 4;
   static constexpr int kWK = D * KB / 32;              // index words per K row
   static constexpr int kWV = D * VB / 32;
-  static constexpr int kPWK = 16 / KB;                 // pairs per word
-  static constexpr int kPWV = 16 / VB;
+  static constexpr bool kWin = KB == 3 || KB == 5;     // window mode: 3- and 5-bit rows
+  static constexpr int kPWK = kWin ? 1 : 16 / KB;       // pairs per word (2- and 4-bit rows)
+  static constexpr int kPWV = kWin ? 1 : 16 / VB;
   static constexpr int kKSteps = D / 16;               // score k-steps
   static constexpr int kMTiles = D / 32;               // value m-tiles
   static constexpr int kNT = (2 * G + 7) / 8;          // value n-tiles (N = 2G)
@@ -190,14 +211,32 @@ struct TcCfg {
   // address, so one PRMT of (packed word, T base | lane * 4) yields the absolute
   // address of an entry.
   static constexpr bool kHasT = KB == 4 || VB == 4;
-  static constexpr int kTBytes = kHasT ? 256 * 256 : 0;
   // The small tables (K lo parts of byte fields, read only by tiles that need the exact
   // score, and the nibble-field tables of 2-bit indices) have one copy each and live in
   // the fixed part of the shared memory.
-  static_assert(kWK % 4 == 0, "K row must split into 4 interleaved word columns");
-  static_assert(kWV % 8 == 0, "V row must split into 8 interleaved word columns");
+  // Window mode (3- and 5-bit rows, whose fields cross word boundaries).  K: lane c of a
+  // row owns the pairs [c D/8, (c + 1) D/8), KB D/128 whole words from word KB D/128 c,
+  // taken in chunks of KB words (32 coordinates, 8 k-steps); k-step s takes pairs
+  // c D/8 + 2s and + 2s + 1.  V: lane r owns the pairs [r D/16, (r + 1) D/16) of a token row
+  // (D = 128: 16 VB bits from bit 16 VB r, half-word aligned; D = 256: VB whole words);
+  // m-tile i takes pairs r D/16 + 2i and + 2i + 1.  3-bit rows look up a pair per 6-bit
+  // field in a 64-entry table of (fp16 hi, fp16 hi) pairs; 5-bit rows look up each
+  // coordinate in a 32-entry table of (fp16 hi, fp16 lo x 2^12) and join two with a PRMT.
+  // Both tables are replicated per lane (entry e of lane l at e * 128 + 4 l), K then V,
+  // at a shared address aligned to one table, so the address of an entry is the field,
+  // shifted to bit 7, OR'd into (table base | lane * 4).
+  static constexpr int kTabEntries = KB == 3 ? 64 : 32;
+  static constexpr int kKLaneWords = KB * D / 128;  // K words per lane and row (window mode)
+  // Table region: T (64 KB, 64 KB aligned) for 4-bit rows, the window-mode tables (2 x 8 KB
+  // or 2 x 4 KB, aligned to one) for 3- and 5-bit rows, none for 2-bit rows.
+  static constexpr int kTBytes = kHasT ? 256 * 256 : (kWin ? 2 * kTabEntries * 128 : 0);
+  static constexpr int kTAlign = kHasT ? 65536 : kTabEntries * 128;
+  static_assert(kWin || kWK % 4 == 0, "K row must split into 4 interleaved word columns");
+  static_assert(kWin || kWV % 8 == 0, "V row must split into 8 interleaved word columns");
   static_assert(G == 4 || G == 8, "GQA group 4 or 8");
-  static_assert((KB == 2 || KB == 4) && (VB == 2 || VB == 4), "2- or 4-bit indices");
+  static_assert(KB >= 2 && KB <= 5 && VB >= 2 && VB <= 5, "2- to 5-bit indices");
+  static_assert(kWin == (VB == 3 || VB == 5) && (!kWin || KB == VB), "3- and 5-bit rows: equal K and V widths");
+  static_assert(!kWin || D == 128 || D == 256, "3- and 5-bit rows at head_dim 128 or 256");
 };
 
 struct TcArgs {
@@ -232,7 +271,9 @@ constexpr int kOffK2 = kOffScan + 36 * 4;                   // nibble K table, 1
 constexpr int kOffV2 = kOffK2 + 16 * 8;                     // nibble V table (hi, lo), 16 x 8 bytes
 constexpr int kOffL = kOffV2 + 16 * 8;                      // byte K lo table, 256 x 4 bytes
 constexpr int kOffVL = kOffL + 256 * 4;                     // byte V lo table, 256 x 4 bytes
-constexpr int kMiscBytes = (kOffVL + 256 * 4 + 127) / 128 * 128;
+constexpr int kOffK3L = kOffVL + 256 * 4;                   // 6-bit K lo table, 64 x 4 bytes
+constexpr int kOffV3L = kOffK3L + 64 * 4;                   // 6-bit V lo table, 64 x 4 bytes
+constexpr int kMiscBytes = (kOffV3L + 64 * 4 + 127) / 128 * 128;
 
 constexpr float kRescaleSlack = 6.0f;  // log2 units the running max may lag behind
 // Largest bound nu_k * ||q_rot|| (log2 units) of a tile scored with the fp16-hi key part
@@ -248,6 +289,9 @@ constexpr float kFastScoreBound = 48.0f;
 // the output element itself is small.
 constexpr float kFastValueNorm = 32.0f;
 
+// At most 9 warps (8 consumers + the producer).  The register file is granted to a CTA
+// in groups of 4 warps, so 288 threads take 12 warps' worth: 168 registers a thread at most
+// (a launch at more registers is refused).
 template <int D, int KB, int VB, int G, int WPH>
 __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   using Cfg = TcCfg<D, KB, VB, G, WPH>;
@@ -264,7 +308,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t t_base = smem_base + (uint32_t)args.t_off;
-  if (Cfg::kHasT && (t_base & 0xFFFFu) != 0u) {  // layout computed for another shared window
+  if (Cfg::kTBytes > 0 && (t_base & (uint32_t)(Cfg::kTAlign - 1)) != 0u) {  // layout for another shared window
     if (tid == 0 && a.status) atomicMax(a.status, (int32_t)kUnsupported);
     return;
   }
@@ -273,6 +317,10 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   unsigned char* lutK2 = smem + kOffK2;
   unsigned char* lutV2 = smem + kOffV2;
   unsigned char* lutVL = smem + kOffVL;
+  unsigned char* lutK3L = smem + kOffK3L;
+  unsigned char* lutV3L = smem + kOffV3L;
+  unsigned char* lutKW = smem + args.t_off;  // window-mode tables (3- and 5-bit rows)
+  unsigned char* lutVW = smem + args.t_off + Cfg::kTabEntries * 128;
   BlockMeta* meta = reinterpret_cast<BlockMeta*>(smem + kOffMeta);
   int* scan_tmp = reinterpret_cast<int*>(smem + kOffScan);
   auto bar_full = [&](int i) -> uint32_t { return smem_base + kOffBar + 8u * i; };
@@ -478,6 +526,38 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
     return ld32(lutV2 + (((w >> (4 * e)) & 15u) << 3) + 4);
   };
 
+  // Window mode: the A registers of pair j of a window w (fp16 hi parts of coordinates 2j,
+  // 2j + 1; and their remainders, for the exact paths).
+  const uint32_t kw_lane = t_base | (uint32_t)(lane * 4);  // K table, this lane's copy
+  const uint32_t vw_lane = (t_base + (uint32_t)(Cfg::kTabEntries * 128)) | (uint32_t)(lane * 4);
+  auto win_hi = [&](const uint32_t* w, int j, uint32_t lane_base) -> uint32_t {
+    if constexpr (KB == 3) return lds32(win_addr<6>(w, j, lane_base));
+    else return __byte_perm(lds32(win_addr<5>(w, 2 * j, lane_base)), lds32(win_addr<5>(w, 2 * j + 1, lane_base)), 0x5410u);
+  };
+  auto win_lo = [&](const uint32_t* w, int j, uint32_t lane_base, const unsigned char* lo3) -> uint32_t {
+    if constexpr (KB == 3) return ld32(lo3 + (win_field<6>(w, j) << 2));
+    else return __byte_perm(lds32(win_addr<5>(w, 2 * j, lane_base)), lds32(win_addr<5>(w, 2 * j + 1, lane_base)), 0x7632u);
+  };
+  // V window of token row `row` for this lane (pairs [r D/16, (r + 1) D/16)), from bit 0
+  auto v_window = [&](const unsigned char* row, uint32_t (&w)[5]) {
+#pragma unroll
+    for (int i = 0; i < 5; ++i) w[i] = 0u;
+    if (D == 128) {
+      constexpr int NL = (VB + 1) / 2;  // words spanning 16 VB bits from a half-word offset
+      const int wi = (VB * r) >> 1;
+      const uint32_t sh = 16u * (uint32_t)(r & 1);
+      uint32_t x[NL];
+#pragma unroll
+      for (int i = 0; i < NL; ++i) x[i] = ld32(row + (wi + i) * 4);
+#pragma unroll
+      for (int i = 0; i + 1 < NL; ++i) w[i] = __funnelshift_r(x[i], x[i + 1], sh);
+      w[NL - 1] = x[NL - 1] >> sh;
+    } else {
+#pragma unroll
+      for (int i = 0; i < VB; ++i) w[i] = ld32(row + (VB * r + i) * 4);
+    }
+  };
+
   // Query B fragments.  G = 4: one set whose columns 0-3 hold the fp16 hi part of the
   // rotated query and columns 4-7 (the unused half of the n = 8 MMA) its fp16 lo part,
   // so one MMA yields both products.  G = 8: separate hi and lo sets.
@@ -562,7 +642,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       for (int u = 0; u < 2; ++u) {
         const int q = 2 * s + u;
         const int jw = q / Cfg::kPWK, e = q % Cfg::kPWK;
-        const int p = Cfg::kPWK * (c + 4 * jw) + e;  // pair index; coordinates 2p, 2p+1
+        // pair index (coordinates 2p, 2p+1) of local pair u of k-step s on this lane column
+        const int p = Cfg::kWin ? (D / 8) * c + q : Cfg::kPWK * (c + 4 * jw) + e;
         const int src = (2 * p) / E;
         const int off = (2 * p) % E;  // identical on every lane (see the pair layout)
         float x0 = 0.f, x1 = 0.f;
@@ -621,7 +702,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int q = 2 * i + half;
-            const int pv = Cfg::kPWV * (r + 8 * (q / Cfg::kPWV)) + (q % Cfg::kPWV);
+            const int pv = Cfg::kWin ? (D / 16) * r + q : Cfg::kPWV * (r + 8 * (q / Cfg::kPWV)) + (q % Cfg::kPWV);
             float2 v;
             v.x = empty ? 0.f : o_acc[nt][i][2 * half] * inv_alpha;
             v.y = empty ? 0.f : o_acc[nt][i][2 * half + 1] * inv_alpha;
@@ -697,27 +778,48 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       for (int t = 0; t < NTL; ++t)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc1[t][e] = 0.f;
-#pragma unroll
-      for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
-        uint32_t w0[NTL], w1[NTL];
-#pragma unroll
-        for (int t = 0; t < NTL; ++t) {
-          w0[t] = ld32(kbase[t] + r * kts + (c + 4 * jw) * 4);
-          w1[t] = ld32(kbase[t] + (r + 8) * kts + (c + 4 * jw) * 4);
+      auto kstep = [&](int t, int s, uint32_t h00, uint32_t h10, uint32_t h01, uint32_t h11) {
+        if (G == 8) {
+          mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+          mma16816(sacc1[t], h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+        } else {
+          mma16816((NTL == 1 && (s & 1)) ? sacc1[t] : sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
         }
+      };
+      if constexpr (Cfg::kWin) {
+        // chunks of KB words of this lane's window: 16 pairs, 8 k-steps each
 #pragma unroll
-        for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
-          const int s = (jw * Cfg::kPWK + e2) >> 1;
+        for (int ch = 0; ch < D / 128; ++ch) {
+          uint32_t w0[NTL][KB], w1[NTL][KB];
+#pragma unroll
+          for (int t = 0; t < NTL; ++t)
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+              w0[t][i] = ld32(kbase[t] + r * kts + (Cfg::kKLaneWords * c + KB * ch + i) * 4);
+              w1[t][i] = ld32(kbase[t] + (r + 8) * kts + (Cfg::kKLaneWords * c + KB * ch + i) * 4);
+            }
+#pragma unroll
+          for (int s8 = 0; s8 < 8; ++s8)
+#pragma unroll
+            for (int t = 0; t < NTL; ++t)
+              kstep(t, 8 * ch + s8, win_hi(w0[t], 2 * s8, kw_lane), win_hi(w1[t], 2 * s8, kw_lane),
+                    win_hi(w0[t], 2 * s8 + 1, kw_lane), win_hi(w1[t], 2 * s8 + 1, kw_lane));
+        }
+      } else {
+#pragma unroll
+        for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
+          uint32_t w0[NTL], w1[NTL];
 #pragma unroll
           for (int t = 0; t < NTL; ++t) {
-            const uint32_t h00 = k_hi(w0[t], e2), h10 = k_hi(w1[t], e2);
-            const uint32_t h01 = k_hi(w0[t], e2 + 1), h11 = k_hi(w1[t], e2 + 1);
-            if (G == 8) {
-              mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
-              mma16816(sacc1[t], h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
-            } else {
-              mma16816((NTL == 1 && (s & 1)) ? sacc1[t] : sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
-            }
+            w0[t] = ld32(kbase[t] + r * kts + (c + 4 * jw) * 4);
+            w1[t] = ld32(kbase[t] + (r + 8) * kts + (c + 4 * jw) * 4);
+          }
+#pragma unroll
+          for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
+            const int s = (jw * Cfg::kPWK + e2) >> 1;
+#pragma unroll
+            for (int t = 0; t < NTL; ++t)
+              kstep(t, s, k_hi(w0[t], e2), k_hi(w1[t], e2), k_hi(w0[t], e2 + 1), k_hi(w1[t], e2 + 1));
           }
         }
       }
@@ -732,18 +834,38 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
       for (int t = 0; t < NTL; ++t) {
         float sacc1[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
+        auto kstep_ex = [&](int s, uint32_t h00, uint32_t h10, uint32_t h01, uint32_t h11, uint32_t l00,
+                            uint32_t l10, uint32_t l01, uint32_t l11) {
+          mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+          if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
+          mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
+        };
+        if constexpr (Cfg::kWin) {
 #pragma unroll
-        for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
-          const uint32_t w0 = ld32(kbase[t] + r * kts + (c + 4 * jw) * 4);
-          const uint32_t w1 = ld32(kbase[t] + (r + 8) * kts + (c + 4 * jw) * 4);
+          for (int ch = 0; ch < D / 128; ++ch) {
+            uint32_t w0[KB], w1[KB];
 #pragma unroll
-          for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2) {
-            const int s = (jw * Cfg::kPWK + e2) >> 1;
-            const uint32_t h00 = k_hi(w0, e2), h10 = k_hi(w1, e2), h01 = k_hi(w0, e2 + 1), h11 = k_hi(w1, e2 + 1);
-            const uint32_t l00 = k_lo(w0, e2), l10 = k_lo(w1, e2), l01 = k_lo(w0, e2 + 1), l11 = k_lo(w1, e2 + 1);
-            mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
-            if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
-            mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
+            for (int i = 0; i < KB; ++i) {
+              w0[i] = ld32(kbase[t] + r * kts + (Cfg::kKLaneWords * c + KB * ch + i) * 4);
+              w1[i] = ld32(kbase[t] + (r + 8) * kts + (Cfg::kKLaneWords * c + KB * ch + i) * 4);
+            }
+#pragma unroll
+            for (int s8 = 0; s8 < 8; ++s8) {
+              const int j0 = 2 * s8, j1 = 2 * s8 + 1;
+              kstep_ex(8 * ch + s8, win_hi(w0, j0, kw_lane), win_hi(w1, j0, kw_lane), win_hi(w0, j1, kw_lane),
+                       win_hi(w1, j1, kw_lane), win_lo(w0, j0, kw_lane, lutK3L), win_lo(w1, j0, kw_lane, lutK3L),
+                       win_lo(w0, j1, kw_lane, lutK3L), win_lo(w1, j1, kw_lane, lutK3L));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int jw = 0; jw < Cfg::kWK / 4; ++jw) {
+            const uint32_t w0 = ld32(kbase[t] + r * kts + (c + 4 * jw) * 4);
+            const uint32_t w1 = ld32(kbase[t] + (r + 8) * kts + (c + 4 * jw) * 4);
+#pragma unroll
+            for (int e2 = 0; e2 < Cfg::kPWK; e2 += 2)
+              kstep_ex((jw * Cfg::kPWK + e2) >> 1, k_hi(w0, e2), k_hi(w1, e2), k_hi(w0, e2 + 1), k_hi(w1, e2 + 1),
+                       k_lo(w0, e2), k_lo(w1, e2), k_lo(w0, e2 + 1), k_lo(w1, e2 + 1));
           }
         }
         // sacc1 (key_hi * q_lo) and sacc2 (key_lo * q) each carry one 2^12 scale
@@ -856,26 +978,41 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
               bu[nt][1] = __byte_perm(z1, 0u, sel_b);
             }
           }
+          // m-tile i: the A fragment (pairs q = 2i (row r), 2i+1 (row r+8) of tokens t0, t1)
+          auto vstep = [&](int i, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t l0, uint32_t l1,
+                           uint32_t l2, uint32_t l3) {
 #pragma unroll
-          for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
-            const uint32_t wa = ld32(vbase[t] + t0 * vts + (r + 8 * jw) * 4);
-            const uint32_t wb = ld32(vbase[t] + t1 * vts + (r + 8 * jw) * 4);
+            for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
+            if (EXV) {
 #pragma unroll
-            for (int e = 0; e < Cfg::kPWV; e += 2) {
-              const int i = (jw * Cfg::kPWV + e) >> 1;  // m-tile: pairs q = 2i (row r), 2i+1 (row r+8)
-              const uint32_t a0 = v_lookup(wa, e), a1 = v_lookup(wa, e + 1);
-              const uint32_t a2 = v_lookup(wb, e), a3 = v_lookup(wb, e + 1);
-#pragma unroll
-              for (int nt = 0; nt < Cfg::kNT; ++nt) mma16816(o_acc[nt][i], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
-              if (EXV) {
-                const uint32_t l0 = v_lookup_lo(wa, e), l1 = v_lookup_lo(wa, e + 1);
-                const uint32_t l2 = v_lookup_lo(wb, e), l3 = v_lookup_lo(wb, e + 1);
-#pragma unroll
-                for (int nt = 0; nt < Cfg::kNT; ++nt) {
-                  mma16816(o_acc[nt][i], l0, l1, l2, l3, bu[nt][0], bu[nt][1]);  // V_lo 2^12 * P' 2^-12
-                  mma16816(o_acc[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);  // V_hi * P'_lo
-                }
+              for (int nt = 0; nt < Cfg::kNT; ++nt) {
+                mma16816(o_acc[nt][i], l0, l1, l2, l3, bu[nt][0], bu[nt][1]);  // V_lo 2^12 * P' 2^-12
+                mma16816(o_acc[nt][i], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);  // V_hi * P'_lo
               }
+            }
+          };
+          if constexpr (Cfg::kWin) {
+            uint32_t wa[5], wb[5];
+            v_window(vbase[t] + t0 * vts, wa);
+            v_window(vbase[t] + t1 * vts, wb);
+#pragma unroll
+            for (int i = 0; i < Cfg::kMTiles; ++i) {
+              const int j0 = 2 * i, j1 = 2 * i + 1;
+              // the remainder lookups are dead code (and dropped) unless EXV
+              vstep(i, win_hi(wa, j0, vw_lane), win_hi(wa, j1, vw_lane), win_hi(wb, j0, vw_lane),
+                    win_hi(wb, j1, vw_lane), win_lo(wa, j0, vw_lane, lutV3L), win_lo(wa, j1, vw_lane, lutV3L),
+                    win_lo(wb, j0, vw_lane, lutV3L), win_lo(wb, j1, vw_lane, lutV3L));
+            }
+          } else {
+#pragma unroll
+            for (int jw = 0; jw < Cfg::kWV / 8; ++jw) {
+              const uint32_t wa = ld32(vbase[t] + t0 * vts + (r + 8 * jw) * 4);
+              const uint32_t wb = ld32(vbase[t] + t1 * vts + (r + 8 * jw) * 4);
+#pragma unroll
+              for (int e = 0; e < Cfg::kPWV; e += 2)
+                vstep((jw * Cfg::kPWV + e) >> 1, v_lookup(wa, e), v_lookup(wa, e + 1), v_lookup(wb, e),
+                      v_lookup(wb, e + 1), v_lookup_lo(wa, e), v_lookup_lo(wa, e + 1), v_lookup_lo(wb, e),
+                      v_lookup_lo(wb, e + 1));
             }
           }
         }
@@ -943,7 +1080,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         *reinterpret_cast<uint32_t*>(lutT + f * 256 + copy * 4) = __byte_perm(pa, pb, 0x5410);
         if (copy == 0) *reinterpret_cast<uint32_t*>(lutL + f * 4) = __byte_perm(pa, pb, 0x7632);
       }
-    } else {
+    } else if (KB == 2) {
       for (int f = tid; f < 16; f += 32 * ncons) {
         __half ha, la, hb, lb;
         split_half(__ldg(a.k_centroids + (f & 3)) * args.k_alpha, ha, la);
@@ -966,7 +1103,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         *reinterpret_cast<uint32_t*>(lutT + f * 256 + 128 + copy * 4) = __byte_perm(pa, pb, 0x5410);
         if (copy == 0) *reinterpret_cast<uint32_t*>(lutVL + f * 4) = __byte_perm(pa, pb, 0x7632);
       }
-    } else {
+    } else if (VB == 2) {
       for (int f = tid; f < 16; f += 32 * ncons) {
         __half ha, la, hb, lb;
         split_half(__ldg(a.v_centroids + (f & 3)) * args.v_alpha, ha, la);
@@ -976,6 +1113,32 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         v.x = *reinterpret_cast<uint32_t*>(&hi2);
         v.y = *reinterpret_cast<uint32_t*>(&lo2);
         *reinterpret_cast<uint2*>(lutV2 + f * 8) = v;
+      }
+    }
+    if constexpr (Cfg::kWin) {
+      // window-mode tables, one copy per lane.  3-bit: entry f = the fp16 hi parts of
+      // (c[f & 7], c[f >> 3]), their remainders (x 2^12) in one copy.  5-bit: entry e =
+      // (fp16 hi, fp16 lo x 2^12) of c[e].
+#pragma unroll
+      for (int comp = 0; comp < 2; ++comp) {
+        const float* cents = comp == 0 ? a.k_centroids : a.v_centroids;
+        const float alpha = comp == 0 ? args.k_alpha : args.v_alpha;
+        unsigned char* tab = comp == 0 ? lutKW : lutVW;
+        unsigned char* tlo = comp == 0 ? lutK3L : lutV3L;
+        __half hi_l, lo_l;
+        split_half(__ldg(cents + (lane & (KB == 3 ? 7 : 31))) * alpha, hi_l, lo_l);
+        const uint32_t pair_l = (uint32_t)__half_as_ushort(hi_l) | ((uint32_t)__half_as_ushort(lo_l) << 16);
+        for (int i = tid; i < Cfg::kTabEntries * 32; i += 32 * ncons) {
+          const int f = i >> 5, copy = i & 31;
+          if (KB == 3) {
+            const uint32_t pa = __shfl_sync(kFullMask, pair_l, f & 7);  // (hi, lo) of c[f & 7]
+            const uint32_t pb = __shfl_sync(kFullMask, pair_l, f >> 3);
+            *reinterpret_cast<uint32_t*>(tab + f * 128 + copy * 4) = __byte_perm(pa, pb, 0x5410);
+            if (copy == 0) *reinterpret_cast<uint32_t*>(tlo + f * 4) = __byte_perm(pa, pb, 0x7632);
+          } else {
+            *reinterpret_cast<uint32_t*>(tab + f * 128 + copy * 4) = __shfl_sync(kFullMask, pair_l, f);
+          }
+        }
       }
     }
   asm volatile("bar.sync 1, %0;\n" ::"r"(32 * ncons) : "memory");  // consumer warps only
@@ -1119,8 +1282,8 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   t.k_alpha = a.k_alpha > 0.f ? a.k_alpha : 1.0f;
   t.wait_tries = wait_tries();
 
-  // Shared-memory layout: [misc | buffers ... | T (64 KB, at a 64 KB aligned shared
-  // address) | buffers ...].  Dynamic shared memory starts right after the per-block
+  // Shared-memory layout: [misc | buffers ... | table region (T: 64 KB at a 64 KB aligned
+  // shared address; 3-bit pair tables: 16 KB at an 8 KB aligned one) | buffers ...].  Dynamic shared memory starts right after the per-block
   // reserved bytes in the shared window (the kernel checks the T alignment it gets).
   int dev = 0, reserved = 0, max_dyn = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -1130,16 +1293,16 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   t.buf_bytes = (t.k_slab_smem + t.v_slab_smem + 127) / 128 * 128;
   int total_bufs = 0;
   t.buf_lo = kMiscBytes;
-  if (Cfg::kHasT) {
-    int t_off = (65536 - reserved % 65536) % 65536;
-    while (t_off < kMiscBytes) t_off += 65536;
+  if (Cfg::kTBytes > 0) {
+    int t_off = (Cfg::kTAlign - reserved % Cfg::kTAlign) % Cfg::kTAlign;
+    while (t_off < kMiscBytes) t_off += Cfg::kTAlign;
     t.t_off = t_off;
     t.n_lo = (t_off - kMiscBytes) / t.buf_bytes;
     t.buf_hi = t_off + Cfg::kTBytes;
     total_bufs = t.n_lo + std::max(0, (max_dyn - t.buf_hi) / t.buf_bytes);
   } else {
     t.t_off = 0;
-    t.n_lo = (max_dyn - kMiscBytes) / t.buf_bytes;
+    t.n_lo = (max_dyn - t.buf_lo) / t.buf_bytes;
     t.buf_hi = 0;
     total_bufs = t.n_lo;
   }
@@ -1147,11 +1310,11 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   if (t.nst < 2) return cudaErrorInvalidConfiguration;
   const int nbuf = t.nst * WPH;
   size_t smem = 0;
-  if (Cfg::kHasT) {
+  if (Cfg::kTBytes > 0) {
     smem = (size_t)t.t_off + Cfg::kTBytes;
     if (nbuf > t.n_lo) smem = (size_t)t.buf_hi + (size_t)(nbuf - t.n_lo) * t.buf_bytes;
   } else {
-    smem = (size_t)kMiscBytes + (size_t)nbuf * t.buf_bytes;
+    smem = (size_t)t.buf_lo + (size_t)nbuf * t.buf_bytes;
   }
 
   const int B = a.batch, Hq = a.num_q_heads;
@@ -1185,8 +1348,8 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
 }
 
 
-// Instantiations: D 128 (2 blocks per stage) and 256 (1) x all 2/4-bit combos x G 4/8, and
-// D 64 at 4/4 bits.
+// Instantiations: D 128 (2 blocks per stage) and 256 (1) x all 2/4-bit combos, 3/3 and 5/5
+// bits x G 4/8, and D 64 at 4/4 bits.
 cudaError_t launch_decode_tc_dispatch(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
   const int G = a.num_q_heads / a.num_kv_heads;
 #define TQ_TC_CASE(D, KB, VB, GG, WPH)                                                    \
@@ -1198,6 +1361,14 @@ cudaError_t launch_decode_tc_dispatch(const DecodeArgs& a, const DecodePlan& p, 
   TQ_TC_BITS(128, 8, 2)
   TQ_TC_BITS(256, 4, 1)
   TQ_TC_BITS(256, 8, 1)
+  TQ_TC_CASE(128, 3, 3, 4, 2)
+  TQ_TC_CASE(128, 3, 3, 8, 2)
+  TQ_TC_CASE(256, 3, 3, 4, 1)
+  TQ_TC_CASE(256, 3, 3, 8, 1)
+  TQ_TC_CASE(128, 5, 5, 4, 2)
+  TQ_TC_CASE(128, 5, 5, 8, 2)
+  TQ_TC_CASE(256, 5, 5, 4, 1)
+  TQ_TC_CASE(256, 5, 5, 8, 1)
   TQ_TC_CASE(64, 4, 4, 4, 2)
   TQ_TC_CASE(64, 4, 4, 8, 2)
 #undef TQ_TC_BITS

@@ -81,6 +81,19 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(kFullMask, v, m);
   return v;
 }
+// 2^k for k in [-126, 127], from its bits.
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+// x * 2^k, exact while the result is representable, for |k| <= 252 (two normal factors).
+__device__ __forceinline__ float scale_pow2(float x, int k) {
+  const int a = k / 2;
+  return x * pow2i(a) * pow2i(k - a);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, m));
+  return v;
+}
 
 // Unnormalised natural-order Walsh-Hadamard transform of a D = 32 * E vector held by
 // one warp, lane l owning elements [l*E, l*E + E).  Strides below E are butterflies

@@ -67,11 +67,32 @@ write_rows_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads,
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < E; ++i) ss = fmaf(v[i], v[i], ss);
-    const float nu = sqrtf(warp_sum(ss));
+    ss = warp_sum(ss);
+    // A row whose sum of squares leaves [2^-100, 2^100] is scaled by an exact power of two
+    // 2^-ex from its largest |x| first (u is scale free; the norm is scaled back).
+    int ex = 0;
+    if (!(ss >= 0x1p-100f && ss <= 0x1p100f)) {
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < E; ++i) m = fmaxf(m, fabsf(v[i]));
+      m = warp_max(m);
+      if (m > 0.f && m <= 3.402823466e38f) {  // zero and non-finite rows keep their sums
+        frexpf(m, &ex);
+        ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          v[i] = scale_pow2(v[i], -ex);
+          ss = fmaf(v[i], v[i], ss);
+        }
+        ss = warp_sum(ss);
+      }
+    }
+    const float nu_s = sqrtf(ss);  // norm of the (scaled) row
+    const float nu = scale_pow2(nu_s, ex);
 #pragma unroll
     for (int i = 0; i < E; ++i) v[i] *= sg[i];
     fwht_warp<E>(v);
-    const float inv = nu > 0.f ? inv_sqrt_d / nu : 0.f;  // y = H(s*x)/(sqrt(D) nu)
+    const float inv = nu_s > 0.f ? inv_sqrt_d / nu_s : 0.f;  // y = H(s*x)/(sqrt(D) nu)
 
     for (int w = lane; w < row_words; w += 32) buf[w] = 0u;
     __syncwarp();

@@ -1,4 +1,5 @@
-// Tensor-core packed-KV row writer (fp16 / bf16 rows, head_dim 64, 128 or 256, 2 to 5 bits).
+// Tensor-core packed-KV row writer (fp16 / bf16 rows at head_dim 64, 128 or 256, fp32 rows at
+// 64 or 128; 2 to 5 bits).
 //
 // TurboQuant docs: "vLLM Usage" (TQ Byte Layout, Slot Mapping, TQ Packed Page Contract:
 // write_tq4_kv) and "Architecture" (PackedPageCache).
@@ -10,7 +11,10 @@
 //    accumulator), followed by the H_{D/16} butterflies across blocks, in registers.
 //    (D = 256: the signs flip the A operand instead -- an XOR of fp16 sign bits -- and B
 //    is H_16 itself, which keeps 32 sign masks in registers instead of 64 B fragments;
-//    one CTA of 8 warps per SM.)
+//    one CTA of 8 warps per SM.)  fp32 rows are split exactly into three bf16 parts,
+//    x = hi + mid + lo (8 significant bits each), and the three MMAs accumulate into one
+//    fp32 result; the products with +-1 are exact, so only the fp32 accumulation rounds,
+//    as in an fp32 transform.
 //  * Norm.  ||y||^2 = D ||x||^2: a sum of the thread's squares plus two quad shuffles.
 //  * Quantiser.  u = y / sqrt(sum y^2) lies in [-1, 1]; N equal cells cover that range
 //    and each stores (number of decision points below the cell, the first decision point
@@ -81,6 +85,30 @@ __device__ __forceinline__ void mma_rot<__nv_bfloat16>(float (&d)[4], uint32_t a
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
+// d = A * B + d, bf16 operands (the parts of fp32 rows)
+__device__ __forceinline__ void mma_acc_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Exact split of two fp32 values into three bf16 pairs: x = hi + mid + lo.  Each
+// difference below is exact in fp32 (it keeps the low bits of a number within a factor of
+// two of the one rounded), and what is left after two roundings to 8 significant bits has
+// at most 8 of its own.
+__device__ __forceinline__ void split3_bf16(float2 x, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+  const float2 minus1 = make_float2(-1.f, -1.f);
+  const float2 r1 = __ffma2_rn(__bfloat1622float2(h), minus1, x);  // x - hi, exact
+  const __nv_bfloat162 m = __floats2bfloat162_rn(r1.x, r1.y);
+  const float2 r2 = __ffma2_rn(__bfloat1622float2(m), minus1, r1);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(r2.x, r2.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  mid = *reinterpret_cast<const uint32_t*>(&m);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // +-1 pair in the operand type: sign bits of the two halves from s0, s1 (true = negative)
 template <typename T>
 __device__ __forceinline__ uint32_t pm1_pair(bool neg0, bool neg1) {
@@ -134,12 +162,22 @@ __device__ bool choose_grid(const float* b, int m, int lane, float& q_a, float& 
   return false;
 }
 
+// CTAs per SM: one where the raw tiles of 8 warps take 8 KB each (16 rows of 256 fp16 or of
+// 128 fp32 coordinates), two otherwise.
+template <typename T, int D>
+constexpr int write_tc_ctas_per_sm() {
+  return D * (int)sizeof(T) >= 512 ? 1 : 2;
+}
+
 template <typename T, int D, int BITS>
-__global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kernel(WriteTcArgs args) {
+__global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D>()) write_tc_kernel(WriteTcArgs args) {
+  constexpr bool kF32Rows = std::is_same<T, float>::value;
+  using OpT = typename std::conditional<kF32Rows, __nv_bfloat16, T>::type;  // MMA operand type
+  static_assert(!kF32Rows || D <= 128, "fp32 rows at head_dim 64 or 128");
   constexpr int NB = D / 16;            // 16-column blocks
   constexpr int RB = D * BITS / 8 + 4;  // row bytes
   constexpr int IB = D * BITS / 8;      // index bytes
-  constexpr int ROWB = D * 2;           // raw row bytes
+  constexpr int ROWB = D * (int)sizeof(T);  // raw row bytes
   constexpr int TILE_BYTES = 16 * ROWB;
   const WriteArgs& a = args.a;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -225,7 +263,7 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
         const bool s1 = kSignOnA ? false : (__ldg(a.signs + 16 * j + k1) < 0.f);
         const bool n0 = s0 ^ (__popc(k0 & n) & 1);
         const bool n1 = s1 ^ (__popc(k1 & n) & 1);
-        bfr[j][nt][part] = pm1_pair<T>(n0, n1);
+        bfr[j][nt][part] = pm1_pair<OpT>(n0, n1);
       }
     }
   }
@@ -293,6 +331,29 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
     // acc[j][nt] = (row r: cols 2c, 2c+1 | row r+8: cols 2c, 2c+1) of block j, n-tile nt
     float acc[NB][2][4];
     const uint32_t tbase = smem_addr(raw_buf + buf * TILE_BYTES);
+    if constexpr (kF32Rows) {
+      // A fragment of block j from the fp32 tile: a0 row r cols 16j + 2c, +1; a1 row r + 8;
+      // a2, a3 the same at cols + 8 (8-byte loads from the swizzled 16-byte chunks)
+      const unsigned char* tb = raw_buf + buf * TILE_BYTES;
+      auto ld2 = [&](int row, int col) -> float2 {
+        const int chunk = col >> 2;
+        return *reinterpret_cast<const float2*>(tb + row * ROWB + ((chunk ^ (row & 7)) << 4) + (col & 3) * 4);
+      };
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        uint32_t h[4], m[4], l[4];
+        split3_bf16(ld2(r, 16 * j + 2 * c), h[0], m[0], l[0]);
+        split3_bf16(ld2(r + 8, 16 * j + 2 * c), h[1], m[1], l[1]);
+        split3_bf16(ld2(r, 16 * j + 2 * c + 8), h[2], m[2], l[2]);
+        split3_bf16(ld2(r + 8, 16 * j + 2 * c + 8), h[3], m[3], l[3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          mma_rot<OpT>(acc[j][nt], h[0], h[1], h[2], h[3], bfr[j][nt][0], bfr[j][nt][1]);
+          mma_acc_bf16(acc[j][nt], m[0], m[1], m[2], m[3], bfr[j][nt][0], bfr[j][nt][1]);
+          mma_acc_bf16(acc[j][nt], l[0], l[1], l[2], l[3], bfr[j][nt][0], bfr[j][nt][1]);
+        }
+      }
+    } else {
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
       // ldmatrix.x4: lanes 0-7 rows 0-7 cols 16j..+7, 8-15 rows 8-15, 16-23 rows 0-7 cols +8, 24-31 rows 8-15 cols +8
@@ -309,6 +370,7 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
       const int jb = kSignOnA ? 0 : j;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) mma_rot<T>(acc[j][nt], a0, a1, a2, a3, bfr[jb][nt][0], bfr[jb][nt][1]);
+    }
     }
     const float2 minus1 = make_float2(-1.f, -1.f);
 #pragma unroll
@@ -332,23 +394,59 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
       }
     }
     // ---- norms of rows r (e = 0, 1) and r + 8 (e = 2, 3) -----------------------------
-    float2 ssv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // row r: independent chains
-    float2 ssw[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // row r + 8
+    auto row_sums = [&](float& ss0, float& ss1) {
+      float2 ssv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // row r: independent chains
+      float2 ssw[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // row r + 8
 #pragma unroll
-    for (int j = 0; j < NB; ++j)
+      for (int j = 0; j < NB; ++j)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float2 p = make_float2(acc[j][nt][0], acc[j][nt][1]);
-        const float2 q = make_float2(acc[j][nt][2], acc[j][nt][3]);
-        ssv[nt] = __ffma2_rn(p, p, ssv[nt]);
-        ssw[nt] = __ffma2_rn(q, q, ssw[nt]);
-      }
-    float ss0 = (ssv[0].x + ssv[0].y) + (ssv[1].x + ssv[1].y);
-    float ss1 = (ssw[0].x + ssw[0].y) + (ssw[1].x + ssw[1].y);
-    ss0 += __shfl_xor_sync(kFullMask, ss0, 1);
-    ss0 += __shfl_xor_sync(kFullMask, ss0, 2);
-    ss1 += __shfl_xor_sync(kFullMask, ss1, 1);
-    ss1 += __shfl_xor_sync(kFullMask, ss1, 2);
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 p = make_float2(acc[j][nt][0], acc[j][nt][1]);
+          const float2 q = make_float2(acc[j][nt][2], acc[j][nt][3]);
+          ssv[nt] = __ffma2_rn(p, p, ssv[nt]);
+          ssw[nt] = __ffma2_rn(q, q, ssw[nt]);
+        }
+      ss0 = (ssv[0].x + ssv[0].y) + (ssv[1].x + ssv[1].y);
+      ss1 = (ssw[0].x + ssw[0].y) + (ssw[1].x + ssw[1].y);
+      ss0 += __shfl_xor_sync(kFullMask, ss0, 1);
+      ss0 += __shfl_xor_sync(kFullMask, ss0, 2);
+      ss1 += __shfl_xor_sync(kFullMask, ss1, 1);
+      ss1 += __shfl_xor_sync(kFullMask, ss1, 2);
+    };
+    float ss0, ss1;
+    row_sums(ss0, ss1);
+    // A row whose sum of squares leaves [2^-100, 2^100] (coordinates beyond about 1e14 or
+    // below about 1e-16: bf16 and fp32 rows can) is brought back by an exact power of two
+    // 2^-ex taken from its largest |y|; u is scale free, and the norm is scaled back by 2^ex.
+    int ex0 = 0, ex1 = 0;
+    const bool odd0 = !(ss0 >= 0x1p-100f && ss0 <= 0x1p100f), odd1 = !(ss1 >= 0x1p-100f && ss1 <= 0x1p100f);
+    if (__any_sync(kFullMask, odd0 || odd1)) {
+      float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          m0 = fmaxf(m0, fmaxf(fabsf(acc[j][nt][0]), fabsf(acc[j][nt][1])));
+          m1 = fmaxf(m1, fmaxf(fabsf(acc[j][nt][2]), fabsf(acc[j][nt][3])));
+        }
+      m0 = fmaxf(m0, __shfl_xor_sync(kFullMask, m0, 1));
+      m0 = fmaxf(m0, __shfl_xor_sync(kFullMask, m0, 2));
+      m1 = fmaxf(m1, __shfl_xor_sync(kFullMask, m1, 1));
+      m1 = fmaxf(m1, __shfl_xor_sync(kFullMask, m1, 2));
+      // zero rows and non-finite rows keep their sums (handled below)
+      if (odd0 && m0 > 0.f && m0 <= 3.402823466e38f) frexpf(m0, &ex0);
+      if (odd1 && m1 > 0.f && m1 <= 3.402823466e38f) frexpf(m1, &ex1);
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          acc[j][nt][0] = scale_pow2(acc[j][nt][0], -ex0);
+          acc[j][nt][1] = scale_pow2(acc[j][nt][1], -ex0);
+          acc[j][nt][2] = scale_pow2(acc[j][nt][2], -ex1);
+          acc[j][nt][3] = scale_pow2(acc[j][nt][3], -ex1);
+        }
+      row_sums(ss0, ss1);
+    }
     // ||x|| = sqrt(ss / D); u = y / sqrt(ss); grid coordinate g = u * q_a + q_b.
     // Every partial sum above only grows, so y^2 <= ss (1 + 2^-23) + 2^-150 for each y of
     // the row, even when ss is subnormal; adding 2^-149 under the root keeps |u| within a
@@ -358,7 +456,7 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
     // and the stored norm ss * rsqrt(ss) / sqrt(D) by < 1e-6 relative.
     const float rs0 = rsqrtf(ss0 + 0x1p-149f), rs1 = rsqrtf(ss1 + 0x1p-149f);
     const float inv_sqrt_d = 1.0f / sqrtf((float)D);
-    float nu0 = ss0 * rs0 * inv_sqrt_d, nu1 = ss1 * rs1 * inv_sqrt_d;
+    float nu0 = scale_pow2(ss0 * rs0 * inv_sqrt_d, ex0), nu1 = scale_pow2(ss1 * rs1 * inv_sqrt_d, ex1);
     const float ga0 = q_a * rs0, ga1 = q_a * rs1;
     // A NaN or infinite input (the only way to a non-finite sum) would give a NaN grid
     // coordinate, whose bits address nothing: such rows are quantised as zero rows.
@@ -482,7 +580,7 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 256 ? 1 : 2) write_tc_kerne
 }  // namespace
 
 bool write_tc_supported(const WriteArgs& a) {
-  const bool dt = a.dtype == kF16 || a.dtype == kBF16;
+  const bool dt = a.dtype == kF16 || a.dtype == kBF16 || (a.dtype == kF32 && a.head_dim <= 128);
   const bool hd = a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256;
   const bool bt = a.bits >= 2 && a.bits <= 5;
   return dt && hd && bt && a.num_kv_heads >= 1;
@@ -513,13 +611,16 @@ cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
 #define TQ_WTC(T, D, BITS)                                                                                    \
   if (a.head_dim == D && a.bits == BITS) {                                                                    \
     constexpr int RB = D * BITS / 8 + 4;                                                                      \
-    const size_t smem = kQCells * kQCopies * sizeof(QCell) + kWWarps * (2 * 16 * D * 2 + 16 * RB + 16);      \
+    const size_t smem = kQCells * kQCopies * sizeof(QCell) + kWWarps * (2 * 16 * D * sizeof(T) + 16 * RB + 16); \
     auto kern = write_tc_kernel<T, D, BITS>;                                                                  \
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
     if (err != cudaSuccess) return err;                                                                       \
     return launch_dependent(kern, grid, smem, stream, t);                                                     \
   }
-  if (a.dtype == kF16) {
+  if (a.dtype == kF32) {
+    TQ_WTC(float, 64, 2) TQ_WTC(float, 64, 3) TQ_WTC(float, 64, 4) TQ_WTC(float, 64, 5)
+    TQ_WTC(float, 128, 2) TQ_WTC(float, 128, 3) TQ_WTC(float, 128, 4) TQ_WTC(float, 128, 5)
+  } else if (a.dtype == kF16) {
     TQ_WTC(__half, 64, 2) TQ_WTC(__half, 64, 3) TQ_WTC(__half, 64, 4) TQ_WTC(__half, 64, 5)
     TQ_WTC(__half, 128, 2) TQ_WTC(__half, 128, 3) TQ_WTC(__half, 128, 4) TQ_WTC(__half, 128, 5)
     TQ_WTC(__half, 256, 2) TQ_WTC(__half, 256, 3) TQ_WTC(__half, 256, 4) TQ_WTC(__half, 256, 5)

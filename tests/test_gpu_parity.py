@@ -296,9 +296,11 @@ def test_decode_empty_batch(tq):
 
 
 # ---------------------------------------------------------------- tensor-core decode edge cases
-# (block size 16, K/V bits in {2, 4}, GQA group 4 or 8: the shapes the tensor-core kernel takes)
+# (block size 16, K/V bits in {2, 4}, both 3 or both 5, GQA group 4 or 8: the shapes the
+# tensor-core kernel takes)
 
-@pytest.mark.parametrize("kb,vb,hq", [(4, 4, 32), (4, 2, 32), (2, 4, 64), (2, 2, 64), (4, 2, 64)])
+@pytest.mark.parametrize("kb,vb,hq", [(4, 4, 32), (4, 2, 32), (2, 4, 64), (2, 2, 64), (4, 2, 64), (3, 3, 32),
+                                      (3, 3, 64), (5, 5, 32), (5, 5, 64)])
 def test_tc_decode_ragged_and_empty_sequences(tq, kb, vb, hq):
     # lengths with empty sequences in the middle, ragged last blocks, a single token, and
     # fewer blocks in total than there are SMs (some CTAs own no block)
@@ -310,9 +312,10 @@ def test_tc_decode_ragged_and_empty_sequences(tq, kb, vb, hq):
     assert np.all(got[1] == 0) and np.all(got[5] == 0)
 
 
-@pytest.mark.parametrize("d", [64, 256])
-def test_tc_decode_other_head_dims(tq, d):
-    w, kp, vp = _small_case(tq, d=d, h=4, hq=16, kb=4, vb=4, lens=(70, 3, 129), bs=16, seed=d)
+@pytest.mark.parametrize("d,bits,hq", [(64, 4, 16), (256, 4, 16), (256, 3, 16), (256, 3, 32), (256, 5, 16),
+                                       (256, 5, 32)])
+def test_tc_decode_other_head_dims(tq, d, bits, hq):
+    w, kp, vp = _small_case(tq, d=d, h=4, hq=hq, kb=bits, vb=bits, lens=(70, 3, 129), bs=16, seed=d + bits)
     got, st = gpu_decode(tq, w, kp, vp)
     assert st == 0
     assert_decode_close(got, oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(d)))
@@ -355,7 +358,9 @@ def test_tc_decode_many_short_sequences(tq):
 # (fp16 / bf16 rows, head_dim 64, 128 or 256, 2 to 5 bits; H dividing the 16-row tile or
 # not; 3- and 5-bit fields cross bytes; D 256 puts the signs on the A operand)
 
-@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+# fp32 rows: the tensor-core writer at D 64 / 128 (three exact bf16 parts), the SIMT writer at
+# D 256
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("d,bits", [(64, 2), (64, 3), (64, 4), (64, 5), (128, 2), (128, 3), (128, 4), (128, 5),
                                     (256, 2), (256, 3), (256, 4), (256, 5)])
 @pytest.mark.parametrize("h", [1, 3, 8, 16])
@@ -366,7 +371,7 @@ def test_tc_writer_shapes(tq, dtype, d, bits, h):
     raw32[5] = 0.0  # an all-zero token
     slots = rng.permutation(48)[:t].astype(np.int64)
     slots[rng.random(t) < 0.2] = -1
-    raw_t = torch.from_numpy(raw32).to(torch.float16 if dtype == "f16" else torch.bfloat16)
+    raw_t = torch.from_numpy(raw32).to({"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[dtype])
     raw_exact = raw_t.float().numpy()
     pages = torch.zeros(12, 4, h, o.row_bytes(d, bits), dtype=torch.uint8, device="cuda")
     st = tq.tq_write_kv(raw_t.cuda(), pages, torch.from_numpy(slots).cuda(), tq.tq_build_rotation(d, 42, "cuda"),
@@ -375,6 +380,30 @@ def test_tc_writer_shapes(tq, dtype, d, bits, h):
     pages_np = pages.cpu().numpy()
     check_written_rows(pages_np, raw_exact, slots, bits, OracleCodec(d))
     check_untouched(pages_np, slots)
+
+
+@pytest.mark.parametrize("d,dtype", [(64, torch.float32), (128, torch.float32), (256, torch.float32),
+                                     (64, torch.bfloat16), (128, torch.bfloat16), (256, torch.bfloat16)])
+def test_writer_rows_across_the_fp32_range(tq, d, dtype):
+    # rows from 1e-25 to 1e30 in scale, and one along an axis at 3e38 (far outside fp16's
+    # range, inside bf16's and fp32's): their sums of squares leave fp32's range, so the
+    # writers rescale them by an exact power of two first; u is scale free.  fp32 at D 64 /
+    # 128 and bf16 take the tensor-core writer (fp32 rows as three exact bf16 parts, all
+    # normal numbers at these scales), fp32 at D 256 the SIMT writer.
+    rng = np.random.default_rng(11 + d)
+    t, h = 61, 4
+    raw32 = rng.standard_normal((t, h, d)).astype(np.float32)
+    raw32 *= (10.0 ** rng.uniform(-25, 30, (t, h, 1))).astype(np.float32)
+    raw32[7, 2, :] = 0.0
+    raw32[9, 1, :] = 0.0
+    raw32[9, 1, 3] = 3e38  # a row along one axis, near the top of the range
+    raw_t = torch.from_numpy(raw32).to(dtype)
+    slots = np.arange(t, dtype=np.int64)
+    pages = torch.zeros(4, 16, h, o.row_bytes(d, 4), dtype=torch.uint8, device="cuda")
+    st = tq.tq_write_kv(raw_t.cuda(), pages, torch.from_numpy(slots).cuda(), tq.tq_build_rotation(d, 42, "cuda"),
+                        lib_codebook(tq, d, 4), check=False)
+    assert int(st.item()) == 0
+    check_written_rows(pages.cpu().numpy(), raw_t.float().numpy(), slots, 4, OracleCodec(d))
 
 
 def test_tc_writer_large_values_and_tiny_rows(tq):
@@ -392,14 +421,15 @@ def test_tc_writer_large_values_and_tiny_rows(tq):
     check_written_rows(pages.cpu().numpy(), raw_t.float().numpy(), slots, 4, OracleCodec(128))
 
 
-@pytest.mark.parametrize("d,bits", [(256, 5), (256, 3), (128, 5), (64, 5)])
-def test_index_flip_rate_at_scale(tq, d, bits):
+@pytest.mark.parametrize("d,bits,dt", [(256, 5, np.float16), (256, 3, np.float16), (128, 5, np.float16),
+                                       (64, 5, np.float16), (128, 5, np.float32), (64, 3, np.float32)])
+def test_index_flip_rate_at_scale(tq, d, bits, dt):
     # the index-byte bar measured as a rate: 3.4e7 coordinates of the densest codebooks
-    # (fp16 rows N(0,1) times a lognormal(0, 0.5) scale per (head, channel), 8 heads),
-    # every exception within 1e-6 of a decision point and fewer than 1e-5 of all
+    # (rows N(0,1) times a lognormal(0, 0.5) scale per (head, channel), 8 heads, fp16 or
+    # fp32), every exception within 1e-6 of a decision point and fewer than 1e-5 of all
     rng = np.random.default_rng(7 + d + bits)
     ntok, h = 33_554_432 // (8 * d), 8
-    raw = (rng.standard_normal((ntok, h, d)) * rng.lognormal(0, 0.5, (h, d))).astype(np.float16)
+    raw = (rng.standard_normal((ntok, h, d)) * rng.lognormal(0, 0.5, (h, d))).astype(dt)
     slots = np.arange(ntok, dtype=np.int64)
     pages, st = gpu_write(tq, raw, slots, ntok // 16, 16, bits)
     assert st == 0
