@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[t][e] = 0.f;
     if (!exact) {
-      // G = 4: columns 0-3 get key_hi * q_hi, 4-7 key_hi * q_lo; one tile runs its even and
+      // G = 4: columns 0-3 get key_hi * q_hi, 4-7 key_hi * q_lo; each tile runs its even and
       // odd k-steps as two chains.  G = 8: a q_lo chain per tile.
       float sacc1[NTL][4];
 #pragma unroll
@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
           mma16816(sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
           mma16816(sacc1[t], h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
         } else {
-          mma16816((NTL == 1 && (s & 1)) ? sacc1[t] : sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
+          mma16816((s & 1) ? sacc1[t] : sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
         }
       };
       if constexpr (Cfg::kWin) {
@@ -1046,6 +1046,19 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   };
   using One = std::integral_constant<int, 1>;
   using Two = std::integral_constant<int, 2>;
+  // Whether the tile of block buffer `kblk` (ntok valid rows) takes an exact path: the
+  // same vote as in `tiles`, from the row norms alone.
+  auto tile_exact = [&](const unsigned char* kblk, int ntok) -> bool {
+    const unsigned char* kb = kblk + h * Cfg::kRBK;
+    const unsigned char* vb = kblk + args.k_slab_smem + h * Cfg::kRBV;
+    float k0 = fabsf(__uint_as_float(ld32(kb + r * kts + Cfg::kWK * 4)));
+    float k1 = fabsf(__uint_as_float(ld32(kb + (r + 8) * kts + Cfg::kWK * 4)));
+    float v0 = __uint_as_float(ld32(vb + r * vts + Cfg::kWV * 4));
+    float v1 = __uint_as_float(ld32(vb + (r + 8) * vts + Cfg::kWV * 4));
+    if (r >= ntok) k0 = v0 = 0.f;
+    if (r + 8 >= ntok) k1 = v1 = 0.f;
+    return __any_sync(kFullMask, fmaxf(v0, v1) > kFastValueNorm || fmaxf(k0, k1) * qnorm_max > kFastScoreBound);
+  };
 
   // ---- main pipeline -----------------------------------------------------------------
   // Stage st lives in ring slot st % nst; full[slot] completes when its copies landed,
@@ -1156,10 +1169,15 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
     }
     const BlockMeta m0 = meta[slot * WPH];
     const BlockMeta m1 = meta[slot * WPH + WPH - 1];
-    if (WPH == 2 && m0.ntok == kBS && m0.valid && m1.ntok != 0 && m1.valid && m1.b == m0.b) {
+    bool fused = WPH == 2 && m0.ntok == kBS && m0.valid && m1.ntok != 0 && m1.valid && m1.b == m0.b;
+    if (fused) {
       if (m0.b != cur_b) enter_sequence(m0.b);
-      tiles(Two{}, smem + buf_off(slot, 0), smem + buf_off(slot, 1), m1.ntok);
-    } else {
+      // a fused step runs the slower exact path for both tiles if either needs it: when
+      // only one does (rows of large norm are rare), the tiles run one at a time
+      fused = tile_exact(smem + buf_off(slot, 0), kBS) == tile_exact(smem + buf_off(slot, 1), m1.ntok);
+      if (fused) tiles(Two{}, smem + buf_off(slot, 0), smem + buf_off(slot, 1), m1.ntok);
+    }
+    if (!fused) {
 #pragma unroll
       for (int u = 0; u < WPH; ++u) {
         const BlockMeta m = u == 0 ? m0 : m1;

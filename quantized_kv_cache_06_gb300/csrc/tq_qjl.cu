@@ -10,7 +10,8 @@
 // an estimate of <q, x> that is unbiased over the draw of S.  Values stay MSE rows.
 //
 // Kernels:
-//   write_prod_kernel       one warp per (token, head) row: norm, rotation (warp FWHT),
+//   write_prod_kernel       (shapes without the tensor-core writer of tq_write_tc.cu: fp32
+//                           rows at D = 128) one warp per (token, head) row: norm, rotation (warp FWHT),
 //                           indices, residual; the D projections S r come from S^T staged
 //                           in shared memory, output i = lane + 32 e, so a warp ballot per
 //                           e is directly sign word e of the row.
@@ -351,6 +352,11 @@ cudaError_t launch_write_prod(const WriteArgs& a, const float* smat, cudaStream_
   err = launch_validate_slots(a, stream, num_sms);
   if (err != cudaSuccess) return err;
   const int64_t rows = a.num_tokens * a.num_kv_heads;
+  if (write_prod_tc_supported(a)) {
+    const int64_t tiles = (rows + 15) / 16;
+    return launch_write_prod_tc(a, smat, stream,
+                                (int)std::max<int64_t>(1, std::min<int64_t>((tiles + 7) / 8, (int64_t)num_sms * 2)));
+  }
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kProdWarps - 1) / kProdWarps, (int64_t)num_sms * 3));
   const size_t smem = (size_t)a.head_dim * (a.head_dim + 1) * sizeof(float);
 #define TQ_PROD_W(T, E)                                                                                       \

@@ -28,6 +28,16 @@
 //    lane pair of coordinates, 2-bit ones a byte per quad; 3- and 5-bit fields cross
 //    bytes, so their index pairs are staged (in the raw tile buffer the MMAs have
 //    consumed) and each lane then packs 32 coordinates of a row into 3 or 5 whole words.
+//  * Product rows (PROD, "QJL residual" keys: (b - 1)-bit MSE indices, D sign bits, nu,
+//    gamma).  The quantiser also looks up c[idx] (a per-lane replicated copy of the
+//    codebook), leaving the rotated residual r = u - c[idx] in the accumulators, and
+//    gamma = ||r||.  The sketch S r is a [16 rows x D] x [D x D] product on the same
+//    m16n8k16 MMAs: the accumulator layout of r is already the A layout, split into fp16
+//    hi + lo (r scaled by 2^10, lo by 2^12 more); S sits in shared memory as fp16 hi + lo
+//    (lo x 2^12, 16-byte chunks XOR-swizzled by row for ldmatrix), and
+//    r_hi S_hi + (r_lo S_hi + r_hi S_lo) 2^-12 carries ~22 bits, so a sign flips only where
+//    the projection is within ~1e-6 of zero.  Each 32-output sign word is assembled from
+//    its quad's bits with two shuffles.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -85,6 +95,14 @@ __device__ __forceinline__ void mma_rot<__nv_bfloat16>(float (&d)[4], uint32_t a
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
+// d = A * B + d, fp16 operands (the sketch of product rows)
+__device__ __forceinline__ void mma_f16_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 // d = A * B + d, bf16 operands (the parts of fp32 rows)
 __device__ __forceinline__ void mma_acc_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                              uint32_t b0, uint32_t b1) {
@@ -123,6 +141,7 @@ struct QCell {
 
 struct WriteTcArgs {
   WriteArgs a;
+  const float* smat;  // product rows: S, fp32 [D][D] row-major
 };
 
 // Quantiser grid g = u A + B, B = A + phi with 0 < phi < 1, cell = floor(g).  u is a
@@ -163,19 +182,32 @@ __device__ bool choose_grid(const float* b, int m, int lane, float& q_a, float& 
 }
 
 // CTAs per SM: one where the raw tiles of 8 warps take 8 KB each (16 rows of 256 fp16 or of
-// 128 fp32 coordinates), two otherwise.
-template <typename T, int D>
-constexpr int write_tc_ctas_per_sm() {
-  return D * (int)sizeof(T) >= 512 ? 1 : 2;
+// 128 fp32 coordinates) or the sketch matrix takes 64 KB (product rows at D = 128), two
+// otherwise.
+template <typename T, int D, bool PROD>
+__host__ __device__ constexpr int write_tc_ctas_per_sm() {
+  return (D * (int)sizeof(T) >= 512 || (PROD && D == 128)) ? 1 : 2;
+}
+// Bytes of the shared-memory part ahead of the per-warp buffers: quantiser table, and for
+// product rows the codebook copies and S hi / lo.
+template <int D, bool PROD>
+__host__ __device__ constexpr int write_tc_fixed_smem() {
+  return kQCells * kQCopies * (int)sizeof(QCell) + (PROD ? 16 * 32 * 4 + 2 * D * D * 2 : 0);
+}
+template <int D, int BITS, bool PROD>
+__host__ __device__ constexpr int write_tc_row_bytes() {
+  return PROD ? D * BITS / 8 + D / 8 + 8 : D * BITS / 8 + 4;
 }
 
-template <typename T, int D, int BITS>
-__global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D>()) write_tc_kernel(WriteTcArgs args) {
+// Product rows: BITS is the MSE index width (b - 1).
+template <typename T, int D, int BITS, bool PROD>
+__global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>()) write_tc_kernel(WriteTcArgs args) {
   constexpr bool kF32Rows = std::is_same<T, float>::value;
   using OpT = typename std::conditional<kF32Rows, __nv_bfloat16, T>::type;  // MMA operand type
   static_assert(!kF32Rows || D <= 128, "fp32 rows at head_dim 64 or 128");
+  static_assert(!PROD || (D <= 128 && BITS >= 2 && BITS <= 4), "product rows: D 64 / 128, 2- to 4-bit indices");
   constexpr int NB = D / 16;            // 16-column blocks
-  constexpr int RB = D * BITS / 8 + 4;  // row bytes
+  constexpr int RB = write_tc_row_bytes<D, BITS, PROD>();  // row bytes
   constexpr int IB = D * BITS / 8;      // index bytes
   constexpr int ROWB = D * (int)sizeof(T);  // raw row bytes
   constexpr int TILE_BYTES = 16 * ROWB;
@@ -187,7 +219,11 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D>()) wr
 
   // shared memory: quantiser table | per warp: 2 raw tiles + 1 packed tile
   QCell* qtab = reinterpret_cast<QCell*>(smem);
-  unsigned char* wbase = smem + kQCells * kQCopies * sizeof(QCell) + warp * (2 * TILE_BYTES + 16 * RB + 16);
+  // product rows: codebook, 32 lane copies (entry k of lane l at 4 (32 k + l)); S hi, S lo
+  float* ctab = reinterpret_cast<float*>(smem + kQCells * kQCopies * sizeof(QCell));
+  unsigned char* s_hi = smem + kQCells * kQCopies * sizeof(QCell) + 16 * 32 * 4;
+  unsigned char* s_lo = s_hi + D * D * 2;
+  unsigned char* wbase = smem + write_tc_fixed_smem<D, PROD>() + warp * (2 * TILE_BYTES + 16 * RB + 16);
   unsigned char* raw_buf = wbase;
   unsigned char* pack_buf = wbase + 2 * TILE_BYTES;
 
@@ -231,6 +267,20 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D>()) wr
     q.point = point - 0.5f;  // in g' (exact, and +inf stays +inf)
 #pragma unroll
     for (int copy = 0; copy < kQCopies; ++copy) qtab[cell * kQCopies + copy] = q;
+  }
+  if constexpr (PROD) {
+    for (int i = threadIdx.x; i < NC * 32; i += blockDim.x) ctab[i] = a.centroids[i >> 5];
+    // S[n][k] (n: projection, k: coordinate) as fp16 hi and lo x 2^12, row n at 2 D n bytes,
+    // 16-byte chunk k / 8 stored at chunk (k / 8) ^ (n & 7)
+    for (int i = threadIdx.x; i < D * D; i += blockDim.x) {
+      const int n = i / D, k = i - n * D;
+      const float sv = __ldg(args.smat + i);
+      const __half hi = __float2half_rn(sv);
+      const __half lo = __float2half_rn((sv - __half2float(hi)) * 4096.0f);
+      const int off = n * (2 * D) + ((((k >> 3) ^ (n & 7))) << 4) + (k & 7) * 2;
+      *reinterpret_cast<__half*>(s_hi + off) = hi;
+      *reinterpret_cast<__half*>(s_lo + off) = lo;
+    }
   }
   __syncthreads();
 
@@ -488,6 +538,8 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D>()) wr
     // stage[rr * D / 2 + p]; the tile's raw buffer is free once its MMAs have read it
     uint16_t* stage = reinterpret_cast<uint16_t*>(raw_buf + buf * TILE_BYTES);
     static_assert(16 * D <= TILE_BYTES, "index staging must fit the raw tile buffer");
+    const uint32_t ctab_lane = smem_addr(ctab) + (uint32_t)(lane * 4);
+    float rr[2] = {0.f, 0.f};  // product rows: sum of squared residuals of rows r, r + 8
 #pragma unroll
     for (int half = 0; half < 2; ++half) {  // row r (half 0) / row r + 8 (half 1)
       const float ga = half ? ga1 : ga0;
@@ -501,6 +553,17 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D>()) wr
           const float2 m = __fadd2_rn(g, magic2);
           const uint32_t i0 = quant(g.x, m.x);
           const uint32_t i1 = quant(g.y, m.y);
+          if constexpr (PROD) {  // residual r = u - c[idx], u = y / sqrt(sum y^2)
+            const float rsh = half ? rs1 : rs0;
+            float c0, c1;
+            asm("ld.shared.f32 %0, [%1];\n" : "=f"(c0) : "r"(ctab_lane + i0 * 128u));
+            asm("ld.shared.f32 %0, [%1];\n" : "=f"(c1) : "r"(ctab_lane + i1 * 128u));
+            const float e0 = fmaf(acc[j][nt][2 * half], rsh, -c0);
+            const float e1 = fmaf(acc[j][nt][2 * half + 1], rsh, -c1);
+            acc[j][nt][2 * half] = e0;
+            acc[j][nt][2 * half + 1] = e1;
+            rr[half] = fmaf(e0, e0, fmaf(e1, e1, rr[half]));
+          }
           // columns 16 j + 8 nt + 2c, +1
           if (BITS == 3 || BITS == 5) {
             stage[(r + 8 * half) * (D / 2) + 8 * j + 4 * nt + c] = (uint16_t)(i0 | (i1 << BITS));
@@ -514,7 +577,79 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D>()) wr
           }
         }
       }
-      if (c == 0) *reinterpret_cast<float*>(prow + IB) = half ? nu1 : nu0;
+      if constexpr (PROD) {
+        rr[half] += __shfl_xor_sync(kFullMask, rr[half], 1);
+        rr[half] += __shfl_xor_sync(kFullMask, rr[half], 2);
+        if (c == 0) {
+          *reinterpret_cast<float*>(prow + IB + D / 8) = half ? nu1 : nu0;
+          *reinterpret_cast<float*>(prow + IB + D / 8 + 4) = sqrtf(rr[half]);
+        }
+      } else {
+        if (c == 0) *reinterpret_cast<float*>(prow + IB) = half ? nu1 : nu0;
+      }
+    }
+    if constexpr (PROD) {
+      // ---- sketch S r: A = r (fp16 hi / lo), B = S^T from shared memory ----------------
+      uint32_t ah[NB][4], al[NB][4];
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // q: 0 row r cols 2c.., 1 row r+8, 2 row r cols 2c+8.., 3 row r+8 cols 2c+8..
+          const int nt = q >> 1, e = 2 * (q & 1);
+          const float x0 = acc[j][nt][e] * 1024.0f, x1 = acc[j][nt][e + 1] * 1024.0f;
+          const __half2 h = __floats2half2_rn(x0, x1);
+          const float2 hf = __half22float2(h);
+          const __half2 l = __floats2half2_rn((x0 - hf.x) * 4096.0f, (x1 - hf.y) * 4096.0f);
+          ah[j][q] = *reinterpret_cast<const uint32_t*>(&h);
+          al[j][q] = *reinterpret_cast<const uint32_t*>(&l);
+        }
+      const uint32_t shi = smem_addr(s_hi), slo = smem_addr(s_lo);
+      const int mq = lane >> 3, mr = lane & 7;  // ldmatrix: this lane addresses row mr of matrix mq
+#pragma unroll 1
+      for (int w = 0; w < D / 32; ++w) {  // sign word w: outputs 32 w .. 32 w + 31 (4 n-tiles)
+        float m0[4][4], m1[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m0[nt][e] = m1[nt][e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+#pragma unroll
+          for (int np = 0; np < 2; ++np) {  // n-tiles 2 np, 2 np + 1
+            const int n = 32 * w + 16 * np + 8 * (mq >> 1) + mr;
+            const uint32_t off = (uint32_t)(n * (2 * D) + (((2 * j + (mq & 1)) ^ (n & 7)) << 4));
+            uint32_t bh[4], bl[4];
+            ldmatrix_x4(shi + off, bh[0], bh[1], bh[2], bh[3]);
+            ldmatrix_x4(slo + off, bl[0], bl[1], bl[2], bl[3]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int nt = 2 * np + u;
+              mma_f16_acc(m0[nt], ah[j][0], ah[j][1], ah[j][2], ah[j][3], bh[2 * u], bh[2 * u + 1]);
+              mma_f16_acc(m1[nt], al[j][0], al[j][1], al[j][2], al[j][3], bh[2 * u], bh[2 * u + 1]);
+              mma_f16_acc(m1[nt], ah[j][0], ah[j][1], ah[j][2], ah[j][3], bl[2 * u], bl[2 * u + 1]);
+            }
+          }
+        }
+        // bit 8 nt + 2 c + e of the word of row r (m*[nt][e]) and of row r + 8 (m*[nt][2 + e])
+        uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int bit = 8 * nt + 2 * c + e;
+            if (fmaf(m1[nt][e], 1.0f / 4096, m0[nt][e]) >= 0.f) w0 |= 1u << bit;
+            if (fmaf(m1[nt][2 + e], 1.0f / 4096, m0[nt][2 + e]) >= 0.f) w1 |= 1u << bit;
+          }
+        w0 |= __shfl_xor_sync(kFullMask, w0, 1);
+        w0 |= __shfl_xor_sync(kFullMask, w0, 2);
+        w1 |= __shfl_xor_sync(kFullMask, w1, 1);
+        w1 |= __shfl_xor_sync(kFullMask, w1, 2);
+        if (c == 0) {
+          *reinterpret_cast<uint32_t*>(pack_buf + r * RB + IB + 4 * w) = w0;
+          *reinterpret_cast<uint32_t*>(pack_buf + (r + 8) * RB + IB + 4 * w) = w1;
+        }
+      }
     }
     __syncwarp();
     if constexpr (BITS == 3 || BITS == 5) {
@@ -610,9 +745,9 @@ cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
   t.a = a;
 #define TQ_WTC(T, D, BITS)                                                                                    \
   if (a.head_dim == D && a.bits == BITS) {                                                                    \
-    constexpr int RB = D * BITS / 8 + 4;                                                                      \
-    const size_t smem = kQCells * kQCopies * sizeof(QCell) + kWWarps * (2 * 16 * D * sizeof(T) + 16 * RB + 16); \
-    auto kern = write_tc_kernel<T, D, BITS>;                                                                  \
+    constexpr int RB = write_tc_row_bytes<D, BITS, false>();                                                  \
+    const size_t smem = write_tc_fixed_smem<D, false>() + kWWarps * (2 * 16 * D * sizeof(T) + 16 * RB + 16);  \
+    auto kern = write_tc_kernel<T, D, BITS, false>;                                                           \
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
     if (err != cudaSuccess) return err;                                                                       \
     return launch_dependent(kern, grid, smem, stream, t);                                                     \
@@ -631,6 +766,38 @@ cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
     TQ_WTC(__nv_bfloat16, 256, 3) TQ_WTC(__nv_bfloat16, 256, 4) TQ_WTC(__nv_bfloat16, 256, 5)
   }
 #undef TQ_WTC
+  return cudaErrorInvalidValue;
+}
+
+bool write_prod_tc_supported(const WriteArgs& a) {
+  const bool dt = a.dtype == kF16 || a.dtype == kBF16 || (a.dtype == kF32 && a.head_dim == 64);
+  const bool hd = a.head_dim == 64 || a.head_dim == 128;
+  return dt && hd && a.bits >= 3 && a.bits <= 5 && a.num_kv_heads >= 1;
+}
+
+cudaError_t launch_write_prod_tc(const WriteArgs& a, const float* smat, cudaStream_t stream, int grid) {
+  WriteTcArgs t;
+  t.a = a;
+  t.smat = smat;
+#define TQ_WTP(T, D, MB)                                                                                      \
+  if (a.head_dim == D && a.bits == MB + 1) {                                                                  \
+    constexpr int RB = write_tc_row_bytes<D, MB, true>();                                                     \
+    const size_t smem = write_tc_fixed_smem<D, true>() + kWWarps * (2 * 16 * D * sizeof(T) + 16 * RB + 16);   \
+    auto kern = write_tc_kernel<T, D, MB, true>;                                                              \
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
+    if (err != cudaSuccess) return err;                                                                       \
+    return launch_dependent(kern, grid, smem, stream, t);                                                     \
+  }
+  if (a.dtype == kF32) {
+    TQ_WTP(float, 64, 2) TQ_WTP(float, 64, 3) TQ_WTP(float, 64, 4)
+  } else if (a.dtype == kF16) {
+    TQ_WTP(__half, 64, 2) TQ_WTP(__half, 64, 3) TQ_WTP(__half, 64, 4)
+    TQ_WTP(__half, 128, 2) TQ_WTP(__half, 128, 3) TQ_WTP(__half, 128, 4)
+  } else if (a.dtype == kBF16) {
+    TQ_WTP(__nv_bfloat16, 64, 2) TQ_WTP(__nv_bfloat16, 64, 3) TQ_WTP(__nv_bfloat16, 64, 4)
+    TQ_WTP(__nv_bfloat16, 128, 2) TQ_WTP(__nv_bfloat16, 128, 3) TQ_WTP(__nv_bfloat16, 128, 4)
+  }
+#undef TQ_WTP
   return cudaErrorInvalidValue;
 }
 
