@@ -21,7 +21,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libtq_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["tq_api.cpp", "tq_write.cu", "tq_write_tc.cu", "tq_decode.cu", "tq_decode_tc.cu", "tq_prefill_mq.cu",
+SOURCES = ["tq_api.cpp", "tq_write.cu", "tq_write_tc.cu", "tq_decode.cu", "tq_decode_tc.cu", "tq_decode_tc_a.cu",
+           "tq_decode_tc_b.cu", "tq_decode_tc_c.cu", "tq_decode_tc_d.cu", "tq_decode_tc_p.cu",
+           "tq_decode_tc_q.cu", "tq_prefill_mq.cu",
            "tq_dequant.cu", "tq_qjl.cu", "tq_recipe.cu", "tq_query.cu",
            "tq_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

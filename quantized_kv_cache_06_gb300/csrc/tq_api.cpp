@@ -686,7 +686,9 @@ tq_status tq_paged_decode_prod(const void* q, tq_dtype q_dtype, int batch, int n
   a.out_dtype = (int)out_dtype;
   a.workspace = workspace;
   a.status = status_dev;
-  a.v_alpha = a.k_alpha = 1.0f;
+  // centroid scales of the tensor-core form's fp16 tables (the SIMT form reads fp32 centroids)
+  a.k_alpha = fp16_scale_for(head_dim, k_bits - 1);
+  a.v_alpha = fp16_scale_for(head_dim, v_bits);
   return check_cuda(tq::launch_decode_prod(a, qjl_matrix, plan, static_cast<cudaStream_t>(stream)), name);
 }
 

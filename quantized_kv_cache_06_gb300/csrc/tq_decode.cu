@@ -246,7 +246,7 @@ cudaError_t launch_split(const DecodeArgs& a, const DecodePlan& p, SplitView par
 
 DecodePlan plan_decode(const DecodeArgs& a, int num_sms) {
   DecodePlan p{};
-  if (a.k_bits > 0 && tc_decode_supported(a)) {
+  if (a.k_bits > 0 && !a.bt_rows && tc_decode_supported(a)) {  // (row-mapped batches: no tensor-core form)
     // Tensor-core kernel: one CTA per SM over the flat block list; partial slots for
     // every (CTA, sequence) pair and warp slot, plus the block prefix sums.
     p.kernel = 2;

@@ -121,6 +121,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   asm("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint32_t lds32_off128(uint32_t addr) {
   uint32_t v;
   asm("ld.shared.b32 %0, [%1+128];\n" : "=r"(v) : "r"(addr));
@@ -193,15 +198,20 @@ __device__ __forceinline__ uint32_t win_addr(const uint32_t* w, int i, uint32_t 
   return (x & (((1u << W) - 1u) << 7)) | lane_base;
 }
 
-template <int D, int KB, int VB, int G, int WPH>
+// PROD: product-quantised ("QJL residual") key rows -- KB-bit MSE indices, then D sign bits,
+// then fp32 nu and gamma.
+template <int D, int KB, int VB, int G, int WPH, bool PROD = false>
 struct TcCfg {
-  static constexpr int kRBK = D * KB / 8 + 4;          // row bytes
+  static constexpr int kRBK = D * KB / 8 + (PROD ? D / 8 + 8 : 4);  // row bytes
+  static constexpr int kKNormOff = D * KB / 8 + (PROD ? D / 8 : 0);   // byte of nu in a K row
+  static constexpr int kSignOff = D * KB / 8;                          // product rows: sign bits
   static constexpr int kRBV = D * VB / 8 + 4;
   static constexpr int kWK = D * KB / 32;              // index words per K row
   static constexpr int kWV = D * VB / 32;
-  static constexpr bool kWin = KB == 3 || KB == 5;     // window mode: 3- and 5-bit rows
-  static constexpr int kPWK = kWin ? 1 : 16 / KB;       // pairs per word (2- and 4-bit rows)
-  static constexpr int kPWV = kWin ? 1 : 16 / VB;
+  static constexpr bool kKWin = KB == 3 || KB == 5;    // window mode: 3- and 5-bit rows
+  static constexpr bool kVWin = VB == 3 || VB == 5;
+  static constexpr int kPWK = kKWin ? 1 : 16 / KB;      // pairs per word (2- and 4-bit rows)
+  static constexpr int kPWV = kVWin ? 1 : 16 / VB;
   static constexpr int kKSteps = D / 16;               // score k-steps
   static constexpr int kMTiles = D / 32;               // value m-tiles
   static constexpr int kNT = (2 * G + 7) / 8;          // value n-tiles (N = 2G)
@@ -222,21 +232,27 @@ struct TcCfg {
   // m-tile i takes pairs r D/16 + 2i and + 2i + 1.  3-bit rows look up a pair per 6-bit
   // field in a 64-entry table of (fp16 hi, fp16 hi) pairs; 5-bit rows look up each
   // coordinate in a 32-entry table of (fp16 hi, fp16 lo x 2^12) and join two with a PRMT.
-  // Both tables are replicated per lane (entry e of lane l at e * 128 + 4 l), K then V,
-  // at a shared address aligned to one table, so the address of an entry is the field,
-  // shifted to bit 7, OR'd into (table base | lane * 4).
-  static constexpr int kTabEntries = KB == 3 ? 64 : 32;
+  // Each table is replicated per lane (entry e of lane l at e * 128 + 4 l) in an 8 KB slot
+  // aligned to 8 KB, so the address of an entry is the field, shifted to bit 7, OR'd into
+  // (table base | lane * 4).  K and V widths are independent: each component takes its own
+  // form.
   static constexpr int kKLaneWords = KB * D / 128;  // K words per lane and row (window mode)
-  // Table region: T (64 KB, 64 KB aligned) for 4-bit rows, the window-mode tables (2 x 8 KB
-  // or 2 x 4 KB, aligned to one) for 3- and 5-bit rows, none for 2-bit rows.
-  static constexpr int kTBytes = kHasT ? 256 * 256 : (kWin ? 2 * kTabEntries * 128 : 0);
-  static constexpr int kTAlign = kHasT ? 65536 : kTabEntries * 128;
-  static_assert(kWin || kWK % 4 == 0, "K row must split into 4 interleaved word columns");
-  static_assert(kWin || kWV % 8 == 0, "V row must split into 8 interleaved word columns");
+  // Table region: T (64 KB, 64 KB aligned) when either width is 4, then an 8 KB slot for a
+  // window-mode K table and one for a window-mode V table; empty for 2-bit rows.
+  static constexpr int kWinSlot = 64 * 128;
+  static constexpr int kKWOff = kHasT ? 256 * 256 : 0;
+  static constexpr int kVWOff = kKWOff + (kKWin ? kWinSlot : 0);
+  // product rows: the sign table, (+-1, +-1) fp16 pairs for the four bits of a nibble, per
+  // lane (entry n of lane l at 256 n + 8 l), in one more slot
+  static constexpr int kSgnOff = kVWOff + (kVWin ? kWinSlot : 0);
+  static constexpr int kTBytes = kSgnOff + (PROD ? kWinSlot : 0);
+  static constexpr int kTAlign = kHasT ? 256 * 256 : kWinSlot;
+  static_assert(kKWin || kWK % 4 == 0, "K row must split into 4 interleaved word columns");
+  static_assert(kVWin || kWV % 8 == 0, "V row must split into 8 interleaved word columns");
   static_assert(G == 4 || G == 8, "GQA group 4 or 8");
   static_assert(KB >= 2 && KB <= 5 && VB >= 2 && VB <= 5, "2- to 5-bit indices");
-  static_assert(kWin == (VB == 3 || VB == 5) && (!kWin || KB == VB), "3- and 5-bit rows: equal K and V widths");
-  static_assert(!kWin || D == 128 || D == 256, "3- and 5-bit rows at head_dim 128 or 256");
+  static_assert(!(kKWin || kVWin) || D == 128 || D == 256, "3- and 5-bit rows at head_dim 128 or 256");
+  static_assert(!PROD || KB <= 4, "product rows: 2- to 4-bit MSE indices");
 };
 
 struct TcArgs {
@@ -259,6 +275,8 @@ struct TcArgs {
   uint32_t wait_tries;    // tries of a pipeline wait before it reports kTimeout
   float* part_acc;        // [WPH*(C+B)][Hq][D]
   float* part_ml;         // [WPH*(C+B)][Hq][2]
+  const float* p_all;     // product rows: p = S q~ per (sequence, q head), [B][Hq][D]
+  float sketch;           // product rows: sqrt(pi / 2) / D
   int* prefix;            // [B+1] block prefix sums (written by CTA 0)
 };
 
@@ -292,9 +310,9 @@ constexpr float kFastValueNorm = 32.0f;
 // At most 9 warps (8 consumers + the producer).  The register file is granted to a CTA
 // in groups of 4 warps, so 288 threads take 12 warps' worth: 168 registers a thread at most
 // (a launch at more registers is refused).
-template <int D, int KB, int VB, int G, int WPH>
+template <int D, int KB, int VB, int G, int WPH, bool PROD = false>
 __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
-  using Cfg = TcCfg<D, KB, VB, G, WPH>;
+  using Cfg = TcCfg<D, KB, VB, G, WPH, PROD>;
   const DecodeArgs& a = args.a;
   extern __shared__ __align__(128) unsigned char smem[];
   const int H = a.num_kv_heads;
@@ -319,8 +337,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   unsigned char* lutVL = smem + kOffVL;
   unsigned char* lutK3L = smem + kOffK3L;
   unsigned char* lutV3L = smem + kOffV3L;
-  unsigned char* lutKW = smem + args.t_off;  // window-mode tables (3- and 5-bit rows)
-  unsigned char* lutVW = smem + args.t_off + Cfg::kTabEntries * 128;
+  unsigned char* lutKW = smem + args.t_off + Cfg::kKWOff;  // window-mode tables (3- and 5-bit rows)
+  unsigned char* lutVW = smem + args.t_off + Cfg::kVWOff;
   BlockMeta* meta = reinterpret_cast<BlockMeta*>(smem + kOffMeta);
   int* scan_tmp = reinterpret_cast<int*>(smem + kOffScan);
   auto bar_full = [&](int i) -> uint32_t { return smem_base + kOffBar + 8u * i; };
@@ -528,14 +546,16 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 
   // Window mode: the A registers of pair j of a window w (fp16 hi parts of coordinates 2j,
   // 2j + 1; and their remainders, for the exact paths).
-  const uint32_t kw_lane = t_base | (uint32_t)(lane * 4);  // K table, this lane's copy
-  const uint32_t vw_lane = (t_base + (uint32_t)(Cfg::kTabEntries * 128)) | (uint32_t)(lane * 4);
-  auto win_hi = [&](const uint32_t* w, int j, uint32_t lane_base) -> uint32_t {
-    if constexpr (KB == 3) return lds32(win_addr<6>(w, j, lane_base));
+  const uint32_t kw_lane = (t_base + (uint32_t)Cfg::kKWOff) | (uint32_t)(lane * 4);  // K table, this lane's copy
+  const uint32_t vw_lane = (t_base + (uint32_t)Cfg::kVWOff) | (uint32_t)(lane * 4);
+  using KBt = std::integral_constant<int, KB>;
+  using VBt = std::integral_constant<int, VB>;
+  auto win_hi = [&](auto bits_tag, const uint32_t* w, int j, uint32_t lane_base) -> uint32_t {
+    if constexpr (decltype(bits_tag)::value == 3) return lds32(win_addr<6>(w, j, lane_base));
     else return __byte_perm(lds32(win_addr<5>(w, 2 * j, lane_base)), lds32(win_addr<5>(w, 2 * j + 1, lane_base)), 0x5410u);
   };
-  auto win_lo = [&](const uint32_t* w, int j, uint32_t lane_base, const unsigned char* lo3) -> uint32_t {
-    if constexpr (KB == 3) return ld32(lo3 + (win_field<6>(w, j) << 2));
+  auto win_lo = [&](auto bits_tag, const uint32_t* w, int j, uint32_t lane_base, const unsigned char* lo3) -> uint32_t {
+    if constexpr (decltype(bits_tag)::value == 3) return ld32(lo3 + (win_field<6>(w, j) << 2));
     else return __byte_perm(lds32(win_addr<5>(w, 2 * j, lane_base)), lds32(win_addr<5>(w, 2 * j + 1, lane_base)), 0x7632u);
   };
   // V window of token row `row` for this lane (pairs [r D/16, (r + 1) D/16)), from bit 0
@@ -563,6 +583,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   // so one MMA yields both products.  G = 8: separate hi and lo sets.
   constexpr int kQSets = G == 4 ? 1 : 2;
   uint32_t bq[kQSets][Cfg::kKSteps][2];
+  uint32_t pq[kQSets][Cfg::kKSteps][2];  // product rows: p = S q~, same layout (unused otherwise)
   float qnorm_max = 0.f;  // max over this warp's heads of ||rotated query|| (log2 units)
   float o_acc[Cfg::kNT][Cfg::kMTiles][4];
   float m_run[2], l_run[2], m_thr[2];  // running max, sum, and max + kRescaleSlack per head
@@ -592,6 +613,45 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       for (int i = 0; i < Cfg::kMTiles; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o_acc[nt][i][e] *= cg;
+    }
+  };
+
+  // B fragments from per-lane natural-order values x[g][i] (coordinate lane E + i of head g):
+  // the fp16 hi / lo split of the pair order the K rows use.
+  auto build_frags = [&](const float (&x)[G][D / 32], uint32_t (&frag)[kQSets][Cfg::kKSteps][2]) {
+    constexpr int E = D / 32;
+    const int gq = G == 4 ? (r & 3) : r;  // this lane's B column -> q head
+#pragma unroll
+    for (int s = 0; s < Cfg::kKSteps; ++s) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = 2 * s + u;
+        const int jw = q / Cfg::kPWK, e = q % Cfg::kPWK;
+        // pair index (coordinates 2p, 2p+1) of local pair u of k-step s on this lane column
+        const int p = Cfg::kKWin ? (D / 8) * c + q : Cfg::kPWK * (c + 4 * jw) + e;
+        const int src = (2 * p) / E;
+        const int off = (2 * p) % E;  // identical on every lane (see the pair layout)
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float v0 = __shfl_sync(kFullMask, x[g][off], src);
+          const float v1 = __shfl_sync(kFullMask, x[g][(off + 1) % E], E == 1 ? src + 1 : src);
+          if (g == gq) {
+            x0 = v0;
+            x1 = v1;
+          }
+        }
+        __half h0, l0, h1, l1;
+        split_half(x0, h0, l0);
+        split_half(x1, h1, l1);
+        __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
+        if (G == 4) {
+          frag[0][s][u] = r < 4 ? *reinterpret_cast<uint32_t*>(&hh) : *reinterpret_cast<uint32_t*>(&ll);
+        } else {
+          frag[0][s][u] = *reinterpret_cast<uint32_t*>(&hh);
+          frag[kQSets - 1][s][u] = *reinterpret_cast<uint32_t*>(&ll);
+        }
+      }
     }
   };
 
@@ -635,38 +695,14 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
       }
       qnorm_max = fmaxf(qnorm_max, sqrtf(warp_sum(ss)));
     }
-    const int gq = G == 4 ? (r & 3) : r;  // this lane's B column -> q head
+    build_frags(qr, bq);
+    if constexpr (PROD) {  // p = S q~ of the same heads, into the sketch fragments
+      const float* pb = args.p_all + base;
 #pragma unroll
-    for (int s = 0; s < Cfg::kKSteps; ++s) {
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = 2 * s + u;
-        const int jw = q / Cfg::kPWK, e = q % Cfg::kPWK;
-        // pair index (coordinates 2p, 2p+1) of local pair u of k-step s on this lane column
-        const int p = Cfg::kWin ? (D / 8) * c + q : Cfg::kPWK * (c + 4 * jw) + e;
-        const int src = (2 * p) / E;
-        const int off = (2 * p) % E;  // identical on every lane (see the pair layout)
-        float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float v0 = __shfl_sync(kFullMask, qr[g][off], src);
-          const float v1 = __shfl_sync(kFullMask, qr[g][(off + 1) % E], E == 1 ? src + 1 : src);
-          if (g == gq) {
-            x0 = v0;
-            x1 = v1;
-          }
-        }
-        __half h0, l0, h1, l1;
-        split_half(x0, h0, l0);
-        split_half(x1, h1, l1);
-        __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
-        if (G == 4) {
-          bq[0][s][u] = r < 4 ? *reinterpret_cast<uint32_t*>(&hh) : *reinterpret_cast<uint32_t*>(&ll);
-        } else {
-          bq[0][s][u] = *reinterpret_cast<uint32_t*>(&hh);
-          bq[kQSets - 1][s][u] = *reinterpret_cast<uint32_t*>(&ll);
-        }
-      }
+        for (int i = 0; i < E; ++i) qr[g][i] = __ldg(pb + g * D + i);
+      build_frags(qr, pq);
     }
   };
 
@@ -702,7 +738,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int q = 2 * i + half;
-            const int pv = Cfg::kWin ? (D / 16) * r + q : Cfg::kPWV * (r + 8 * (q / Cfg::kPWV)) + (q % Cfg::kPWV);
+            const int pv = Cfg::kVWin ? (D / 16) * r + q : Cfg::kPWV * (r + 8 * (q / Cfg::kPWV)) + (q % Cfg::kPWV);
             float2 v;
             v.x = empty ? 0.f : o_acc[nt][i][2 * half] * inv_alpha;
             v.y = empty ? 0.f : o_acc[nt][i][2 * half + 1] * inv_alpha;
@@ -739,8 +775,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
     for (int t = 0; t < NTL; ++t) {
       vbase[t] = kbase[t] - h * Cfg::kRBK + args.k_slab_smem + h * Cfg::kRBV;
-      kn[t][0] = __uint_as_float(ld32(kbase[t] + r * kts + Cfg::kWK * 4));
-      kn[t][1] = __uint_as_float(ld32(kbase[t] + (r + 8) * kts + Cfg::kWK * 4));
+      kn[t][0] = __uint_as_float(ld32(kbase[t] + r * kts + Cfg::kKNormOff));
+      kn[t][1] = __uint_as_float(ld32(kbase[t] + (r + 8) * kts + Cfg::kKNormOff));
       vn[t][0] = __uint_as_float(ld32(vbase[t] + r * vts + Cfg::kWV * 4));
       vn[t][1] = __uint_as_float(ld32(vbase[t] + (r + 8) * vts + Cfg::kWV * 4));
       kmax = fmaxf(kmax, fmaxf(fabsf(kn[t][0]), fabsf(kn[t][1])));
@@ -786,7 +822,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
           mma16816((s & 1) ? sacc1[t] : sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
         }
       };
-      if constexpr (Cfg::kWin) {
+      if constexpr (Cfg::kKWin) {
         // chunks of KB words of this lane's window: 16 pairs, 8 k-steps each
 #pragma unroll
         for (int ch = 0; ch < D / 128; ++ch) {
@@ -802,8 +838,8 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
           for (int s8 = 0; s8 < 8; ++s8)
 #pragma unroll
             for (int t = 0; t < NTL; ++t)
-              kstep(t, 8 * ch + s8, win_hi(w0[t], 2 * s8, kw_lane), win_hi(w1[t], 2 * s8, kw_lane),
-                    win_hi(w0[t], 2 * s8 + 1, kw_lane), win_hi(w1[t], 2 * s8 + 1, kw_lane));
+              kstep(t, 8 * ch + s8, win_hi(KBt{}, w0[t], 2 * s8, kw_lane), win_hi(KBt{}, w1[t], 2 * s8, kw_lane),
+                    win_hi(KBt{}, w0[t], 2 * s8 + 1, kw_lane), win_hi(KBt{}, w1[t], 2 * s8 + 1, kw_lane));
         }
       } else {
 #pragma unroll
@@ -840,7 +876,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
           if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
           mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
         };
-        if constexpr (Cfg::kWin) {
+        if constexpr (Cfg::kKWin) {
 #pragma unroll
           for (int ch = 0; ch < D / 128; ++ch) {
             uint32_t w0[KB], w1[KB];
@@ -852,9 +888,10 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
             for (int s8 = 0; s8 < 8; ++s8) {
               const int j0 = 2 * s8, j1 = 2 * s8 + 1;
-              kstep_ex(8 * ch + s8, win_hi(w0, j0, kw_lane), win_hi(w1, j0, kw_lane), win_hi(w0, j1, kw_lane),
-                       win_hi(w1, j1, kw_lane), win_lo(w0, j0, kw_lane, lutK3L), win_lo(w1, j0, kw_lane, lutK3L),
-                       win_lo(w0, j1, kw_lane, lutK3L), win_lo(w1, j1, kw_lane, lutK3L));
+              kstep_ex(8 * ch + s8, win_hi(KBt{}, w0, j0, kw_lane), win_hi(KBt{}, w1, j0, kw_lane),
+                       win_hi(KBt{}, w0, j1, kw_lane), win_hi(KBt{}, w1, j1, kw_lane),
+                       win_lo(KBt{}, w0, j0, kw_lane, lutK3L), win_lo(KBt{}, w1, j0, kw_lane, lutK3L),
+                       win_lo(KBt{}, w0, j1, kw_lane, lutK3L), win_lo(KBt{}, w1, j1, kw_lane, lutK3L));
             }
           }
         } else {
@@ -871,6 +908,38 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         // sacc1 (key_hi * q_lo) and sacc2 (key_lo * q) each carry one 2^12 scale
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[t][e] = fmaf(sacc1[e] + sacc2[e], kLoUnscale, sacc[t][e]);
+      }
+    }
+    if constexpr (PROD) {
+      // sketch term of product rows: gamma kappa <p, 2 z - 1>.  The A operand is the +-1 pairs
+      // of the row's sign bits (the nibble of k-step s holds both pairs of the lane), the B
+      // operand p = S q~ split like the query; added to the MSE score before the fold (for
+      // G = 4 the p_lo columns carry the same 2^12 as the q_lo ones).
+      const uint32_t sgn_lane = (t_base + (uint32_t)Cfg::kSgnOff) | (uint32_t)(lane * 8);
+      auto sign_pairs = [&](const unsigned char* row, int s) -> uint2 {
+        const int q = 2 * s, jw = q / Cfg::kPWK, e = q % Cfg::kPWK;
+        const int bo = 2 * (Cfg::kKWin ? (D / 8) * c + q : Cfg::kPWK * (c + 4 * jw) + e);  // first sign bit
+        const uint32_t w = ld32(row + Cfg::kSignOff + (bo >> 5) * 4);
+        return lds64(sgn_lane | (((w >> (bo & 31)) & 15u) << 8));
+      };
+#pragma unroll
+      for (int t = 0; t < NTL; ++t) {
+        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+        const unsigned char* ra = kbase[t] + r * kts;
+        const unsigned char* rb = kbase[t] + (r + 8) * kts;
+        const float g0 = __uint_as_float(ld32(ra + Cfg::kKNormOff + 4)) * args.sketch;
+        const float g1 = __uint_as_float(ld32(rb + Cfg::kKNormOff + 4)) * args.sketch;
+#pragma unroll
+        for (int s = 0; s < Cfg::kKSteps; ++s) {
+          const uint2 za = sign_pairs(ra, s), zb = sign_pairs(rb, s);
+          mma16816(z0, za.x, zb.x, za.y, zb.y, pq[0][s][0], pq[0][s][1]);
+          if (G == 8) mma16816(z1, za.x, zb.x, za.y, zb.y, pq[kQSets - 1][s][0], pq[kQSets - 1][s][1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float zz = G == 8 ? fmaf(z1[e], kLoUnscale, z0[e]) : z0[e];  // G = 8: z1 holds p_lo x 2^12
+          sacc[t][e] = fmaf(e < 2 ? g0 : g1, zz, sacc[t][e]);
+        }
       }
     }
     float sc[NTL][4];
@@ -991,7 +1060,7 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
               }
             }
           };
-          if constexpr (Cfg::kWin) {
+          if constexpr (Cfg::kVWin) {
             uint32_t wa[5], wb[5];
             v_window(vbase[t] + t0 * vts, wa);
             v_window(vbase[t] + t1 * vts, wb);
@@ -999,9 +1068,10 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
             for (int i = 0; i < Cfg::kMTiles; ++i) {
               const int j0 = 2 * i, j1 = 2 * i + 1;
               // the remainder lookups are dead code (and dropped) unless EXV
-              vstep(i, win_hi(wa, j0, vw_lane), win_hi(wa, j1, vw_lane), win_hi(wb, j0, vw_lane),
-                    win_hi(wb, j1, vw_lane), win_lo(wa, j0, vw_lane, lutV3L), win_lo(wa, j1, vw_lane, lutV3L),
-                    win_lo(wb, j0, vw_lane, lutV3L), win_lo(wb, j1, vw_lane, lutV3L));
+              vstep(i, win_hi(VBt{}, wa, j0, vw_lane), win_hi(VBt{}, wa, j1, vw_lane), win_hi(VBt{}, wb, j0, vw_lane),
+                    win_hi(VBt{}, wb, j1, vw_lane), win_lo(VBt{}, wa, j0, vw_lane, lutV3L),
+                    win_lo(VBt{}, wa, j1, vw_lane, lutV3L), win_lo(VBt{}, wb, j0, vw_lane, lutV3L),
+                    win_lo(VBt{}, wb, j1, vw_lane, lutV3L));
             }
           } else {
 #pragma unroll
@@ -1046,19 +1116,6 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   };
   using One = std::integral_constant<int, 1>;
   using Two = std::integral_constant<int, 2>;
-  // Whether the tile of block buffer `kblk` (ntok valid rows) takes an exact path: the
-  // same vote as in `tiles`, from the row norms alone.
-  auto tile_exact = [&](const unsigned char* kblk, int ntok) -> bool {
-    const unsigned char* kb = kblk + h * Cfg::kRBK;
-    const unsigned char* vb = kblk + args.k_slab_smem + h * Cfg::kRBV;
-    float k0 = fabsf(__uint_as_float(ld32(kb + r * kts + Cfg::kWK * 4)));
-    float k1 = fabsf(__uint_as_float(ld32(kb + (r + 8) * kts + Cfg::kWK * 4)));
-    float v0 = __uint_as_float(ld32(vb + r * vts + Cfg::kWV * 4));
-    float v1 = __uint_as_float(ld32(vb + (r + 8) * vts + Cfg::kWV * 4));
-    if (r >= ntok) k0 = v0 = 0.f;
-    if (r + 8 >= ntok) k1 = v1 = 0.f;
-    return __any_sync(kFullMask, fmaxf(v0, v1) > kFastValueNorm || fmaxf(k0, k1) * qnorm_max > kFastScoreBound);
-  };
 
   // ---- main pipeline -----------------------------------------------------------------
   // Stage st lives in ring slot st % nst; full[slot] completes when its copies landed,
@@ -1128,22 +1185,24 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         *reinterpret_cast<uint2*>(lutV2 + f * 8) = v;
       }
     }
-    if constexpr (Cfg::kWin) {
+    if constexpr (Cfg::kKWin || Cfg::kVWin) {
       // window-mode tables, one copy per lane.  3-bit: entry f = the fp16 hi parts of
       // (c[f & 7], c[f >> 3]), their remainders (x 2^12) in one copy.  5-bit: entry e =
       // (fp16 hi, fp16 lo x 2^12) of c[e].
 #pragma unroll
       for (int comp = 0; comp < 2; ++comp) {
+        const int cb = comp == 0 ? KB : VB;
+        if ((comp == 0 && !Cfg::kKWin) || (comp == 1 && !Cfg::kVWin)) continue;
         const float* cents = comp == 0 ? a.k_centroids : a.v_centroids;
         const float alpha = comp == 0 ? args.k_alpha : args.v_alpha;
         unsigned char* tab = comp == 0 ? lutKW : lutVW;
         unsigned char* tlo = comp == 0 ? lutK3L : lutV3L;
         __half hi_l, lo_l;
-        split_half(__ldg(cents + (lane & (KB == 3 ? 7 : 31))) * alpha, hi_l, lo_l);
+        split_half(__ldg(cents + (lane & (cb == 3 ? 7 : 31))) * alpha, hi_l, lo_l);
         const uint32_t pair_l = (uint32_t)__half_as_ushort(hi_l) | ((uint32_t)__half_as_ushort(lo_l) << 16);
-        for (int i = tid; i < Cfg::kTabEntries * 32; i += 32 * ncons) {
+        for (int i = tid; i < (cb == 3 ? 64 : 32) * 32; i += 32 * ncons) {
           const int f = i >> 5, copy = i & 31;
-          if (KB == 3) {
+          if (cb == 3) {
             const uint32_t pa = __shfl_sync(kFullMask, pair_l, f & 7);  // (hi, lo) of c[f & 7]
             const uint32_t pb = __shfl_sync(kFullMask, pair_l, f >> 3);
             *reinterpret_cast<uint32_t*>(tab + f * 128 + copy * 4) = __byte_perm(pa, pb, 0x5410);
@@ -1152,6 +1211,16 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
             *reinterpret_cast<uint32_t*>(tab + f * 128 + copy * 4) = __shfl_sync(kFullMask, pair_l, f);
           }
         }
+      }
+    }
+    if constexpr (PROD) {  // sign table: entry n = (+-1, +-1), (+-1, +-1) of the 4 bits of n
+      unsigned char* sg = smem + args.t_off + Cfg::kSgnOff;
+      for (int i = tid; i < 16 * 32; i += 32 * ncons) {
+        const int n = i >> 5, copy = i & 31;
+        uint2 v;
+        v.x = ((n & 1) ? 0x3C00u : 0xBC00u) | (((n & 2) ? 0x3C00u : 0xBC00u) << 16);
+        v.y = ((n & 4) ? 0x3C00u : 0xBC00u) | (((n & 8) ? 0x3C00u : 0xBC00u) << 16);
+        *reinterpret_cast<uint2*>(sg + n * 256 + copy * 8) = v;
       }
     }
   asm volatile("bar.sync 1, %0;\n" ::"r"(32 * ncons) : "memory");  // consumer warps only
@@ -1169,15 +1238,10 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
     }
     const BlockMeta m0 = meta[slot * WPH];
     const BlockMeta m1 = meta[slot * WPH + WPH - 1];
-    bool fused = WPH == 2 && m0.ntok == kBS && m0.valid && m1.ntok != 0 && m1.valid && m1.b == m0.b;
-    if (fused) {
+    if (WPH == 2 && m0.ntok == kBS && m0.valid && m1.ntok != 0 && m1.valid && m1.b == m0.b) {
       if (m0.b != cur_b) enter_sequence(m0.b);
-      // a fused step runs the slower exact path for both tiles if either needs it: when
-      // only one does (rows of large norm are rare), the tiles run one at a time
-      fused = tile_exact(smem + buf_off(slot, 0), kBS) == tile_exact(smem + buf_off(slot, 1), m1.ntok);
-      if (fused) tiles(Two{}, smem + buf_off(slot, 0), smem + buf_off(slot, 1), m1.ntok);
-    }
-    if (!fused) {
+      tiles(Two{}, smem + buf_off(slot, 0), smem + buf_off(slot, 1), m1.ntok);
+    } else {
 #pragma unroll
       for (int u = 0; u < WPH; ++u) {
         const BlockMeta m = u == 0 ? m0 : m1;
@@ -1278,9 +1342,10 @@ combine_tc_kernel(DecodeArgs a, int num_ctas, const float* __restrict__ part_acc
     store_from_f32(a.out, (int64_t)row * D + lane * E + k, a.out_dtype, v[k] * __ldg(a.signs + lane * E + k) * rs);
 }
 
-template <int D, int KB, int VB, int G, int WPH>
-cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
-  using Cfg = TcCfg<D, KB, VB, G, WPH>;
+template <int D, int KB, int VB, int G, int WPH, bool PROD = false>
+cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream,
+                            const float* p_all = nullptr) {
+  using Cfg = TcCfg<D, KB, VB, G, WPH, PROD>;
   TcArgs t{};
   t.a = a;
   t.num_ctas = p.num_splits;
@@ -1340,7 +1405,9 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   t.part_acc = static_cast<float*>(a.workspace);
   t.part_ml = t.part_acc + slots * Hq * D;
   t.prefix = reinterpret_cast<int*>(t.part_ml + slots * Hq * 2);
-  auto kern = decode_tc_kernel<D, KB, VB, G, WPH>;
+  t.p_all = p_all;
+  t.sketch = 1.2533141373155003f / (float)D;  // sqrt(pi / 2) / D
+  auto kern = decode_tc_kernel<D, KB, VB, G, WPH, PROD>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   kern<<<p.num_splits, 32 * (H + 1), smem, stream>>>(t);
@@ -1366,33 +1433,32 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
 }
 
 
-// Instantiations: D 128 (2 blocks per stage) and 256 (1) x all 2/4-bit combos, 3/3 and 5/5
-// bits x G 4/8, and D 64 at 4/4 bits.
-cudaError_t launch_decode_tc_dispatch(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
-  const int G = a.num_q_heads / a.num_kv_heads;
-#define TQ_TC_CASE(D, KB, VB, GG, WPH)                                                    \
-  if (a.head_dim == D && a.k_bits == KB && a.v_bits == VB && G == GG)                     \
+// One instantiation per translation unit line: the forms are split over several .cu files
+// (tq_decode_tc*.cu) so that they compile in parallel.
+#define TQ_TC_CASE(D, KB, VB, GG, WPH)                                                             \
+  if (a.head_dim == D && a.k_bits == KB && a.v_bits == VB && a.num_q_heads / a.num_kv_heads == GG) \
     return launch_tc_typed<D, KB, VB, GG, WPH>(a, p, stream);
-#define TQ_TC_BITS(D, GG, WPH) \
-  TQ_TC_CASE(D, 4, 4, GG, WPH) TQ_TC_CASE(D, 4, 2, GG, WPH) TQ_TC_CASE(D, 2, 4, GG, WPH) TQ_TC_CASE(D, 2, 2, GG, WPH)
-  TQ_TC_BITS(128, 4, 2)
-  TQ_TC_BITS(128, 8, 2)
-  TQ_TC_BITS(256, 4, 1)
-  TQ_TC_BITS(256, 8, 1)
-  TQ_TC_CASE(128, 3, 3, 4, 2)
-  TQ_TC_CASE(128, 3, 3, 8, 2)
-  TQ_TC_CASE(256, 3, 3, 4, 1)
-  TQ_TC_CASE(256, 3, 3, 8, 1)
-  TQ_TC_CASE(128, 5, 5, 4, 2)
-  TQ_TC_CASE(128, 5, 5, 8, 2)
-  TQ_TC_CASE(256, 5, 5, 4, 1)
-  TQ_TC_CASE(256, 5, 5, 8, 1)
-  TQ_TC_CASE(64, 4, 4, 4, 2)
-  TQ_TC_CASE(64, 4, 4, 8, 2)
-#undef TQ_TC_BITS
-#undef TQ_TC_CASE
-  return cudaErrorInvalidValue;
-}
+#define TQ_TC_VBITS(D, KB, WPH)                                                                      \
+  TQ_TC_CASE(D, KB, 2, 4, WPH) TQ_TC_CASE(D, KB, 3, 4, WPH) TQ_TC_CASE(D, KB, 4, 4, WPH)            \
+  TQ_TC_CASE(D, KB, 5, 4, WPH) TQ_TC_CASE(D, KB, 2, 8, WPH) TQ_TC_CASE(D, KB, 3, 8, WPH)            \
+  TQ_TC_CASE(D, KB, 4, 8, WPH) TQ_TC_CASE(D, KB, 5, 8, WPH)
+// product-quantised key rows at D = 128: MB-bit MSE indices (a.k_bits = MB + 1), every V width
+#define TQ_TCP_CASE(MB, VB, GG)                                                                \
+  if (a.k_bits == MB + 1 && a.v_bits == VB) return launch_tc_typed<128, MB, VB, GG, 2, true>(a, p, stream, p_all);
+#define TQ_TCP_V(MB, GG) TQ_TCP_CASE(MB, 2, GG) TQ_TCP_CASE(MB, 3, GG) TQ_TCP_CASE(MB, 4, GG) TQ_TCP_CASE(MB, 5, GG)
 
 }  // namespace
+}  // namespace tq
+
+namespace tq {
+// Launchers of the instantiated forms, one per translation unit: each returns
+// cudaErrorNotSupported for a shape it does not hold.  D 128 / 256 at K width 2 and 4
+// (part a / c), 3 and 5 (part b / d), every V width, G 4 / 8; D 64 at 4/4 bits (part e).
+cudaError_t launch_tc_part_a(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
+cudaError_t launch_tc_part_b(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
+cudaError_t launch_tc_part_c(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
+cudaError_t launch_tc_part_d(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
+cudaError_t launch_tc_part_e(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
+// Product-quantised key rows, GQA group 8 (tq_decode_tc_q.cu).
+cudaError_t launch_tc_prod_g8(const DecodeArgs& a, const DecodePlan& p, const float* p_all, cudaStream_t stream);
 }  // namespace tq

@@ -139,6 +139,12 @@ cudaError_t launch_quantize_queries(const void* q, int q_dtype, int64_t rows, in
 bool tc_decode_supported(const DecodeArgs& a);
 int tc_partials_per_sequence_split();
 cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
+// Its product-quantised key form (tq_decode_tc_p.cu): a.k_bits is the total key width,
+// p_all the projection p = S q~ per (sequence, q head); p.num_splits CTAs.
+bool tc_prod_decode_supported(const DecodeArgs& a);
+cudaError_t launch_tc_prod(const DecodeArgs& a, const DecodePlan& p, const float* p_all, cudaStream_t stream);
+// SM count of the current device (tq_write.cu).
+int device_sms();
 
 bool prefill_mq_supported(const DecodeArgs& a);
 MqPlan plan_prefill_mq(const DecodeArgs& a, int num_sms, bool one_row_per_window);

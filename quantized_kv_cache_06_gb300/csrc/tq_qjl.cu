@@ -1,4 +1,5 @@
-// Product-quantised ("QJL residual") key rows: writer and paged decode (sm_103a, SIMT).
+// Product-quantised ("QJL residual") key rows: writer and paged decode (sm_103a, SIMT forms;
+// the tensor-core forms are in tq_write_tc.cu and tq_decode_tc_p.cu / _q.cu).
 //
 // TurboQuant docs: "vLLM Reference Audit" (File Map: "MSE and QJL codecs" with indices,
 // norms and signs, TurboQuantMSE / TurboQuantProd; Feature Checklist: "QJL residual").
@@ -15,7 +16,7 @@
 //                           indices, residual; the D projections S r come from S^T staged
 //                           in shared memory, output i = lane + 32 e, so a warp ballot per
 //                           e is directly sign word e of the row.
-//   qjl_project_kernel      one warp per (sequence, q head): q_rot = R q times the softmax
+//   qjl_project_kernel      S^T staged once per CTA; a warp per (sequence, q head): q_rot = R q times the softmax
 //                           scale and log2(e) (as the decode uses it) and p = S q_rot,
 //                           written to the workspace.
 //   decode_prod_split_kernel  the SIMT split decode with the sketch term added to the MSE
@@ -128,31 +129,63 @@ write_prod_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads,
 }
 
 // p[row][i] = sum_j S[i][j] q_rot[j] for row = (sequence, q head), q_rot = R q times the
-// softmax scale and log2(e) -- the decode's own rotated query.
+// softmax scale and log2(e) -- the decode's own rotated query.  A CTA of 8 warps takes
+// kProjRows rows per warp: S^T is staged in shared memory once (padded to D + 1 columns, so
+// the staging stores and the reads of column i by lane i are conflict free), each query row
+// goes through the warp FWHT, and lane l accumulates outputs l + 32 e over j.
+constexpr int kProjRows = 4;
 template <int E>
 __global__ void __launch_bounds__(256)
 qjl_project_kernel(DecodeArgs a, const float* __restrict__ smat, float* __restrict__ p_out) {
   constexpr int D = 32 * E;
+  extern __shared__ float s_t[];  // S^T, padded: s_t[j * (D + 1) + i] = S[i][j]
   __shared__ float qs[8][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + warp;
-  if (row >= (int64_t)a.batch * a.num_q_heads) return;
+  for (int k = threadIdx.x; k < D * D; k += blockDim.x) {
+    const int i = k / D, j = k - i * D;
+    s_t[j * (D + 1) + i] = __ldg(smat + k);
+  }
+  __syncthreads();
+  const int64_t rows = (int64_t)a.batch * a.num_q_heads;
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kProdLog2e / sqrtf((float)D);
-  float qr[E];
+  for (int k = 0; k < kProjRows; ++k) {
+    const int64_t row = ((int64_t)blockIdx.x * 8 + warp) * kProjRows + k;
+    if (row >= rows) break;
+    float qr[E];
 #pragma unroll
-  for (int i = 0; i < E; ++i) qr[i] = load_as_f32(a.q, row * D + lane * E + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
-  fwht_warp<E>(qr);
+    for (int i = 0; i < E; ++i) qr[i] = load_as_f32(a.q, row * D + lane * E + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
+    fwht_warp<E>(qr);
 #pragma unroll
-  for (int i = 0; i < E; ++i) qs[warp][lane * E + i] = qr[i] * qmul;
-  __syncwarp();
+    for (int i = 0; i < E; ++i) qs[warp][lane * E + i] = qr[i] * qmul;
+    __syncwarp();
+    float acc[E];
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int i = lane + 32 * e;
-    float acc = 0.f;
-    for (int j = 0; j < D; ++j) acc = fmaf(__ldg(smat + (int64_t)i * D + j), qs[warp][j], acc);
-    p_out[row * D + i] = acc;
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int j = 0; j < D; ++j) {
+      const float qj = qs[warp][j];
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(s_t[j * (D + 1) + lane + 32 * e], qj, acc[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) p_out[row * D + lane + 32 * e] = acc[e];
+    __syncwarp();
   }
+}
+
+// Enqueues the projection of every (sequence, q head) of `a` into p_out [rows][D].
+template <int E>
+cudaError_t launch_qjl_project(const DecodeArgs& a, const float* smat, float* p_out, cudaStream_t stream) {
+  constexpr int D = 32 * E;
+  const int64_t rows = (int64_t)a.batch * a.num_q_heads;
+  const size_t smem = (size_t)D * (D + 1) * sizeof(float);
+  cudaError_t err = cudaFuncSetAttribute(qjl_project_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int64_t per_cta = 8 * kProjRows;
+  qjl_project_kernel<E><<<(unsigned)((rows + per_cta - 1) / per_cta), 256, smem, stream>>>(a, smat, p_out);
+  err = cudaGetLastError();
+  if (err == cudaSuccess) count_launches(1);
+  return err;
 }
 
 struct ProdSplitView {
@@ -317,10 +350,8 @@ cudaError_t launch_prod_decode_e(const DecodeArgs& a, const float* smat, const D
   part.acc = static_cast<float*>(a.workspace);
   part.ml = part.acc + (size_t)qrows * p.num_splits * D;
   float* p_all = part.ml + (size_t)qrows * p.num_splits * 2;
-  qjl_project_kernel<E><<<(unsigned)((qrows + 7) / 8), 256, 0, stream>>>(a, smat, p_all);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_qjl_project<E>(a, smat, p_all, stream);
   if (err != cudaSuccess) return err;
-  count_launches(1);
   const int G = a.num_q_heads / a.num_kv_heads;
   dim3 grid(p.num_splits, a.num_kv_heads, a.batch);
   switch (G) {
@@ -340,9 +371,25 @@ cudaError_t launch_prod_decode_e(const DecodeArgs& a, const float* smat, const D
 
 bool prod_supported(int head_dim, int bits) { return (head_dim == 64 || head_dim == 128) && bits >= 3 && bits <= 5; }
 
+namespace {
+// The tensor-core form: one CTA per SM, the split partials and prefix sums of the
+// tensor-core decode, then p (16-byte aligned).
+DecodePlan prod_tc_plan(const DecodeArgs& a) {
+  DecodePlan p{};
+  p.kernel = 2;
+  p.num_splits = device_sms();
+  const size_t slots = (size_t)tc_partials_per_sequence_split() * (p.num_splits + std::max(0, a.batch));
+  p.workspace_bytes =
+      (slots * a.num_q_heads * (a.head_dim + 2) * sizeof(float) + (std::max(0, a.batch) + 1) * sizeof(int) + 15) / 16 * 16;
+  return p;
+}
+}  // namespace
+
 size_t prod_decode_workspace(const DecodeArgs& a, const DecodePlan& p) {
   const size_t qrows = (size_t)std::max(0, a.batch) * a.num_q_heads;
-  return qrows * p.num_splits * (a.head_dim + 2) * sizeof(float) + qrows * a.head_dim * sizeof(float) + 16;
+  const size_t simt = qrows * p.num_splits * (a.head_dim + 2) * sizeof(float) + qrows * a.head_dim * sizeof(float) + 16;
+  const size_t tc = prod_tc_plan(a).workspace_bytes + qrows * a.head_dim * sizeof(float) + 16;
+  return std::max(simt, tc);  // either form fits, whatever the widths
 }
 
 cudaError_t launch_write_prod(const WriteArgs& a, const float* smat, cudaStream_t stream, int num_sms) {
@@ -391,6 +438,14 @@ cudaError_t launch_decode_prod(const DecodeArgs& a, const float* smat, const Dec
     if (err != cudaSuccess) return err;
   }
   if (a.batch == 0) return cudaSuccess;
+  if (tc_prod_decode_supported(a)) {
+    // p = S q~ after the tensor-core partials, then the tensor-core split kernel and combine
+    const DecodePlan tp = prod_tc_plan(a);
+    float* p_all = reinterpret_cast<float*>(static_cast<unsigned char*>(a.workspace) + tp.workspace_bytes);
+    const cudaError_t err = launch_qjl_project<4>(a, smat, p_all, stream);
+    if (err != cudaSuccess) return err;
+    return launch_tc_prod(a, tp, p_all, stream);
+  }
   if (a.head_dim == 64) return launch_prod_decode_e<2>(a, smat, p, stream);
   if (a.head_dim == 128) return launch_prod_decode_e<4>(a, smat, p, stream);
   return cudaErrorInvalidValue;

@@ -116,13 +116,6 @@ write_rows_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads,
   }
 }
 
-int device_sms() {
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  return sms > 0 ? sms : 1;
-}
-
 template <typename T>
 cudaError_t launch_write_typed(const WriteArgs& a, cudaStream_t stream, int grid) {
   const int64_t rows = a.num_tokens * a.num_kv_heads;
@@ -148,6 +141,13 @@ cudaError_t launch_write_typed(const WriteArgs& a, cudaStream_t stream, int grid
 }
 
 }  // namespace
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
+}
 
 cudaError_t launch_validate_slots(const WriteArgs& a, cudaStream_t stream, int num_sms) {
   const int vgrid = (int)std::min<int64_t>((a.num_tokens + 255) / 256, (int64_t)num_sms * 4);

@@ -296,11 +296,13 @@ def test_decode_empty_batch(tq):
 
 
 # ---------------------------------------------------------------- tensor-core decode edge cases
-# (block size 16, K/V bits in {2, 4}, both 3 or both 5, GQA group 4 or 8: the shapes the
-# tensor-core kernel takes)
+# (block size 16, K and V widths 2 to 5 bits each, GQA group 4 or 8: the shapes the
+# tensor-core kernel takes; 3- and 5-bit widths use its window mode, independently for K
+# and V)
 
 @pytest.mark.parametrize("kb,vb,hq", [(4, 4, 32), (4, 2, 32), (2, 4, 64), (2, 2, 64), (4, 2, 64), (3, 3, 32),
-                                      (3, 3, 64), (5, 5, 32), (5, 5, 64)])
+                                      (3, 3, 64), (5, 5, 32), (5, 5, 64), (3, 4, 32), (4, 3, 64), (5, 2, 32),
+                                      (2, 5, 64), (3, 5, 32), (5, 3, 64)])
 def test_tc_decode_ragged_and_empty_sequences(tq, kb, vb, hq):
     # lengths with empty sequences in the middle, ragged last blocks, a single token, and
     # fewer blocks in total than there are SMs (some CTAs own no block)
@@ -312,10 +314,10 @@ def test_tc_decode_ragged_and_empty_sequences(tq, kb, vb, hq):
     assert np.all(got[1] == 0) and np.all(got[5] == 0)
 
 
-@pytest.mark.parametrize("d,bits,hq", [(64, 4, 16), (256, 4, 16), (256, 3, 16), (256, 3, 32), (256, 5, 16),
-                                       (256, 5, 32)])
-def test_tc_decode_other_head_dims(tq, d, bits, hq):
-    w, kp, vp = _small_case(tq, d=d, h=4, hq=hq, kb=bits, vb=bits, lens=(70, 3, 129), bs=16, seed=d + bits)
+@pytest.mark.parametrize("d,kb,vb,hq", [(64, 4, 4, 16), (256, 4, 4, 16), (256, 3, 3, 16), (256, 3, 3, 32),
+                                         (256, 5, 5, 16), (256, 5, 5, 32), (256, 3, 4, 16), (256, 5, 2, 32)])
+def test_tc_decode_other_head_dims(tq, d, kb, vb, hq):
+    w, kp, vp = _small_case(tq, d=d, h=4, hq=hq, kb=kb, vb=vb, lens=(70, 3, 129), bs=16, seed=d + kb + 7 * vb)
     got, st = gpu_decode(tq, w, kp, vp)
     assert st == 0
     assert_decode_close(got, oracle_decode(w, kp.cpu().numpy(), vp.cpu().numpy(), OracleCodec(d)))

@@ -168,12 +168,18 @@ def assert_close(got, want):
     assert err.max() <= 0.0, float(err.max())
 
 
+# D 128, block size 16, GQA group 4 or 8 take the tensor-core decode (the sketch term as a
+# second MMA over the +-1 sign pairs); the others the SIMT split decode
 @pytest.mark.parametrize("d,hq,h,kb,vb,bs,lens,qdtype", [
     (64, 4, 4, 3, 2, 16, [1, 17, 200, 0], torch.float32),
     (64, 8, 4, 5, 5, 8, [33, 64, 5], torch.float16),
     (128, 32, 8, 4, 4, 16, [300, 129, 16, 1], torch.bfloat16),
     (128, 16, 2, 5, 3, 16, [257, 100], torch.float32),
     (128, 8, 1, 3, 4, 32, [500], torch.float16),
+    (128, 32, 8, 3, 2, 16, [0, 45, 700, 1], torch.float16),
+    (128, 64, 8, 4, 5, 16, [130, 17], torch.float32),
+    (128, 16, 4, 5, 4, 16, [33, 0, 250], torch.bfloat16),
+    (128, 16, 2, 3, 3, 16, [160, 31], torch.float16),
 ])
 def test_prod_decode_matches_oracle(tq, d, hq, h, kb, vb, bs, lens, qdtype):
     rng = np.random.default_rng(3000 + d + hq + kb * 7 + vb)
@@ -241,3 +247,34 @@ def test_prod_decode_bad_block_and_long_length(tq):
                                   torch.from_numpy(codec.centroids(vb)).cuda(), s_gpu, status=st)
     torch.cuda.synchronize()
     assert out.shape == (0, hq, d) and int(st.item()) == 0
+
+
+@pytest.mark.parametrize("hq", [32, 64])
+def test_prod_decode_tc_bad_block_and_large_norms(tq, hq):
+    # the tensor-core form: a block id past the pages is skipped and reported; key rows of
+    # norm up to ~300 and value rows up to 1e4 take its exact paths.  (Keys far larger make
+    # scores of thousands of log2 units, where fp32-level rounding of a score, ~1e-6 of its
+    # terms, already moves near-tied softmax weights by more than the output bar allows.)
+    d, h, kb, vb, bs, lens = 128, 8, 4, 4, 16, [70, 300]
+    rng = np.random.default_rng(53 + hq)
+    codec = OracleCodec(d)
+    _, s64 = sketch(tq, d)
+    bt, nb = tables(rng, lens, bs)
+    n = nb * bs * h
+    kx = rng.standard_normal((n, d)) * (10.0 ** rng.uniform(-2, 2.5, (n, 1)))
+    enc = qo.encode_prod(kx, codec.rot, codec.centroids(kb - 1), s64)
+    kp = qo.pack_prod_rows(enc["idx"], enc["z"], enc["nu"], enc["gamma"], kb).reshape(nb, bs, h, -1)
+    vx = rng.standard_normal((n, d)) * (10.0 ** rng.uniform(-2, 4, (n, 1)))
+    vidx, vnu, _ = o.encode_rows(vx, codec.rot, codec.centroids(vb))
+    vp = o.make_rows(vidx, vnu, vb).reshape(nb, bs, h, -1)
+    kp, vp = np.ascontiguousarray(kp), np.ascontiguousarray(vp)
+    q = rng.standard_normal((2, hq, d)).astype(np.float32)
+    st = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    got = run_prod_decode(tq, codec, q, kp, vp, bt, lens, kb, vb, status=st)
+    assert int(st.item()) == 0
+    assert_close(got, oracle_prod(codec, q, kp, vp, bt, lens, kb, vb, s64))
+    bad = bt.copy()
+    bad[1, 3] = nb + 9
+    got = run_prod_decode(tq, codec, q, kp, vp, bad, lens, kb, vb, status=st)
+    assert int(st.item()) == tq.TQ_ERR_BLOCK_OUT_OF_RANGE
+    assert_close(got, oracle_prod(codec, q, kp, vp, bad, lens, kb, vb, s64))
