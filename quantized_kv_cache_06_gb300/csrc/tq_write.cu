@@ -92,13 +92,16 @@ write_rows_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads,
 #pragma unroll
     for (int i = 0; i < E; ++i) v[i] *= sg[i];
     fwht_warp<E>(v);
-    const float inv = nu_s > 0.f ? inv_sqrt_d / nu_s : 0.f;  // y = H(s*x)/(sqrt(D) nu)
+    // y = H(s*x)/(sqrt(D) nu); a zero row and a row with a non-finite sum (NaN or infinite
+    // input) get u = 0, the zero row's indices, the latter with its non-finite norm
+    const bool bad = !(nu_s <= 3.402823466e38f);
+    const float inv = (nu_s > 0.f && !bad) ? inv_sqrt_d / nu_s : 0.f;
 
     for (int w = lane; w < row_words; w += 32) buf[w] = 0u;
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < E; ++i) {
-      const float u = v[i] * inv;
+      const float u = bad ? 0.f : v[i] * inv;
       int idx = 0;  // #{k : boundary_k < u}, branch-free binary search
       for (int s = nc >> 1; s > 0; s >>= 1)
         if (u > boundary[idx + s - 1]) idx += s;

@@ -31,13 +31,15 @@
 //  * Product rows (PROD, "QJL residual" keys: (b - 1)-bit MSE indices, D sign bits, nu,
 //    gamma).  The quantiser also looks up c[idx] (a per-lane replicated copy of the
 //    codebook), leaving the rotated residual r = u - c[idx] in the accumulators, and
-//    gamma = ||r||.  The sketch S r is a [16 rows x D] x [D x D] product on the same
-//    m16n8k16 MMAs: the accumulator layout of r is already the A layout, split into fp16
-//    hi + lo (r scaled by 2^10, lo by 2^12 more); S sits in shared memory as fp16 hi + lo
-//    (lo x 2^12, 16-byte chunks XOR-swizzled by row for ldmatrix), and
-//    r_hi S_hi + (r_lo S_hi + r_hi S_lo) 2^-12 carries ~22 bits, so a sign flips only where
-//    the projection is within ~1e-6 of zero.  Each 32-output sign word is assembled from
-//    its quad's bits with two shuffles.
+//    gamma = ||r||.  The sketch S r of the CTA's 128 rows (8 warps x 16) is a
+//    [128 x D] x [D x D] product on the 5th-generation tensor cores: each warp writes its
+//    rows of r (scaled by 2^10) as fp16 hi + lo (lo x 2^12 more) into the A operand in the
+//    canonical K-major layout, S sits in shared memory as fp16 hi + lo the same way, and one
+//    thread issues tcgen05.mma (M 128, N D, K 16) for r_hi S_hi into one TMEM accumulator
+//    and r_lo S_hi + r_hi S_lo into a second; r_hi S_hi + (r_lo S_hi + r_hi S_lo) 2^-12
+//    carries ~22 bits, so a sign flips only where the projection is within ~1e-6 of zero.
+//    Each warp reads its TMEM lane quarter back (32 rows x D/2 columns): one thread per row,
+//    so 32 consecutive columns are a sign word.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -95,14 +97,52 @@ __device__ __forceinline__ void mma_rot<__nv_bfloat16>(float (&d)[4], uint32_t a
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
-// d = A * B + d, fp16 operands (the sketch of product rows)
-__device__ __forceinline__ void mma_f16_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                            uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// ---- tcgen05 (the sketch of product rows) ------------------------------------------------
+// Shared-memory matrix descriptor of an operand in the canonical K-major layout without
+// swizzle: 8-row x 16-byte core matrices of 128 contiguous bytes, `lbo` bytes between the
+// two core matrices of a 16-element k-step, `sbo` bytes between 8-row groups.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
+         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | ((uint64_t)1 << 46);
 }
+// D[tmem] (+)= A B^T, kind::f16 (issued by one thread)
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+// the mbarrier completes when every MMA issued so far by this thread has
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape, one warp)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Waits for the phase of `bar` with parity `parity`; false after `tries` unsuccessful tries.
+__device__ __forceinline__ bool mbar_wait_w(uint32_t bar, uint32_t parity, uint32_t tries) {
+  for (uint32_t i = 0; i < tries; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
 // d = A * B + d, bf16 operands (the parts of fp32 rows)
 __device__ __forceinline__ void mma_acc_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                              uint32_t b0, uint32_t b1) {
@@ -192,7 +232,9 @@ __host__ __device__ constexpr int write_tc_ctas_per_sm() {
 // product rows the codebook copies and S hi / lo.
 template <int D, bool PROD>
 __host__ __device__ constexpr int write_tc_fixed_smem() {
-  return kQCells * kQCopies * (int)sizeof(QCell) + (PROD ? 16 * 32 * 4 + 2 * D * D * 2 : 0);
+  // product rows: codebook copies, S hi / lo (D x D fp16 each), the sketch's A operand hi / lo
+  // (128 rows x D fp16 each)
+  return kQCells * kQCopies * (int)sizeof(QCell) + (PROD ? 16 * 32 * 4 + 4 * D * D + 512 * D : 0);
 }
 template <int D, int BITS, bool PROD>
 __host__ __device__ constexpr int write_tc_row_bytes() {
@@ -218,14 +260,26 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
   const int H = a.num_kv_heads;
 
   // shared memory: quantiser table | per warp: 2 raw tiles + 1 packed tile
+  constexpr int kQC = kQCopies;
   QCell* qtab = reinterpret_cast<QCell*>(smem);
-  // product rows: codebook, 32 lane copies (entry k of lane l at 4 (32 k + l)); S hi, S lo
-  float* ctab = reinterpret_cast<float*>(smem + kQCells * kQCopies * sizeof(QCell));
-  unsigned char* s_hi = smem + kQCells * kQCopies * sizeof(QCell) + 16 * 32 * 4;
+  // product rows: codebook, 32 lane copies (entry k of lane l at 4 (32 k + l)); S hi, S lo;
+  // the sketch's A operand hi, lo (all operands in the canonical K-major layout, kSbo bytes
+  // between 8-row groups)
+  float* ctab = reinterpret_cast<float*>(smem + kQCells * kQC * sizeof(QCell));
+  unsigned char* s_hi = smem + kQCells * kQC * sizeof(QCell) + 16 * 32 * 4;
   unsigned char* s_lo = s_hi + D * D * 2;
-  unsigned char* wbase = smem + write_tc_fixed_smem<D, PROD>() + warp * (2 * TILE_BYTES + 16 * RB + 16);
+  unsigned char* a_hi = s_lo + D * D * 2;
+  unsigned char* a_lo = a_hi + 128 * D * 2;
+  constexpr int kSbo = 16 * D;
+  // instruction descriptor: fp32 D, fp16 A and B, both K-major, N = D, M = 128
+  constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(D >> 3) << 17) | (8u << 24);
+  // per warp: 2 raw tiles; once a tile's MMAs have read it, its buffer holds the 3/5-bit
+  // index staging (kStage entries a row) and then the packed rows (at kPackOff)
+  unsigned char* wbase = smem + write_tc_fixed_smem<D, PROD>() + warp * (2 * TILE_BYTES);
+  constexpr int kStage = D / 2 + 8;
+  constexpr int kPackOff = (BITS == 3 || BITS == 5) ? 16 * kStage * 2 : 0;
+  static_assert(kPackOff + 16 * RB <= TILE_BYTES, "staging and packed rows must fit a raw tile buffer");
   unsigned char* raw_buf = wbase;
-  unsigned char* pack_buf = wbase + 2 * TILE_BYTES;
 
   // decision points (correctly rounded midpoints of neighbouring fp32 centroids) and
   // the quantiser grid
@@ -266,18 +320,18 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
     q.lo = below;
     q.point = point - 0.5f;  // in g' (exact, and +inf stays +inf)
 #pragma unroll
-    for (int copy = 0; copy < kQCopies; ++copy) qtab[cell * kQCopies + copy] = q;
+    for (int copy = 0; copy < kQC; ++copy) qtab[cell * kQC + copy] = q;
   }
   if constexpr (PROD) {
     for (int i = threadIdx.x; i < NC * 32; i += blockDim.x) ctab[i] = a.centroids[i >> 5];
-    // S[n][k] (n: projection, k: coordinate) as fp16 hi and lo x 2^12, row n at 2 D n bytes,
-    // 16-byte chunk k / 8 stored at chunk (k / 8) ^ (n & 7)
+    // S[n][k] (n: projection, k: coordinate) as fp16 hi and lo x 2^12, the B operand of the
+    // sketch: N = D rows of D k-columns, canonical K-major
     for (int i = threadIdx.x; i < D * D; i += blockDim.x) {
       const int n = i / D, k = i - n * D;
       const float sv = __ldg(args.smat + i);
       const __half hi = __float2half_rn(sv);
       const __half lo = __float2half_rn((sv - __half2float(hi)) * 4096.0f);
-      const int off = n * (2 * D) + ((((k >> 3) ^ (n & 7))) << 4) + (k & 7) * 2;
+      const int off = (n >> 3) * kSbo + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
       *reinterpret_cast<__half*>(s_hi + off) = hi;
       *reinterpret_cast<__half*>(s_lo + off) = lo;
     }
@@ -320,12 +374,29 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
   // shared address of cell n, this lane's copy: bits(g' + 1.5 * 2^23) * 128 + q_addr_bias
   constexpr uint32_t kMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
   const uint32_t q_addr_bias =
-      smem_addr(qtab) + (uint32_t)((lane & 15) * sizeof(QCell)) - kMagicBits * (uint32_t)(kQCopies * sizeof(QCell));
+      smem_addr(qtab) + (uint32_t)((lane & (kQC - 1)) * sizeof(QCell)) - kMagicBits * (uint32_t)(kQC * sizeof(QCell));
 
   // launched as a programmatic dependent of the slot validation: the set-up above overlaps
   // it; the status word is read once that grid has completed
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (*a.status != kOk) return;  // a slot failed validation: write nothing
+  // product rows: 2 D TMEM columns (D_main, D_lo of the sketch) and the MMA mbarrier
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t mma_bar;
+  uint32_t tmem = 0, mma_phase = 0;
+  if constexpr (PROD) {
+    if (warp == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(&tmem_slot)),
+                   "n"(2 * D)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    if (threadIdx.x == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&mma_bar)) : "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    tmem = tmem_slot;
+  }
 
   const int64_t num_rows = a.num_tokens * H;
   const int64_t num_tiles = (num_rows + 15) / 16;
@@ -366,8 +437,12 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
   int64_t tile = (int64_t)blockIdx.x * kWWarps + warp;
   int buf = 0;
   load_tile(tile, 0);
-  for (; tile < num_tiles; tile += wstride, buf ^= 1) {
+  // every warp of a CTA runs the same iterations (product rows meet at CTA barriers); a warp
+  // whose tile is past the end only keeps up
+  for (int64_t ctile = (int64_t)blockIdx.x * kWWarps; ctile < num_tiles; ctile += wstride, tile += wstride, buf ^= 1) {
+    const bool active = tile < num_tiles;
     load_tile(tile + wstride, buf ^ 1);
+    unsigned char* pack_buf = raw_buf + buf * TILE_BYTES + kPackOff;
     // slot of the tile's token `lane` for the slab store below (a global load, read early)
     int64_t my_slot = -1;
     if (16 % H == 0 && lane < 16 / H) {
@@ -376,7 +451,7 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
     }
     cp_wait_w<1>();
     __syncwarp();
-
+    if (active) {
     // ---- rotation: MMA per block, then butterflies across blocks ------------------
     // acc[j][nt] = (row r: cols 2c, 2c+1 | row r+8: cols 2c, 2c+1) of block j, n-tile nt
     float acc[NB][2][4];
@@ -465,10 +540,15 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
     };
     float ss0, ss1;
     row_sums(ss0, ss1);
-    // A row whose sum of squares leaves [2^-100, 2^100] (coordinates beyond about 1e14 or
-    // below about 1e-16: bf16 and fp32 rows can) is brought back by an exact power of two
-    // 2^-ex taken from its largest |y|; u is scale free, and the norm is scaled back by 2^ex.
+    // One vote keeps two rare cases off the common path.  A row whose sum of squares leaves
+    // [2^-100, 2^100] (coordinates beyond about 1e14 or below about 1e-16: bf16 and fp32 rows
+    // can) is brought back by an exact power of two 2^-ex taken from its largest |y|; u is
+    // scale free, and the norm is scaled back by 2^ex.  A row whose sum stays non-finite (a
+    // NaN or infinite input) is quantised as a zero row: its coordinates and its row scale
+    // are set to 0, so every grid coordinate is a valid cell, and it keeps the non-finite sum
+    // as its norm, as sqrt would give.
     int ex0 = 0, ex1 = 0;
+    bool bad0 = false, bad1 = false;
     const bool odd0 = !(ss0 >= 0x1p-100f && ss0 <= 0x1p100f), odd1 = !(ss1 >= 0x1p-100f && ss1 <= 0x1p100f);
     if (__any_sync(kFullMask, odd0 || odd1)) {
       float m0 = 0.f, m1 = 0.f;
@@ -483,8 +563,7 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
       m0 = fmaxf(m0, __shfl_xor_sync(kFullMask, m0, 2));
       m1 = fmaxf(m1, __shfl_xor_sync(kFullMask, m1, 1));
       m1 = fmaxf(m1, __shfl_xor_sync(kFullMask, m1, 2));
-      // zero rows and non-finite rows keep their sums (handled below)
-      if (odd0 && m0 > 0.f && m0 <= 3.402823466e38f) frexpf(m0, &ex0);
+      if (odd0 && m0 > 0.f && m0 <= 3.402823466e38f) frexpf(m0, &ex0);  // zero and infinite rows: none
       if (odd1 && m1 > 0.f && m1 <= 3.402823466e38f) frexpf(m1, &ex1);
 #pragma unroll
       for (int j = 0; j < NB; ++j)
@@ -496,24 +575,8 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
           acc[j][nt][3] = scale_pow2(acc[j][nt][3], -ex1);
         }
       row_sums(ss0, ss1);
-    }
-    // ||x|| = sqrt(ss / D); u = y / sqrt(ss); grid coordinate g = u * q_a + q_b.
-    // Every partial sum above only grows, so y^2 <= ss (1 + 2^-23) + 2^-150 for each y of
-    // the row, even when ss is subnormal; adding 2^-149 under the root keeps |u| within a
-    // few ulp of 1 and g inside [1/4, 2 q_a + 1/2) with no clamp (it moves ss by at most one
-    // ulp, and only below 2^-124; an all-zero row gets g = q_b, i.e. u = 0).  rsqrtf (2 ulp)
-    // is enough: it moves g by < 1e-4 cell and u by < 1e-6, inside the decision tolerance,
-    // and the stored norm ss * rsqrt(ss) / sqrt(D) by < 1e-6 relative.
-    const float rs0 = rsqrtf(ss0 + 0x1p-149f), rs1 = rsqrtf(ss1 + 0x1p-149f);
-    const float inv_sqrt_d = 1.0f / sqrtf((float)D);
-    float nu0 = scale_pow2(ss0 * rs0 * inv_sqrt_d, ex0), nu1 = scale_pow2(ss1 * rs1 * inv_sqrt_d, ex1);
-    const float ga0 = q_a * rs0, ga1 = q_a * rs1;
-    // A NaN or infinite input (the only way to a non-finite sum) would give a NaN grid
-    // coordinate, whose bits address nothing: such rows are quantised as zero rows.
-    if (__any_sync(kFullMask, !(ss0 <= 3.402823466e38f) || !(ss1 <= 3.402823466e38f))) {
-      const bool bad0 = !(ss0 <= 3.402823466e38f), bad1 = !(ss1 <= 3.402823466e38f);
-      if (bad0) nu0 = ss0;  // +inf (a sum that overflowed) or NaN, as sqrt would give
-      if (bad1) nu1 = ss1;
+      bad0 = !(ss0 <= 3.402823466e38f);
+      bad1 = !(ss1 <= 3.402823466e38f);
 #pragma unroll
       for (int j = 0; j < NB; ++j)
 #pragma unroll
@@ -522,22 +585,35 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
           if (bad1) acc[j][nt][2] = acc[j][nt][3] = 0.f;
         }
     }
+    // ||x|| = sqrt(ss / D); u = y / sqrt(ss); grid coordinate g = u * q_a + q_b.
+    // Every partial sum above only grows, so y^2 <= ss (1 + 2^-23) + 2^-150 for each y of
+    // the row, even when ss is subnormal; adding 2^-149 under the root keeps |u| within a
+    // few ulp of 1 and g inside [1/4, 2 q_a + 1/2) with no clamp (it moves ss by at most one
+    // ulp, and only below 2^-124; an all-zero row gets g = q_b, i.e. u = 0).  rsqrtf (2 ulp)
+    // is enough: it moves g by < 1e-4 cell and u by < 1e-6, inside the decision tolerance,
+    // and the stored norm ss * rsqrt(ss) / sqrt(D) by < 1e-6 relative.
+    const float rs0 = bad0 ? 0.f : rsqrtf(ss0 + 0x1p-149f), rs1 = bad1 ? 0.f : rsqrtf(ss1 + 0x1p-149f);
+    const float inv_sqrt_d = 1.0f / sqrtf((float)D);
+    const float nu0 = bad0 ? ss0 : scale_pow2(ss0 * rs0 * inv_sqrt_d, ex0);
+    const float nu1 = bad1 ? ss1 : scale_pow2(ss1 * rs1 * inv_sqrt_d, ex1);
+    const float ga0 = q_a * rs0, ga1 = q_a * rs1;
 
     // ---- quantise and pack into this warp's row buffer ------------------------------
     // the cell and the comparison both use the grid coordinate; exact for every u not
     // within a few ulp of a decision point, whichever neighbouring cell it lands in
     // g: shifted grid coordinate g'; m: g' + 1.5 * 2^23 (its bits give the cell)
     auto quant = [&](float g, float m) -> uint32_t {
-      const uint32_t addr = __float_as_uint(m) * (uint32_t)(kQCopies * sizeof(QCell)) + q_addr_bias;
+      const uint32_t addr = __float_as_uint(m) * (uint32_t)(kQC * sizeof(QCell)) + q_addr_bias;
       uint32_t lo, pt;
       asm("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(lo), "=r"(pt) : "r"(addr));
       return lo + (g > __uint_as_float(pt) ? 1u : 0u);
     };
     const float2 magic2 = make_float2(12582912.0f, 12582912.0f);
     // 3/5 bits: index pairs (2 BITS bits each) of row rr, coordinates 2p, 2p + 1, at
-    // stage[rr * D / 2 + p]; the tile's raw buffer is free once its MMAs have read it
+    // stage[rr * kStage + p]; the tile's raw buffer is free once its MMAs have read it.  Rows
+    // are kStage = D / 2 + 8 entries apart (16-byte aligned for the packing's loads, and 4 banks
+    // apart, so the 8 rows of a store land in different banks)
     uint16_t* stage = reinterpret_cast<uint16_t*>(raw_buf + buf * TILE_BYTES);
-    static_assert(16 * D <= TILE_BYTES, "index staging must fit the raw tile buffer");
     const uint32_t ctab_lane = smem_addr(ctab) + (uint32_t)(lane * 4);
     float rr[2] = {0.f, 0.f};  // product rows: sum of squared residuals of rows r, r + 8
 #pragma unroll
@@ -566,7 +642,7 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
           }
           // columns 16 j + 8 nt + 2c, +1
           if (BITS == 3 || BITS == 5) {
-            stage[(r + 8 * half) * (D / 2) + 8 * j + 4 * nt + c] = (uint16_t)(i0 | (i1 << BITS));
+            stage[(r + 8 * half) * kStage + 8 * j + 4 * nt + c] = (uint16_t)(i0 | (i1 << BITS));
           } else if (BITS == 4) {
             prow[8 * j + 4 * nt + c] = (unsigned char)(i0 + (i1 << 4));
           } else {
@@ -589,67 +665,23 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
       }
     }
     if constexpr (PROD) {
-      // ---- sketch S r: A = r (fp16 hi / lo), B = S^T from shared memory ----------------
-      uint32_t ah[NB][4], al[NB][4];
+      // ---- this warp's rows of the sketch's A operand: r x 2^10 as fp16 hi and lo x 2^12,
+      // rows 16 warp + r (+ 8) of the CTA tile, in the canonical K-major layout.  The
+      // accumulator layout already is the A layout: block j, part q holds row r (+ 8 for odd q),
+      // columns 16 j + 2c, +1 (+ 8 for q >= 2).
 #pragma unroll
       for (int j = 0; j < NB; ++j)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          // q: 0 row r cols 2c.., 1 row r+8, 2 row r cols 2c+8.., 3 row r+8 cols 2c+8..
           const int nt = q >> 1, e = 2 * (q & 1);
           const float x0 = acc[j][nt][e] * 1024.0f, x1 = acc[j][nt][e + 1] * 1024.0f;
           const __half2 h = __floats2half2_rn(x0, x1);
           const float2 hf = __half22float2(h);
           const __half2 l = __floats2half2_rn((x0 - hf.x) * 4096.0f, (x1 - hf.y) * 4096.0f);
-          ah[j][q] = *reinterpret_cast<const uint32_t*>(&h);
-          al[j][q] = *reinterpret_cast<const uint32_t*>(&l);
+          const int off = (2 * warp + (q & 1)) * kSbo + (2 * j + (q >> 1)) * 128 + r * 16 + c * 4;
+          *reinterpret_cast<__half2*>(a_hi + off) = h;
+          *reinterpret_cast<__half2*>(a_lo + off) = l;
         }
-      const uint32_t shi = smem_addr(s_hi), slo = smem_addr(s_lo);
-      const int mq = lane >> 3, mr = lane & 7;  // ldmatrix: this lane addresses row mr of matrix mq
-#pragma unroll 1
-      for (int w = 0; w < D / 32; ++w) {  // sign word w: outputs 32 w .. 32 w + 31 (4 n-tiles)
-        float m0[4][4], m1[4][4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m0[nt][e] = m1[nt][e] = 0.f;
-#pragma unroll
-        for (int j = 0; j < NB; ++j) {
-#pragma unroll
-          for (int np = 0; np < 2; ++np) {  // n-tiles 2 np, 2 np + 1
-            const int n = 32 * w + 16 * np + 8 * (mq >> 1) + mr;
-            const uint32_t off = (uint32_t)(n * (2 * D) + (((2 * j + (mq & 1)) ^ (n & 7)) << 4));
-            uint32_t bh[4], bl[4];
-            ldmatrix_x4(shi + off, bh[0], bh[1], bh[2], bh[3]);
-            ldmatrix_x4(slo + off, bl[0], bl[1], bl[2], bl[3]);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int nt = 2 * np + u;
-              mma_f16_acc(m0[nt], ah[j][0], ah[j][1], ah[j][2], ah[j][3], bh[2 * u], bh[2 * u + 1]);
-              mma_f16_acc(m1[nt], al[j][0], al[j][1], al[j][2], al[j][3], bh[2 * u], bh[2 * u + 1]);
-              mma_f16_acc(m1[nt], ah[j][0], ah[j][1], ah[j][2], ah[j][3], bl[2 * u], bl[2 * u + 1]);
-            }
-          }
-        }
-        // bit 8 nt + 2 c + e of the word of row r (m*[nt][e]) and of row r + 8 (m*[nt][2 + e])
-        uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int bit = 8 * nt + 2 * c + e;
-            if (fmaf(m1[nt][e], 1.0f / 4096, m0[nt][e]) >= 0.f) w0 |= 1u << bit;
-            if (fmaf(m1[nt][2 + e], 1.0f / 4096, m0[nt][2 + e]) >= 0.f) w1 |= 1u << bit;
-          }
-        w0 |= __shfl_xor_sync(kFullMask, w0, 1);
-        w0 |= __shfl_xor_sync(kFullMask, w0, 2);
-        w1 |= __shfl_xor_sync(kFullMask, w1, 1);
-        w1 |= __shfl_xor_sync(kFullMask, w1, 2);
-        if (c == 0) {
-          *reinterpret_cast<uint32_t*>(pack_buf + r * RB + IB + 4 * w) = w0;
-          *reinterpret_cast<uint32_t*>(pack_buf + (r + 8) * RB + IB + 4 * w) = w1;
-        }
-      }
     }
     __syncwarp();
     if constexpr (BITS == 3 || BITS == 5) {
@@ -658,7 +690,7 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
 #pragma unroll
       for (int k = 0; k < 16 * GPR / 32; ++k) {
         const int g = lane + 32 * k, row = g / GPR, q = g % GPR;
-        const uint4* src = reinterpret_cast<const uint4*>(stage + row * (D / 2) + q * 16);
+        const uint4* src = reinterpret_cast<const uint4*>(stage + row * kStage + q * 16);
         const uint4 v0 = src[0], v1 = src[1];
         const uint32_t w8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         uint32_t out[BITS];
@@ -678,6 +710,57 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
       __syncwarp();
     }
 
+    }  // active
+
+    if constexpr (PROD) {
+      // ---- sketch S r of the CTA's 128 rows on the tensor cores (tcgen05): D_main =
+      // r_hi S_hi^T, D_lo = r_lo S_hi^T + r_hi S_lo^T in TMEM, one 128 x D x 16 MMA per
+      // k-step and product, issued by one thread; then each warp reads 32 rows (its TMEM lane
+      // quarter) x D/2 columns back and writes their sign words to the owners' row buffers.
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+        const uint32_t ah = smem_addr(a_hi), al = smem_addr(a_lo), bh = smem_addr(s_hi), bl = smem_addr(s_lo);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ko = (uint32_t)(256 * k);  // two 8-column core matrices per k-step
+          umma_f16(tmem, umma_desc(ah + ko, 128, kSbo), umma_desc(bh + ko, 128, kSbo), kIdesc, k > 0);
+          umma_f16(tmem + D, umma_desc(al + ko, 128, kSbo), umma_desc(bh + ko, 128, kSbo), kIdesc, k > 0);
+          umma_f16(tmem + D, umma_desc(ah + ko, 128, kSbo), umma_desc(bl + ko, 128, kSbo), kIdesc, true);
+        }
+        umma_commit(smem_addr(&mma_bar));
+      }
+      const bool landed = mbar_wait_w(smem_addr(&mma_bar), mma_phase, kDefaultWaitTries);
+      if (__syncthreads_or(!landed)) {  // the MMAs did not complete in time: stop, no rows written
+        if (threadIdx.x == 0) atomicMax(a.status, (int32_t)kTimeout);
+        mbar_wait_w(smem_addr(&mma_bar), mma_phase, kDefaultWaitTries);
+        break;
+      }
+      mma_phase ^= 1u;
+      asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+      const int quarter = warp & 3, part = warp >> 2;
+      const int crow = 32 * quarter + lane;  // this thread's row of the CTA tile
+      unsigned char* owner = smem + write_tc_fixed_smem<D, PROD>() + (crow >> 4) * (2 * TILE_BYTES) + buf * TILE_BYTES +
+                             kPackOff + (crow & 15) * RB + IB;
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int col = part * (D / 2) + 32 * cc;
+        uint32_t vm[32], vl[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)col, vm);
+        tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(D + col), vl);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+        uint32_t word = 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (fmaf(__uint_as_float(vl[j]), 1.0f / 4096, __uint_as_float(vm[j])) >= 0.f) word |= 1u << j;
+        *reinterpret_cast<uint32_t*>(owner + 4 * (col >> 5)) = word;
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+      __syncthreads();
+    }
+
+    if (active) {
     // ---- store: token slabs (H rows) or single rows ---------------------------------
     const int64_t row0 = tile * 16;
     if (16 % H == 0 && (H * RB) % 16 == 0) {
@@ -707,9 +790,16 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
         }
       }
     }
+    }  // active
     __syncwarp();
   }
   cp_wait_w<0>();
+  if constexpr (PROD) {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "n"(2 * D) : "memory");
+  }
 }
 
 }  // namespace
@@ -745,8 +835,7 @@ cudaError_t launch_write_tc(const WriteArgs& a, cudaStream_t stream, int grid) {
   t.a = a;
 #define TQ_WTC(T, D, BITS)                                                                                    \
   if (a.head_dim == D && a.bits == BITS) {                                                                    \
-    constexpr int RB = write_tc_row_bytes<D, BITS, false>();                                                  \
-    const size_t smem = write_tc_fixed_smem<D, false>() + kWWarps * (2 * 16 * D * sizeof(T) + 16 * RB + 16);  \
+    const size_t smem = write_tc_fixed_smem<D, false>() + kWWarps * (2 * 16 * D * sizeof(T));                  \
     auto kern = write_tc_kernel<T, D, BITS, false>;                                                           \
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
     if (err != cudaSuccess) return err;                                                                       \
@@ -781,8 +870,7 @@ cudaError_t launch_write_prod_tc(const WriteArgs& a, const float* smat, cudaStre
   t.smat = smat;
 #define TQ_WTP(T, D, MB)                                                                                      \
   if (a.head_dim == D && a.bits == MB + 1) {                                                                  \
-    constexpr int RB = write_tc_row_bytes<D, MB, true>();                                                     \
-    const size_t smem = write_tc_fixed_smem<D, true>() + kWWarps * (2 * 16 * D * sizeof(T) + 16 * RB + 16);   \
+    const size_t smem = write_tc_fixed_smem<D, true>() + kWWarps * (2 * 16 * D * sizeof(T));                   \
     auto kern = write_tc_kernel<T, D, MB, true>;                                                              \
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
     if (err != cudaSuccess) return err;                                                                       \

@@ -408,6 +408,38 @@ def test_writer_rows_across_the_fp32_range(tq, d, dtype):
     check_written_rows(pages.cpu().numpy(), raw_t.float().numpy(), slots, 4, OracleCodec(d))
 
 
+@pytest.mark.parametrize("d,dtype", [(128, torch.float32), (128, torch.float16), (128, torch.bfloat16),
+                                     (64, torch.float32), (256, torch.float16), (256, torch.float32)])
+def test_writer_non_finite_rows_are_zero_rows(tq, d, dtype):
+    # a row with a NaN or infinite coordinate is stored with the zero row's indices and a
+    # non-finite norm; the rows around it (same 16-row tiles) are unaffected
+    t, h = 40, 4
+    rng = np.random.default_rng(71 + d)
+    raw32 = rng.standard_normal((t, h, d)).astype(np.float32)
+    raw32[3, 1, 7] = np.nan
+    raw32[10, 0, :] = np.inf
+    raw32[17, 2, 5] = -np.inf
+    raw32[21, 3, :] = 0.0
+    raw_t = torch.from_numpy(raw32).to(dtype)
+    slots = np.arange(t, dtype=np.int64)
+    pages = torch.zeros(3, 16, h, o.row_bytes(d, 4), dtype=torch.uint8, device="cuda")
+    st = tq.tq_write_kv(raw_t.cuda(), pages, torch.from_numpy(slots).cuda(), tq.tq_build_rotation(d, 42, "cuda"),
+                        lib_codebook(tq, d, 4), check=False)
+    assert int(st.item()) == 0
+    rows = pages.cpu().numpy().reshape(-1, h, o.row_bytes(d, 4))[:t]
+    nb = o.index_bytes(d, 4)
+    nu = np.ascontiguousarray(rows[..., nb:nb + 4]).view("<f4")[..., 0]
+    bad = ~np.isfinite(raw_t.float().numpy()).all(axis=2)
+    assert bad.sum() == 3
+    assert np.all(~np.isfinite(nu[bad]))
+    zero_idx = rows[21, 3, :nb]
+    for i, j in np.argwhere(bad):
+        assert np.array_equal(rows[i, j, :nb], zero_idx)
+    good = ~bad
+    stats = compare_rows(rows[good], raw_t.float().numpy().astype(np.float64)[good], OracleCodec(d), 4)
+    assert_rows_match(stats)
+
+
 def test_tc_writer_large_values_and_tiny_rows(tq):
     # rows spanning many binades (tiny, huge) still quantise exactly: u is scale free
     rng = np.random.default_rng(3)
