@@ -143,8 +143,11 @@ tq_status tq_codebook(int head_dim, int bits, float* centroids_host, float* boun
  *
  * Each row x is encoded as: nu = ||x||_2 (fp32), u = x / nu (0 if nu == 0),
  * y = R u (fp32, in-register FWHT), index_j = #{k : boundary_k < y_j} (the nearest
- * centroid, ties to the lower index), packed LSB-first, norm appended.  Rows of
- * skipped tokens keep their previous bytes.  Duplicate non-negative slots: which
+ * centroid, ties to the lower index), packed LSB-first, norm appended.  Rows of any
+ * finite scale are encoded the same way (a row whose fp32 sum of squares would leave
+ * [2^-100, 2^100] is first scaled by an exact power of two).  A row with a NaN or an
+ * infinite coordinate is stored as a zero row's indices with a non-finite norm.  Rows
+ * of skipped tokens keep their previous bytes.  Duplicate non-negative slots: which
  * token's row survives is unspecified.  Asynchronous unless status_dev is NULL; errors
  * detected on the host: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA. */
 tq_status tq_write_kv(const void* raw, tq_dtype raw_dtype, int64_t num_tokens, int num_kv_heads,
