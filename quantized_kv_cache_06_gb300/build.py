@@ -22,7 +22,8 @@ LIB_NAME = "libtq_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["tq_api.cpp", "tq_write.cu", "tq_write_tc.cu", "tq_decode.cu", "tq_decode_tc.cu", "tq_decode_tc_a.cu",
-           "tq_decode_tc_b.cu", "tq_decode_tc_c.cu", "tq_decode_tc_d.cu", "tq_decode_tc_p.cu",
+           "tq_decode_tc_b.cu", "tq_decode_tc_c.cu", "tq_decode_tc_d.cu", "tq_decode_tc_e.cu",
+           "tq_decode_tc_f.cu", "tq_decode_tc_p.cu",
            "tq_decode_tc_q.cu", "tq_prefill_mq.cu",
            "tq_dequant.cu", "tq_qjl.cu", "tq_recipe.cu", "tq_query.cu",
            "tq_small.cu"]

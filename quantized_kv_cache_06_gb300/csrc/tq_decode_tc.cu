@@ -1,4 +1,4 @@
-// Tensor-core paged decode (sm_103a): the host entry points and the D = 64 forms.
+// Tensor-core paged decode (sm_103a): the host entry points.
 // The kernels and their description are in tq_decode_tc.cuh.
 #include "tq_decode_tc.cuh"
 
@@ -7,9 +7,8 @@ namespace tq {
 bool tc_decode_supported(const DecodeArgs& a) {
   const int G = a.num_kv_heads > 0 ? a.num_q_heads / a.num_kv_heads : 0;
   const bool bits_ok = a.k_bits >= 2 && a.k_bits <= 5 && a.v_bits >= 2 && a.v_bits <= 5;
-  // exactly the instantiations of launch_tc_part_a..e
-  const bool dim_ok =
-      a.head_dim == 128 || a.head_dim == 256 || (a.head_dim == 64 && a.k_bits == 4 && a.v_bits == 4);
+  // exactly the instantiations of launch_tc_part_a..f
+  const bool dim_ok = a.head_dim == 64 || a.head_dim == 128 || a.head_dim == 256;
   return a.block_size == kBS && a.num_kv_heads >= 1 && a.num_kv_heads <= 8 && (G == 4 || G == 8) && bits_ok && dim_ok;
 }
 
@@ -20,7 +19,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStrea
   // the shapes the multi-query kernel does not take to the SIMT decode.
   if (a.bt_rows) return cudaErrorInvalidValue;
   cudaError_t (*const parts[])(const DecodeArgs&, const DecodePlan&, cudaStream_t) = {
-      launch_tc_part_a, launch_tc_part_b, launch_tc_part_c, launch_tc_part_d, launch_tc_part_e};
+      launch_tc_part_a, launch_tc_part_b, launch_tc_part_c, launch_tc_part_d, launch_tc_part_e, launch_tc_part_f};
   for (auto part : parts) {
     const cudaError_t err = part(a, p, stream);
     if (err != cudaErrorNotSupported) return err;
@@ -28,10 +27,5 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const DecodePlan& p, cudaStrea
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_tc_part_e(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream) {
-  TQ_TC_CASE(64, 4, 4, 4, 2)
-  TQ_TC_CASE(64, 4, 4, 8, 2)
-  return cudaErrorNotSupported;
-}
 
 }  // namespace tq

@@ -209,7 +209,8 @@ struct TcCfg {
   static constexpr int kWK = D * KB / 32;              // index words per K row
   static constexpr int kWV = D * VB / 32;
   static constexpr bool kKWin = KB == 3 || KB == 5;    // window mode: 3- and 5-bit rows
-  static constexpr bool kVWin = VB == 3 || VB == 5;
+  // (and 2-bit values at D = 64, whose 4 index words do not split into 8 word columns)
+  static constexpr bool kVWin = VB == 3 || VB == 5 || (VB == 2 && D == 64);
   static constexpr int kPWK = kKWin ? 1 : 16 / KB;      // pairs per word (2- and 4-bit rows)
   static constexpr int kPWV = kVWin ? 1 : 16 / VB;
   static constexpr int kKSteps = D / 16;               // score k-steps
@@ -226,10 +227,12 @@ struct TcCfg {
   // the fixed part of the shared memory.
   // Window mode (3- and 5-bit rows, whose fields cross word boundaries).  K: lane c of a
   // row owns the pairs [c D/8, (c + 1) D/8), KB D/128 whole words from word KB D/128 c,
-  // taken in chunks of KB words (32 coordinates, 8 k-steps); k-step s takes pairs
-  // c D/8 + 2s and + 2s + 1.  V: lane r owns the pairs [r D/16, (r + 1) D/16) of a token row
-  // (D = 128: 16 VB bits from bit 16 VB r, half-word aligned; D = 256: VB whole words);
-  // m-tile i takes pairs r D/16 + 2i and + 2i + 1.  3-bit rows look up a pair per 6-bit
+  // taken in chunks of KB words (32 coordinates, 8 k-steps) -- at D = 64, 16 KB bits from
+  // bit 16 KB c (half-word aligned), 4 k-steps; k-step s takes pairs c D/8 + 2s and + 2s + 1.
+  // V: lane r owns the pairs [r D/16, (r + 1) D/16) of a token row (D = 64: 8 VB bits from
+  // bit 8 VB r, byte aligned; D = 128: 16 VB bits from bit 16 VB r, half-word aligned;
+  // D = 256: VB whole words); m-tile i takes pairs r D/16 + 2i and + 2i + 1.  2-bit values at
+  // D = 64 take this mode with 4-bit pair fields (a 16-entry pair table).  3-bit rows look up a pair per 6-bit
   // field in a 64-entry table of (fp16 hi, fp16 hi) pairs; 5-bit rows look up each
   // coordinate in a 32-entry table of (fp16 hi, fp16 lo x 2^12) and join two with a PRMT.
   // Each table is replicated per lane (entry e of lane l at e * 128 + 4 l) in an 8 KB slot
@@ -251,7 +254,7 @@ struct TcCfg {
   static_assert(kVWin || kWV % 8 == 0, "V row must split into 8 interleaved word columns");
   static_assert(G == 4 || G == 8, "GQA group 4 or 8");
   static_assert(KB >= 2 && KB <= 5 && VB >= 2 && VB <= 5, "2- to 5-bit indices");
-  static_assert(!(kKWin || kVWin) || D == 128 || D == 256, "3- and 5-bit rows at head_dim 128 or 256");
+  static_assert(!(kKWin || kVWin) || D == 64 || D == 128 || D == 256, "window mode at head_dim 64, 128 or 256");
   static_assert(!PROD || KB <= 4, "product rows: 2- to 4-bit MSE indices");
 };
 
@@ -551,18 +554,31 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
   using KBt = std::integral_constant<int, KB>;
   using VBt = std::integral_constant<int, VB>;
   auto win_hi = [&](auto bits_tag, const uint32_t* w, int j, uint32_t lane_base) -> uint32_t {
-    if constexpr (decltype(bits_tag)::value == 3) return lds32(win_addr<6>(w, j, lane_base));
+    constexpr int WB = decltype(bits_tag)::value;
+    if constexpr (WB == 3) return lds32(win_addr<6>(w, j, lane_base));
+    else if constexpr (WB == 2) return lds32(win_addr<4>(w, j, lane_base));
     else return __byte_perm(lds32(win_addr<5>(w, 2 * j, lane_base)), lds32(win_addr<5>(w, 2 * j + 1, lane_base)), 0x5410u);
   };
+  // remainders: 3-bit pairs from their one-copy table, 2-bit pairs from the nibble table
+  // (hi, lo) entries, 5-bit coordinates from the high halves of their own entries
   auto win_lo = [&](auto bits_tag, const uint32_t* w, int j, uint32_t lane_base, const unsigned char* lo3) -> uint32_t {
-    if constexpr (decltype(bits_tag)::value == 3) return ld32(lo3 + (win_field<6>(w, j) << 2));
+    constexpr int WB = decltype(bits_tag)::value;
+    if constexpr (WB == 3) return ld32(lo3 + (win_field<6>(w, j) << 2));
+    else if constexpr (WB == 2) return ld32(lutV2 + (win_field<4>(w, j) << 3) + 4);
     else return __byte_perm(lds32(win_addr<5>(w, 2 * j, lane_base)), lds32(win_addr<5>(w, 2 * j + 1, lane_base)), 0x7632u);
   };
   // V window of token row `row` for this lane (pairs [r D/16, (r + 1) D/16)), from bit 0
   auto v_window = [&](const unsigned char* row, uint32_t (&w)[5]) {
 #pragma unroll
     for (int i = 0; i < 5; ++i) w[i] = 0u;
-    if (D == 128) {
+    if (D == 64) {  // 8 VB bits from bit 8 VB r: two words hold them at any byte offset
+      const int bit0 = 8 * VB * r;
+      const int wi = bit0 >> 5;
+      const uint32_t sh = (uint32_t)(bit0 & 31);
+      const uint32_t x0 = ld32(row + wi * 4), x1 = ld32(row + wi * 4 + 4);
+      w[0] = __funnelshift_r(x0, x1, sh);
+      w[1] = x1 >> sh;
+    } else if (D == 128) {
       constexpr int NL = (VB + 1) / 2;  // words spanning 16 VB bits from a half-word offset
       const int wi = (VB * r) >> 1;
       const uint32_t sh = 16u * (uint32_t)(r & 1);
@@ -576,6 +592,22 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
 #pragma unroll
       for (int i = 0; i < VB; ++i) w[i] = ld32(row + (VB * r + i) * 4);
     }
+  };
+
+  // K window of row `row` for this lane at D = 64 (pairs [8c, 8c + 8)): 16 KB bits from bit
+  // 16 KB c, half-word aligned
+  auto k_window64 = [&](const unsigned char* row, uint32_t (&w)[3]) {
+    constexpr int NL = (KB + 1) / 2;
+    const int wi = (KB * c) >> 1;
+    const uint32_t sh = 16u * (uint32_t)(c & 1);
+    uint32_t x[NL];
+#pragma unroll
+    for (int i = 0; i < NL; ++i) x[i] = ld32(row + (wi + i) * 4);
+#pragma unroll
+    for (int i = 0; i + 1 < NL; ++i) w[i] = __funnelshift_r(x[i], x[i + 1], sh);
+    w[NL - 1] = x[NL - 1] >> sh;
+#pragma unroll
+    for (int i = NL; i < 3; ++i) w[i] = 0u;
   };
 
   // Query B fragments.  G = 4: one set whose columns 0-3 hold the fp16 hi part of the
@@ -822,7 +854,20 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
           mma16816((s & 1) ? sacc1[t] : sacc[t], h00, h10, h01, h11, bq[0][s][0], bq[0][s][1]);
         }
       };
-      if constexpr (Cfg::kKWin) {
+      if constexpr (Cfg::kKWin && D == 64) {
+        uint32_t w0[NTL][3], w1[NTL][3];
+#pragma unroll
+        for (int t = 0; t < NTL; ++t) {
+          k_window64(kbase[t] + r * kts, w0[t]);
+          k_window64(kbase[t] + (r + 8) * kts, w1[t]);
+        }
+#pragma unroll
+        for (int s8 = 0; s8 < 4; ++s8)
+#pragma unroll
+          for (int t = 0; t < NTL; ++t)
+            kstep(t, s8, win_hi(KBt{}, w0[t], 2 * s8, kw_lane), win_hi(KBt{}, w1[t], 2 * s8, kw_lane),
+                  win_hi(KBt{}, w0[t], 2 * s8 + 1, kw_lane), win_hi(KBt{}, w1[t], 2 * s8 + 1, kw_lane));
+      } else if constexpr (Cfg::kKWin) {
         // chunks of KB words of this lane's window: 16 pairs, 8 k-steps each
 #pragma unroll
         for (int ch = 0; ch < D / 128; ++ch) {
@@ -876,7 +921,19 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
           if (G == 8) mma16816(sacc1, h00, h10, h01, h11, bq[kQSets - 1][s][0], bq[kQSets - 1][s][1]);
           mma16816(sacc2, l00, l10, l01, l11, bq[0][s][0], bq[0][s][1]);
         };
-        if constexpr (Cfg::kKWin) {
+        if constexpr (Cfg::kKWin && D == 64) {
+          uint32_t w0[3], w1[3];
+          k_window64(kbase[t] + r * kts, w0);
+          k_window64(kbase[t] + (r + 8) * kts, w1);
+#pragma unroll
+          for (int s8 = 0; s8 < 4; ++s8) {
+            const int j0 = 2 * s8, j1 = 2 * s8 + 1;
+            kstep_ex(s8, win_hi(KBt{}, w0, j0, kw_lane), win_hi(KBt{}, w1, j0, kw_lane),
+                     win_hi(KBt{}, w0, j1, kw_lane), win_hi(KBt{}, w1, j1, kw_lane),
+                     win_lo(KBt{}, w0, j0, kw_lane, lutK3L), win_lo(KBt{}, w1, j0, kw_lane, lutK3L),
+                     win_lo(KBt{}, w0, j1, kw_lane, lutK3L), win_lo(KBt{}, w1, j1, kw_lane, lutK3L));
+          }
+        } else if constexpr (Cfg::kKWin) {
 #pragma unroll
           for (int ch = 0; ch < D / 128; ++ch) {
             uint32_t w0[KB], w1[KB];
@@ -1198,11 +1255,15 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
         unsigned char* tab = comp == 0 ? lutKW : lutVW;
         unsigned char* tlo = comp == 0 ? lutK3L : lutV3L;
         __half hi_l, lo_l;
-        split_half(__ldg(cents + (lane & (cb == 3 ? 7 : 31))) * alpha, hi_l, lo_l);
+        split_half(__ldg(cents + (lane & (cb == 3 ? 7 : (cb == 2 ? 3 : 31)))) * alpha, hi_l, lo_l);
         const uint32_t pair_l = (uint32_t)__half_as_ushort(hi_l) | ((uint32_t)__half_as_ushort(lo_l) << 16);
-        for (int i = tid; i < (cb == 3 ? 64 : 32) * 32; i += 32 * ncons) {
+        for (int i = tid; i < (cb == 3 ? 64 : (cb == 2 ? 16 : 32)) * 32; i += 32 * ncons) {
           const int f = i >> 5, copy = i & 31;
-          if (cb == 3) {
+          if (cb == 2) {  // entry f = the fp16 hi parts of (c[f & 3], c[f >> 2]); remainders in lutV2
+            const uint32_t pa = __shfl_sync(kFullMask, pair_l, f & 3);
+            const uint32_t pb = __shfl_sync(kFullMask, pair_l, f >> 2);
+            *reinterpret_cast<uint32_t*>(tab + f * 128 + copy * 4) = __byte_perm(pa, pb, 0x5410);
+          } else if (cb == 3) {
             const uint32_t pa = __shfl_sync(kFullMask, pair_l, f & 7);  // (hi, lo) of c[f & 7]
             const uint32_t pb = __shfl_sync(kFullMask, pair_l, f >> 3);
             *reinterpret_cast<uint32_t*>(tab + f * 128 + copy * 4) = __byte_perm(pa, pb, 0x5410);
@@ -1452,13 +1513,14 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
 
 namespace tq {
 // Launchers of the instantiated forms, one per translation unit: each returns
-// cudaErrorNotSupported for a shape it does not hold.  D 128 / 256 at K width 2 and 4
-// (part a / c), 3 and 5 (part b / d), every V width, G 4 / 8; D 64 at 4/4 bits (part e).
+// cudaErrorNotSupported for a shape it does not hold.  D 128 / 256 / 64 at K width 2 and 4
+// (part a / c / e), 3 and 5 (part b / d / f), every V width, G 4 / 8.
 cudaError_t launch_tc_part_a(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 cudaError_t launch_tc_part_b(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 cudaError_t launch_tc_part_c(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 cudaError_t launch_tc_part_d(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 cudaError_t launch_tc_part_e(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
+cudaError_t launch_tc_part_f(const DecodeArgs& a, const DecodePlan& p, cudaStream_t stream);
 // Product-quantised key rows, GQA group 8 (tq_decode_tc_q.cu).
 cudaError_t launch_tc_prod_g8(const DecodeArgs& a, const DecodePlan& p, const float* p_all, cudaStream_t stream);
 }  // namespace tq

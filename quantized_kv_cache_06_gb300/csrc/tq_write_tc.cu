@@ -550,7 +550,8 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
     int ex0 = 0, ex1 = 0;
     bool bad0 = false, bad1 = false;
     const bool odd0 = !(ss0 >= 0x1p-100f && ss0 <= 0x1p100f), odd1 = !(ss1 >= 0x1p-100f && ss1 <= 0x1p100f);
-    if (__any_sync(kFullMask, odd0 || odd1)) {
+    const bool any_odd = __any_sync(kFullMask, odd0 || odd1);
+    if (any_odd) {
       float m0 = 0.f, m1 = 0.f;
 #pragma unroll
       for (int j = 0; j < NB; ++j)
@@ -592,10 +593,15 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
     // ulp, and only below 2^-124; an all-zero row gets g = q_b, i.e. u = 0).  rsqrtf (2 ulp)
     // is enough: it moves g by < 1e-4 cell and u by < 1e-6, inside the decision tolerance,
     // and the stored norm ss * rsqrt(ss) / sqrt(D) by < 1e-6 relative.
-    const float rs0 = bad0 ? 0.f : rsqrtf(ss0 + 0x1p-149f), rs1 = bad1 ? 0.f : rsqrtf(ss1 + 0x1p-149f);
+    float rs0 = rsqrtf(ss0 + 0x1p-149f), rs1 = rsqrtf(ss1 + 0x1p-149f);
     const float inv_sqrt_d = 1.0f / sqrtf((float)D);
-    const float nu0 = bad0 ? ss0 : scale_pow2(ss0 * rs0 * inv_sqrt_d, ex0);
-    const float nu1 = bad1 ? ss1 : scale_pow2(ss1 * rs1 * inv_sqrt_d, ex1);
+    float nu0 = ss0 * rs0 * inv_sqrt_d, nu1 = ss1 * rs1 * inv_sqrt_d;
+    if (any_odd) {  // (the same rare tiles) norms scaled back; non-finite rows: u = 0, norm as summed
+      nu0 = bad0 ? ss0 : scale_pow2(nu0, ex0);
+      nu1 = bad1 ? ss1 : scale_pow2(nu1, ex1);
+      if (bad0) rs0 = 0.f;
+      if (bad1) rs1 = 0.f;
+    }
     const float ga0 = q_a * rs0, ga1 = q_a * rs1;
 
     // ---- quantise and pack into this warp's row buffer ------------------------------

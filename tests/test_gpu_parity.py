@@ -315,7 +315,9 @@ def test_tc_decode_ragged_and_empty_sequences(tq, kb, vb, hq):
 
 
 @pytest.mark.parametrize("d,kb,vb,hq", [(64, 4, 4, 16), (256, 4, 4, 16), (256, 3, 3, 16), (256, 3, 3, 32),
-                                         (256, 5, 5, 16), (256, 5, 5, 32), (256, 3, 4, 16), (256, 5, 2, 32)])
+                                         (256, 5, 5, 16), (256, 5, 5, 32), (256, 3, 4, 16), (256, 5, 2, 32),
+                                         (64, 2, 2, 16), (64, 3, 3, 32), (64, 5, 5, 16), (64, 2, 5, 32),
+                                         (64, 3, 4, 16), (64, 5, 2, 32), (64, 4, 3, 32), (64, 2, 4, 16)])
 def test_tc_decode_other_head_dims(tq, d, kb, vb, hq):
     w, kp, vp = _small_case(tq, d=d, h=4, hq=hq, kb=kb, vb=vb, lens=(70, 3, 129), bs=16, seed=d + kb + 7 * vb)
     got, st = gpu_decode(tq, w, kp, vp)

@@ -27,11 +27,11 @@ LENS = [37, 301, 1000, 16, 5]
 BS = 16
 
 # (D, k_bits, v_bits, Hq, H): tensor-core decode (4/4 G4, 4/2 G8, D256 2/4, D64 4/4, 3/3 G4,
-# D256 5/5 G4, 5/5 G8, D256 3/3 G8), multi-query kernel (D64 5/5 G2), SIMT decode (D256
-# 5/5 G2)
+# D256 5/5 G4, 5/5 G8, D256 3/3 G8, D64 3/2 G8, D64 5/3 G4), multi-query kernel (D64 5/5 G2),
+# SIMT decode (D256 5/5 G2)
 SHAPES = [(128, 4, 4, 8, 2), (128, 4, 2, 16, 2), (256, 2, 4, 8, 2), (64, 4, 4, 8, 2),
           (128, 3, 3, 8, 2), (64, 5, 5, 4, 2), (256, 5, 5, 8, 2), (128, 5, 5, 16, 2), (256, 3, 3, 16, 2),
-          (256, 5, 5, 4, 2)]
+          (256, 5, 5, 4, 2), (64, 3, 2, 16, 2), (64, 5, 3, 8, 2)]
 
 
 @pytest.fixture(scope="module")
