@@ -167,6 +167,10 @@ __device__ __forceinline__ void split3_bf16(float2 x, uint32_t& hi, uint32_t& mi
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
 // +-1 pair in the operand type: sign bits of the two halves from s0, s1 (true = negative)
 template <typename T>
 __device__ __forceinline__ uint32_t pm1_pair(bool neg0, bool neg1) {
@@ -443,6 +447,79 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
     const bool active = tile < num_tiles;
     load_tile(tile + wstride, buf ^ 1);
     unsigned char* pack_buf = raw_buf + buf * TILE_BYTES + kPackOff;
+    // Re-encode of the tile rows in `rows` (bit rr: row rr) from their raw values, one row at a
+    // time by the whole warp, lane l holding coordinates [l E, l E + E): the row is first
+    // scaled by 2^-ex (ex the exponent of its largest |x|; exact), then rotated (warp FWHT),
+    // its indices found as #{b_k < u} and OR'd into the cleared index bytes, its norm scaled
+    // back; a row with a NaN or infinite coordinate gets u = 0 and its non-finite sum as the
+    // norm.  Product rows also get their residual norm and their rows of the sketch operand.
+    auto reencode_rows = [&](uint32_t rows) {
+      constexpr int E = D / 32;
+      while (rows != 0u) {
+        const int rr = __ffs(rows) - 1;
+        rows &= rows - 1u;
+        if (tile * 16 + rr >= num_rows) continue;  // the zero-filled tail of the last tile
+        const T* src = raw + (tile * 16 + rr) * (int64_t)D + lane * E;
+        float x[E];
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          x[i] = to_f32(src[i]);
+          m = fmaxf(m, fabsf(x[i]));
+        }
+        m = warp_max(m);
+        int ex = 0;
+        if (m > 0.f && m <= 3.402823466e38f) frexpf(m, &ex);
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          x[i] = scale_pow2(x[i], -ex);
+          ss = fmaf(x[i], x[i], ss);
+        }
+        ss = warp_sum(ss);
+        const bool bad = !(ss <= 3.402823466e38f);
+#pragma unroll
+        for (int i = 0; i < E; ++i) x[i] *= __ldg(a.signs + lane * E + i);
+        fwht_warp<E>(x);
+        const float inv = (bad || !(ss > 0.f)) ? 0.f : 1.0f / sqrtf((float)D * ss);
+        const float nu = bad ? ss : scale_pow2(sqrtf(ss), ex);
+        unsigned char* prow = pack_buf + rr * RB;
+        for (int w = lane; w < IB / 4; w += 32) reinterpret_cast<uint32_t*>(prow)[w] = 0u;
+        __syncwarp();
+        float rsq = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const float u = bad ? 0.f : x[i] * inv;
+          int idx = 0;
+          for (int k = 0; k < NC - 1; ++k) idx += u > bnd[k] ? 1 : 0;
+          const int j = lane * E + i;
+          const int bit = j * BITS, wi = bit >> 5, o = bit & 31;
+          atomicOr(reinterpret_cast<uint32_t*>(prow) + wi, (uint32_t)idx << o);
+          if (o + BITS > 32) atomicOr(reinterpret_cast<uint32_t*>(prow) + wi + 1, (uint32_t)idx >> (32 - o));
+          if constexpr (PROD) {
+            const float rv = u - ctab[idx * 32 + lane];
+            rsq = fmaf(rv, rv, rsq);
+            const float xx = rv * 1024.0f;
+            const __half hi = __float2half_rn(xx);
+            const __half lo = __float2half_rn((xx - __half2float(hi)) * 4096.0f);
+            const int arow = 16 * warp + rr;
+            const int off = (arow >> 3) * kSbo + (j >> 3) * 128 + (arow & 7) * 16 + (j & 7) * 2;
+            *reinterpret_cast<__half*>(a_hi + off) = hi;
+            *reinterpret_cast<__half*>(a_lo + off) = lo;
+          }
+        }
+        if constexpr (PROD) {
+          const float gamma = sqrtf(warp_sum(rsq));
+          if (lane == 0) {
+            *reinterpret_cast<float*>(prow + IB + D / 8) = nu;
+            *reinterpret_cast<float*>(prow + IB + D / 8 + 4) = gamma;
+          }
+        } else {
+          if (lane == 0) *reinterpret_cast<float*>(prow + IB) = nu;
+        }
+        __syncwarp();
+      }
+    };
     // slot of the tile's token `lane` for the slab store below (a global load, read early)
     int64_t my_slot = -1;
     if (16 % H == 0 && lane < 16 / H) {
@@ -540,52 +617,13 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
     };
     float ss0, ss1;
     row_sums(ss0, ss1);
-    // One vote keeps two rare cases off the common path.  A row whose sum of squares leaves
-    // [2^-100, 2^100] (coordinates beyond about 1e14 or below about 1e-16: bf16 and fp32 rows
-    // can) is brought back by an exact power of two 2^-ex taken from its largest |y|; u is
-    // scale free, and the norm is scaled back by 2^ex.  A row whose sum stays non-finite (a
-    // NaN or infinite input) is quantised as a zero row: its coordinates and its row scale
-    // are set to 0, so every grid coordinate is a valid cell, and it keeps the non-finite sum
-    // as its norm, as sqrt would give.
-    int ex0 = 0, ex1 = 0;
-    bool bad0 = false, bad1 = false;
-    const bool odd0 = !(ss0 >= 0x1p-100f && ss0 <= 0x1p100f), odd1 = !(ss1 >= 0x1p-100f && ss1 <= 0x1p100f);
-    const bool any_odd = __any_sync(kFullMask, odd0 || odd1);
-    if (any_odd) {
-      float m0 = 0.f, m1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < NB; ++j)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          m0 = fmaxf(m0, fmaxf(fabsf(acc[j][nt][0]), fabsf(acc[j][nt][1])));
-          m1 = fmaxf(m1, fmaxf(fabsf(acc[j][nt][2]), fabsf(acc[j][nt][3])));
-        }
-      m0 = fmaxf(m0, __shfl_xor_sync(kFullMask, m0, 1));
-      m0 = fmaxf(m0, __shfl_xor_sync(kFullMask, m0, 2));
-      m1 = fmaxf(m1, __shfl_xor_sync(kFullMask, m1, 1));
-      m1 = fmaxf(m1, __shfl_xor_sync(kFullMask, m1, 2));
-      if (odd0 && m0 > 0.f && m0 <= 3.402823466e38f) frexpf(m0, &ex0);  // zero and infinite rows: none
-      if (odd1 && m1 > 0.f && m1 <= 3.402823466e38f) frexpf(m1, &ex1);
-#pragma unroll
-      for (int j = 0; j < NB; ++j)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          acc[j][nt][0] = scale_pow2(acc[j][nt][0], -ex0);
-          acc[j][nt][1] = scale_pow2(acc[j][nt][1], -ex0);
-          acc[j][nt][2] = scale_pow2(acc[j][nt][2], -ex1);
-          acc[j][nt][3] = scale_pow2(acc[j][nt][3], -ex1);
-        }
-      row_sums(ss0, ss1);
-      bad0 = !(ss0 <= 3.402823466e38f);
-      bad1 = !(ss1 <= 3.402823466e38f);
-#pragma unroll
-      for (int j = 0; j < NB; ++j)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          if (bad0) acc[j][nt][0] = acc[j][nt][1] = 0.f;
-          if (bad1) acc[j][nt][2] = acc[j][nt][3] = 0.f;
-        }
-    }
+    // Rows whose sum of squares leaves [2^-100, 2^100] -- rows of extreme scale (bf16 and fp32
+    // coordinates beyond about 1e14 or below about 1e-16), zero rows, and rows with a NaN or
+    // infinite coordinate -- are encoded here as zero rows (coordinates and row scale 0, so
+    // every grid coordinate is a valid cell) and re-encoded after packing by the warp from
+    // their raw values (`odd_rows`, below), away from this common path.
+    const bool odd0 = !(ss0 <= 0x1p100f) || ss0 < 0x1p-100f;  // (zero rows too: their sum may have underflowed)
+    const bool odd1 = !(ss1 <= 0x1p100f) || ss1 < 0x1p-100f;
     // ||x|| = sqrt(ss / D); u = y / sqrt(ss); grid coordinate g = u * q_a + q_b.
     // Every partial sum above only grows, so y^2 <= ss (1 + 2^-23) + 2^-150 for each y of
     // the row, even when ss is subnormal; adding 2^-149 under the root keeps |u| within a
@@ -593,14 +631,21 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
     // ulp, and only below 2^-124; an all-zero row gets g = q_b, i.e. u = 0).  rsqrtf (2 ulp)
     // is enough: it moves g by < 1e-4 cell and u by < 1e-6, inside the decision tolerance,
     // and the stored norm ss * rsqrt(ss) / sqrt(D) by < 1e-6 relative.
-    float rs0 = rsqrtf(ss0 + 0x1p-149f), rs1 = rsqrtf(ss1 + 0x1p-149f);
+    const float rs0 = odd0 ? 0.f : rsqrtf(ss0 + 0x1p-149f), rs1 = odd1 ? 0.f : rsqrtf(ss1 + 0x1p-149f);
     const float inv_sqrt_d = 1.0f / sqrtf((float)D);
-    float nu0 = ss0 * rs0 * inv_sqrt_d, nu1 = ss1 * rs1 * inv_sqrt_d;
-    if (any_odd) {  // (the same rare tiles) norms scaled back; non-finite rows: u = 0, norm as summed
-      nu0 = bad0 ? ss0 : scale_pow2(nu0, ex0);
-      nu1 = bad1 ? ss1 : scale_pow2(nu1, ex1);
-      if (bad0) rs0 = 0.f;
-      if (bad1) rs1 = 0.f;
+    const float nu0 = ss0 * rs0 * inv_sqrt_d, nu1 = ss1 * rs1 * inv_sqrt_d;
+    // bit rr: row rr of the tile needs the re-encode (each quad votes for its rows r, r + 8)
+    const uint32_t odd_b0 = __ballot_sync(kFullMask, odd0), odd_b1 = __ballot_sync(kFullMask, odd1);
+    if (__builtin_expect((odd_b0 | odd_b1) != 0u, 0)) {
+      // the flagged rows' coordinates may be NaN or infinite: zero them, so that with the row
+      // scale 0 their grid coordinate is q_b exactly (a valid cell) and their residual finite
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          if (odd0) acc[j][nt][0] = acc[j][nt][1] = 0.f;
+          if (odd1) acc[j][nt][2] = acc[j][nt][3] = 0.f;
+        }
     }
     const float ga0 = q_a * rs0, ga1 = q_a * rs1;
 
@@ -716,6 +761,13 @@ __global__ void __launch_bounds__(kWWarps * 32, write_tc_ctas_per_sm<T, D, PROD>
       __syncwarp();
     }
 
+      // ---- re-encode of the rows flagged above, one row at a time by the whole warp -------
+      if (__builtin_expect((odd_b0 | odd_b1) != 0u, 0)) {
+        uint32_t odd_rows = 0u;  // bit rr: row rr of the tile
+#pragma unroll
+        for (int q = 0; q < 8; ++q) odd_rows |= ((odd_b0 >> (4 * q)) & 1u) << q | ((odd_b1 >> (4 * q)) & 1u) << (q + 8);
+        reencode_rows(odd_rows);
+      }
     }  // active
 
     if constexpr (PROD) {
