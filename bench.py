@@ -698,7 +698,9 @@ def qjl_measure(tq, w, dev, kraw, slots, slots_np, vp, bt, lens, q, signs, cv, f
             "write_frac_of_hbm": wr_gbs / peak, "sketch_tflops": rows * 2.0 * d * d / wr_s / 1e12,
             "decode_us": dec_s * 1e6, "decode_gbs": dec_gbs, "decode_frac_of_hbm": dec_gbs / peak,
             "algorithmic_bytes": {"write": wr_bytes, "decode": dec_bytes}, "peak": peak, "peak_source": peak_kind,
-            "kernels": "SIMT (write_prod_kernel; qjl_project_kernel + decode_prod_split_kernel + combine)",
+            "kernels": ("write_tc_kernel<fp16, 128, 3, PROD> (mma.sync rotation, tcgen05 sketch S r); "
+                        "qjl_project_kernel (p = S q~) + decode_tc_kernel<128, 3, 4, 4, 2, PROD> "
+                        "(mma.sync, sketch term as a second MMA) + combine_tc_kernel"),
             "gpu_launches": tq.tq_launch_count() - launches0}
 
 

@@ -729,11 +729,14 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_tc_kernel(TcArgs args) {
     }
     build_frags(qr, bq);
     if constexpr (PROD) {  // p = S q~ of the same heads, into the sketch fragments
+      // p is written by the projection grid this one may depend on programmatically: wait
+      // for it (immediate once it has completed, or without such a launch), plain loads
+      asm volatile("griddepcontrol.wait;\n" ::: "memory");
       const float* pb = args.p_all + base;
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int i = 0; i < E; ++i) qr[g][i] = __ldg(pb + g * D + i);
+        for (int i = 0; i < E; ++i) qr[g][i] = pb[g * D + i];
       build_frags(qr, pq);
     }
   };
@@ -1471,8 +1474,25 @@ cudaError_t launch_tc_typed(const DecodeArgs& a, const DecodePlan& p, cudaStream
   auto kern = decode_tc_kernel<D, KB, VB, G, WPH, PROD>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<p.num_splits, 32 * (H + 1), smem, stream>>>(t);
-  err = cudaGetLastError();
+  if constexpr (PROD) {
+    // a programmatic dependent of the projection p = S q~ (the previous launch on the
+    // stream): the block-table scan and the first page copies overlap its tail; the
+    // consumer warps wait for it before they read p
+    cudaLaunchConfig_t kcfg{};
+    kcfg.gridDim = dim3(p.num_splits);
+    kcfg.blockDim = dim3(32 * (H + 1));
+    kcfg.dynamicSmemBytes = smem;
+    kcfg.stream = stream;
+    cudaLaunchAttribute kattr[1];
+    kattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    kattr[0].val.programmaticStreamSerializationAllowed = 1;
+    kcfg.attrs = kattr;
+    kcfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&kcfg, kern, t);
+  } else {
+    kern<<<p.num_splits, 32 * (H + 1), smem, stream>>>(t);
+    err = cudaGetLastError();
+  }
   if (err != cudaSuccess) return err;
   count_launches(1);
   const int rows = B * Hq;

@@ -132,45 +132,73 @@ write_prod_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads,
 // softmax scale and log2(e) -- the decode's own rotated query.  A CTA of 8 warps takes
 // kProjRows rows per warp: S^T is staged in shared memory once (padded to D + 1 columns, so
 // the staging stores and the reads of column i by lane i are conflict free), each query row
-// goes through the warp FWHT, and lane l accumulates outputs l + 32 e over j.
-constexpr int kProjRows = 4;
+// goes through the warp FWHT, and lane l accumulates outputs l + 32 e of the warp's rows
+// together over j (one shared load of S^T serves every row; the sum over j runs in order).
+// The product-key split kernel is launched as a programmatic dependent of this grid and
+// reads p only after waiting for it.
+constexpr int kProjRows = 2;
 template <int E>
 __global__ void __launch_bounds__(256)
 qjl_project_kernel(DecodeArgs a, const float* __restrict__ smat, float* __restrict__ p_out) {
   constexpr int D = 32 * E;
   extern __shared__ float s_t[];  // S^T, padded: s_t[j * (D + 1) + i] = S[i][j]
-  __shared__ float qs[8][D];
+  __shared__ __align__(16) float qs[8][kProjRows][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int k = threadIdx.x; k < D * D; k += blockDim.x) {
     const int i = k / D, j = k - i * D;
     s_t[j * (D + 1) + i] = __ldg(smat + k);
   }
   __syncthreads();
+  // the dependent split grid may be scheduled now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int64_t rows = (int64_t)a.batch * a.num_q_heads;
+  const int64_t row0 = ((int64_t)blockIdx.x * 8 + warp) * kProjRows;
+  if (row0 >= rows) return;
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kProdLog2e / sqrtf((float)D);
-  for (int k = 0; k < kProjRows; ++k) {
-    const int64_t row = ((int64_t)blockIdx.x * 8 + warp) * kProjRows + k;
-    if (row >= rows) break;
+#pragma unroll
+  for (int r = 0; r < kProjRows; ++r) {
     float qr[E];
+    if (row0 + r < rows) {
 #pragma unroll
-    for (int i = 0; i < E; ++i) qr[i] = load_as_f32(a.q, row * D + lane * E + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
-    fwht_warp<E>(qr);
+      for (int i = 0; i < E; ++i)
+        qr[i] = load_as_f32(a.q, (row0 + r) * D + lane * E + i, a.q_dtype) * __ldg(a.signs + lane * E + i);
+      fwht_warp<E>(qr);
+    } else {
 #pragma unroll
-    for (int i = 0; i < E; ++i) qs[warp][lane * E + i] = qr[i] * qmul;
-    __syncwarp();
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int j = 0; j < D; ++j) {
-      const float qj = qs[warp][j];
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(s_t[j * (D + 1) + lane + 32 * e], qj, acc[e]);
+      for (int i = 0; i < E; ++i) qr[i] = 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) p_out[row * D + lane + 32 * e] = acc[e];
-    __syncwarp();
+    for (int i = 0; i < E; ++i) qs[warp][r][lane * E + i] = qr[i] * qmul;
   }
+  __syncwarp();
+  float acc[kProjRows][E];
+#pragma unroll
+  for (int r = 0; r < kProjRows; ++r)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
+#pragma unroll 2
+  for (int j = 0; j < D; j += 4) {
+    float4 q4[kProjRows];
+#pragma unroll
+    for (int r = 0; r < kProjRows; ++r) q4[r] = *reinterpret_cast<const float4*>(&qs[warp][r][j]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float sv = s_t[(j + u) * (D + 1) + lane + 32 * e];
+#pragma unroll
+        for (int r = 0; r < kProjRows; ++r) {
+          const float qj = u == 0 ? q4[r].x : u == 1 ? q4[r].y : u == 2 ? q4[r].z : q4[r].w;
+          acc[r][e] = fmaf(sv, qj, acc[r][e]);
+        }
+      }
+  }
+#pragma unroll
+  for (int r = 0; r < kProjRows; ++r)
+    if (row0 + r < rows)
+#pragma unroll
+      for (int e = 0; e < E; ++e) p_out[(row0 + r) * D + lane + 32 * e] = acc[r][e];
 }
 
 // Enqueues the projection of every (sequence, q head) of `a` into p_out [rows][D].
