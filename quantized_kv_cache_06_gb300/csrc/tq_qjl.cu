@@ -144,7 +144,8 @@ qjl_project_kernel(DecodeArgs a, const float* __restrict__ smat, float* __restri
   extern __shared__ float s_t[];  // S^T, padded: s_t[j * (D + 1) + i] = S[i][j]
   __shared__ __align__(16) float qs[8][kProjRows][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int k = threadIdx.x; k < D * D; k += blockDim.x) {
+#pragma unroll 16
+  for (int k = threadIdx.x; k < D * D; k += blockDim.x) {  // 16 loads in flight per thread
     const int i = k / D, j = k - i * D;
     s_t[j * (D + 1) + i] = __ldg(smat + k);
   }

@@ -19,10 +19,11 @@
 // by K and V, which both use recipe rows.
 //
 // Kernels:
-//   write_recipe_kernel        one warp per (token, head, group): channel gather, norm,
-//                              rotation (warp FWHT), indices, residual, and the sketch
-//                              signs from S_d^T staged in shared memory (output i = lane
-//                              + 32 e, so one ballot per e is sign word e).
+//   write_recipe_kernel        a warp per four (token, head, group) units: channel gather,
+//                              norm, rotation (warp FWHT), indices and residual of each, then
+//                              the sketch signs of the four from S_d^T staged in shared
+//                              memory (output i = lane + 32 e, so one ballot per e is sign
+//                              word e).
 //   recipe_project_kernel      one warp per (sequence, q head): per group the rotated
 //                              gathered query q_g = R_d q[order_g] (times the softmax scale
 //                              and log2 e) and its projection p_g = S_d q_g.
@@ -58,23 +59,31 @@ constexpr float kRecSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi / 2)
 // nu, gamma.
 __host__ __device__ constexpr int group_words(int d, int bits) { return d * (bits - 1) / 32 + d / 32 + 2; }
 
+// Units (row, group) are taken four at a time per warp (two rows, both groups): each unit's
+// gather, norm, rotation, indices and residual first, then the sketch of all four residuals
+// together -- every shared load of S_d^T serves the four, with each sum over j in order.
+constexpr int kRecUnits = 4;
 template <typename T, int E>
-__global__ void __launch_bounds__(kRecWarps * 32)
+__global__ void __launch_bounds__(kRecWarps * 32, 4)
 write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads, const int64_t* __restrict__ slots,
                     uint8_t* __restrict__ pages, RecipeArgs rc, const float* __restrict__ signs,
                     const int32_t* __restrict__ status) {
   constexpr int d = 32 * E, D = 2 * d;
+  constexpr int kUnitWords = 3 * E + E + 2;  // largest group: 3-bit indices, signs, nu, gamma
   extern __shared__ float s_t[];  // S_d^T, padded: s_t[j * (d + 1) + i] = S[i][j]
   __shared__ float bnd[2][8], cen[2][8];
-  __shared__ float rbuf[kRecWarps][d];
-  __shared__ uint32_t rowbuf[kRecWarps][3 * E + E + 2];
+  __shared__ __align__(16) float rbuf[kRecWarps][d][kRecUnits];  // residual coordinate j of each unit
+  __shared__ uint32_t rowbuf[kRecWarps][kRecUnits][kUnitWords];
 
   const int tid = threadIdx.x;
   const int mb0 = rc.bits_hi - 1, mb1 = rc.bits_lo - 1;
   const int nc0 = 1 << mb0, nc1 = 1 << mb1;
-  if (tid < nc0 - 1) bnd[0][tid] = 0.5f * (rc.mse_hi[tid] + rc.mse_hi[tid + 1]);
+  // decision points, padded with +inf to 7 (so a 3-step search counts them for any width)
+  if (tid < 8) {
+    bnd[0][tid] = tid < nc0 - 1 ? 0.5f * (rc.mse_hi[tid] + rc.mse_hi[tid + 1]) : INFINITY;
+    bnd[1][tid] = tid < nc1 - 1 ? 0.5f * (rc.mse_lo[tid] + rc.mse_lo[tid + 1]) : INFINITY;
+  }
   if (tid < nc0) cen[0][tid] = rc.mse_hi[tid];
-  if (tid < nc1 - 1) bnd[1][tid] = 0.5f * (rc.mse_lo[tid] + rc.mse_lo[tid + 1]);
   if (tid < nc1) cen[1][tid] = rc.mse_lo[tid];
   for (int k = tid; k < d * d; k += blockDim.x) {  // coalesced reads, conflict-free stores
     const int i = k / d, j = k - i * d;
@@ -89,70 +98,139 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_head
   float sg[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) sg[i] = __ldg(signs + lane * E + i);
-  uint32_t* buf = rowbuf[warp];
-  float* res = rbuf[warp];
+  float(*res)[kRecUnits] = rbuf[warp];
 
   const int64_t units = 2 * num_rows;
-  for (int64_t u = (int64_t)blockIdx.x * kRecWarps + warp; u < units; u += (int64_t)gridDim.x * kRecWarps) {
-    const int64_t r = u >> 1;
-    const int g = (int)(u & 1);
-    const int64_t t = r / num_kv_heads;
-    const int h = (int)(r - t * num_kv_heads);
-    const int64_t slot = __ldg(slots + t);
-    if (slot < 0) continue;  // "Slot Mapping": negative slots are ignored
-    const int mb = g ? mb1 : mb0, nc = g ? nc1 : nc0;
+  const int64_t ustride = (int64_t)gridDim.x * kRecWarps * kRecUnits;
+  for (int64_t u0 = ((int64_t)blockIdx.x * kRecWarps + warp) * kRecUnits; u0 < units; u0 += ustride) {
+    int64_t slot_k[kRecUnits];
+    float nu_k[kRecUnits], gamma_k[kRecUnits];
+    // the four units' slots, channel indices and gathered values first (all loads in flight
+    // together), then their norms and rotations side by side
+    float v[kRecUnits][E];
+    // units u0 .. u0 + 3: rows r0 and r0 + 1 (both groups each); one division for both
+    const int64_t r0 = u0 >> 1;
+    const int64_t t0 = r0 / num_kv_heads;
+    const int h0 = (int)(r0 - t0 * num_kv_heads);
+    const bool wrap = h0 + 1 == num_kv_heads;
+    const int64_t t1 = wrap ? t0 + 1 : t0;
+    const int h1 = wrap ? 0 : h0 + 1;
+#pragma unroll
+    for (int k = 0; k < kRecUnits; ++k) {
+      const int64_t u = u0 + k;
+      const int64_t r = r0 + (k >> 1);
+      const int g = k & 1;
+      const int64_t t = (k >> 1) ? t1 : t0;
+      const int h = (k >> 1) ? h1 : h0;
+      slot_k[k] = u < units ? __ldg(slots + t) : -1;
+      const int32_t* ord = rc.order + (int64_t)h * D + g * d + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i) v[k][i] = u < units ? to_f32<T>(raw[r * D + __ldg(ord + i)]) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kRecUnits; ++k) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < E; ++i) ss = fmaf(v[k][i], v[k][i], ss);
+      nu_k[k] = ss;
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+      for (int k = 0; k < kRecUnits; ++k) nu_k[k] += __shfl_xor_sync(kFullMask, nu_k[k], m);
+#pragma unroll
+    for (int k = 0; k < kRecUnits; ++k) {
+      nu_k[k] = sqrtf(nu_k[k]);
+#pragma unroll
+      for (int i = 0; i < E; ++i) v[k][i] *= sg[i];
+      fwht_warp<E>(v[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < kRecUnits; ++k) {
+      const int g = k & 1;
+      uint32_t* buf = rowbuf[warp][k];
+      gamma_k[k] = 0.f;
+      if (slot_k[k] < 0) {  // "Slot Mapping": negative slots are ignored (zero residual)
+#pragma unroll
+        for (int i = 0; i < E; ++i) res[lane * E + i][k] = 0.f;
+        continue;
+      }
+      const int mb = g ? mb1 : mb0;
+      const float nu = nu_k[k];
+      const float inv = nu > 0.f ? inv_sqrt_d / nu : 0.f;  // y = H(s*x)/(sqrt(d) nu)
 
-    float v[E];
-    const int32_t* ord = rc.order + (int64_t)h * D + g * d + lane * E;
+      const int index_words = d * mb / 32;
+      const int gw = index_words + E + 2;
+      for (int w = lane; w < gw; w += 32) buf[w] = 0u;
+      __syncwarp();
+      float rs = 0.f;
 #pragma unroll
-    for (int i = 0; i < E; ++i) v[i] = to_f32<T>(raw[r * D + __ldg(ord + i)]);
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < E; ++i) ss = fmaf(v[i], v[i], ss);
-    const float nu = sqrtf(warp_sum(ss));
-#pragma unroll
-    for (int i = 0; i < E; ++i) v[i] *= sg[i];
-    fwht_warp<E>(v);
-    const float inv = nu > 0.f ? inv_sqrt_d / nu : 0.f;  // y = H(s*x)/(sqrt(d) nu)
-
-    const int index_words = d * mb / 32;
-    const int gw = index_words + E + 2;
-    for (int w = lane; w < gw; w += 32) buf[w] = 0u;
-    __syncwarp();
-    float rs = 0.f;
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-      const float y = v[i] * inv;
-      int idx = 0;  // #{k : boundary_k < y}
-      for (int s = nc >> 1; s > 0; s >>= 1)
-        if (y > bnd[g][idx + s - 1]) idx += s;
-      const int bit = (lane * E + i) * mb;
-      const int w = bit >> 5, o = bit & 31;
-      atomicOr(&buf[w], (uint32_t)idx << o);
-      if (o + mb > 32) atomicOr(&buf[w + 1], (uint32_t)idx >> (32 - o));
-      const float dr = y - cen[g][idx];
-      res[lane * E + i] = dr;
-      rs = fmaf(dr, dr, rs);
+      for (int i = 0; i < E; ++i) {
+        const float y = v[k][i] * inv;
+        // idx = #{k : boundary_k < y}: three steps over the 7 (padded) decision points
+        int idx = y > bnd[g][3] ? 4 : 0;
+        idx += y > bnd[g][idx + 1] ? 2 : 0;
+        idx += y > bnd[g][idx] ? 1 : 0;
+        const int bit = (lane * E + i) * mb;
+        const int w = bit >> 5, o = bit & 31;
+        atomicOr(&buf[w], (uint32_t)idx << o);
+        if (o + mb > 32) atomicOr(&buf[w + 1], (uint32_t)idx >> (32 - o));
+        const float dr = y - cen[g][idx];
+        res[lane * E + i][k] = dr;
+        rs = fmaf(dr, dr, rs);
+      }
+      gamma_k[k] = rs;
     }
-    const float gamma = sqrtf(warp_sum(rs));
-    __syncwarp();
-    // sign word e: bit `lane` is [(S r)_(lane + 32 e) >= 0]
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int i = lane + 32 * e;
-      float acc = 0.f;
-      for (int j = 0; j < d; ++j) acc = fmaf(s_t[j * (d + 1) + i], res[j], acc);
-      const uint32_t mask = __ballot_sync(kFullMask, acc >= 0.f);
-      if (lane == 0) buf[index_words + e] = mask;
-    }
-    if (lane == 0) {
-      buf[index_words + E] = __float_as_uint(nu);
-      buf[index_words + E + 1] = __float_as_uint(gamma);
-    }
+    for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+      for (int k = 0; k < kRecUnits; ++k) gamma_k[k] += __shfl_xor_sync(kFullMask, gamma_k[k], m);
+#pragma unroll
+    for (int k = 0; k < kRecUnits; ++k) gamma_k[k] = sqrtf(gamma_k[k]);
     __syncwarp();
-    uint32_t* dst = reinterpret_cast<uint32_t*>(pages + (slot * num_kv_heads + h) * (int64_t)(row_words * 4)) +
-                    (g ? group_words(d, rc.bits_hi) : 0);
-    for (int w = lane; w < gw; w += 32) dst[w] = buf[w];
+    // (S r_k)_(lane + 32 e) for the four units; one load of S_d^T and one of the four
+    // residual coordinates j per step
+    float acc[kRecUnits][E];
+#pragma unroll
+    for (int k = 0; k < kRecUnits; ++k)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < d; ++j) {
+      const float4 r4 = *reinterpret_cast<const float4*>(res[j]);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float sv = s_t[j * (d + 1) + lane + 32 * e];
+        acc[0][e] = fmaf(sv, r4.x, acc[0][e]);
+        acc[1][e] = fmaf(sv, r4.y, acc[1][e]);
+        acc[2][e] = fmaf(sv, r4.z, acc[2][e]);
+        acc[3][e] = fmaf(sv, r4.w, acc[3][e]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRecUnits; ++k) {
+      if (slot_k[k] < 0) continue;  // (uniform across the warp)
+      const int g = k & 1;
+      const int h = (k >> 1) ? h1 : h0;
+      const int mb = g ? mb1 : mb0;
+      const int index_words = d * mb / 32;
+      const int gw = index_words + E + 2;
+      uint32_t* buf = rowbuf[warp][k];
+      // sign word e: bit `lane` is [(S r)_(lane + 32 e) >= 0]
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const uint32_t mask = __ballot_sync(kFullMask, acc[k][e] >= 0.f);
+        if (lane == 0) buf[index_words + e] = mask;
+      }
+      if (lane == 0) {
+        buf[index_words + E] = __float_as_uint(nu_k[k]);
+        buf[index_words + E + 1] = __float_as_uint(gamma_k[k]);
+      }
+      __syncwarp();
+      uint32_t* dst = reinterpret_cast<uint32_t*>(pages + (slot_k[k] * num_kv_heads + h) * (int64_t)(row_words * 4)) +
+                      (g ? group_words(d, rc.bits_hi) : 0);
+      for (int w = lane; w < gw; w += 32) dst[w] = buf[w];
+    }
     __syncwarp();
   }
 }
@@ -445,7 +523,8 @@ template <typename T, int E>
 cudaError_t launch_write_recipe_typed(const WriteArgs& a, const RecipeArgs& rc, cudaStream_t stream, int num_sms) {
   constexpr int d = 32 * E;
   const int64_t units = 2 * a.num_tokens * a.num_kv_heads;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((units + kRecWarps - 1) / kRecWarps, (int64_t)num_sms * 4));
+  const int64_t per_cta = (int64_t)kRecWarps * kRecUnits;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((units + per_cta - 1) / per_cta, (int64_t)num_sms * 4));
   const size_t smem = (size_t)d * (d + 1) * sizeof(float);
   auto kern = write_recipe_kernel<T, E>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
