@@ -27,7 +27,10 @@
 //   recipe_project_kernel      one warp per (sequence, q head): per group the rotated
 //                              gathered query q_g = R_d q[order_g] (times the softmax scale
 //                              and log2 e) and its projection p_g = S_d q_g.
-//   decode_recipe_split_kernel the SIMT split decode.  Score of key row k:
+//   decode_recipe_split_kernel the SIMT split decode, 32-token tiles per warp: scores with
+//                              a lane per token (every q head at once), one softmax step
+//                              per tile, values with lanes over coordinates.  Score of key
+//                              row k:
 //                                sum_g nu_g (<q_g, c_g[idx]> + gamma_g kappa <p_g, 2z - 1>),
 //                              kappa = sqrt(pi / 2) / d.  The value reconstruction
 //                              nu R_d^T (c[idx] + gamma kappa S_d^T (2z - 1)) is linear, so
@@ -305,43 +308,88 @@ __device__ __forceinline__ GroupView<E> read_group(const uint32_t* __restrict__ 
   return v;
 }
 
-template <int E, int G>
+// Score of one key group for every q head of the kv head, by one lane for its own token:
+// sc[g] += nu (sum_j q_g[j] c[idx_j] + gamma kappa sum_j p_g[j] (2 z_j - 1)), with
+// sum_j p_g[j] (2 z_j - 1) = 2 sum_j z_j p_g[j] - sum_j p_g[j].  q and p come from shared
+// memory ([coordinate][head], the same address on every lane).
+template <int E, int G, int MB>
+__device__ __forceinline__ void recipe_group_score(const uint32_t* __restrict__ gw, const float (*qs)[G],
+                                                   const float (*ps)[G], const float* cent, const float* psum,
+                                                   float kappa, float (&sc)[G]) {
+  constexpr int d = 32 * E, IW = d * MB / 32;
+  uint32_t w[IW + E + 2];
+#pragma unroll
+  for (int k = 0; k < IW + E + 2; ++k) w[k] = __ldg(gw + k);
+  float sm[G], sz[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) sm[g] = sz[g] = 0.f;
+#pragma unroll
+  for (int j = 0; j < d; ++j) {
+    const int bit = j * MB, wi = bit >> 5, o = bit & 31;
+    uint32_t f = w[wi] >> o;
+    if (o + MB > 32) f |= w[wi + 1] << (32 - o);
+    const float c = cent[f & ((1u << MB) - 1u)];
+    const float z = (float)((w[IW + (j >> 5)] >> (j & 31)) & 1u);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      sm[g] = fmaf(qs[j][g], c, sm[g]);
+      sz[g] = fmaf(ps[j][g], z, sz[g]);
+    }
+  }
+  const float nu = __uint_as_float(w[IW + E]), gk = __uint_as_float(w[IW + E + 1]) * kappa;
+#pragma unroll
+  for (int g = 0; g < G; ++g) sc[g] = fmaf(nu, fmaf(gk, fmaf(2.f, sz[g], -psum[g]), sm[g]), sc[g]);
+}
+
+// Tiles of 32 tokens per warp.  Scores: lane = token, every q head of the kv head at once
+// (no per-token reductions); the tile's softmax step (running max, correction, weights) once
+// per tile; values: lanes over coordinates, the tile's tokens accumulated with their weights
+// from shared memory.  MB0 / MB1: MSE index bits of the high / low group.
+template <int E, int G, int MB0, int MB1>
 __global__ void __launch_bounds__(kRecDecodeWarps * 32)
 decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p_all, int num_splits,
                            int blocks_per_split, RecipeSplitView part) {
   constexpr int d = 32 * E, D = 2 * d;
+  constexpr int kWh = d * MB0 / 32 + E + 2;  // words of the high group
+  constexpr int rbw = kWh + d * MB1 / 32 + E + 2;  // words of a row
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.num_kv_heads, bs = a.block_size;
-  const int mb[2] = {rc.bits_hi - 1, rc.bits_lo - 1};
-  const int w_hi = group_words(d, rc.bits_hi);
-  const int rb = 4 * (w_hi + group_words(d, rc.bits_lo));
 
   __shared__ float cent[2][8];
+  __shared__ __align__(16) float qs[2][d][G];  // rotated query, coordinate j of group grp, head g
+  __shared__ __align__(16) float ps[2][d][G];  // its projection p = S_d q, coordinate j
+  __shared__ float psum[2][G];                 // sum_j p[j]
+  __shared__ __align__(16) float pt[kRecDecodeWarps][32][G];  // the tile's weights (0: no token)
+  __shared__ int64_t trow[kRecDecodeWarps][32];               // the tile's page rows (-1: none)
   __shared__ float red_ml[kRecDecodeWarps][G][2];
   __shared__ float red_acc[kRecDecodeWarps][G][2 * D];
-  if (threadIdx.x < (1 << mb[0])) cent[0][threadIdx.x] = rc.mse_hi[threadIdx.x];
-  if (threadIdx.x < (1 << mb[1])) cent[1][threadIdx.x] = rc.mse_lo[threadIdx.x];
+  if (threadIdx.x < (1 << MB0)) cent[0][threadIdx.x] = rc.mse_hi[threadIdx.x];
+  if (threadIdx.x < (1 << MB1)) cent[1][threadIdx.x] = rc.mse_lo[threadIdx.x];
 
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kRecLog2e / sqrtf((float)d);
   const float kappa = kRecSqrtHalfPi / (float)d;
-  float qr[G][2][E], pp[G][2][E];  // rotated query (coordinates lane E + i), projection (lane + 32 e)
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
+  for (int g = warp; g < G; g += kRecDecodeWarps) {
     const int64_t qrow = (int64_t)b * a.num_q_heads + (int64_t)h * G + g;
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
+      float qr[E];
       const int32_t* ord = rc.order + (int64_t)h * D + grp * d + lane * E;
 #pragma unroll
       for (int i = 0; i < E; ++i)
-        qr[g][grp][i] = load_as_f32(a.q, qrow * D + __ldg(ord + i), a.q_dtype) * __ldg(a.signs + lane * E + i);
-      fwht_warp<E>(qr[g][grp]);
+        qr[i] = load_as_f32(a.q, qrow * D + __ldg(ord + i), a.q_dtype) * __ldg(a.signs + lane * E + i);
+      fwht_warp<E>(qr);
+      float ssum = 0.f;
 #pragma unroll
       for (int i = 0; i < E; ++i) {
-        qr[g][grp][i] *= qmul;
-        pp[g][grp][i] = __ldg(p_all + (qrow * 2 + grp) * d + lane + 32 * i);
+        qs[grp][lane * E + i][g] = qr[i] * qmul;
+        const float pv = __ldg(p_all + (qrow * 2 + grp) * d + lane + 32 * i);
+        ps[grp][lane + 32 * i][g] = pv;
+        ssum += pv;
       }
+      ssum = warp_sum(ssum);
+      if (lane == 0) psum[grp][g] = ssum;
     }
   }
 
@@ -367,57 +415,79 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
   __syncthreads();
 
   bool bad_block = false;
-  for (int t = t_lo + warp; t < t_hi; t += kRecDecodeWarps) {
-    const int bid = __ldg(a.block_table + (int64_t)b * a.max_blocks_per_seq + t / bs);
-    if (bid < 0 || (int64_t)bid >= a.num_blocks) {
-      bad_block = true;
-      continue;
+  for (int tb = t_lo + 32 * warp; tb < t_hi; tb += 32 * kRecDecodeWarps) {
+    // ---- scores: this lane's token ---------------------------------------------------
+    const int t = tb + lane;
+    int64_t row = -1;
+    if (t < t_hi) {
+      const int bid = __ldg(a.block_table + (int64_t)b * a.max_blocks_per_seq + t / bs);
+      if (bid < 0 || (int64_t)bid >= a.num_blocks) bad_block = true;
+      else row = ((int64_t)bid * bs + t % bs) * H + h;
     }
-    const int64_t row = ((int64_t)bid * bs + t % bs) * H + h;
-    const uint32_t* kr = reinterpret_cast<const uint32_t*>(a.k_pages + row * rb);
-    const uint32_t* vr = reinterpret_cast<const uint32_t*>(a.v_pages + row * rb);
-    float s[G];
+    float sc[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) s[g] = 0.f;
-    float vc[2][E], vz[2][E];  // this token's value terms: nu c[idx] and nu gamma kappa (2z - 1)
-#pragma unroll
-    for (int grp = 0; grp < 2; ++grp) {
-      const GroupView<E> k = read_group<E>(kr + (grp ? w_hi : 0), mb[grp], lane);
-      const GroupView<E> v = read_group<E>(vr + (grp ? w_hi : 0), mb[grp], lane);
-      const float kz = k.gamma * kappa;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float sm = 0.f, sz = 0.f;
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-          sm = fmaf(qr[g][grp][i], cent[grp][k.idx[i]], sm);
-          sz = fmaf(pp[g][grp][i], ((k.zw[i] >> lane) & 1u) ? 1.f : -1.f, sz);
-        }
-        s[g] = fmaf(k.nu, fmaf(kz, sz, sm), s[g]);
-      }
-      const float vzs = v.nu * v.gamma * kappa;
-#pragma unroll
-      for (int i = 0; i < E; ++i) {
-        vc[grp][i] = v.nu * cent[grp][v.idx[i]];
-        vz[grp][i] = ((v.zw[i] >> lane) & 1u) ? vzs : -vzs;
-      }
+    for (int g = 0; g < G; ++g) sc[g] = row >= 0 ? 0.f : -INFINITY;
+    if (row >= 0) {
+      const uint32_t* kr = reinterpret_cast<const uint32_t*>(a.k_pages) + row * rbw;
+      recipe_group_score<E, G, MB0>(kr, qs[0], ps[0], cent[0], psum[0], kappa, sc);
+      recipe_group_score<E, G, MB1>(kr + kWh, qs[1], ps[1], cent[1], psum[1], kappa, sc);
     }
+    trow[warp][lane] = row;
+    // ---- the tile's softmax step (m, l, the correction: the same on every lane) -----
+    float corr[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float sc = warp_sum(s[g]);
-      const float mn = fmaxf(m[g], sc);
-      const float corr = exp2f(m[g] - mn);
-      const float p = exp2f(sc - mn);
-      l[g] = l[g] * corr + p;
+      const float tmax = warp_max(sc[g]);
+      const float mn = fmaxf(m[g], tmax);
+      corr[g] = 1.f;
+      float p = 0.f;
+      if (mn != -INFINITY) {  // some token of this or an earlier tile
+        corr[g] = exp2f(m[g] - mn);  // 0 while m is -inf
+        p = exp2f(sc[g] - mn);       // 0 for a masked token
+      }
+      l[g] = fmaf(l[g], corr[g], warp_sum(p));
+      m[g] = mn;
+      pt[warp][lane][g] = p;
+    }
+    __syncwarp();
+    // ---- values: lanes over coordinates, the tile's tokens in order -----------------
+#pragma unroll
+    for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp)
 #pragma unroll
         for (int i = 0; i < E; ++i) {
-          acc_c[g][grp][i] = fmaf(p, vc[grp][i], acc_c[g][grp][i] * corr);
-          acc_z[g][grp][i] = fmaf(p, vz[grp][i], acc_z[g][grp][i] * corr);
+          acc_c[g][grp][i] *= corr[g];
+          acc_z[g][grp][i] *= corr[g];
         }
-      m[g] = mn;
+    const int nt = min(32, t_hi - tb);
+    for (int k = 0; k < nt; ++k) {
+      const int64_t vrow = trow[warp][k];
+      if (vrow < 0) continue;  // (the same on every lane)
+      const uint32_t* vr = reinterpret_cast<const uint32_t*>(a.v_pages) + vrow * rbw;
+      float pk[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) pk[g] = pt[warp][k][g];
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp) {
+        const GroupView<E> v = read_group<E>(vr + (grp ? kWh : 0), grp ? MB1 : MB0, lane);
+        const float vzs = v.nu * v.gamma * kappa;
+        float vc[E], vz[E];  // nu c[idx] and nu gamma kappa (2z - 1)
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          vc[i] = v.nu * cent[grp][v.idx[i]];
+          vz[i] = ((v.zw[i] >> lane) & 1u) ? vzs : -vzs;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int i = 0; i < E; ++i) {
+            acc_c[g][grp][i] = fmaf(pk[g], vc[i], acc_c[g][grp][i]);
+            acc_z[g][grp][i] = fmaf(pk[g], vz[i], acc_z[g][grp][i]);
+          }
+      }
     }
+    __syncwarp();  // the next tile rewrites pt / trow
   }
   if (__any_sync(kFullMask, bad_block) && lane == 0 && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
 
@@ -543,6 +613,19 @@ cudaError_t launch_write_recipe_dim(const WriteArgs& a, const RecipeArgs& rc, cu
   return cudaErrorInvalidValue;
 }
 
+template <int E, int MB0, int MB1>
+cudaError_t launch_recipe_split_g(int G, dim3 grid, cudaStream_t stream, const DecodeArgs& a, const RecipeArgs& rc,
+                                  const float* p_all, const DecodePlan& p, RecipeSplitView part) {
+  switch (G) {
+    case 1: decode_recipe_split_kernel<E, 1, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    case 2: decode_recipe_split_kernel<E, 2, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    case 4: decode_recipe_split_kernel<E, 4, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    case 8: decode_recipe_split_kernel<E, 8, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 template <int E>
 cudaError_t launch_decode_recipe_e(const DecodeArgs& a, const RecipeArgs& rc, const DecodePlan& p,
                                    cudaStream_t stream) {
@@ -559,13 +642,15 @@ cudaError_t launch_decode_recipe_e(const DecodeArgs& a, const RecipeArgs& rc, co
   count_launches(1);
   const int G = a.num_q_heads / a.num_kv_heads;
   dim3 grid(p.num_splits, a.num_kv_heads, a.batch);
-  switch (G) {
-    case 1: decode_recipe_split_kernel<E, 1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    case 2: decode_recipe_split_kernel<E, 2><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    case 4: decode_recipe_split_kernel<E, 4><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    case 8: decode_recipe_split_kernel<E, 8><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    default: return cudaErrorInvalidValue;
+  const int mb0 = rc.bits_hi - 1, mb1 = rc.bits_lo - 1;
+  if (mb0 == 2 && mb1 == 1) {  // turboquant25
+    err = launch_recipe_split_g<E, 2, 1>(G, grid, stream, a, rc, p_all, p, part);
+  } else if (mb0 == 3 && mb1 == 2) {  // turboquant35
+    err = launch_recipe_split_g<E, 3, 2>(G, grid, stream, a, rc, p_all, p, part);
+  } else {
+    return cudaErrorInvalidValue;
   }
+  if (err != cudaSuccess) return err;
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   count_launches(1);
