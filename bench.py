@@ -864,6 +864,16 @@ def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5, c
 
     one()
     torch.cuda.synchronize()
+    # the host link on its own, right before the steps: plain copies of the step's raw rows
+    # (the link is shared with whatever else uses this host's memory, so it is taken per run)
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(copy_stream)
+    for _ in range(2):
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+    l1.record(copy_stream)
+    torch.cuda.synchronize()
+    link_gbs = 2 * (hk.numel() * hk.element_size() + hv.numel() * hv.element_size()) / (l0.elapsed_time(l1) / 1e3) / 1e9
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(steps):
@@ -875,7 +885,8 @@ def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5, c
     h2d = sum(t_.numel() * t_.element_size() for t_ in (hk, hv, hs, hq, hbt, hl))
     return {"value": world * dbytes / sec / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": hout.numel() * hout.element_size(), "ms_per_step": sec * 1e3,
-            "h2d_chunks": chunks}
+            "h2d_chunks": chunks, "host_link_gbs": link_gbs,
+            "h2d_frac_of_link": h2d / sec / 1e9 / link_gbs}
 
 
 def main():
