@@ -312,6 +312,23 @@ __device__ __forceinline__ GroupView<E> read_group(const uint32_t* __restrict__ 
 // sc[g] += nu (sum_j q_g[j] c[idx_j] + gamma kappa sum_j p_g[j] (2 z_j - 1)), with
 // sum_j p_g[j] (2 z_j - 1) = 2 sum_j z_j p_g[j] - sum_j p_g[j].  q and p come from shared
 // memory ([coordinate][head], the same address on every lane).
+// read_group from a row staged in shared memory
+template <int E>
+__device__ __forceinline__ GroupView<E> read_group_s(const uint32_t* gw, int mb, int lane) {
+  constexpr int d = 32 * E;
+  GroupView<E> v;
+  const int bit0 = lane * E * mb;
+  const uint64_t win = (uint64_t)gw[bit0 >> 5] | ((uint64_t)gw[(bit0 >> 5) + 1] << 32);
+#pragma unroll
+  for (int i = 0; i < E; ++i) v.idx[i] = rfield(win, (bit0 & 31) + i * mb, mb);
+  const int iw = d * mb / 32;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v.zw[e] = gw[iw + e];
+  v.nu = __uint_as_float(gw[iw + E]);
+  v.gamma = __uint_as_float(gw[iw + E + 1]);
+  return v;
+}
+
 template <int E, int G, int MB>
 __device__ __forceinline__ void recipe_group_score(const uint32_t* __restrict__ gw, const float (*qs)[G],
                                                    const float (*ps)[G], const float* cent, const float* psum,
@@ -363,7 +380,13 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
   __shared__ __align__(16) float pt[kRecDecodeWarps][32][G];  // the tile's weights (0: no token)
   __shared__ int64_t trow[kRecDecodeWarps][32];               // the tile's page rows (-1: none)
   __shared__ float red_ml[kRecDecodeWarps][G][2];
-  __shared__ float red_acc[kRecDecodeWarps][G][2 * D];
+  // The tile's value rows (fetched by the lane of each token while it scores it; an odd row
+  // stride keeps those stores conflict free), sharing memory with the final merge's buffer.
+  constexpr int kVStride = (rbw % 2 == 0) ? rbw + 1 : rbw;
+  constexpr int kRedBytes = kRecDecodeWarps * G * 2 * D * 4, kVBytes = kRecDecodeWarps * 32 * kVStride * 4;
+  __shared__ __align__(16) unsigned char merge_u[kRedBytes > kVBytes ? kRedBytes : kVBytes];
+  float(*red_acc)[G][2 * D] = reinterpret_cast<float(*)[G][2 * D]>(merge_u);
+  uint32_t(*vbuf)[32][kVStride] = reinterpret_cast<uint32_t(*)[32][kVStride]>(merge_u);
   if (threadIdx.x < (1 << MB0)) cent[0][threadIdx.x] = rc.mse_hi[threadIdx.x];
   if (threadIdx.x < (1 << MB1)) cent[1][threadIdx.x] = rc.mse_lo[threadIdx.x];
 
@@ -428,9 +451,15 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
 #pragma unroll
     for (int g = 0; g < G; ++g) sc[g] = row >= 0 ? 0.f : -INFINITY;
     if (row >= 0) {
+      const uint32_t* vr = reinterpret_cast<const uint32_t*>(a.v_pages) + row * rbw;
+      uint32_t vw[rbw];  // this token's value row, in flight while the key row is scored
+#pragma unroll
+      for (int k = 0; k < rbw; ++k) vw[k] = __ldg(vr + k);
       const uint32_t* kr = reinterpret_cast<const uint32_t*>(a.k_pages) + row * rbw;
       recipe_group_score<E, G, MB0>(kr, qs[0], ps[0], cent[0], psum[0], kappa, sc);
       recipe_group_score<E, G, MB1>(kr + kWh, qs[1], ps[1], cent[1], psum[1], kappa, sc);
+#pragma unroll
+      for (int k = 0; k < rbw; ++k) vbuf[warp][lane][k] = vw[k];
     }
     trow[warp][lane] = row;
     // ---- the tile's softmax step (m, l, the correction: the same on every lane) -----
@@ -462,15 +491,14 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
         }
     const int nt = min(32, t_hi - tb);
     for (int k = 0; k < nt; ++k) {
-      const int64_t vrow = trow[warp][k];
-      if (vrow < 0) continue;  // (the same on every lane)
-      const uint32_t* vr = reinterpret_cast<const uint32_t*>(a.v_pages) + vrow * rbw;
+      if (trow[warp][k] < 0) continue;  // (the same on every lane)
+      const uint32_t* vr = vbuf[warp][k];
       float pk[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) pk[g] = pt[warp][k][g];
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
-        const GroupView<E> v = read_group<E>(vr + (grp ? kWh : 0), grp ? MB1 : MB0, lane);
+        const GroupView<E> v = read_group_s<E>(vr + (grp ? kWh : 0), grp ? MB1 : MB0, lane);
         const float vzs = v.nu * v.gamma * kappa;
         float vc[E], vz[E];  // nu c[idx] and nu gamma kappa (2z - 1)
 #pragma unroll
@@ -490,6 +518,7 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
     __syncwarp();  // the next tile rewrites pt / trow
   }
   if (__any_sync(kFullMask, bad_block) && lane == 0 && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+  __syncthreads();  // every warp is done with its value rows: the merge buffer may be written
 
   // merge the warps of this CTA, then write the split partial
 #pragma unroll
