@@ -19,11 +19,10 @@
 // by K and V, which both use recipe rows.
 //
 // Kernels:
-//   write_recipe_kernel        a warp per four (token, head, group) units: channel gather,
+//   write_recipe_kernel        a warp per sixteen (token, head, group) units: channel gather,
 //                              norm, rotation (warp FWHT), indices and residual of each, then
-//                              the sketch signs of the four from S_d^T staged in shared
-//                              memory (output i = lane + 32 e, so one ballot per e is sign
-//                              word e).
+//                              the sketch of the sixteen as m16n8k16 MMAs (fp16 hi / lo
+//                              splits of r and S_d) and the sign words from ballots.
 //   recipe_project_kernel      one warp per (sequence, q head): per group the rotated
 //                              gathered query q_g = R_d q[order_g] (times the softmax scale
 //                              and log2 e) and its projection p_g = S_d q_g.
@@ -62,21 +61,57 @@ constexpr float kRecSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi / 2)
 // nu, gamma.
 __host__ __device__ constexpr int group_words(int d, int bits) { return d * (bits - 1) / 32 + d / 32 + 2; }
 
-// Units (row, group) are taken four at a time per warp (two rows, both groups): each unit's
-// gather, norm, rotation, indices and residual first, then the sketch of all four residuals
-// together -- every shared load of S_d^T serves the four, with each sum over j in order.
-constexpr int kRecUnits = 4;
+// Units (row, group) are taken sixteen at a time per warp (eight rows, both groups), in
+// batches of four: each unit's gather, norm, rotation, indices and residual (the four units'
+// loads issued together, their reductions interleaved), the residual r stored into the warp's
+// A tile as fp16 hi = r 2^10 and lo = (r 2^10 - hi) 2^12.  Then the sketch S_d r of the
+// sixteen on the tensor cores (m16n8k16): r_hi S_hi into one accumulator, r_lo S_hi +
+// r_hi S_lo into another (~22 significant bits, as in an fp32 sum), and each sign word from
+// ballots of the accumulators, assembled by one lane.
+constexpr int kRecUnits = 16;
+constexpr int kRecBatch = 4;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void rec_mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void rec_ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+// bit c of a nibble to bit 2 c
+__device__ __forceinline__ uint32_t spread_nibble(uint32_t x) {
+  x = (x | (x << 2)) & 0x33u;
+  return (x | (x << 1)) & 0x55u;
+}
+
+// Shared memory of the writer: S hi and lo, then per warp its A tile hi and lo; rows of
+// d + 8 halves (16 bytes of padding put the 8 rows of an ldmatrix in different banks).
+__host__ __device__ constexpr int recipe_write_smem(int d) { return (2 * d + kRecWarps * 2 * kRecUnits) * (d + 8) * 2; }
+
 template <typename T, int E>
-__global__ void __launch_bounds__(kRecWarps * 32, 4)
+__global__ void __launch_bounds__(kRecWarps * 32, 3)
 write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads, const int64_t* __restrict__ slots,
                     uint8_t* __restrict__ pages, RecipeArgs rc, const float* __restrict__ signs,
                     const int32_t* __restrict__ status) {
   constexpr int d = 32 * E, D = 2 * d;
   constexpr int kUnitWords = 3 * E + E + 2;  // largest group: 3-bit indices, signs, nu, gamma
-  extern __shared__ float s_t[];  // S_d^T, padded: s_t[j * (d + 1) + i] = S[i][j]
+  constexpr int kRow = d + 8;
+  extern __shared__ __align__(16) unsigned char rec_smem[];
+  __half* s_hi = reinterpret_cast<__half*>(rec_smem);  // S[i][j] (i: projection, j: coordinate)
+  __half* s_lo = s_hi + d * kRow;                       // (S - hi) 2^12
   __shared__ float bnd[2][8], cen[2][8];
-  __shared__ __align__(16) float rbuf[kRecWarps][d][kRecUnits];  // residual coordinate j of each unit
   __shared__ uint32_t rowbuf[kRecWarps][kRecUnits][kUnitWords];
+  __shared__ int64_t slot_s[kRecWarps][kRecUnits];
+  __shared__ int head_s[kRecWarps][kRecUnits];
 
   const int tid = threadIdx.x;
   const int mb0 = rc.bits_hi - 1, mb1 = rc.bits_lo - 1;
@@ -88,9 +123,12 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_head
   }
   if (tid < nc0) cen[0][tid] = rc.mse_hi[tid];
   if (tid < nc1) cen[1][tid] = rc.mse_lo[tid];
-  for (int k = tid; k < d * d; k += blockDim.x) {  // coalesced reads, conflict-free stores
+  for (int k = tid; k < d * d; k += blockDim.x) {
     const int i = k / d, j = k - i * d;
-    s_t[j * (d + 1) + i] = __ldg(rc.smat + k);
+    const float sv = __ldg(rc.smat + k);
+    const __half hi = __float2half_rn(sv);
+    s_hi[i * kRow + j] = hi;
+    s_lo[i * kRow + j] = __float2half_rn((sv - __half2float(hi)) * 4096.0f);
   }
   __syncthreads();
   if (*status != kOk) return;  // a slot failed validation: write nothing
@@ -101,138 +139,170 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_head
   float sg[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) sg[i] = __ldg(signs + lane * E + i);
-  float(*res)[kRecUnits] = rbuf[warp];
+  __half* a_hi = s_lo + d * kRow + warp * (2 * kRecUnits * kRow);  // this warp's A tile: unit k, coordinate j
+  __half* a_lo = a_hi + kRecUnits * kRow;
+  // ldmatrix lane addresses: A rows (units) lane & 15, k half lane >> 4; B rows (projections)
+  // (lane & 7) + 8 (lane >> 4), k half (lane >> 3) & 1
+  const uint32_t a_lane = smem_u32(a_hi) + (uint32_t)(((lane & 15) * kRow + (lane >> 4) * 8) * 2);
+  const uint32_t a_lo_off = (uint32_t)(kRecUnits * kRow * 2);
+  const uint32_t b_lane = smem_u32(s_hi) + (uint32_t)((((lane & 7) + 8 * (lane >> 4)) * kRow + ((lane >> 3) & 1) * 8) * 2);
+  const uint32_t b_lo_off = (uint32_t)(d * kRow * 2);
 
   const int64_t units = 2 * num_rows;
   const int64_t ustride = (int64_t)gridDim.x * kRecWarps * kRecUnits;
   for (int64_t u0 = ((int64_t)blockIdx.x * kRecWarps + warp) * kRecUnits; u0 < units; u0 += ustride) {
-    int64_t slot_k[kRecUnits];
-    float nu_k[kRecUnits], gamma_k[kRecUnits];
-    // the four units' slots, channel indices and gathered values first (all loads in flight
-    // together), then their norms and rotations side by side
-    float v[kRecUnits][E];
-    // units u0 .. u0 + 3: rows r0 and r0 + 1 (both groups each); one division for both
-    const int64_t r0 = u0 >> 1;
-    const int64_t t0 = r0 / num_kv_heads;
-    const int h0 = (int)(r0 - t0 * num_kv_heads);
-    const bool wrap = h0 + 1 == num_kv_heads;
-    const int64_t t1 = wrap ? t0 + 1 : t0;
-    const int h1 = wrap ? 0 : h0 + 1;
+#pragma unroll 1
+    for (int q = 0; q < kRecUnits / kRecBatch; ++q) {
+      const int64_t ub = u0 + kRecBatch * q;  // units ub .. ub + 3: rows r0, r0 + 1, both groups
+      int64_t slot_k[kRecBatch];
+      float nu_k[kRecBatch], gamma_k[kRecBatch];
+      float v[kRecBatch][E];
+      const int64_t r0 = ub >> 1;
+      const int64_t t0 = r0 / num_kv_heads;
+      const int h0 = (int)(r0 - t0 * num_kv_heads);
+      const bool wrap = h0 + 1 == num_kv_heads;
+      const int64_t t1 = wrap ? t0 + 1 : t0;
+      const int h1 = wrap ? 0 : h0 + 1;
 #pragma unroll
-    for (int k = 0; k < kRecUnits; ++k) {
-      const int64_t u = u0 + k;
-      const int64_t r = r0 + (k >> 1);
-      const int g = k & 1;
-      const int64_t t = (k >> 1) ? t1 : t0;
-      const int h = (k >> 1) ? h1 : h0;
-      slot_k[k] = u < units ? __ldg(slots + t) : -1;
-      const int32_t* ord = rc.order + (int64_t)h * D + g * d + lane * E;
+      for (int k = 0; k < kRecBatch; ++k) {
+        const int64_t u = ub + k;
+        const int64_t r = r0 + (k >> 1);
+        const int g = k & 1;
+        const int64_t t = (k >> 1) ? t1 : t0;
+        const int h = (k >> 1) ? h1 : h0;
+        slot_k[k] = u < units ? __ldg(slots + t) : -1;
+        const int32_t* ord = rc.order + (int64_t)h * D + g * d + lane * E;
 #pragma unroll
-      for (int i = 0; i < E; ++i) v[k][i] = u < units ? to_f32<T>(raw[r * D + __ldg(ord + i)]) : 0.f;
-    }
-#pragma unroll
-    for (int k = 0; k < kRecUnits; ++k) {
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < E; ++i) ss = fmaf(v[k][i], v[k][i], ss);
-      nu_k[k] = ss;
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1)
-#pragma unroll
-      for (int k = 0; k < kRecUnits; ++k) nu_k[k] += __shfl_xor_sync(kFullMask, nu_k[k], m);
-#pragma unroll
-    for (int k = 0; k < kRecUnits; ++k) {
-      nu_k[k] = sqrtf(nu_k[k]);
-#pragma unroll
-      for (int i = 0; i < E; ++i) v[k][i] *= sg[i];
-      fwht_warp<E>(v[k]);
-    }
-#pragma unroll
-    for (int k = 0; k < kRecUnits; ++k) {
-      const int g = k & 1;
-      uint32_t* buf = rowbuf[warp][k];
-      gamma_k[k] = 0.f;
-      if (slot_k[k] < 0) {  // "Slot Mapping": negative slots are ignored (zero residual)
-#pragma unroll
-        for (int i = 0; i < E; ++i) res[lane * E + i][k] = 0.f;
-        continue;
+        for (int i = 0; i < E; ++i) v[k][i] = u < units ? to_f32<T>(raw[r * D + __ldg(ord + i)]) : 0.f;
+        if (lane == 0) {
+          slot_s[warp][kRecBatch * q + k] = slot_k[k];
+          head_s[warp][kRecBatch * q + k] = h;
+        }
       }
-      const int mb = g ? mb1 : mb0;
-      const float nu = nu_k[k];
-      const float inv = nu > 0.f ? inv_sqrt_d / nu : 0.f;  // y = H(s*x)/(sqrt(d) nu)
+#pragma unroll
+      for (int k = 0; k < kRecBatch; ++k) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) ss = fmaf(v[k][i], v[k][i], ss);
+        nu_k[k] = ss;
+      }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+        for (int k = 0; k < kRecBatch; ++k) nu_k[k] += __shfl_xor_sync(kFullMask, nu_k[k], m);
+#pragma unroll
+      for (int k = 0; k < kRecBatch; ++k) {
+        nu_k[k] = sqrtf(nu_k[k]);
+#pragma unroll
+        for (int i = 0; i < E; ++i) v[k][i] *= sg[i];
+        fwht_warp<E>(v[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < kRecBatch; ++k) {
+        const int g = k & 1;
+        const int uk = kRecBatch * q + k;
+        uint32_t* buf = rowbuf[warp][uk];
+        __half* arow_hi = a_hi + uk * kRow + lane * E;
+        __half* arow_lo = a_lo + uk * kRow + lane * E;
+        gamma_k[k] = 0.f;
+        if (slot_k[k] < 0) {  // "Slot Mapping": negative slots are ignored (zero residual)
+#pragma unroll
+          for (int i = 0; i < E; ++i) arow_hi[i] = arow_lo[i] = __float2half_rn(0.f);
+          continue;
+        }
+        const int mb = g ? mb1 : mb0;
+        const float nu = nu_k[k];
+        const float inv = nu > 0.f ? inv_sqrt_d / nu : 0.f;  // y = H(s*x)/(sqrt(d) nu)
 
-      const int index_words = d * mb / 32;
-      const int gw = index_words + E + 2;
-      for (int w = lane; w < gw; w += 32) buf[w] = 0u;
-      __syncwarp();
-      float rs = 0.f;
+        const int index_words = d * mb / 32;
+        for (int w = lane; w < index_words; w += 32) buf[w] = 0u;
+        __syncwarp();
+        float rs = 0.f;
 #pragma unroll
-      for (int i = 0; i < E; ++i) {
-        const float y = v[k][i] * inv;
-        // idx = #{k : boundary_k < y}: three steps over the 7 (padded) decision points
-        int idx = y > bnd[g][3] ? 4 : 0;
-        idx += y > bnd[g][idx + 1] ? 2 : 0;
-        idx += y > bnd[g][idx] ? 1 : 0;
-        const int bit = (lane * E + i) * mb;
-        const int w = bit >> 5, o = bit & 31;
-        atomicOr(&buf[w], (uint32_t)idx << o);
-        if (o + mb > 32) atomicOr(&buf[w + 1], (uint32_t)idx >> (32 - o));
-        const float dr = y - cen[g][idx];
-        res[lane * E + i][k] = dr;
-        rs = fmaf(dr, dr, rs);
+        for (int i = 0; i < E; ++i) {
+          const float y = v[k][i] * inv;
+          // idx = #{k : boundary_k < y}: three steps over the 7 (padded) decision points
+          int idx = y > bnd[g][3] ? 4 : 0;
+          idx += y > bnd[g][idx + 1] ? 2 : 0;
+          idx += y > bnd[g][idx] ? 1 : 0;
+          const int bit = (lane * E + i) * mb;
+          const int w = bit >> 5, o = bit & 31;
+          atomicOr(&buf[w], (uint32_t)idx << o);
+          if (o + mb > 32) atomicOr(&buf[w + 1], (uint32_t)idx >> (32 - o));
+          const float dr = y - cen[g][idx];
+          rs = fmaf(dr, dr, rs);
+          const float x = dr * 1024.0f;
+          const __half xh = __float2half_rn(x);
+          arow_hi[i] = xh;
+          arow_lo[i] = __float2half_rn((x - __half2float(xh)) * 4096.0f);
+        }
+        gamma_k[k] = rs;
       }
-      gamma_k[k] = rs;
-    }
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1)
+      for (int m = 16; m >= 1; m >>= 1)
 #pragma unroll
-      for (int k = 0; k < kRecUnits; ++k) gamma_k[k] += __shfl_xor_sync(kFullMask, gamma_k[k], m);
-#pragma unroll
-    for (int k = 0; k < kRecUnits; ++k) gamma_k[k] = sqrtf(gamma_k[k]);
-    __syncwarp();
-    // (S r_k)_(lane + 32 e) for the four units; one load of S_d^T and one of the four
-    // residual coordinates j per step
-    float acc[kRecUnits][E];
-#pragma unroll
-    for (int k = 0; k < kRecUnits; ++k)
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < d; ++j) {
-      const float4 r4 = *reinterpret_cast<const float4*>(res[j]);
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float sv = s_t[j * (d + 1) + lane + 32 * e];
-        acc[0][e] = fmaf(sv, r4.x, acc[0][e]);
-        acc[1][e] = fmaf(sv, r4.y, acc[1][e]);
-        acc[2][e] = fmaf(sv, r4.z, acc[2][e]);
-        acc[3][e] = fmaf(sv, r4.w, acc[3][e]);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kRecUnits; ++k) {
-      if (slot_k[k] < 0) continue;  // (uniform across the warp)
-      const int g = k & 1;
-      const int h = (k >> 1) ? h1 : h0;
-      const int mb = g ? mb1 : mb0;
-      const int index_words = d * mb / 32;
-      const int gw = index_words + E + 2;
-      uint32_t* buf = rowbuf[warp][k];
-      // sign word e: bit `lane` is [(S r)_(lane + 32 e) >= 0]
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const uint32_t mask = __ballot_sync(kFullMask, acc[k][e] >= 0.f);
-        if (lane == 0) buf[index_words + e] = mask;
-      }
+        for (int k = 0; k < kRecBatch; ++k) gamma_k[k] += __shfl_xor_sync(kFullMask, gamma_k[k], m);
       if (lane == 0) {
-        buf[index_words + E] = __float_as_uint(nu_k[k]);
-        buf[index_words + E + 1] = __float_as_uint(gamma_k[k]);
+#pragma unroll
+        for (int k = 0; k < kRecBatch; ++k) {
+          if (slot_k[k] < 0) continue;
+          const int iw = d * ((k & 1) ? mb1 : mb0) / 32;
+          rowbuf[warp][kRecBatch * q + k][iw + E] = __float_as_uint(nu_k[k]);
+          rowbuf[warp][kRecBatch * q + k][iw + E + 1] = __float_as_uint(sqrtf(gamma_k[k]));
+        }
       }
-      __syncwarp();
-      uint32_t* dst = reinterpret_cast<uint32_t*>(pages + (slot_k[k] * num_kv_heads + h) * (int64_t)(row_words * 4)) +
+    }
+    __syncwarp();
+    // ---- sketch of the sixteen residuals: sign word e holds projections 32 e .. 32 e + 31
+    // (n-tiles 4 e .. 4 e + 3); lane u < 16 assembles unit u's word
+    const int u = lane & 15, ur = u & 7, uh = u >> 3;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      uint32_t word = 0u;
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {  // n-tiles 4 e + 2 np and 4 e + 2 np + 1
+        float am[2][4], al[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) am[n][x] = al[n][x] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < d / 16; ++ks) {
+          uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+          rec_ldsm_x4(a_lane + ks * 32, h0, h1, h2, h3);
+          rec_ldsm_x4(a_lane + a_lo_off + ks * 32, l0, l1, l2, l3);
+          const uint32_t boff = (uint32_t)((32 * e + 16 * np) * kRow * 2 + ks * 32);
+          uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
+          rec_ldsm_x4(b_lane + boff, b0, b1, b2, b3);
+          rec_ldsm_x4(b_lane + b_lo_off + boff, c0, c1, c2, c3);
+          rec_mma(am[0], h0, h1, h2, h3, b0, b1);
+          rec_mma(am[1], h0, h1, h2, h3, b2, b3);
+          rec_mma(al[0], l0, l1, l2, l3, b0, b1);
+          rec_mma(al[1], l0, l1, l2, l3, b2, b3);
+          rec_mma(al[0], h0, h1, h2, h3, c0, c1);
+          rec_mma(al[1], h0, h1, h2, h3, c2, c3);
+        }
+        // accumulator x of n-tile 4 e + 2 np + n on lane (g, c): unit g + 8 (x >> 1),
+        // projection 32 e + 8 (2 np + n) + 2 c + (x & 1); its ballot bit 4 g + c
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const uint32_t bal = __ballot_sync(kFullMask, fmaf(al[n][x], 1.0f / 4096, am[n][x]) >= 0.f);
+            if ((x >> 1) == uh) word |= spread_nibble((bal >> (4 * ur)) & 15u) << (8 * (2 * np + n) + (x & 1));
+          }
+      }
+      if (lane < 16 && slot_s[warp][u] >= 0) rowbuf[warp][u][d * ((u & 1) ? mb1 : mb0) / 32 + e] = word;
+    }
+    __syncwarp();
+    for (int k = 0; k < kRecUnits; ++k) {
+      const int64_t slot = slot_s[warp][k];
+      if (slot < 0) continue;  // (the same on every lane)
+      const int g = k & 1;
+      const int gw = d * (g ? mb1 : mb0) / 32 + E + 2;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(pages + (slot * num_kv_heads + head_s[warp][k]) * (int64_t)(row_words * 4)) +
                       (g ? group_words(d, rc.bits_hi) : 0);
-      for (int w = lane; w < gw; w += 32) dst[w] = buf[w];
+      for (int w = lane; w < gw; w += 32) dst[w] = rowbuf[warp][k][w];
     }
     __syncwarp();
   }
@@ -623,8 +693,8 @@ cudaError_t launch_write_recipe_typed(const WriteArgs& a, const RecipeArgs& rc, 
   constexpr int d = 32 * E;
   const int64_t units = 2 * a.num_tokens * a.num_kv_heads;
   const int64_t per_cta = (int64_t)kRecWarps * kRecUnits;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((units + per_cta - 1) / per_cta, (int64_t)num_sms * 4));
-  const size_t smem = (size_t)d * (d + 1) * sizeof(float);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((units + per_cta - 1) / per_cta, (int64_t)num_sms * 3));
+  const size_t smem = (size_t)recipe_write_smem(d);
   auto kern = write_recipe_kernel<T, E>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
