@@ -867,11 +867,12 @@ def e2e_measure(tq, w, dev, signs, ck, cv, kp, vp, ws, dbytes, world, steps=5, c
     # the host link on its own, right before the steps: plain copies of the step's raw rows
     # (the link is shared with whatever else uses this host's memory, so it is taken per run)
     l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    l0.record(copy_stream)
-    for _ in range(2):
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-    l1.record(copy_stream)
+    with torch.cuda.stream(copy_stream):
+        l0.record(copy_stream)
+        for _ in range(2):
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+        l1.record(copy_stream)
     torch.cuda.synchronize()
     link_gbs = 2 * (hk.numel() * hk.element_size() + hv.numel() * hv.element_size()) / (l0.elapsed_time(l1) / 1e3) / 1e9
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
