@@ -4,8 +4,9 @@ row_bytes] of any size; Slot Mapping: slots index the whole tensor).
 
 The K and V pages hold 2^31 bytes plus 256 blocks each, and the sequences live in blocks
 drawn from the top 256, so the byte offsets of their rows exceed 2^31 in both tensors.
-The writer, the tensor-core decode, the mixed prefill/decode and the readback are compared
-with the oracle, which sees the same rows gathered into compact pages (block ids remapped).
+The writer, the tensor-core decode, the mixed prefill/decode, the readback and the
+product-key write and decode are compared with the oracle, which sees the same rows gathered
+into compact pages (block ids remapped).
 """
 
 import numpy as np
@@ -130,3 +131,51 @@ def test_readback_past_2gib(tq, case):
     nu = np.stack([c["kc"][s // BS, s % BS, :, -4:].copy().view("<f4").reshape(-1) for s in c["slots_c"][sel]])
     err = np.abs(out.cpu().numpy().astype(np.float64) - want)
     assert np.all(err <= 4e-6 * nu[..., None] + 1e-30), float(np.max(err))
+
+
+def test_product_keys_past_2gib(tq, case):
+    # product-quantised key rows ("QJL residual", 72 B at K4) in a third page tensor with the
+    # same block count: the same blocks start past 2^31 bytes there too; written, then decoded
+    # with the V pages above, against the oracle of the product-key path
+    from oracle import qjl_oracle as qo
+    from parity import BAND, NORM_RTOL, allowed_flips
+
+    c = case
+    dev, codec = c["dev"], c["codec"]
+    rbp = tq.tq_prod_row_bytes(D, KB)
+    assert (c["nblk"] - TOP) * BS * H * rbp >= 1 << 31
+    kpp = torch.zeros(c["nblk"], BS, H, rbp, dtype=torch.uint8, device=dev)
+    s_lib = tq.tq_build_qjl_matrix(D, 43)
+    s64 = qo.normal_matrix(D, D, 43).astype(np.float32).astype(np.float64)
+    kc = codec.centroids(KB - 1)
+    st = tq.tq_write_kv_prod(c["k_h"].to(dev), kpp, torch.from_numpy(c["slots"]).to(dev), c["signs"],
+                             torch.from_numpy(kc).to(dev), s_lib.to(dev))
+    assert int(st.item()) == 0
+    # the compact copy in the order the case fixture used (block ids remapped the same way)
+    order = np.zeros(int(c["bt_c"].max()) + 1, dtype=np.int64)
+    for b in range(len(LENS)):
+        n = -(-LENS[b] // BS)
+        order[c["bt_c"][b, :n]] = c["bt"][b, :n]
+    kpc = kpp[torch.from_numpy(order).to(dev)].cpu().numpy()
+    t = c["slots"].shape[0]
+    rows = kpc.reshape(-1, H, rbp)[c["slots_c"]].reshape(t * H, rbp)
+    x = c["k_h"].float().numpy().astype(np.float64).reshape(t * H, D)
+    enc = qo.encode_prod(x, codec.rot, kc, s64)
+    _, _, margin = o.encode_rows(x, codec.rot, kc)
+    gidx, gz, gnu, ggam = qo.unpack_prod_rows(rows, D, KB)
+    diff = gidx != enc["idx"]
+    assert int((diff & (margin >= BAND)).sum()) == 0 and diff.sum() <= allowed_flips(diff.size)
+    assert np.all(np.abs(gnu - enc["nu"]) <= NORM_RTOL * enc["nu"])
+    clean = ~diff.any(axis=1)
+    proj = enc["residual"] @ s64.T
+    assert int(((gz != enc["z"]) & clean[:, None] & (np.abs(proj) >= 1e-5)).sum()) == 0
+    q = np.random.default_rng(17).standard_normal((len(LENS), HQ, D)).astype(np.float32)
+    lens = np.array(LENS, dtype=np.int32)
+    st = torch.full((1,), -7, dtype=torch.int32, device=dev)
+    got = tq.tq_paged_decode_prod(torch.from_numpy(q).to(dev), kpp, c["vp"], torch.from_numpy(c["bt"]).to(dev),
+                                  torch.from_numpy(lens).to(dev), c["signs"], torch.from_numpy(kc).to(dev), c["cv"],
+                                  s_lib.to(dev), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = qo.paged_decode_prod_keys(q, kpc, c["vc"], KB, VB, c["bt_c"], lens, codec.signs, kc, codec.centroids(VB), s64)
+    assert_decode_close(got.cpu().numpy(), ref)
