@@ -399,14 +399,24 @@ __device__ __forceinline__ GroupView<E> read_group_s(const uint32_t* gw, int mb,
   return v;
 }
 
-template <int E, int G, int MB>
+// PAIRS: the group's words start 8-byte aligned and are even in number (64-bit loads).
+template <int E, int G, int MB, bool PAIRS>
 __device__ __forceinline__ void recipe_group_score(const uint32_t* __restrict__ gw, const float (*qs)[G],
                                                    const float (*ps)[G], const float* cent, const float* psum,
                                                    float kappa, float (&sc)[G]) {
   constexpr int d = 32 * E, IW = d * MB / 32;
   uint32_t w[IW + E + 2];
+  if constexpr (PAIRS) {
 #pragma unroll
-  for (int k = 0; k < IW + E + 2; ++k) w[k] = __ldg(gw + k);
+    for (int k = 0; k < (IW + E + 2) / 2; ++k) {
+      const uint2 x = __ldg(reinterpret_cast<const uint2*>(gw) + k);
+      w[2 * k] = x.x;
+      w[2 * k + 1] = x.y;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < IW + E + 2; ++k) w[k] = __ldg(gw + k);
+  }
   float sm[G], sz[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) sm[g] = sz[g] = 0.f;
@@ -439,6 +449,8 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
   constexpr int d = 32 * E, D = 2 * d;
   constexpr int kWh = d * MB0 / 32 + E + 2;  // words of the high group
   constexpr int rbw = kWh + d * MB1 / 32 + E + 2;  // words of a row
+  // rows and both groups 8-byte aligned (pages are 16-byte aligned): 64-bit row loads
+  constexpr bool kPairs = rbw % 2 == 0 && kWh % 2 == 0 && (d * MB1 / 32 + E + 2) % 2 == 0;
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.num_kv_heads, bs = a.block_size;
@@ -523,11 +535,20 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
     if (row >= 0) {
       const uint32_t* vr = reinterpret_cast<const uint32_t*>(a.v_pages) + row * rbw;
       uint32_t vw[rbw];  // this token's value row, in flight while the key row is scored
+      if constexpr (kPairs) {
 #pragma unroll
-      for (int k = 0; k < rbw; ++k) vw[k] = __ldg(vr + k);
+        for (int k = 0; k < rbw / 2; ++k) {
+          const uint2 x = __ldg(reinterpret_cast<const uint2*>(vr) + k);
+          vw[2 * k] = x.x;
+          vw[2 * k + 1] = x.y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < rbw; ++k) vw[k] = __ldg(vr + k);
+      }
       const uint32_t* kr = reinterpret_cast<const uint32_t*>(a.k_pages) + row * rbw;
-      recipe_group_score<E, G, MB0>(kr, qs[0], ps[0], cent[0], psum[0], kappa, sc);
-      recipe_group_score<E, G, MB1>(kr + kWh, qs[1], ps[1], cent[1], psum[1], kappa, sc);
+      recipe_group_score<E, G, MB0, kPairs>(kr, qs[0], ps[0], cent[0], psum[0], kappa, sc);
+      recipe_group_score<E, G, MB1, kPairs>(kr + kWh, qs[1], ps[1], cent[1], psum[1], kappa, sc);
 #pragma unroll
       for (int k = 0; k < rbw; ++k) vbuf[warp][lane][k] = vw[k];
     }
