@@ -97,7 +97,18 @@ __device__ __forceinline__ uint32_t spread_nibble(uint32_t x) {
 // d + 8 halves (16 bytes of padding put the 8 rows of an ldmatrix in different banks).
 __host__ __device__ constexpr int recipe_write_smem(int d) { return (2 * d + kRecWarps * 2 * kRecUnits) * (d + 8) * 2; }
 
-template <typename T, int E>
+// idx = #{k : b_k < y} over the 2^MB - 1 decision points held in registers (ties and NaN: the
+// lower index)
+template <int MB>
+__device__ __forceinline__ int rec_index(float y, const float (&b)[7]) {
+  int idx = 0;
+#pragma unroll
+  for (int k = 0; k < (1 << MB) - 1; ++k) idx += y > b[k] ? 1 : 0;
+  return idx;
+}
+
+// MB0 / MB1: MSE index bits of the high / low group.
+template <typename T, int E, int MB0, int MB1>
 __global__ void __launch_bounds__(kRecWarps * 32, 3)
 write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads, const int64_t* __restrict__ slots,
                     uint8_t* __restrict__ pages, RecipeArgs rc, const float* __restrict__ signs,
@@ -108,18 +119,20 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_head
   extern __shared__ __align__(16) unsigned char rec_smem[];
   __half* s_hi = reinterpret_cast<__half*>(rec_smem);  // S[i][j] (i: projection, j: coordinate)
   __half* s_lo = s_hi + d * kRow;                       // (S - hi) 2^12
-  __shared__ float bnd[2][8], cen[2][8];
+  __shared__ float cen[2][8];
   __shared__ uint32_t rowbuf[kRecWarps][kRecUnits][kUnitWords];
   __shared__ int64_t slot_s[kRecWarps][kRecUnits];
   __shared__ int head_s[kRecWarps][kRecUnits];
 
   const int tid = threadIdx.x;
-  const int mb0 = rc.bits_hi - 1, mb1 = rc.bits_lo - 1;
-  const int nc0 = 1 << mb0, nc1 = 1 << mb1;
-  // decision points, padded with +inf to 7 (so a 3-step search counts them for any width)
-  if (tid < 8) {
-    bnd[0][tid] = tid < nc0 - 1 ? 0.5f * (rc.mse_hi[tid] + rc.mse_hi[tid + 1]) : INFINITY;
-    bnd[1][tid] = tid < nc1 - 1 ? 0.5f * (rc.mse_lo[tid] + rc.mse_lo[tid + 1]) : INFINITY;
+  constexpr int mb0 = MB0, mb1 = MB1;
+  constexpr int nc0 = 1 << MB0, nc1 = 1 << MB1;
+  // the decision points of both groups, in registers
+  float bhi[7], blo[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) {
+    bhi[k] = k < nc0 - 1 ? 0.5f * (__ldg(rc.mse_hi + k) + __ldg(rc.mse_hi + k + 1)) : INFINITY;
+    blo[k] = k < nc1 - 1 ? 0.5f * (__ldg(rc.mse_lo + k) + __ldg(rc.mse_lo + k + 1)) : INFINITY;
   }
   if (tid < nc0) cen[0][tid] = rc.mse_hi[tid];
   if (tid < nc1) cen[1][tid] = rc.mse_lo[tid];
@@ -221,10 +234,7 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_head
 #pragma unroll
         for (int i = 0; i < E; ++i) {
           const float y = v[k][i] * inv;
-          // idx = #{k : boundary_k < y}: three steps over the 7 (padded) decision points
-          int idx = y > bnd[g][3] ? 4 : 0;
-          idx += y > bnd[g][idx + 1] ? 2 : 0;
-          idx += y > bnd[g][idx] ? 1 : 0;
+          const int idx = g ? rec_index<MB1>(y, blo) : rec_index<MB0>(y, bhi);
           const int bit = (lane * E + i) * mb;
           const int w = bit >> 5, o = bit & 31;
           atomicOr(&buf[w], (uint32_t)idx << o);
@@ -709,14 +719,14 @@ combine_recipe_kernel(DecodeArgs a, RecipeArgs rc, int num_splits, RecipeSplitVi
   }
 }
 
-template <typename T, int E>
-cudaError_t launch_write_recipe_typed(const WriteArgs& a, const RecipeArgs& rc, cudaStream_t stream, int num_sms) {
+template <typename T, int E, int MB0, int MB1>
+cudaError_t launch_write_recipe_mb(const WriteArgs& a, const RecipeArgs& rc, cudaStream_t stream, int num_sms) {
   constexpr int d = 32 * E;
   const int64_t units = 2 * a.num_tokens * a.num_kv_heads;
   const int64_t per_cta = (int64_t)kRecWarps * kRecUnits;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((units + per_cta - 1) / per_cta, (int64_t)num_sms * 3));
   const size_t smem = (size_t)recipe_write_smem(d);
-  auto kern = write_recipe_kernel<T, E>;
+  auto kern = write_recipe_kernel<T, E, MB0, MB1>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   kern<<<grid, kRecWarps * 32, smem, stream>>>(static_cast<const T*>(a.raw), a.num_tokens * a.num_kv_heads,
@@ -724,6 +734,13 @@ cudaError_t launch_write_recipe_typed(const WriteArgs& a, const RecipeArgs& rc, 
   err = cudaGetLastError();
   if (err == cudaSuccess) count_launches(1);
   return err;
+}
+
+template <typename T, int E>
+cudaError_t launch_write_recipe_typed(const WriteArgs& a, const RecipeArgs& rc, cudaStream_t stream, int num_sms) {
+  if (rc.bits_hi == 3 && rc.bits_lo == 2) return launch_write_recipe_mb<T, E, 2, 1>(a, rc, stream, num_sms);  // turboquant25
+  if (rc.bits_hi == 4 && rc.bits_lo == 3) return launch_write_recipe_mb<T, E, 3, 2>(a, rc, stream, num_sms);  // turboquant35
+  return cudaErrorInvalidValue;
 }
 
 template <typename T>
