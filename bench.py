@@ -761,8 +761,9 @@ def recipe_measure(tq, w, dev, kraw, vraw, slots, slots_np, bt, lens, q, flush, 
     out.update({"workload": f"the step's {int((slots_np >= 0).sum()) * w.num_kv_heads} K rows (and V rows, untimed) "
                             f"as recipe rows at D{d}, then the decode of the {w.batch} sequences over K and V recipe "
                             "pages", "peak": peak, "peak_source": peak_kind,
-                "kernels": "SIMT (write_recipe_kernel; recipe_project_kernel + decode_recipe_split_kernel + "
-                           "combine_recipe_kernel)"})
+                "kernels": "write_recipe_kernel (SIMT rotation and quantiser, m16n8k16 sketch); "
+                           "recipe_project_kernel + decode_recipe_tc_kernel (m16n8k16 scores and values) + "
+                           "combine_recipe_kernel"})
     return out
 
 

@@ -448,6 +448,37 @@ __device__ __forceinline__ void recipe_group_score(const uint32_t* __restrict__ 
   for (int g = 0; g < G; ++g) sc[g] = fmaf(nu, fmaf(gk, fmaf(2.f, sz[g], -psum[g]), sm[g]), sc[g]);
 }
 
+// Merges the NW warps' partials of one CTA (running max in log2 units and sum per q head;
+// value accumulators as in RecipeSplitView) and writes the CTA's split partial for q rows
+// row0 + g.  Called after a barrier that makes every warp's partial visible.
+template <int NW, int G, int D>
+__device__ __forceinline__ void recipe_merge_write(const float (*red_ml)[G][2], const float (*red_acc)[G][2 * D],
+                                                   int64_t row0, int num_splits, int split, RecipeSplitView part,
+                                                   int warp, int lane) {
+  for (int g = warp; g < G; g += NW) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) mx = fmaxf(mx, red_ml[w][g][0]);
+    float wt[NW], lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      wt[w] = red_ml[w][g][0] == -INFINITY ? 0.f : exp2f(red_ml[w][g][0] - mx);
+      lsum = fmaf(wt[w], red_ml[w][g][1], lsum);
+    }
+    const int64_t slot = (row0 + g) * num_splits + split;
+    for (int k = lane; k < 2 * D; k += 32) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) sum = fmaf(wt[w], red_acc[w][g][k], sum);
+      part.acc[slot * 2 * D + k] = sum;
+    }
+    if (lane == 0) {
+      part.ml[slot * 2 + 0] = mx;
+      part.ml[slot * 2 + 1] = lsum;
+    }
+  }
+}
+
 // Tiles of 32 tokens per warp.  Scores: lane = token, every q head of the kv head at once
 // (no per-token reductions); the tile's softmax step (running max, correction, weights) once
 // per tile; values: lanes over coordinates, the tile's tokens accumulated with their weights
@@ -637,28 +668,426 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
       }
   }
   __syncthreads();
-  for (int g = warp; g < G; g += kRecDecodeWarps) {
-    float mx = -INFINITY;
+  recipe_merge_write<kRecDecodeWarps, G, D>(red_ml, red_acc, (int64_t)b * a.num_q_heads + (int64_t)h * G, num_splits,
+                                            split, part, warp, lane);
+}
+
+// ---- tensor-core split decode (G <= 4) -------------------------------------------------
+// Each warp takes 16-token tiles of its split in turn.  The tile's K and V rows are staged in
+// shared memory by cp.async (the next tile's copies in flight while this one is computed;
+// rows of tokens past the sequence end or in a block with a bad id are zero-filled).  Every
+// contraction is an m16n8k16 MMA with fp32 accumulation whose n = 8 columns hold q heads 0-3
+// twice: columns 0-3 take the fp16 hi part of the B operand, columns 4-7 its remainder, so one
+// MMA gives both products and every product keeps ~22 significant bits.
+//
+// Scores of a group: A = the K tile (tokens x coordinates); the lane of column c takes the
+// coordinates [8E c, 8E c + 8E) in pairs, each A register one entry of a pair table (the
+// centroids of two adjacent coordinates: fp16 hi in .x, remainder in .y; sixteen copies, so a
+// 64-bit lookup by a half warp never conflicts) addressed by the pair's 2 MB-bit field;
+// B = the rotated query.  The sign term takes A = +-1 built from two sign bits 16 apart (one
+// shift, one LOP3 per register) against B = p = S_d q.  score = sum_g nu_g (m_g + gamma_g
+// kappa s_g).
+//
+// Values of a group: A = the V tile transposed (coordinates x tokens); the lane of row gr
+// takes the coordinates [4E gr, 4E gr + 4E) of four tokens, two table entries merged by PRMT
+// per register, and the sign term from bytes of two tokens' sign words.  B = the weights
+// p nu 2^(12 - e) (values) and p nu gamma kappa 2^(12 - e) (signs), where 2^e bounds every
+// value norm the warp has seen (when e grows the accumulators are scaled by the same power of
+// two, exactly, with the softmax correction), so no weight leaves fp16 range.
+constexpr int kRecTcWarps = 4;
+
+__device__ __forceinline__ void rec_cp8(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void rec_cp4(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void rec_cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void rec_cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// (x0, x1) as an fp16 pair (x0 in the low half): the rounded values, or with `rem` the
+// remainders x - fp16(x)
+__device__ __forceinline__ uint32_t rec_split_pack(float x0, float x1, bool rem) {
+  const __half2 hi = __floats2half2_rn(x0, x1);
+  const __half2 lo = __floats2half2_rn(x0 - __low2float(hi), x1 - __high2float(hi));
+  const __half2 r = rem ? lo : hi;
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+// fp16 pair of +-1 from bits 15 and 31 of x (bit set: +1)
+__device__ __forceinline__ uint32_t rec_sign2(uint32_t x) { return (~x & 0x80008000u) | 0x3C003C00u; }
+// Byte offset, within a pair table, of the entry whose fbits-bit field sits at bit sh of x,
+// in the copy of this lane (lane8 = 8 (lane mod 16); entries are 128 bytes apart).
+__device__ __forceinline__ uint32_t rec_tab_off(uint32_t x, int sh, int fbits, uint32_t lane8) {
+  const uint32_t y = sh >= 7 ? (x >> (sh - 7)) : (x << (7 - sh));
+  return (y & (((1u << fbits) - 1u) << 7)) | lane8;
+}
+// Pair-table entry f of a codebook of 2^mb centroids: (c[f mod 2^mb], c[f / 2^mb]).
+__device__ __forceinline__ uint2 rec_pair_entry(const float* __restrict__ cent, int f, int mb) {
+  const float c0 = __ldg(cent + (f & ((1 << mb) - 1))), c1 = __ldg(cent + (f >> mb));
+  uint2 e;
+  e.x = rec_split_pack(c0, c1, false);
+  e.y = rec_split_pack(c0, c1, true);
+  return e;
+}
+
+template <int E, int G, int MB0, int MB1>
+__global__ void __launch_bounds__(kRecTcWarps * 32, 3)
+decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p_all, int num_splits,
+                        int blocks_per_split, RecipeSplitView part) {
+  static_assert(G <= 4, "the eight MMA columns hold four q heads' hi and lo parts");
+  constexpr int d = 32 * E, D = 2 * d;
+  constexpr int kWh = E * MB0 + E + 2;        // words of the high group
+  constexpr int rbw = kWh + E * MB1 + E + 2;  // words of a row
+  constexpr bool kPairs = rbw % 2 == 0;       // rows, groups and (nu, gamma) 8-byte aligned
+  static_assert(!kPairs || (kWh % 2 == 0 && (E * MB0 + E) % 2 == 0 && (E * MB1 + E) % 2 == 0), "alignment");
+  constexpr int kTok = 2 * rbw;    // staged words of one token: its K row, then its V row
+  constexpr int kBuf = 16 * kTok;  // one tile
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gr = lane >> 2, c = lane & 3;
+  const int H = a.num_kv_heads, bs = a.block_size;
+
+  __shared__ __align__(16) uint2 tab0[1 << (2 * MB0)][16];
+  __shared__ __align__(16) uint2 tab1[1 << (2 * MB1)][16];
+  __shared__ __align__(16) float qv[2][2][4][d];          // [q | p][group][q head][coordinate]
+  __shared__ __align__(16) float pt[kRecTcWarps][4][16];  // the tile's weights [q head][token]
+  __shared__ float red_ml[kRecTcWarps][G][2];
+  constexpr int kStageWords = kRecTcWarps * 2 * kBuf, kRedWords = kRecTcWarps * G * 2 * D;
+  // the warps' staged tiles, then (after the last tile) the merge buffer
+  __shared__ __align__(16) uint32_t stage_u[kStageWords > kRedWords ? kStageWords : kRedWords];
+  float(*red_acc)[G][2 * D] = reinterpret_cast<float(*)[G][2 * D]>(stage_u);
+
+  for (int i = threadIdx.x; i < (1 << (2 * MB0)) * 16; i += blockDim.x) tab0[i >> 4][i & 15] = rec_pair_entry(rc.mse_hi, i >> 4, MB0);
+  for (int i = threadIdx.x; i < (1 << (2 * MB1)) * 16; i += blockDim.x) tab1[i >> 4][i & 15] = rec_pair_entry(rc.mse_lo, i >> 4, MB1);
+  const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
+  const float qmul = scale * kRecLog2e / sqrtf((float)d);
+  const float kappa = kRecSqrtHalfPi / (float)d;
+  for (int g = warp; g < 4; g += kRecTcWarps) {  // heads past G: zero query, never written
+    const int64_t qrow = (int64_t)b * a.num_q_heads + (int64_t)h * G + g;
 #pragma unroll
-    for (int w = 0; w < kRecDecodeWarps; ++w) mx = fmaxf(mx, red_ml[w][g][0]);
-    float wt[kRecDecodeWarps], lsum = 0.f;
+    for (int grp = 0; grp < 2; ++grp) {
+      float qr[E];
+      const int32_t* ord = rc.order + (int64_t)h * D + grp * d + lane * E;
 #pragma unroll
-    for (int w = 0; w < kRecDecodeWarps; ++w) {
-      wt[w] = red_ml[w][g][0] == -INFINITY ? 0.f : exp2f(red_ml[w][g][0] - mx);
-      lsum = fmaf(wt[w], red_ml[w][g][1], lsum);
-    }
-    const int64_t slot = ((int64_t)b * a.num_q_heads + (int64_t)h * G + g) * num_splits + split;
-    for (int k = lane; k < 2 * D; k += 32) {
-      float sum = 0.f;
+      for (int i = 0; i < E; ++i)
+        qr[i] = g < G ? load_as_f32(a.q, qrow * D + __ldg(ord + i), a.q_dtype) * __ldg(a.signs + lane * E + i) : 0.f;
+      fwht_warp<E>(qr);
 #pragma unroll
-      for (int w = 0; w < kRecDecodeWarps; ++w) sum = fmaf(wt[w], red_acc[w][g][k], sum);
-      part.acc[slot * 2 * D + k] = sum;
-    }
-    if (lane == 0) {
-      part.ml[slot * 2 + 0] = mx;
-      part.ml[slot * 2 + 1] = lsum;
+      for (int i = 0; i < E; ++i) {
+        qv[0][grp][g][lane * E + i] = qr[i] * qmul;
+        qv[1][grp][g][lane + 32 * i] = g < G ? __ldg(p_all + (qrow * 2 + grp) * d + lane + 32 * i) : 0.f;
+      }
     }
   }
+
+  int len = __ldg(a.seq_lens + b);
+  const int cap = a.max_blocks_per_seq * bs;
+  if (len < 0 || len > cap) {
+    if (threadIdx.x == 0 && split == 0 && h == 0 && a.status) atomicMax(a.status, (int32_t)kInvalidArg);
+    len = len < 0 ? 0 : cap;
+  }
+  const int t_lo = split * blocks_per_split * bs;
+  const int t_hi = min(len, (split + 1) * blocks_per_split * bs);
+  __syncthreads();
+
+  // B operands of the scores: column n = gr is q head gr mod 4, its fp16 hi part for gr < 4
+  // and its remainder for gr >= 4.  Pair kp = 2 s + slot of k-step s: coordinates
+  // 8E c + 2 kp (+1) for the centroid term; for the sign term the pair P = 4E c + kp,
+  // coordinates 32 (P / 16) + P mod 16 and 16 above.
+  const bool rem_col = gr >= 4;
+  const int hq = gr & 3;
+  uint32_t bq[2][2 * E][2], bp[2][2 * E][2];
+#pragma unroll
+  for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+    for (int s = 0; s < 2 * E; ++s)
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        const int kp = 2 * s + slot;
+        const int j = 8 * E * c + 2 * kp;
+        bq[grp][s][slot] = rec_split_pack(qv[0][grp][hq][j], qv[0][grp][hq][j + 1], rem_col);
+        const int pp = 4 * E * c + kp;
+        const int js = 32 * (pp >> 4) + (pp & 15);
+        bp[grp][s][slot] = rec_split_pack(qv[1][grp][hq][js], qv[1][grp][hq][js + 16], rem_col);
+      }
+  const int sw_k = (4 * E * c) >> 4, sh_k = (4 * E * c) & 15;  // this lane's sign word, first bit
+  const uint32_t lane8 = (uint32_t)(lane & 15) << 3;
+  const unsigned char* tabs[2] = {reinterpret_cast<const unsigned char*>(&tab0[0][0]),
+                                  reinterpret_cast<const unsigned char*>(&tab1[0][0])};
+
+  // staging: lane L copies the K (L < 16) or V row of token L mod 16
+  const uint32_t* stage_w = stage_u + warp * 2 * kBuf;
+  const uint32_t stage_base = smem_u32(stage_w);
+  const int tt = lane & 15, kv = lane >> 4;
+  const unsigned char* pages = kv ? a.v_pages : a.k_pages;
+  const bool bs_pow2 = (bs & (bs - 1)) == 0;
+  const int bs_shift = __ffs(bs) - 1;
+  bool bad_block = false;
+  // Issues the copies of the tile at token t0 into buffer buf; returns its valid-token mask.
+  auto issue = [&](int t0, int buf) -> uint32_t {
+    const int t = t0 + tt;
+    bool ok = false;
+    int64_t row = 0;
+    if (t < t_hi) {
+      const int blk = bs_pow2 ? (t >> bs_shift) : t / bs;
+      const int bid = __ldg(a.block_table + (int64_t)b * a.max_blocks_per_seq + blk);
+      if (bid < 0 || (int64_t)bid >= a.num_blocks) {
+        bad_block = true;
+      } else {
+        ok = true;
+        row = ((int64_t)bid * bs + (t - blk * bs)) * H + h;
+      }
+    }
+    const unsigned char* src = pages + row * (int64_t)(4 * rbw);
+    const uint32_t dst = stage_base + (uint32_t)((buf * 16 + tt) * kTok + kv * rbw) * 4u;
+    if constexpr (kPairs) {
+      const uint32_t nb = ok ? 8u : 0u;
+#pragma unroll
+      for (int k = 0; k < rbw / 2; ++k) rec_cp8(dst + 8 * k, src + 8 * k, nb);
+    } else {
+      const uint32_t nb = ok ? 4u : 0u;
+#pragma unroll
+      for (int k = 0; k < rbw; ++k) rec_cp4(dst + 4 * k, src + 4 * k, nb);
+    }
+    rec_cp_commit();
+    return __ballot_sync(kFullMask, ok) & 0xffffu;
+  };
+
+  float ov[2][2 * E][4], oz[2][2 * E][4];  // value accumulators: rows coordinates, columns heads
+#pragma unroll
+  for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+    for (int u = 0; u < 2 * E; ++u)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ov[grp][u][i] = oz[grp][u][i] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // q heads 2 (c mod 2) + e
+  int e_run = -115;  // every value norm seen so far is below 2^e_run
+
+  int t0 = t_lo + 16 * warp;
+  uint32_t vm = t0 < t_hi ? issue(t0, 0) : 0u;
+  for (int it = 0; t0 < t_hi; ++it, t0 += 16 * kRecTcWarps) {
+    const int buf = it & 1;
+    const int tn = t0 + 16 * kRecTcWarps;
+    uint32_t vm_next = 0u;
+    if (tn < t_hi) {
+      vm_next = issue(tn, buf ^ 1);
+      rec_cp_wait<1>();
+    } else {
+      rec_cp_wait<0>();
+    }
+    __syncwarp();
+    const uint32_t* tile = stage_w + buf * kBuf;
+
+    // ---- scores of tokens gr + 8 r, q heads 2 (c mod 2) + e (this lane's column part) ----
+    float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const int MB = grp ? MB1 : MB0, goff = grp ? kWh : 0, IW = E * MB;
+      const unsigned char* tabp = tabs[grp];
+      uint32_t ch[2][E], sg[2];
+      float nk[2], gk[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t* kr = tile + (gr + 8 * r) * kTok + goff;
+#pragma unroll
+        for (int q = 0; q < E; ++q) {  // coordinates [8E c + 8 q, + 8)
+          const int bit = (8 * E * c + 8 * q) * MB;
+          ch[r][q] = __funnelshift_r(kr[bit >> 5], kr[(bit >> 5) + 1], bit & 31);
+        }
+        sg[r] = kr[IW + sw_k] >> sh_k;
+        nk[r] = __uint_as_float(kr[IW + E]);
+        gk[r] = __uint_as_float(kr[IW + E + 1]) * kappa;
+      }
+      float am[4] = {0.f, 0.f, 0.f, 0.f}, as[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < 2 * E; ++s) {
+        uint2 tv[2][2];
+        uint32_t sv[2][2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int slot = 0; slot < 2; ++slot) {
+            const int kp = 2 * s + slot;
+            tv[r][slot] = *reinterpret_cast<const uint2*>(tabp + rec_tab_off(ch[r][kp >> 2], 2 * MB * (kp & 3), 2 * MB, lane8));
+            sv[r][slot] = rec_sign2(sg[r] << (15 - kp));
+          }
+        rec_mma(am, tv[0][0].x, tv[1][0].x, tv[0][1].x, tv[1][1].x, bq[grp][s][0], bq[grp][s][1]);
+        rec_mma(am, tv[0][0].y, tv[1][0].y, tv[0][1].y, tv[1][1].y, bq[grp][s][0], bq[grp][s][1]);
+        rec_mma(as, sv[0][0], sv[1][0], sv[0][1], sv[1][1], bp[grp][s][0], bp[grp][s][1]);
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) sc[r][e] = fmaf(nk[r], fmaf(gk[r], as[2 * r + e], am[2 * r + e]), sc[r][e]);
+    }
+    // hi + lo column parts; masked tokens
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        sc[r][e] += __shfl_xor_sync(kFullMask, sc[r][e], 2);
+        if (!((vm >> (gr + 8 * r)) & 1u)) sc[r][e] = -INFINITY;
+      }
+
+    // ---- the tile's softmax step ----
+    float corr[2], p[2][2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float tm = fmaxf(sc[0][e], sc[1][e]);
+      tm = fmaxf(tm, __shfl_xor_sync(kFullMask, tm, 4));
+      tm = fmaxf(tm, __shfl_xor_sync(kFullMask, tm, 8));
+      tm = fmaxf(tm, __shfl_xor_sync(kFullMask, tm, 16));
+      const float mn = fmaxf(m_run[e], tm);
+      corr[e] = 1.f;
+      p[0][e] = p[1][e] = 0.f;
+      if (mn != -INFINITY) {  // some token of this or an earlier tile
+        corr[e] = exp2f(m_run[e] - mn);
+        p[0][e] = exp2f(sc[0][e] - mn);
+        p[1][e] = exp2f(sc[1][e] - mn);
+      }
+      l_run[e] = fmaf(l_run[e], corr[e], p[0][e] + p[1][e]);
+      m_run[e] = mn;
+    }
+    if (c < 2) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) pt[warp][2 * c + e][gr + 8 * r] = p[r][e];
+    }
+
+    // ---- value norms of this lane's tokens 2c, 2c + 1, 2c + 8, 2c + 9; the weight scale ----
+    float nv[4][2], gv[4][2];
+    float vmax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t* vr = tile + (2 * c + (k & 1) + 8 * (k >> 1)) * kTok + rbw;
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp) {
+        const int w = (grp ? kWh + E * MB1 : E * MB0) + E;
+        nv[k][grp] = __uint_as_float(vr[w]);
+        gv[k][grp] = __uint_as_float(vr[w + 1]) * kappa;
+      }
+      vmax = fmaxf(vmax, fmaxf(nv[k][0], nv[k][1]));
+    }
+    vmax = fmaxf(vmax, __shfl_xor_sync(kFullMask, vmax, 1));
+    vmax = fmaxf(vmax, __shfl_xor_sync(kFullMask, vmax, 2));
+    if (vmax > 0.f) {
+      const int ex = (int)((__float_as_uint(vmax) >> 23) & 255u) - 126;  // vmax < 2^ex
+      if (ex > e_run) {
+        const float f = ldexpf(1.f, e_run - ex);
+        corr[0] *= f;
+        corr[1] *= f;
+        e_run = ex;
+      }
+    }
+    if (__any_sync(kFullMask, corr[0] != 1.f || corr[1] != 1.f)) {
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+        for (int u = 0; u < 2 * E; ++u)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            ov[grp][u][i] *= corr[i & 1];
+            oz[grp][u][i] *= corr[i & 1];
+          }
+    }
+    const float wscale = __uint_as_float((uint32_t)(139 - e_run) << 23);  // 2^(12 - e_run)
+    __syncwarp();  // pt
+
+    // ---- value weights (B: column n = gr, q head gr mod 4, hi for gr < 4, remainder else) ----
+    uint32_t bc[2][2], bz[2][2];
+    {
+      const float2 pa = *reinterpret_cast<const float2*>(&pt[warp][hq][2 * c]);
+      const float2 pb = *reinterpret_cast<const float2*>(&pt[warp][hq][2 * c + 8]);
+      const float pw[4] = {pa.x * wscale, pa.y * wscale, pb.x * wscale, pb.y * wscale};
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp) {
+        float wc[4], wz[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          wc[k] = pw[k] * nv[k][grp];
+          wz[k] = wc[k] * gv[k][grp];
+        }
+        bc[grp][0] = rec_split_pack(wc[0], wc[1], rem_col);
+        bc[grp][1] = rec_split_pack(wc[2], wc[3], rem_col);
+        bz[grp][0] = rec_split_pack(wz[0], wz[1], rem_col);
+        bz[grp][1] = rec_split_pack(wz[2], wz[3], rem_col);
+      }
+    }
+
+    // ---- values: rows = coordinates (pairs 4E gr + 2u of the centroid term, 16 u + gr of
+    // the sign term; row gr + 8 the next one), columns = heads ----
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const int MB = grp ? MB1 : MB0, goff = grp ? kWh : 0, IW = E * MB;
+      const unsigned char* tabp = tabs[grp];
+      const int bitv = 4 * E * gr * MB;
+      uint32_t chv[4], sw[4][E];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t* vr = tile + (2 * c + (k & 1) + 8 * (k >> 1)) * kTok + rbw + goff;
+        chv[k] = __funnelshift_r(vr[bitv >> 5], vr[(bitv >> 5) + 1], bitv & 31);
+#pragma unroll
+        for (int w = 0; w < E; ++w) sw[k][w] = vr[IW + w];
+      }
+#pragma unroll
+      for (int u = 0; u < 2 * E; ++u) {
+        uint2 x[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          x[k] = *reinterpret_cast<const uint2*>(tabp + rec_tab_off(chv[k], 2 * MB * u, 2 * MB, lane8));
+        rec_mma(ov[grp][u], __byte_perm(x[0].x, x[1].x, 0x5410), __byte_perm(x[0].x, x[1].x, 0x7632),
+                __byte_perm(x[2].x, x[3].x, 0x5410), __byte_perm(x[2].x, x[3].x, 0x7632), bc[grp][0], bc[grp][1]);
+        rec_mma(ov[grp][u], __byte_perm(x[0].y, x[1].y, 0x5410), __byte_perm(x[0].y, x[1].y, 0x7632),
+                __byte_perm(x[2].y, x[3].y, 0x5410), __byte_perm(x[2].y, x[3].y, 0x7632), bc[grp][0], bc[grp][1]);
+        // sign bits 16 (u mod 2) + gr and + 8 of word u / 2: bytes bb, bb + 1 of two tokens
+        const int bb = 2 * (u & 1);
+        const uint32_t sel = (uint32_t)(bb | (bb + 1) << 4 | (bb + 4) << 8 | (bb + 5) << 12);
+        const uint32_t z01 = __byte_perm(sw[0][u >> 1], sw[1][u >> 1], sel);
+        const uint32_t z23 = __byte_perm(sw[2][u >> 1], sw[3][u >> 1], sel);
+        rec_mma(oz[grp][u], rec_sign2(z01 << (15 - gr)), rec_sign2(z01 << (7 - gr)), rec_sign2(z23 << (15 - gr)),
+                rec_sign2(z23 << (7 - gr)), bz[grp][0], bz[grp][1]);
+      }
+    }
+    __syncwarp();  // the next tile rewrites pt and this buffer
+    vm = vm_next;
+  }
+  if (__any_sync(kFullMask, bad_block) && lane == 0 && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
+  __syncthreads();  // every warp is done with its staged rows: the merge buffer may be written
+
+  // this warp's partial: l over the lane rows, hi + lo columns, the weight scale undone
+  const float unscale = ldexpf(1.f, e_run - 12);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float l = l_run[e];
+    l += __shfl_xor_sync(kFullMask, l, 4);
+    l += __shfl_xor_sync(kFullMask, l, 8);
+    l += __shfl_xor_sync(kFullMask, l, 16);
+    const int g = 2 * c + e;
+    if (gr == 0 && c < 2 && g < G) {
+      red_ml[warp][g][0] = m_run[e];
+      red_ml[warp][g][1] = l;
+    }
+  }
+#pragma unroll
+  for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+    for (int u = 0; u < 2 * E; ++u)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float v = ov[grp][u][i] + __shfl_xor_sync(kFullMask, ov[grp][u][i], 2);
+        const float z = oz[grp][u][i] + __shfl_xor_sync(kFullMask, oz[grp][u][i], 2);
+        const int g = 2 * c + (i & 1), r = i >> 1;
+        if (c < 2 && g < G) {
+          red_acc[warp][g][grp * d + 4 * E * gr + 2 * u + r] = v * unscale;
+          red_acc[warp][g][D + grp * d + 16 * u + gr + 8 * r] = z * unscale;
+        }
+      }
+  __syncthreads();
+  recipe_merge_write<kRecTcWarps, G, D>(red_ml, red_acc, (int64_t)b * a.num_q_heads + (int64_t)h * G, num_splits,
+                                        split, part, warp, lane);
 }
 
 template <int E>
@@ -753,10 +1182,10 @@ cudaError_t launch_write_recipe_dim(const WriteArgs& a, const RecipeArgs& rc, cu
 template <int E, int MB0, int MB1>
 cudaError_t launch_recipe_split_g(int G, dim3 grid, cudaStream_t stream, const DecodeArgs& a, const RecipeArgs& rc,
                                   const float* p_all, const DecodePlan& p, RecipeSplitView part) {
-  switch (G) {
-    case 1: decode_recipe_split_kernel<E, 1, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    case 2: decode_recipe_split_kernel<E, 2, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    case 4: decode_recipe_split_kernel<E, 4, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+  switch (G) {  // tensor-core tiles for up to four q heads per kv head, else the SIMT tiles
+    case 1: decode_recipe_tc_kernel<E, 1, MB0, MB1><<<grid, kRecTcWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    case 2: decode_recipe_tc_kernel<E, 2, MB0, MB1><<<grid, kRecTcWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+    case 4: decode_recipe_tc_kernel<E, 4, MB0, MB1><<<grid, kRecTcWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
     case 8: decode_recipe_split_kernel<E, 8, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
     default: return cudaErrorInvalidValue;
   }

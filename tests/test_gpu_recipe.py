@@ -136,7 +136,8 @@ def test_recipe_writer_bad_slot_and_empty_batch(tq):
 
 @pytest.mark.parametrize("recipe", RECIPES)
 @pytest.mark.parametrize("d,hq,h,bs,qdt", [(128, 32, 8, 16, np.float16), (128, 8, 8, 16, np.float32),
-                                           (64, 8, 4, 8, np.float32), (128, 16, 2, 32, np.float16)])
+                                           (64, 8, 4, 8, np.float32), (128, 16, 2, 32, np.float16),
+                                           (128, 8, 2, 12, np.float32)])
 def test_recipe_decode_matches_oracle(tq, recipe, d, hq, h, bs, qdt):
     rng = np.random.default_rng(77 + hq + d)
     lens = [0, 1, 37, 300, 1000]
@@ -215,3 +216,35 @@ def test_recipe_decode_bad_block_and_over_long_length(tq):
                               torch.from_numpy(bt).cuda(), torch.from_numpy(long).cuda(), order, gpu, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == tq.TQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("recipe", RECIPES)
+def test_recipe_decode_wide_value_norms(tq, recipe):
+    # value rows whose norms span 1e-3 .. 1e5 within every 16-token tile (the weights' power-of-
+    # two scale follows the largest value norm seen; no weight may leave fp16 range), keys of
+    # moderate norm so that many tokens carry weight; fp32 and fp16 queries
+    rng = np.random.default_rng(41)
+    d, hq, h, bs = 128, 8, 2, 16
+    lens = [700, 33, 16]
+    nblk, bt, slots = _layout(rng, lens, bs)
+    gpu, oc = codecs(tq, recipe, d)
+    t = slots.shape[0]
+    kraw = rng.standard_normal((t, h, d)) * 0.3
+    vraw = rng.standard_normal((t, h, d)) * 10.0 ** rng.uniform(-3.0, 5.0, (t, h, 1))
+    high = ro.calibrate_high_groups(kraw[:200], recipe)
+    rb = gpu.row_bytes
+    kp = ro.write_recipe_kv(kraw, np.zeros((nblk, bs, h, rb), np.uint8), slots, high, oc)
+    vp = ro.write_recipe_kv(vraw, np.zeros((nblk, bs, h, rb), np.uint8), slots, high, oc)
+    order = tq.tq_recipe_channel_order(recipe, d, high).cuda()
+    for qdt in (np.float32, np.float16):
+        q = rng.standard_normal((len(lens), hq, d)).astype(qdt)
+        st = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+        got = tq.tq_paged_decode_recipe(torch.from_numpy(q).cuda(), torch.from_numpy(kp).cuda(),
+                                        torch.from_numpy(vp).cuda(), torch.from_numpy(bt).cuda(),
+                                        torch.from_numpy(np.array(lens, np.int32)).cuda(), order, gpu,
+                                        out_dtype=torch.float32, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref = ro.paged_decode_recipe(q, kp, vp, bt, np.array(lens), high, oc)
+        assert np.abs(ref).max() > 1e3  # the large norms reach the output
+        assert_decode_close(got.cpu().numpy(), ref)
