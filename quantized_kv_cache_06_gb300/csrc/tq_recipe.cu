@@ -693,8 +693,11 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
 // per register, and the sign term from bytes of two tokens' sign words.  B = the weights
 // p nu 2^(12 - e) (values) and p nu gamma kappa 2^(12 - e) (signs), where 2^e bounds every
 // value norm the warp has seen (when e grows the accumulators are scaled by the same power of
-// two, exactly, with the softmax correction), so no weight leaves fp16 range.
+// two, exactly, with the softmax correction) and p <= 2^3 (the running max lags a score by
+// at most three log2 units), so no weight leaves fp16 range.
 constexpr int kRecTcWarps = 4;
+constexpr int kRecTcStages = 3;  // tiles staged per warp: the current one and two in flight
+constexpr float kRecSlack = 3.0f;  // log2 units the running max may lag behind a score
 
 __device__ __forceinline__ void rec_cp8(uint32_t dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
@@ -742,8 +745,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
   constexpr int rbw = kWh + E * MB1 + E + 2;  // words of a row
   constexpr bool kPairs = rbw % 2 == 0;       // rows, groups and (nu, gamma) 8-byte aligned
   static_assert(!kPairs || (kWh % 2 == 0 && (E * MB0 + E) % 2 == 0 && (E * MB1 + E) % 2 == 0), "alignment");
-  constexpr int kTok = 2 * rbw;    // staged words of one token: its K row, then its V row
-  constexpr int kBuf = 16 * kTok;  // one tile
+  constexpr int kBuf = 32 * rbw;  // one staged tile: the 16 K rows, then the 16 V rows
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, c = lane & 3;
@@ -754,7 +756,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
   __shared__ __align__(16) float qv[2][2][4][d];          // [q | p][group][q head][coordinate]
   __shared__ __align__(16) float pt[kRecTcWarps][4][16];  // the tile's weights [q head][token]
   __shared__ float red_ml[kRecTcWarps][G][2];
-  constexpr int kStageWords = kRecTcWarps * 2 * kBuf, kRedWords = kRecTcWarps * G * 2 * D;
+  constexpr int kStageWords = kRecTcWarps * kRecTcStages * kBuf, kRedWords = kRecTcWarps * G * 2 * D;
   // the warps' staged tiles, then (after the last tile) the merge buffer
   __shared__ __align__(16) uint32_t stage_u[kStageWords > kRedWords ? kStageWords : kRedWords];
   float(*red_acc)[G][2 * D] = reinterpret_cast<float(*)[G][2 * D]>(stage_u);
@@ -817,42 +819,59 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
   const unsigned char* tabs[2] = {reinterpret_cast<const unsigned char*>(&tab0[0][0]),
                                   reinterpret_cast<const unsigned char*>(&tab1[0][0])};
 
-  // staging: lane L copies the K (L < 16) or V row of token L mod 16
-  const uint32_t* stage_w = stage_u + warp * 2 * kBuf;
+  // staging: the lane (gr, c) copies chunks c, c + 4, ... of the K and V rows of its tokens
+  // gr and gr + 8 (the tokens it scores), so one copy instruction touches eight rows
+  const uint32_t* stage_w = stage_u + warp * kRecTcStages * kBuf;
   const uint32_t stage_base = smem_u32(stage_w);
-  const int tt = lane & 15, kv = lane >> 4;
-  const unsigned char* pages = kv ? a.v_pages : a.k_pages;
   const bool bs_pow2 = (bs & (bs - 1)) == 0;
   const int bs_shift = __ffs(bs) - 1;
   bool bad_block = false;
-  // Issues the copies of the tile at token t0 into buffer buf; returns its valid-token mask.
-  auto issue = [&](int t0, int buf) -> uint32_t {
-    const int t = t0 + tt;
-    bool ok = false;
-    int64_t row = 0;
-    if (t < t_hi) {
-      const int blk = bs_pow2 ? (t >> bs_shift) : t / bs;
-      const int bid = __ldg(a.block_table + (int64_t)b * a.max_blocks_per_seq + blk);
-      if (bid < 0 || (int64_t)bid >= a.num_blocks) {
-        bad_block = true;
-      } else {
-        ok = true;
-        row = ((int64_t)bid * bs + (t - blk * bs)) * H + h;
+  // Block id of this lane's token gr + 8 r of the tile at t0 (loaded an iteration before its
+  // copies; -1 past the end).
+  auto load_bid = [&](int t0, int r) -> int {
+    const int t = t0 + gr + 8 * r;
+    if (t >= t_hi) return -1;
+    return __ldg(a.block_table + (int64_t)b * a.max_blocks_per_seq + (bs_pow2 ? (t >> bs_shift) : t / bs));
+  };
+  // Issues the copies of the tile at token t0 into buffer buf and commits them as one group;
+  // returns bit r set when token gr + 8 r is valid (rows of other tokens are zero-filled).
+  auto issue = [&](int t0, int bid0, int bid1, int buf) -> uint32_t {
+    uint32_t okm = 0u;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = t0 + gr + 8 * r;
+      const int bid = r ? bid1 : bid0;
+      bool ok = false;
+      int64_t row = 0;
+      if (t < t_hi) {
+        const int blk = bs_pow2 ? (t >> bs_shift) : t / bs;
+        if (bid < 0 || (int64_t)bid >= a.num_blocks) {
+          bad_block = true;
+        } else {
+          ok = true;
+          row = ((int64_t)bid * bs + (t - blk * bs)) * H + h;
+        }
+      }
+      okm |= ok ? (1u << r) : 0u;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const unsigned char* src = (kv ? a.v_pages : a.k_pages) + row * (int64_t)(4 * rbw);
+        const uint32_t dst = stage_base + (uint32_t)((buf * 32 + kv * 16 + gr + 8 * r) * rbw) * 4u;
+        if constexpr (kPairs) {
+          const uint32_t nb = ok ? 8u : 0u;
+#pragma unroll
+          for (int k = 0; k < (rbw / 2 + 3) / 4; ++k)
+            if (c + 4 * k < rbw / 2) rec_cp8(dst + 8 * (c + 4 * k), src + 8 * (c + 4 * k), nb);
+        } else {
+          const uint32_t nb = ok ? 4u : 0u;
+#pragma unroll
+          for (int k = 0; k < (rbw + 3) / 4; ++k)
+            if (c + 4 * k < rbw) rec_cp4(dst + 4 * (c + 4 * k), src + 4 * (c + 4 * k), nb);
+        }
       }
     }
-    const unsigned char* src = pages + row * (int64_t)(4 * rbw);
-    const uint32_t dst = stage_base + (uint32_t)((buf * 16 + tt) * kTok + kv * rbw) * 4u;
-    if constexpr (kPairs) {
-      const uint32_t nb = ok ? 8u : 0u;
-#pragma unroll
-      for (int k = 0; k < rbw / 2; ++k) rec_cp8(dst + 8 * k, src + 8 * k, nb);
-    } else {
-      const uint32_t nb = ok ? 4u : 0u;
-#pragma unroll
-      for (int k = 0; k < rbw; ++k) rec_cp4(dst + 4 * k, src + 4 * k, nb);
-    }
     rec_cp_commit();
-    return __ballot_sync(kFullMask, ok) & 0xffffu;
+    return okm;
   };
 
   float ov[2][2 * E][4], oz[2][2 * E][4];  // value accumulators: rows coordinates, columns heads
@@ -865,20 +884,26 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // q heads 2 (c mod 2) + e
   int e_run = -115;  // every value norm seen so far is below 2^e_run
 
+  static_assert(kRecTcStages == 3, "the flags of the tiles in flight are held in vm0, vm1");
+  constexpr int kStep = 16 * kRecTcWarps;
   int t0 = t_lo + 16 * warp;
-  uint32_t vm = t0 < t_hi ? issue(t0, 0) : 0u;
-  for (int it = 0; t0 < t_hi; ++it, t0 += 16 * kRecTcWarps) {
-    const int buf = it & 1;
-    const int tn = t0 + 16 * kRecTcWarps;
-    uint32_t vm_next = 0u;
-    if (tn < t_hi) {
-      vm_next = issue(tn, buf ^ 1);
-      rec_cp_wait<1>();
-    } else {
-      rec_cp_wait<0>();
-    }
+  // prologue: tiles 0 and 1 (a group is committed for each, empty past the end)
+  uint32_t vm0 = 0u, vm1 = 0u;
+  if (t0 < t_hi) vm0 = issue(t0, load_bid(t0, 0), load_bid(t0, 1), 0); else rec_cp_commit();
+  if (t0 + kStep < t_hi) vm1 = issue(t0 + kStep, load_bid(t0 + kStep, 0), load_bid(t0 + kStep, 1), 1); else rec_cp_commit();
+  int bid_n0 = load_bid(t0 + 2 * kStep, 0), bid_n1 = load_bid(t0 + 2 * kStep, 1);
+  int buf = 0;
+  for (; t0 < t_hi; t0 += kStep) {
+    const int tn = t0 + 2 * kStep;
+    const int bufn = buf == 0 ? 2 : buf - 1;  // (buf + 2) mod 3
+    uint32_t vmn = 0u;
+    if (tn < t_hi) vmn = issue(tn, bid_n0, bid_n1, bufn); else rec_cp_commit();
+    bid_n0 = load_bid(tn + kStep, 0);  // used by the next iteration's copies
+    bid_n1 = load_bid(tn + kStep, 1);
+    rec_cp_wait<kRecTcStages - 1>();  // this tile's group is complete
     __syncwarp();
     const uint32_t* tile = stage_w + buf * kBuf;
+    const uint32_t vm = vm0;
 
     // ---- scores of tokens gr + 8 r, q heads 2 (c mod 2) + e (this lane's column part) ----
     float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
@@ -890,7 +915,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
       float nk[2], gk[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const uint32_t* kr = tile + (gr + 8 * r) * kTok + goff;
+        const uint32_t* kr = tile + (gr + 8 * r) * rbw + goff;
 #pragma unroll
         for (int q = 0; q < E; ++q) {  // coordinates [8E c + 8 q, + 8)
           const int bit = (8 * E * c + 8 * q) * MB;
@@ -928,10 +953,12 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         sc[r][e] += __shfl_xor_sync(kFullMask, sc[r][e], 2);
-        if (!((vm >> (gr + 8 * r)) & 1u)) sc[r][e] = -INFINITY;
+        if (!((vm >> r) & 1u)) sc[r][e] = -INFINITY;
       }
 
-    // ---- the tile's softmax step ----
+    // ---- the tile's softmax step: the running max moves only when a score passes it by
+    // more than kRecSlack (so p <= 2^kRecSlack and, with the value scale, every weight stays
+    // below 2^15), and the accumulators are rescaled only then ----
     float corr[2], p[2][2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -939,16 +966,17 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
       tm = fmaxf(tm, __shfl_xor_sync(kFullMask, tm, 4));
       tm = fmaxf(tm, __shfl_xor_sync(kFullMask, tm, 8));
       tm = fmaxf(tm, __shfl_xor_sync(kFullMask, tm, 16));
-      const float mn = fmaxf(m_run[e], tm);
       corr[e] = 1.f;
+      if (tm > m_run[e] + kRecSlack) {  // (never for a tile without tokens: tm = -inf)
+        corr[e] = exp2f(m_run[e] - tm);  // 0 while m is -inf
+        m_run[e] = tm;
+      }
       p[0][e] = p[1][e] = 0.f;
-      if (mn != -INFINITY) {  // some token of this or an earlier tile
-        corr[e] = exp2f(m_run[e] - mn);
-        p[0][e] = exp2f(sc[0][e] - mn);
-        p[1][e] = exp2f(sc[1][e] - mn);
+      if (m_run[e] != -INFINITY) {  // some token of this or an earlier tile
+        p[0][e] = exp2f(sc[0][e] - m_run[e]);
+        p[1][e] = exp2f(sc[1][e] - m_run[e]);
       }
       l_run[e] = fmaf(l_run[e], corr[e], p[0][e] + p[1][e]);
-      m_run[e] = mn;
     }
     if (c < 2) {
 #pragma unroll
@@ -962,7 +990,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
     float vmax = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t* vr = tile + (2 * c + (k & 1) + 8 * (k >> 1)) * kTok + rbw;
+      const uint32_t* vr = tile + (16 + 2 * c + (k & 1) + 8 * (k >> 1)) * rbw;
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
         const int w = (grp ? kWh + E * MB1 : E * MB0) + E;
@@ -1027,7 +1055,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
       uint32_t chv[4], sw[4][E];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t* vr = tile + (2 * c + (k & 1) + 8 * (k >> 1)) * kTok + rbw + goff;
+        const uint32_t* vr = tile + (16 + 2 * c + (k & 1) + 8 * (k >> 1)) * rbw + goff;
         chv[k] = __funnelshift_r(vr[bitv >> 5], vr[(bitv >> 5) + 1], bitv & 31);
 #pragma unroll
         for (int w = 0; w < E; ++w) sw[k][w] = vr[IW + w];
@@ -1051,9 +1079,12 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
                 rec_sign2(z23 << (7 - gr)), bz[grp][0], bz[grp][1]);
       }
     }
-    __syncwarp();  // the next tile rewrites pt and this buffer
-    vm = vm_next;
+    __syncwarp();  // the next tile rewrites pt; the one after it this buffer
+    vm0 = vm1;
+    vm1 = vmn;
+    buf = buf == 2 ? 0 : buf + 1;
   }
+  rec_cp_wait<0>();  // (the trailing groups are empty)
   if (__any_sync(kFullMask, bad_block) && lane == 0 && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
   __syncthreads();  // every warp is done with its staged rows: the merge buffer may be written
 
