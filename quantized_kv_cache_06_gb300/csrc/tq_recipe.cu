@@ -52,7 +52,7 @@
 namespace tq {
 namespace {
 
-constexpr int kRecWarps = 8;
+constexpr int kRecWarps = 4;
 constexpr int kRecDecodeWarps = 4;
 constexpr float kRecLog2e = 1.4426950408889634f;
 constexpr float kRecSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi / 2)
@@ -61,15 +61,20 @@ constexpr float kRecSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi / 2)
 // nu, gamma.
 __host__ __device__ constexpr int group_words(int d, int bits) { return d * (bits - 1) / 32 + d / 32 + 2; }
 
-// Units (row, group) are taken sixteen at a time per warp (eight rows, both groups), in
-// batches of four: each unit's gather, norm, rotation, indices and residual (the four units'
-// loads issued together, their reductions interleaved), the residual r stored into the warp's
-// A tile as fp16 hi = r 2^10 and lo = (r 2^10 - hi) 2^12.  Then the sketch S_d r of the
-// sixteen on the tensor cores (m16n8k16): r_hi S_hi into one accumulator, r_lo S_hi +
-// r_hi S_lo into another (~22 significant bits, as in an fp32 sum), and each sign word from
-// ballots of the accumulators, assembled by one lane.
-constexpr int kRecUnits = 16;
-constexpr int kRecBatch = 4;
+// Rows (token, kv head) are taken 32 at a time per warp, all of one kv head.  The warp stages
+// the 32 raw rows in shared memory (4-byte cp.async copies; rows an odd number of words apart,
+// so that a lane per row reads any column without bank conflicts), then encodes group 0 and
+// group 1 in turn with a lane per row: the gather of the group's d channels through the
+// channel order (the head's order bytes broadcast from shared memory), the sign flip as a
+// sign-bit XOR, the d-point FWHT in registers (the stage order of the warp transform), the
+// norm, the indices (a count of the decision points below the coordinate, held in registers),
+// their packing, and the residual r, stored as fp16 hi = r 2^10 and lo = (r 2^10 - hi) 2^12.
+// The residuals go to the warp's A tile sixteen at a time, and the sketch S_d r of the sixteen
+// runs as m16n8k16 MMAs: r_hi S_hi into one accumulator, r_lo S_hi + r_hi S_lo into another
+// (~22 significant bits, as in an fp32 sum), each sign word assembled from ballots of the
+// accumulators.  Each lane then writes its unit's group words (indices, signs, nu, gamma).
+constexpr int kRecRows = 32;   // rows per warp tile
+constexpr int kRecUnits = 16;  // units per sketch pass
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -93,9 +98,12 @@ __device__ __forceinline__ uint32_t spread_nibble(uint32_t x) {
   return (x | (x << 1)) & 0x55u;
 }
 
-// Shared memory of the writer: S hi and lo, then per warp its A tile hi and lo; rows of
-// d + 8 halves (16 bytes of padding put the 8 rows of an ldmatrix in different banks).
-__host__ __device__ constexpr int recipe_write_smem(int d) { return (2 * d + kRecWarps * 2 * kRecUnits) * (d + 8) * 2; }
+// Shared memory of the writer: S hi and lo, then per warp its A tile hi and lo (rows of d + 8
+// halves: 16 bytes of padding put the 8 rows of an ldmatrix in different banks), then per warp
+// its staged raw rows (stride raw_words + 1 words) and its head's D order bytes.
+__host__ __device__ constexpr int recipe_write_smem(int d, int raw_words) {
+  return (2 * d + kRecWarps * 2 * kRecUnits) * (d + 8) * 2 + kRecWarps * (kRecRows * (raw_words + 1) * 4 + 2 * d);
+}
 
 // idx = #{k : b_k < y} over the 2^MB - 1 decision points held in registers (ties and NaN: the
 // lower index)
@@ -107,25 +115,32 @@ __device__ __forceinline__ int rec_index(float y, const float (&b)[7]) {
   return idx;
 }
 
+__device__ __forceinline__ void rec_cp4w(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
+template <typename T>
+__device__ __forceinline__ float rec_raw_at(const uint32_t* row, int ch) {
+  return to_f32<T>(reinterpret_cast<const T*>(row)[ch]);
+}
+
 // MB0 / MB1: MSE index bits of the high / low group.
 template <typename T, int E, int MB0, int MB1>
 __global__ void __launch_bounds__(kRecWarps * 32, 3)
-write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_heads, const int64_t* __restrict__ slots,
+write_recipe_kernel(const T* __restrict__ raw, int64_t num_tokens, int num_kv_heads, const int64_t* __restrict__ slots,
                     uint8_t* __restrict__ pages, RecipeArgs rc, const float* __restrict__ signs,
                     const int32_t* __restrict__ status) {
   constexpr int d = 32 * E, D = 2 * d;
-  constexpr int kUnitWords = 3 * E + E + 2;  // largest group: 3-bit indices, signs, nu, gamma
   constexpr int kRow = d + 8;
+  constexpr int kRawWords = D * (int)sizeof(T) / 4;  // words of one raw row
+  constexpr int kRS = kRawWords + 1;
+  constexpr int kWh = group_words(d, MB0 + 1);
+  constexpr int kRowWords = kWh + group_words(d, MB1 + 1);
   extern __shared__ __align__(16) unsigned char rec_smem[];
   __half* s_hi = reinterpret_cast<__half*>(rec_smem);  // S[i][j] (i: projection, j: coordinate)
   __half* s_lo = s_hi + d * kRow;                       // (S - hi) 2^12
   __shared__ float cen[2][8];
-  __shared__ uint32_t rowbuf[kRecWarps][kRecUnits][kUnitWords];
-  __shared__ int64_t slot_s[kRecWarps][kRecUnits];
-  __shared__ int head_s[kRecWarps][kRecUnits];
 
-  const int tid = threadIdx.x;
-  constexpr int mb0 = MB0, mb1 = MB1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int nc0 = 1 << MB0, nc1 = 1 << MB1;
   // the decision points of both groups, in registers
   float bhi[7], blo[7];
@@ -143,17 +158,19 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_head
     s_hi[i * kRow + j] = hi;
     s_lo[i * kRow + j] = __float2half_rn((sv - __half2float(hi)) * 4096.0f);
   }
+  // the signs of R_d as bits (bit j of word w: coordinate 32 w + j negative)
+  uint32_t sgm[E];
+#pragma unroll
+  for (int w = 0; w < E; ++w) sgm[w] = __ballot_sync(kFullMask, __ldg(signs + 32 * w + lane) < 0.f);
   __syncthreads();
   if (*status != kOk) return;  // a slot failed validation: write nothing
 
-  const int warp = tid >> 5, lane = tid & 31;
-  const int row_words = group_words(d, rc.bits_hi) + group_words(d, rc.bits_lo);
   const float inv_sqrt_d = 1.0f / sqrtf((float)d);
-  float sg[E];
-#pragma unroll
-  for (int i = 0; i < E; ++i) sg[i] = __ldg(signs + lane * E + i);
   __half* a_hi = s_lo + d * kRow + warp * (2 * kRecUnits * kRow);  // this warp's A tile: unit k, coordinate j
   __half* a_lo = a_hi + kRecUnits * kRow;
+  uint32_t* raw_s = reinterpret_cast<uint32_t*>(rec_smem + (size_t)(2 * d + kRecWarps * 2 * kRecUnits) * kRow * 2) +
+                    warp * (kRecRows * kRS + D / 4);
+  uint32_t* ord_s = raw_s + kRecRows * kRS;  // the tile's head: its D channel-order bytes
   // ldmatrix lane addresses: A rows (units) lane & 15, k half lane >> 4; B rows (projections)
   // (lane & 7) + 8 (lane >> 4), k half (lane >> 3) & 1
   const uint32_t a_lane = smem_u32(a_hi) + (uint32_t)(((lane & 15) * kRow + (lane >> 4) * 8) * 2);
@@ -161,110 +178,33 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_head
   const uint32_t b_lane = smem_u32(s_hi) + (uint32_t)((((lane & 7) + 8 * (lane >> 4)) * kRow + ((lane >> 3) & 1) * 8) * 2);
   const uint32_t b_lo_off = (uint32_t)(d * kRow * 2);
 
-  const int64_t units = 2 * num_rows;
-  const int64_t ustride = (int64_t)gridDim.x * kRecWarps * kRecUnits;
-  for (int64_t u0 = ((int64_t)blockIdx.x * kRecWarps + warp) * kRecUnits; u0 < units; u0 += ustride) {
-#pragma unroll 1
-    for (int q = 0; q < kRecUnits / kRecBatch; ++q) {
-      const int64_t ub = u0 + kRecBatch * q;  // units ub .. ub + 3: rows r0, r0 + 1, both groups
-      int64_t slot_k[kRecBatch];
-      float nu_k[kRecBatch], gamma_k[kRecBatch];
-      float v[kRecBatch][E];
-      const int64_t r0 = ub >> 1;
-      const int64_t t0 = r0 / num_kv_heads;
-      const int h0 = (int)(r0 - t0 * num_kv_heads);
-      const bool wrap = h0 + 1 == num_kv_heads;
-      const int64_t t1 = wrap ? t0 + 1 : t0;
-      const int h1 = wrap ? 0 : h0 + 1;
-#pragma unroll
-      for (int k = 0; k < kRecBatch; ++k) {
-        const int64_t u = ub + k;
-        const int64_t r = r0 + (k >> 1);
-        const int g = k & 1;
-        const int64_t t = (k >> 1) ? t1 : t0;
-        const int h = (k >> 1) ? h1 : h0;
-        slot_k[k] = u < units ? __ldg(slots + t) : -1;
-        const int32_t* ord = rc.order + (int64_t)h * D + g * d + lane * E;
-#pragma unroll
-        for (int i = 0; i < E; ++i) v[k][i] = u < units ? to_f32<T>(raw[r * D + __ldg(ord + i)]) : 0.f;
-        if (lane == 0) {
-          slot_s[warp][kRecBatch * q + k] = slot_k[k];
-          head_s[warp][kRecBatch * q + k] = h;
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kRecBatch; ++k) {
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < E; ++i) ss = fmaf(v[k][i], v[k][i], ss);
-        nu_k[k] = ss;
-      }
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1)
-#pragma unroll
-        for (int k = 0; k < kRecBatch; ++k) nu_k[k] += __shfl_xor_sync(kFullMask, nu_k[k], m);
-#pragma unroll
-      for (int k = 0; k < kRecBatch; ++k) {
-        nu_k[k] = sqrtf(nu_k[k]);
-#pragma unroll
-        for (int i = 0; i < E; ++i) v[k][i] *= sg[i];
-        fwht_warp<E>(v[k]);
-      }
-#pragma unroll
-      for (int k = 0; k < kRecBatch; ++k) {
-        const int g = k & 1;
-        const int uk = kRecBatch * q + k;
-        uint32_t* buf = rowbuf[warp][uk];
-        __half* arow_hi = a_hi + uk * kRow + lane * E;
-        __half* arow_lo = a_lo + uk * kRow + lane * E;
-        gamma_k[k] = 0.f;
-        if (slot_k[k] < 0) {  // "Slot Mapping": negative slots are ignored (zero residual)
-#pragma unroll
-          for (int i = 0; i < E; ++i) arow_hi[i] = arow_lo[i] = __float2half_rn(0.f);
-          continue;
-        }
-        const int mb = g ? mb1 : mb0;
-        const float nu = nu_k[k];
-        const float inv = nu > 0.f ? inv_sqrt_d / nu : 0.f;  // y = H(s*x)/(sqrt(d) nu)
+  // finished rows of a tile, staged in the A tile (free once the second group's sketch is done)
+  constexpr int kOutStride = kRowWords | 1;
+  static_assert(kRecRows * kOutStride * 4 <= 2 * kRecUnits * kRow * 2, "the tile's rows fit in the A tile");
+  uint32_t* out_s = reinterpret_cast<uint32_t*>(a_hi);
 
-        const int index_words = d * mb / 32;
-        for (int w = lane; w < index_words; w += 32) buf[w] = 0u;
-        __syncwarp();
-        float rs = 0.f;
+  const int64_t ntb = (num_tokens + kRecRows - 1) / kRecRows;
+  const int64_t tiles = ntb * num_kv_heads;
+  const int64_t tstride = (int64_t)gridDim.x * kRecWarps;
+  // Stages tile tl (its head's order bytes, its raw rows) and commits the copies as one group.
+  auto stage = [&](int64_t tl) {
+    const int64_t tb = tl / num_kv_heads;
+    const int h = (int)(tl - tb * num_kv_heads);
+    const int64_t t0 = tb * kRecRows;
+    const int nrows = (int)min((int64_t)kRecRows, num_tokens - t0);
+    for (int i = lane; i < D; i += 32) reinterpret_cast<uint8_t*>(ord_s)[i] = (uint8_t)__ldg(rc.order + (int64_t)h * D + i);
+    const uint32_t dst0 = smem_u32(raw_s);
+    for (int r = 0; r < nrows; ++r) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(raw + ((t0 + r) * num_kv_heads + h) * D);
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
-          const float y = v[k][i] * inv;
-          const int idx = g ? rec_index<MB1>(y, blo) : rec_index<MB0>(y, bhi);
-          const int bit = (lane * E + i) * mb;
-          const int w = bit >> 5, o = bit & 31;
-          atomicOr(&buf[w], (uint32_t)idx << o);
-          if (o + mb > 32) atomicOr(&buf[w + 1], (uint32_t)idx >> (32 - o));
-          const float dr = y - cen[g][idx];
-          rs = fmaf(dr, dr, rs);
-          const float x = dr * 1024.0f;
-          const __half xh = __float2half_rn(x);
-          arow_hi[i] = xh;
-          arow_lo[i] = __float2half_rn((x - __half2float(xh)) * 4096.0f);
-        }
-        gamma_k[k] = rs;
-      }
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1)
-#pragma unroll
-        for (int k = 0; k < kRecBatch; ++k) gamma_k[k] += __shfl_xor_sync(kFullMask, gamma_k[k], m);
-      if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < kRecBatch; ++k) {
-          if (slot_k[k] < 0) continue;
-          const int iw = d * ((k & 1) ? mb1 : mb0) / 32;
-          rowbuf[warp][kRecBatch * q + k][iw + E] = __float_as_uint(nu_k[k]);
-          rowbuf[warp][kRecBatch * q + k][iw + E + 1] = __float_as_uint(sqrtf(gamma_k[k]));
-        }
-      }
+      for (int w = lane; w < kRawWords; w += 32) rec_cp4w(dst0 + (uint32_t)(r * kRS + w) * 4u, src + w);
     }
-    __syncwarp();
-    // ---- sketch of the sixteen residuals: sign word e holds projections 32 e .. 32 e + 31
-    // (n-tiles 4 e .. 4 e + 3); lane u < 16 assembles unit u's word
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+
+  // The sketch of the sixteen units of pass p held in the A tile: sign word e of unit 16 p + u
+  // is kept by lane 16 p + u.
+  auto sketch = [&](int p, uint32_t (&sw)[E]) {
     const int u = lane & 15, ur = u & 7, uh = u >> 3;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -302,20 +242,137 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_rows, int num_kv_head
             if ((x >> 1) == uh) word |= spread_nibble((bal >> (4 * ur)) & 15u) << (8 * (2 * np + n) + (x & 1));
           }
       }
-      if (lane < 16 && slot_s[warp][u] >= 0) rowbuf[warp][u][d * ((u & 1) ? mb1 : mb0) / 32 + e] = word;
+      if ((lane >> 4) == p) sw[e] = word;
     }
+  };
+
+  int64_t tl = (int64_t)blockIdx.x * kRecWarps + warp;
+  if (tl < tiles) stage(tl);
+  for (; tl < tiles; tl += tstride) {
+    const int64_t tb = tl / num_kv_heads;
+    const int h = (int)(tl - tb * num_kv_heads);
+    const int64_t t0 = tb * kRecRows;
+    const bool valid = t0 + lane < num_tokens;
+    const int64_t slot = valid ? __ldg(slots + t0 + lane) : -1;
+    const bool live = slot >= 0;  // "Slot Mapping": negative slots are ignored
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     __syncwarp();
-    for (int k = 0; k < kRecUnits; ++k) {
-      const int64_t slot = slot_s[warp][k];
-      if (slot < 0) continue;  // (the same on every lane)
-      const int g = k & 1;
-      const int gw = d * (g ? mb1 : mb0) / 32 + E + 2;
-      uint32_t* dst = reinterpret_cast<uint32_t*>(pages + (slot * num_kv_heads + head_s[warp][k]) * (int64_t)(row_words * 4)) +
-                      (g ? group_words(d, rc.bits_hi) : 0);
-      for (int w = lane; w < gw; w += 32) dst[w] = rowbuf[warp][k][w];
+    const uint32_t* rrow = raw_s + lane * kRS;
+    uint32_t gw0[E * MB0 + E + 2];  // the first group's words, held until the row is written
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const int mb = g ? MB1 : MB0;
+      float y[d];
+      // gather of the group's channels (this lane's row), sign flip, norm (eight partial sums
+      // of squares, added as a tree)
+      float ssp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j4 = 0; j4 < d / 4; ++j4) {
+        const uint32_t o4 = ord_s[g * (d / 4) + j4];  // (the same word on every lane)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = 4 * j4 + q;
+          const float x = live ? rec_raw_at<T>(rrow, (int)((o4 >> (8 * q)) & 255u)) : 0.f;
+          ssp[j & 7] = fmaf(x, x, ssp[j & 7]);
+          y[j] = __uint_as_float(__float_as_uint(x) ^ ((sgm[j >> 5] << (31 - (j & 31))) & 0x80000000u));
+        }
+      }
+      if (g == 1) {  // the raw tile is consumed: stage the next tile behind this group's encode
+        __syncwarp();
+        if (tl + tstride < tiles) stage(tl + tstride);
+      }
+      // y = H (s * x) / (sqrt(d) nu): the d-point FWHT in registers
+#pragma unroll
+      for (int hs = 1; hs < d; hs <<= 1)
+#pragma unroll
+        for (int i = 0; i < d; ++i)
+          if ((i & hs) == 0) {
+            const float p0 = y[i], p1 = y[i + hs];
+            y[i] = p0 + p1;
+            y[i + hs] = p0 - p1;
+          }
+      const float nu = sqrtf(((ssp[0] + ssp[1]) + (ssp[2] + ssp[3])) + ((ssp[4] + ssp[5]) + (ssp[6] + ssp[7])));
+      const float inv = nu > 0.f ? inv_sqrt_d / nu : 0.f;
+      // indices (packed LSB first), residual (fp16 hi / lo pairs), gamma^2
+      constexpr int kIW = E * (MB0 > MB1 ? MB0 : MB1);
+      uint32_t iw[kIW];
+#pragma unroll
+      for (int w = 0; w < kIW; ++w) iw[w] = 0u;
+      uint32_t rh[d / 2], rl[d / 2];
+      float rsp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < d; ++j) {
+        const float yv = y[j] * inv;
+        const int idx = g ? rec_index<MB1>(yv, blo) : rec_index<MB0>(yv, bhi);
+        const int bit = j * mb, w = bit >> 5, o = bit & 31;
+        iw[w] |= (uint32_t)idx << o;
+        if (o + mb > 32) iw[w + 1] |= (uint32_t)idx >> (32 - o);
+        const float dr = yv - cen[g][idx];
+        rsp[j & 3] = fmaf(dr, dr, rsp[j & 3]);
+        const float x = dr * 1024.0f;
+        const __half xh = __float2half_rn(x);
+        const __half xl = __float2half_rn((x - __half2float(xh)) * 4096.0f);
+        const uint32_t bh = live ? (uint32_t)__half_as_ushort(xh) : 0u, bl = live ? (uint32_t)__half_as_ushort(xl) : 0u;
+        if (j & 1) {
+          rh[j >> 1] |= bh << 16;
+          rl[j >> 1] |= bl << 16;
+        } else {
+          rh[j >> 1] = bh;
+          rl[j >> 1] = bl;
+        }
+      }
+      // the sketch, sixteen units per pass
+      uint32_t sw[E];
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        if ((lane >> 4) == pass) {
+          uint4* dh = reinterpret_cast<uint4*>(a_hi + (lane & 15) * kRow);
+          uint4* dl = reinterpret_cast<uint4*>(a_lo + (lane & 15) * kRow);
+#pragma unroll
+          for (int k = 0; k < d / 8; ++k) {
+            dh[k] = make_uint4(rh[4 * k], rh[4 * k + 1], rh[4 * k + 2], rh[4 * k + 3]);
+            dl[k] = make_uint4(rl[4 * k], rl[4 * k + 1], rl[4 * k + 2], rl[4 * k + 3]);
+          }
+        }
+        __syncwarp();
+        sketch(pass, sw);
+        __syncwarp();  // the A tile is rewritten by the next pass
+      }
+      const int iwn = E * mb;
+      if (g == 0) {
+#pragma unroll
+        for (int w = 0; w < E * MB0; ++w) gw0[w] = iw[w];
+#pragma unroll
+        for (int e = 0; e < E; ++e) gw0[E * MB0 + e] = sw[e];
+        gw0[E * MB0 + E] = __float_as_uint(nu);
+        gw0[E * MB0 + E + 1] = __float_as_uint(sqrtf((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])));
+      } else {
+        // this lane's row into the staging rows, then the tile's rows written with lanes over
+        // consecutive words
+        uint32_t* orow = out_s + lane * kOutStride;
+#pragma unroll
+        for (int w = 0; w < kWh; ++w) orow[w] = gw0[w];
+#pragma unroll
+        for (int w = 0; w < E * MB1; ++w) orow[kWh + w] = iw[w];
+#pragma unroll
+        for (int e = 0; e < E; ++e) orow[kWh + iwn + e] = sw[e];
+        orow[kWh + iwn + E] = __float_as_uint(nu);
+        orow[kWh + iwn + E + 1] = __float_as_uint(sqrtf((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])));
+        __syncwarp();
+#pragma unroll 2
+        for (int q = lane; q < kRecRows * kRowWords; q += 32) {
+          const int r = q / kRowWords, w = q - r * kRowWords;
+          const int64_t sr = __shfl_sync(kFullMask, slot, r);
+          if (sr >= 0) {
+            uint32_t* dst = reinterpret_cast<uint32_t*>(pages + (sr * num_kv_heads + h) * (int64_t)(kRowWords * 4));
+            dst[w] = out_s[r * kOutStride + w];
+          }
+        }
+        __syncwarp();  // the A tile is the next tile's again
+      }
     }
-    __syncwarp();
   }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
 // p[row][g][i] = sum_j S[i][j] q_g[j], q_g = R_d q[row][order_g] times the softmax scale
@@ -1182,15 +1239,19 @@ combine_recipe_kernel(DecodeArgs a, RecipeArgs rc, int num_splits, RecipeSplitVi
 template <typename T, int E, int MB0, int MB1>
 cudaError_t launch_write_recipe_mb(const WriteArgs& a, const RecipeArgs& rc, cudaStream_t stream, int num_sms) {
   constexpr int d = 32 * E;
-  const int64_t units = 2 * a.num_tokens * a.num_kv_heads;
-  const int64_t per_cta = (int64_t)kRecWarps * kRecUnits;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((units + per_cta - 1) / per_cta, (int64_t)num_sms * 3));
-  const size_t smem = (size_t)recipe_write_smem(d);
+  const int64_t tiles = (a.num_tokens + kRecRows - 1) / kRecRows * a.num_kv_heads;
+  const int64_t per_cta = kRecWarps;
+  const int64_t want = (tiles + per_cta - 1) / per_cta;
+  const size_t smem = (size_t)recipe_write_smem(d, 2 * d * (int)sizeof(T) / 4);
   auto kern = write_recipe_kernel<T, E, MB0, MB1>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<grid, kRecWarps * 32, smem, stream>>>(static_cast<const T*>(a.raw), a.num_tokens * a.num_kv_heads,
-                                               a.num_kv_heads, a.slots, a.pages, rc, a.signs, a.status);
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRecWarps * 32, smem);
+  if (err != cudaSuccess) return err;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * std::max(1, per_sm)));
+  kern<<<grid, kRecWarps * 32, smem, stream>>>(static_cast<const T*>(a.raw), a.num_tokens, a.num_kv_heads, a.slots,
+                                               a.pages, rc, a.signs, a.status);
   err = cudaGetLastError();
   if (err == cudaSuccess) count_launches(1);
   return err;
