@@ -1,5 +1,5 @@
 // Recipe cache modes turboquant25 / turboquant35: grouped product-quantised rows, writer
-// and paged decode (sm_103a, SIMT).
+// and paged decode (sm_103a: m16n8k16 MMAs for the sketch, the scores and the values).
 //
 // TurboQuant docs: "vLLM Usage" (Cache Dtypes: turboquant25 and turboquant35, recipe
 // modes require metadata; Metadata Validation Rules; Page Geometry: recipe row bytes) and
@@ -19,14 +19,19 @@
 // by K and V, which both use recipe rows.
 //
 // Kernels:
-//   write_recipe_kernel        a warp per sixteen (token, head, group) units: channel gather,
-//                              norm, rotation (warp FWHT), indices and residual of each, then
-//                              the sketch of the sixteen as m16n8k16 MMAs (fp16 hi / lo
-//                              splits of r and S_d) and the sign words from ballots.
+//   write_recipe_kernel        32 staged rows of one kv head per warp, a lane per (row, group)
+//                              unit: channel gather, norm, rotation (FWHT in registers),
+//                              indices and residual; then the sketch of sixteen units at a
+//                              time as m16n8k16 MMAs (fp16 hi / lo splits of r and S_d) and
+//                              the sign words from ballots.
 //   recipe_project_kernel      one warp per (sequence, q head): per group the rotated
 //                              gathered query q_g = R_d q[order_g] (times the softmax scale
 //                              and log2 e) and its projection p_g = S_d q_g.
-//   decode_recipe_split_kernel the SIMT split decode, 32-token tiles per warp: scores with
+//   decode_recipe_tc_kernel    the split decode for up to four q heads per kv head: 16-token
+//                              tiles staged by cp.async, scores and values as m16n8k16 MMAs
+//                              (pair tables of centroids, +-1 sign operands).
+//   decode_recipe_split_kernel the SIMT split decode (eight q heads per kv head), 32-token
+//                              tiles per warp: scores with
 //                              a lane per token (every q head at once), one softmax step
 //                              per tile, values with lanes over coordinates.  Score of key
 //                              row k:
