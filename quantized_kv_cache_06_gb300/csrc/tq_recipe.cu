@@ -277,7 +277,7 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_tokens, int num_kv_he
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int j = 4 * j4 + q;
-          const float x = live ? rec_raw_at<T>(rrow, (int)((o4 >> (8 * q)) & 255u)) : 0.f;
+          const float x = live ? rec_raw_at<T>(rrow, (int)__byte_perm(o4, 0u, 0x4440u + q)) : 0.f;
           ssp[j & 7] = fmaf(x, x, ssp[j & 7]);
           y[j] = __uint_as_float(__float_as_uint(x) ^ ((sgm[j >> 5] << (31 - (j & 31))) & 0x80000000u));
         }
@@ -306,25 +306,26 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_tokens, int num_kv_he
       uint32_t rh[d / 2], rl[d / 2];
       float rsp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < d; ++j) {
-        const float yv = y[j] * inv;
-        const int idx = g ? rec_index<MB1>(yv, blo) : rec_index<MB0>(yv, bhi);
-        const int bit = j * mb, w = bit >> 5, o = bit & 31;
-        iw[w] |= (uint32_t)idx << o;
-        if (o + mb > 32) iw[w + 1] |= (uint32_t)idx >> (32 - o);
-        const float dr = yv - cen[g][idx];
-        rsp[j & 3] = fmaf(dr, dr, rsp[j & 3]);
-        const float x = dr * 1024.0f;
-        const __half xh = __float2half_rn(x);
-        const __half xl = __float2half_rn((x - __half2float(xh)) * 4096.0f);
-        const uint32_t bh = live ? (uint32_t)__half_as_ushort(xh) : 0u, bl = live ? (uint32_t)__half_as_ushort(xl) : 0u;
-        if (j & 1) {
-          rh[j >> 1] |= bh << 16;
-          rl[j >> 1] |= bl << 16;
-        } else {
-          rh[j >> 1] = bh;
-          rl[j >> 1] = bl;
+      for (int j = 0; j < d; j += 2) {  // a pair of coordinates: one packed fp16 conversion each
+        float x2[2];
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int jj = j + e2;
+          const float yv = y[jj] * inv;
+          const int idx = g ? rec_index<MB1>(yv, blo) : rec_index<MB0>(yv, bhi);
+          const int bit = jj * mb, w = bit >> 5, o = bit & 31;
+          iw[w] |= (uint32_t)idx << o;
+          if (o + mb > 32) iw[w + 1] |= (uint32_t)idx >> (32 - o);
+          const float dr = yv - cen[g][idx];
+          rsp[jj & 3] = fmaf(dr, dr, rsp[jj & 3]);
+          x2[e2] = dr * 1024.0f;
         }
+        // (rows of dead lanes gathered zeros: their residual is finite and never written)
+        const __half2 h2 = __floats2half2_rn(x2[0], x2[1]);
+        const float2 hf = __half22float2(h2);
+        const __half2 l2 = __floats2half2_rn((x2[0] - hf.x) * 4096.0f, (x2[1] - hf.y) * 4096.0f);
+        rh[j >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+        rl[j >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
       }
       // the sketch, sixteen units per pass
       uint32_t sw[E];
