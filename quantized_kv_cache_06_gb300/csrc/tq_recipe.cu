@@ -97,11 +97,6 @@ __device__ __forceinline__ void rec_ldsm_x4(uint32_t addr, uint32_t& r0, uint32_
                : "r"(addr)
                : "memory");
 }
-// bit c of a nibble to bit 2 c
-__device__ __forceinline__ uint32_t spread_nibble(uint32_t x) {
-  x = (x | (x << 2)) & 0x33u;
-  return (x | (x << 1)) & 0x55u;
-}
 
 // Shared memory of the writer: S hi and lo, then per warp its A tile hi and lo (rows of d + 8
 // halves: 16 bytes of padding put the 8 rows of an ldmatrix in different banks), then per warp
@@ -210,10 +205,11 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_tokens, int num_kv_he
   // The sketch of the sixteen units of pass p held in the A tile: sign word e of unit 16 p + u
   // is kept by lane 16 p + u.
   auto sketch = [&](int p, uint32_t (&sw)[E]) {
-    const int u = lane & 15, ur = u & 7, uh = u >> 3;
+    const int u = lane & 15;
+    const uint32_t cbit = 1u << (2 * (lane & 3));  // this lane's column pair in a byte
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      uint32_t word = 0u;
+      uint32_t pw[2] = {0u, 0u};  // partial sign words of units lane / 4 and lane / 4 + 8
 #pragma unroll
       for (int np = 0; np < 2; ++np) {  // n-tiles 4 e + 2 np and 4 e + 2 np + 1
         float am[2][4], al[2][4];
@@ -238,16 +234,23 @@ write_recipe_kernel(const T* __restrict__ raw, int64_t num_tokens, int num_kv_he
           rec_mma(al[1], h0, h1, h2, h3, c2, c3);
         }
         // accumulator x of n-tile 4 e + 2 np + n on lane (g, c): unit g + 8 (x >> 1),
-        // projection 32 e + 8 (2 np + n) + 2 c + (x & 1); its ballot bit 4 g + c
+        // projection 32 e + 8 (2 np + n) + 2 c + (x & 1)
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const uint32_t bal = __ballot_sync(kFullMask, fmaf(al[n][x], 1.0f / 4096, am[n][x]) >= 0.f);
-            if ((x >> 1) == uh) word |= spread_nibble((bal >> (4 * ur)) & 15u) << (8 * (2 * np + n) + (x & 1));
-          }
+          for (int x = 0; x < 4; ++x)
+            if (fmaf(al[n][x], 1.0f / 4096, am[n][x]) >= 0.f) pw[x >> 1] |= cbit << (8 * (2 * np + n) + (x & 1));
       }
-      if ((lane >> 4) == p) sw[e] = word;
+      // the four lanes of a unit pair hold disjoint bits: OR them, then unit u's word from
+      // lane 4 (u mod 8)
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        pw[0] |= __shfl_xor_sync(kFullMask, pw[0], m);
+        pw[1] |= __shfl_xor_sync(kFullMask, pw[1], m);
+      }
+      const uint32_t wa = __shfl_sync(kFullMask, pw[0], 4 * (u & 7));
+      const uint32_t wb = __shfl_sync(kFullMask, pw[1], 4 * (u & 7));
+      if ((lane >> 4) == p) sw[e] = (u >> 3) ? wb : wa;
     }
   };
 
