@@ -802,7 +802,7 @@ __device__ __forceinline__ uint2 rec_pair_entry(const float* __restrict__ cent, 
 }
 
 template <int E, int G, int MB0, int MB1>
-__global__ void __launch_bounds__(kRecTcWarps * 32, 3)
+__global__ void __launch_bounds__(kRecTcWarps * 32, MB0 == 2 ? 4 : 3)
 decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p_all, int num_splits,
                         int blocks_per_split, RecipeSplitView part) {
   static_assert(G <= 4, "the eight MMA columns hold four q heads' hi and lo parts");
@@ -866,20 +866,39 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
   // coordinates 32 (P / 16) + P mod 16 and 16 above.
   const bool rem_col = gr >= 4;
   const int hq = gr & 3;
-  uint32_t bq[2][2 * E][2], bp[2][2 * E][2];
+  // (the same for every warp of the CTA: kept once in shared memory, over the query, and
+  // loaded per k-step)
+  uint2 bqr[2][2 * E], bpr[2][2 * E];
 #pragma unroll
   for (int grp = 0; grp < 2; ++grp)
 #pragma unroll
-    for (int s = 0; s < 2 * E; ++s)
+    for (int s = 0; s < 2 * E; ++s) {
+      uint32_t fq[2], fp[2];
 #pragma unroll
       for (int slot = 0; slot < 2; ++slot) {
         const int kp = 2 * s + slot;
         const int j = 8 * E * c + 2 * kp;
-        bq[grp][s][slot] = rec_split_pack(qv[0][grp][hq][j], qv[0][grp][hq][j + 1], rem_col);
+        fq[slot] = rec_split_pack(qv[0][grp][hq][j], qv[0][grp][hq][j + 1], rem_col);
         const int pp = 4 * E * c + kp;
         const int js = 32 * (pp >> 4) + (pp & 15);
-        bp[grp][s][slot] = rec_split_pack(qv[1][grp][hq][js], qv[1][grp][hq][js + 16], rem_col);
+        fp[slot] = rec_split_pack(qv[1][grp][hq][js], qv[1][grp][hq][js + 16], rem_col);
       }
+      bqr[grp][s] = make_uint2(fq[0], fq[1]);
+      bpr[grp][s] = make_uint2(fp[0], fp[1]);
+    }
+  static_assert(2 * 2 * 2 * E * 32 * 8 <= (int)sizeof(qv), "the fragments fit over the query");
+  uint2(*bfr)[2][2 * E][32] = reinterpret_cast<uint2(*)[2][2 * E][32]>(&qv[0][0][0][0]);  // [q | p][group][s][lane]
+  __syncthreads();  // every warp has read the query
+  if (warp == 0) {
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+      for (int s = 0; s < 2 * E; ++s) {
+        bfr[0][grp][s][lane] = bqr[grp][s];
+        bfr[1][grp][s][lane] = bpr[grp][s];
+      }
+  }
+  __syncthreads();
   const int sw_k = (4 * E * c) >> 4, sh_k = (4 * E * c) & 15;  // this lane's sign word, first bit
   const uint32_t lane8 = (uint32_t)(lane & 15) << 3;
   const unsigned char* tabs[2] = {reinterpret_cast<const unsigned char*>(&tab0[0][0]),
@@ -1004,9 +1023,10 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
             tv[r][slot] = *reinterpret_cast<const uint2*>(tabp + rec_tab_off(ch[r][kp >> 2], 2 * MB * (kp & 3), 2 * MB, lane8));
             sv[r][slot] = rec_sign2(sg[r] << (15 - kp));
           }
-        rec_mma(am, tv[0][0].x, tv[1][0].x, tv[0][1].x, tv[1][1].x, bq[grp][s][0], bq[grp][s][1]);
-        rec_mma(am, tv[0][0].y, tv[1][0].y, tv[0][1].y, tv[1][1].y, bq[grp][s][0], bq[grp][s][1]);
-        rec_mma(as, sv[0][0], sv[1][0], sv[0][1], sv[1][1], bp[grp][s][0], bp[grp][s][1]);
+        const uint2 bq = bfr[0][grp][s][lane], bp = bfr[1][grp][s][lane];
+        rec_mma(am, tv[0][0].x, tv[1][0].x, tv[0][1].x, tv[1][1].x, bq.x, bq.y);
+        rec_mma(am, tv[0][0].y, tv[1][0].y, tv[0][1].y, tv[1][1].y, bq.x, bq.y);
+        rec_mma(as, sv[0][0], sv[1][0], sv[0][1], sv[1][1], bp.x, bp.y);
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
