@@ -248,3 +248,35 @@ def test_recipe_decode_wide_value_norms(tq, recipe):
         ref = ro.paged_decode_recipe(q, kp, vp, bt, np.array(lens), high, oc)
         assert np.abs(ref).max() > 1e3  # the large norms reach the output
         assert_decode_close(got.cpu().numpy(), ref)
+
+
+def test_recipe_writer_many_tiles_per_warp(tq):
+    # 16384 tokens x 8 heads: 4096 tiles of 32 rows, more than the resident warps take at once,
+    # so warps stage the next tile while they encode the current one; rows checked on a sample
+    recipe, d, t, h, bs = "turboquant35", 128, 16384, 8, 16
+    rng = np.random.default_rng(909)
+    nb = t // bs + 4
+    raw32 = (rng.standard_normal((t, h, d)) * rng.lognormal(0.0, 0.6, (1, h, d))).astype(np.float32)
+    raw = torch.from_numpy(raw32).half()
+    raw64 = raw.double().numpy()
+    high = tq.tq_recipe_calibrate(recipe, raw.float().numpy()[:256])
+    order = tq.tq_recipe_channel_order(recipe, d, high)
+    gpu, oc = codecs(tq, recipe, d)
+    slots = rng.permutation(nb * bs)[:t].astype(np.int64)
+    slots[5::97] = -1
+    rb = gpu.row_bytes
+    pages = torch.full((nb, bs, h, rb), 0x5A, dtype=torch.uint8, device="cuda")
+    st = tq.tq_write_kv_recipe(raw.cuda(), pages, torch.from_numpy(slots).cuda(), order.cuda(), gpu, check=False)
+    assert int(st.item()) == 0
+    pg = pages.cpu().numpy().reshape(nb * bs, h, rb)
+    written = np.zeros(nb * bs, dtype=bool)
+    written[slots[slots >= 0]] = True
+    assert np.all(pg[~written] == 0x5A)
+    tok = rng.choice(np.nonzero(slots >= 0)[0], size=1500, replace=False)
+    nh = qo.prod_row_bytes(d // 2, oc.bits[0])
+    ordn = order.numpy()
+    for k in range(h):
+        rows = pg[slots[tok], k]
+        for g, (lo, hi) in enumerate(((0, nh), (nh, rb))):
+            chans = ordn[k, g * (d // 2):(g + 1) * (d // 2)]
+            check_group_rows(rows[:, lo:hi], raw64[tok, k][:, chans], oc.bits[g], oc)
