@@ -740,7 +740,8 @@ decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict_
 
 // ---- tensor-core split decode (G <= 4) -------------------------------------------------
 // Each warp takes 16-token tiles of its split in turn.  The tile's K and V rows are staged in
-// shared memory by cp.async (the next tile's copies in flight while this one is computed;
+// shared memory by cp.async, three tiles per warp (the next two tiles' copies in flight while
+// this one is computed, their block ids loaded an iteration earlier; four lanes copy a row;
 // rows of tokens past the sequence end or in a block with a bad id are zero-filled).  Every
 // contraction is an m16n8k16 MMA with fp32 accumulation whose n = 8 columns hold q heads 0-3
 // twice: columns 0-3 take the fp16 hi part of the B operand, columns 4-7 its remainder, so one
@@ -801,6 +802,9 @@ __device__ __forceinline__ uint2 rec_pair_entry(const float* __restrict__ cent, 
   return e;
 }
 
+// CTAs per SM: four for turboquant25 (128 registers, a few bytes of spills, measured faster
+// than three), three for turboquant35 (its three staged tiles per warp take 43 KB of shared
+// memory, and four CTAs at 128 registers measured slower).
 template <int E, int G, int MB0, int MB1>
 __global__ void __launch_bounds__(kRecTcWarps * 32, MB0 == 2 ? 4 : 3)
 decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p_all, int num_splits,
@@ -866,8 +870,8 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
   // coordinates 32 (P / 16) + P mod 16 and 16 above.
   const bool rem_col = gr >= 4;
   const int hq = gr & 3;
-  // (the same for every warp of the CTA: kept once in shared memory, over the query, and
-  // loaded per k-step)
+  // The fragments are the same for every warp of the CTA: warp 0 stores them once in shared
+  // memory, over the query they were built from, and each k-step loads its pair (64 bits).
   uint2 bqr[2][2 * E], bpr[2][2 * E];
 #pragma unroll
   for (int grp = 0; grp < 2; ++grp)
