@@ -23,18 +23,13 @@
 //                              unit: channel gather, norm, rotation (FWHT in registers),
 //                              indices and residual; then the sketch of sixteen units at a
 //                              time as m16n8k16 MMAs (fp16 hi / lo splits of r and S_d) and
-//                              the sign words from ballots.
+//                              the sign words from per-lane partial words.
 //   recipe_project_kernel      one warp per (sequence, q head): per group the rotated
 //                              gathered query q_g = R_d q[order_g] (times the softmax scale
 //                              and log2 e) and its projection p_g = S_d q_g.
-//   decode_recipe_tc_kernel    the split decode for up to four q heads per kv head: 16-token
-//                              tiles staged by cp.async, scores and values as m16n8k16 MMAs
-//                              (pair tables of centroids, +-1 sign operands).
-//   decode_recipe_split_kernel the SIMT split decode (eight q heads per kv head), 32-token
-//                              tiles per warp: scores with
-//                              a lane per token (every q head at once), one softmax step
-//                              per tile, values with lanes over coordinates.  Score of key
-//                              row k:
+//   decode_recipe_tc_kernel    the split decode: 16-token tiles staged by cp.async, scores
+//                              and values as m16n8k16 MMAs (pair tables of centroids, +-1
+//                              sign operands).  Score of key row k:
 //                                sum_g nu_g (<q_g, c_g[idx]> + gamma_g kappa <p_g, 2z - 1>),
 //                              kappa = sqrt(pi / 2) / d.  The value reconstruction
 //                              nu R_d^T (c[idx] + gamma kappa S_d^T (2z - 1)) is linear, so
@@ -58,7 +53,6 @@ namespace tq {
 namespace {
 
 constexpr int kRecWarps = 4;
-constexpr int kRecDecodeWarps = 4;
 constexpr float kRecLog2e = 1.4426950408889634f;
 constexpr float kRecSqrtHalfPi = 1.2533141373155003f;  // sqrt(pi / 2)
 
@@ -76,8 +70,9 @@ __host__ __device__ constexpr int group_words(int d, int bits) { return d * (bit
 // their packing, and the residual r, stored as fp16 hi = r 2^10 and lo = (r 2^10 - hi) 2^12.
 // The residuals go to the warp's A tile sixteen at a time, and the sketch S_d r of the sixteen
 // runs as m16n8k16 MMAs: r_hi S_hi into one accumulator, r_lo S_hi + r_hi S_lo into another
-// (~22 significant bits, as in an fp32 sum), each sign word assembled from ballots of the
-// accumulators.  Each lane then writes its unit's group words (indices, signs, nu, gamma).
+// (~22 significant bits, as in an fp32 sum); each lane sets the sign bits of its own
+// accumulators into partial words, ORed across the four lanes of a unit pair.  The tile's
+// finished rows are staged in the A tile and written with lanes over consecutive words.
 constexpr int kRecRows = 32;   // rows per warp tile
 constexpr int kRecUnits = 16;  // units per sketch pass
 
@@ -425,95 +420,6 @@ struct RecipeSplitView {
   float* ml;   // [rows][nsplit][2]  (running max in log2 units, sum)
 };
 
-__device__ __forceinline__ int rfield(uint64_t win, int bitpos, int bits) {
-  return (int)((win >> bitpos) & ((1u << bits) - 1u));
-}
-
-// One group of one packed row, as this lane needs it: the MSE indices of coordinates
-// lane E + i, the sign words (bit `lane` of word e: coordinate lane + 32 e), nu, gamma.
-template <int E>
-struct GroupView {
-  int idx[E];
-  uint32_t zw[E];
-  float nu, gamma;
-};
-
-template <int E>
-__device__ __forceinline__ GroupView<E> read_group(const uint32_t* __restrict__ gw, int mb, int lane) {
-  constexpr int d = 32 * E;
-  GroupView<E> v;
-  const int bit0 = lane * E * mb;
-  const uint64_t win = (uint64_t)__ldg(gw + (bit0 >> 5)) | ((uint64_t)__ldg(gw + (bit0 >> 5) + 1) << 32);
-#pragma unroll
-  for (int i = 0; i < E; ++i) v.idx[i] = rfield(win, (bit0 & 31) + i * mb, mb);
-  const int iw = d * mb / 32;
-#pragma unroll
-  for (int e = 0; e < E; ++e) v.zw[e] = __ldg(gw + iw + e);
-  v.nu = __uint_as_float(__ldg(gw + iw + E));
-  v.gamma = __uint_as_float(__ldg(gw + iw + E + 1));
-  return v;
-}
-
-// Score of one key group for every q head of the kv head, by one lane for its own token:
-// sc[g] += nu (sum_j q_g[j] c[idx_j] + gamma kappa sum_j p_g[j] (2 z_j - 1)), with
-// sum_j p_g[j] (2 z_j - 1) = 2 sum_j z_j p_g[j] - sum_j p_g[j].  q and p come from shared
-// memory ([coordinate][head], the same address on every lane).
-// read_group from a row staged in shared memory
-template <int E>
-__device__ __forceinline__ GroupView<E> read_group_s(const uint32_t* gw, int mb, int lane) {
-  constexpr int d = 32 * E;
-  GroupView<E> v;
-  const int bit0 = lane * E * mb;
-  const uint64_t win = (uint64_t)gw[bit0 >> 5] | ((uint64_t)gw[(bit0 >> 5) + 1] << 32);
-#pragma unroll
-  for (int i = 0; i < E; ++i) v.idx[i] = rfield(win, (bit0 & 31) + i * mb, mb);
-  const int iw = d * mb / 32;
-#pragma unroll
-  for (int e = 0; e < E; ++e) v.zw[e] = gw[iw + e];
-  v.nu = __uint_as_float(gw[iw + E]);
-  v.gamma = __uint_as_float(gw[iw + E + 1]);
-  return v;
-}
-
-// PAIRS: the group's words start 8-byte aligned and are even in number (64-bit loads).
-template <int E, int G, int MB, bool PAIRS>
-__device__ __forceinline__ void recipe_group_score(const uint32_t* __restrict__ gw, const float (*qs)[G],
-                                                   const float (*ps)[G], const float* cent, const float* psum,
-                                                   float kappa, float (&sc)[G]) {
-  constexpr int d = 32 * E, IW = d * MB / 32;
-  uint32_t w[IW + E + 2];
-  if constexpr (PAIRS) {
-#pragma unroll
-    for (int k = 0; k < (IW + E + 2) / 2; ++k) {
-      const uint2 x = __ldg(reinterpret_cast<const uint2*>(gw) + k);
-      w[2 * k] = x.x;
-      w[2 * k + 1] = x.y;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < IW + E + 2; ++k) w[k] = __ldg(gw + k);
-  }
-  float sm[G], sz[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) sm[g] = sz[g] = 0.f;
-#pragma unroll
-  for (int j = 0; j < d; ++j) {
-    const int bit = j * MB, wi = bit >> 5, o = bit & 31;
-    uint32_t f = w[wi] >> o;
-    if (o + MB > 32) f |= w[wi + 1] << (32 - o);
-    const float c = cent[f & ((1u << MB) - 1u)];
-    const float z = (float)((w[IW + (j >> 5)] >> (j & 31)) & 1u);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      sm[g] = fmaf(qs[j][g], c, sm[g]);
-      sz[g] = fmaf(ps[j][g], z, sz[g]);
-    }
-  }
-  const float nu = __uint_as_float(w[IW + E]), gk = __uint_as_float(w[IW + E + 1]) * kappa;
-#pragma unroll
-  for (int g = 0; g < G; ++g) sc[g] = fmaf(nu, fmaf(gk, fmaf(2.f, sz[g], -psum[g]), sm[g]), sc[g]);
-}
-
 // Merges the NW warps' partials of one CTA (running max in log2 units and sum per q head;
 // value accumulators as in RecipeSplitView) and writes the CTA's split partial for q rows
 // row0 + g.  Called after a barrier that makes every warp's partial visible.
@@ -545,200 +451,7 @@ __device__ __forceinline__ void recipe_merge_write(const float (*red_ml)[G][2], 
   }
 }
 
-// Tiles of 32 tokens per warp.  Scores: lane = token, every q head of the kv head at once
-// (no per-token reductions); the tile's softmax step (running max, correction, weights) once
-// per tile; values: lanes over coordinates, the tile's tokens accumulated with their weights
-// from shared memory.  MB0 / MB1: MSE index bits of the high / low group.
-template <int E, int G, int MB0, int MB1>
-__global__ void __launch_bounds__(kRecDecodeWarps * 32)
-decode_recipe_split_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p_all, int num_splits,
-                           int blocks_per_split, RecipeSplitView part) {
-  constexpr int d = 32 * E, D = 2 * d;
-  constexpr int kWh = d * MB0 / 32 + E + 2;  // words of the high group
-  constexpr int rbw = kWh + d * MB1 / 32 + E + 2;  // words of a row
-  // rows and both groups 8-byte aligned (pages are 16-byte aligned): 64-bit row loads
-  constexpr bool kPairs = rbw % 2 == 0 && kWh % 2 == 0 && (d * MB1 / 32 + E + 2) % 2 == 0;
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = a.num_kv_heads, bs = a.block_size;
-
-  __shared__ float cent[2][8];
-  __shared__ __align__(16) float qs[2][d][G];  // rotated query, coordinate j of group grp, head g
-  __shared__ __align__(16) float ps[2][d][G];  // its projection p = S_d q, coordinate j
-  __shared__ float psum[2][G];                 // sum_j p[j]
-  __shared__ __align__(16) float pt[kRecDecodeWarps][32][G];  // the tile's weights (0: no token)
-  __shared__ int64_t trow[kRecDecodeWarps][32];               // the tile's page rows (-1: none)
-  __shared__ float red_ml[kRecDecodeWarps][G][2];
-  // The tile's value rows (fetched by the lane of each token while it scores it; an odd row
-  // stride keeps those stores conflict free), sharing memory with the final merge's buffer.
-  constexpr int kVStride = (rbw % 2 == 0) ? rbw + 1 : rbw;
-  constexpr int kRedBytes = kRecDecodeWarps * G * 2 * D * 4, kVBytes = kRecDecodeWarps * 32 * kVStride * 4;
-  __shared__ __align__(16) unsigned char merge_u[kRedBytes > kVBytes ? kRedBytes : kVBytes];
-  float(*red_acc)[G][2 * D] = reinterpret_cast<float(*)[G][2 * D]>(merge_u);
-  uint32_t(*vbuf)[32][kVStride] = reinterpret_cast<uint32_t(*)[32][kVStride]>(merge_u);
-  if (threadIdx.x < (1 << MB0)) cent[0][threadIdx.x] = rc.mse_hi[threadIdx.x];
-  if (threadIdx.x < (1 << MB1)) cent[1][threadIdx.x] = rc.mse_lo[threadIdx.x];
-
-  const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
-  const float qmul = scale * kRecLog2e / sqrtf((float)d);
-  const float kappa = kRecSqrtHalfPi / (float)d;
-  for (int g = warp; g < G; g += kRecDecodeWarps) {
-    const int64_t qrow = (int64_t)b * a.num_q_heads + (int64_t)h * G + g;
-#pragma unroll
-    for (int grp = 0; grp < 2; ++grp) {
-      float qr[E];
-      const int32_t* ord = rc.order + (int64_t)h * D + grp * d + lane * E;
-#pragma unroll
-      for (int i = 0; i < E; ++i)
-        qr[i] = load_as_f32(a.q, qrow * D + __ldg(ord + i), a.q_dtype) * __ldg(a.signs + lane * E + i);
-      fwht_warp<E>(qr);
-      float ssum = 0.f;
-#pragma unroll
-      for (int i = 0; i < E; ++i) {
-        qs[grp][lane * E + i][g] = qr[i] * qmul;
-        const float pv = __ldg(p_all + (qrow * 2 + grp) * d + lane + 32 * i);
-        ps[grp][lane + 32 * i][g] = pv;
-        ssum += pv;
-      }
-      ssum = warp_sum(ssum);
-      if (lane == 0) psum[grp][g] = ssum;
-    }
-  }
-
-  int len = __ldg(a.seq_lens + b);
-  const int cap = a.max_blocks_per_seq * bs;
-  if (len < 0 || len > cap) {
-    if (threadIdx.x == 0 && split == 0 && h == 0 && a.status) atomicMax(a.status, (int32_t)kInvalidArg);
-    len = len < 0 ? 0 : cap;
-  }
-  const int t_lo = split * blocks_per_split * bs;
-  const int t_hi = min(len, (split + 1) * blocks_per_split * bs);
-
-  float m[G], l[G], acc_c[G][2][E], acc_z[G][2][E];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int grp = 0; grp < 2; ++grp)
-#pragma unroll
-      for (int i = 0; i < E; ++i) acc_c[g][grp][i] = acc_z[g][grp][i] = 0.f;
-  }
-  __syncthreads();
-
-  bool bad_block = false;
-  for (int tb = t_lo + 32 * warp; tb < t_hi; tb += 32 * kRecDecodeWarps) {
-    // ---- scores: this lane's token ---------------------------------------------------
-    const int t = tb + lane;
-    int64_t row = -1;
-    if (t < t_hi) {
-      const int bid = __ldg(a.block_table + (int64_t)b * a.max_blocks_per_seq + t / bs);
-      if (bid < 0 || (int64_t)bid >= a.num_blocks) bad_block = true;
-      else row = ((int64_t)bid * bs + t % bs) * H + h;
-    }
-    float sc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) sc[g] = row >= 0 ? 0.f : -INFINITY;
-    if (row >= 0) {
-      const uint32_t* vr = reinterpret_cast<const uint32_t*>(a.v_pages) + row * rbw;
-      uint32_t vw[rbw];  // this token's value row, in flight while the key row is scored
-      if constexpr (kPairs) {
-#pragma unroll
-        for (int k = 0; k < rbw / 2; ++k) {
-          const uint2 x = __ldg(reinterpret_cast<const uint2*>(vr) + k);
-          vw[2 * k] = x.x;
-          vw[2 * k + 1] = x.y;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < rbw; ++k) vw[k] = __ldg(vr + k);
-      }
-      const uint32_t* kr = reinterpret_cast<const uint32_t*>(a.k_pages) + row * rbw;
-      recipe_group_score<E, G, MB0, kPairs>(kr, qs[0], ps[0], cent[0], psum[0], kappa, sc);
-      recipe_group_score<E, G, MB1, kPairs>(kr + kWh, qs[1], ps[1], cent[1], psum[1], kappa, sc);
-#pragma unroll
-      for (int k = 0; k < rbw; ++k) vbuf[warp][lane][k] = vw[k];
-    }
-    trow[warp][lane] = row;
-    // ---- the tile's softmax step (m, l, the correction: the same on every lane) -----
-    float corr[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float tmax = warp_max(sc[g]);
-      const float mn = fmaxf(m[g], tmax);
-      corr[g] = 1.f;
-      float p = 0.f;
-      if (mn != -INFINITY) {  // some token of this or an earlier tile
-        corr[g] = exp2f(m[g] - mn);  // 0 while m is -inf
-        p = exp2f(sc[g] - mn);       // 0 for a masked token
-      }
-      l[g] = fmaf(l[g], corr[g], warp_sum(p));
-      m[g] = mn;
-      pt[warp][lane][g] = p;
-    }
-    __syncwarp();
-    // ---- values: lanes over coordinates, the tile's tokens in order -----------------
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int grp = 0; grp < 2; ++grp)
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-          acc_c[g][grp][i] *= corr[g];
-          acc_z[g][grp][i] *= corr[g];
-        }
-    const int nt = min(32, t_hi - tb);
-    for (int k = 0; k < nt; ++k) {
-      if (trow[warp][k] < 0) continue;  // (the same on every lane)
-      const uint32_t* vr = vbuf[warp][k];
-      float pk[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) pk[g] = pt[warp][k][g];
-#pragma unroll
-      for (int grp = 0; grp < 2; ++grp) {
-        const GroupView<E> v = read_group_s<E>(vr + (grp ? kWh : 0), grp ? MB1 : MB0, lane);
-        const float vzs = v.nu * v.gamma * kappa;
-        float vc[E], vz[E];  // nu c[idx] and nu gamma kappa (2z - 1)
-#pragma unroll
-        for (int i = 0; i < E; ++i) {
-          vc[i] = v.nu * cent[grp][v.idx[i]];
-          vz[i] = ((v.zw[i] >> lane) & 1u) ? vzs : -vzs;
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int i = 0; i < E; ++i) {
-            acc_c[g][grp][i] = fmaf(pk[g], vc[i], acc_c[g][grp][i]);
-            acc_z[g][grp][i] = fmaf(pk[g], vz[i], acc_z[g][grp][i]);
-          }
-      }
-    }
-    __syncwarp();  // the next tile rewrites pt / trow
-  }
-  if (__any_sync(kFullMask, bad_block) && lane == 0 && a.status) atomicMax(a.status, (int32_t)kBlockOutOfRange);
-  __syncthreads();  // every warp is done with its value rows: the merge buffer may be written
-
-  // merge the warps of this CTA, then write the split partial
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if (lane == 0) {
-      red_ml[warp][g][0] = m[g];
-      red_ml[warp][g][1] = l[g];
-    }
-#pragma unroll
-    for (int grp = 0; grp < 2; ++grp)
-#pragma unroll
-      for (int i = 0; i < E; ++i) {
-        red_acc[warp][g][grp * d + lane * E + i] = acc_c[g][grp][i];
-        red_acc[warp][g][D + grp * d + lane + 32 * i] = acc_z[g][grp][i];
-      }
-  }
-  __syncthreads();
-  recipe_merge_write<kRecDecodeWarps, G, D>(red_ml, red_acc, (int64_t)b * a.num_q_heads + (int64_t)h * G, num_splits,
-                                            split, part, warp, lane);
-}
-
-// ---- tensor-core split decode (G <= 4) -------------------------------------------------
+// ---- tensor-core split decode ------------------------------------------------------------
 // Each warp takes 16-token tiles of its split in turn.  The tile's K and V rows are staged in
 // shared memory by cp.async, three tiles per warp (the next two tiles' copies in flight while
 // this one is computed, their block ids loaded an iteration earlier; four lanes copy a row;
@@ -806,10 +519,16 @@ __device__ __forceinline__ uint2 rec_pair_entry(const float* __restrict__ cent, 
 // than three), three for turboquant35 (its three staged tiles per warp take 43 KB of shared
 // memory, and four CTAs at 128 registers measured slower).
 template <int E, int G, int MB0, int MB1>
-__global__ void __launch_bounds__(kRecTcWarps * 32, MB0 == 2 ? 4 : 3)
+__global__ void __launch_bounds__(kRecTcWarps * 32, (MB0 == 2 && G <= 4) ? 4 : 3)
 decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p_all, int num_splits,
                         int blocks_per_split, RecipeSplitView part) {
-  static_assert(G <= 4, "the eight MMA columns hold four q heads' hi and lo parts");
+  // G <= 4: the eight MMA columns hold four q heads' hi parts (columns 0-3) and remainders
+  // (4-7) of one B operand.  G = 8: they hold the eight heads, and the hi parts and the
+  // remainders are two B operands, each with its own MMA into the same accumulators.
+  static_assert(G <= 4 || G == 8, "up to four q heads, or eight");
+  constexpr bool kG8 = G == 8;
+  constexpr int GC = kG8 ? 8 : 4;      // q heads held (the ones past G are zero)
+  constexpr int kSets = kG8 ? 2 : 1;   // B operands per product
   constexpr int d = 32 * E, D = 2 * d;
   constexpr int kWh = E * MB0 + E + 2;        // words of the high group
   constexpr int rbw = kWh + E * MB1 + E + 2;  // words of a row
@@ -823,12 +542,12 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
 
   __shared__ __align__(16) uint2 tab0[1 << (2 * MB0)][16];
   __shared__ __align__(16) uint2 tab1[1 << (2 * MB1)][16];
-  __shared__ __align__(16) float qv[2][2][4][d];          // [q | p][group][q head][coordinate]
-  __shared__ __align__(16) float pt[kRecTcWarps][4][16];  // the tile's weights [q head][token]
+  __shared__ __align__(16) float qv[2][2][GC][d];          // [q | p][group][q head][coordinate]
+  __shared__ __align__(16) float pt[kRecTcWarps][GC][16];  // the tile's weights [q head][token]
   __shared__ float red_ml[kRecTcWarps][G][2];
-  constexpr int kStageWords = kRecTcWarps * kRecTcStages * kBuf, kRedWords = kRecTcWarps * G * 2 * D;
-  // the warps' staged tiles, then (after the last tile) the merge buffer
-  __shared__ __align__(16) uint32_t stage_u[kStageWords > kRedWords ? kStageWords : kRedWords];
+  // the warps' staged tiles, then (after the last tile) the merge buffer: dynamic shared
+  // memory of recipe_tc_dyn_words words
+  extern __shared__ __align__(16) uint32_t stage_u[];
   float(*red_acc)[G][2 * D] = reinterpret_cast<float(*)[G][2 * D]>(stage_u);
 
   for (int i = threadIdx.x; i < (1 << (2 * MB0)) * 16; i += blockDim.x) tab0[i >> 4][i & 15] = rec_pair_entry(rc.mse_hi, i >> 4, MB0);
@@ -836,7 +555,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
   const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
   const float qmul = scale * kRecLog2e / sqrtf((float)d);
   const float kappa = kRecSqrtHalfPi / (float)d;
-  for (int g = warp; g < 4; g += kRecTcWarps) {  // heads past G: zero query, never written
+  for (int g = warp; g < GC; g += kRecTcWarps) {  // heads past G: zero query, never written
     const int64_t qrow = (int64_t)b * a.num_q_heads + (int64_t)h * G + g;
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
@@ -865,42 +584,49 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
   __syncthreads();
 
   // B operands of the scores: column n = gr is q head gr mod 4, its fp16 hi part for gr < 4
-  // and its remainder for gr >= 4.  Pair kp = 2 s + slot of k-step s: coordinates
-  // 8E c + 2 kp (+1) for the centroid term; for the sign term the pair P = 4E c + kp,
-  // coordinates 32 (P / 16) + P mod 16 and 16 above.
-  const bool rem_col = gr >= 4;
-  const int hq = gr & 3;
+  // and its remainder for gr >= 4 (G <= 4), or q head gr, hi parts in set 0 and remainders in
+  // set 1 (G = 8).  Pair kp = 2 s + slot of k-step s: coordinates 8E c + 2 kp (+1) for the
+  // centroid term; for the sign term the pair P = 4E c + kp, coordinates 32 (P / 16) + P mod 16
+  // and 16 above.
+  const bool rem_col = !kG8 && gr >= 4;
+  const int hq = kG8 ? gr : (gr & 3);
   // The fragments are the same for every warp of the CTA: warp 0 stores them once in shared
   // memory, over the query they were built from, and each k-step loads its pair (64 bits).
-  uint2 bqr[2][2 * E], bpr[2][2 * E];
+  uint2 bqr[kSets][2][2 * E], bpr[kSets][2][2 * E];
 #pragma unroll
-  for (int grp = 0; grp < 2; ++grp)
-#pragma unroll
-    for (int s = 0; s < 2 * E; ++s) {
-      uint32_t fq[2], fp[2];
-#pragma unroll
-      for (int slot = 0; slot < 2; ++slot) {
-        const int kp = 2 * s + slot;
-        const int j = 8 * E * c + 2 * kp;
-        fq[slot] = rec_split_pack(qv[0][grp][hq][j], qv[0][grp][hq][j + 1], rem_col);
-        const int pp = 4 * E * c + kp;
-        const int js = 32 * (pp >> 4) + (pp & 15);
-        fp[slot] = rec_split_pack(qv[1][grp][hq][js], qv[1][grp][hq][js + 16], rem_col);
-      }
-      bqr[grp][s] = make_uint2(fq[0], fq[1]);
-      bpr[grp][s] = make_uint2(fp[0], fp[1]);
-    }
-  static_assert(2 * 2 * 2 * E * 32 * 8 <= (int)sizeof(qv), "the fragments fit over the query");
-  uint2(*bfr)[2][2 * E][32] = reinterpret_cast<uint2(*)[2][2 * E][32]>(&qv[0][0][0][0]);  // [q | p][group][s][lane]
-  __syncthreads();  // every warp has read the query
-  if (warp == 0) {
+  for (int st = 0; st < kSets; ++st)
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp)
 #pragma unroll
       for (int s = 0; s < 2 * E; ++s) {
-        bfr[0][grp][s][lane] = bqr[grp][s];
-        bfr[1][grp][s][lane] = bpr[grp][s];
+        uint32_t fq[2], fp[2];
+        const bool rem = kG8 ? st == 1 : rem_col;
+#pragma unroll
+        for (int slot = 0; slot < 2; ++slot) {
+          const int kp = 2 * s + slot;
+          const int j = 8 * E * c + 2 * kp;
+          fq[slot] = rec_split_pack(qv[0][grp][hq][j], qv[0][grp][hq][j + 1], rem);
+          const int pp = 4 * E * c + kp;
+          const int js = 32 * (pp >> 4) + (pp & 15);
+          fp[slot] = rec_split_pack(qv[1][grp][hq][js], qv[1][grp][hq][js + 16], rem);
+        }
+        bqr[st][grp][s] = make_uint2(fq[0], fq[1]);
+        bpr[st][grp][s] = make_uint2(fp[0], fp[1]);
       }
+  static_assert(kSets * 2 * 2 * 2 * E * 32 * 8 <= (int)sizeof(qv), "the fragments fit over the query");
+  // [set][q | p][group][s][lane]
+  uint2(*bfr)[2][2][2 * E][32] = reinterpret_cast<uint2(*)[2][2][2 * E][32]>(&qv[0][0][0][0]);
+  __syncthreads();  // every warp has read the query
+  if (warp == 0) {
+#pragma unroll
+    for (int st = 0; st < kSets; ++st)
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+        for (int s = 0; s < 2 * E; ++s) {
+          bfr[st][0][grp][s][lane] = bqr[st][grp][s];
+          bfr[st][1][grp][s][lane] = bpr[st][grp][s];
+        }
   }
   __syncthreads();
   const int sw_k = (4 * E * c) >> 4, sh_k = (4 * E * c) & 15;  // this lane's sign word, first bit
@@ -994,7 +720,8 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
     const uint32_t* tile = stage_w + buf * kBuf;
     const uint32_t vm = vm0;
 
-    // ---- scores of tokens gr + 8 r, q heads 2 (c mod 2) + e (this lane's column part) ----
+    // ---- scores of tokens gr + 8 r, q heads 2 (c mod 2) + e (G <= 4: this lane's column
+    // part) or 2 c + e (G = 8) ----
     float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
@@ -1027,10 +754,15 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
             tv[r][slot] = *reinterpret_cast<const uint2*>(tabp + rec_tab_off(ch[r][kp >> 2], 2 * MB * (kp & 3), 2 * MB, lane8));
             sv[r][slot] = rec_sign2(sg[r] << (15 - kp));
           }
-        const uint2 bq = bfr[0][grp][s][lane], bp = bfr[1][grp][s][lane];
+        const uint2 bq = bfr[0][0][grp][s][lane], bp = bfr[0][1][grp][s][lane];
         rec_mma(am, tv[0][0].x, tv[1][0].x, tv[0][1].x, tv[1][1].x, bq.x, bq.y);
         rec_mma(am, tv[0][0].y, tv[1][0].y, tv[0][1].y, tv[1][1].y, bq.x, bq.y);
         rec_mma(as, sv[0][0], sv[1][0], sv[0][1], sv[1][1], bp.x, bp.y);
+        if constexpr (kG8) {  // the remainders of q and p (centroid remainder x q remainder: dropped)
+          const uint2 bq1 = bfr[kSets - 1][0][grp][s][lane], bp1 = bfr[kSets - 1][1][grp][s][lane];
+          rec_mma(am, tv[0][0].x, tv[1][0].x, tv[0][1].x, tv[1][1].x, bq1.x, bq1.y);
+          rec_mma(as, sv[0][0], sv[1][0], sv[0][1], sv[1][1], bp1.x, bp1.y);
+        }
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
@@ -1042,7 +774,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
     for (int r = 0; r < 2; ++r)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        sc[r][e] += __shfl_xor_sync(kFullMask, sc[r][e], 2);
+        if constexpr (!kG8) sc[r][e] += __shfl_xor_sync(kFullMask, sc[r][e], 2);
         if (!((vm >> r) & 1u)) sc[r][e] = -INFINITY;
       }
 
@@ -1068,7 +800,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
       }
       l_run[e] = fmaf(l_run[e], corr[e], p[0][e] + p[1][e]);
     }
-    if (c < 2) {
+    if (kG8 || c < 2) {
 #pragma unroll
       for (int r = 0; r < 2; ++r)
 #pragma unroll
@@ -1114,8 +846,9 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
     const float wscale = __uint_as_float((uint32_t)(139 - e_run) << 23);  // 2^(12 - e_run)
     __syncwarp();  // pt
 
-    // ---- value weights (B: column n = gr, q head gr mod 4, hi for gr < 4, remainder else) ----
-    uint32_t bc[2][2], bz[2][2];
+    // ---- value weights (B: column n = gr, q head gr mod 4, hi for gr < 4 and remainder else;
+    // or q head gr, hi in set 0 and remainder in set 1) ----
+    uint32_t bc[kSets][2][2], bz[kSets][2][2];
     {
       const float2 pa = *reinterpret_cast<const float2*>(&pt[warp][hq][2 * c]);
       const float2 pb = *reinterpret_cast<const float2*>(&pt[warp][hq][2 * c + 8]);
@@ -1128,10 +861,14 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
           wc[k] = pw[k] * nv[k][grp];
           wz[k] = wc[k] * gv[k][grp];
         }
-        bc[grp][0] = rec_split_pack(wc[0], wc[1], rem_col);
-        bc[grp][1] = rec_split_pack(wc[2], wc[3], rem_col);
-        bz[grp][0] = rec_split_pack(wz[0], wz[1], rem_col);
-        bz[grp][1] = rec_split_pack(wz[2], wz[3], rem_col);
+#pragma unroll
+        for (int st = 0; st < kSets; ++st) {
+          const bool rem = kG8 ? st == 1 : rem_col;
+          bc[st][grp][0] = rec_split_pack(wc[0], wc[1], rem);
+          bc[st][grp][1] = rec_split_pack(wc[2], wc[3], rem);
+          bz[st][grp][0] = rec_split_pack(wz[0], wz[1], rem);
+          bz[st][grp][1] = rec_split_pack(wz[2], wz[3], rem);
+        }
       }
     }
 
@@ -1156,17 +893,21 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           x[k] = *reinterpret_cast<const uint2*>(tabp + rec_tab_off(chv[k], 2 * MB * u, 2 * MB, lane8));
-        rec_mma(ov[grp][u], __byte_perm(x[0].x, x[1].x, 0x5410), __byte_perm(x[0].x, x[1].x, 0x7632),
-                __byte_perm(x[2].x, x[3].x, 0x5410), __byte_perm(x[2].x, x[3].x, 0x7632), bc[grp][0], bc[grp][1]);
+        const uint32_t h0 = __byte_perm(x[0].x, x[1].x, 0x5410), h1 = __byte_perm(x[0].x, x[1].x, 0x7632);
+        const uint32_t h2 = __byte_perm(x[2].x, x[3].x, 0x5410), h3 = __byte_perm(x[2].x, x[3].x, 0x7632);
+        rec_mma(ov[grp][u], h0, h1, h2, h3, bc[0][grp][0], bc[0][grp][1]);
         rec_mma(ov[grp][u], __byte_perm(x[0].y, x[1].y, 0x5410), __byte_perm(x[0].y, x[1].y, 0x7632),
-                __byte_perm(x[2].y, x[3].y, 0x5410), __byte_perm(x[2].y, x[3].y, 0x7632), bc[grp][0], bc[grp][1]);
+                __byte_perm(x[2].y, x[3].y, 0x5410), __byte_perm(x[2].y, x[3].y, 0x7632), bc[0][grp][0], bc[0][grp][1]);
+        if constexpr (kG8) rec_mma(ov[grp][u], h0, h1, h2, h3, bc[kSets - 1][grp][0], bc[kSets - 1][grp][1]);
         // sign bits 16 (u mod 2) + gr and + 8 of word u / 2: bytes bb, bb + 1 of two tokens
         const int bb = 2 * (u & 1);
         const uint32_t sel = (uint32_t)(bb | (bb + 1) << 4 | (bb + 4) << 8 | (bb + 5) << 12);
         const uint32_t z01 = __byte_perm(sw[0][u >> 1], sw[1][u >> 1], sel);
         const uint32_t z23 = __byte_perm(sw[2][u >> 1], sw[3][u >> 1], sel);
-        rec_mma(oz[grp][u], rec_sign2(z01 << (15 - gr)), rec_sign2(z01 << (7 - gr)), rec_sign2(z23 << (15 - gr)),
-                rec_sign2(z23 << (7 - gr)), bz[grp][0], bz[grp][1]);
+        const uint32_t s0 = rec_sign2(z01 << (15 - gr)), s1 = rec_sign2(z01 << (7 - gr));
+        const uint32_t s2 = rec_sign2(z23 << (15 - gr)), s3 = rec_sign2(z23 << (7 - gr));
+        rec_mma(oz[grp][u], s0, s1, s2, s3, bz[0][grp][0], bz[0][grp][1]);
+        if constexpr (kG8) rec_mma(oz[grp][u], s0, s1, s2, s3, bz[kSets - 1][grp][0], bz[kSets - 1][grp][1]);
       }
     }
     __syncwarp();  // the next tile rewrites pt; the one after it this buffer
@@ -1187,7 +928,7 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
     l += __shfl_xor_sync(kFullMask, l, 8);
     l += __shfl_xor_sync(kFullMask, l, 16);
     const int g = 2 * c + e;
-    if (gr == 0 && c < 2 && g < G) {
+    if (gr == 0 && (kG8 || c < 2) && g < G) {
       red_ml[warp][g][0] = m_run[e];
       red_ml[warp][g][1] = l;
     }
@@ -1198,10 +939,11 @@ decode_recipe_tc_kernel(DecodeArgs a, RecipeArgs rc, const float* __restrict__ p
     for (int u = 0; u < 2 * E; ++u)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float v = ov[grp][u][i] + __shfl_xor_sync(kFullMask, ov[grp][u][i], 2);
-        const float z = oz[grp][u][i] + __shfl_xor_sync(kFullMask, oz[grp][u][i], 2);
+        // (G <= 4: hi + remainder columns)
+        const float v = kG8 ? ov[grp][u][i] : ov[grp][u][i] + __shfl_xor_sync(kFullMask, ov[grp][u][i], 2);
+        const float z = kG8 ? oz[grp][u][i] : oz[grp][u][i] + __shfl_xor_sync(kFullMask, oz[grp][u][i], 2);
         const int g = 2 * c + (i & 1), r = i >> 1;
-        if (c < 2 && g < G) {
+        if ((kG8 || c < 2) && g < G) {
           red_acc[warp][g][grp * d + 4 * E * gr + 2 * u + r] = v * unscale;
           red_acc[warp][g][D + grp * d + 16 * u + gr + 8 * r] = z * unscale;
         }
@@ -1304,14 +1046,34 @@ cudaError_t launch_write_recipe_dim(const WriteArgs& a, const RecipeArgs& rc, cu
   return cudaErrorInvalidValue;
 }
 
+// Dynamic shared memory of decode_recipe_tc_kernel, in words: the larger of the warps'
+// staged tiles and the merge buffer.
+template <int E, int G, int MB0, int MB1>
+constexpr int recipe_tc_dyn_words() {
+  constexpr int rbw = (E * MB0 + E + 2) + (E * MB1 + E + 2);
+  constexpr int kStageWords = kRecTcWarps * kRecTcStages * 32 * rbw, kRedWords = kRecTcWarps * G * 2 * 64 * E;
+  return kStageWords > kRedWords ? kStageWords : kRedWords;
+}
+
+template <int E, int G, int MB0, int MB1>
+cudaError_t launch_recipe_tc(dim3 grid, cudaStream_t stream, const DecodeArgs& a, const RecipeArgs& rc,
+                             const float* p_all, const DecodePlan& p, RecipeSplitView part) {
+  auto kern = decode_recipe_tc_kernel<E, G, MB0, MB1>;
+  const int smem = 4 * recipe_tc_dyn_words<E, G, MB0, MB1>();
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kRecTcWarps * 32, smem, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part);
+  return cudaGetLastError();
+}
+
 template <int E, int MB0, int MB1>
 cudaError_t launch_recipe_split_g(int G, dim3 grid, cudaStream_t stream, const DecodeArgs& a, const RecipeArgs& rc,
                                   const float* p_all, const DecodePlan& p, RecipeSplitView part) {
-  switch (G) {  // tensor-core tiles for up to four q heads per kv head, else the SIMT tiles
-    case 1: decode_recipe_tc_kernel<E, 1, MB0, MB1><<<grid, kRecTcWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    case 2: decode_recipe_tc_kernel<E, 2, MB0, MB1><<<grid, kRecTcWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    case 4: decode_recipe_tc_kernel<E, 4, MB0, MB1><<<grid, kRecTcWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
-    case 8: decode_recipe_split_kernel<E, 8, MB0, MB1><<<grid, kRecDecodeWarps * 32, 0, stream>>>(a, rc, p_all, p.num_splits, p.blocks_per_split, part); break;
+  switch (G) {  // the tensor-core tiles at every GQA ratio
+    case 1: return launch_recipe_tc<E, 1, MB0, MB1>(grid, stream, a, rc, p_all, p, part);
+    case 2: return launch_recipe_tc<E, 2, MB0, MB1>(grid, stream, a, rc, p_all, p, part);
+    case 4: return launch_recipe_tc<E, 4, MB0, MB1>(grid, stream, a, rc, p_all, p, part);
+    case 8: return launch_recipe_tc<E, 8, MB0, MB1>(grid, stream, a, rc, p_all, p, part);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
